@@ -1,0 +1,170 @@
+/*
+ * dit_attn.h -- C-ABI of the GB300 (sm_103a) video-DiT attention library.
+ *
+ * The library computes the data-parallel hot path of video diffusion-transformer
+ * attention over token sequences padded to whole 128-row tiles:
+ *   - split-halves rotary embedding (RoPE) on q and k,
+ *   - self-attention with the pad keys masked out and the RoPE rotation fused into the
+ *     q/k tile load, emitting O and the log-sum-exp (LSE),
+ *   - short-KV cross-attention of video queries against a text sequence,
+ *   - the merge of partial attention results over key shards through their LSEs.
+ * Sources: Difflet PR #153 "TPU sequence parallelism: ... Wan padding + split RoPE"
+ * (row padding to whole tiles, pad keys dropped exactly, identity rotation for pad rows,
+ * split-halves RoPE); maxdiffusion PR #491 (Wan fast inference: lane padding to a
+ * multiple of 128, pad keys masked through the real KV length, fused short-KV
+ * cross-attention); mstar PR #376 (LTX-2.5 TP/SP: attention that also returns the LSE in
+ * natural log, attention over sharded keys merged through the LSE).
+ *
+ * Conventions for every call
+ *   - Tensors are contiguous BSHD: q/k/v/out [B, S, H, D] bf16 (raw 16-bit storage passed
+ *     as void*), LSE [B, S, H] fp32, natural log of the sum of exp of the SCALED scores.
+ *   - Pointers are device pointers unless marked "host". The caller owns every buffer;
+ *     the library allocates no device memory and keeps no state other than one per-device
+ *     status word (see dit_device_status).
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream). Device
+ *     calls are asynchronous on that stream and never synchronize the host.
+ *   - Padded lengths (Sq, Skv, S) are multiples of 128. D is 64 or 128. Valid lengths are
+ *     runtime arguments, so one compiled kernel serves every length.
+ *   - The library fails closed: invalid or unsupported arguments return an error status
+ *     before any device work is queued; it never runs unpadded or unmasked instead.
+ *   - Calls are thread-safe. The last CUDA error code seen by a call on the calling thread
+ *     is available through dit_last_cuda_error().
+ */
+#ifndef DIT_ATTN_H_
+#define DIT_ATTN_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes returned by every call. */
+#define DIT_OK 0
+#define DIT_ERR_INVALID_ARG (-1) /* null pointer, length out of range, bad count or scale   */
+#define DIT_ERR_UNSUPPORTED (-2) /* D not in {64, 128}, padded length not a multiple of 128 */
+#define DIT_ERR_ALIGNMENT (-3)   /* a device pointer not 16-byte aligned (TMA / 16-B loads) */
+#define DIT_ERR_CUDA (-4)        /* a CUDA call or launch failed; see dit_last_cuda_error() */
+#define DIT_ERR_TIMEOUT (-5)     /* a kernel gave up on a bounded wait (dit_device_status)  */
+
+/* Human-readable name of a status code (static string; never NULL). */
+const char* dit_status_string(int status);
+
+/* cudaError_t value of the last failing CUDA call made by this thread inside the library
+ * (0 if none). */
+int dit_last_cuda_error(void);
+
+/* Reads the current device's status word into *status_out (host pointer) and clears it if
+ * `clear` is non-zero. Bits are set by kernels that gave up on a bounded internal wait
+ * (each wait is limited to about two seconds, after which the kernel records the bit,
+ * releases its resources and exits instead of hanging). Synchronizes the current device.
+ * Returns DIT_OK, DIT_ERR_INVALID_ARG (null pointer) or DIT_ERR_CUDA. */
+int dit_device_status(unsigned int* status_out, int clear);
+
+/* ---------------------------------------------------------------------------------------
+ * RoPE cos/sin tables (host). Difflet PR #153: split-halves rotary pairs channel i with
+ * channel i + D/2; pad rows get the identity rotation.
+ *
+ * cos, sin: host arrays [S_pad, D/2] fp32, row r = token r. Angles are computed in fp64 and
+ * rounded to fp32. Rows r >= L (1-D) or r >= T*Hh*W (3-D) hold cos = 1, sin = 0.
+ * ------------------------------------------------------------------------------------- */
+
+/* 1-D: angle[r][i] = (pos_offset + r) * theta^(-2 i / D) for r < L.
+ * Errors: DIT_ERR_INVALID_ARG (null, L < 0, L > S_pad, theta <= 0), DIT_ERR_UNSUPPORTED
+ * (D odd or < 2). */
+int dit_rope_table_1d(float* cos_out, float* sin_out, int S_pad, int L, int D, double theta,
+                      int pos_offset);
+
+/* 3-D over a T x Hh x W latent grid, tokens in row-major order (t slowest). The D/2 pairs
+ * are cut into consecutive blocks of d_t/2, d_h/2, d_w/2 pairs (Wan: 44/42/42 channels);
+ * pair j of an axis block rotates by coord_axis * theta^(-2 j / d_axis).
+ * Errors: DIT_ERR_INVALID_ARG (null, T*Hh*W > S_pad, negative sizes, theta <= 0),
+ * DIT_ERR_UNSUPPORTED (d_t + d_h + d_w != D or an odd axis width). */
+int dit_rope_table_3d(float* cos_out, float* sin_out, int S_pad, int T, int Hh, int W, int D,
+                      int d_t, int d_h, int d_w, double theta);
+
+/* ---------------------------------------------------------------------------------------
+ * Standalone split-halves RoPE (Difflet PR #153, split RoPE commit; maxdiffusion PR #491,
+ * fused RoPE kernel):
+ *   y[.., i]       = x[.., i] cos - x[.., i + D/2] sin
+ *   y[.., i + D/2] = x[.., i] sin + x[.., i + D/2] cos,   (cos, sin) = table row s, col i.
+ * x, y: [B, S, H, D] bf16 (y may equal x for in place); cos, sin: [S, D/2] fp32 (device).
+ * Math in fp32, result rounded to nearest-even bf16.
+ * Errors: DIT_ERR_INVALID_ARG (null, B/S/H < 1), DIT_ERR_UNSUPPORTED (D not 64/128),
+ * DIT_ERR_ALIGNMENT (x, y, cos, sin not 16-byte aligned), DIT_ERR_CUDA.
+ * ------------------------------------------------------------------------------------- */
+int dit_rope_split_halves(const void* x, void* y, const float* cos_tab, const float* sin_tab,
+                          int B, int S, int H, int D, void* stream);
+
+/* ---------------------------------------------------------------------------------------
+ * Self-attention forward over padded sequences (also used for one key shard).
+ * Difflet PR #153 (pad keys dropped exactly), maxdiffusion PR #491 (real KV length as the
+ * ragged tail), mstar PR #376 (LSE returned in natural log).
+ *
+ * For batch b, head h and query row i < q_valid_len:
+ *   q~_i = R(cos_q, sin_q row i) q_i,  k~_j = R(cos_k, sin_k row j) k_j   (if tables given)
+ *   s_j = softmax_scale * q~_i . k~_j,  j < kv_valid_len only
+ *   lse[b,i,h] = ln sum_j exp(s_j),  out[b,i,h,:] = sum_j exp(s_j - lse) v_j
+ * Query rows i >= q_valid_len get out = 0 and lse = -inf. If kv_valid_len == 0 every row
+ * does. Pad rows of q, k and v (rows >= the valid length) are never read, so their
+ * contents (even NaN/Inf) cannot change any output.
+ *
+ * q: [B, Sq, H, D]; k, v: [B, Skv, H, D]; out: [B, Sq, H, D] (bf16); lse: [B, Sq, H] fp32.
+ * cos_q/sin_q: [Sq, D/2], cos_k/sin_k: [Skv, D/2] fp32 device tables; all four NULL = no
+ * RoPE (all four or none must be given). q~ and k~ are rounded to bf16 before the tensor-
+ * core products; P is rounded to bf16 before P.V; accumulation and softmax are fp32.
+ * Constraints: Sq, Skv multiples of 128; D in {64, 128}; 0 <= q_valid_len <= Sq;
+ * 0 <= kv_valid_len <= Skv; softmax_scale > 0 and finite (callers normally pass 1/sqrt(D)).
+ * Errors: DIT_ERR_INVALID_ARG, DIT_ERR_UNSUPPORTED, DIT_ERR_ALIGNMENT (q, k, v, out, tables
+ * not 16-byte aligned; lse not 4-byte aligned), DIT_ERR_CUDA.
+ * ------------------------------------------------------------------------------------- */
+int dit_attn_fwd(const void* q, const void* k, const void* v, int B, int Sq, int Skv, int H,
+                 int D, int q_valid_len, int kv_valid_len, const float* cos_q,
+                 const float* sin_q, const float* cos_k, const float* sin_k,
+                 float softmax_scale, void* out, float* lse, void* stream);
+
+/* ---------------------------------------------------------------------------------------
+ * Short-KV cross-attention (maxdiffusion PR #491: fused short-KV cross-attention of the video
+ * queries against the text sequence). As dit_attn_fwd without RoPE, with one valid key
+ * length per batch read on the device: kv_valid_len_dev[b] in [0, Skv] (int32, device
+ * array of B entries; values outside are clamped into that range). Skv <= 512.
+ * Errors as dit_attn_fwd; DIT_ERR_UNSUPPORTED also for Skv > 512.
+ * ------------------------------------------------------------------------------------- */
+int dit_cross_attn_shortkv(const void* q, const void* k, const void* v, int B, int Sq,
+                           int Skv, int H, int D, int q_valid_len,
+                           const int32_t* kv_valid_len_dev, float softmax_scale, void* out,
+                           float* lse, void* stream);
+
+/* ---------------------------------------------------------------------------------------
+ * LSE merge of partial results over key shards (mstar PR #376, attention over sharded keys):
+ *   lse = ln sum_s exp(lse_s),  out = sum_s exp(lse_s - lse) * O_s.
+ * A row whose n partial LSEs are all -inf (no shard saw a key) gets out = 0, lse = -inf.
+ * partial_o: [n][B, S, H, D] bf16, contiguous; partial_lse: [n][B, S, H] fp32;
+ * out: [B, S, H, D] bf16 (rounded to nearest even from fp32); lse: [B, S, H] fp32.
+ * S need not be padded here. 1 <= n <= 64.
+ * Errors: DIT_ERR_INVALID_ARG, DIT_ERR_UNSUPPORTED (D not 64/128), DIT_ERR_ALIGNMENT
+ * (partial_o, out not 16-byte aligned; lse arrays not 4-byte aligned), DIT_ERR_CUDA.
+ * ------------------------------------------------------------------------------------- */
+int dit_attn_lse_merge(const void* partial_o, const float* partial_lse, int n, int B, int S,
+                       int H, int D, void* out, float* lse, void* stream);
+
+/* ---------------------------------------------------------------------------------------
+ * Token padding at the boundary (Difflet PR #153: the first block pads the patch sequence,
+ * the last cuts the pad; maxdiffusion PR #491: pad the tokens at the tail, unpad the output).
+ *
+ * dit_pad_tokens copies rows [0, L) of x [B, L, row_bytes] into x_pad [B, S_pad, row_bytes];
+ * pad rows of x_pad are left untouched (attention never reads them).
+ * dit_unpad_tokens copies rows [0, L) of x_pad [B, S_pad, row_bytes] into x [B, L, row_bytes].
+ * row_bytes is the size of one token row (H*D*2 for q/k/v/O, H*4 for LSE), any value >= 1.
+ * Errors: DIT_ERR_INVALID_ARG (null, B < 1, L < 0, L > S_pad, row_bytes < 1), DIT_ERR_CUDA.
+ * ------------------------------------------------------------------------------------- */
+int dit_pad_tokens(const void* x, void* x_pad, int B, int L, int S_pad, long long row_bytes,
+                   void* stream);
+int dit_unpad_tokens(const void* x_pad, void* x, int B, int L, int S_pad, long long row_bytes,
+                     void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DIT_ATTN_H_ */

@@ -1,0 +1,139 @@
+"""The C-ABI library without a GPU: it loads, exports every function include/dit_attn.h
+declares, its host-side table builders agree with the oracle's angles, and invalid
+arguments return the documented status before any CUDA call is made."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+from oracle.rope import pad_angles, rope_angles_1d, rope_angles_3d
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dit_attn.h")
+LIB = os.path.join(ROOT, "video_dit_attention_gb300", "libdit_attn.so")
+
+
+@pytest.fixture(scope="module")
+def clib():
+    if not os.path.exists(LIB):
+        from video_dit_attention_gb300.build import build
+        build()
+    return ctypes.CDLL(LIB)
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dit_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_four_hot_path_calls():
+    names = declared_functions()
+    for n in ("dit_rope_split_halves", "dit_attn_fwd", "dit_cross_attn_shortkv", "dit_attn_lse_merge"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(clib):
+    for name in declared_functions():
+        assert hasattr(clib, name), f"{name} declared in dit_attn.h but not exported"
+
+
+def test_binding_defines_every_declared_symbol():
+    import ast
+    src = open(os.path.join(ROOT, "video_dit_attention_gb300", "dit_attn.py")).read()
+    defined = {n.name for n in ast.parse(src).body if isinstance(n, ast.FunctionDef)}
+    missing = [n for n in declared_functions() if n not in defined and n != "dit_last_cuda_error"]
+    assert not missing, missing
+
+
+def _tables(clib, fn, *args, S_pad, half):
+    cos = np.empty((S_pad, half), dtype=np.float32)
+    sin = np.empty((S_pad, half), dtype=np.float32)
+    fp = ctypes.POINTER(ctypes.c_float)
+    st = fn(cos.ctypes.data_as(fp), sin.ctypes.data_as(fp), *args)
+    return st, cos, sin
+
+
+def test_rope_table_1d_matches_oracle_angles(clib):
+    fn = clib.dit_rope_table_1d
+    fn.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                   ctypes.c_double, ctypes.c_int]
+    st, c, s = _tables(clib, fn, 300, 290, 64, 10000.0, 37799 - 290, S_pad=300, half=32)
+    assert st == 0
+    ang = pad_angles(rope_angles_1d(np.arange(290) + 37799 - 290, 64), 300)
+    assert np.max(np.abs(c - np.cos(ang))) < 1e-7 and np.max(np.abs(s - np.sin(ang))) < 1e-7
+    assert np.all(c[290:] == 1.0) and np.all(s[290:] == 0.0)
+
+
+def test_rope_table_3d_matches_oracle_angles(clib):
+    fn = clib.dit_rope_table_3d
+    fn.argtypes = [ctypes.c_void_p, ctypes.c_void_p] + [ctypes.c_int] * 8 + [ctypes.c_double]
+    st, c, s = _tables(clib, fn, 4736, 3, 30, 52, 128, 44, 42, 42, 10000.0, S_pad=4736, half=64)
+    assert st == 0
+    ang = pad_angles(rope_angles_3d(3, 30, 52), 4736)
+    assert np.max(np.abs(c - np.cos(ang))) < 1e-7 and np.max(np.abs(s - np.sin(ang))) < 1e-7
+    # bad channel split
+    st2, _, _ = _tables(clib, fn, 4736, 3, 30, 52, 128, 44, 42, 40, 10000.0, S_pad=4736, half=64)
+    assert st2 == -2
+    st3, _, _ = _tables(clib, fn, 100, 3, 30, 52, 128, 44, 42, 42, 10000.0, S_pad=100, half=64)
+    assert st3 == -1
+
+
+def _attn(clib):
+    fn = clib.dit_attn_fwd
+    fn.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 7 + [ctypes.c_void_p] * 4 + \
+                  [ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+    fn.restype = ctypes.c_int
+    return fn
+
+
+def test_attention_argument_validation_before_any_cuda_call(clib):
+    fn = _attn(clib)
+    P = 0x10000   # never dereferenced: every case below fails validation first
+    base = dict(q=P, k=P, v=P, B=1, Sq=256, Skv=256, H=2, D=128, qv=256, kv=256,
+                cq=None, sq=None, ck=None, sk=None, scale=0.088, out=P, lse=P, stream=None)
+
+    def call(**over):
+        a = dict(base, **over)
+        return fn(a["q"], a["k"], a["v"], a["B"], a["Sq"], a["Skv"], a["H"], a["D"], a["qv"], a["kv"],
+                  a["cq"], a["sq"], a["ck"], a["sk"], a["scale"], a["out"], a["lse"], a["stream"])
+
+    assert call(q=None) == -1
+    assert call(B=0) == -1
+    assert call(qv=257) == -1
+    assert call(kv=-1) == -1
+    assert call(scale=0.0) == -1
+    assert call(scale=float("nan")) == -1
+    assert call(cq=P) == -1                 # some tables but not all four
+    assert call(D=96) == -2
+    assert call(Sq=200, qv=200) == -2
+    assert call(Skv=300) == -2
+    assert call(q=P + 8) == -3
+    assert call(lse=P + 2) == -3
+
+
+def test_cross_and_merge_validation(clib):
+    cross = clib.dit_cross_attn_shortkv
+    cross.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 6 + [ctypes.c_void_p, ctypes.c_float,
+                                                                   ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+    P = 0x10000
+    assert cross(P, P, P, 2, 256, 640, 2, 128, 256, P, 0.1, P, P, None) == -2     # Skv > 512
+    assert cross(P, P, P, 2, 256, 512, 2, 128, 256, None, 0.1, P, P, None) == -1  # no lengths
+    merge = clib.dit_attn_lse_merge
+    merge.argtypes = [ctypes.c_void_p, ctypes.c_void_p] + [ctypes.c_int] * 5 + [ctypes.c_void_p] * 3
+    assert merge(P, P, 0, 1, 8, 2, 128, P, P, None) == -1
+    assert merge(P, P, 65, 1, 8, 2, 128, P, P, None) == -1
+    assert merge(P, P, 2, 1, 8, 2, 32, P, P, None) == -2
+    assert merge(P + 4, P, 2, 1, 8, 2, 128, P, P, None) == -3
+    rope = clib.dit_rope_split_halves
+    rope.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int] * 4 + [ctypes.c_void_p]
+    assert rope(P, P, P, P, 1, 8, 2, 80, None) == -2
+    assert rope(P, P, P + 4, P, 1, 8, 2, 64, None) == -3
+
+
+def test_status_strings(clib):
+    clib.dit_status_string.restype = ctypes.c_char_p
+    for code in (0, -1, -2, -3, -4, -5):
+        assert clib.dit_status_string(code).startswith(b"DIT_")

@@ -1,0 +1,157 @@
+"""GPU parity of short-KV cross-attention, the LSE merge, the sharded-keys flow, the
+standalone RoPE kernel and the pad/unpad copies, against the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+from helpers import LSE_TOL, O_TOL, compare, dev_bf16
+from oracle.attention import attention, lse_merge
+from oracle.rope import pad_angles, rope_angles_1d, rope_angles_3d, rope_split_halves
+from video_dit_attention_gb300.inputs import (AttnCase, ShardedCase, cross_case, make_qkv,
+                                              make_sharded, sample_rows, sharded_case)
+
+pytestmark = pytest.mark.gpu
+
+
+def _run_cross(lib, case, q, k, v):
+    kv = torch.tensor(case.kv_valid, dtype=torch.int32, device="cuda")
+    out, lse = lib.dit_cross_attn_shortkv(dev_bf16(q), dev_bf16(k), dev_bf16(v), case.q_valid, kv,
+                                          softmax_scale=case.scale)
+    torch.cuda.synchronize()
+    return out.float().cpu().numpy(), lse.cpu().numpy()
+
+
+@pytest.mark.parametrize("kv", [[1, 512], [128, 129], [300, 7], [511, 384], [0, 200]])
+def test_cross_small(lib, kv):
+    case = AttnCase("cross", B=2, H=3, D=128, Sq=384, Skv=512, q_valid=333, kv_valid=kv, seed=70)
+    q, k, v = make_qkv(case)
+    O, L = _run_cross(lib, case, q, k, v)
+    Or, Lr = attention(q, k, v, case.q_valid, kv, case.scale)
+    compare(O, L, Or, Lr, case.q_valid)
+
+
+def test_cross_pad_garbage_is_nan_safe(lib):
+    case = AttnCase("crossnan", B=2, H=2, D=64, Sq=256, Skv=256, q_valid=256, kv_valid=[77, 200], seed=71)
+    q, k, v = make_qkv(case)
+    O1, L1 = _run_cross(lib, case, q, k, v)
+    k[0, 77:] = np.nan
+    v[0, 77:] = np.inf
+    v[1, 200:] = np.nan
+    O2, L2 = _run_cross(lib, case, q, k, v)
+    assert np.array_equal(O1, O2) and np.array_equal(L1, L2)
+    Or, Lr = attention(q, k, v, case.q_valid, case.kv_valid, case.scale)
+    compare(O2, L2, Or, Lr, case.q_valid)
+
+
+def test_cross_workload_full(lib):
+    case = cross_case()
+    q, k, v = make_qkv(case)
+    O, L = _run_cross(lib, case, q, k, v)
+    rows = sample_rows(case.q_valid, case.Sq, 64, seed=8)
+    Or, Lr = attention(q, k, v, case.q_valid, case.kv_valid, case.scale, rows=rows)
+    compare(O, L, Or, Lr, case.q_valid, rows=rows)
+    assert np.all(O[:, case.q_valid:] == 0) and np.all(L[:, case.q_valid:] == -np.inf)
+    assert lib.dit_device_status() == 0
+
+
+def test_lse_merge_kernel_against_oracle(lib):
+    rng = np.random.Generator(np.random.PCG64(72))
+    n, B, S, H, D = 4, 2, 130, 3, 128
+    po = torch.from_numpy(rng.standard_normal((n, B, S, H, D), dtype=np.float32)).to(torch.bfloat16)
+    pl = rng.standard_normal((n, B, S, H)).astype(np.float32) * 5
+    pl[1, 0, :10] = -np.inf            # an empty shard for some rows
+    pl[:, 1, 5, 2] = -np.inf           # a row no shard saw
+    out, lse = lib.dit_attn_lse_merge(po.cuda(), torch.from_numpy(pl).cuda())
+    torch.cuda.synchronize()
+    Or, Lr = lse_merge(po.float().numpy(), pl)
+    og, lg = out.float().cpu().numpy(), lse.cpu().numpy()
+    fin = np.isfinite(Lr)
+    assert np.array_equal(np.isfinite(lg), fin)
+    assert np.max(np.abs(lg[fin] - Lr[fin])) <= LSE_TOL
+    assert np.max(np.abs(og - Or)) <= O_TOL
+    assert np.all(og[1, 5, 2] == 0)
+
+
+def _sharded_gpu(lib, case, q, shards):
+    """One dit_attn_fwd per key shard (RoPE at the shard's global positions), then the merge."""
+    D = case.D
+    cq, sq = lib.dit_rope_table_1d(case.Sq, case.q_valid, D, case.theta, 0)
+    cq, sq = torch.from_numpy(cq).cuda(), torch.from_numpy(sq).cuda()
+    qd = dev_bf16(q)
+    n = len(shards)
+    po = torch.empty((n,) + tuple(q.shape), dtype=torch.bfloat16, device="cuda")
+    pl = torch.empty((n,) + tuple(q.shape[:3]), dtype=torch.float32, device="cuda")
+    for s, ((k, v), off, nv, npad) in enumerate(zip(shards, case.offsets, case.shard_valid, case.shard_pad)):
+        ck, sk = lib.dit_rope_table_1d(npad, nv, D, case.theta, off)
+        lib.dit_attn_fwd(qd, dev_bf16(k), dev_bf16(v), case.q_valid, nv, cq, sq,
+                         torch.from_numpy(ck).cuda(), torch.from_numpy(sk).cuda(),
+                         out=po[s], lse=pl[s])
+    out, lse = lib.dit_attn_lse_merge(po, pl)
+    torch.cuda.synchronize()
+    return out.float().cpu().numpy(), lse.cpu().numpy()
+
+
+def _oracle_unsharded(case, q, shards, rows, heads):
+    k = np.concatenate([kv[0][:, :n] for kv, n in zip(shards, case.shard_valid)], axis=1)
+    v = np.concatenate([kv[1][:, :n] for kv, n in zip(shards, case.shard_valid)], axis=1)
+    L = k.shape[1]
+    aq = pad_angles(rope_angles_1d(np.arange(case.q_valid), case.D, case.theta), case.Sq)
+    ak = rope_angles_1d(np.arange(L), case.D, case.theta)
+    return attention(q, k, v, case.q_valid, L, case.scale, aq, ak, rows=rows, heads=heads)
+
+
+def test_sharded_small_equals_unsharded(lib):
+    case = ShardedCase("sh", B=1, H=2, D=128, Sq=256, q_valid=250, shard_valid=(300, 128, 1, 77), seed=73)
+    q, shards = make_sharded(case)
+    O, L = _sharded_gpu(lib, case, q, shards)
+    Or, Lr = _oracle_unsharded(case, q, shards, None, None)
+    compare(O, L, Or, Lr, case.q_valid)
+
+
+def test_sharded_workload_full_size_sampled_rows(lib):
+    case = sharded_case()
+    q, shards = make_sharded(case)
+    O, L = _sharded_gpu(lib, case, q, shards)
+    rows = sample_rows(case.q_valid, case.Sq, 40, seed=9)
+    heads = [0, 13, 31]
+    Or, Lr = _oracle_unsharded(case, q, shards, rows, heads)
+    compare(O, L, Or, Lr, case.q_valid, rows=rows, heads=heads)
+    assert np.all(np.isfinite(L))
+    assert lib.dit_device_status() == 0
+
+
+@pytest.mark.parametrize("D,rope", [(64, "1d"), (128, "1d"), (128, "3d")])
+def test_standalone_rope_kernel(lib, D, rope):
+    B, S, H = 2, 300, 3
+    rng = np.random.Generator(np.random.PCG64(74))
+    x = torch.from_numpy(rng.standard_normal((B, S, H, D), dtype=np.float32)).to(torch.bfloat16)
+    if rope == "1d":
+        c, s = lib.dit_rope_table_1d(S, 280, D, 10000.0, 5)
+        ang = pad_angles(rope_angles_1d(np.arange(280) + 5, D), S)
+    else:
+        c, s = lib.dit_rope_table_3d(S, (2, 10, 14), D)
+        ang = pad_angles(rope_angles_3d(2, 10, 14), S)
+    y = lib.dit_rope_split_halves(x.cuda(), torch.from_numpy(c).cuda(), torch.from_numpy(s).cuda())
+    torch.cuda.synchronize()
+    ref = rope_split_halves(x.float().numpy(), ang)
+    err = np.abs(y.float().cpu().numpy() - ref)
+    # one bf16 rounding of the result (2^-8 relative) plus fp32 table/arithmetic error
+    assert np.all(err <= np.abs(ref) * 2.0 ** -8 + 1e-5)
+    # in place gives the same bits
+    xi = x.cuda()
+    lib.dit_rope_split_halves(xi, torch.from_numpy(c).cuda(), torch.from_numpy(s).cuda(), out=xi)
+    torch.cuda.synchronize()
+    assert torch.equal(xi.cpu(), y.cpu())
+
+
+def test_pad_and_unpad_copies(lib):
+    rng = np.random.Generator(np.random.PCG64(75))
+    x = torch.from_numpy(rng.standard_normal((2, 300, 5, 64), dtype=np.float32)).to(torch.bfloat16).cuda()
+    xp = lib.dit_pad_tokens(x, 384)
+    back = lib.dit_unpad_tokens(xp, 300)
+    l = torch.from_numpy(rng.standard_normal((2, 300, 5), dtype=np.float32)).cuda()   # 20-byte rows
+    lp = lib.dit_pad_tokens(l, 384)
+    lb = lib.dit_unpad_tokens(lp, 300)
+    torch.cuda.synchronize()
+    assert torch.equal(back, x) and torch.equal(xp[:, :300], x)
+    assert torch.equal(lb, l) and torch.equal(lp[:, :300], l)

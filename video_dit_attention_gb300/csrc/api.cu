@@ -1,0 +1,166 @@
+// C-ABI entry points (include/dit_attn.h): argument validation, TMA descriptor encoding and
+// kernel launches. No device memory is allocated here; every buffer belongs to the caller.
+
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/dit_attn.h"
+#include "common.h"
+
+namespace dit {
+namespace {
+
+thread_local int t_last_cuda_error = 0;
+
+int cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return DIT_OK;
+  t_last_cuda_error = static_cast<int>(e);
+  return DIT_ERR_CUDA;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// Shared checks of the attention entry points.
+int check_attn_shapes(const void* q, const void* k, const void* v, int B, int Sq, int Skv,
+                      int H, int D, int q_valid, float scale, const void* out, const float* lse) {
+  if (!q || !k || !v || !out || !lse) return DIT_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || Sq < 1 || Skv < 1) return DIT_ERR_INVALID_ARG;
+  if (!(scale > 0.f) || !std::isfinite(scale)) return DIT_ERR_INVALID_ARG;
+  if (q_valid < 0 || q_valid > Sq) return DIT_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return DIT_ERR_UNSUPPORTED;
+  if ((Sq % 128) != 0 || (Skv % 128) != 0) return DIT_ERR_UNSUPPORTED;
+  if (H > 65535 || B > 65535) return DIT_ERR_UNSUPPORTED;   // grid.y / grid.z limits
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16) ||
+      !aligned(lse, 4))
+    return DIT_ERR_ALIGNMENT;
+  return DIT_OK;
+}
+
+}  // namespace
+
+bool encode_bshd_map(CUtensorMap* map, const void* base, int B, int s_extent, int s_rows, int H,
+                     int D) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
+                              static_cast<cuuint64_t>(s_extent), static_cast<cuuint64_t>(B)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2,
+                                 static_cast<cuuint64_t>(H) * D * 2,
+                                 static_cast<cuuint64_t>(s_rows) * H * D * 2};
+  const cuuint32_t box[4] = {64, 1, 128, 1};
+  const cuuint32_t elem_strides[4] = {1, 1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
+            elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace dit
+
+using namespace dit;
+
+extern "C" const char* dit_status_string(int status) {
+  switch (status) {
+    case DIT_OK: return "DIT_OK";
+    case DIT_ERR_INVALID_ARG: return "DIT_ERR_INVALID_ARG: null pointer or value out of range";
+    case DIT_ERR_UNSUPPORTED: return "DIT_ERR_UNSUPPORTED: head dim or padded length not supported";
+    case DIT_ERR_ALIGNMENT: return "DIT_ERR_ALIGNMENT: device pointer not aligned";
+    case DIT_ERR_CUDA: return "DIT_ERR_CUDA: CUDA call or launch failed";
+    case DIT_ERR_TIMEOUT: return "DIT_ERR_TIMEOUT: a kernel gave up on a bounded wait";
+    default: return "unknown status";
+  }
+}
+
+extern "C" int dit_last_cuda_error(void) { return t_last_cuda_error; }
+
+extern "C" int dit_device_status(unsigned int* status_out, int clear) {
+  if (!status_out) return DIT_ERR_INVALID_ARG;
+  return cuda_status(read_device_status(status_out, clear != 0));
+}
+
+extern "C" int dit_rope_split_halves(const void* x, void* y, const float* cos_tab,
+                                     const float* sin_tab, int B, int S, int H, int D,
+                                     void* stream) {
+  if (!x || !y || !cos_tab || !sin_tab || B < 1 || S < 1 || H < 1) return DIT_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return DIT_ERR_UNSUPPORTED;
+  if (!aligned(x, 16) || !aligned(y, 16) || !aligned(cos_tab, 16) || !aligned(sin_tab, 16))
+    return DIT_ERR_ALIGNMENT;
+  return cuda_status(launch_rope_split_halves(x, y, cos_tab, sin_tab, B, S, H, D,
+                                              static_cast<cudaStream_t>(stream)));
+}
+
+extern "C" int dit_attn_fwd(const void* q, const void* k, const void* v, int B, int Sq, int Skv,
+                            int H, int D, int q_valid_len, int kv_valid_len, const float* cos_q,
+                            const float* sin_q, const float* cos_k, const float* sin_k,
+                            float softmax_scale, void* out, float* lse, void* stream) {
+  int st = check_attn_shapes(q, k, v, B, Sq, Skv, H, D, q_valid_len, softmax_scale, out, lse);
+  if (st != DIT_OK) return st;
+  if (kv_valid_len < 0 || kv_valid_len > Skv) return DIT_ERR_INVALID_ARG;
+  const int n_tables = (cos_q != nullptr) + (sin_q != nullptr) + (cos_k != nullptr) + (sin_k != nullptr);
+  if (n_tables != 0 && n_tables != 4) return DIT_ERR_INVALID_ARG;
+  if (n_tables == 4 && (!aligned(cos_q, 16) || !aligned(sin_q, 16) || !aligned(cos_k, 16) ||
+                        !aligned(sin_k, 16)))
+    return DIT_ERR_ALIGNMENT;
+  AttnArgs a{q, k, v, B, Sq, Skv, H, D, q_valid_len, kv_valid_len, nullptr,
+             cos_q, sin_q, cos_k, sin_k, softmax_scale, out, lse, static_cast<cudaStream_t>(stream)};
+  return cuda_status(launch_attn_fwd(a, n_tables == 4 ? kModeRope : kModePlain));
+}
+
+extern "C" int dit_cross_attn_shortkv(const void* q, const void* k, const void* v, int B, int Sq,
+                                      int Skv, int H, int D, int q_valid_len,
+                                      const int32_t* kv_valid_len_dev, float softmax_scale,
+                                      void* out, float* lse, void* stream) {
+  int st = check_attn_shapes(q, k, v, B, Sq, Skv, H, D, q_valid_len, softmax_scale, out, lse);
+  if (st != DIT_OK) return st;
+  if (!kv_valid_len_dev) return DIT_ERR_INVALID_ARG;
+  if (Skv > 512) return DIT_ERR_UNSUPPORTED;
+  if (!aligned(kv_valid_len_dev, 4)) return DIT_ERR_ALIGNMENT;
+  AttnArgs a{q, k, v, B, Sq, Skv, H, D, q_valid_len, Skv, kv_valid_len_dev,
+             nullptr, nullptr, nullptr, nullptr, softmax_scale, out, lse,
+             static_cast<cudaStream_t>(stream)};
+  return cuda_status(launch_attn_fwd(a, kModeCross));
+}
+
+extern "C" int dit_attn_lse_merge(const void* partial_o, const float* partial_lse, int n, int B,
+                                  int S, int H, int D, void* out, float* lse, void* stream) {
+  if (!partial_o || !partial_lse || !out || !lse) return DIT_ERR_INVALID_ARG;
+  if (n < 1 || n > 64 || B < 1 || S < 1 || H < 1) return DIT_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return DIT_ERR_UNSUPPORTED;
+  if (!aligned(partial_o, 16) || !aligned(out, 16) || !aligned(partial_lse, 4) || !aligned(lse, 4))
+    return DIT_ERR_ALIGNMENT;
+  return cuda_status(launch_lse_merge(partial_o, partial_lse, n, B, S, H, D, out, lse,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+extern "C" int dit_pad_tokens(const void* x, void* x_pad, int B, int L, int S_pad,
+                              long long row_bytes, void* stream) {
+  if (!x || !x_pad || B < 1 || L < 0 || L > S_pad || row_bytes < 1) return DIT_ERR_INVALID_ARG;
+  return cuda_status(launch_copy_rows(x, x_pad, B, L, L, S_pad, row_bytes,
+                                      static_cast<cudaStream_t>(stream)));
+}
+
+extern "C" int dit_unpad_tokens(const void* x_pad, void* x, int B, int L, int S_pad,
+                                long long row_bytes, void* stream) {
+  if (!x || !x_pad || B < 1 || L < 0 || L > S_pad || row_bytes < 1) return DIT_ERR_INVALID_ARG;
+  return cuda_status(launch_copy_rows(x_pad, x, B, L, S_pad, L, row_bytes,
+                                      static_cast<cudaStream_t>(stream)));
+}

@@ -1,0 +1,576 @@
+// Flash-attention forward for sm_103a on tcgen05 tensor cores, with exact pad-key masking,
+// natural-log LSE output and (optionally) split-halves RoPE fused into the q/k tile load.
+//
+// What it computes (Difflet PR #153: pad keys dropped exactly, pad rows rotated by the
+// identity; maxdiffusion PR #491: the real KV length as the ragged tail; mstar PR #376: the
+// LSE in natural log returned beside O): for every (batch b, head h, query row i < q_valid)
+//   s_j = scale * (R_q(i) q_i) . (R_k(j) k_j)   for j < kv_valid
+//   lse_i = ln sum_j exp(s_j),  O_i = sum_j exp(s_j - lse_i) v_j,
+// and O = 0, lse = -inf for pad query rows. It is the online-softmax (flash) form of that
+// definition: keys are visited in 128-key tiles and the running max/sum are rescaled.
+//
+// One CTA owns a 128-row query tile of one (b, h). Warp roles (384 threads):
+//   warp 0     TMA producer: Q once, then K_j / V_j into a ring of shared-memory stages.
+//   warp 1     TMEM allocator and single-thread tcgen05.mma issuer:
+//              S_j = Q K_j^T into one of two TMEM S buffers, O += P_j V_j into TMEM.
+//   warps 4-7  softmax: thread t owns query row t (TMEM lane t). Reads S_j with tcgen05.ld,
+//              masks keys >= kv_valid, keeps the running max m and sum l, writes P_j (bf16)
+//              to shared memory; rescales O in TMEM only when m grows by more than 2^8
+//              (the final O / l is exact for any reference max); epilogue O / l, LSE.
+//   warps 8-11 auxiliary: RoPE rotation of the landed Q and K tiles in shared memory
+//              (pairs (i, i + D/2) sit at the same swizzled offset of the two 64-column
+//              halves of a row), or, for cross-attention, zeroing of V rows past the
+//              per-batch valid length so that 0 * (pad garbage) cannot reach O.
+//              The rotation is computed in fp32 from the bf16 inputs and stored as fp16
+//              (11-bit significand, 8x finer than bf16; saturating at +-65504), and S =
+//              q~ k~^T then runs as an fp16 x fp16 MMA at the same tensor-core rate. Without
+//              RoPE, q and k are used as the bf16 values they are.
+// Every mbarrier wait is bounded (ptx.cuh); on a timeout the CTA records a status bit,
+// drains what it has in flight, frees TMEM and exits.
+//
+// Shared memory (128-byte swizzle, tiles 1024-byte aligned): Q [128 x D], K and V stages
+// [128 x D] each, P [128 x 128]. Each [128 x D] tile is D/64 sub-tiles of 128 rows x 128 B.
+// TMEM: 512 columns = S buffer 0 (0..127), S buffer 1 (128..255), O (256..256+D).
+
+#include <cuda_bf16.h>
+
+#include "common.h"
+#include "ptx.cuh"
+
+namespace dit {
+
+__device__ unsigned int g_dit_status;
+
+namespace {
+
+constexpr int kThreads = 384;
+constexpr float kLn2 = 0.69314718055994530942f;
+constexpr float kLog2e = 1.44269504088896340736f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only if m grows by > 2^8
+
+template <int D>
+struct Cfg {
+  static constexpr int kSub = D / 64;               // 64-column sub-tiles per row
+  static constexpr int kTileBytes = 128 * D * 2;    // one 128-row q/k/v tile
+  static constexpr int kStages = (D == 128) ? 2 : 3;
+  static constexpr int kPBytes = 128 * 128 * 2;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kOffQ + kTileBytes;
+  static constexpr int kOffV = kOffK + kStages * kTileBytes;
+  static constexpr int kOffP = kOffV + kStages * kTileBytes;
+  static constexpr int kOffBar = kOffP + kPBytes;
+  static constexpr int kSmemBytes = kOffBar + 512 + 1024;   // barriers + alignment slack
+};
+
+struct Bars {
+  uint64_t q_full, q_ready;
+  uint64_t k_full[4], k_ready[4], k_empty[4];
+  uint64_t v_full[4], v_ready[4], v_empty[4];
+  uint64_t s_full[2];
+  uint64_t p_full, o_done, drain;
+  uint32_t tmem_base;
+  int abort;
+  int aux_go;   // outcome of the auxiliary warpgroup's last wait, broadcast to the group
+};
+
+struct KParams {
+  int Sq, Skv, H;
+  int q_valid, kv_valid;
+  const int32_t* kv_valid_dev;
+  const float* cos_q;
+  const float* sin_q;
+  const float* cos_k;
+  const float* sin_k;
+  float scale_log2;
+  uint16_t* out;
+  float* lse;
+};
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+// Bounded wait taken by lane 0 of the warp and broadcast, so that every lane leaves with
+// the same outcome (the warp then stays converged at .sync.aligned tcgen05 instructions).
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          unsigned int* status, unsigned int code) {
+  int ok = 0;
+  if ((threadIdx.x & 31) == 0) ok = bounded_wait(bar, parity, abort_flag, status, code) ? 1 : 0;
+  ok = __shfl_sync(0xffffffffu, ok, 0);
+  return ok != 0;
+}
+
+// Bounded wait taken by one thread of the 128-thread auxiliary warpgroup and broadcast to
+// the group through shared memory and named barrier 1 (all 128 threads call this).
+__device__ __forceinline__ bool group_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                           unsigned int* status, unsigned int code,
+                                           volatile int* go, int at) {
+  if (at == 0) *go = bounded_wait(bar, parity, abort_flag, status, code) ? 1 : 0;
+  named_bar_sync(1, 128);
+  return *go != 0;
+}
+
+// Rotates 8 channel pairs: a holds channels c..c+7 of the first half, b the matching
+// channels of the second half (bf16x2 words in, f16x2 words out); cs/sn the 8 cos/sin.
+__device__ __forceinline__ void rotate8(uint4& a, uint4& b, const float4 c0, const float4 c1,
+                                        const float4 s0, const float4 s1) {
+  const float cs[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+  const float sn[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+  uint32_t aw[4] = {a.x, a.y, a.z, a.w};
+  uint32_t bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    const float x1l = bf16lo_to_f32(aw[w]), x1h = bf16hi_to_f32(aw[w]);
+    const float x2l = bf16lo_to_f32(bw[w]), x2h = bf16hi_to_f32(bw[w]);
+    const float cl = cs[2 * w], ch = cs[2 * w + 1], sl = sn[2 * w], sh = sn[2 * w + 1];
+    aw[w] = pack_f16x2_satfinite(fmaf(x1l, cl, -x2l * sl), fmaf(x1h, ch, -x2h * sh));
+    bw[w] = pack_f16x2_satfinite(fmaf(x1l, sl, x2l * cl), fmaf(x1h, sh, x2h * ch));
+  }
+  a = make_uint4(aw[0], aw[1], aw[2], aw[3]);
+  b = make_uint4(bw[0], bw[1], bw[2], bw[3]);
+}
+
+// Rotates one landed [128 x D] tile in place with table rows row0 .. row0+127.
+// Called by the 128 threads of the auxiliary warpgroup (at = 0..127).
+template <int D>
+__device__ __forceinline__ void rope_tile(uint32_t tile, const float* __restrict__ cos_t,
+                                          const float* __restrict__ sin_t, int row0, int at) {
+  constexpr int kHalf = D / 2;
+  constexpr int kChunks = kHalf / 8;                 // 16-byte chunks per half row
+  constexpr int kItems = 128 * kChunks;
+  constexpr int kPerThread = kItems / 128;
+#pragma unroll
+  for (int it0 = 0; it0 < kPerThread; it0 += 4) {
+    uint4 a[4], b[4];
+    float4 c0[4], c1[4], s0[4], s1[4];
+    uint32_t offa[4], offb[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int item = at + 128 * (it0 + u);
+      const int row = item / kChunks, ch = item % kChunks;
+      if (D == 128) {
+        offa[u] = sw128_offset(row, ch);
+        offb[u] = 16384u + offa[u];
+      } else {
+        offa[u] = sw128_offset(row, ch);
+        offb[u] = sw128_offset(row, ch + 4);
+      }
+      a[u] = lds128(tile + offa[u]);
+      b[u] = lds128(tile + offb[u]);
+      const size_t t = static_cast<size_t>(row0 + row) * kHalf + ch * 8;
+      c0[u] = __ldg(reinterpret_cast<const float4*>(cos_t + t));
+      c1[u] = __ldg(reinterpret_cast<const float4*>(cos_t + t + 4));
+      s0[u] = __ldg(reinterpret_cast<const float4*>(sin_t + t));
+      s1[u] = __ldg(reinterpret_cast<const float4*>(sin_t + t + 4));
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      rotate8(a[u], b[u], c0[u], c1[u], s0[u], s1[u]);
+      sts128(tile + offa[u], a[u]);
+      sts128(tile + offb[u], b[u]);
+    }
+  }
+}
+
+// Zeroes rows [first_row, 128) of a landed [128 x D] V tile (all sub-tiles).
+template <int D>
+__device__ __forceinline__ void zero_rows(uint32_t tile, int first_row, int at) {
+  constexpr int kSub = D / 64;
+  const int nrows = 128 - first_row;
+  const int nchunks = nrows * 8 * kSub;
+  for (int i = at; i < nchunks; i += 128) {
+    const int sub = i / (nrows * 8);
+    const int rem = i % (nrows * 8);
+    const int row = first_row + rem / 8;
+    sts128(tile + sub * 16384 + row * 128 + (rem % 8) * 16, make_uint4(0, 0, 0, 0));
+  }
+}
+
+template <int D, int kMode>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const KParams p) {
+  using C = Cfg<D>;
+  constexpr int NS = C::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t s_base = smem_u32(smem);
+  const uint32_t sQ = s_base + C::kOffQ;
+  const uint32_t sK0 = s_base + C::kOffK;
+  const uint32_t sV0 = s_base + C::kOffV;
+  const uint32_t sP = s_base + C::kOffP;
+  Bars* bars = reinterpret_cast<Bars*>(smem + C::kOffBar);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int q0 = blockIdx.x * 128, h = blockIdx.y, b = blockIdx.z;
+  int kv_valid = p.kv_valid;
+  if (kMode == kModeCross) kv_valid = min(max(p.kv_valid_dev[b], 0), p.Skv);
+  const bool live = (q0 < p.q_valid) && (kv_valid > 0);
+
+  if (!live) {
+    // The whole tile is pad rows, or there are no keys: O = 0, LSE = -inf.
+    for (int i = tid; i < 128 * (D / 8); i += kThreads) {
+      const int row = i / (D / 8), ch = i % (D / 8);
+      uint16_t* dst = p.out + ((static_cast<size_t>(b) * p.Sq + q0 + row) * p.H + h) * D + ch * 8;
+      *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+    }
+    if (tid < 128) p.lse[(static_cast<size_t>(b) * p.Sq + q0 + tid) * p.H + h] = -INFINITY;
+    return;
+  }
+  const int n_kv = (kv_valid + 127) / 128;
+
+  volatile int* abort_flag = &bars->abort;
+  unsigned int* status = &g_dit_status;
+  const uint32_t b_q_full = smem_u32(&bars->q_full), b_q_ready = smem_u32(&bars->q_ready);
+  const uint32_t b_p_full = smem_u32(&bars->p_full), b_o_done = smem_u32(&bars->o_done);
+
+  if (tid == 0) {
+    bars->abort = 0;
+    mbar_init(b_q_full, 1);
+    mbar_init(b_q_ready, 1);
+    for (int s = 0; s < NS; ++s) {
+      mbar_init(smem_u32(&bars->k_full[s]), 1);
+      mbar_init(smem_u32(&bars->k_ready[s]), 1);
+      mbar_init(smem_u32(&bars->k_empty[s]), 1);
+      mbar_init(smem_u32(&bars->v_full[s]), 1);
+      mbar_init(smem_u32(&bars->v_ready[s]), 1);
+      mbar_init(smem_u32(&bars->v_empty[s]), 1);
+    }
+    mbar_init(smem_u32(&bars->s_full[0]), 1);
+    mbar_init(smem_u32(&bars->s_full[1]), 1);
+    mbar_init(b_p_full, 128);
+    mbar_init(b_o_done, 1);
+    mbar_init(smem_u32(&bars->drain), 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&bars->tmem_base), 512);
+    tmem_relinquish();
+  }
+  if (tid == 32) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tbase = bars->tmem_base;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ TMA producer
+      int nk[NS], nvl[NS];
+#pragma unroll
+      for (int s = 0; s < NS; ++s) nk[s] = nvl[s] = 0;
+      mbar_arrive_expect_tx(b_q_full, C::kTileBytes);
+#pragma unroll
+      for (int c = 0; c < C::kSub; ++c) tma_load_4d(sQ + c * 16384, &tm_q, b_q_full, c * 64, h, q0, b);
+      for (int j = 0; j < n_kv; ++j) {
+        const int s = j % NS, u = j / NS;
+        const uint32_t kf = smem_u32(&bars->k_full[s]), vf = smem_u32(&bars->v_full[s]);
+        if (u > 0 && !bounded_wait(smem_u32(&bars->k_empty[s]), (u - 1) & 1, abort_flag, status,
+                                   kStatusTimeoutLoad))
+          break;
+        mbar_arrive_expect_tx(kf, C::kTileBytes);
+#pragma unroll
+        for (int c = 0; c < C::kSub; ++c)
+          tma_load_4d(sK0 + s * C::kTileBytes + c * 16384, &tm_k, kf, c * 64, h, j * 128, b);
+        ++nk[s];
+        if (u > 0 && !bounded_wait(smem_u32(&bars->v_empty[s]), (u - 1) & 1, abort_flag, status,
+                                   kStatusTimeoutLoad))
+          break;
+        mbar_arrive_expect_tx(vf, C::kTileBytes);
+#pragma unroll
+        for (int c = 0; c < C::kSub; ++c)
+          tma_load_4d(sV0 + s * C::kTileBytes + c * 16384, &tm_v, vf, c * 64, h, j * 128, b);
+        ++nvl[s];
+      }
+      if (*abort_flag) {
+        // Let every copy this thread started land before the CTA gives up its memory.
+        drain_wait(b_q_full, 0, status);
+        for (int s = 0; s < NS; ++s) {
+          if (nk[s] > 0) drain_wait(smem_u32(&bars->k_full[s]), (nk[s] - 1) & 1, status);
+          if (nvl[s] > 0) drain_wait(smem_u32(&bars->v_full[s]), (nvl[s] - 1) & 1, status);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ MMA issuer
+      // S = Q K^T: fp16 operands after the fused rotation, the raw bf16 inputs otherwise.
+      constexpr uint32_t kIdS = idesc_f16kind_f32(128, 128, kMode != kModeRope, false, false);
+      constexpr uint32_t kIdO = idesc_bf16_f32(128, D, false, true);
+      const uint32_t tO = tbase + 256;
+      bool ok = bounded_wait(kMode == kModeRope ? b_q_ready : b_q_full, 0, abort_flag, status,
+                             kStatusTimeoutMma);
+      auto issue_s = [&](int j) -> bool {
+        const int s = j % NS;
+        const uint32_t kbar = (kMode == kModeRope) ? smem_u32(&bars->k_ready[s]) : smem_u32(&bars->k_full[s]);
+        if (!bounded_wait(kbar, (j / NS) & 1, abort_flag, status, kStatusTimeoutMma)) return false;
+        tc_fence_after_sync();
+        const uint32_t sK = sK0 + s * C::kTileBytes;
+        const uint32_t d = tbase + (j & 1) * 128;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
+          mma_bf16_ss(d, smem_desc_sw128(sQ + off, 16, 1024), smem_desc_sw128(sK + off, 16, 1024),
+                      kIdS, kk > 0);
+        }
+        mma_commit(smem_u32(&bars->s_full[j & 1]));
+        mma_commit(smem_u32(&bars->k_empty[s]));
+        return true;
+      };
+      auto issue_pv = [&](int j) -> bool {
+        const int s = j % NS;
+        if (!bounded_wait(b_p_full, j & 1, abort_flag, status, kStatusTimeoutMma)) return false;
+        const uint32_t vbar = (kMode == kModeCross) ? smem_u32(&bars->v_ready[s]) : smem_u32(&bars->v_full[s]);
+        if (!bounded_wait(vbar, (j / NS) & 1, abort_flag, status, kStatusTimeoutMma)) return false;
+        tc_fence_after_sync();
+        const uint32_t sV = sV0 + s * C::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t a = smem_desc_sw128(sP + (kk / 4) * 16384 + (kk % 4) * 32, 16, 1024);
+          const uint64_t bd = smem_desc_sw128(sV + kk * 2048, 16384, 1024);
+          mma_bf16_ss(tO, a, bd, kIdO, (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(b_o_done);
+        mma_commit(smem_u32(&bars->v_empty[s]));
+        return true;
+      };
+      if (ok) ok = issue_s(0);
+      for (int j = 1; ok && j < n_kv; ++j) {
+        ok = issue_s(j);
+        if (ok) ok = issue_pv(j - 1);
+      }
+      if (ok) ok = issue_pv(n_kv - 1);
+      if (*abort_flag) {
+        // Wait for every MMA issued so far before TMEM and shared memory are released.
+        mma_commit(smem_u32(&bars->drain));
+        drain_wait(smem_u32(&bars->drain), 0, status);
+      }
+    }
+  } else if (warp >= 4 && warp < 8) {
+    // -------------------------------------------------------------- softmax + epilogue
+    const int r = tid - 128;                         // query row within the tile = TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>((warp - 4) * 32) << 16;
+    const uint32_t tO = tbase + lane_off + 256;
+    const float sl2 = p.scale_log2;
+    float m_used = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_kv; ++j) {
+      if (!warp_wait(smem_u32(&bars->s_full[j & 1]), (j >> 1) & 1, abort_flag, status,
+                     kStatusTimeoutSoftmax)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      const uint32_t tS = tbase + lane_off + (j & 1) * 128;
+      const int nv = min(128, kv_valid - j * 128);   // valid keys in this tile (>= 1)
+      // Pass 1: row max over the valid keys.
+      float mx = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t sr[32];
+        tmem_ld32(tS + c * 32, sr);
+        if (nv == 128) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(sr[i]));
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (c * 32 + i < nv) mx = fmaxf(mx, __uint_as_float(sr[i]));
+        }
+      }
+      const float mt = mx * sl2;
+      const bool resc = mt > m_used + kRescaleThreshold;
+      const float m_new = resc ? mt : m_used;
+      const float alpha = ex2_approx(m_used - m_new);   // 1 if kept; 0 on the first tile
+      if (j > 0) {
+        // P_{j-1} V_{j-1} must be complete: it frees the P buffer and updates O.
+        if (!warp_wait(b_o_done, (j - 1) & 1, abort_flag, status, kStatusTimeoutSoftmax)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        if (__any_sync(0xffffffffu, resc)) {
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t orr[32];
+            tmem_ld32(tO + c * 32, orr);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
+            tmem_st32(tO + c * 32, orr);
+          }
+        }
+      }
+      l *= alpha;
+      m_used = m_new;
+      const float neg_m = -m_used;
+      // Pass 2: P = 2^(s * scale * log2 e - m), masked; row sum; P (bf16) to shared memory.
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t sr[32];
+        tmem_ld32(tS + c * 32, sr);
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const int col = c * 32 + 2 * i;
+          float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * i]), sl2, neg_m));
+          float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * i + 1]), sl2, neg_m));
+          if (nv < 128) {
+            p0 = (col < nv) ? p0 : 0.f;
+            p1 = (col + 1 < nv) ? p1 : 0.f;
+          }
+          l += p0 + p1;
+          pk[i] = pack_bf16x2(p0, p1);
+        }
+        const uint32_t sub = sP + (c / 2) * 16384;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4)
+          sts128(sub + sw128_offset(r, (c % 2) * 4 + q4),
+                 make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]));
+      }
+      fence_proxy_async_smem();
+      tc_fence_before_sync();
+      mbar_arrive(b_p_full);
+    }
+    if (ok && warp_wait(b_o_done, (n_kv - 1) & 1, abort_flag, status, kStatusTimeoutSoftmax)) {
+      tc_fence_after_sync();
+      const int qrow = q0 + r;
+      const bool valid_row = qrow < p.q_valid;
+      const float inv_l = 1.f / l;
+      uint16_t* dst = p.out + ((static_cast<size_t>(b) * p.Sq + qrow) * p.H + h) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t orr[32];
+        tmem_ld32(tO + c * 32, orr);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          uint4 w = make_uint4(0, 0, 0, 0);
+          if (valid_row) {
+            const float* f = reinterpret_cast<const float*>(&orr[8 * q4]);
+            w.x = pack_bf16x2(f[0] * inv_l, f[1] * inv_l);
+            w.y = pack_bf16x2(f[2] * inv_l, f[3] * inv_l);
+            w.z = pack_bf16x2(f[4] * inv_l, f[5] * inv_l);
+            w.w = pack_bf16x2(f[6] * inv_l, f[7] * inv_l);
+          }
+          *reinterpret_cast<uint4*>(dst + c * 32 + q4 * 8) = w;
+        }
+      }
+      p.lse[(static_cast<size_t>(b) * p.Sq + qrow) * p.H + h] =
+          valid_row ? (m_used + log2f(l)) * kLn2 : -INFINITY;
+    }
+  } else if (warp >= 8) {
+    // ------------------------------------------------------------ auxiliary warpgroup
+    const int at = tid - 256;
+    volatile int* go = &bars->aux_go;
+    if (kMode == kModeRope) {
+      if (group_wait(b_q_full, 0, abort_flag, status, kStatusTimeoutRope, go, at)) {
+        rope_tile<D>(sQ, p.cos_q, p.sin_q, q0, at);
+        fence_proxy_async_smem();
+        named_bar_sync(1, 128);
+        if (at == 0) mbar_arrive(b_q_ready);
+        for (int j = 0; j < n_kv; ++j) {
+          const int s = j % NS;
+          if (!group_wait(smem_u32(&bars->k_full[s]), (j / NS) & 1, abort_flag, status,
+                          kStatusTimeoutRope, go, at))
+            break;
+          rope_tile<D>(sK0 + s * C::kTileBytes, p.cos_k, p.sin_k, j * 128, at);
+          fence_proxy_async_smem();
+          named_bar_sync(1, 128);
+          if (at == 0) mbar_arrive(smem_u32(&bars->k_ready[s]));
+        }
+      }
+    } else if (kMode == kModeCross) {
+      for (int j = 0; j < n_kv; ++j) {
+        const int s = j % NS;
+        if (!group_wait(smem_u32(&bars->v_full[s]), (j / NS) & 1, abort_flag, status,
+                        kStatusTimeoutRope, go, at))
+          break;
+        const int nv = min(128, kv_valid - j * 128);
+        if (nv < 128) {
+          zero_rows<D>(sV0 + s * C::kTileBytes, nv, at);
+          fence_proxy_async_smem();
+        }
+        named_bar_sync(1, 128);
+        if (at == 0) mbar_arrive(smem_u32(&bars->v_ready[s]));
+      }
+    }
+  }
+  __syncwarp();
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  if (warp == 1) tmem_dealloc(tbase, 512);
+}
+
+template <int D, int kMode>
+cudaError_t launch_mode(const AttnArgs& a) {
+  CUtensorMap mq, mk, mv;
+  const int qext = a.q_valid > 0 ? a.q_valid : 1;
+  // Cross-attention reads up to Skv rows and masks per batch on the device; self-attention
+  // cuts the key/value extent to the valid length so pad rows are never even loaded.
+  const int kvext = (kMode == kModeCross) ? a.Skv : (a.kv_valid > 0 ? a.kv_valid : 1);
+  if (!encode_bshd_map(&mq, a.q, a.B, qext, a.Sq, a.H, D) ||
+      !encode_bshd_map(&mk, a.k, a.B, kvext, a.Skv, a.H, D) ||
+      !encode_bshd_map(&mv, a.v, a.B, kvext, a.Skv, a.H, D))
+    return cudaErrorInvalidValue;
+  KParams p;
+  p.Sq = a.Sq;
+  p.Skv = a.Skv;
+  p.H = a.H;
+  p.q_valid = a.q_valid;
+  p.kv_valid = a.kv_valid;
+  p.kv_valid_dev = a.kv_valid_dev;
+  p.cos_q = a.cos_q;
+  p.sin_q = a.sin_q;
+  p.cos_k = a.cos_k;
+  p.sin_k = a.sin_k;
+  p.scale_log2 = a.scale * kLog2e;
+  p.out = static_cast<uint16_t*>(a.out);
+  p.lse = a.lse;
+  auto kern = attn_fwd_kernel<D, kMode>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  dim3 grid(a.Sq / 128, a.H, a.B);
+  kern<<<grid, kThreads, Cfg<D>::kSmemBytes, a.stream>>>(mq, mk, mv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_attn_fwd(const AttnArgs& a, AttnMode mode) {
+  if (a.D == 128) {
+    if (mode == kModeRope) return launch_mode<128, kModeRope>(a);
+    if (mode == kModeCross) return launch_mode<128, kModeCross>(a);
+    return launch_mode<128, kModePlain>(a);
+  }
+  if (mode == kModeRope) return launch_mode<64, kModeRope>(a);
+  if (mode == kModeCross) return launch_mode<64, kModeCross>(a);
+  return launch_mode<64, kModePlain>(a);
+}
+
+cudaError_t read_device_status(unsigned int* out, bool clear) {
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return e;
+  e = cudaMemcpyFromSymbol(out, g_dit_status, sizeof(unsigned int));
+  if (e != cudaSuccess) return e;
+  if (clear) {
+    const unsigned int zero = 0;
+    e = cudaMemcpyToSymbol(g_dit_status, &zero, sizeof(unsigned int));
+  }
+  return e;
+}
+
+}  // namespace dit

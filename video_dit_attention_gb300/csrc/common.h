@@ -1,0 +1,56 @@
+// Internal declarations shared by the C-ABI layer (api.cu) and the kernel files.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace dit {
+
+// One attention launch: self-attention (optionally with fused RoPE) or short-KV
+// cross-attention. Pointers are device pointers; shapes as in include/dit_attn.h.
+struct AttnArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  int B, Sq, Skv, H, D;
+  int q_valid;
+  int kv_valid;                 // self-attention: one length for every batch
+  const int32_t* kv_valid_dev;  // cross-attention: per-batch lengths on the device
+  const float* cos_q;
+  const float* sin_q;
+  const float* cos_k;
+  const float* sin_k;
+  float scale;
+  void* out;
+  float* lse;
+  cudaStream_t stream;
+};
+
+enum AttnMode : int {
+  kModePlain = 0,  // no RoPE, one kv length
+  kModeRope = 1,   // RoPE fused into the q/k tile load
+  kModeCross = 2,  // no RoPE, per-batch kv length read on the device
+};
+
+cudaError_t launch_attn_fwd(const AttnArgs& a, AttnMode mode);
+
+cudaError_t launch_rope_split_halves(const void* x, void* y, const float* cos_tab,
+                                     const float* sin_tab, int B, int S, int H, int D,
+                                     cudaStream_t stream);
+
+cudaError_t launch_lse_merge(const void* partial_o, const float* partial_lse, int n, int B,
+                             int S, int H, int D, void* out, float* lse, cudaStream_t stream);
+
+cudaError_t launch_copy_rows(const void* src, void* dst, int B, int L, long long src_rows,
+                             long long dst_rows, long long row_bytes, cudaStream_t stream);
+
+cudaError_t read_device_status(unsigned int* out, bool clear);
+
+// Encodes a TMA descriptor for a BSHD bf16 tensor [B, S_rows, H, D] whose sequence extent is
+// cut to `s_extent` rows (reads past it return zeros), with a box of 64 channels x 1 head x
+// 128 rows x 1 batch and the 128-byte swizzle. Returns false if the driver rejects it.
+bool encode_bshd_map(CUtensorMap* map, const void* base, int B, int s_extent, int s_rows, int H,
+                     int D);
+
+}  // namespace dit

@@ -1,0 +1,245 @@
+"""Python binding of libdit_attn.so: one function per C-ABI entry point, same names.
+
+This layer only marshals arguments: it checks tensor placement, dtype, layout and shapes,
+allocates outputs with torch (device memory only), passes raw pointers and the current CUDA
+stream, and raises ``DitError`` on a non-zero status. Every step of the computation runs in
+the library's CUDA kernels; there is no fallback. Importing this module raises ImportError
+if the library has not been built (``video_dit_attention_gb300/build.py``).
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libdit_attn.so")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is missing: build it with `python video_dit_attention_gb300/build.py` "
+                      "(nvcc, sm_103a). There is no CPU fallback.")
+_lib = ctypes.CDLL(LIB_PATH)
+
+_vp, _i, _f, _d, _ll = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_double, ctypes.c_longlong
+_fp = ctypes.POINTER(ctypes.c_float)
+
+_SIGNATURES = {
+    "dit_status_string": ([_i], ctypes.c_char_p),
+    "dit_last_cuda_error": ([], _i),
+    "dit_device_status": ([ctypes.POINTER(ctypes.c_uint), _i], _i),
+    "dit_rope_table_1d": ([_fp, _fp, _i, _i, _i, _d, _i], _i),
+    "dit_rope_table_3d": ([_fp, _fp, _i, _i, _i, _i, _i, _i, _i, _i, _d], _i),
+    "dit_rope_split_halves": ([_vp, _vp, _vp, _vp, _i, _i, _i, _i, _vp], _i),
+    "dit_attn_fwd": ([_vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _f, _vp, _vp, _vp], _i),
+    "dit_cross_attn_shortkv": ([_vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _f, _vp, _vp, _vp], _i),
+    "dit_attn_lse_merge": ([_vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp], _i),
+    "dit_pad_tokens": ([_vp, _vp, _i, _i, _i, _ll, _vp], _i),
+    "dit_unpad_tokens": ([_vp, _vp, _i, _i, _i, _ll, _vp], _i),
+}
+for _name, (_args, _res) in _SIGNATURES.items():
+    _fn = getattr(_lib, _name)
+    _fn.argtypes = _args
+    _fn.restype = _res
+
+DIT_OK, DIT_ERR_INVALID_ARG, DIT_ERR_UNSUPPORTED, DIT_ERR_ALIGNMENT, DIT_ERR_CUDA, DIT_ERR_TIMEOUT = 0, -1, -2, -3, -4, -5
+
+
+class DitError(ValueError):
+    """A library call returned a non-zero status."""
+
+    def __init__(self, name, status):
+        msg = _lib.dit_status_string(status).decode()
+        if status == DIT_ERR_CUDA:
+            msg += f" (cudaError {_lib.dit_last_cuda_error()})"
+        super().__init__(f"{name}: {msg}")
+        self.status = status
+
+
+def _check(name, status):
+    if status != DIT_OK:
+        raise DitError(name, status)
+
+
+def _stream_handle(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _need(t, name, dtype, ndim=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor (the library has no CPU path)")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
+
+
+def dit_status_string(status: int) -> str:
+    return _lib.dit_status_string(status).decode()
+
+
+def dit_device_status(clear: bool = True) -> int:
+    """Status word of the current device (bits of kernels that gave up on a bounded wait)."""
+    out = ctypes.c_uint(0)
+    _check("dit_device_status", _lib.dit_device_status(ctypes.byref(out), 1 if clear else 0))
+    return int(out.value)
+
+
+# ----------------------------------------------------------------------------- RoPE tables
+def dit_rope_table_1d(S_pad: int, L: int, D: int, theta: float = 10000.0, pos_offset: int = 0):
+    """Host cos/sin tables [S_pad, D/2] fp32 (numpy) for positions pos_offset .. pos_offset+L-1;
+    rows >= L are the identity rotation."""
+    cos = np.empty((S_pad, D // 2), dtype=np.float32)
+    sin = np.empty((S_pad, D // 2), dtype=np.float32)
+    _check("dit_rope_table_1d", _lib.dit_rope_table_1d(
+        cos.ctypes.data_as(_fp), sin.ctypes.data_as(_fp), S_pad, L, D, float(theta), pos_offset))
+    return cos, sin
+
+
+def dit_rope_table_3d(S_pad: int, grid, D: int = 128, axis_dims=(44, 42, 42), theta: float = 10000.0):
+    """Host cos/sin tables [S_pad, D/2] fp32 (numpy) for a T x Hh x W token grid (row-major);
+    rows >= T*Hh*W are the identity rotation."""
+    T, Hh, W = grid
+    cos = np.empty((S_pad, D // 2), dtype=np.float32)
+    sin = np.empty((S_pad, D // 2), dtype=np.float32)
+    _check("dit_rope_table_3d", _lib.dit_rope_table_3d(
+        cos.ctypes.data_as(_fp), sin.ctypes.data_as(_fp), S_pad, T, Hh, W, D,
+        axis_dims[0], axis_dims[1], axis_dims[2], float(theta)))
+    return cos, sin
+
+
+# ----------------------------------------------------------------------------- device calls
+def dit_rope_split_halves(x, cos, sin, out=None, stream=None):
+    """y = split-halves RoPE of x [B, S, H, D] bf16 with device tables [S, D/2] fp32.
+    out may be x itself (in place)."""
+    _need(x, "x", torch.bfloat16, 4)
+    B, S, H, D = x.shape
+    _need(cos, "cos", torch.float32, 2)
+    _need(sin, "sin", torch.float32, 2)
+    if tuple(cos.shape) != (S, D // 2) or tuple(sin.shape) != (S, D // 2):
+        raise ValueError(f"tables must be [{S}, {D // 2}]")
+    if out is None:
+        out = torch.empty_like(x)
+    _need(out, "out", torch.bfloat16, 4)
+    if out.shape != x.shape:
+        raise ValueError("out must have x's shape")
+    _check("dit_rope_split_halves", _lib.dit_rope_split_halves(
+        _ptr(x), _ptr(out), _ptr(cos), _ptr(sin), B, S, H, D, _stream_handle(stream)))
+    return out
+
+
+def _attn_outputs(q, out, lse):
+    B, Sq, H, D = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((B, Sq, H), dtype=torch.float32, device=q.device)
+    _need(out, "out", torch.bfloat16, 4)
+    _need(lse, "lse", torch.float32, 3)
+    if out.shape != q.shape or tuple(lse.shape) != (B, Sq, H):
+        raise ValueError("out must be [B, Sq, H, D] and lse [B, Sq, H]")
+    return out, lse
+
+
+def dit_attn_fwd(q, k, v, q_valid_len: int, kv_valid_len: int, cos_q=None, sin_q=None,
+                 cos_k=None, sin_k=None, softmax_scale=None, out=None, lse=None, stream=None):
+    """Masked attention over padded BSHD bf16 tensors, RoPE fused when tables are given.
+    Returns (out [B, Sq, H, D] bf16, lse [B, Sq, H] fp32, natural log)."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, torch.bfloat16, 4)
+    B, Sq, H, D = q.shape
+    Skv = k.shape[1]
+    if tuple(k.shape) != (B, Skv, H, D) or v.shape != k.shape:
+        raise ValueError("k and v must be [B, Skv, H, D] matching q")
+    tables = (cos_q, sin_q, cos_k, sin_k)
+    if any(t is not None for t in tables):
+        if any(t is None for t in tables):
+            raise ValueError("give all four RoPE tables or none")
+        for t, n, rows in ((cos_q, "cos_q", Sq), (sin_q, "sin_q", Sq), (cos_k, "cos_k", Skv), (sin_k, "sin_k", Skv)):
+            _need(t, n, torch.float32, 2)
+            if tuple(t.shape) != (rows, D // 2):
+                raise ValueError(f"{n} must be [{rows}, {D // 2}]")
+    scale = 1.0 / math.sqrt(D) if softmax_scale is None else float(softmax_scale)
+    out, lse = _attn_outputs(q, out, lse)
+    _check("dit_attn_fwd", _lib.dit_attn_fwd(
+        _ptr(q), _ptr(k), _ptr(v), B, Sq, Skv, H, D, int(q_valid_len), int(kv_valid_len),
+        _ptr(cos_q), _ptr(sin_q), _ptr(cos_k), _ptr(sin_k), scale, _ptr(out), _ptr(lse),
+        _stream_handle(stream)))
+    return out, lse
+
+
+def dit_cross_attn_shortkv(q, k, v, q_valid_len: int, kv_valid_len_dev, softmax_scale=None,
+                           out=None, lse=None, stream=None):
+    """Short-KV cross-attention; kv_valid_len_dev: int32 CUDA tensor [B] of valid key counts."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, torch.bfloat16, 4)
+    _need(kv_valid_len_dev, "kv_valid_len_dev", torch.int32, 1)
+    B, Sq, H, D = q.shape
+    Skv = k.shape[1]
+    if tuple(k.shape) != (B, Skv, H, D) or v.shape != k.shape or kv_valid_len_dev.shape[0] != B:
+        raise ValueError("k, v must be [B, Skv, H, D] and kv_valid_len_dev [B]")
+    scale = 1.0 / math.sqrt(D) if softmax_scale is None else float(softmax_scale)
+    out, lse = _attn_outputs(q, out, lse)
+    _check("dit_cross_attn_shortkv", _lib.dit_cross_attn_shortkv(
+        _ptr(q), _ptr(k), _ptr(v), B, Sq, Skv, H, D, int(q_valid_len), _ptr(kv_valid_len_dev),
+        scale, _ptr(out), _ptr(lse), _stream_handle(stream)))
+    return out, lse
+
+
+def dit_attn_lse_merge(partial_o, partial_lse, out=None, lse=None, stream=None):
+    """Merges n partials: partial_o [n, B, S, H, D] bf16, partial_lse [n, B, S, H] fp32."""
+    _need(partial_o, "partial_o", torch.bfloat16, 5)
+    _need(partial_lse, "partial_lse", torch.float32, 4)
+    n, B, S, H, D = partial_o.shape
+    if tuple(partial_lse.shape) != (n, B, S, H):
+        raise ValueError("partial_lse must be [n, B, S, H]")
+    if out is None:
+        out = torch.empty((B, S, H, D), dtype=torch.bfloat16, device=partial_o.device)
+    if lse is None:
+        lse = torch.empty((B, S, H), dtype=torch.float32, device=partial_o.device)
+    _need(out, "out", torch.bfloat16, 4)
+    _need(lse, "lse", torch.float32, 3)
+    _check("dit_attn_lse_merge", _lib.dit_attn_lse_merge(
+        _ptr(partial_o), _ptr(partial_lse), n, B, S, H, D, _ptr(out), _ptr(lse), _stream_handle(stream)))
+    return out, lse
+
+
+def dit_pad_tokens(x, S_pad: int, out=None, stream=None):
+    """Copies x [B, L, ...] into the first L rows of a [B, S_pad, ...] buffer (pad rows untouched)."""
+    if not x.is_cuda or not x.is_contiguous():
+        raise ValueError("x must be a contiguous CUDA tensor")
+    B, L = x.shape[:2]
+    if out is None:
+        out = torch.empty((B, S_pad) + tuple(x.shape[2:]), dtype=x.dtype, device=x.device)
+    if not out.is_contiguous() or out.dtype != x.dtype or tuple(out.shape) != (B, S_pad) + tuple(x.shape[2:]):
+        raise ValueError("out must be a contiguous [B, S_pad, ...] tensor of x's dtype")
+    row_bytes = x[0, 0].numel() * x.element_size() if L > 0 else out[0, 0].numel() * out.element_size()
+    _check("dit_pad_tokens", _lib.dit_pad_tokens(_ptr(x), _ptr(out), B, L, S_pad, row_bytes,
+                                                 _stream_handle(stream)))
+    return out
+
+
+def dit_unpad_tokens(x_pad, L: int, out=None, stream=None):
+    """Copies the first L rows of x_pad [B, S_pad, ...] into a [B, L, ...] tensor."""
+    if not x_pad.is_cuda or not x_pad.is_contiguous():
+        raise ValueError("x_pad must be a contiguous CUDA tensor")
+    B, S_pad = x_pad.shape[:2]
+    if out is None:
+        out = torch.empty((B, L) + tuple(x_pad.shape[2:]), dtype=x_pad.dtype, device=x_pad.device)
+    if not out.is_contiguous() or out.dtype != x_pad.dtype or tuple(out.shape) != (B, L) + tuple(x_pad.shape[2:]):
+        raise ValueError("out must be a contiguous [B, L, ...] tensor of x_pad's dtype")
+    row_bytes = x_pad[0, 0].numel() * x_pad.element_size()
+    _check("dit_unpad_tokens", _lib.dit_unpad_tokens(_ptr(x_pad), _ptr(out), B, L, S_pad, row_bytes,
+                                                     _stream_handle(stream)))
+    return out

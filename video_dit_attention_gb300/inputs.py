@@ -27,11 +27,15 @@ def padded_len(n: int, multiple: int = TILE) -> int:
 
 
 def bf16_round(x: np.ndarray) -> np.ndarray:
-    """fp32 -> nearest bf16 value (ties to even), returned as fp32. Inputs must be finite."""
-    x = np.ascontiguousarray(x, dtype=np.float32)
-    u = x.view(np.uint32).astype(np.uint64)
-    u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
-    return u.astype(np.uint32).view(np.float32).reshape(x.shape)
+    """fp32 -> nearest bf16 value (ties to even), returned as fp32. Inputs must be finite
+    (then the 32-bit integer sums below cannot overflow)."""
+    x = np.array(x, dtype=np.float32, copy=True, order="C")
+    u = x.view(np.uint32)
+    lsb = (u >> 16) & np.uint32(1)
+    u += np.uint32(0x7FFF)
+    u += lsb
+    u &= np.uint32(0xFFFF0000)
+    return x
 
 
 def _normal(rng: np.random.Generator, shape, sigma: float = 1.0) -> np.ndarray:
