@@ -82,15 +82,15 @@ def attention(q, k, v, q_valid, kv_valid, scale, angles_q=None, angles_k=None,
     for b in range(B):
         L = kv_list[b]
         # Only the valid prefix of k and v is ever touched: pad keys cannot contribute.
-        kb = k[b:b + 1, :L].astype(np.float64)
-        vb = v[b, :L].astype(np.float64)
-        qb = q[b:b + 1, qrows].astype(np.float64)
+        kb = k[b:b + 1, :L][:, :, heads].astype(np.float64)
+        vb = v[b, :L][:, heads].astype(np.float64)
+        qb = q[b:b + 1, qrows][:, :, heads].astype(np.float64)
         if angles_k is not None:
             kb = rope_split_halves(kb, angles_k[:L])
         if angles_q is not None:
             qb = rope_split_halves(qb, angles_q[qrows])
-        for hi, h in enumerate(heads):
-            o, lse = _rows_attention(qb[0, :, h, :], kb[0, :, h, :], vb[:, h, :], float(scale))
+        for hi in range(len(heads)):
+            o, lse = _rows_attention(qb[0, :, hi, :], kb[0, :, hi, :], vb[:, hi, :], float(scale))
             O[b, valid_sel, hi, :] = o
             LSE[b, valid_sel, hi] = lse
     return O, LSE
