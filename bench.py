@@ -1,0 +1,553 @@
+#!/usr/bin/env python3
+"""Benchmark of the video-DiT attention hot path on GB300 (one JSON line on rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+Workloads (synthetic, seeded; the token grids of the Wan / LTX runs the pages describe):
+  wan480  (default) Wan 480x832x9 self-attention: B1 H40 D128, 3x30x52 = 4680 tokens padded
+          to 4736, 3-D split-halves RoPE fused into the kernel, pad keys masked.
+  wan720  Wan 720p 81-frame self-attention: 21x45x80 = 75,600 tokens padded to 75,648.
+  cross   short-KV cross-attention: B2 H40 D128, 4680 (4736) queries x 512 text slots,
+          per-batch valid lengths uniform on [1, 512].
+  sharded 1024 queries over 37,800 keys in 4 shards (partials + LSE merge), B1 H32 D128.
+  tiny    B1 H2 D64, 300 tokens padded to 384 (correctness-sized).
+
+One step = one pass of the hot path over one batch held in HBM (padded layout, as the
+sequence stays padded between blocks): the attention launch(es) of the workload (for
+`sharded` the four partial launches and the merge). `value` is the algorithmic TFLOP/s on
+valid tokens (4 * B * H * Lq * Lkv * D per attention) over all ranks. Three distinct input
+sets rotate between steps, so every step reads inputs that are not L2-resident. `e2e` is the
+same metric through the C-ABI with host buffers: every step copies the unpadded q/k/v from
+pinned host memory, pads them with dit_pad_tokens, runs the attention, unpads O and LSE with
+dit_unpad_tokens and copies them back. `--impl reference` times the fp64 CPU oracle instead,
+on the host cores, on a bounded sample of the same workload.
+
+Multi-GPU: `python -m torch.distributed.run --nproc-per-node N bench.py --gpus N`; each rank
+runs an independent replica (the problems are independent; no data-path collective), the
+barrier and the max over ranks bracket the timed region, and units add up (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention TFLOP/s (valid tokens) and % of GB300 BF16 peak; ms per call"
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}
+
+
+# ----------------------------------------------------------------------------- helpers
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"bf16_tflops": float(d["bf16_tflops"]),
+                "bf16_tflops_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                "hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    except Exception:
+        return dict(FALLBACK_PEAKS, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def reduce_over_ranks(elapsed_s: float, units: float, world: int):
+    """(max elapsed over ranks, sum of units over ranks); identity for one rank."""
+    if world <= 1:
+        return elapsed_s, units
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([elapsed_s], dtype=torch.float64, device=dev)
+    u = torch.tensor([units], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+class ClockSampler:
+    """nvidia-smi samples (100 ms) of SM clock, power and throttle reasons, host-timestamped."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", gpu_id, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                self.samples.append((time.time(), float(parts[0]), float(parts[1]),
+                                     parts[3:7]))
+            except ValueError:
+                pass
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t0, t1, load_t0):
+        win = [s for s in self.samples if t0 <= s[0] <= t1]
+        where = "timed region"
+        if len(win) < 2:
+            win = [s for s in self.samples if load_t0 <= s[0] <= t1]
+            where = "warm-up and timed region (timed region shorter than the sampling interval)"
+        if not win:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "window": "none"}
+        reasons = sorted({self.NAMES[i] for s in win for i, v in enumerate(s[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(s[1] for s in win), "sm_max_mhz": max(s[2] for s in win),
+                "reasons": reasons, "samples": len(win), "window": where}
+
+
+def gpu_id_for_smi(dev_index: int) -> str:
+    import torch
+    try:
+        p = torch.cuda.get_device_properties(dev_index)
+        return f"{p.pci_domain_id:08X}:{p.pci_bus_id:02X}:{p.pci_device_id:02X}.0"
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        return vis.split(",")[dev_index] if vis else str(dev_index)
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+# ----------------------------------------------------------------------------- workloads
+def workload_spec(name):
+    from video_dit_attention_gb300 import inputs as I
+    if name in ("wan480", "wan720", "tiny"):
+        case = {"wan480": I.wan480_case, "wan720": I.wan720_case, "tiny": I.tiny_case}[name]()
+        return case
+    if name == "cross":
+        return I.cross_case()
+    if name == "sharded":
+        return I.sharded_case()
+    raise SystemExit(f"unknown workload {name}")
+
+
+def config_dict(name, spec):
+    if name == "sharded":
+        return {"workload": "sharded-key attention + LSE merge", "B": spec.B, "H": spec.H, "D": spec.D,
+                "queries": spec.Sq, "keys": sum(spec.shard_valid), "shards": list(spec.shard_valid),
+                "rope": "1-D split halves, theta 10000, global key positions",
+                "l2": "3 rotating input sets of 0.69 GB each (> 129 MB L2)"}
+    d = {"workload": {"wan480": "Wan 480x832x9 self-attention", "wan720": "Wan 720p 81-frame self-attention",
+                      "tiny": "tiny self-attention", "cross": "short-KV cross-attention"}[name],
+         "B": spec.B, "H": spec.H, "D": spec.D, "q_valid": spec.q_valid, "q_padded": spec.Sq,
+         "kv_valid": spec.kv_valid, "kv_padded": spec.Skv}
+    if spec.rope == "3d":
+        d["rope"] = f"3-D split halves fused, grid {'x'.join(map(str, spec.grid))}, 44/42/42, theta 10000"
+    elif spec.rope == "1d":
+        d["rope"] = "1-D split halves fused, theta 10000"
+    else:
+        d["rope"] = "none"
+    d["l2"] = "3 rotating input sets, each larger than the 129 MB L2" if name != "tiny" else "tiny: L2-resident"
+    return d
+
+
+def step_flops(name, spec):
+    if name == "sharded":
+        return sum(4.0 * spec.B * spec.H * spec.q_valid * n * spec.D for n in spec.shard_valid)
+    if name == "cross":
+        return sum(4.0 * spec.H * spec.q_valid * L * spec.D for L in spec.kv_valid)
+    return 4.0 * spec.B * spec.H * spec.q_valid * int(spec.kv_valid) * spec.D
+
+
+class GpuWorkload:
+    """Device buffers and the launch sequence of one step."""
+
+    def __init__(self, name, spec, seed_offset=0):
+        import torch
+
+        from video_dit_attention_gb300 import dit_attn as lib
+        from video_dit_attention_gb300 import inputs as I
+        self.torch, self.lib, self.name, self.spec = torch, lib, name, spec
+        dev = torch.device("cuda")
+        bf = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(torch.bfloat16).to(dev)
+        self.sets = []
+        if name == "sharded":
+            spec.seed += seed_offset
+            q, shards = I.make_sharded(spec)
+            base = (bf(q), [(bf(k), bf(v)) for k, v in shards])
+            self.host = (q, shards)
+            cq, sq = lib.dit_rope_table_1d(spec.Sq, spec.q_valid, spec.D, spec.theta, 0)
+            self.tq = (torch.from_numpy(cq).to(dev), torch.from_numpy(sq).to(dev))
+            self.tk = []
+            for off, n, npad in zip(spec.offsets, spec.shard_valid, spec.shard_pad):
+                ck, sk = lib.dit_rope_table_1d(npad, n, spec.D, spec.theta, off)
+                self.tk.append((torch.from_numpy(ck).to(dev), torch.from_numpy(sk).to(dev)))
+            for r in range(3):
+                qq = torch.roll(base[0], r, dims=2).contiguous()
+                kv = [(torch.roll(k, r, dims=2).contiguous(), torch.roll(v, r, dims=2).contiguous())
+                      for k, v in base[1]]
+                n = len(kv)
+                po = torch.empty((n,) + tuple(qq.shape), dtype=torch.bfloat16, device=dev)
+                pl = torch.empty((n,) + tuple(qq.shape[:3]), dtype=torch.float32, device=dev)
+                out = torch.empty_like(qq)
+                lse = torch.empty(tuple(qq.shape[:3]), dtype=torch.float32, device=dev)
+                self.sets.append((qq, kv, po, pl, out, lse))
+            self.launches_per_step = len(spec.shard_valid) + 1
+        else:
+            spec.seed += seed_offset
+            q, k, v = I.make_qkv(spec)
+            self.host = (q, k, v)
+            base = (bf(q), bf(k), bf(v))
+            if spec.rope == "3d":
+                cq, sq = lib.dit_rope_table_3d(spec.Sq, spec.grid, spec.D, spec.axis_dims, spec.theta)
+                ck, sk = lib.dit_rope_table_3d(spec.Skv, spec.grid, spec.D, spec.axis_dims, spec.theta)
+                self.tables = tuple(torch.from_numpy(t).to(dev) for t in (cq, sq, ck, sk))
+            elif spec.rope == "1d":
+                cq, sq = lib.dit_rope_table_1d(spec.Sq, spec.q_valid, spec.D, spec.theta, 0)
+                ck, sk = lib.dit_rope_table_1d(spec.Skv, int(spec.kv_valid), spec.D, spec.theta, 0)
+                self.tables = tuple(torch.from_numpy(t).to(dev) for t in (cq, sq, ck, sk))
+            else:
+                self.tables = (None, None, None, None)
+            if name == "cross":
+                self.kv_dev = torch.tensor(spec.kv_valid, dtype=torch.int32, device=dev)
+            nsets = 1 if name == "tiny" else 3
+            for r in range(nsets):
+                qq, kk, vv = (torch.roll(t, r, dims=2).contiguous() for t in base)
+                out = torch.empty_like(qq)
+                lse = torch.empty(tuple(qq.shape[:3]), dtype=torch.float32, device=dev)
+                self.sets.append((qq, kk, vv, out, lse))
+            self.launches_per_step = 1
+        torch.cuda.synchronize()
+
+    def step(self, i, ev=None):
+        """Launches one step on the current stream; ev = (start, end) events around the
+        dominant kernel (the attention launch; for `sharded`, the four partial launches)."""
+        lib, spec = self.lib, self.spec
+        s = self.sets[i % len(self.sets)]
+        if ev is not None:
+            ev[0].record()
+        if self.name == "sharded":
+            qq, kv, po, pl, out, lse = s
+            for j, ((k, v), (ck, sk), n) in enumerate(zip(kv, self.tk, spec.shard_valid)):
+                lib.dit_attn_fwd(qq, k, v, spec.q_valid, n, self.tq[0], self.tq[1], ck, sk,
+                                 out=po[j], lse=pl[j])
+            if ev is not None:
+                ev[1].record()
+            lib.dit_attn_lse_merge(po, pl, out=out, lse=lse)
+            return
+        qq, kk, vv, out, lse = s
+        if self.name == "cross":
+            lib.dit_cross_attn_shortkv(qq, kk, vv, spec.q_valid, self.kv_dev, out=out, lse=lse)
+        else:
+            lib.dit_attn_fwd(qq, kk, vv, spec.q_valid, int(spec.kv_valid), *self.tables, out=out, lse=lse)
+        if ev is not None:
+            ev[1].record()
+
+    def dominant_bytes(self):
+        """Algorithmic HBM bytes of the dominant kernel per step (valid rows of q, k, v read;
+        O and LSE written)."""
+        sp = self.spec
+        if self.name == "sharded":
+            kv = sum(2 * sp.B * n * sp.H * sp.D * 2 for n in sp.shard_valid)
+            return kv + len(sp.shard_valid) * (sp.B * sp.q_valid * sp.H * (sp.D * 2 * 2 + 4))
+        Lkv = sum(sp.kv_valid) if self.name == "cross" else sp.B * int(sp.kv_valid)
+        return (sp.B * sp.q_valid * sp.H * sp.D * 2 + 2 * Lkv * sp.H * sp.D * 2
+                + sp.B * sp.q_valid * sp.H * (sp.D * 2 + 4))
+
+
+class E2E:
+    """Host-buffer path through the C-ABI: pinned host q/k/v (unpadded) -> H2D -> pad ->
+    attention -> unpad -> D2H of O and LSE (self-attention and cross workloads)."""
+
+    def __init__(self, wl):
+        torch = wl.torch
+        self.wl, self.torch = wl, torch
+        sp = wl.spec
+        q, k, v = wl.host
+        Lq = sp.q_valid
+        Lk = int(sp.kv_valid) if wl.name != "cross" else sp.Skv
+        pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(torch.bfloat16).pin_memory()
+        self.hq, self.hk, self.hv = pin(q[:, :Lq]), pin(k[:, :Lk]), pin(v[:, :Lk])
+        dev = torch.device("cuda")
+        self.dq = torch.empty(self.hq.shape, dtype=torch.bfloat16, device=dev)
+        self.dk = torch.empty(self.hk.shape, dtype=torch.bfloat16, device=dev)
+        self.dv = torch.empty(self.hv.shape, dtype=torch.bfloat16, device=dev)
+        self.qp = torch.empty((sp.B, sp.Sq, sp.H, sp.D), dtype=torch.bfloat16, device=dev)
+        self.kp = torch.empty((sp.B, sp.Skv, sp.H, sp.D), dtype=torch.bfloat16, device=dev)
+        self.vp = torch.empty_like(self.kp)
+        self.out = torch.empty_like(self.qp)
+        self.lse = torch.empty((sp.B, sp.Sq, sp.H), dtype=torch.float32, device=dev)
+        self.o_u = torch.empty((sp.B, Lq, sp.H, sp.D), dtype=torch.bfloat16, device=dev)
+        self.l_u = torch.empty((sp.B, Lq, sp.H), dtype=torch.float32, device=dev)
+        self.ho = torch.empty(self.o_u.shape, dtype=torch.bfloat16).pin_memory()
+        self.hl = torch.empty(self.l_u.shape, dtype=torch.float32).pin_memory()
+        self.Lq, self.Lk = Lq, Lk
+        self.h2d = sum(t.numel() * t.element_size() for t in (self.hq, self.hk, self.hv))
+        self.d2h = self.ho.numel() * 2 + self.hl.numel() * 4
+        self.launches_per_step = 6
+
+    def step(self):
+        lib, wl, sp = self.wl.lib, self.wl, self.wl.spec
+        self.dq.copy_(self.hq, non_blocking=True)
+        self.dk.copy_(self.hk, non_blocking=True)
+        self.dv.copy_(self.hv, non_blocking=True)
+        lib.dit_pad_tokens(self.dq, sp.Sq, out=self.qp)
+        lib.dit_pad_tokens(self.dk, sp.Skv, out=self.kp)
+        lib.dit_pad_tokens(self.dv, sp.Skv, out=self.vp)
+        if wl.name == "cross":
+            lib.dit_cross_attn_shortkv(self.qp, self.kp, self.vp, sp.q_valid, wl.kv_dev, out=self.out, lse=self.lse)
+        else:
+            lib.dit_attn_fwd(self.qp, self.kp, self.vp, sp.q_valid, int(sp.kv_valid), *wl.tables,
+                             out=self.out, lse=self.lse)
+        lib.dit_unpad_tokens(self.out, self.Lq, out=self.o_u)
+        lib.dit_unpad_tokens(self.lse, self.Lq, out=self.l_u)
+        self.ho.copy_(self.o_u, non_blocking=True)
+        self.hl.copy_(self.l_u, non_blocking=True)
+
+
+# ----------------------------------------------------------------------------- oracle arm
+def oracle_sample(name, spec, host, n_rows, n_heads, seed=0):
+    """Runs the fp64 oracle once on (n_rows query rows) x (n_heads heads) of the workload;
+    returns (seconds, algorithmic FLOPs of the sample)."""
+    from oracle.attention import attention, lse_merge
+    from oracle.rope import pad_angles, rope_angles_1d, rope_angles_3d
+    rng = np.random.Generator(np.random.PCG64(seed))
+    heads = sorted(rng.choice(spec.H, size=min(n_heads, spec.H), replace=False).tolist())
+    rows = sorted(rng.choice(spec.q_valid, size=min(n_rows, spec.q_valid), replace=False).tolist())
+    t0 = time.perf_counter()
+    if name == "sharded":
+        q, shards = host
+        aq = pad_angles(rope_angles_1d(np.arange(spec.q_valid), spec.D, spec.theta), spec.Sq)
+        po, pl = [], []
+        for (k, v), off, n in zip(shards, spec.offsets, spec.shard_valid):
+            ak = pad_angles(rope_angles_1d(np.arange(n) + off, spec.D, spec.theta), k.shape[1])
+            O, L = attention(q, k, v, spec.q_valid, n, spec.scale, aq, ak, rows=rows, heads=heads)
+            po.append(O)
+            pl.append(L)
+        lse_merge(np.stack(po), np.stack(pl))
+        flops = sum(4.0 * len(rows) * len(heads) * n * spec.D for n in spec.shard_valid) * spec.B
+    else:
+        q, k, v = host
+        aq = ak = None
+        if spec.rope == "3d":
+            a = rope_angles_3d(*spec.grid, spec.D, spec.axis_dims, spec.theta)
+            aq, ak = pad_angles(a, spec.Sq), pad_angles(a, spec.Skv)
+        elif spec.rope == "1d":
+            aq = pad_angles(rope_angles_1d(np.arange(spec.q_valid), spec.D, spec.theta), spec.Sq)
+            ak = pad_angles(rope_angles_1d(np.arange(int(spec.kv_valid)), spec.D, spec.theta), spec.Skv)
+        attention(q, k, v, spec.q_valid, spec.kv_valid, spec.scale, aq, ak, rows=rows, heads=heads)
+        Ls = spec.kv_valid if name == "cross" else [int(spec.kv_valid)] * spec.B
+        flops = sum(4.0 * len(rows) * len(heads) * L * spec.D for L in Ls)
+    return time.perf_counter() - t0, flops
+
+
+def host_inputs(name, spec):
+    from video_dit_attention_gb300 import inputs as I
+    if name == "sharded":
+        return I.make_sharded(spec)
+    return I.make_qkv(spec)
+
+
+def cpu_baseline(name, spec, host, budget_s=12.0):
+    """Times the oracle, as it stands, on a bounded sample (about budget_s of CPU work)."""
+    n_rows, n_heads = 32, min(8, spec.H)
+    dt, fl = oracle_sample(name, spec, host, n_rows, n_heads, seed=1)
+    reps = max(1, int(budget_s / max(dt, 1e-3)))
+    tot_t, tot_f = dt, fl
+    for r in range(reps - 1):
+        d, f = oracle_sample(name, spec, host, n_rows, n_heads, seed=2 + r)
+        tot_t += d
+        tot_f += f
+    return {"value": tot_f / tot_t / 1e12, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+            "sample": f"{reps} oracle calls of {n_rows} random valid query rows x {n_heads} heads "
+                      f"(all valid keys), {tot_t:.1f} s of fp64 numpy on the host cores"}
+
+
+def run_reference(args, name, spec, rank, world):
+    if rank != 0:
+        return
+    host = host_inputs(name, spec)
+    # size one step so that warm-up + timed steps end within about two minutes
+    n_rows, n_heads = 16, min(4, spec.H)
+    dt, _ = oracle_sample(name, spec, host, n_rows, n_heads, seed=0)
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    while dt > budget and (n_rows > 1 or n_heads > 1):
+        if n_rows > 1:
+            n_rows //= 2
+        else:
+            n_heads = max(1, n_heads // 2)
+        dt, _ = oracle_sample(name, spec, host, n_rows, n_heads, seed=0)
+    for w in range(args.warmup):
+        oracle_sample(name, spec, host, n_rows, n_heads, seed=100 + w)
+    tt, tf = 0.0, 0.0
+    for s in range(args.steps):
+        d, f = oracle_sample(name, spec, host, n_rows, n_heads, seed=1000 + s)
+        tt += d
+        tf += f
+    value = tf / tt / 1e12
+    sample = (f"each step: the fp64 oracle on {n_rows} random valid query rows x {n_heads} heads "
+              f"with all valid keys (algorithmic FLOPs of that sample)")
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "impl": "reference", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": tt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": config_dict(name, spec),
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="wan480", choices=["wan480", "wan720", "cross", "sharded", "tiny"])
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be >= 3")
+    rank, world, local = dist_env()
+    name = args.workload
+    spec = workload_spec(name)
+
+    if args.impl == "reference":
+        run_reference(args, name, spec, rank, world)
+        return
+
+    import torch
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    peaks = load_peaks()
+    wl = GpuWorkload(name, spec, seed_offset=rank)
+    flops = step_flops(name, spec)
+    stream = torch.cuda.current_stream()
+
+    sampler = ClockSampler(gpu_id_for_smi(local))
+    load_t0 = time.time()
+    for i in range(args.warmup):
+        wl.step(i)
+    torch.cuda.synchronize()
+
+    # timed region: K steps, barrier + synchronize on both sides, per-launch events
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    start.record(stream)
+    for i in range(args.steps):
+        wl.step(i, evs[i])
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    t1 = time.time()
+    elapsed = start.elapsed_time(end) / 1e3
+    kern_s = sum(a.elapsed_time(b) for a, b in evs) / 1e3 / args.steps
+    status = wl.lib.dit_device_status()
+    if status != 0:
+        raise SystemExit(f"device status word {status:#x}: a kernel gave up on a bounded wait")
+
+    # e2e through the C-ABI with host buffers (self / cross workloads)
+    e2e = None
+    if name != "sharded":
+        ee = E2E(wl)
+        for _ in range(max(3, min(args.warmup, 10))):
+            ee.step()
+        torch.cuda.synchronize()
+        n_e2e = max(3, min(args.steps, 200 if name != "wan720" else 10))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize()
+        a.record(stream)
+        for _ in range(n_e2e):
+            ee.step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        e_el, e_units = reduce_over_ranks(a.elapsed_time(b) / 1e3, flops * n_e2e, world)
+        e2e = {"value": e_units / e_el / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": ee.h2d,
+               "d2h_bytes_per_step": ee.d2h, "steps": n_e2e,
+               "path": "pinned host q/k/v -> H2D -> dit_pad_tokens -> attention -> dit_unpad_tokens -> D2H O, LSE"}
+    sampler.stop()
+
+    max_el, units = reduce_over_ranks(elapsed, flops * args.steps, world)
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+    clocks = sampler.summary(t0, t1, load_t0)
+    achieved = flops / kern_s / 1e12
+    peak = peaks["bf16_tflops"]
+    line = {
+        "metric": METRIC, "value": units / max_el / 1e12, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": max_el / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": config_dict(name, spec),
+        "pct_of_bf16_peak": 100.0 * (units / max_el / 1e12) / (peak * world),
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "kernel": "attn_fwd_kernel" if name != "cross" else "attn_fwd_kernel (cross mode)",
+                     "kernel_ms": kern_s * 1e3, "algorithmic_bytes": wl.dominant_bytes(),
+                     "peak_source": f"bf16_tflops (burst) of {peaks['source']} peaks"},
+        "gpu_launches": wl.launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    if e2e is not None:
+        line["e2e"] = e2e
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(name, spec, wl.host)
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
