@@ -150,6 +150,24 @@ def gpu_id_for_smi(dev_index: int) -> str:
         return vis.split(",")[dev_index] if vis else str(dev_index)
 
 
+def profiled_traffic(name):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu summary of this
+    workload, or None if there is none or the kernel sources changed since it was taken."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", {"wan480": "attn_fwd_wan480x832x9.md"}.get(name, "-"))
+    if not os.path.exists(path):
+        return None
+    srcs = [os.path.join(ROOT, "video_dit_attention_gb300", "csrc", f) for f in ("attn_fwd.cu", "ptx.cuh")]
+    h = hashlib.sha256(b"".join(open(f, "rb").read() for f in srcs)).hexdigest()[:16]
+    sha = traffic = None
+    for line in open(path):
+        if line.startswith("kernel sources sha256"):
+            sha = line.split(":")[-1].strip()
+        elif line.startswith("traffic_bytes_per_launch:"):
+            traffic = int(line.split(":")[1])
+    return traffic if sha == h else None
+
+
 def blas_threads():
     try:
         from threadpoolctl import threadpool_info
@@ -533,7 +551,7 @@ def main():
         "data": "synthetic", "config": config_dict(name, spec),
         "pct_of_bf16_peak": 100.0 * (units / max_el / 1e12) / (peak * world),
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": None,
+                     "frac": achieved / peak, "traffic": profiled_traffic(name),
                      "kernel": "attn_fwd_kernel" if name != "cross" else "attn_fwd_kernel (cross mode)",
                      "kernel_ms": kern_s * 1e3, "algorithmic_bytes": wl.dominant_bytes(),
                      "peak_source": f"bf16_tflops (burst) of {peaks['source']} peaks"},
