@@ -9,28 +9,35 @@
 // and O = 0, lse = -inf for pad query rows. It is the online-softmax (flash) form of that
 // definition: keys are visited in 128-key tiles and the running max/sum are rescaled.
 //
-// One CTA owns a 128-row query tile of one (b, h). Warp roles (384 threads):
-//   warp 0     TMA producer: Q once, then K_j / V_j into a ring of shared-memory stages.
-//   warp 1     TMEM allocator and single-thread tcgen05.mma issuer:
-//              S_j = Q K_j^T into one of two TMEM S buffers, O += P_j V_j into TMEM.
-//   warps 4-7  softmax: thread t owns query row t (TMEM lane t). Reads S_j with tcgen05.ld,
-//              masks keys >= kv_valid, keeps the running max m and sum l, writes P_j (bf16)
-//              to shared memory; rescales O in TMEM only when m grows by more than 2^8
-//              (the final O / l is exact for any reference max); epilogue O / l, LSE.
-//   warps 8-11 auxiliary: RoPE rotation of the landed Q and K tiles in shared memory
-//              (pairs (i, i + D/2) sit at the same swizzled offset of the two 64-column
-//              halves of a row), or, for cross-attention, zeroing of V rows past the
-//              per-batch valid length so that 0 * (pad garbage) cannot reach O.
-//              The rotation is computed in fp32 from the bf16 inputs and stored as fp16
-//              (11-bit significand, 8x finer than bf16; saturating at +-65504), and S =
-//              q~ k~^T then runs as an fp16 x fp16 MMA at the same tensor-core rate. Without
-//              RoPE, q and k are used as the bf16 values they are.
+// One CTA owns two 128-row query tiles (Q0, Q1) of one (b, h); they share every K/V tile
+// and its rotation. Warp roles (512 threads):
+//   warp 0       TMA producer: Q0/Q1 once, then K_j / V_j into a ring of shared-memory stages.
+//   warp 1       TMEM allocator and single-thread tcgen05.mma issuer. Per key tile j it
+//                issues, in this order, O0 += P0_{j-1} V_{j-1}, S0_j = Q0 K_j^T,
+//                O1 += P1_{j-1} V_{j-1}, S1_j = Q1 K_j^T. tcgen05.mma ops of a CTA run in
+//                issue order, so S_t,j may reuse the TMEM columns that held P_t,j-1 and its
+//                completion also implies that O_t holds P_t,j-1 V_j-1.
+//   warps 4-7    softmax of Q0, warps 8-11 softmax of Q1 (thread = query row = TMEM lane).
+//                Each reads S_t,j with tcgen05.ld, masks keys >= kv_valid, keeps the running
+//                max m and sum l, and writes P_t,j as bf16 over the first 64 columns of S_t,j
+//                in TMEM (the A operand of the P V MMA). While one group computes softmax the
+//                tensor core works on the other tile (ping-pong). O_t is rescaled in TMEM only
+//                when m grows by more than 2^8; the final O / l is exact for any reference m.
+//                Epilogue: O / l to bf16, LSE.
+//   warps 12-15  auxiliary: RoPE rotation of the landed Q and K tiles in shared memory
+//                (pairs (i, i + D/2) sit at the same swizzled offset of the two 64-column
+//                halves of a row), or, for cross-attention, zeroing of V rows past the
+//                per-batch valid length so that 0 * (pad garbage) cannot reach O.
+//                The rotation is computed in fp32 from the bf16 inputs and stored as fp16
+//                (11-bit significand, 8x finer than bf16; saturating at +-65504), and S =
+//                q~ k~^T then runs as an fp16 x fp16 MMA at the same tensor-core rate. Without
+//                RoPE, q and k are used as the bf16 values they are.
 // Every mbarrier wait is bounded (ptx.cuh); on a timeout the CTA records a status bit,
 // drains what it has in flight, frees TMEM and exits.
 //
-// Shared memory (128-byte swizzle, tiles 1024-byte aligned): Q [128 x D], K and V stages
-// [128 x D] each, P [128 x 128]. Each [128 x D] tile is D/64 sub-tiles of 128 rows x 128 B.
-// TMEM: 512 columns = S buffer 0 (0..127), S buffer 1 (128..255), O (256..256+D).
+// Shared memory (128-byte swizzle, tiles 1024-byte aligned): Q0, Q1 [128 x D], K and V
+// stages [128 x D]. Each [128 x D] tile is D/64 sub-tiles of 128 rows x 128 B.
+// TMEM (512 columns): S0/P0 0..127, S1/P1 128..255, O0 256..383, O1 384..511.
 
 #include <cuda_bf16.h>
 
@@ -43,7 +50,7 @@ __device__ unsigned int g_dit_status;
 
 namespace {
 
-constexpr int kThreads = 384;
+constexpr int kThreads = 512;
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kLog2e = 1.44269504088896340736f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only if m grows by > 2^8
@@ -52,13 +59,11 @@ template <int D>
 struct Cfg {
   static constexpr int kSub = D / 64;               // 64-column sub-tiles per row
   static constexpr int kTileBytes = 128 * D * 2;    // one 128-row q/k/v tile
-  static constexpr int kStages = (D == 128) ? 2 : 3;
-  static constexpr int kPBytes = 128 * 128 * 2;
-  static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kOffQ + kTileBytes;
+  static constexpr int kStages = (D == 128) ? 2 : 4;
+  static constexpr int kOffQ = 0;                   // Q0, Q1
+  static constexpr int kOffK = kOffQ + 2 * kTileBytes;
   static constexpr int kOffV = kOffK + kStages * kTileBytes;
-  static constexpr int kOffP = kOffV + kStages * kTileBytes;
-  static constexpr int kOffBar = kOffP + kPBytes;
+  static constexpr int kOffBar = kOffV + kStages * kTileBytes;
   static constexpr int kSmemBytes = kOffBar + 512 + 1024;   // barriers + alignment slack
 };
 
@@ -66,8 +71,8 @@ struct Bars {
   uint64_t q_full, q_ready;
   uint64_t k_full[4], k_ready[4], k_empty[4];
   uint64_t v_full[4], v_ready[4], v_empty[4];
-  uint64_t s_full[2];
-  uint64_t p_full, o_done, drain;
+  uint64_t s_full[2], p_full[2], o_done[2];
+  uint64_t drain;
   uint32_t tmem_base;
   int abort;
   int aux_go;   // outcome of the auxiliary warpgroup's last wait, broadcast to the group
@@ -146,34 +151,29 @@ __device__ __forceinline__ void rope_tile(uint32_t tile, const float* __restrict
                                           const float* __restrict__ sin_t, int row0, int at) {
   constexpr int kHalf = D / 2;
   constexpr int kChunks = kHalf / 8;                 // 16-byte chunks per half row
-  constexpr int kItems = 128 * kChunks;
-  constexpr int kPerThread = kItems / 128;
+  constexpr int kPerThread = kChunks;                // 128 rows x kChunks items / 128 threads
+  constexpr int kBatch = 2;
 #pragma unroll
-  for (int it0 = 0; it0 < kPerThread; it0 += 4) {
-    uint4 a[4], b[4];
-    float4 c0[4], c1[4], s0[4], s1[4];
-    uint32_t offa[4], offb[4];
+  for (int it0 = 0; it0 < kPerThread; it0 += kBatch) {
+    uint4 a[kBatch], b[kBatch];
+    float4 c0[kBatch], c1[kBatch], s0[kBatch], s1[kBatch];
+    uint32_t offa[kBatch], offb[kBatch];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < kBatch; ++u) {
       const int item = at + 128 * (it0 + u);
       const int row = item / kChunks, ch = item % kChunks;
-      if (D == 128) {
-        offa[u] = sw128_offset(row, ch);
-        offb[u] = 16384u + offa[u];
-      } else {
-        offa[u] = sw128_offset(row, ch);
-        offb[u] = sw128_offset(row, ch + 4);
-      }
-      a[u] = lds128(tile + offa[u]);
-      b[u] = lds128(tile + offb[u]);
+      offa[u] = sw128_offset(row, ch);
+      offb[u] = (D == 128) ? 16384u + offa[u] : sw128_offset(row, ch + 4);
       const size_t t = static_cast<size_t>(row0 + row) * kHalf + ch * 8;
       c0[u] = __ldg(reinterpret_cast<const float4*>(cos_t + t));
       c1[u] = __ldg(reinterpret_cast<const float4*>(cos_t + t + 4));
       s0[u] = __ldg(reinterpret_cast<const float4*>(sin_t + t));
       s1[u] = __ldg(reinterpret_cast<const float4*>(sin_t + t + 4));
+      a[u] = lds128(tile + offa[u]);
+      b[u] = lds128(tile + offb[u]);
     }
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < kBatch; ++u) {
       rotate8(a[u], b[u], c0[u], c1[u], s0[u], s1[u]);
       sts128(tile + offa[u], a[u]);
       sts128(tile + offb[u], b[u]);
@@ -195,6 +195,20 @@ __device__ __forceinline__ void zero_rows(uint32_t tile, int first_row, int at) 
   }
 }
 
+// O = 0, LSE = -inf for the 128 rows of the query tile starting at q_first (a tile that is
+// all pad rows, or a problem with no keys). `tid` ranges over `nthr` cooperating threads.
+template <int D>
+__device__ __forceinline__ void write_empty_tile(const KParams& p, int b, int h, int q_first,
+                                                 int tid, int nthr) {
+  for (int i = tid; i < 128 * (D / 8); i += nthr) {
+    const int row = i / (D / 8), ch = i % (D / 8);
+    uint16_t* dst = p.out + ((static_cast<size_t>(b) * p.Sq + q_first + row) * p.H + h) * D + ch * 8;
+    *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
+  }
+  for (int r = tid; r < 128; r += nthr)
+    p.lse[(static_cast<size_t>(b) * p.Sq + q_first + r) * p.H + h] = -INFINITY;
+}
+
 template <int D, int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -208,23 +222,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sQ = s_base + C::kOffQ;
   const uint32_t sK0 = s_base + C::kOffK;
   const uint32_t sV0 = s_base + C::kOffV;
-  const uint32_t sP = s_base + C::kOffP;
   Bars* bars = reinterpret_cast<Bars*>(smem + C::kOffBar);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int q0 = blockIdx.x * 128, h = blockIdx.y, b = blockIdx.z;
+  const int q0 = blockIdx.x * 256, h = blockIdx.y, b = blockIdx.z;
   int kv_valid = p.kv_valid;
   if (kMode == kModeCross) kv_valid = min(max(p.kv_valid_dev[b], 0), p.Skv);
-  const bool live = (q0 < p.q_valid) && (kv_valid > 0);
+  // Tile t covers query rows q0 + 128 t .. +127; it exists if those rows are inside Sq and
+  // is live if it holds a valid query row and there is at least one key.
+  const bool has1 = q0 + 128 < p.Sq;
+  const bool live0 = (q0 < p.q_valid) && (kv_valid > 0);
+  const bool live1 = has1 && (q0 + 128 < p.q_valid) && (kv_valid > 0);
+  const int n_live = live1 ? 2 : (live0 ? 1 : 0);
 
-  if (!live) {
-    // The whole tile is pad rows, or there are no keys: O = 0, LSE = -inf.
-    for (int i = tid; i < 128 * (D / 8); i += kThreads) {
-      const int row = i / (D / 8), ch = i % (D / 8);
-      uint16_t* dst = p.out + ((static_cast<size_t>(b) * p.Sq + q0 + row) * p.H + h) * D + ch * 8;
-      *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
-    }
-    if (tid < 128) p.lse[(static_cast<size_t>(b) * p.Sq + q0 + tid) * p.H + h] = -INFINITY;
+  if (n_live == 0) {
+    write_empty_tile<D>(p, b, h, q0, tid, kThreads);
+    if (has1) write_empty_tile<D>(p, b, h, q0 + 128, tid, kThreads);
     return;
   }
   const int n_kv = (kv_valid + 127) / 128;
@@ -232,7 +245,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = &bars->abort;
   unsigned int* status = &g_dit_status;
   const uint32_t b_q_full = smem_u32(&bars->q_full), b_q_ready = smem_u32(&bars->q_ready);
-  const uint32_t b_p_full = smem_u32(&bars->p_full), b_o_done = smem_u32(&bars->o_done);
 
   if (tid == 0) {
     bars->abort = 0;
@@ -246,10 +258,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&bars->v_ready[s]), 1);
       mbar_init(smem_u32(&bars->v_empty[s]), 1);
     }
-    mbar_init(smem_u32(&bars->s_full[0]), 1);
-    mbar_init(smem_u32(&bars->s_full[1]), 1);
-    mbar_init(b_p_full, 128);
-    mbar_init(b_o_done, 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(smem_u32(&bars->s_full[t]), 1);
+      mbar_init(smem_u32(&bars->p_full[t]), 128);
+      mbar_init(smem_u32(&bars->o_done[t]), 1);
+    }
     mbar_init(smem_u32(&bars->drain), 1);
     fence_mbar_init();
   }
@@ -273,9 +286,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       int nk[NS], nvl[NS];
 #pragma unroll
       for (int s = 0; s < NS; ++s) nk[s] = nvl[s] = 0;
-      mbar_arrive_expect_tx(b_q_full, C::kTileBytes);
+      mbar_arrive_expect_tx(b_q_full, n_live * C::kTileBytes);
+      for (int t = 0; t < n_live; ++t)
 #pragma unroll
-      for (int c = 0; c < C::kSub; ++c) tma_load_4d(sQ + c * 16384, &tm_q, b_q_full, c * 64, h, q0, b);
+        for (int c = 0; c < C::kSub; ++c)
+          tma_load_4d(sQ + t * C::kTileBytes + c * 16384, &tm_q, b_q_full, c * 64, h, q0 + 128 * t, b);
       for (int j = 0; j < n_kv; ++j) {
         const int s = j % NS, u = j / NS;
         const uint32_t kf = smem_u32(&bars->k_full[s]), vf = smem_u32(&bars->v_full[s]);
@@ -311,99 +326,127 @@ __global__ void __launch_bounds__(kThreads, 1)
       // S = Q K^T: fp16 operands after the fused rotation, the raw bf16 inputs otherwise.
       constexpr uint32_t kIdS = idesc_f16kind_f32(128, 128, kMode != kModeRope, false, false);
       constexpr uint32_t kIdO = idesc_bf16_f32(128, D, false, true);
-      const uint32_t tO = tbase + 256;
       bool ok = bounded_wait(kMode == kModeRope ? b_q_ready : b_q_full, 0, abort_flag, status,
                              kStatusTimeoutMma);
-      auto issue_s = [&](int j) -> bool {
+      auto wait_k = [&](int j) -> bool {
         const int s = j % NS;
         const uint32_t kbar = (kMode == kModeRope) ? smem_u32(&bars->k_ready[s]) : smem_u32(&bars->k_full[s]);
         if (!bounded_wait(kbar, (j / NS) & 1, abort_flag, status, kStatusTimeoutMma)) return false;
         tc_fence_after_sync();
-        const uint32_t sK = sK0 + s * C::kTileBytes;
-        const uint32_t d = tbase + (j & 1) * 128;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
-          mma_bf16_ss(d, smem_desc_sw128(sQ + off, 16, 1024), smem_desc_sw128(sK + off, 16, 1024),
-                      kIdS, kk > 0);
-        }
-        mma_commit(smem_u32(&bars->s_full[j & 1]));
-        mma_commit(smem_u32(&bars->k_empty[s]));
         return true;
       };
-      auto issue_pv = [&](int j) -> bool {
+      auto wait_v = [&](int j) -> bool {
         const int s = j % NS;
-        if (!bounded_wait(b_p_full, j & 1, abort_flag, status, kStatusTimeoutMma)) return false;
         const uint32_t vbar = (kMode == kModeCross) ? smem_u32(&bars->v_ready[s]) : smem_u32(&bars->v_full[s]);
         if (!bounded_wait(vbar, (j / NS) & 1, abort_flag, status, kStatusTimeoutMma)) return false;
         tc_fence_after_sync();
-        const uint32_t sV = sV0 + s * C::kTileBytes;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t a = smem_desc_sw128(sP + (kk / 4) * 16384 + (kk % 4) * 32, 16, 1024);
-          const uint64_t bd = smem_desc_sw128(sV + kk * 2048, 16384, 1024);
-          mma_bf16_ss(tO, a, bd, kIdO, (j > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(b_o_done);
-        mma_commit(smem_u32(&bars->v_empty[s]));
         return true;
       };
-      if (ok) ok = issue_s(0);
-      for (int j = 1; ok && j < n_kv; ++j) {
-        ok = issue_s(j);
-        if (ok) ok = issue_pv(j - 1);
+      auto wait_p = [&](int t, int j) -> bool {
+        if (!bounded_wait(smem_u32(&bars->p_full[t]), j & 1, abort_flag, status, kStatusTimeoutMma))
+          return false;
+        tc_fence_after_sync();
+        return true;
+      };
+      auto issue_s = [&](int t, int j) {
+        const uint32_t sK = sK0 + (j % NS) * C::kTileBytes;
+        const uint32_t sQt = sQ + t * C::kTileBytes;
+        const uint32_t d = tbase + t * 128;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
+          mma_bf16_ss(d, smem_desc_sw128(sQt + off, 16, 1024), smem_desc_sw128(sK + off, 16, 1024),
+                      kIdS, kk > 0);
+        }
+        mma_commit(smem_u32(&bars->s_full[t]));
+      };
+      auto issue_pv = [&](int t, int j) {
+        const uint32_t sV = sV0 + (j % NS) * C::kTileBytes;
+        const uint32_t a_tmem = tbase + t * 128;          // P_t: bf16 pairs in TMEM
+        const uint32_t d = tbase + 256 + t * 128;         // O_t
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_bf16_ts(d, a_tmem + kk * 8, smem_desc_sw128(sV + kk * 2048, 16384, 1024), kIdO,
+                      (j > 0 || kk > 0) ? 1u : 0u);
+      };
+      if (ok) ok = wait_k(0);
+      if (ok) {
+        issue_s(0, 0);
+        if (n_live == 2) issue_s(1, 0);
+        mma_commit(smem_u32(&bars->k_empty[0]));
       }
-      if (ok) ok = issue_pv(n_kv - 1);
+      for (int j = 1; ok && j < n_kv; ++j) {
+        if (!(ok = wait_v(j - 1) && wait_p(0, j - 1))) break;
+        issue_pv(0, j - 1);
+        if (!(ok = wait_k(j))) break;
+        issue_s(0, j);
+        if (n_live == 2) {
+          if (!(ok = wait_p(1, j - 1))) break;
+          issue_pv(1, j - 1);
+          issue_s(1, j);
+        }
+        mma_commit(smem_u32(&bars->v_empty[(j - 1) % NS]));
+        mma_commit(smem_u32(&bars->k_empty[j % NS]));
+      }
+      if (ok) ok = wait_v(n_kv - 1) && wait_p(0, n_kv - 1);
+      if (ok) {
+        issue_pv(0, n_kv - 1);
+        mma_commit(smem_u32(&bars->o_done[0]));
+        if (n_live == 2 && (ok = wait_p(1, n_kv - 1))) {
+          issue_pv(1, n_kv - 1);
+          mma_commit(smem_u32(&bars->o_done[1]));
+        }
+        mma_commit(smem_u32(&bars->v_empty[(n_kv - 1) % NS]));
+      }
       if (*abort_flag) {
         // Wait for every MMA issued so far before TMEM and shared memory are released.
         mma_commit(smem_u32(&bars->drain));
         drain_wait(smem_u32(&bars->drain), 0, status);
       }
     }
-  } else if (warp >= 4 && warp < 8) {
+  } else if (warp >= 4 && warp < 12) {
     // -------------------------------------------------------------- softmax + epilogue
-    const int r = tid - 128;                         // query row within the tile = TMEM lane
-    const uint32_t lane_off = static_cast<uint32_t>((warp - 4) * 32) << 16;
-    const uint32_t tO = tbase + lane_off + 256;
-    const float sl2 = p.scale_log2;
-    float m_used = -INFINITY, l = 0.f;
-    bool ok = true;
-    for (int j = 0; j < n_kv; ++j) {
-      if (!warp_wait(smem_u32(&bars->s_full[j & 1]), (j >> 1) & 1, abort_flag, status,
-                     kStatusTimeoutSoftmax)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after_sync();
-      const uint32_t tS = tbase + lane_off + (j & 1) * 128;
-      const int nv = min(128, kv_valid - j * 128);   // valid keys in this tile (>= 1)
-      // Pass 1: row max over the valid keys.
-      float mx = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t sr[32];
-        tmem_ld32(tS + c * 32, sr);
-        if (nv == 128) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(sr[i]));
-        } else {
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (c * 32 + i < nv) mx = fmaxf(mx, __uint_as_float(sr[i]));
-        }
-      }
-      const float mt = mx * sl2;
-      const bool resc = mt > m_used + kRescaleThreshold;
-      const float m_new = resc ? mt : m_used;
-      const float alpha = ex2_approx(m_used - m_new);   // 1 if kept; 0 on the first tile
-      if (j > 0) {
-        // P_{j-1} V_{j-1} must be complete: it frees the P buffer and updates O.
-        if (!warp_wait(b_o_done, (j - 1) & 1, abort_flag, status, kStatusTimeoutSoftmax)) {
+    const int t = (warp - 4) >> 2;                   // query tile of this warpgroup
+    const int r = (tid - 128) & 127;                 // row within the tile = TMEM lane
+    const int qrow = q0 + 128 * t + r;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tbase + lane_off + t * 128;  // S_t (and P_t in its first 64 columns)
+    const uint32_t tO = tbase + lane_off + 256 + t * 128;
+    if (t >= n_live) {
+      if (has1) write_empty_tile<D>(p, b, h, q0 + 128, r, 128);
+    } else {
+      const float sl2 = p.scale_log2;
+      float m_used = -INFINITY, l = 0.f;
+      bool ok = true;
+      for (int j = 0; j < n_kv; ++j) {
+        if (!warp_wait(smem_u32(&bars->s_full[t]), j & 1, abort_flag, status, kStatusTimeoutSoftmax)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
-        if (__any_sync(0xffffffffu, resc)) {
+        const int nv = min(128, kv_valid - j * 128);   // valid keys in this tile (>= 1)
+        // Pass 1: row max over the valid keys.
+        float mx = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t sr[32];
+          tmem_ld32(tS + c * 32, sr);
+          if (nv == 128) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(sr[i]));
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (c * 32 + i < nv) mx = fmaxf(mx, __uint_as_float(sr[i]));
+          }
+        }
+        const float mt = mx * sl2;
+        const bool resc = mt > m_used + kRescaleThreshold;
+        const float m_new = resc ? mt : m_used;
+        const float alpha = ex2_approx(m_used - m_new);   // 1 if kept; 0 on the first tile
+        // S_t,j completing implies P_t,j-1 V_j-1 has completed too (issue order), so O_t is
+        // current and nothing else writes it until this group arrives on p_full.
+        if (j > 0 && __any_sync(0xffffffffu, resc)) {
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
             uint32_t orr[32];
@@ -413,71 +456,68 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st32(tO + c * 32, orr);
           }
         }
-      }
-      l *= alpha;
-      m_used = m_new;
-      const float neg_m = -m_used;
-      // Pass 2: P = 2^(s * scale * log2 e - m), masked; row sum; P (bf16) to shared memory.
+        l *= alpha;
+        m_used = m_new;
+        const float neg_m = -m_used;
+        // Pass 2: P = 2^(s * scale * log2 e - m), masked; row sum; P (bf16) into TMEM over
+        // columns already consumed (P chunk c lands in S columns 16c..16c+15 < 32 (c + 1)).
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t sr[32];
-        tmem_ld32(tS + c * 32, sr);
-        uint32_t pk[16];
+        for (int c = 0; c < 4; ++c) {
+          uint32_t sr[32];
+          tmem_ld32(tS + c * 32, sr);
+          uint32_t pk[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int col = c * 32 + 2 * i;
-          float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * i]), sl2, neg_m));
-          float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * i + 1]), sl2, neg_m));
-          if (nv < 128) {
-            p0 = (col < nv) ? p0 : 0.f;
-            p1 = (col + 1 < nv) ? p1 : 0.f;
+          for (int i = 0; i < 16; ++i) {
+            const int col = c * 32 + 2 * i;
+            float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * i]), sl2, neg_m));
+            float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * i + 1]), sl2, neg_m));
+            if (nv < 128) {
+              p0 = (col < nv) ? p0 : 0.f;
+              p1 = (col + 1 < nv) ? p1 : 0.f;
+            }
+            l += p0 + p1;
+            pk[i] = pack_bf16x2(p0, p1);
           }
-          l += p0 + p1;
-          pk[i] = pack_bf16x2(p0, p1);
+          tmem_st16_nowait(tS + c * 16, pk);
         }
-        const uint32_t sub = sP + (c / 2) * 16384;
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4)
-          sts128(sub + sw128_offset(r, (c % 2) * 4 + q4),
-                 make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]));
+        tmem_st_wait();
+        tc_fence_before_sync();
+        mbar_arrive(smem_u32(&bars->p_full[t]));
       }
-      fence_proxy_async_smem();
-      tc_fence_before_sync();
-      mbar_arrive(b_p_full);
-    }
-    if (ok && warp_wait(b_o_done, (n_kv - 1) & 1, abort_flag, status, kStatusTimeoutSoftmax)) {
-      tc_fence_after_sync();
-      const int qrow = q0 + r;
-      const bool valid_row = qrow < p.q_valid;
-      const float inv_l = 1.f / l;
-      uint16_t* dst = p.out + ((static_cast<size_t>(b) * p.Sq + qrow) * p.H + h) * D;
+      if (ok && warp_wait(smem_u32(&bars->o_done[t]), 0, abort_flag, status, kStatusTimeoutSoftmax)) {
+        tc_fence_after_sync();
+        const bool valid_row = qrow < p.q_valid;
+        const float inv_l = 1.f / l;
+        uint16_t* dst = p.out + ((static_cast<size_t>(b) * p.Sq + qrow) * p.H + h) * D;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t orr[32];
-        tmem_ld32(tO + c * 32, orr);
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t orr[32];
+          tmem_ld32(tO + c * 32, orr);
 #pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          uint4 w = make_uint4(0, 0, 0, 0);
-          if (valid_row) {
-            const float* f = reinterpret_cast<const float*>(&orr[8 * q4]);
-            w.x = pack_bf16x2(f[0] * inv_l, f[1] * inv_l);
-            w.y = pack_bf16x2(f[2] * inv_l, f[3] * inv_l);
-            w.z = pack_bf16x2(f[4] * inv_l, f[5] * inv_l);
-            w.w = pack_bf16x2(f[6] * inv_l, f[7] * inv_l);
+          for (int q4 = 0; q4 < 4; ++q4) {
+            uint4 w = make_uint4(0, 0, 0, 0);
+            if (valid_row) {
+              const float* f = reinterpret_cast<const float*>(&orr[8 * q4]);
+              w.x = pack_bf16x2(f[0] * inv_l, f[1] * inv_l);
+              w.y = pack_bf16x2(f[2] * inv_l, f[3] * inv_l);
+              w.z = pack_bf16x2(f[4] * inv_l, f[5] * inv_l);
+              w.w = pack_bf16x2(f[6] * inv_l, f[7] * inv_l);
+            }
+            *reinterpret_cast<uint4*>(dst + c * 32 + q4 * 8) = w;
           }
-          *reinterpret_cast<uint4*>(dst + c * 32 + q4 * 8) = w;
         }
+        p.lse[(static_cast<size_t>(b) * p.Sq + qrow) * p.H + h] =
+            valid_row ? (m_used + log2f(l)) * kLn2 : -INFINITY;
       }
-      p.lse[(static_cast<size_t>(b) * p.Sq + qrow) * p.H + h] =
-          valid_row ? (m_used + log2f(l)) * kLn2 : -INFINITY;
     }
-  } else if (warp >= 8) {
+  } else if (warp >= 12) {
     // ------------------------------------------------------------ auxiliary warpgroup
-    const int at = tid - 256;
+    const int at = tid - 384;
     volatile int* go = &bars->aux_go;
     if (kMode == kModeRope) {
       if (group_wait(b_q_full, 0, abort_flag, status, kStatusTimeoutRope, go, at)) {
-        rope_tile<D>(sQ, p.cos_q, p.sin_q, q0, at);
+        for (int t = 0; t < n_live; ++t)
+          rope_tile<D>(sQ + t * C::kTileBytes, p.cos_q, p.sin_q, q0 + 128 * t, at);
         fence_proxy_async_smem();
         named_bar_sync(1, 128);
         if (at == 0) mbar_arrive(b_q_ready);
@@ -543,7 +583,7 @@ cudaError_t launch_mode(const AttnArgs& a) {
   auto kern = attn_fwd_kernel<D, kMode>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmemBytes);
   if (e != cudaSuccess) return e;
-  dim3 grid(a.Sq / 128, a.H, a.B);
+  dim3 grid((a.Sq + 255) / 256, a.H, a.B);
   kern<<<grid, kThreads, Cfg<D>::kSmemBytes, a.stream>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }

@@ -302,6 +302,18 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// Stores without waiting; pair with tmem_st_wait() after the last store of a batch.
+__device__ __forceinline__ void tmem_st16_nowait(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      DIT_S8(0), DIT_S8(8)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 #undef DIT_R8
 #undef DIT_W8
 #undef DIT_S8
