@@ -59,11 +59,12 @@ template <int D>
 struct Cfg {
   static constexpr int kSub = D / 64;               // 64-column sub-tiles per row
   static constexpr int kTileBytes = 128 * D * 2;    // one 128-row q/k/v tile
-  static constexpr int kStages = (D == 128) ? 2 : 4;
+  static constexpr int kStagesK = (D == 128) ? 3 : 4;
+  static constexpr int kStagesV = (D == 128) ? 2 : 4;
   static constexpr int kOffQ = 0;                   // Q0, Q1
   static constexpr int kOffK = kOffQ + 2 * kTileBytes;
-  static constexpr int kOffV = kOffK + kStages * kTileBytes;
-  static constexpr int kOffBar = kOffV + kStages * kTileBytes;
+  static constexpr int kOffV = kOffK + kStagesK * kTileBytes;
+  static constexpr int kOffBar = kOffV + kStagesV * kTileBytes;
   static constexpr int kSmemBytes = kOffBar + 512 + 1024;   // barriers + alignment slack
 };
 
@@ -144,42 +145,66 @@ __device__ __forceinline__ void rotate8(uint4& a, uint4& b, const float4 c0, con
   b = make_uint4(bw[0], bw[1], bw[2], bw[3]);
 }
 
-// Rotates one landed [128 x D] tile in place with table rows row0 .. row0+127.
-// Called by the 128 threads of the auxiliary warpgroup (at = 0..127).
+// cos/sin of two 8-pair chunks (one "batch") of one thread's share of a tile.
+struct TabBatch {
+  float4 c0[2], c1[2], s0[2], s1[2];
+};
+
+// Tile rotation by the 128 threads of the auxiliary warpgroup (at = 0..127). Thread `at`
+// owns 16-byte chunk ch = at % kChunks of rows at / kChunks + i * (128 / kChunks); its items
+// go in batches of two, and the table loads of the next batch (or of the next tile's first
+// batch) are issued before the current batch is rotated, so the L2 latency of the cos/sin
+// rows overlaps the rotation and the wait for the next tile to land.
 template <int D>
-__device__ __forceinline__ void rope_tile(uint32_t tile, const float* __restrict__ cos_t,
-                                          const float* __restrict__ sin_t, int row0, int at) {
-  constexpr int kHalf = D / 2;
-  constexpr int kChunks = kHalf / 8;                 // 16-byte chunks per half row
-  constexpr int kPerThread = kChunks;                // 128 rows x kChunks items / 128 threads
-  constexpr int kBatch = 2;
+struct Rotator {
+  static constexpr int kHalf = D / 2;
+  static constexpr int kChunks = kHalf / 8;          // 16-byte chunks per half row
+  static constexpr int kRowStep = 128 / kChunks;     // rows between a thread's items
+  static constexpr int kBatches = kChunks / 2;       // kChunks items per thread, 2 per batch
+
+  __device__ __forceinline__ static void load(TabBatch& t, const float* __restrict__ cos_t,
+                                              const float* __restrict__ sin_t, int row0, int at,
+                                              int batch) {
 #pragma unroll
-  for (int it0 = 0; it0 < kPerThread; it0 += kBatch) {
-    uint4 a[kBatch], b[kBatch];
-    float4 c0[kBatch], c1[kBatch], s0[kBatch], s1[kBatch];
-    uint32_t offa[kBatch], offb[kBatch];
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int item = at + 128 * (it0 + u);
-      const int row = item / kChunks, ch = item % kChunks;
-      offa[u] = sw128_offset(row, ch);
-      offb[u] = (D == 128) ? 16384u + offa[u] : sw128_offset(row, ch + 4);
-      const size_t t = static_cast<size_t>(row0 + row) * kHalf + ch * 8;
-      c0[u] = __ldg(reinterpret_cast<const float4*>(cos_t + t));
-      c1[u] = __ldg(reinterpret_cast<const float4*>(cos_t + t + 4));
-      s0[u] = __ldg(reinterpret_cast<const float4*>(sin_t + t));
-      s1[u] = __ldg(reinterpret_cast<const float4*>(sin_t + t + 4));
-      a[u] = lds128(tile + offa[u]);
-      b[u] = lds128(tile + offb[u]);
-    }
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      rotate8(a[u], b[u], c0[u], c1[u], s0[u], s1[u]);
-      sts128(tile + offa[u], a[u]);
-      sts128(tile + offb[u], b[u]);
+    for (int u = 0; u < 2; ++u) {
+      const int row = at / kChunks + (2 * batch + u) * kRowStep;
+      const size_t o = static_cast<size_t>(row0 + row) * kHalf + (at % kChunks) * 8;
+      t.c0[u] = __ldg(reinterpret_cast<const float4*>(cos_t + o));
+      t.c1[u] = __ldg(reinterpret_cast<const float4*>(cos_t + o + 4));
+      t.s0[u] = __ldg(reinterpret_cast<const float4*>(sin_t + o));
+      t.s1[u] = __ldg(reinterpret_cast<const float4*>(sin_t + o + 4));
     }
   }
-}
+
+  __device__ __forceinline__ static void rotate(uint32_t tile, const TabBatch& t, int at, int batch) {
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int row = at / kChunks + (2 * batch + u) * kRowStep, ch = at % kChunks;
+      const uint32_t offa = sw128_offset(row, ch);
+      const uint32_t offb = (D == 128) ? 16384u + offa : sw128_offset(row, ch + 4);
+      uint4 a = lds128(tile + offa), b = lds128(tile + offb);
+      rotate8(a, b, t.c0[u], t.c1[u], t.s0[u], t.s1[u]);
+      sts128(tile + offa, a);
+      sts128(tile + offb, b);
+    }
+  }
+
+  // Rotates `tile` (its batch-0 table values already in buf[0]); before returning, starts
+  // loading batch 0 of the next tile (next_cos == nullptr: none) into buf[0].
+  __device__ __forceinline__ static void tile(uint32_t tile, TabBatch (&buf)[2],
+                                              const float* cos_t, const float* sin_t, int row0,
+                                              const float* next_cos, const float* next_sin,
+                                              int next_row0, int at) {
+#pragma unroll
+    for (int bt = 0; bt < kBatches; ++bt) {
+      if (bt + 1 < kBatches)
+        load(buf[(bt + 1) & 1], cos_t, sin_t, row0, at, bt + 1);
+      else if (next_cos != nullptr)
+        load(buf[(bt + 1) & 1], next_cos, next_sin, next_row0, at, 0);
+      rotate(tile, buf[bt & 1], at, bt);
+    }
+  }
+};
 
 // Zeroes rows [first_row, 128) of a landed [128 x D] V tile (all sub-tiles).
 template <int D>
@@ -214,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const KParams p) {
   using C = Cfg<D>;
-  constexpr int NS = C::kStages;
+  constexpr int NSK = C::kStagesK, NSV = C::kStagesV;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -250,10 +275,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     bars->abort = 0;
     mbar_init(b_q_full, 1);
     mbar_init(b_q_ready, 1);
-    for (int s = 0; s < NS; ++s) {
+    for (int s = 0; s < NSK; ++s) {
       mbar_init(smem_u32(&bars->k_full[s]), 1);
       mbar_init(smem_u32(&bars->k_ready[s]), 1);
       mbar_init(smem_u32(&bars->k_empty[s]), 1);
+    }
+    for (int s = 0; s < NSV; ++s) {
       mbar_init(smem_u32(&bars->v_full[s]), 1);
       mbar_init(smem_u32(&bars->v_ready[s]), 1);
       mbar_init(smem_u32(&bars->v_empty[s]), 1);
@@ -283,41 +310,43 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ TMA producer
-      int nk[NS], nvl[NS];
+      int nk[NSK], nvl[NSV];
 #pragma unroll
-      for (int s = 0; s < NS; ++s) nk[s] = nvl[s] = 0;
+      for (int s = 0; s < NSK; ++s) nk[s] = 0;
+#pragma unroll
+      for (int s = 0; s < NSV; ++s) nvl[s] = 0;
       mbar_arrive_expect_tx(b_q_full, n_live * C::kTileBytes);
       for (int t = 0; t < n_live; ++t)
 #pragma unroll
         for (int c = 0; c < C::kSub; ++c)
           tma_load_4d(sQ + t * C::kTileBytes + c * 16384, &tm_q, b_q_full, c * 64, h, q0 + 128 * t, b);
       for (int j = 0; j < n_kv; ++j) {
-        const int s = j % NS, u = j / NS;
-        const uint32_t kf = smem_u32(&bars->k_full[s]), vf = smem_u32(&bars->v_full[s]);
-        if (u > 0 && !bounded_wait(smem_u32(&bars->k_empty[s]), (u - 1) & 1, abort_flag, status,
-                                   kStatusTimeoutLoad))
+        const int sk = j % NSK, uk = j / NSK, sv = j % NSV, uv = j / NSV;
+        const uint32_t kf = smem_u32(&bars->k_full[sk]), vf = smem_u32(&bars->v_full[sv]);
+        if (uk > 0 && !bounded_wait(smem_u32(&bars->k_empty[sk]), (uk - 1) & 1, abort_flag, status,
+                                    kStatusTimeoutLoad))
           break;
         mbar_arrive_expect_tx(kf, C::kTileBytes);
 #pragma unroll
         for (int c = 0; c < C::kSub; ++c)
-          tma_load_4d(sK0 + s * C::kTileBytes + c * 16384, &tm_k, kf, c * 64, h, j * 128, b);
-        ++nk[s];
-        if (u > 0 && !bounded_wait(smem_u32(&bars->v_empty[s]), (u - 1) & 1, abort_flag, status,
-                                   kStatusTimeoutLoad))
+          tma_load_4d(sK0 + sk * C::kTileBytes + c * 16384, &tm_k, kf, c * 64, h, j * 128, b);
+        ++nk[sk];
+        if (uv > 0 && !bounded_wait(smem_u32(&bars->v_empty[sv]), (uv - 1) & 1, abort_flag, status,
+                                    kStatusTimeoutLoad))
           break;
         mbar_arrive_expect_tx(vf, C::kTileBytes);
 #pragma unroll
         for (int c = 0; c < C::kSub; ++c)
-          tma_load_4d(sV0 + s * C::kTileBytes + c * 16384, &tm_v, vf, c * 64, h, j * 128, b);
-        ++nvl[s];
+          tma_load_4d(sV0 + sv * C::kTileBytes + c * 16384, &tm_v, vf, c * 64, h, j * 128, b);
+        ++nvl[sv];
       }
       if (*abort_flag) {
         // Let every copy this thread started land before the CTA gives up its memory.
         drain_wait(b_q_full, 0, status);
-        for (int s = 0; s < NS; ++s) {
+        for (int s = 0; s < NSK; ++s)
           if (nk[s] > 0) drain_wait(smem_u32(&bars->k_full[s]), (nk[s] - 1) & 1, status);
+        for (int s = 0; s < NSV; ++s)
           if (nvl[s] > 0) drain_wait(smem_u32(&bars->v_full[s]), (nvl[s] - 1) & 1, status);
-        }
       }
     }
   } else if (warp == 1) {
@@ -329,16 +358,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = bounded_wait(kMode == kModeRope ? b_q_ready : b_q_full, 0, abort_flag, status,
                              kStatusTimeoutMma);
       auto wait_k = [&](int j) -> bool {
-        const int s = j % NS;
+        const int s = j % NSK;
         const uint32_t kbar = (kMode == kModeRope) ? smem_u32(&bars->k_ready[s]) : smem_u32(&bars->k_full[s]);
-        if (!bounded_wait(kbar, (j / NS) & 1, abort_flag, status, kStatusTimeoutMma)) return false;
+        if (!bounded_wait(kbar, (j / NSK) & 1, abort_flag, status, kStatusTimeoutMma)) return false;
         tc_fence_after_sync();
         return true;
       };
       auto wait_v = [&](int j) -> bool {
-        const int s = j % NS;
+        const int s = j % NSV;
         const uint32_t vbar = (kMode == kModeCross) ? smem_u32(&bars->v_ready[s]) : smem_u32(&bars->v_full[s]);
-        if (!bounded_wait(vbar, (j / NS) & 1, abort_flag, status, kStatusTimeoutMma)) return false;
+        if (!bounded_wait(vbar, (j / NSV) & 1, abort_flag, status, kStatusTimeoutMma)) return false;
         tc_fence_after_sync();
         return true;
       };
@@ -349,7 +378,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       };
       auto issue_s = [&](int t, int j) {
-        const uint32_t sK = sK0 + (j % NS) * C::kTileBytes;
+        const uint32_t sK = sK0 + (j % NSK) * C::kTileBytes;
         const uint32_t sQt = sQ + t * C::kTileBytes;
         const uint32_t d = tbase + t * 128;
 #pragma unroll
@@ -361,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(smem_u32(&bars->s_full[t]));
       };
       auto issue_pv = [&](int t, int j) {
-        const uint32_t sV = sV0 + (j % NS) * C::kTileBytes;
+        const uint32_t sV = sV0 + (j % NSV) * C::kTileBytes;
         const uint32_t a_tmem = tbase + t * 128;          // P_t: bf16 pairs in TMEM
         const uint32_t d = tbase + 256 + t * 128;         // O_t
 #pragma unroll
@@ -385,8 +414,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           issue_pv(1, j - 1);
           issue_s(1, j);
         }
-        mma_commit(smem_u32(&bars->v_empty[(j - 1) % NS]));
-        mma_commit(smem_u32(&bars->k_empty[j % NS]));
+        mma_commit(smem_u32(&bars->v_empty[(j - 1) % NSV]));
+        mma_commit(smem_u32(&bars->k_empty[j % NSK]));
       }
       if (ok) ok = wait_v(n_kv - 1) && wait_p(0, n_kv - 1);
       if (ok) {
@@ -396,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           issue_pv(1, n_kv - 1);
           mma_commit(smem_u32(&bars->o_done[1]));
         }
-        mma_commit(smem_u32(&bars->v_empty[(n_kv - 1) % NS]));
+        mma_commit(smem_u32(&bars->v_empty[(n_kv - 1) % NSV]));
       }
       if (*abort_flag) {
         // Wait for every MMA issued so far before TMEM and shared memory are released.
@@ -425,21 +454,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after_sync();
         const int nv = min(128, kv_valid - j * 128);   // valid keys in this tile (>= 1)
-        // Pass 1: row max over the valid keys.
-        float mx = -INFINITY;
+        // Pass 1: row max over the valid keys. Two 32-column loads in flight at a time and
+        // eight independent partial maxima keep the dependency chains short.
+        float mx8[8];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t sr[32];
-          tmem_ld32(tS + c * 32, sr);
+        for (int i = 0; i < 8; ++i) mx8[i] = -INFINITY;
+#pragma unroll
+        for (int c = 0; c < 4; c += 2) {
+          uint32_t sa[32], sb[32];
+          tmem_ld32_nowait(tS + c * 32, sa);
+          tmem_ld32_nowait(tS + c * 32 + 32, sb);
+          tmem_ld_wait_tied(sa);
+          tmem_reg_tie(sb);
           if (nv == 128) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(sr[i]));
+            for (int i = 0; i < 32; ++i) {
+              mx8[i & 7] = fmaxf(mx8[i & 7], __uint_as_float(sa[i]));
+              mx8[i & 7] = fmaxf(mx8[i & 7], __uint_as_float(sb[i]));
+            }
           } else {
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              if (c * 32 + i < nv) mx = fmaxf(mx, __uint_as_float(sr[i]));
+            for (int i = 0; i < 32; ++i) {
+              if (c * 32 + i < nv) mx8[i & 7] = fmaxf(mx8[i & 7], __uint_as_float(sa[i]));
+              if (c * 32 + 32 + i < nv) mx8[i & 7] = fmaxf(mx8[i & 7], __uint_as_float(sb[i]));
+            }
           }
         }
+        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
         const float mt = mx * sl2;
         const bool resc = mt > m_used + kRescaleThreshold;
         const float m_new = resc ? mt : m_used;
@@ -456,30 +498,40 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st32(tO + c * 32, orr);
           }
         }
-        l *= alpha;
         m_used = m_new;
         const float neg_m = -m_used;
-        // Pass 2: P = 2^(s * scale * log2 e - m), masked; row sum; P (bf16) into TMEM over
-        // columns already consumed (P chunk c lands in S columns 16c..16c+15 < 32 (c + 1)).
+        // Pass 2: P = 2^(s * scale * log2 e - m), masked; row sum in eight partial sums; P
+        // (bf16) into TMEM over columns already consumed (P chunk c lands in S columns
+        // 16c..16c+15 < 32 (c + 1)). The load of chunk c + 1 is in flight while chunk c is
+        // exponentiated.
+        float l8[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) l8[i] = 0.f;
+        uint32_t sr[2][32];
+        tmem_ld32_nowait(tS, sr[0]);
+        tmem_ld_wait_tied(sr[0]);
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          uint32_t sr[32];
-          tmem_ld32(tS + c * 32, sr);
+          if (c + 1 < 4) tmem_ld32_nowait(tS + (c + 1) * 32, sr[(c + 1) & 1]);
+          const uint32_t (&cur)[32] = sr[c & 1];
           uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const int col = c * 32 + 2 * i;
-            float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * i]), sl2, neg_m));
-            float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * i + 1]), sl2, neg_m));
+            float p0 = ex2_approx(fmaf(__uint_as_float(cur[2 * i]), sl2, neg_m));
+            float p1 = ex2_approx(fmaf(__uint_as_float(cur[2 * i + 1]), sl2, neg_m));
             if (nv < 128) {
               p0 = (col < nv) ? p0 : 0.f;
               p1 = (col + 1 < nv) ? p1 : 0.f;
             }
-            l += p0 + p1;
+            l8[(2 * i) & 7] += p0;
+            l8[(2 * i + 1) & 7] += p1;
             pk[i] = pack_bf16x2(p0, p1);
           }
           tmem_st16_nowait(tS + c * 16, pk);
+          if (c + 1 < 4) tmem_ld_wait_tied(sr[(c + 1) & 1]);
         }
+        l = l * alpha + (((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7])));
         tmem_st_wait();
         tc_fence_before_sync();
         mbar_arrive(smem_u32(&bars->p_full[t]));
@@ -515,18 +567,26 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int at = tid - 384;
     volatile int* go = &bars->aux_go;
     if (kMode == kModeRope) {
+      using R = Rotator<D>;
+      TabBatch buf[2];
+      R::load(buf[0], p.cos_q, p.sin_q, q0, at, 0);
       if (group_wait(b_q_full, 0, abort_flag, status, kStatusTimeoutRope, go, at)) {
-        for (int t = 0; t < n_live; ++t)
-          rope_tile<D>(sQ + t * C::kTileBytes, p.cos_q, p.sin_q, q0 + 128 * t, at);
+        for (int t = 0; t < n_live; ++t) {
+          const bool last_q = (t + 1 == n_live);
+          R::tile(sQ + t * C::kTileBytes, buf, p.cos_q, p.sin_q, q0 + 128 * t,
+                  last_q ? p.cos_k : p.cos_q, last_q ? p.sin_k : p.sin_q, last_q ? 0 : q0 + 128 * (t + 1), at);
+        }
         fence_proxy_async_smem();
         named_bar_sync(1, 128);
         if (at == 0) mbar_arrive(b_q_ready);
         for (int j = 0; j < n_kv; ++j) {
-          const int s = j % NS;
-          if (!group_wait(smem_u32(&bars->k_full[s]), (j / NS) & 1, abort_flag, status,
+          const int s = j % NSK;
+          if (!group_wait(smem_u32(&bars->k_full[s]), (j / NSK) & 1, abort_flag, status,
                           kStatusTimeoutRope, go, at))
             break;
-          rope_tile<D>(sK0 + s * C::kTileBytes, p.cos_k, p.sin_k, j * 128, at);
+          const bool more = j + 1 < n_kv;
+          R::tile(sK0 + s * C::kTileBytes, buf, p.cos_k, p.sin_k, j * 128,
+                  more ? p.cos_k : nullptr, p.sin_k, (j + 1) * 128, at);
           fence_proxy_async_smem();
           named_bar_sync(1, 128);
           if (at == 0) mbar_arrive(smem_u32(&bars->k_ready[s]));
@@ -534,8 +594,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     } else if (kMode == kModeCross) {
       for (int j = 0; j < n_kv; ++j) {
-        const int s = j % NS;
-        if (!group_wait(smem_u32(&bars->v_full[s]), (j / NS) & 1, abort_flag, status,
+        const int s = j % NSV;
+        if (!group_wait(smem_u32(&bars->v_full[s]), (j / NSV) & 1, abort_flag, status,
                         kStatusTimeoutRope, go, at))
           break;
         const int nv = min(128, kv_valid - j * 128);

@@ -270,6 +270,29 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
                : "memory");
 }
 
+// Issues the load of 32 columns without waiting; the registers are valid only after a
+// later tmem_ld_wait_tied() / tmem_reg_tie() pair names them.
+__device__ __forceinline__ void tmem_ld32_nowait(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : DIT_R8(0), DIT_R8(8), DIT_R8(16), DIT_R8(24)
+      : "r"(taddr)
+      : "memory");
+}
+// Waits for every outstanding tcgen05.ld of this thread; names r so no use moves above it.
+__device__ __forceinline__ void tmem_ld_wait_tied(uint32_t (&r)[32]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : DIT_W8(0), DIT_W8(8), DIT_W8(16), DIT_W8(24)
+               :
+               : "memory");
+}
+// Orders uses of r after the preceding volatile asm (an empty statement that "writes" r).
+__device__ __forceinline__ void tmem_reg_tie(uint32_t (&r)[32]) {
+  asm volatile("" : DIT_W8(0), DIT_W8(8), DIT_W8(16), DIT_W8(24) : : "memory");
+}
+
 // 16 columns.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
