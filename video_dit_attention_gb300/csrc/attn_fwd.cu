@@ -59,12 +59,15 @@ template <int D>
 struct Cfg {
   static constexpr int kSub = D / 64;               // 64-column sub-tiles per row
   static constexpr int kTileBytes = 128 * D * 2;    // one 128-row q/k/v tile
-  static constexpr int kStagesK = (D == 128) ? 3 : 4;
+  static constexpr int kStagesK = (D == 128) ? 2 : 4;
   static constexpr int kStagesV = (D == 128) ? 2 : 4;
+  static constexpr int kTabRows = 32;                       // rows per staged table quarter
+  static constexpr int kTabBoxBytes = kTabRows * (D / 2) * 4;  // cos (or sin) of a quarter
   static constexpr int kOffQ = 0;                   // Q0, Q1
   static constexpr int kOffK = kOffQ + 2 * kTileBytes;
   static constexpr int kOffV = kOffK + kStagesK * kTileBytes;
-  static constexpr int kOffBar = kOffV + kStagesV * kTileBytes;
+  static constexpr int kOffT = kOffV + kStagesV * kTileBytes;   // 2 x (cos, sin) quarters
+  static constexpr int kOffBar = kOffT + 2 * 2 * kTabBoxBytes;
   static constexpr int kSmemBytes = kOffBar + 512 + 1024;   // barriers + alignment slack
 };
 
@@ -73,6 +76,7 @@ struct Bars {
   uint64_t k_full[4], k_ready[4], k_empty[4];
   uint64_t v_full[4], v_ready[4], v_empty[4];
   uint64_t s_full[2], p_full[2], o_done[2];
+  uint64_t t_full[2], t_empty[2];
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
@@ -145,63 +149,35 @@ __device__ __forceinline__ void rotate8(uint4& a, uint4& b, const float4 c0, con
   b = make_uint4(bw[0], bw[1], bw[2], bw[3]);
 }
 
-// cos/sin of two 8-pair chunks (one "batch") of one thread's share of a tile.
-struct TabBatch {
-  float4 c0[2], c1[2], s0[2], s1[2];
-};
-
-// Tile rotation by the 128 threads of the auxiliary warpgroup (at = 0..127). Thread `at`
-// owns 16-byte chunk ch = at % kChunks of rows at / kChunks + i * (128 / kChunks); its items
-// go in batches of two, and the table loads of the next batch (or of the next tile's first
-// batch) are issued before the current batch is rotated, so the L2 latency of the cos/sin
-// rows overlaps the rotation and the wait for the next tile to land.
+// Rotation of one landed [128 x D] tile by the 128 threads of the auxiliary warpgroup
+// (at = 0..127), one 32-row quarter at a time, with that quarter's cos/sin rows staged in
+// shared memory by TMA (fp32, [32][D/2] each, unswizzled). Thread `at` owns 16-byte chunk
+// ch = at % kChunks of rows at / kChunks + u * (128 / kChunks) within the quarter.
 template <int D>
 struct Rotator {
   static constexpr int kHalf = D / 2;
   static constexpr int kChunks = kHalf / 8;          // 16-byte chunks per half row
   static constexpr int kRowStep = 128 / kChunks;     // rows between a thread's items
-  static constexpr int kBatches = kChunks / 2;       // kChunks items per thread, 2 per batch
+  static constexpr int kItems = 32 * kChunks / 128;  // items per thread per quarter
 
-  __device__ __forceinline__ static void load(TabBatch& t, const float* __restrict__ cos_t,
-                                              const float* __restrict__ sin_t, int row0, int at,
-                                              int batch) {
+  __device__ __forceinline__ static void quarter(uint32_t tile, uint32_t tab_cos, uint32_t tab_sin,
+                                                 int quarter_idx, int at) {
 #pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const int row = at / kChunks + (2 * batch + u) * kRowStep;
-      const size_t o = static_cast<size_t>(row0 + row) * kHalf + (at % kChunks) * 8;
-      t.c0[u] = __ldg(reinterpret_cast<const float4*>(cos_t + o));
-      t.c1[u] = __ldg(reinterpret_cast<const float4*>(cos_t + o + 4));
-      t.s0[u] = __ldg(reinterpret_cast<const float4*>(sin_t + o));
-      t.s1[u] = __ldg(reinterpret_cast<const float4*>(sin_t + o + 4));
-    }
-  }
-
-  __device__ __forceinline__ static void rotate(uint32_t tile, const TabBatch& t, int at, int batch) {
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      const int row = at / kChunks + (2 * batch + u) * kRowStep, ch = at % kChunks;
+    for (int u = 0; u < kItems; ++u) {
+      const int rq = at / kChunks + u * kRowStep, ch = at % kChunks;   // row within the quarter
+      const int row = quarter_idx * 32 + rq;
+      const uint32_t toff = static_cast<uint32_t>(rq * kHalf + ch * 8) * 4u;
+      const uint4 c0 = lds128(tab_cos + toff), c1 = lds128(tab_cos + toff + 16);
+      const uint4 s0 = lds128(tab_sin + toff), s1 = lds128(tab_sin + toff + 16);
       const uint32_t offa = sw128_offset(row, ch);
       const uint32_t offb = (D == 128) ? 16384u + offa : sw128_offset(row, ch + 4);
       uint4 a = lds128(tile + offa), b = lds128(tile + offb);
-      rotate8(a, b, t.c0[u], t.c1[u], t.s0[u], t.s1[u]);
+      rotate8(a, b, make_float4(__uint_as_float(c0.x), __uint_as_float(c0.y), __uint_as_float(c0.z), __uint_as_float(c0.w)),
+              make_float4(__uint_as_float(c1.x), __uint_as_float(c1.y), __uint_as_float(c1.z), __uint_as_float(c1.w)),
+              make_float4(__uint_as_float(s0.x), __uint_as_float(s0.y), __uint_as_float(s0.z), __uint_as_float(s0.w)),
+              make_float4(__uint_as_float(s1.x), __uint_as_float(s1.y), __uint_as_float(s1.z), __uint_as_float(s1.w)));
       sts128(tile + offa, a);
       sts128(tile + offb, b);
-    }
-  }
-
-  // Rotates `tile` (its batch-0 table values already in buf[0]); before returning, starts
-  // loading batch 0 of the next tile (next_cos == nullptr: none) into buf[0].
-  __device__ __forceinline__ static void tile(uint32_t tile, TabBatch (&buf)[2],
-                                              const float* cos_t, const float* sin_t, int row0,
-                                              const float* next_cos, const float* next_sin,
-                                              int next_row0, int at) {
-#pragma unroll
-    for (int bt = 0; bt < kBatches; ++bt) {
-      if (bt + 1 < kBatches)
-        load(buf[(bt + 1) & 1], cos_t, sin_t, row0, at, bt + 1);
-      else if (next_cos != nullptr)
-        load(buf[(bt + 1) & 1], next_cos, next_sin, next_row0, at, 0);
-      rotate(tile, buf[bt & 1], at, bt);
     }
   }
 };
@@ -237,7 +213,9 @@ __device__ __forceinline__ void write_empty_tile(const KParams& p, int b, int h,
 template <int D, int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, const KParams p) {
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_cq,
+                    const __grid_constant__ CUtensorMap tm_sq, const __grid_constant__ CUtensorMap tm_ck,
+                    const __grid_constant__ CUtensorMap tm_sk, const KParams p) {
   using C = Cfg<D>;
   constexpr int NSK = C::kStagesK, NSV = C::kStagesV;
   extern __shared__ uint8_t smem_raw[];
@@ -247,6 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sQ = s_base + C::kOffQ;
   const uint32_t sK0 = s_base + C::kOffK;
   const uint32_t sV0 = s_base + C::kOffV;
+  const uint32_t sT0 = s_base + C::kOffT;
   Bars* bars = reinterpret_cast<Bars*>(smem + C::kOffBar);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -289,6 +268,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&bars->s_full[t]), 1);
       mbar_init(smem_u32(&bars->p_full[t]), 128);
       mbar_init(smem_u32(&bars->o_done[t]), 1);
+      mbar_init(smem_u32(&bars->t_full[t]), 1);
+      mbar_init(smem_u32(&bars->t_empty[t]), 1);
     }
     mbar_init(smem_u32(&bars->drain), 1);
     fence_mbar_init();
@@ -301,14 +282,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
+    if (kMode == kModeRope) {
+      tma_prefetch_desc(&tm_cq);
+      tma_prefetch_desc(&tm_sq);
+      tma_prefetch_desc(&tm_ck);
+      tma_prefetch_desc(&tm_sk);
+    }
   }
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tbase = bars->tmem_base;
-
-  if (warp == 0) {
-    if (lane == 0) {
+  // Register budgets per warpgroup (56 / 200 / 200 / 56) add up to the launch's 512 x 128;
+  // each is set at the top of its role's branch so that the role's code is compiled to it.
+  if (warp < 4) {
+    regs_dec<56>();
+    if (warp == 0 && lane == 0) {
       // ------------------------------------------------------------ TMA producer
       int nk[NSK], nvl[NSV];
 #pragma unroll
@@ -348,9 +337,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < NSV; ++s)
           if (nvl[s] > 0) drain_wait(smem_u32(&bars->v_full[s]), (nvl[s] - 1) & 1, status);
       }
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {
+    } else if (kMode == kModeRope && warp == 2 && lane == 0) {
+      // ------------------------------------------------------------ table producer
+      // Streams the cos/sin rows of every tile the auxiliary group rotates (Q0, Q1, then
+      // K_0 .. K_n-1), 32 rows at a time, through a 2-buffer ring in shared memory.
+      const int n_rot = n_live + n_kv;
+      int issued = 0;
+      for (int g = 0; g < n_rot * 4; ++g) {
+        const int tile_i = g >> 2, qtr = g & 3, buf = g & 1, use = g >> 1;
+        const bool is_q = tile_i < n_live;
+        const int row = (is_q ? q0 + 128 * tile_i : (tile_i - n_live) * 128) + 32 * qtr;
+        if (use > 0 && !bounded_wait(smem_u32(&bars->t_empty[buf]), (use - 1) & 1, abort_flag,
+                                     status, kStatusTimeoutLoad))
+          break;
+        const uint32_t tf = smem_u32(&bars->t_full[buf]);
+        const uint32_t dst = sT0 + buf * 2 * C::kTabBoxBytes;
+        mbar_arrive_expect_tx(tf, 2 * C::kTabBoxBytes);
+        tma_load_2d(dst, is_q ? &tm_cq : &tm_ck, tf, 0, row);
+        tma_load_2d(dst + C::kTabBoxBytes, is_q ? &tm_sq : &tm_sk, tf, 0, row);
+        ++issued;
+      }
+      if (*abort_flag) {
+        // The last load of each buffer is the only one that can still be in flight.
+        for (int g = issued - 2; g < issued; ++g)
+          if (g >= 0) drain_wait(smem_u32(&bars->t_full[g & 1]), (g >> 1) & 1, status);
+      }
+    } else if (warp == 1 && lane == 0) {
       // ------------------------------------------------------------ MMA issuer
       // S = Q K^T: fp16 operands after the fused rotation, the raw bf16 inputs otherwise.
       constexpr uint32_t kIdS = idesc_f16kind_f32(128, 128, kMode != kModeRope, false, false);
@@ -433,7 +445,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         drain_wait(smem_u32(&bars->drain), 0, status);
       }
     }
-  } else if (warp >= 4 && warp < 12) {
+  } else if (warp < 12) {
+    regs_inc<200>();
     // -------------------------------------------------------------- softmax + epilogue
     const int t = (warp - 4) >> 2;                   // query tile of this warpgroup
     const int r = (tid - 128) & 127;                 // row within the tile = TMEM lane
@@ -454,34 +467,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after_sync();
         const int nv = min(128, kv_valid - j * 128);   // valid keys in this tile (>= 1)
-        // Pass 1: row max over the valid keys. Two 32-column loads in flight at a time and
-        // eight independent partial maxima keep the dependency chains short.
+        // The whole S row in registers: four 32-column loads in flight, one wait.
+        uint32_t sr[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32_nowait(tS + c * 32, sr[c]);
+        tmem_ld_wait_tied(sr[0]);
+        tmem_reg_tie(sr[1]);
+        tmem_reg_tie(sr[2]);
+        tmem_reg_tie(sr[3]);
+        if (nv < 128) {   // keys past the valid length score -inf (whatever S holds there)
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (c * 32 + i >= nv) sr[c][i] = 0xff800000u;
+        }
+        // Row max with eight independent three-input chains.
         float mx8[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) mx8[i] = -INFINITY;
+        for (int k = 0; k < 8; ++k)
+          mx8[k] = fmaxf(__uint_as_float(sr[k >> 1][(k & 1) * 16]), __uint_as_float(sr[k >> 1][(k & 1) * 16 + 1]));
 #pragma unroll
-        for (int c = 0; c < 4; c += 2) {
-          uint32_t sa[32], sb[32];
-          tmem_ld32_nowait(tS + c * 32, sa);
-          tmem_ld32_nowait(tS + c * 32 + 32, sb);
-          tmem_ld_wait_tied(sa);
-          tmem_reg_tie(sb);
-          if (nv == 128) {
+        for (int k = 0; k < 8; ++k)
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              mx8[i & 7] = fmaxf(mx8[i & 7], __uint_as_float(sa[i]));
-              mx8[i & 7] = fmaxf(mx8[i & 7], __uint_as_float(sb[i]));
-            }
-          } else {
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-              if (c * 32 + i < nv) mx8[i & 7] = fmaxf(mx8[i & 7], __uint_as_float(sa[i]));
-              if (c * 32 + 32 + i < nv) mx8[i & 7] = fmaxf(mx8[i & 7], __uint_as_float(sb[i]));
-            }
-          }
-        }
-        const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                               fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+          for (int i = 2; i < 16; i += 2)
+            mx8[k] = fmax3(mx8[k], __uint_as_float(sr[k >> 1][(k & 1) * 16 + i]),
+                           __uint_as_float(sr[k >> 1][(k & 1) * 16 + i + 1]));
+        const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                               fmaxf(mx8[6], mx8[7]));
         const float mt = mx * sl2;
         const bool resc = mt > m_used + kRescaleThreshold;
         const float m_new = resc ? mt : m_used;
@@ -500,36 +513,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         m_used = m_new;
         const float neg_m = -m_used;
-        // Pass 2: P = 2^(s * scale * log2 e - m), masked; row sum in eight partial sums; P
-        // (bf16) into TMEM over columns already consumed (P chunk c lands in S columns
-        // 16c..16c+15 < 32 (c + 1)). The load of chunk c + 1 is in flight while chunk c is
-        // exponentiated.
+        // P = 2^(s * scale * log2 e - m); row sum in four packed partial sums; P (bf16) into
+        // the first 64 columns of S_t in TMEM (the row is already in registers).
         float l8[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) l8[i] = 0.f;
-        uint32_t sr[2][32];
-        tmem_ld32_nowait(tS, sr[0]);
-        tmem_ld_wait_tied(sr[0]);
+        for (int k = 0; k < 8; ++k) l8[k] = 0.f;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-          if (c + 1 < 4) tmem_ld32_nowait(tS + (c + 1) * 32, sr[(c + 1) & 1]);
-          const uint32_t (&cur)[32] = sr[c & 1];
           uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const int col = c * 32 + 2 * i;
-            float p0 = ex2_approx(fmaf(__uint_as_float(cur[2 * i]), sl2, neg_m));
-            float p1 = ex2_approx(fmaf(__uint_as_float(cur[2 * i + 1]), sl2, neg_m));
-            if (nv < 128) {
-              p0 = (col < nv) ? p0 : 0.f;
-              p1 = (col + 1 < nv) ? p1 : 0.f;
-            }
-            l8[(2 * i) & 7] += p0;
-            l8[(2 * i + 1) & 7] += p1;
+            float x0, x1;
+            fma2_bc(x0, x1, __uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1]), sl2, neg_m);
+            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+            add2(l8[2 * (i & 3)], l8[2 * (i & 3) + 1], p0, p1);
             pk[i] = pack_bf16x2(p0, p1);
           }
           tmem_st16_nowait(tS + c * 16, pk);
-          if (c + 1 < 4) tmem_ld_wait_tied(sr[(c + 1) & 1]);
         }
         l = l * alpha + (((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7])));
         tmem_st_wait();
@@ -562,35 +562,44 @@ __global__ void __launch_bounds__(kThreads, 1)
             valid_row ? (m_used + log2f(l)) * kLn2 : -INFINITY;
       }
     }
-  } else if (warp >= 12) {
+  } else {
+    regs_dec<56>();
     // ------------------------------------------------------------ auxiliary warpgroup
     const int at = tid - 384;
     volatile int* go = &bars->aux_go;
     if (kMode == kModeRope) {
       using R = Rotator<D>;
-      TabBatch buf[2];
-      R::load(buf[0], p.cos_q, p.sin_q, q0, at, 0);
-      if (group_wait(b_q_full, 0, abort_flag, status, kStatusTimeoutRope, go, at)) {
-        for (int t = 0; t < n_live; ++t) {
-          const bool last_q = (t + 1 == n_live);
-          R::tile(sQ + t * C::kTileBytes, buf, p.cos_q, p.sin_q, q0 + 128 * t,
-                  last_q ? p.cos_k : p.cos_q, last_q ? p.sin_k : p.sin_q, last_q ? 0 : q0 + 128 * (t + 1), at);
+      // Rotates tile `tile_i` of the sequence Q0, (Q1), K_0, ... whose shared-memory tile is
+      // `sm`, consuming its four staged table quarters; false if a wait gave up.
+      auto rotate_tile = [&](int tile_i, uint32_t sm) -> bool {
+        for (int qtr = 0; qtr < 4; ++qtr) {
+          const int g = tile_i * 4 + qtr, buf = g & 1;
+          if (!group_wait(smem_u32(&bars->t_full[buf]), (g >> 1) & 1, abort_flag, status,
+                          kStatusTimeoutRope, go, at))
+            return false;
+          const uint32_t tc = sT0 + buf * 2 * C::kTabBoxBytes;
+          R::quarter(sm, tc, tc + C::kTabBoxBytes, qtr, at);
+          named_bar_sync(1, 128);                        // every thread is done with the buffer
+          if (at == 0) mbar_arrive(smem_u32(&bars->t_empty[buf]));
         }
+        return true;
+      };
+      bool ok = group_wait(b_q_full, 0, abort_flag, status, kStatusTimeoutRope, go, at);
+      for (int t = 0; ok && t < n_live; ++t) ok = rotate_tile(t, sQ + t * C::kTileBytes);
+      if (ok) {
         fence_proxy_async_smem();
         named_bar_sync(1, 128);
         if (at == 0) mbar_arrive(b_q_ready);
-        for (int j = 0; j < n_kv; ++j) {
-          const int s = j % NSK;
-          if (!group_wait(smem_u32(&bars->k_full[s]), (j / NSK) & 1, abort_flag, status,
-                          kStatusTimeoutRope, go, at))
-            break;
-          const bool more = j + 1 < n_kv;
-          R::tile(sK0 + s * C::kTileBytes, buf, p.cos_k, p.sin_k, j * 128,
-                  more ? p.cos_k : nullptr, p.sin_k, (j + 1) * 128, at);
-          fence_proxy_async_smem();
-          named_bar_sync(1, 128);
-          if (at == 0) mbar_arrive(smem_u32(&bars->k_ready[s]));
-        }
+      }
+      for (int j = 0; ok && j < n_kv; ++j) {
+        const int s = j % NSK;
+        if (!(ok = group_wait(smem_u32(&bars->k_full[s]), (j / NSK) & 1, abort_flag, status,
+                              kStatusTimeoutRope, go, at)))
+          break;
+        if (!(ok = rotate_tile(n_live + j, sK0 + s * C::kTileBytes))) break;
+        fence_proxy_async_smem();
+        named_bar_sync(1, 128);
+        if (at == 0) mbar_arrive(smem_u32(&bars->k_ready[s]));
       }
     } else if (kMode == kModeCross) {
       for (int j = 0; j < n_kv; ++j) {
@@ -626,6 +635,15 @@ cudaError_t launch_mode(const AttnArgs& a) {
       !encode_bshd_map(&mk, a.k, a.B, kvext, a.Skv, a.H, D) ||
       !encode_bshd_map(&mv, a.v, a.B, kvext, a.Skv, a.H, D))
     return cudaErrorInvalidValue;
+  // RoPE tables [rows, D/2] fp32, read 32 rows at a time (a copy of the Q map when unused).
+  CUtensorMap mcq = mq, msq = mq, mck = mq, msk = mq;
+  if (kMode == kModeRope) {
+    if (!encode_rows_map_f32(&mcq, a.cos_q, a.Sq, D / 2, Cfg<D>::kTabRows) ||
+        !encode_rows_map_f32(&msq, a.sin_q, a.Sq, D / 2, Cfg<D>::kTabRows) ||
+        !encode_rows_map_f32(&mck, a.cos_k, a.Skv, D / 2, Cfg<D>::kTabRows) ||
+        !encode_rows_map_f32(&msk, a.sin_k, a.Skv, D / 2, Cfg<D>::kTabRows))
+      return cudaErrorInvalidValue;
+  }
   KParams p;
   p.Sq = a.Sq;
   p.Skv = a.Skv;
@@ -644,7 +662,7 @@ cudaError_t launch_mode(const AttnArgs& a) {
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmemBytes);
   if (e != cudaSuccess) return e;
   dim3 grid((a.Sq + 255) / 256, a.H, a.B);
-  kern<<<grid, kThreads, Cfg<D>::kSmemBytes, a.stream>>>(mq, mk, mv, p);
+  kern<<<grid, kThreads, Cfg<D>::kSmemBytes, a.stream>>>(mq, mk, mv, mcq, msq, mck, msk, p);
   return cudaGetLastError();
 }
 

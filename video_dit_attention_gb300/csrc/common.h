@@ -53,4 +53,8 @@ cudaError_t read_device_status(unsigned int* out, bool clear);
 bool encode_bshd_map(CUtensorMap* map, const void* base, int B, int s_extent, int s_rows, int H,
                      int D);
 
+// Encodes a TMA descriptor for a row-major fp32 matrix [rows, cols] (cols * 4 a multiple of
+// 16 bytes) read in unswizzled boxes of box_rows full rows.
+bool encode_rows_map_f32(CUtensorMap* map, const float* base, int rows, int cols, int box_rows);
+
 }  // namespace dit

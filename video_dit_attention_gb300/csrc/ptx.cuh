@@ -342,8 +342,42 @@ __device__ __forceinline__ void tmem_st_wait() {
 #undef DIT_S8
 
 // ---------------------------------------------------------------------------
+// Per-warpgroup register budgets (all 128 threads of a warpgroup execute these).
+// ---------------------------------------------------------------------------
+template <uint32_t N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// ---------------------------------------------------------------------------
 // Small numeric helpers
 // ---------------------------------------------------------------------------
+// (d0, d1) = (a0, a1) * (b, b) + (c, c) with one packed fp32x2 FMA.
+__device__ __forceinline__ void fma2_bc(float& d0, float& d1, float a0, float a1, float b, float c) {
+  asm("{\n\t.reg .b64 A, B, C, D;\n\t"
+      "mov.b64 A, {%2, %3};\n\tmov.b64 B, {%4, %4};\n\tmov.b64 C, {%5, %5};\n\t"
+      "fma.rn.f32x2 D, A, B, C;\n\tmov.b64 {%0, %1}, D;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b), "f"(c));
+}
+// (d0, d1) += (a0, a1) with one packed fp32x2 add.
+__device__ __forceinline__ void add2(float& d0, float& d1, float a0, float a1) {
+  asm("{\n\t.reg .b64 A, D;\n\t"
+      "mov.b64 A, {%2, %3};\n\tmov.b64 D, {%0, %1};\n\t"
+      "add.f32x2 D, D, A;\n\tmov.b64 {%0, %1}, D;\n\t}"
+      : "+f"(d0), "+f"(d1)
+      : "f"(a0), "f"(a1));
+}
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
 // 2^x on the special-function unit (PTX ex2.approx.ftz.f32; 2^-inf = +0).
 __device__ __forceinline__ float ex2_approx(float x) {
   float y;
