@@ -163,6 +163,17 @@ int dit_pad_tokens(const void* x, void* x_pad, int B, int L, int S_pad, long lon
 int dit_unpad_tokens(const void* x_pad, void* x, int B, int L, int S_pad, long long row_bytes,
                      void* stream);
 
+/* ---------------------------------------------------------------------------------------
+ * Diagnostic: the FMA-pipe exponential the attention softmax uses for part of its
+ * exponentials (the rest go to the special-function unit), applied elementwise:
+ * y[i] ~ 2^x[i] for x[i] <= 126, max relative error 2.6e-6 (degree-4 minimax polynomial
+ * after Cody-Waite range reduction); inputs below -125 give 2^-125 (the kernel only feeds it
+ * arguments where that is negligible). x, y: device fp32 arrays of n elements. No page
+ * defines this; it exists so the approximation can be tested against exp2f.
+ * Errors: DIT_ERR_INVALID_ARG, DIT_ERR_ALIGNMENT (not 4-byte aligned), DIT_ERR_CUDA.
+ * ------------------------------------------------------------------------------------- */
+int dit_exp2_fma_eval(const float* x, float* y, long long n, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -155,3 +155,21 @@ def test_pad_and_unpad_copies(lib):
     torch.cuda.synchronize()
     assert torch.equal(back, x) and torch.equal(xp[:, :300], x)
     assert torch.equal(lb, l) and torch.equal(lp[:, :300], l)
+
+
+def test_fma_exp2_against_exp2f_and_its_bound(lib):
+    """The softmax's FMA-pipe exponential: within its stated 2.6e-6 relative error of the
+    exact 2^x (fp64) over the range the kernel feeds it, and close to CUDA's exp2f."""
+    x = torch.cat([torch.linspace(-125.0, 8.0, 1_000_001), torch.tensor([0.0, -0.5, 0.5, 1.0, -1.0, 7.99])])
+    xd = x.cuda()
+    y = lib.dit_exp2_fma_eval(xd)
+    ref_cuda = torch.exp2(xd)
+    torch.cuda.synchronize()
+    exact = np.exp2(x.double().numpy())
+    rel = np.abs(y.cpu().double().numpy() / exact - 1.0)
+    assert rel.max() <= 3e-6, rel.max()
+    assert torch.max(torch.abs(y / ref_cuda - 1.0)).item() <= 4e-6
+    # below the clamp the result is 2^-125, never negative, NaN or a wrapped exponent
+    z = lib.dit_exp2_fma_eval(torch.tensor([-126.0, -200.0, float("-inf")], device="cuda"))
+    torch.cuda.synchronize()
+    assert torch.all(z > 0) and torch.all(z < 1e-37)

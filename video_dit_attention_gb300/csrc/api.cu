@@ -176,3 +176,10 @@ extern "C" int dit_unpad_tokens(const void* x_pad, void* x, int B, int L, int S_
   return cuda_status(launch_copy_rows(x_pad, x, B, L, S_pad, L, row_bytes,
                                       static_cast<cudaStream_t>(stream)));
 }
+
+extern "C" int dit_exp2_fma_eval(const float* x, float* y, long long n, void* stream) {
+  if (!x || !y || n < 0) return DIT_ERR_INVALID_ARG;
+  if (!aligned(x, 4) || !aligned(y, 4)) return DIT_ERR_ALIGNMENT;
+  if (n == 0) return DIT_OK;
+  return cuda_status(launch_exp2_fma(x, y, n, static_cast<cudaStream_t>(stream)));
+}

@@ -42,6 +42,7 @@
 #include <cuda_bf16.h>
 
 #include "common.h"
+#include "exp2_fma.cuh"
 #include "ptx.cuh"
 
 namespace dit {
@@ -54,6 +55,10 @@ constexpr int kThreads = 512;
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kLog2e = 1.44269504088896340736f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only if m grows by > 2^8
+// Column pairs (index mod 8 within a 32-column chunk) whose exponentials run on the FMA pipe
+// (exp2_fma2) instead of the special-function unit. Measured on GB300 at 1/4, 3/8 and 1/2 of
+// the pairs this was slower than none (the softmax is not bound by ex2 throughput), so none.
+constexpr uint32_t kFmaExpPairs = 0;
 
 template <int D>
 struct Cfg {
@@ -523,9 +528,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t pk[16];
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            float x0, x1;
+            float x0, x1, p0, p1;
             fma2_bc(x0, x1, __uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1]), sl2, neg_m);
-            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+            if ((kFmaExpPairs >> (i & 7)) & 1u) {
+              exp2_fma2(p0, p1, x0, x1);
+            } else {
+              p0 = ex2_approx(x0);
+              p1 = ex2_approx(x1);
+            }
             add2(l8[2 * (i & 3)], l8[2 * (i & 3) + 1], p0, p1);
             pk[i] = pack_bf16x2(p0, p1);
           }

@@ -45,6 +45,8 @@ cudaError_t launch_lse_merge(const void* partial_o, const float* partial_lse, in
 cudaError_t launch_copy_rows(const void* src, void* dst, int B, int L, long long src_rows,
                              long long dst_rows, long long row_bytes, cudaStream_t stream);
 
+cudaError_t launch_exp2_fma(const float* x, float* y, long long n, cudaStream_t stream);
+
 cudaError_t read_device_status(unsigned int* out, bool clear);
 
 // Encodes a TMA descriptor for a BSHD bf16 tensor [B, S_rows, H, D] whose sequence extent is

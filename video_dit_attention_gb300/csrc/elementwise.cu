@@ -6,6 +6,7 @@
 #include <cuda_bf16.h>
 
 #include "common.h"
+#include "exp2_fma.cuh"
 #include "ptx.cuh"
 
 namespace dit {
@@ -135,7 +136,24 @@ __global__ void __launch_bounds__(256) copy_rows_kernel(const uint8_t* __restric
   }
 }
 
+// The attention kernel's FMA-pipe exp2 applied to an array (diagnostic).
+__global__ void __launch_bounds__(256) exp2_fma_kernel(const float* __restrict__ x,
+                                                       float* __restrict__ y, long long n) {
+  for (long long i = 2 * (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x); i < n;
+       i += 2 * static_cast<long long>(gridDim.x) * blockDim.x) {
+    float y0, y1;
+    exp2_fma2(y0, y1, x[i], i + 1 < n ? x[i + 1] : 0.f);
+    y[i] = y0;
+    if (i + 1 < n) y[i + 1] = y1;
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_exp2_fma(const float* x, float* y, long long n, cudaStream_t stream) {
+  exp2_fma_kernel<<<grid_for((n + 1) / 2, 256), 256, 0, stream>>>(x, y, n);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_rope_split_halves(const void* x, void* y, const float* cos_tab,
                                      const float* sin_tab, int B, int S, int H, int D,

@@ -38,6 +38,7 @@ _SIGNATURES = {
     "dit_attn_lse_merge": ([_vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp], _i),
     "dit_pad_tokens": ([_vp, _vp, _i, _i, _i, _ll, _vp], _i),
     "dit_unpad_tokens": ([_vp, _vp, _i, _i, _i, _ll, _vp], _i),
+    "dit_exp2_fma_eval": ([_vp, _vp, _ll, _vp], _i),
 }
 for _name, (_args, _res) in _SIGNATURES.items():
     _fn = getattr(_lib, _name)
@@ -242,4 +243,14 @@ def dit_unpad_tokens(x_pad, L: int, out=None, stream=None):
     row_bytes = x_pad[0, 0].numel() * x_pad.element_size()
     _check("dit_unpad_tokens", _lib.dit_unpad_tokens(_ptr(x_pad), _ptr(out), B, L, S_pad, row_bytes,
                                                      _stream_handle(stream)))
+    return out
+
+
+def dit_exp2_fma_eval(x, out=None, stream=None):
+    """Diagnostic: the softmax's FMA-pipe 2^x applied to a float32 CUDA tensor."""
+    _need(x, "x", torch.float32)
+    if out is None:
+        out = torch.empty_like(x)
+    _need(out, "out", torch.float32)
+    _check("dit_exp2_fma_eval", _lib.dit_exp2_fma_eval(_ptr(x), _ptr(out), x.numel(), _stream_handle(stream)))
     return out
