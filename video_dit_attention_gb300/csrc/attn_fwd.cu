@@ -9,10 +9,11 @@
 // and O = 0, lse = -inf for pad query rows. It is the online-softmax (flash) form of that
 // definition: keys are visited in 128-key tiles and the running max/sum are rescaled.
 //
-// One CTA owns two 128-row query tiles (Q0, Q1) of one (b, h); they share every K/V tile
-// and its rotation. Warp roles (512 threads):
+// Work items are two 128-row query tiles (Q0, Q1) of one (b, h), which share every K/V tile
+// and its rotation; the kernel is persistent (one CTA per SM, items round-robin, see below).
+// Warp roles (512 threads):
 //   warp 0       TMA producer: Q0/Q1 once, then K_j / V_j into a ring of shared-memory stages.
-//   warp 1       TMEM allocator and single-thread tcgen05.mma issuer. Per key tile j it
+//   warp 12      single-thread tcgen05.mma issuer (warp 1 allocates TMEM). Per key tile j it
 //                issues, in this order, O0 += P0_{j-1} V_{j-1}, S0_j = Q0 K_j^T,
 //                O1 += P1_{j-1} V_{j-1}, S1_j = Q1 K_j^T. tcgen05.mma ops of a CTA run in
 //                issue order, so S_t,j may reuse the TMEM columns that held P_t,j-1 and its
@@ -24,7 +25,7 @@
 //                tensor core works on the other tile (ping-pong). O_t is rescaled in TMEM only
 //                when m grows by more than 2^8; the final O / l is exact for any reference m.
 //                Epilogue: O / l to bf16, LSE.
-//   warps 12-15  auxiliary: RoPE rotation of the landed Q and K tiles in shared memory
+//   warps 13-15  auxiliary: RoPE rotation of the landed Q and K tiles in shared memory
 //                (pairs (i, i + D/2) sit at the same swizzled offset of the two 64-column
 //                halves of a row), or, for cross-attention, zeroing of V rows past the
 //                per-batch valid length so that 0 * (pad garbage) cannot reach O.
@@ -52,10 +53,13 @@ __device__ unsigned int g_dit_status;
 namespace {
 
 constexpr int kThreads = 512;
+constexpr int kAuxThreads = 96;   // warps 13-15: RoPE rotation, or zeroing of V pad rows
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kLog2e = 1.44269504088896340736f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale O only if m grows by > 2^8
-// Column pairs (index mod 8 within a 32-column chunk) whose exponentials run on the FMA pipe
+constexpr int kPrefetchLead = 6;  // key tiles before an item's end at which the next is warmed
+constexpr int kPrefetchKV = 4;    // K/V tiles of the next item warmed in L2
+// Column pairs (index 0..7 within a 16-column piece) whose exponentials run on the FMA pipe
 // (exp2_fma2) instead of the special-function unit. Measured on GB300 at 1/4, 3/8 and 1/2 of
 // the pairs this was slower than none (the softmax is not bound by ex2 throughput), so none.
 constexpr uint32_t kFmaExpPairs = 0;
@@ -80,7 +84,8 @@ struct Bars {
   uint64_t q_full, q_ready;
   uint64_t k_full[4], k_ready[4], k_empty[4];
   uint64_t v_full[4], v_ready[4], v_empty[4];
-  uint64_t s_full[2], p_full[2], o_done[2];
+  uint64_t q_empty;
+  uint64_t s_full[2], p_full[2], o_done[2], o_free[2];
   uint64_t t_full[2], t_empty[2];
   uint64_t drain;
   uint32_t tmem_base;
@@ -90,6 +95,7 @@ struct Bars {
 
 struct KParams {
   int Sq, Skv, H;
+  int n_pairs, n_items;   // query-tile pairs per (b, h); B * H * n_pairs work items
   int q_valid, kv_valid;
   const int32_t* kv_valid_dev;
   const float* cos_q;
@@ -124,13 +130,13 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
   return ok != 0;
 }
 
-// Bounded wait taken by one thread of the 128-thread auxiliary warpgroup and broadcast to
-// the group through shared memory and named barrier 1 (all 128 threads call this).
+// Bounded wait taken by one thread of the auxiliary group (warps 13-15) and broadcast to
+// the group through shared memory and named barrier 1 (all of its threads call this).
 __device__ __forceinline__ bool group_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                            unsigned int* status, unsigned int code,
                                            volatile int* go, int at) {
   if (at == 0) *go = bounded_wait(bar, parity, abort_flag, status, code) ? 1 : 0;
-  named_bar_sync(1, 128);
+  named_bar_sync(1, kAuxThreads);
   return *go != 0;
 }
 
@@ -154,22 +160,21 @@ __device__ __forceinline__ void rotate8(uint4& a, uint4& b, const float4 c0, con
   b = make_uint4(bw[0], bw[1], bw[2], bw[3]);
 }
 
-// Rotation of one landed [128 x D] tile by the 128 threads of the auxiliary warpgroup
-// (at = 0..127), one 32-row quarter at a time, with that quarter's cos/sin rows staged in
-// shared memory by TMA (fp32, [32][D/2] each, unswizzled). Thread `at` owns 16-byte chunk
-// ch = at % kChunks of rows at / kChunks + u * (128 / kChunks) within the quarter.
+// Rotation of one landed [128 x D] tile by the auxiliary group (at = 0 .. kAuxThreads-1),
+// one 32-row quarter at a time, with that quarter's cos/sin rows staged in shared memory by
+// TMA (fp32, [32][D/2] each, unswizzled). Item i of a quarter is 16-byte chunk i % kChunks of
+// row i / kChunks (of the first half and the matching chunk of the second half).
 template <int D>
 struct Rotator {
   static constexpr int kHalf = D / 2;
   static constexpr int kChunks = kHalf / 8;          // 16-byte chunks per half row
-  static constexpr int kRowStep = 128 / kChunks;     // rows between a thread's items
-  static constexpr int kItems = 32 * kChunks / 128;  // items per thread per quarter
+  static constexpr int kItems = 32 * kChunks;        // items per quarter
 
   __device__ __forceinline__ static void quarter(uint32_t tile, uint32_t tab_cos, uint32_t tab_sin,
                                                  int quarter_idx, int at) {
 #pragma unroll
-    for (int u = 0; u < kItems; ++u) {
-      const int rq = at / kChunks + u * kRowStep, ch = at % kChunks;   // row within the quarter
+    for (int item = at; item < kItems; item += kAuxThreads) {
+      const int rq = item / kChunks, ch = item % kChunks;   // row within the quarter, chunk
       const int row = quarter_idx * 32 + rq;
       const uint32_t toff = static_cast<uint32_t>(rq * kHalf + ch * 8) * 4u;
       const uint4 c0 = lds128(tab_cos + toff), c1 = lds128(tab_cos + toff + 16);
@@ -193,7 +198,7 @@ __device__ __forceinline__ void zero_rows(uint32_t tile, int first_row, int at) 
   constexpr int kSub = D / 64;
   const int nrows = 128 - first_row;
   const int nchunks = nrows * 8 * kSub;
-  for (int i = at; i < nchunks; i += 128) {
+  for (int i = at; i < nchunks; i += kAuxThreads) {
     const int sub = i / (nrows * 8);
     const int rem = i % (nrows * 8);
     const int row = first_row + rem / 8;
@@ -215,6 +220,35 @@ __device__ __forceinline__ void write_empty_tile(const KParams& p, int b, int h,
     p.lse[(static_cast<size_t>(b) * p.Sq + q_first + r) * p.H + h] = -INFINITY;
 }
 
+// One unit of work: query rows q0 .. q0 + 255 (two 128-row tiles) of one (b, h).
+struct Item {
+  int b, h, q0, n_live, n_kv, kv_valid;
+  bool has1;   // tile 1 (rows q0 + 128 ..) lies inside the padded sequence
+};
+
+template <int kMode>
+__device__ __forceinline__ Item decode_item(const KParams& p, int it) {
+  Item w;
+  const int pair = it % p.n_pairs, bh = it / p.n_pairs;
+  w.h = bh % p.H;
+  w.b = bh / p.H;
+  w.q0 = pair * 256;
+  int kv = p.kv_valid;
+  if (kMode == kModeCross) kv = min(max(p.kv_valid_dev[w.b], 0), p.Skv);
+  w.kv_valid = kv;
+  // Tile t is live if it holds a valid query row and there is at least one key.
+  w.has1 = w.q0 + 128 < p.Sq;
+  const bool live0 = (w.q0 < p.q_valid) && kv > 0;
+  const bool live1 = w.has1 && (w.q0 + 128 < p.q_valid) && kv > 0;
+  w.n_live = live1 ? 2 : (live0 ? 1 : 0);
+  w.n_kv = (kv + 127) / 128;
+  return w;
+}
+
+// Persistent kernel: one CTA per SM walks the items it + k * gridDim.x. Concurrent CTAs thus
+// work on neighbouring items of the same heads and share their K/V tiles in L2. Every ring
+// and barrier phase runs on counters that continue across items, so the loads, the rotation
+// and the first MMAs of the next item overlap the epilogue of the current one.
 template <int D, int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -234,31 +268,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   Bars* bars = reinterpret_cast<Bars*>(smem + C::kOffBar);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int q0 = blockIdx.x * 256, h = blockIdx.y, b = blockIdx.z;
-  int kv_valid = p.kv_valid;
-  if (kMode == kModeCross) kv_valid = min(max(p.kv_valid_dev[b], 0), p.Skv);
-  // Tile t covers query rows q0 + 128 t .. +127; it exists if those rows are inside Sq and
-  // is live if it holds a valid query row and there is at least one key.
-  const bool has1 = q0 + 128 < p.Sq;
-  const bool live0 = (q0 < p.q_valid) && (kv_valid > 0);
-  const bool live1 = has1 && (q0 + 128 < p.q_valid) && (kv_valid > 0);
-  const int n_live = live1 ? 2 : (live0 ? 1 : 0);
-
-  if (n_live == 0) {
-    write_empty_tile<D>(p, b, h, q0, tid, kThreads);
-    if (has1) write_empty_tile<D>(p, b, h, q0 + 128, tid, kThreads);
-    return;
-  }
-  const int n_kv = (kv_valid + 127) / 128;
-
   volatile int* abort_flag = &bars->abort;
   unsigned int* status = &g_dit_status;
   const uint32_t b_q_full = smem_u32(&bars->q_full), b_q_ready = smem_u32(&bars->q_ready);
+  const uint32_t b_q_empty = smem_u32(&bars->q_empty);
 
   if (tid == 0) {
     bars->abort = 0;
     mbar_init(b_q_full, 1);
     mbar_init(b_q_ready, 1);
+    mbar_init(b_q_empty, 1);
     for (int s = 0; s < NSK; ++s) {
       mbar_init(smem_u32(&bars->k_full[s]), 1);
       mbar_init(smem_u32(&bars->k_ready[s]), 1);
@@ -273,6 +292,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&bars->s_full[t]), 1);
       mbar_init(smem_u32(&bars->p_full[t]), 128);
       mbar_init(smem_u32(&bars->o_done[t]), 1);
+      mbar_init(smem_u32(&bars->o_free[t]), 128);
       mbar_init(smem_u32(&bars->t_full[t]), 1);
       mbar_init(smem_u32(&bars->t_empty[t]), 1);
     }
@@ -298,175 +318,134 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tbase = bars->tmem_base;
-  // Register budgets per warpgroup (56 / 200 / 200 / 56) add up to the launch's 512 x 128;
+  const int it0 = blockIdx.x, it_step = gridDim.x;
+
+  // Register budgets per warpgroup (40 / 200 / 200 / 72) add up to the launch's 512 x 128;
   // each is set at the top of its role's branch so that the role's code is compiled to it.
+  // Warpgroup 0 holds the TMA producers, 1 and 2 the softmax, 3 the MMA issuer and the
+  // auxiliary group.
   if (warp < 4) {
-    regs_dec<56>();
+    regs_dec<40>();
     if (warp == 0 && lane == 0) {
       // ------------------------------------------------------------ TMA producer
-      int nk[NSK], nvl[NSV];
-#pragma unroll
-      for (int s = 0; s < NSK; ++s) nk[s] = 0;
-#pragma unroll
-      for (int s = 0; s < NSV; ++s) nvl[s] = 0;
-      mbar_arrive_expect_tx(b_q_full, n_live * C::kTileBytes);
-      for (int t = 0; t < n_live; ++t)
-#pragma unroll
-        for (int c = 0; c < C::kSub; ++c)
-          tma_load_4d(sQ + t * C::kTileBytes + c * 16384, &tm_q, b_q_full, c * 64, h, q0 + 128 * t, b);
-      for (int j = 0; j < n_kv; ++j) {
-        const int sk = j % NSK, uk = j / NSK, sv = j % NSV, uv = j / NSV;
-        const uint32_t kf = smem_u32(&bars->k_full[sk]), vf = smem_u32(&bars->v_full[sv]);
-        if (uk > 0 && !bounded_wait(smem_u32(&bars->k_empty[sk]), (uk - 1) & 1, abort_flag, status,
-                                    kStatusTimeoutLoad))
+      int kv_cnt = 0, q_cnt = 0, k_issued = 0, v_issued = 0;
+      bool ok = true;
+      for (int it = it0; ok && it < p.n_items; it += it_step) {
+        const Item w = decode_item<kMode>(p, it);
+        if (w.n_live == 0) continue;
+        // The Q buffers are free once every S MMA of the previous item has completed.
+        if (q_cnt > 0 && !(ok = bounded_wait(b_q_empty, (q_cnt - 1) & 1, abort_flag, status,
+                                             kStatusTimeoutLoad)))
           break;
-        mbar_arrive_expect_tx(kf, C::kTileBytes);
+        mbar_arrive_expect_tx(b_q_full, w.n_live * C::kTileBytes);
+        for (int t = 0; t < w.n_live; ++t)
 #pragma unroll
-        for (int c = 0; c < C::kSub; ++c)
-          tma_load_4d(sK0 + sk * C::kTileBytes + c * 16384, &tm_k, kf, c * 64, h, j * 128, b);
-        ++nk[sk];
-        if (uv > 0 && !bounded_wait(smem_u32(&bars->v_empty[sv]), (uv - 1) & 1, abort_flag, status,
-                                    kStatusTimeoutLoad))
-          break;
-        mbar_arrive_expect_tx(vf, C::kTileBytes);
+          for (int c = 0; c < C::kSub; ++c)
+            tma_load_4d(sQ + t * C::kTileBytes + c * 16384, &tm_q, b_q_full, c * 64, w.h,
+                        w.q0 + 128 * t, w.b);
+        ++q_cnt;
+        for (int j = 0; j < w.n_kv; ++j) {
+          if (j == (w.n_kv > kPrefetchLead ? w.n_kv - kPrefetchLead : 0)) {
+            // The next item of this CTA usually starts a head no CTA has read yet, at the same
+            // moment as every other CTA: warm L2 with its Q tiles and first K/V tiles now.
+            const int nit = it + it_step;
+            if (nit < p.n_items) {
+              const Item nw = decode_item<kMode>(p, nit);
+              for (int t = 0; t < nw.n_live; ++t)
 #pragma unroll
-        for (int c = 0; c < C::kSub; ++c)
-          tma_load_4d(sV0 + sv * C::kTileBytes + c * 16384, &tm_v, vf, c * 64, h, j * 128, b);
-        ++nvl[sv];
+                for (int c = 0; c < C::kSub; ++c)
+                  tma_prefetch_l2_4d(&tm_q, c * 64, nw.h, nw.q0 + 128 * t, nw.b);
+              for (int jj = 0; jj < nw.n_kv && jj < kPrefetchKV; ++jj)
+#pragma unroll
+                for (int c = 0; c < C::kSub; ++c) {
+                  tma_prefetch_l2_4d(&tm_k, c * 64, nw.h, jj * 128, nw.b);
+                  tma_prefetch_l2_4d(&tm_v, c * 64, nw.h, jj * 128, nw.b);
+                }
+            }
+          }
+          const int g = kv_cnt + j, sk = g % NSK, uk = g / NSK, sv = g % NSV, uv = g / NSV;
+          if (uk > 0 && !(ok = bounded_wait(smem_u32(&bars->k_empty[sk]), (uk - 1) & 1, abort_flag,
+                                            status, kStatusTimeoutLoad)))
+            break;
+          const uint32_t kf = smem_u32(&bars->k_full[sk]);
+          mbar_arrive_expect_tx(kf, C::kTileBytes);
+#pragma unroll
+          for (int c = 0; c < C::kSub; ++c)
+            tma_load_4d(sK0 + sk * C::kTileBytes + c * 16384, &tm_k, kf, c * 64, w.h, j * 128, w.b);
+          ++k_issued;
+          if (uv > 0 && !(ok = bounded_wait(smem_u32(&bars->v_empty[sv]), (uv - 1) & 1, abort_flag,
+                                            status, kStatusTimeoutLoad)))
+            break;
+          const uint32_t vf = smem_u32(&bars->v_full[sv]);
+          mbar_arrive_expect_tx(vf, C::kTileBytes);
+#pragma unroll
+          for (int c = 0; c < C::kSub; ++c)
+            tma_load_4d(sV0 + sv * C::kTileBytes + c * 16384, &tm_v, vf, c * 64, w.h, j * 128, w.b);
+          ++v_issued;
+        }
+        kv_cnt += w.n_kv;
       }
       if (*abort_flag) {
-        // Let every copy this thread started land before the CTA gives up its memory.
-        drain_wait(b_q_full, 0, status);
-        for (int s = 0; s < NSK; ++s)
-          if (nk[s] > 0) drain_wait(smem_u32(&bars->k_full[s]), (nk[s] - 1) & 1, status);
-        for (int s = 0; s < NSV; ++s)
-          if (nvl[s] > 0) drain_wait(smem_u32(&bars->v_full[s]), (nvl[s] - 1) & 1, status);
+        // Let the copies still in flight land before the CTA gives up its shared memory: the
+        // last Q load and the last load of every K and V stage.
+        if (q_cnt > 0) drain_wait(b_q_full, (q_cnt - 1) & 1, status);
+        for (int g = k_issued - NSK > 0 ? k_issued - NSK : 0; g < k_issued; ++g)
+          drain_wait(smem_u32(&bars->k_full[g % NSK]), (g / NSK) & 1, status);
+        for (int g = v_issued - NSV > 0 ? v_issued - NSV : 0; g < v_issued; ++g)
+          drain_wait(smem_u32(&bars->v_full[g % NSV]), (g / NSV) & 1, status);
       }
     } else if (kMode == kModeRope && warp == 2 && lane == 0) {
       // ------------------------------------------------------------ table producer
-      // Streams the cos/sin rows of every tile the auxiliary group rotates (Q0, Q1, then
-      // K_0 .. K_n-1), 32 rows at a time, through a 2-buffer ring in shared memory.
-      const int n_rot = n_live + n_kv;
-      int issued = 0;
-      for (int g = 0; g < n_rot * 4; ++g) {
-        const int tile_i = g >> 2, qtr = g & 3, buf = g & 1, use = g >> 1;
-        const bool is_q = tile_i < n_live;
-        const int row = (is_q ? q0 + 128 * tile_i : (tile_i - n_live) * 128) + 32 * qtr;
-        if (use > 0 && !bounded_wait(smem_u32(&bars->t_empty[buf]), (use - 1) & 1, abort_flag,
-                                     status, kStatusTimeoutLoad))
-          break;
-        const uint32_t tf = smem_u32(&bars->t_full[buf]);
-        const uint32_t dst = sT0 + buf * 2 * C::kTabBoxBytes;
-        mbar_arrive_expect_tx(tf, 2 * C::kTabBoxBytes);
-        tma_load_2d(dst, is_q ? &tm_cq : &tm_ck, tf, 0, row);
-        tma_load_2d(dst + C::kTabBoxBytes, is_q ? &tm_sq : &tm_sk, tf, 0, row);
-        ++issued;
+      // Streams the cos/sin rows of every tile the auxiliary group rotates (per item: Q0,
+      // Q1, then K_0 .. K_n-1), 32 rows at a time, through a 2-buffer ring in shared memory.
+      int g = 0;
+      bool ok = true;
+      for (int it = it0; ok && it < p.n_items; it += it_step) {
+        const Item w = decode_item<kMode>(p, it);
+        if (w.n_live == 0) continue;
+        const int n_rot = w.n_live + w.n_kv;
+        for (int r = 0; ok && r < n_rot * 4; ++r, ++g) {
+          const int tile_i = r >> 2, qtr = r & 3, buf = g & 1, use = g >> 1;
+          const bool is_q = tile_i < w.n_live;
+          const int row = (is_q ? w.q0 + 128 * tile_i : (tile_i - w.n_live) * 128) + 32 * qtr;
+          if (use > 0 && !(ok = bounded_wait(smem_u32(&bars->t_empty[buf]), (use - 1) & 1,
+                                             abort_flag, status, kStatusTimeoutLoad)))
+            break;
+          const uint32_t tf = smem_u32(&bars->t_full[buf]);
+          const uint32_t dst = sT0 + buf * 2 * C::kTabBoxBytes;
+          mbar_arrive_expect_tx(tf, 2 * C::kTabBoxBytes);
+          tma_load_2d(dst, is_q ? &tm_cq : &tm_ck, tf, 0, row);
+          tma_load_2d(dst + C::kTabBoxBytes, is_q ? &tm_sq : &tm_sk, tf, 0, row);
+        }
       }
       if (*abort_flag) {
         // The last load of each buffer is the only one that can still be in flight.
-        for (int g = issued - 2; g < issued; ++g)
-          if (g >= 0) drain_wait(smem_u32(&bars->t_full[g & 1]), (g >> 1) & 1, status);
-      }
-    } else if (warp == 1 && lane == 0) {
-      // ------------------------------------------------------------ MMA issuer
-      // S = Q K^T: fp16 operands after the fused rotation, the raw bf16 inputs otherwise.
-      constexpr uint32_t kIdS = idesc_f16kind_f32(128, 128, kMode != kModeRope, false, false);
-      constexpr uint32_t kIdO = idesc_bf16_f32(128, D, false, true);
-      bool ok = bounded_wait(kMode == kModeRope ? b_q_ready : b_q_full, 0, abort_flag, status,
-                             kStatusTimeoutMma);
-      auto wait_k = [&](int j) -> bool {
-        const int s = j % NSK;
-        const uint32_t kbar = (kMode == kModeRope) ? smem_u32(&bars->k_ready[s]) : smem_u32(&bars->k_full[s]);
-        if (!bounded_wait(kbar, (j / NSK) & 1, abort_flag, status, kStatusTimeoutMma)) return false;
-        tc_fence_after_sync();
-        return true;
-      };
-      auto wait_v = [&](int j) -> bool {
-        const int s = j % NSV;
-        const uint32_t vbar = (kMode == kModeCross) ? smem_u32(&bars->v_ready[s]) : smem_u32(&bars->v_full[s]);
-        if (!bounded_wait(vbar, (j / NSV) & 1, abort_flag, status, kStatusTimeoutMma)) return false;
-        tc_fence_after_sync();
-        return true;
-      };
-      auto wait_p = [&](int t, int j) -> bool {
-        if (!bounded_wait(smem_u32(&bars->p_full[t]), j & 1, abort_flag, status, kStatusTimeoutMma))
-          return false;
-        tc_fence_after_sync();
-        return true;
-      };
-      auto issue_s = [&](int t, int j) {
-        const uint32_t sK = sK0 + (j % NSK) * C::kTileBytes;
-        const uint32_t sQt = sQ + t * C::kTileBytes;
-        const uint32_t d = tbase + t * 128;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk / 4) * 16384 + (kk % 4) * 32;
-          mma_bf16_ss(d, smem_desc_sw128(sQt + off, 16, 1024), smem_desc_sw128(sK + off, 16, 1024),
-                      kIdS, kk > 0);
-        }
-        mma_commit(smem_u32(&bars->s_full[t]));
-      };
-      auto issue_pv = [&](int t, int j) {
-        const uint32_t sV = sV0 + (j % NSV) * C::kTileBytes;
-        const uint32_t a_tmem = tbase + t * 128;          // P_t: bf16 pairs in TMEM
-        const uint32_t d = tbase + 256 + t * 128;         // O_t
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          mma_bf16_ts(d, a_tmem + kk * 8, smem_desc_sw128(sV + kk * 2048, 16384, 1024), kIdO,
-                      (j > 0 || kk > 0) ? 1u : 0u);
-      };
-      if (ok) ok = wait_k(0);
-      if (ok) {
-        issue_s(0, 0);
-        if (n_live == 2) issue_s(1, 0);
-        mma_commit(smem_u32(&bars->k_empty[0]));
-      }
-      for (int j = 1; ok && j < n_kv; ++j) {
-        if (!(ok = wait_v(j - 1) && wait_p(0, j - 1))) break;
-        issue_pv(0, j - 1);
-        if (!(ok = wait_k(j))) break;
-        issue_s(0, j);
-        if (n_live == 2) {
-          if (!(ok = wait_p(1, j - 1))) break;
-          issue_pv(1, j - 1);
-          issue_s(1, j);
-        }
-        mma_commit(smem_u32(&bars->v_empty[(j - 1) % NSV]));
-        mma_commit(smem_u32(&bars->k_empty[j % NSK]));
-      }
-      if (ok) ok = wait_v(n_kv - 1) && wait_p(0, n_kv - 1);
-      if (ok) {
-        issue_pv(0, n_kv - 1);
-        mma_commit(smem_u32(&bars->o_done[0]));
-        if (n_live == 2 && (ok = wait_p(1, n_kv - 1))) {
-          issue_pv(1, n_kv - 1);
-          mma_commit(smem_u32(&bars->o_done[1]));
-        }
-        mma_commit(smem_u32(&bars->v_empty[(n_kv - 1) % NSV]));
-      }
-      if (*abort_flag) {
-        // Wait for every MMA issued so far before TMEM and shared memory are released.
-        mma_commit(smem_u32(&bars->drain));
-        drain_wait(smem_u32(&bars->drain), 0, status);
+        for (int x = g - 2; x < g; ++x)
+          if (x >= 0) drain_wait(smem_u32(&bars->t_full[x & 1]), (x >> 1) & 1, status);
       }
     }
   } else if (warp < 12) {
     regs_inc<200>();
     // -------------------------------------------------------------- softmax + epilogue
-    const int t = (warp - 4) >> 2;                   // query tile of this warpgroup
+    const int t = (warp - 4) >> 2;                   // query-tile slot of this warpgroup
     const int r = (tid - 128) & 127;                 // row within the tile = TMEM lane
-    const int qrow = q0 + 128 * t + r;
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tS = tbase + lane_off + t * 128;  // S_t (and P_t in its first 64 columns)
     const uint32_t tO = tbase + lane_off + 256 + t * 128;
-    if (t >= n_live) {
-      if (has1) write_empty_tile<D>(p, b, h, q0 + 128, r, 128);
-    } else {
-      const float sl2 = p.scale_log2;
+    const float sl2 = p.scale_log2;
+    int sc = 0, epi = 0;
+    bool ok = true;
+    for (int it = it0; ok && it < p.n_items; it += it_step) {
+      const Item w = decode_item<kMode>(p, it);
+      if (t >= w.n_live) {
+        if (t == 0 || w.has1) write_empty_tile<D>(p, w.b, w.h, w.q0 + 128 * t, r, 128);
+        continue;
+      }
+      const int n_kv = w.n_kv, kv_valid = w.kv_valid;
       float m_used = -INFINITY, l = 0.f;
-      bool ok = true;
       for (int j = 0; j < n_kv; ++j) {
-        if (!warp_wait(smem_u32(&bars->s_full[t]), j & 1, abort_flag, status, kStatusTimeoutSoftmax)) {
+        if (!warp_wait(smem_u32(&bars->s_full[t]), (sc + j) & 1, abort_flag, status,
+                       kStatusTimeoutSoftmax)) {
           ok = false;
           break;
         }
@@ -487,19 +466,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 32; ++i)
               if (c * 32 + i >= nv) sr[c][i] = 0xff800000u;
         }
-        // Row max with eight independent three-input chains.
-        float mx8[8];
+        // Row max with four independent three-input chains (one per 32-column chunk).
+        float mx4[4];
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-          mx8[k] = fmaxf(__uint_as_float(sr[k >> 1][(k & 1) * 16]), __uint_as_float(sr[k >> 1][(k & 1) * 16 + 1]));
+        for (int c = 0; c < 4; ++c) {
+          mx4[c] = fmaxf(__uint_as_float(sr[c][0]), __uint_as_float(sr[c][1]));
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-#pragma unroll
-          for (int i = 2; i < 16; i += 2)
-            mx8[k] = fmax3(mx8[k], __uint_as_float(sr[k >> 1][(k & 1) * 16 + i]),
-                           __uint_as_float(sr[k >> 1][(k & 1) * 16 + i + 1]));
-        const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
-                               fmaxf(mx8[6], mx8[7]));
+          for (int i = 2; i < 32; i += 2)
+            mx4[c] = fmax3(mx4[c], __uint_as_float(sr[c][i]), __uint_as_float(sr[c][i + 1]));
+        }
+        const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
         const float mt = mx * sl2;
         const bool resc = mt > m_used + kRescaleThreshold;
         const float m_new = resc ? mt : m_used;
@@ -520,111 +496,238 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float neg_m = -m_used;
         // P = 2^(s * scale * log2 e - m); row sum in four packed partial sums; P (bf16) into
         // the first 64 columns of S_t in TMEM (the row is already in registers).
-        float l8[8];
+        float l4[4];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) l8[k] = 0.f;
+        for (int k = 0; k < 4; ++k) l4[k] = 0.f;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t pk[16];
+        for (int c = 0; c < 8; ++c) {           // 16 columns at a time
+          uint32_t pk[8];
 #pragma unroll
-          for (int i = 0; i < 16; ++i) {
+          for (int i = 0; i < 8; ++i) {
             float x0, x1, p0, p1;
-            fma2_bc(x0, x1, __uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1]), sl2, neg_m);
-            if ((kFmaExpPairs >> (i & 7)) & 1u) {
+            fma2_bc(x0, x1, __uint_as_float(sr[c >> 1][(c & 1) * 16 + 2 * i]),
+                    __uint_as_float(sr[c >> 1][(c & 1) * 16 + 2 * i + 1]), sl2, neg_m);
+            if ((kFmaExpPairs >> i) & 1u) {
               exp2_fma2(p0, p1, x0, x1);
             } else {
               p0 = ex2_approx(x0);
               p1 = ex2_approx(x1);
             }
-            add2(l8[2 * (i & 3)], l8[2 * (i & 3) + 1], p0, p1);
+            add2(l4[2 * (i & 1)], l4[2 * (i & 1) + 1], p0, p1);
             pk[i] = pack_bf16x2(p0, p1);
           }
-          tmem_st16_nowait(tS + c * 16, pk);
+          tmem_st8_nowait(tS + c * 8, pk);
         }
-        l = l * alpha + (((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7])));
+        l = l * alpha + ((l4[0] + l4[1]) + (l4[2] + l4[3]));
         tmem_st_wait();
         tc_fence_before_sync();
         mbar_arrive(smem_u32(&bars->p_full[t]));
       }
-      if (ok && warp_wait(smem_u32(&bars->o_done[t]), 0, abort_flag, status, kStatusTimeoutSoftmax)) {
-        tc_fence_after_sync();
-        const bool valid_row = qrow < p.q_valid;
-        const float inv_l = 1.f / l;
-        uint16_t* dst = p.out + ((static_cast<size_t>(b) * p.Sq + qrow) * p.H + h) * D;
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t orr[32];
-          tmem_ld32(tO + c * 32, orr);
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            uint4 w = make_uint4(0, 0, 0, 0);
-            if (valid_row) {
-              const float* f = reinterpret_cast<const float*>(&orr[8 * q4]);
-              w.x = pack_bf16x2(f[0] * inv_l, f[1] * inv_l);
-              w.y = pack_bf16x2(f[2] * inv_l, f[3] * inv_l);
-              w.z = pack_bf16x2(f[4] * inv_l, f[5] * inv_l);
-              w.w = pack_bf16x2(f[6] * inv_l, f[7] * inv_l);
-            }
-            *reinterpret_cast<uint4*>(dst + c * 32 + q4 * 8) = w;
-          }
-        }
-        p.lse[(static_cast<size_t>(b) * p.Sq + qrow) * p.H + h] =
-            valid_row ? (m_used + log2f(l)) * kLn2 : -INFINITY;
+      if (!ok || !warp_wait(smem_u32(&bars->o_done[t]), epi & 1, abort_flag, status,
+                            kStatusTimeoutSoftmax)) {
+        ok = false;
+        break;
       }
+      tc_fence_after_sync();
+      const int qrow = w.q0 + 128 * t + r;
+      const bool valid_row = qrow < p.q_valid;
+      const float inv_l = 1.f / l;
+      uint16_t* dst = p.out + ((static_cast<size_t>(w.b) * p.Sq + qrow) * p.H + w.h) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t orr[32];
+        tmem_ld32(tO + c * 32, orr);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          uint4 o = make_uint4(0, 0, 0, 0);
+          if (valid_row) {
+            const float* f = reinterpret_cast<const float*>(&orr[8 * q4]);
+            o.x = pack_bf16x2(f[0] * inv_l, f[1] * inv_l);
+            o.y = pack_bf16x2(f[2] * inv_l, f[3] * inv_l);
+            o.z = pack_bf16x2(f[4] * inv_l, f[5] * inv_l);
+            o.w = pack_bf16x2(f[6] * inv_l, f[7] * inv_l);
+          }
+          *reinterpret_cast<uint4*>(dst + c * 32 + q4 * 8) = o;
+        }
+      }
+      // O_t has been read out of TMEM: the next item may overwrite it.
+      tc_fence_before_sync();
+      mbar_arrive(smem_u32(&bars->o_free[t]));
+      p.lse[(static_cast<size_t>(w.b) * p.Sq + qrow) * p.H + w.h] =
+          valid_row ? (m_used + log2f(l)) * kLn2 : -INFINITY;
+      sc += n_kv;
+      ++epi;
     }
   } else {
-    regs_dec<56>();
-    // ------------------------------------------------------------ auxiliary warpgroup
-    const int at = tid - 384;
+    regs_dec<72>();
+    if (warp == 12) {
+     if (lane == 0) {
+      // ------------------------------------------------------------ MMA issuer
+      // S = Q K^T: fp16 operands after the fused rotation, the raw bf16 inputs otherwise.
+      constexpr uint32_t kIdS = idesc_f16kind_f32(128, 128, kMode != kModeRope, false, false);
+      constexpr uint32_t kIdO = idesc_bf16_f32(128, D, false, true);
+      int kv_cnt = 0, q_cnt = 0;
+      // Per query-tile slot: S tiles issued so far (p_full phases) and items whose O_t has gone
+      // to the epilogue (o_free phases); scalars, so that they stay in registers.
+      int sc0 = 0, sc1 = 0, epi0 = 0, epi1 = 0;
+      bool ok = true;
+      auto wait_k = [&](int g) -> bool {
+        const int s = g % NSK;
+        const uint32_t kbar = (kMode == kModeRope) ? smem_u32(&bars->k_ready[s]) : smem_u32(&bars->k_full[s]);
+        if (!bounded_wait(kbar, (g / NSK) & 1, abort_flag, status, kStatusTimeoutMma)) return false;
+        tc_fence_after_sync();
+        return true;
+      };
+      auto wait_v = [&](int g) -> bool {
+        const int s = g % NSV;
+        const uint32_t vbar = (kMode == kModeCross) ? smem_u32(&bars->v_ready[s]) : smem_u32(&bars->v_full[s]);
+        if (!bounded_wait(vbar, (g / NSV) & 1, abort_flag, status, kStatusTimeoutMma)) return false;
+        tc_fence_after_sync();
+        return true;
+      };
+      auto wait_bar = [&](uint32_t bar, int phase) -> bool {
+        if (!bounded_wait(bar, phase & 1, abort_flag, status, kStatusTimeoutMma)) return false;
+        tc_fence_after_sync();
+        return true;
+      };
+      // Descriptors are built once per tile and advanced by constant offsets (the address
+      // field counts 16-byte units), which keeps this thread's register needs small.
+      auto issue_s = [&](int t, int g) {
+        const uint64_t da = smem_desc_sw128(sQ + t * C::kTileBytes, 16, 1024);
+        const uint64_t db = smem_desc_sw128(sK0 + (g % NSK) * C::kTileBytes, 16, 1024);
+        const uint32_t d = tbase + t * 128;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint64_t off = ((kk / 4) * 16384 + (kk % 4) * 32) >> 4;
+          mma_bf16_ss(d, da + off, db + off, kIdS, kk > 0);
+        }
+        mma_commit(smem_u32(&bars->s_full[t]));
+      };
+      // O_t (+)= P_t V_g; the first key tile of an item overwrites O_t, so it waits until the
+      // epilogue of the previous item that used this slot has read O_t out of TMEM.
+      auto issue_pv = [&](int t, int g, int j) -> bool {
+        const int sct = t ? sc1 : sc0, epit = t ? epi1 : epi0;
+        if (!wait_bar(smem_u32(&bars->p_full[t]), sct + j)) return false;
+        if (j == 0 && epit > 0 && !wait_bar(smem_u32(&bars->o_free[t]), epit - 1)) return false;
+        const uint64_t db = smem_desc_sw128(sV0 + (g % NSV) * C::kTileBytes, 16384, 1024);
+        const uint32_t a_tmem = tbase + t * 128;          // P_t: bf16 pairs in TMEM
+        const uint32_t d = tbase + 256 + t * 128;         // O_t
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          mma_bf16_ts(d, a_tmem + kk * 8, db + static_cast<uint64_t>(kk * 2048 >> 4), kIdO,
+                      (j > 0 || kk > 0) ? 1u : 0u);
+        return true;
+      };
+      for (int it = it0; ok && it < p.n_items; it += it_step) {
+        const Item w = decode_item<kMode>(p, it);
+        if (w.n_live == 0) continue;
+        if (!(ok = wait_bar(kMode == kModeRope ? b_q_ready : b_q_full, q_cnt))) break;
+        if (!(ok = wait_k(kv_cnt))) break;
+        issue_s(0, kv_cnt);
+        if (w.n_live == 2) issue_s(1, kv_cnt);
+        mma_commit(smem_u32(&bars->k_empty[kv_cnt % NSK]));
+        for (int j = 1; ok && j < w.n_kv; ++j) {
+          const int g = kv_cnt + j;
+          if (!(ok = wait_v(g - 1) && issue_pv(0, g - 1, j - 1))) break;
+          if (!(ok = wait_k(g))) break;
+          issue_s(0, g);
+          if (w.n_live == 2) {
+            if (!(ok = issue_pv(1, g - 1, j - 1))) break;
+            issue_s(1, g);
+          }
+          mma_commit(smem_u32(&bars->v_empty[(g - 1) % NSV]));
+          mma_commit(smem_u32(&bars->k_empty[g % NSK]));
+        }
+        if (!ok) break;
+        const int gl = kv_cnt + w.n_kv - 1;
+        if (!(ok = wait_v(gl) && issue_pv(0, gl, w.n_kv - 1))) break;
+        mma_commit(smem_u32(&bars->o_done[0]));
+        if (w.n_live == 2) {
+          if (!(ok = issue_pv(1, gl, w.n_kv - 1))) break;
+          mma_commit(smem_u32(&bars->o_done[1]));
+        }
+        mma_commit(smem_u32(&bars->v_empty[gl % NSV]));
+        mma_commit(b_q_empty);
+        sc0 += w.n_kv;
+        ++epi0;
+        if (w.n_live == 2) {
+          sc1 += w.n_kv;
+          ++epi1;
+        }
+        kv_cnt += w.n_kv;
+        ++q_cnt;
+      }
+      if (*abort_flag) {
+        // Wait for every MMA issued so far before TMEM and shared memory are released.
+        mma_commit(smem_u32(&bars->drain));
+        drain_wait(smem_u32(&bars->drain), 0, status);
+      }
+    }
+    } else {
+    // ------------------------------------------------------------ auxiliary group (96 threads)
+    const int at = tid - 416;
     volatile int* go = &bars->aux_go;
+    int kv_cnt = 0, q_cnt = 0, g = 0;
+    bool ok = true;
     if (kMode == kModeRope) {
       using R = Rotator<D>;
-      // Rotates tile `tile_i` of the sequence Q0, (Q1), K_0, ... whose shared-memory tile is
-      // `sm`, consuming its four staged table quarters; false if a wait gave up.
-      auto rotate_tile = [&](int tile_i, uint32_t sm) -> bool {
-        for (int qtr = 0; qtr < 4; ++qtr) {
-          const int g = tile_i * 4 + qtr, buf = g & 1;
+      // Rotates one tile whose four staged table quarters are next in the ring.
+      auto rotate_tile = [&](uint32_t sm) -> bool {
+        for (int qtr = 0; qtr < 4; ++qtr, ++g) {
+          const int buf = g & 1;
           if (!group_wait(smem_u32(&bars->t_full[buf]), (g >> 1) & 1, abort_flag, status,
                           kStatusTimeoutRope, go, at))
             return false;
           const uint32_t tc = sT0 + buf * 2 * C::kTabBoxBytes;
           R::quarter(sm, tc, tc + C::kTabBoxBytes, qtr, at);
-          named_bar_sync(1, 128);                        // every thread is done with the buffer
+          named_bar_sync(1, kAuxThreads);                // every thread is done with the buffer
           if (at == 0) mbar_arrive(smem_u32(&bars->t_empty[buf]));
         }
         return true;
       };
-      bool ok = group_wait(b_q_full, 0, abort_flag, status, kStatusTimeoutRope, go, at);
-      for (int t = 0; ok && t < n_live; ++t) ok = rotate_tile(t, sQ + t * C::kTileBytes);
-      if (ok) {
-        fence_proxy_async_smem();
-        named_bar_sync(1, 128);
-        if (at == 0) mbar_arrive(b_q_ready);
-      }
-      for (int j = 0; ok && j < n_kv; ++j) {
-        const int s = j % NSK;
-        if (!(ok = group_wait(smem_u32(&bars->k_full[s]), (j / NSK) & 1, abort_flag, status,
-                              kStatusTimeoutRope, go, at)))
+      for (int it = it0; ok && it < p.n_items; it += it_step) {
+        const Item w = decode_item<kMode>(p, it);
+        if (w.n_live == 0) continue;
+        if (!(ok = group_wait(b_q_full, q_cnt & 1, abort_flag, status, kStatusTimeoutRope, go, at)))
           break;
-        if (!(ok = rotate_tile(n_live + j, sK0 + s * C::kTileBytes))) break;
+        for (int t = 0; ok && t < w.n_live; ++t) ok = rotate_tile(sQ + t * C::kTileBytes);
+        if (!ok) break;
         fence_proxy_async_smem();
-        named_bar_sync(1, 128);
-        if (at == 0) mbar_arrive(smem_u32(&bars->k_ready[s]));
+        named_bar_sync(1, kAuxThreads);
+        if (at == 0) mbar_arrive(b_q_ready);
+        for (int j = 0; ok && j < w.n_kv; ++j) {
+          const int gk = kv_cnt + j, s = gk % NSK;
+          if (!(ok = group_wait(smem_u32(&bars->k_full[s]), (gk / NSK) & 1, abort_flag, status,
+                                kStatusTimeoutRope, go, at)))
+            break;
+          if (!(ok = rotate_tile(sK0 + s * C::kTileBytes))) break;
+          fence_proxy_async_smem();
+          named_bar_sync(1, kAuxThreads);
+          if (at == 0) mbar_arrive(smem_u32(&bars->k_ready[s]));
+        }
+        kv_cnt += w.n_kv;
+        ++q_cnt;
       }
     } else if (kMode == kModeCross) {
-      for (int j = 0; j < n_kv; ++j) {
-        const int s = j % NSV;
-        if (!group_wait(smem_u32(&bars->v_full[s]), (j / NSV) & 1, abort_flag, status,
-                        kStatusTimeoutRope, go, at))
-          break;
-        const int nv = min(128, kv_valid - j * 128);
-        if (nv < 128) {
-          zero_rows<D>(sV0 + s * C::kTileBytes, nv, at);
-          fence_proxy_async_smem();
+      for (int it = it0; ok && it < p.n_items; it += it_step) {
+        const Item w = decode_item<kMode>(p, it);
+        if (w.n_live == 0) continue;
+        for (int j = 0; ok && j < w.n_kv; ++j) {
+          const int gv = kv_cnt + j, s = gv % NSV;
+          if (!(ok = group_wait(smem_u32(&bars->v_full[s]), (gv / NSV) & 1, abort_flag, status,
+                                kStatusTimeoutRope, go, at)))
+            break;
+          const int nv = min(128, w.kv_valid - j * 128);
+          if (nv < 128) {
+            zero_rows<D>(sV0 + s * C::kTileBytes, nv, at);
+            fence_proxy_async_smem();
+          }
+          named_bar_sync(1, kAuxThreads);
+          if (at == 0) mbar_arrive(smem_u32(&bars->v_ready[s]));
         }
-        named_bar_sync(1, 128);
-        if (at == 0) mbar_arrive(smem_u32(&bars->v_ready[s]));
+        kv_cnt += w.n_kv;
       }
+    }
     }
   }
   __syncwarp();
@@ -658,6 +761,8 @@ cudaError_t launch_mode(const AttnArgs& a) {
   p.Sq = a.Sq;
   p.Skv = a.Skv;
   p.H = a.H;
+  p.n_pairs = (a.Sq + 255) / 256;
+  p.n_items = a.B * a.H * p.n_pairs;
   p.q_valid = a.q_valid;
   p.kv_valid = a.kv_valid;
   p.kv_valid_dev = a.kv_valid_dev;
@@ -671,7 +776,14 @@ cudaError_t launch_mode(const AttnArgs& a) {
   auto kern = attn_fwd_kernel<D, kMode>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmemBytes);
   if (e != cudaSuccess) return e;
-  dim3 grid((a.Sq + 255) / 256, a.H, a.B);
+  static const int sm_count = [] {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
+      return n;
+    return 148;
+  }();
+  const int grid = p.n_items < sm_count ? p.n_items : sm_count;   // persistent: one CTA per SM
   kern<<<grid, kThreads, Cfg<D>::kSmemBytes, a.stream>>>(mq, mk, mv, mcq, msq, mck, msk, p);
   return cudaGetLastError();
 }
