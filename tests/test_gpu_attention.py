@@ -144,3 +144,44 @@ def test_wan480_full_size_sampled_rows(lib):
     assert np.all(O[:, case.q_valid:] == 0) and np.all(L[:, case.q_valid:] == -np.inf)
     assert np.all(np.isfinite(L[:, :case.q_valid]))
     assert lib.dit_device_status() == 0
+
+
+@pytest.mark.parametrize("D,rope", [(64, "1d"), (128, "1d"), (128, "3d")])
+def test_workspace_rope_path_matches_fused_path_bitwise(lib, D, rope):
+    """dit_attn_fwd_ws rotates each q/k row once into the workspace with the same arithmetic
+    the fused path applies per tile, so the two give the same bits; both match the oracle."""
+    if rope == "3d":
+        case = AttnCase("ws3d", B=2, H=3, D=D, Sq=512, Skv=512, q_valid=495, kv_valid=495,
+                        rope="3d", grid=(3, 5, 33), seed=81)
+    else:
+        case = AttnCase("ws1d", B=2, H=3, D=D, Sq=384, Skv=640, q_valid=300, kv_valid=601,
+                        rope="1d", seed=82 + D, k_pos_offset=900)
+    q, k, v = make_qkv(case)
+    tabs = gpu_tables_self(lib, case)
+    qd, kd, vd = dev_bf16(q), dev_bf16(k), dev_bf16(v)
+    O1, L1 = lib.dit_attn_fwd(qd, kd, vd, case.q_valid, case.kv_valid, *tabs)
+    ws = torch.full((lib.dit_attn_workspace_bytes(case.B, case.Sq, case.Skv, case.H, case.D),), 0xAB,
+                    dtype=torch.uint8, device="cuda")   # stale contents must not matter
+    O2, L2 = lib.dit_attn_fwd_ws(qd, kd, vd, case.q_valid, case.kv_valid, *tabs, workspace=ws)
+    O3, L3 = lib.dit_attn_fwd_ws(qd, kd, vd, case.q_valid, case.kv_valid, *tabs, workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(O1, O2) and torch.equal(L1, L2)
+    assert torch.equal(O2, O3) and torch.equal(L2, L3)
+    Or, Lr = oracle_self(case, q, k, v)
+    compare(O2.float().cpu().numpy(), L2.cpu().numpy(), Or, Lr, case.q_valid)
+    assert lib.dit_device_status() == 0
+
+
+def test_workspace_rope_path_wan480_sampled(lib):
+    case = wan480_case()
+    q, k, v = make_qkv(case)
+    tabs = gpu_tables_self(lib, case)
+    out, lse = lib.dit_attn_fwd_ws(dev_bf16(q), dev_bf16(k), dev_bf16(v), case.q_valid, case.kv_valid, *tabs)
+    torch.cuda.synchronize()
+    O, L = out.float().cpu().numpy(), lse.cpu().numpy()
+    rows = sample_rows(case.q_valid, case.Sq, 32, seed=17)
+    heads = [3, 22, 38]
+    Or, Lr = oracle_self(case, q, k, v, rows=rows, heads=heads)
+    compare(O, L, Or, Lr, case.q_valid, rows=rows, heads=heads)
+    assert np.all(O[:, case.q_valid:] == 0) and np.all(L[:, case.q_valid:] == -np.inf)
+    assert lib.dit_device_status() == 0

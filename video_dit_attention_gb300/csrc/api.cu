@@ -133,8 +133,33 @@ extern "C" int dit_attn_fwd(const void* q, const void* k, const void* v, int B, 
                         !aligned(sin_k, 16)))
     return DIT_ERR_ALIGNMENT;
   AttnArgs a{q, k, v, B, Sq, Skv, H, D, q_valid_len, kv_valid_len, nullptr,
-             cos_q, sin_q, cos_k, sin_k, softmax_scale, out, lse, static_cast<cudaStream_t>(stream)};
+             cos_q, sin_q, cos_k, sin_k, softmax_scale, out, lse, nullptr,
+             static_cast<cudaStream_t>(stream)};
   return cuda_status(launch_attn_fwd(a, n_tables == 4 ? kModeRope : kModePlain));
+}
+
+extern "C" size_t dit_attn_workspace_bytes(int B, int Sq, int Skv, int H, int D) {
+  if (B < 1 || Sq < 1 || Skv < 1 || H < 1 || (D != 64 && D != 128)) return 0;
+  return attn_workspace_bytes(B, Sq, Skv, H, D);
+}
+
+extern "C" int dit_attn_fwd_ws(const void* q, const void* k, const void* v, int B, int Sq, int Skv,
+                               int H, int D, int q_valid_len, int kv_valid_len, const float* cos_q,
+                               const float* sin_q, const float* cos_k, const float* sin_k,
+                               float softmax_scale, void* out, float* lse, void* workspace,
+                               size_t workspace_bytes, void* stream) {
+  int st = check_attn_shapes(q, k, v, B, Sq, Skv, H, D, q_valid_len, softmax_scale, out, lse);
+  if (st != DIT_OK) return st;
+  if (kv_valid_len < 0 || kv_valid_len > Skv) return DIT_ERR_INVALID_ARG;
+  if (!cos_q || !sin_q || !cos_k || !sin_k || !workspace) return DIT_ERR_INVALID_ARG;
+  if (workspace_bytes < attn_workspace_bytes(B, Sq, Skv, H, D)) return DIT_ERR_INVALID_ARG;
+  if (!aligned(cos_q, 16) || !aligned(sin_q, 16) || !aligned(cos_k, 16) || !aligned(sin_k, 16) ||
+      !aligned(workspace, 256))
+    return DIT_ERR_ALIGNMENT;
+  AttnArgs a{q, k, v, B, Sq, Skv, H, D, q_valid_len, kv_valid_len, nullptr,
+             cos_q, sin_q, cos_k, sin_k, softmax_scale, out, lse, workspace,
+             static_cast<cudaStream_t>(stream)};
+  return cuda_status(launch_attn_fwd(a, kModeRopeWs));
 }
 
 extern "C" int dit_cross_attn_shortkv(const void* q, const void* k, const void* v, int B, int Sq,
@@ -147,7 +172,7 @@ extern "C" int dit_cross_attn_shortkv(const void* q, const void* k, const void* 
   if (Skv > 512) return DIT_ERR_UNSUPPORTED;
   if (!aligned(kv_valid_len_dev, 4)) return DIT_ERR_ALIGNMENT;
   AttnArgs a{q, k, v, B, Sq, Skv, H, D, q_valid_len, Skv, kv_valid_len_dev,
-             nullptr, nullptr, nullptr, nullptr, softmax_scale, out, lse,
+             nullptr, nullptr, nullptr, nullptr, softmax_scale, out, lse, nullptr,
              static_cast<cudaStream_t>(stream)};
   return cuda_status(launch_attn_fwd(a, kModeCross));
 }

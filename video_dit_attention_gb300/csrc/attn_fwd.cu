@@ -107,6 +107,18 @@ struct KParams {
   float* lse;
 };
 
+// Rotation-phase parameters of the workspace mode: raw inputs, their rotated fp16 copies
+// (which the TMA maps of q and k point at) and the grid barrier counter (zeroed before
+// launch). Kept apart from KParams so the other modes' parameter block stays small.
+struct WsParams {
+  const uint16_t* q_raw;
+  const uint16_t* k_raw;
+  uint16_t* q_rot;
+  uint16_t* k_rot;
+  unsigned int* grid_bar;
+  int B;
+};
+
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;
   asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];"
@@ -249,12 +261,44 @@ __device__ __forceinline__ Item decode_item(const KParams& p, int it) {
 // work on neighbouring items of the same heads and share their K/V tiles in L2. Every ring
 // and barrier phase runs on counters that continue across items, so the loads, the rotation
 // and the first MMAs of the next item overlap the epilogue of the current one.
+// Writes the split-halves rotation of rows [0, valid) of x [B, S_rows, H, D] (bf16) as fp16
+// into y (same layout), with table rows [S_rows, D/2]; work items are (row, 8-pair chunk), so
+// consecutive threads read and write consecutive 16-byte chunks.
+template <int D>
+__device__ __forceinline__ void rotate_rows_fp16(const uint16_t* __restrict__ x, uint16_t* __restrict__ y,
+                                                 const float* __restrict__ cos_t,
+                                                 const float* __restrict__ sin_t, int B, int S_rows,
+                                                 int valid, int H, long long gtid, long long gthreads) {
+  constexpr int kHalf = D / 2, kChunks = kHalf / 8;
+  const long long items = static_cast<long long>(B) * valid * H * kChunks;
+  for (long long it = gtid; it < items; it += gthreads) {
+    const int ch = static_cast<int>(it % kChunks);
+    long long rest = it / kChunks;
+    const int h = static_cast<int>(rest % H);
+    rest /= H;
+    const int srow = static_cast<int>(rest % valid);
+    const int b = static_cast<int>(rest / valid);
+    const long long row = (static_cast<long long>(b) * S_rows + srow) * H + h;
+    const uint16_t* xr = x + row * D + ch * 8;
+    uint4 a = *reinterpret_cast<const uint4*>(xr);
+    uint4 bb = *reinterpret_cast<const uint4*>(xr + kHalf);
+    const float* ct = cos_t + static_cast<long long>(srow) * kHalf + ch * 8;
+    const float* st = sin_t + static_cast<long long>(srow) * kHalf + ch * 8;
+    rotate8(a, bb, __ldg(reinterpret_cast<const float4*>(ct)), __ldg(reinterpret_cast<const float4*>(ct + 4)),
+            __ldg(reinterpret_cast<const float4*>(st)), __ldg(reinterpret_cast<const float4*>(st + 4)));
+    uint16_t* yr = y + row * D + ch * 8;
+    *reinterpret_cast<uint4*>(yr) = a;
+    *reinterpret_cast<uint4*>(yr + kHalf) = bb;
+  }
+}
+
 template <int D, int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_cq,
                     const __grid_constant__ CUtensorMap tm_sq, const __grid_constant__ CUtensorMap tm_ck,
-                    const __grid_constant__ CUtensorMap tm_sk, const KParams p) {
+                    const __grid_constant__ CUtensorMap tm_sk, const KParams p,
+                    const WsParams ws) {
   using C = Cfg<D>;
   constexpr int NSK = C::kStagesK, NSV = C::kStagesV;
   extern __shared__ uint8_t smem_raw[];
@@ -318,8 +362,40 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tbase = bars->tmem_base;
+  if (kMode == kModeRopeWs) {
+    // ---------------------------------------------------------- phase 1: rotate q and k once
+    // Every q and k row is rotated exactly once (all CTAs, all threads), stored as fp16, and
+    // the attention below reads the rotated copies through its q/k TMA maps.
+    const long long gtid = static_cast<long long>(blockIdx.x) * kThreads + tid;
+    const long long gthreads = static_cast<long long>(gridDim.x) * kThreads;
+    rotate_rows_fp16<D>(ws.q_raw, ws.q_rot, p.cos_q, p.sin_q, ws.B, p.Sq, p.q_valid, p.H, gtid, gthreads);
+    int kv_max = p.kv_valid;
+    rotate_rows_fp16<D>(ws.k_raw, ws.k_rot, p.cos_k, p.sin_k, ws.B, p.Skv, kv_max, p.H, gtid, gthreads);
+    // Grid-wide barrier (the launch is cooperative, so every CTA is resident): the stores
+    // above must be visible, also to the async proxy, before any CTA's TMA reads them.
+    fence_proxy_async_all();
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+      atomicAdd(ws.grid_bar, 1u);
+      const uint64_t t0 = globaltimer_ns();
+      while (atomicAdd(ws.grid_bar, 0u) < gridDim.x) {
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+          bars->abort = 1;
+          atomicOr(status, kStatusTimeoutGrid);
+          break;
+        }
+        __nanosleep(256);
+      }
+      __threadfence();
+    }
+    __syncthreads();
+    fence_proxy_async_all();
+  }
   const int it0 = blockIdx.x, it_step = gridDim.x;
 
+  // After a failed grid barrier no CTA touches the (possibly incomplete) rotated copies.
+  if (!(kMode == kModeRopeWs && *abort_flag)) {
   // Register budgets per warpgroup (40 / 200 / 200 / 72) add up to the launch's 512 x 128;
   // each is set at the top of its role's branch so that the role's code is compiled to it.
   // Warpgroup 0 holds the TMA producers, 1 and 2 the softmax, 3 the MMA issuer and the
@@ -564,7 +640,8 @@ __global__ void __launch_bounds__(kThreads, 1)
      if (lane == 0) {
       // ------------------------------------------------------------ MMA issuer
       // S = Q K^T: fp16 operands after the fused rotation, the raw bf16 inputs otherwise.
-      constexpr uint32_t kIdS = idesc_f16kind_f32(128, 128, kMode != kModeRope, false, false);
+      constexpr uint32_t kIdS = idesc_f16kind_f32(128, 128, kMode == kModePlain || kMode == kModeCross,
+                                                  false, false);
       constexpr uint32_t kIdO = idesc_bf16_f32(128, D, false, true);
       int kv_cnt = 0, q_cnt = 0;
       // Per query-tile slot: S tiles issued so far (p_full phases) and items whose O_t has gone
@@ -730,6 +807,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     }
   }
+  }
   __syncwarp();
   tc_fence_before_sync();
   __syncthreads();
@@ -741,11 +819,18 @@ template <int D, int kMode>
 cudaError_t launch_mode(const AttnArgs& a) {
   CUtensorMap mq, mk, mv;
   const int qext = a.q_valid > 0 ? a.q_valid : 1;
+  // Workspace mode: the q/k TMA maps read the rotated fp16 copies (2-byte elements either way).
+  const size_t q_elems = static_cast<size_t>(a.B) * a.Sq * a.H * D;
+  const size_t q_bytes = (q_elems * 2 + 255) / 256 * 256;
+  uint16_t* q_rot = kMode == kModeRopeWs ? static_cast<uint16_t*>(a.workspace) : nullptr;
+  uint16_t* k_rot = kMode == kModeRopeWs ? reinterpret_cast<uint16_t*>(static_cast<char*>(a.workspace) + q_bytes) : nullptr;
+  const void* q_src = kMode == kModeRopeWs ? static_cast<const void*>(q_rot) : a.q;
+  const void* k_src = kMode == kModeRopeWs ? static_cast<const void*>(k_rot) : a.k;
   // Cross-attention reads up to Skv rows and masks per batch on the device; self-attention
   // cuts the key/value extent to the valid length so pad rows are never even loaded.
   const int kvext = (kMode == kModeCross) ? a.Skv : (a.kv_valid > 0 ? a.kv_valid : 1);
-  if (!encode_bshd_map(&mq, a.q, a.B, qext, a.Sq, a.H, D) ||
-      !encode_bshd_map(&mk, a.k, a.B, kvext, a.Skv, a.H, D) ||
+  if (!encode_bshd_map(&mq, q_src, a.B, qext, a.Sq, a.H, D) ||
+      !encode_bshd_map(&mk, k_src, a.B, kvext, a.Skv, a.H, D) ||
       !encode_bshd_map(&mv, a.v, a.B, kvext, a.Skv, a.H, D))
     return cudaErrorInvalidValue;
   // RoPE tables [rows, D/2] fp32, read 32 rows at a time (a copy of the Q map when unused).
@@ -773,6 +858,17 @@ cudaError_t launch_mode(const AttnArgs& a) {
   p.scale_log2 = a.scale * kLog2e;
   p.out = static_cast<uint16_t*>(a.out);
   p.lse = a.lse;
+  WsParams ws;
+  ws.q_raw = static_cast<const uint16_t*>(a.q);
+  ws.k_raw = static_cast<const uint16_t*>(a.k);
+  ws.q_rot = q_rot;
+  ws.k_rot = k_rot;
+  ws.grid_bar = nullptr;
+  ws.B = a.B;
+  if (kMode == kModeRopeWs) {
+    const size_t k_bytes = (static_cast<size_t>(a.B) * a.Skv * a.H * D * 2 + 255) / 256 * 256;
+    ws.grid_bar = reinterpret_cast<unsigned int*>(static_cast<char*>(a.workspace) + q_bytes + k_bytes);
+  }
   auto kern = attn_fwd_kernel<D, kMode>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmemBytes);
   if (e != cudaSuccess) return e;
@@ -784,18 +880,35 @@ cudaError_t launch_mode(const AttnArgs& a) {
     return 148;
   }();
   const int grid = p.n_items < sm_count ? p.n_items : sm_count;   // persistent: one CTA per SM
-  kern<<<grid, kThreads, Cfg<D>::kSmemBytes, a.stream>>>(mq, mk, mv, mcq, msq, mck, msk, p);
-  return cudaGetLastError();
+  if (kMode != kModeRopeWs) {
+    kern<<<grid, kThreads, Cfg<D>::kSmemBytes, a.stream>>>(mq, mk, mv, mcq, msq, mck, msk, p, ws);
+    return cudaGetLastError();
+  }
+  // The rotation phase ends in a grid-wide barrier: launch cooperatively so that every CTA is
+  // resident, after zeroing the barrier counter on the same stream.
+  e = cudaMemsetAsync(ws.grid_bar, 0, sizeof(unsigned int), a.stream);
+  if (e != cudaSuccess) return e;
+  void* args[] = {&mq, &mk, &mv, &mcq, &msq, &mck, &msk, &p, &ws};
+  return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kern), dim3(grid), dim3(kThreads),
+                                     args, Cfg<D>::kSmemBytes, a.stream);
 }
 
 }  // namespace
 
+size_t attn_workspace_bytes(int B, int Sq, int Skv, int H, int D) {
+  const size_t q = (static_cast<size_t>(B) * Sq * H * D * 2 + 255) / 256 * 256;
+  const size_t k = (static_cast<size_t>(B) * Skv * H * D * 2 + 255) / 256 * 256;
+  return q + k + 256;
+}
+
 cudaError_t launch_attn_fwd(const AttnArgs& a, AttnMode mode) {
   if (a.D == 128) {
+    if (mode == kModeRopeWs) return launch_mode<128, kModeRopeWs>(a);
     if (mode == kModeRope) return launch_mode<128, kModeRope>(a);
     if (mode == kModeCross) return launch_mode<128, kModeCross>(a);
     return launch_mode<128, kModePlain>(a);
   }
+  if (mode == kModeRopeWs) return launch_mode<64, kModeRopeWs>(a);
   if (mode == kModeRope) return launch_mode<64, kModeRope>(a);
   if (mode == kModeCross) return launch_mode<64, kModeCross>(a);
   return launch_mode<64, kModePlain>(a);

@@ -24,6 +24,7 @@ struct AttnArgs {
   float scale;
   void* out;
   float* lse;
+  void* workspace;              // RoPE workspace mode: rotated fp16 q/k and a grid barrier
   cudaStream_t stream;
 };
 
@@ -31,7 +32,12 @@ enum AttnMode : int {
   kModePlain = 0,  // no RoPE, one kv length
   kModeRope = 1,   // RoPE fused into the q/k tile load
   kModeCross = 2,  // no RoPE, per-batch kv length read on the device
+  kModeRopeWs = 3, // RoPE applied once per q/k tile into a workspace, then attention on it
 };
+
+// Workspace layout of kModeRopeWs: rotated q [B, Sq, H, D] fp16, rotated k [B, Skv, H, D]
+// fp16, then a 256-byte block holding the grid barrier counter; every part 256-byte aligned.
+size_t attn_workspace_bytes(int B, int Sq, int Skv, int H, int D);
 
 cudaError_t launch_attn_fwd(const AttnArgs& a, AttnMode mode);
 

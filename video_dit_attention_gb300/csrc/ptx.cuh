@@ -21,6 +21,7 @@ enum : unsigned int {
   kStatusTimeoutSoftmax = 1u << 2,// a softmax/epilogue thread gave up waiting for S or O
   kStatusTimeoutRope = 1u << 3,   // a rotation thread gave up waiting for a landed tile
   kStatusTimeoutDrain = 1u << 4,  // cleanup after an abort did not see in-flight work finish
+  kStatusTimeoutGrid = 1u << 5,   // a CTA gave up waiting at the grid-wide barrier
 };
 
 // Upper bound on any single wait, in nanoseconds of %globaltimer. Every wait in
@@ -116,6 +117,12 @@ __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity,
 // async-proxy (TMA / tcgen05.mma) accesses of the same memory.
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Orders this thread's generic-proxy accesses (all state spaces) with its later async-proxy
+// (TMA) accesses; used around data written with plain stores and read back by TMA.
+__device__ __forceinline__ void fence_proxy_async_all() {
+  asm volatile("fence.proxy.async;" ::: "memory");
 }
 
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
