@@ -5,7 +5,7 @@
 
 Workloads (synthetic, seeded; the token grids of the Wan / LTX runs the pages describe):
   wan480  (default) Wan 480x832x9 self-attention: B1 H40 D128, 3x30x52 = 4680 tokens padded
-          to 4736, 3-D split-halves RoPE fused into the kernel, pad keys masked.
+          to 4736, 3-D split-halves RoPE inside the attention launch, pad keys masked.
   wan720  Wan 720p 81-frame self-attention: 21x45x80 = 75,600 tokens padded to 75,648.
   cross   short-KV cross-attention: B2 H40 D128, 4680 (4736) queries x 512 text slots,
           per-batch valid lengths uniform on [1, 512].
@@ -19,7 +19,10 @@ valid tokens (4 * B * H * Lq * Lkv * D per attention) over all ranks. Three dist
 sets rotate between steps, so every step reads inputs that are not L2-resident. `e2e` is the
 same metric through the C-ABI with host buffers: every step copies the unpadded q/k/v from
 pinned host memory, pads them with dit_pad_tokens, runs the attention, unpads O and LSE with
-dit_unpad_tokens and copies them back. `--impl reference` times the fp64 CPU oracle instead,
+dit_unpad_tokens and copies them back. RoPE runs inside the attention launch: by default
+(`--rope ws`) every q/k row is rotated once into a preallocated fp16 workspace before a grid
+barrier, with `--rope fused` each loaded tile is rotated in shared memory instead.
+`--impl reference` times the fp64 CPU oracle instead,
 on the host cores, on a bounded sample of the same workload.
 
 Multi-GPU: `python -m torch.distributed.run --nproc-per-node N bench.py --gpus N`; each rank
@@ -192,24 +195,33 @@ def workload_spec(name):
     raise SystemExit(f"unknown workload {name}")
 
 
-def config_dict(name, spec):
+def config_dict(name, spec, rope_mode="ws"):
     if name == "sharded":
         return {"workload": "sharded-key attention + LSE merge", "B": spec.B, "H": spec.H, "D": spec.D,
                 "queries": spec.Sq, "keys": sum(spec.shard_valid), "shards": list(spec.shard_valid),
                 "rope": "1-D split halves, theta 10000, global key positions",
+                "rope_path": _ROPE_PATH[rope_mode],
                 "l2": "3 rotating input sets of 0.69 GB each (> 129 MB L2)"}
     d = {"workload": {"wan480": "Wan 480x832x9 self-attention", "wan720": "Wan 720p 81-frame self-attention",
                       "tiny": "tiny self-attention", "cross": "short-KV cross-attention"}[name],
          "B": spec.B, "H": spec.H, "D": spec.D, "q_valid": spec.q_valid, "q_padded": spec.Sq,
          "kv_valid": spec.kv_valid, "kv_padded": spec.Skv}
     if spec.rope == "3d":
-        d["rope"] = f"3-D split halves fused, grid {'x'.join(map(str, spec.grid))}, 44/42/42, theta 10000"
+        d["rope"] = f"3-D split halves, grid {'x'.join(map(str, spec.grid))}, 44/42/42, theta 10000"
     elif spec.rope == "1d":
-        d["rope"] = "1-D split halves fused, theta 10000"
+        d["rope"] = "1-D split halves, theta 10000"
     else:
         d["rope"] = "none"
+    if spec.rope in ("1d", "3d"):
+        d["rope_path"] = _ROPE_PATH[rope_mode]
     d["l2"] = "3 rotating input sets, each larger than the 129 MB L2" if name != "tiny" else "tiny: L2-resident"
     return d
+
+
+_ROPE_PATH = {
+    "ws": "in the attention launch: q/k rotated once into an fp16 workspace, grid barrier, attention",
+    "fused": "in the attention launch: q/k tiles rotated in shared memory as they are loaded",
+}
 
 
 def step_flops(name, spec):
@@ -223,12 +235,14 @@ def step_flops(name, spec):
 class GpuWorkload:
     """Device buffers and the launch sequence of one step."""
 
-    def __init__(self, name, spec, seed_offset=0):
+    def __init__(self, name, spec, seed_offset=0, rope_mode="ws"):
         import torch
 
         from video_dit_attention_gb300 import dit_attn as lib
         from video_dit_attention_gb300 import inputs as I
         self.torch, self.lib, self.name, self.spec = torch, lib, name, spec
+        self.rope_mode = rope_mode
+        self.workspace = None
         dev = torch.device("cuda")
         bf = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(torch.bfloat16).to(dev)
         self.sets = []
@@ -254,6 +268,10 @@ class GpuWorkload:
                 lse = torch.empty(tuple(qq.shape[:3]), dtype=torch.float32, device=dev)
                 self.sets.append((qq, kv, po, pl, out, lse))
             self.launches_per_step = len(spec.shard_valid) + 1
+            if rope_mode == "ws":
+                nb = max(lib.dit_attn_workspace_bytes(spec.B, spec.Sq, npad, spec.H, spec.D)
+                         for npad in spec.shard_pad)
+                self.workspace = torch.empty(nb, dtype=torch.uint8, device=dev)
         else:
             spec.seed += seed_offset
             q, k, v = I.make_qkv(spec)
@@ -278,7 +296,19 @@ class GpuWorkload:
                 lse = torch.empty(tuple(qq.shape[:3]), dtype=torch.float32, device=dev)
                 self.sets.append((qq, kk, vv, out, lse))
             self.launches_per_step = 1
+            if rope_mode == "ws" and self.tables[0] is not None:
+                nb = lib.dit_attn_workspace_bytes(spec.B, spec.Sq, spec.Skv, spec.H, spec.D)
+                self.workspace = torch.empty(nb, dtype=torch.uint8, device=dev)
         torch.cuda.synchronize()
+
+    def attn(self, q, k, v, q_valid, kv_valid, tables, out, lse):
+        """One self-attention launch: the two-phase RoPE path (rotation into the preallocated
+        workspace) when a workspace is set, else the path with RoPE fused per tile."""
+        if self.workspace is not None:
+            self.lib.dit_attn_fwd_ws(q, k, v, q_valid, kv_valid, *tables, workspace=self.workspace,
+                                     out=out, lse=lse)
+        else:
+            self.lib.dit_attn_fwd(q, k, v, q_valid, kv_valid, *tables, out=out, lse=lse)
 
     def step(self, i, ev=None):
         """Launches one step on the current stream; ev = (start, end) events around the
@@ -290,8 +320,7 @@ class GpuWorkload:
         if self.name == "sharded":
             qq, kv, po, pl, out, lse = s
             for j, ((k, v), (ck, sk), n) in enumerate(zip(kv, self.tk, spec.shard_valid)):
-                lib.dit_attn_fwd(qq, k, v, spec.q_valid, n, self.tq[0], self.tq[1], ck, sk,
-                                 out=po[j], lse=pl[j])
+                self.attn(qq, k, v, spec.q_valid, n, (self.tq[0], self.tq[1], ck, sk), po[j], pl[j])
             if ev is not None:
                 ev[1].record()
             lib.dit_attn_lse_merge(po, pl, out=out, lse=lse)
@@ -300,7 +329,7 @@ class GpuWorkload:
         if self.name == "cross":
             lib.dit_cross_attn_shortkv(qq, kk, vv, spec.q_valid, self.kv_dev, out=out, lse=lse)
         else:
-            lib.dit_attn_fwd(qq, kk, vv, spec.q_valid, int(spec.kv_valid), *self.tables, out=out, lse=lse)
+            self.attn(qq, kk, vv, spec.q_valid, int(spec.kv_valid), self.tables, out, lse)
         if ev is not None:
             ev[1].record()
 
@@ -358,8 +387,7 @@ class E2E:
         if wl.name == "cross":
             lib.dit_cross_attn_shortkv(self.qp, self.kp, self.vp, sp.q_valid, wl.kv_dev, out=self.out, lse=self.lse)
         else:
-            lib.dit_attn_fwd(self.qp, self.kp, self.vp, sp.q_valid, int(sp.kv_valid), *wl.tables,
-                             out=self.out, lse=self.lse)
+            wl.attn(self.qp, self.kp, self.vp, sp.q_valid, int(sp.kv_valid), wl.tables, self.out, self.lse)
         lib.dit_unpad_tokens(self.out, self.Lq, out=self.o_u)
         lib.dit_unpad_tokens(self.lse, self.Lq, out=self.l_u)
         self.ho.copy_(self.o_u, non_blocking=True)
@@ -466,6 +494,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default="wan480", choices=["wan480", "wan720", "cross", "sharded", "tiny"])
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--rope", default="ws", choices=["ws", "fused"],
+                    help="ws: rotate q/k once per call into a workspace (default); fused: rotate per tile")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
@@ -484,7 +514,7 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     peaks = load_peaks()
-    wl = GpuWorkload(name, spec, seed_offset=rank)
+    wl = GpuWorkload(name, spec, seed_offset=rank, rope_mode=args.rope)
     flops = step_flops(name, spec)
     stream = torch.cuda.current_stream()
 
@@ -548,7 +578,7 @@ def main():
         "metric": METRIC, "value": units / max_el / 1e12, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": max_el / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic", "config": config_dict(name, spec),
+        "data": "synthetic", "config": config_dict(name, spec, args.rope),
         "pct_of_bf16_peak": 100.0 * (units / max_el / 1e12) / (peak * world),
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": profiled_traffic(name),
