@@ -146,6 +146,45 @@ int dit_attn_fwd_ws(const void* q, const void* k, const void* v, int B, int Sq, 
                     size_t workspace_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------------------
+ * dit_attn_fwd_ws without a caller-supplied workspace. The pages have no counterpart: this
+ * is a library convenience, not part of the method.
+ *
+ * Who needs it: callers that cannot hand in device memory at the call site. Examples are a
+ * plain C caller with no allocator of its own, and code inside a framework whose caching
+ * allocator already holds the device memory. There a cudaMalloc can fail for lack of
+ * memory, and a cudaMalloc or cudaFree per call can synchronise the device. This function
+ * allocates nothing and calls no allocating routine.
+ *
+ * Scratch: a fixed array of DIT_ATTN_STATIC_SCRATCH_BYTES (96 MiB) of device memory,
+ * declared in the library at file scope. The CUDA runtime reserves it on each device where
+ * it loads the library's device code. The size fits the Wan 480p self-attention (B1, 4736
+ * query and key rows, H40, D128), which needs 92.5 MiB.
+ *
+ * Set-up: the first call on each device looks up the array's device address with that
+ * device current, once, under a lock. Make that first call outside any stream capture.
+ *
+ * Zero state: nothing in the array has to start at zero. Each call clears the grid-barrier
+ * word on `stream` before its kernel starts, and the rotated q/k copies are written before
+ * they are read.
+ *
+ * Overlap: there is one array per device per process. Two calls in flight on the same
+ * device at the same time share it. That happens with calls on two streams, or from two
+ * host threads with no ordering between them. Such calls race: they overwrite each other's
+ * rotated copies and barrier word, and their results are wrong. Order such calls on one
+ * stream, or use dit_attn_fwd_ws with one workspace per stream.
+ *
+ * Arguments, outputs and numerics are those of dit_attn_fwd_ws; all four tables are
+ * required. Errors: as dit_attn_fwd_ws. DIT_ERR_UNSUPPORTED also when
+ * dit_attn_workspace_bytes(B, Sq, Skv, H, D) > DIT_ATTN_STATIC_SCRATCH_BYTES, or when the
+ * current device's ordinal is 64 or more. DIT_ERR_CUDA if the set-up lookup fails.
+ * ------------------------------------------------------------------------------------- */
+#define DIT_ATTN_STATIC_SCRATCH_BYTES ((size_t)96 << 20)
+int dit_attn_fwd_ws_static(const void* q, const void* k, const void* v, int B, int Sq, int Skv,
+                           int H, int D, int q_valid_len, int kv_valid_len, const float* cos_q,
+                           const float* sin_q, const float* cos_k, const float* sin_k,
+                           float softmax_scale, void* out, float* lse, void* stream);
+
+/* ---------------------------------------------------------------------------------------
  * Short-KV cross-attention (maxdiffusion PR #491: fused short-KV cross-attention of the video
  * queries against the text sequence). As dit_attn_fwd without RoPE, with one valid key
  * length per batch read on the device: kv_valid_len_dev[b] in [0, Skv] (int32, device

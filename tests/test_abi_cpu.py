@@ -137,3 +137,26 @@ def test_status_strings(clib):
     clib.dit_status_string.restype = ctypes.c_char_p
     for code in (0, -1, -2, -3, -4, -5):
         assert clib.dit_status_string(code).startswith(b"DIT_")
+
+
+def test_static_scratch_size_agrees_between_header_and_binding():
+    h = re.search(r"#define DIT_ATTN_STATIC_SCRATCH_BYTES \(\(size_t\)(\d+) << (\d+)\)", open(HEADER).read())
+    src = open(os.path.join(ROOT, "video_dit_attention_gb300", "dit_attn.py")).read()
+    b = re.search(r"^DIT_ATTN_STATIC_SCRATCH_BYTES = (\d+) << (\d+)$", src, re.M)
+    assert h and b and (int(h[1]) << int(h[2])) == (int(b[1]) << int(b[2])) == 96 << 20
+
+
+def test_static_scratch_entry_rejects_oversized_problems_before_any_cuda_call(clib):
+    fn = clib.dit_attn_fwd_ws_static
+    fn.restype = ctypes.c_int
+    fn.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 7 + [ctypes.c_void_p] * 4 + \
+        [ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
+    ws = clib.dit_attn_workspace_bytes
+    ws.restype = ctypes.c_size_t
+    assert ws(1, 4992, 4992, 40, 128) > 96 << 20 >= ws(1, 4736, 4736, 40, 128)
+    assert fn(None, None, None, 1, 4992, 4992, 40, 128, 4992, 4992, None, None, None, None,
+              0.125, None, None, None) == -2            # DIT_ERR_UNSUPPORTED: needs 97.5 MiB
+    assert fn(None, None, None, 0, 128, 128, 1, 128, 1, 1, None, None, None, None,
+              0.125, None, None, None) == -1            # DIT_ERR_INVALID_ARG
+    assert fn(None, None, None, 1, 128, 128, 1, 96, 1, 1, None, None, None, None,
+              0.125, None, None, None) == -2            # head dim not supported

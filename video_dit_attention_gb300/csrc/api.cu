@@ -208,3 +208,44 @@ extern "C" int dit_exp2_fma_eval(const float* x, float* y, long long n, void* st
   if (n == 0) return DIT_OK;
   return cuda_status(launch_exp2_fma(x, y, n, static_cast<cudaStream_t>(stream)));
 }
+
+// dit_attn_fwd_ws with the workspace taken from a fixed device array instead of the caller.
+namespace dit {
+namespace {
+
+__device__ __align__(256) unsigned char g_attn_static_scratch[DIT_ATTN_STATIC_SCRATCH_BYTES];
+
+constexpr int kStaticScratchDevices = 64;
+std::mutex g_static_scratch_mu;
+void* g_static_scratch_ptr[kStaticScratchDevices] = {};
+
+}  // namespace
+}  // namespace dit
+
+extern "C" int dit_attn_fwd_ws_static(const void* q, const void* k, const void* v, int B, int Sq,
+                                      int Skv, int H, int D, int q_valid_len, int kv_valid_len,
+                                      const float* cos_q, const float* sin_q, const float* cos_k,
+                                      const float* sin_k, float softmax_scale, void* out,
+                                      float* lse, void* stream) {
+  if (B < 1 || Sq < 1 || Skv < 1 || H < 1) return DIT_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return DIT_ERR_UNSUPPORTED;
+  if (attn_workspace_bytes(B, Sq, Skv, H, D) > DIT_ATTN_STATIC_SCRATCH_BYTES) return DIT_ERR_UNSUPPORTED;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_status(e);
+  if (dev < 0 || dev >= kStaticScratchDevices) return DIT_ERR_UNSUPPORTED;
+  void* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_static_scratch_mu);
+    if (!g_static_scratch_ptr[dev]) {
+      // Set-up, once per device, with that device current.
+      void* p = nullptr;
+      e = cudaGetSymbolAddress(&p, g_attn_static_scratch);
+      if (e != cudaSuccess) return cuda_status(e);
+      g_static_scratch_ptr[dev] = p;
+    }
+    scratch = g_static_scratch_ptr[dev];
+  }
+  return dit_attn_fwd_ws(q, k, v, B, Sq, Skv, H, D, q_valid_len, kv_valid_len, cos_q, sin_q, cos_k,
+                         sin_k, softmax_scale, out, lse, scratch, DIT_ATTN_STATIC_SCRATCH_BYTES, stream);
+}

@@ -42,6 +42,8 @@ _SIGNATURES = {
     "dit_attn_workspace_bytes": ([_i, _i, _i, _i, _i], ctypes.c_size_t),
     "dit_attn_fwd_ws": ([_vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _f, _vp, _vp,
                          _vp, ctypes.c_size_t, _vp], _i),
+    "dit_attn_fwd_ws_static": ([_vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _f, _vp,
+                                _vp, _vp], _i),
 }
 for _name, (_args, _res) in _SIGNATURES.items():
     _fn = getattr(_lib, _name)
@@ -212,6 +214,39 @@ def dit_attn_fwd_ws(q, k, v, q_valid_len: int, kv_valid_len: int, cos_q, sin_q, 
         _ptr(q), _ptr(k), _ptr(v), B, Sq, Skv, H, D, int(q_valid_len), int(kv_valid_len),
         _ptr(cos_q), _ptr(sin_q), _ptr(cos_k), _ptr(sin_k), scale, _ptr(out), _ptr(lse),
         _ptr(workspace), workspace.numel(), _stream_handle(stream)))
+    return out, lse
+
+
+# Size of the library's fixed device scratch array used by dit_attn_fwd_ws_static.
+DIT_ATTN_STATIC_SCRATCH_BYTES = 96 << 20
+
+
+def dit_attn_fwd_ws_static(q, k, v, q_valid_len: int, kv_valid_len: int, cos_q, sin_q, cos_k, sin_k,
+                           softmax_scale=None, out=None, lse=None, stream=None):
+    """dit_attn_fwd_ws with the workspace taken from the library's fixed 96 MiB device array,
+    so the C call allocates nothing. Calls in flight at the same time on one device share
+    that array and must not overlap; the first call on a device does a one-time set-up."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, torch.bfloat16, 4)
+    B, Sq, H, D = q.shape
+    Skv = k.shape[1]
+    if tuple(k.shape) != (B, Skv, H, D) or v.shape != k.shape:
+        raise ValueError("k and v must be [B, Skv, H, D] matching q")
+    for t, n, rows in ((cos_q, "cos_q", Sq), (sin_q, "sin_q", Sq), (cos_k, "cos_k", Skv), (sin_k, "sin_k", Skv)):
+        _need(t, n, torch.float32, 2)
+        if tuple(t.shape) != (rows, D // 2):
+            raise ValueError(f"{n} must be [{rows}, {D // 2}]")
+    need = dit_attn_workspace_bytes(B, Sq, Skv, H, D)
+    if need > DIT_ATTN_STATIC_SCRATCH_BYTES:
+        raise ValueError(f"dit_attn_fwd_ws_static: this problem needs {need} bytes of scratch, more than "
+                         f"the library's fixed {DIT_ATTN_STATIC_SCRATCH_BYTES} bytes; "
+                         f"use dit_attn_fwd_ws with a caller workspace")
+    scale = 1.0 / math.sqrt(D) if softmax_scale is None else float(softmax_scale)
+    out, lse = _attn_outputs(q, out, lse)
+    _check("dit_attn_fwd_ws_static", _lib.dit_attn_fwd_ws_static(
+        _ptr(q), _ptr(k), _ptr(v), B, Sq, Skv, H, D, int(q_valid_len), int(kv_valid_len),
+        _ptr(cos_q), _ptr(sin_q), _ptr(cos_k), _ptr(sin_k), scale, _ptr(out), _ptr(lse),
+        _stream_handle(stream)))
     return out, lse
 
 
