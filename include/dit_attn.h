@@ -112,8 +112,9 @@ int dit_rope_split_halves(const void* x, void* y, const float* cos_tab, const fl
  *
  * q: [B, Sq, H, D]; k, v: [B, Skv, H, D]; out: [B, Sq, H, D] (bf16); lse: [B, Sq, H] fp32.
  * cos_q/sin_q: [Sq, D/2], cos_k/sin_k: [Skv, D/2] fp32 device tables; all four NULL = no
- * RoPE (all four or none must be given). q~ and k~ are rounded to bf16 before the tensor-
- * core products; P is rounded to bf16 before P.V; accumulation and softmax are fp32.
+ * RoPE (all four or none must be given). With RoPE, q~ and k~ are computed in fp32 and
+ * rounded to fp16 (saturating) for the tensor-core product; without it q and k enter as
+ * their bf16 values. P is rounded to bf16 before P.V; accumulation and softmax are fp32.
  * Constraints: Sq, Skv multiples of 128; D in {64, 128}; 0 <= q_valid_len <= Sq;
  * 0 <= kv_valid_len <= Skv; softmax_scale > 0 and finite (callers normally pass 1/sqrt(D)).
  * Errors: DIT_ERR_INVALID_ARG, DIT_ERR_UNSUPPORTED, DIT_ERR_ALIGNMENT (q, k, v, out, tables
