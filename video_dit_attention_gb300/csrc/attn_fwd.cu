@@ -1,5 +1,8 @@
 // Flash-attention forward for sm_103a on tcgen05 tensor cores, with exact pad-key masking,
 // natural-log LSE output and (optionally) split-halves RoPE fused into the q/k tile load.
+// This file holds the kernel for RoPE applied per loaded tile (P kept in TMEM); the plain,
+// cross-attention and workspace-RoPE modes run attn_sp_kernel (attn_sp.cuh, P staged in
+// shared memory), which shares the helpers, work items and parameters defined here.
 //
 // What it computes (Difflet PR #153: pad keys dropped exactly, pad rows rotated by the
 // identity; maxdiffusion PR #491: the real KV length as the ragged tail; mstar PR #376: the
@@ -142,13 +145,15 @@ __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatil
   return ok != 0;
 }
 
-// Bounded wait taken by one thread of the auxiliary group (warps 13-15) and broadcast to
-// the group through shared memory and named barrier 1 (all of its threads call this).
+// Bounded wait taken by one thread of an auxiliary group of NT threads (warps 13-15 by
+// default) and broadcast to the group through shared memory and named barrier 1 (all of its
+// threads call this).
+template <int NT = kAuxThreads>
 __device__ __forceinline__ bool group_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                            unsigned int* status, unsigned int code,
                                            volatile int* go, int at) {
   if (at == 0) *go = bounded_wait(bar, parity, abort_flag, status, code) ? 1 : 0;
-  named_bar_sync(1, kAuxThreads);
+  named_bar_sync(1, NT);
   return *go != 0;
 }
 
@@ -204,13 +209,13 @@ struct Rotator {
   }
 };
 
-// Zeroes rows [first_row, 128) of a landed [128 x D] V tile (all sub-tiles).
-template <int D>
+// Zeroes rows [first_row, 128) of a landed [128 x D] V tile (all sub-tiles), with NT threads.
+template <int D, int NT = kAuxThreads>
 __device__ __forceinline__ void zero_rows(uint32_t tile, int first_row, int at) {
   constexpr int kSub = D / 64;
   const int nrows = 128 - first_row;
   const int nchunks = nrows * 8 * kSub;
-  for (int i = at; i < nchunks; i += kAuxThreads) {
+  for (int i = at; i < nchunks; i += NT) {
     const int sub = i / (nrows * 8);
     const int rem = i % (nrows * 8);
     const int row = first_row + rem / 8;
@@ -291,6 +296,8 @@ __device__ __forceinline__ void rotate_rows_fp16(const uint16_t* __restrict__ x,
     *reinterpret_cast<uint4*>(yr + kHalf) = bb;
   }
 }
+
+#include "attn_sp.cuh"
 
 template <int D, int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -869,9 +876,6 @@ cudaError_t launch_mode(const AttnArgs& a) {
     const size_t k_bytes = (static_cast<size_t>(a.B) * a.Skv * a.H * D * 2 + 255) / 256 * 256;
     ws.grid_bar = reinterpret_cast<unsigned int*>(static_cast<char*>(a.workspace) + q_bytes + k_bytes);
   }
-  auto kern = attn_fwd_kernel<D, kMode>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmemBytes);
-  if (e != cudaSuccess) return e;
   static const int sm_count = [] {
     int dev = 0, n = 0;
     if (cudaGetDevice(&dev) == cudaSuccess &&
@@ -880,17 +884,29 @@ cudaError_t launch_mode(const AttnArgs& a) {
     return 148;
   }();
   const int grid = p.n_items < sm_count ? p.n_items : sm_count;   // persistent: one CTA per SM
-  if (kMode != kModeRopeWs) {
+  if constexpr (kMode == kModeRope) {
+    // Per-tile RoPE needs shared memory for its table ring, so it keeps P in TMEM.
+    auto kern = attn_fwd_kernel<D, kMode>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmemBytes);
+    if (e != cudaSuccess) return e;
     kern<<<grid, kThreads, Cfg<D>::kSmemBytes, a.stream>>>(mq, mk, mv, mcq, msq, mck, msk, p, ws);
     return cudaGetLastError();
+  } else {
+    auto kern = attn_sp_kernel<D, kMode>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, CfgSp<D>::kSmemBytes);
+    if (e != cudaSuccess) return e;
+    if (kMode != kModeRopeWs) {
+      kern<<<grid, kThreads, CfgSp<D>::kSmemBytes, a.stream>>>(mq, mk, mv, p, ws);
+      return cudaGetLastError();
+    }
+    // The rotation phase ends in a grid-wide barrier: launch cooperatively so that every CTA
+    // is resident, after zeroing the barrier counter on the same stream.
+    e = cudaMemsetAsync(ws.grid_bar, 0, sizeof(unsigned int), a.stream);
+    if (e != cudaSuccess) return e;
+    void* args[] = {&mq, &mk, &mv, &p, &ws};
+    return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kern), dim3(grid), dim3(kThreads),
+                                       args, CfgSp<D>::kSmemBytes, a.stream);
   }
-  // The rotation phase ends in a grid-wide barrier: launch cooperatively so that every CTA is
-  // resident, after zeroing the barrier counter on the same stream.
-  e = cudaMemsetAsync(ws.grid_bar, 0, sizeof(unsigned int), a.stream);
-  if (e != cudaSuccess) return e;
-  void* args[] = {&mq, &mk, &mv, &mcq, &msq, &mck, &msk, &p, &ws};
-  return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kern), dim3(grid), dim3(kThreads),
-                                     args, Cfg<D>::kSmemBytes, a.stream);
 }
 
 }  // namespace

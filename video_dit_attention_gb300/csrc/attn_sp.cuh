@@ -1,0 +1,506 @@
+// Attention kernel with P staged in shared memory: the plain, cross-attention and
+// workspace-RoPE modes. Included by attn_fwd.cu inside its namespace, after the helpers it
+// uses (KParams, WsParams, Item, decode_item, write_empty_tile, zero_rows,
+// rotate_rows_fp16, warp_wait, group_wait, sts128).
+//
+// Same mathematics, work items, persistence and warp roles as attn_fwd_kernel. What changes
+// is where P lives. There, P_t,j is written as bf16 over S_t,j in TMEM, so S_t,j+1 can only
+// be computed after P_t,j V_j has read P_t,j. Each query tile then runs a serial chain per
+// key tile: softmax, then the PV product, then the next S product. Here each softmax thread
+// writes its P row into shared memory (128-byte swizzle, the K-major A operand of an SS
+// MMA). As soon as the softmax has loaded S_t,j into registers it releases the TMEM columns
+// (s_free), and S_t,j+1 is computed while the softmax is still exponentiating; a softmax
+// only waits for work that was issued a full step earlier.
+// The MMAs come from two threads: warp 12 issues every S_t = Q_t K_j^T, warp 13 every
+// O_t += P_t V_j. A single issuing thread spends about 60 cycles per tcgen05.mma plus its
+// commits and barrier polls, close to the 64 cycles a 128 x 128 x 16 product takes, and left
+// the tensor core idle between groups; two issuers overlap that cost. They touch disjoint
+// TMEM columns and every commit covers only its own thread's MMAs, so they need no ordering
+// between them beyond the barriers below. Cross-attention zeroes V pad rows in warps 14-15.
+// Synchronisation per query-tile slot t (all waits bounded):
+//   s_full[t]  S_t,j computed (commit)          -> softmax t
+//   s_free[t]  S_t,j loaded into registers       -> issuer may overwrite S_t (4 warp arrivals)
+//   p_full[t]  P_t,j stored in shared memory     -> issuer may run P_t,j V_j (128 arrivals)
+//   pv_done[t] P_t,j V_j complete (commit)       -> softmax may rescale O_t / overwrite P_t;
+//                                                    the epilogue may read O_t
+//   o_free[t]  O_t read out by the epilogue      -> the next item's first PV may overwrite it
+// Shared memory at D = 128: Q0, Q1 (64 KB), two K stages (64 KB), one V stage (32 KB),
+// P0, P1 (64 KB). K is loaded one step ahead of V (S_j+1 is issued before P_j V_j), by its
+// own producer thread, so a K load never waits behind a V stage.
+
+template <int D>
+struct CfgSp {
+  static constexpr int kSub = D / 64;
+  static constexpr int kTileBytes = 128 * D * 2;
+  static constexpr int kStagesK = (D == 128) ? 2 : 4;
+  static constexpr int kStagesV = (D == 128) ? 1 : 2;
+  static constexpr int kPBytes = 128 * 128 * 2;           // P tile: 128 query rows x 128 keys
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffK = kOffQ + 2 * kTileBytes;
+  static constexpr int kOffV = kOffK + kStagesK * kTileBytes;
+  static constexpr int kOffP = kOffV + kStagesV * kTileBytes;
+  static constexpr int kOffBar = kOffP + 2 * kPBytes;
+  static constexpr int kSmemBytes = kOffBar + 512 + 1024;  // barriers + alignment slack
+};
+
+struct BarsSp {
+  uint64_t q_full, q_empty;
+  uint64_t k_full[4], k_empty[4];
+  uint64_t v_full[2], v_ready[2], v_empty[2];
+  uint64_t s_full[2], s_free[2], p_full[2], pv_done[2], o_free[2];
+  uint64_t drain[2];
+  uint32_t tmem_base;
+  int abort;
+  int aux_go;
+};
+
+template <int D, int kMode>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_sp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const KParams p, const WsParams ws) {
+  static_assert(kMode == kModePlain || kMode == kModeCross || kMode == kModeRopeWs, "mode");
+  using C = CfgSp<D>;
+  constexpr int NSK = C::kStagesK, NSV = C::kStagesV;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t s_base = smem_u32(smem);
+  const uint32_t sQ = s_base + C::kOffQ;
+  const uint32_t sK0 = s_base + C::kOffK;
+  const uint32_t sV0 = s_base + C::kOffV;
+  const uint32_t sP = s_base + C::kOffP;
+  BarsSp* bars = reinterpret_cast<BarsSp*>(smem + C::kOffBar);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  volatile int* abort_flag = &bars->abort;
+  unsigned int* status = &g_dit_status;
+  const uint32_t b_q_full = smem_u32(&bars->q_full), b_q_empty = smem_u32(&bars->q_empty);
+
+  if (tid == 0) {
+    bars->abort = 0;
+    mbar_init(b_q_full, 1);
+    mbar_init(b_q_empty, 1);
+    for (int s = 0; s < NSK; ++s) {
+      mbar_init(smem_u32(&bars->k_full[s]), 1);
+      mbar_init(smem_u32(&bars->k_empty[s]), 1);
+    }
+    for (int s = 0; s < NSV; ++s) {
+      mbar_init(smem_u32(&bars->v_full[s]), 1);
+      mbar_init(smem_u32(&bars->v_ready[s]), 1);
+      mbar_init(smem_u32(&bars->v_empty[s]), 1);
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(smem_u32(&bars->s_full[t]), 1);
+      mbar_init(smem_u32(&bars->s_free[t]), 4);
+      mbar_init(smem_u32(&bars->p_full[t]), 128);
+      mbar_init(smem_u32(&bars->pv_done[t]), 1);
+      mbar_init(smem_u32(&bars->o_free[t]), 128);
+    }
+    mbar_init(smem_u32(&bars->drain[0]), 1);
+    mbar_init(smem_u32(&bars->drain[1]), 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(&bars->tmem_base), 512);
+    tmem_relinquish();
+  }
+  if (tid == 32) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tbase = bars->tmem_base;
+  if (kMode == kModeRopeWs) {
+    // ---------------------------------------------------------- phase 1: rotate q and k once
+    const long long gtid = static_cast<long long>(blockIdx.x) * kThreads + tid;
+    const long long gthreads = static_cast<long long>(gridDim.x) * kThreads;
+    rotate_rows_fp16<D>(ws.q_raw, ws.q_rot, p.cos_q, p.sin_q, ws.B, p.Sq, p.q_valid, p.H, gtid, gthreads);
+    rotate_rows_fp16<D>(ws.k_raw, ws.k_rot, p.cos_k, p.sin_k, ws.B, p.Skv, p.kv_valid, p.H, gtid, gthreads);
+    // Grid-wide barrier (cooperative launch: every CTA is resident). The rotated rows must be
+    // visible, also to the async proxy, before any CTA's TMA reads them.
+    fence_proxy_async_all();
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) {
+      atomicAdd(ws.grid_bar, 1u);
+      const uint64_t t0 = globaltimer_ns();
+      while (atomicAdd(ws.grid_bar, 0u) < gridDim.x) {
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+          bars->abort = 1;
+          atomicOr(status, kStatusTimeoutGrid);
+          break;
+        }
+        __nanosleep(256);
+      }
+      __threadfence();
+    }
+    __syncthreads();
+    fence_proxy_async_all();
+  }
+  const int it0 = blockIdx.x, it_step = gridDim.x;
+
+  // Two MMA issuers, one thread each: S products (warp 12) and PV products (warp 13). They
+  // share no TMEM columns and each commit covers only the issuing thread's own MMAs, so they
+  // need no ordering between them; two issuers keep the tensor core fed where one thread's
+  // per-instruction issue cost (plus commits and waits) would leave it idle between groups.
+  auto wait_bar = [&](uint32_t bar, int phase) -> bool {
+    if (!bounded_wait(bar, phase & 1, abort_flag, status, kStatusTimeoutMma)) return false;
+    tc_fence_after_sync();
+    return true;
+  };
+  auto s_issuer = [&]() {
+    // ------------------------------------------------------------ S_t = Q_t K_g^T
+    constexpr uint32_t kIdS = idesc_f16kind_f32(128, 128, kMode != kModeRopeWs, false, false);
+    int g0 = 0, q_cnt = 0, ns0 = 0, ns1 = 0;
+    bool ok = true;
+    for (int it = it0; ok && it < p.n_items; it += it_step) {
+      const Item w = decode_item<kMode>(p, it);
+      if (w.n_live == 0) continue;
+      if (!(ok = wait_bar(b_q_full, q_cnt))) break;
+      for (int j = 0; ok && j < w.n_kv; ++j) {
+        const int g = g0 + j;
+        if (!(ok = wait_bar(smem_u32(&bars->k_full[g % NSK]), g / NSK))) break;
+        const uint64_t db = smem_desc_sw128(sK0 + (g % NSK) * C::kTileBytes, 16, 1024);
+        for (int t = 0; t < w.n_live; ++t) {
+          // S_t may be overwritten once the softmax has taken the previous S_t out of TMEM.
+          const int ns = t ? ns1 : ns0;
+          if (ns > 0 && !(ok = wait_bar(smem_u32(&bars->s_free[t]), ns - 1))) break;
+          const uint64_t da = smem_desc_sw128(sQ + t * C::kTileBytes, 16, 1024);
+          const uint32_t d = tbase + t * 128;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint64_t off = ((kk / 4) * 16384 + (kk % 4) * 32) >> 4;
+            mma_bf16_ss(d, da + off, db + off, kIdS, kk > 0);
+          }
+          mma_commit(smem_u32(&bars->s_full[t]));
+          if (t) ++ns1; else ++ns0;
+        }
+        if (!ok) break;
+        mma_commit(smem_u32(&bars->k_empty[g % NSK]));
+      }
+      if (!ok) break;
+      mma_commit(b_q_empty);   // every S product of the item is issued: Q may be reloaded
+      g0 += w.n_kv;
+      ++q_cnt;
+    }
+    if (*abort_flag) {
+      // Wait for every MMA this thread issued before TMEM and shared memory are released.
+      mma_commit(smem_u32(&bars->drain[0]));
+      drain_wait(smem_u32(&bars->drain[0]), 0, status);
+    }
+  };
+  auto pv_issuer = [&]() {
+    // ------------------------------------------------------------ O_t (+)= P_t V_g
+    constexpr uint32_t kIdO = idesc_bf16_f32(128, D, false, true);
+    int g0 = 0, np0 = 0, np1 = 0, epi0 = 0, epi1 = 0;
+    bool ok = true;
+    for (int it = it0; ok && it < p.n_items; it += it_step) {
+      const Item w = decode_item<kMode>(p, it);
+      if (w.n_live == 0) continue;
+      for (int j = 0; ok && j < w.n_kv; ++j) {
+        const int g = g0 + j, sv = g % NSV;
+        if (!(ok = wait_bar(kMode == kModeCross ? smem_u32(&bars->v_ready[sv]) : smem_u32(&bars->v_full[sv]),
+                            g / NSV)))
+          break;
+        const uint64_t db = smem_desc_sw128(sV0 + sv * C::kTileBytes, 16384, 1024);
+        for (int t = 0; t < w.n_live; ++t) {
+          const int np = t ? np1 : np0, epi = t ? epi1 : epi0;
+          if (!(ok = wait_bar(smem_u32(&bars->p_full[t]), np))) break;
+          // The first key tile of an item overwrites O_t, once the epilogue of the slot's
+          // previous item has read it.
+          if (j == 0 && epi > 0 && !(ok = wait_bar(smem_u32(&bars->o_free[t]), epi - 1))) break;
+          const uint64_t da = smem_desc_sw128(sP + t * C::kPBytes, 16, 1024);
+          const uint32_t d = tbase + 256 + t * 128;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint64_t offa = ((kk / 4) * 16384 + (kk % 4) * 32) >> 4;
+            mma_bf16_ss(d, da + offa, db + static_cast<uint64_t>(kk * 2048 >> 4), kIdO,
+                        (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(smem_u32(&bars->pv_done[t]));
+          if (t) ++np1; else ++np0;
+        }
+        if (!ok) break;
+        mma_commit(smem_u32(&bars->v_empty[sv]));
+      }
+      if (!ok) break;
+      ++epi0;
+      if (w.n_live == 2) ++epi1;
+      g0 += w.n_kv;
+    }
+    if (*abort_flag) {
+      mma_commit(smem_u32(&bars->drain[1]));
+      drain_wait(smem_u32(&bars->drain[1]), 0, status);
+    }
+  };
+
+  if (!(kMode == kModeRopeWs && *abort_flag)) {
+  if (warp < 4) {
+    regs_dec<40>();
+    if (warp == 0 && lane == 0) {
+      // ------------------------------------------------------------ producer: Q and K
+      int kv_cnt = 0, q_cnt = 0, k_issued = 0;
+      bool ok = true;
+      for (int it = it0; ok && it < p.n_items; it += it_step) {
+        const Item w = decode_item<kMode>(p, it);
+        if (w.n_live == 0) continue;
+        // The Q buffers are free once every S MMA of the previous item has completed.
+        if (q_cnt > 0 && !(ok = bounded_wait(b_q_empty, (q_cnt - 1) & 1, abort_flag, status,
+                                             kStatusTimeoutLoad)))
+          break;
+        mbar_arrive_expect_tx(b_q_full, w.n_live * C::kTileBytes);
+        for (int t = 0; t < w.n_live; ++t)
+#pragma unroll
+          for (int c = 0; c < C::kSub; ++c)
+            tma_load_4d(sQ + t * C::kTileBytes + c * 16384, &tm_q, b_q_full, c * 64, w.h,
+                        w.q0 + 128 * t, w.b);
+        ++q_cnt;
+        for (int j = 0; j < w.n_kv; ++j) {
+          if (j == (w.n_kv > kPrefetchLead ? w.n_kv - kPrefetchLead : 0)) {
+            // Warm L2 with the next item's Q tiles and first K/V tiles.
+            const int nit = it + it_step;
+            if (nit < p.n_items) {
+              const Item nw = decode_item<kMode>(p, nit);
+              for (int t = 0; t < nw.n_live; ++t)
+#pragma unroll
+                for (int c = 0; c < C::kSub; ++c)
+                  tma_prefetch_l2_4d(&tm_q, c * 64, nw.h, nw.q0 + 128 * t, nw.b);
+              for (int jj = 0; jj < nw.n_kv && jj < kPrefetchKV; ++jj)
+#pragma unroll
+                for (int c = 0; c < C::kSub; ++c) {
+                  tma_prefetch_l2_4d(&tm_k, c * 64, nw.h, jj * 128, nw.b);
+                  tma_prefetch_l2_4d(&tm_v, c * 64, nw.h, jj * 128, nw.b);
+                }
+            }
+          }
+          const int g = kv_cnt + j, s = g % NSK, u = g / NSK;
+          if (u > 0 && !(ok = bounded_wait(smem_u32(&bars->k_empty[s]), (u - 1) & 1, abort_flag,
+                                           status, kStatusTimeoutLoad)))
+            break;
+          const uint32_t kf = smem_u32(&bars->k_full[s]);
+          mbar_arrive_expect_tx(kf, C::kTileBytes);
+#pragma unroll
+          for (int c = 0; c < C::kSub; ++c)
+            tma_load_4d(sK0 + s * C::kTileBytes + c * 16384, &tm_k, kf, c * 64, w.h, j * 128, w.b);
+          ++k_issued;
+        }
+        kv_cnt += w.n_kv;
+      }
+      if (*abort_flag) {
+        // Let the copies still in flight land before the CTA releases its shared memory.
+        if (q_cnt > 0) drain_wait(b_q_full, (q_cnt - 1) & 1, status);
+        for (int g = k_issued - NSK > 0 ? k_issued - NSK : 0; g < k_issued; ++g)
+          drain_wait(smem_u32(&bars->k_full[g % NSK]), (g / NSK) & 1, status);
+      }
+    } else if (warp == 2 && lane == 0) {
+      // ------------------------------------------------------------ producer: V
+      int v_cnt = 0, v_issued = 0;
+      bool ok = true;
+      for (int it = it0; ok && it < p.n_items; it += it_step) {
+        const Item w = decode_item<kMode>(p, it);
+        if (w.n_live == 0) continue;
+        for (int j = 0; j < w.n_kv; ++j) {
+          const int g = v_cnt + j, s = g % NSV, u = g / NSV;
+          if (u > 0 && !(ok = bounded_wait(smem_u32(&bars->v_empty[s]), (u - 1) & 1, abort_flag,
+                                           status, kStatusTimeoutLoad)))
+            break;
+          const uint32_t vf = smem_u32(&bars->v_full[s]);
+          mbar_arrive_expect_tx(vf, C::kTileBytes);
+#pragma unroll
+          for (int c = 0; c < C::kSub; ++c)
+            tma_load_4d(sV0 + s * C::kTileBytes + c * 16384, &tm_v, vf, c * 64, w.h, j * 128, w.b);
+          ++v_issued;
+        }
+        v_cnt += w.n_kv;
+      }
+      if (*abort_flag) {
+        for (int g = v_issued - NSV > 0 ? v_issued - NSV : 0; g < v_issued; ++g)
+          drain_wait(smem_u32(&bars->v_full[g % NSV]), (g / NSV) & 1, status);
+      }
+    }
+  } else if (warp < 12) {
+    regs_inc<200>();
+    // -------------------------------------------------------------- softmax + epilogue
+    const int t = (warp - 4) >> 2;                   // query-tile slot of this warpgroup
+    const int r = (tid - 128) & 127;                 // row within the tile = TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tS = tbase + lane_off + t * 128;
+    const uint32_t tO = tbase + lane_off + 256 + t * 128;
+    // This thread's P row: 16-byte unit x of 64-key chunk c sits at c * 16384 + r * 128 +
+    // ((x ^ (r & 7)) * 16), the 128-byte swizzle the MMA's K-major descriptor reads.
+    const uint32_t p_row = sP + t * C::kPBytes + r * 128;
+    const uint32_t p_sw = static_cast<uint32_t>(r & 7);
+    const uint32_t b_s_full = smem_u32(&bars->s_full[t]), b_s_free = smem_u32(&bars->s_free[t]);
+    const uint32_t b_p_full = smem_u32(&bars->p_full[t]), b_pv_done = smem_u32(&bars->pv_done[t]);
+    const float sl2 = p.scale_log2;
+    int sc = 0;   // S_t tiles consumed so far (= P_t tiles produced = PV_t products issued)
+    bool ok = true;
+    for (int it = it0; ok && it < p.n_items; it += it_step) {
+      const Item w = decode_item<kMode>(p, it);
+      if (t >= w.n_live) {
+        if (t == 0 || w.has1) write_empty_tile<D>(p, w.b, w.h, w.q0 + 128 * t, r, 128);
+        continue;
+      }
+      const int n_kv = w.n_kv, kv_valid = w.kv_valid;
+      float m_used = -INFINITY, l = 0.f;
+      for (int j = 0; j < n_kv; ++j, ++sc) {
+        if (!warp_wait(b_s_full, sc & 1, abort_flag, status, kStatusTimeoutSoftmax)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        uint32_t sr[4][32];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32_nowait(tS + c * 32, sr[c]);
+        tmem_ld_wait_tied(sr[0]);
+        tmem_reg_tie(sr[1]);
+        tmem_reg_tie(sr[2]);
+        tmem_reg_tie(sr[3]);
+        // S_t is in registers: the issuer may compute S_t,j+1 into the same columns.
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(b_s_free);
+        const int nv = min(128, kv_valid - j * 128);   // valid keys in this tile (>= 1)
+        if (nv < 128) {
+#pragma unroll
+          for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (c * 32 + i >= nv) sr[c][i] = 0xff800000u;
+        }
+        float mx4[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          mx4[c] = fmaxf(__uint_as_float(sr[c][0]), __uint_as_float(sr[c][1]));
+#pragma unroll
+          for (int i = 2; i < 32; i += 2)
+            mx4[c] = fmax3(mx4[c], __uint_as_float(sr[c][i]), __uint_as_float(sr[c][i + 1]));
+        }
+        const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+        const float mt = mx * sl2;
+        const bool resc = mt > m_used + kRescaleThreshold;
+        const float m_new = resc ? mt : m_used;
+        const float alpha = ex2_approx(m_used - m_new);   // 1 if kept; 0 on the first tile
+        if (j > 0) {
+          // P_t,j-1 V_j-1 must be complete before O_t is rescaled and before P_t is rewritten.
+          if (!warp_wait(b_pv_done, (sc - 1) & 1, abort_flag, status, kStatusTimeoutSoftmax)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          if (__any_sync(0xffffffffu, resc)) {
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) {
+              uint32_t orr[32];
+              tmem_ld32(tO + c * 32, orr);
+#pragma unroll
+              for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
+              tmem_st32(tO + c * 32, orr);
+            }
+          }
+        }
+        m_used = m_new;
+        const float neg_m = -m_used;
+        float l4[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) l4[k] = 0.f;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {           // 16 keys at a time: two 16-byte units
+          uint32_t pk[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            float x0, x1;
+            fma2_bc(x0, x1, __uint_as_float(sr[c >> 1][(c & 1) * 16 + 2 * i]),
+                    __uint_as_float(sr[c >> 1][(c & 1) * 16 + 2 * i + 1]), sl2, neg_m);
+            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+            add2(l4[2 * (i & 1)], l4[2 * (i & 1) + 1], p0, p1);
+            pk[i] = pack_bf16x2(p0, p1);
+          }
+          const uint32_t chunk = static_cast<uint32_t>(c >> 2) * 16384u;
+          const uint32_t x0 = static_cast<uint32_t>((2 * c) & 7), x1 = static_cast<uint32_t>((2 * c + 1) & 7);
+          sts128(p_row + chunk + ((x0 ^ p_sw) << 4), make_uint4(pk[0], pk[1], pk[2], pk[3]));
+          sts128(p_row + chunk + ((x1 ^ p_sw) << 4), make_uint4(pk[4], pk[5], pk[6], pk[7]));
+        }
+        l = l * alpha + ((l4[0] + l4[1]) + (l4[2] + l4[3]));
+        fence_proxy_async_smem();   // P (generic stores) before the MMA's async-proxy reads
+        tc_fence_before_sync();     // and the O rescale (tcgen05.st) before the next PV
+        mbar_arrive(b_p_full);
+      }
+      if (!ok) break;
+      // Epilogue: wait for the last P_t V of this item, read O_t, normalise, store.
+      if (!warp_wait(b_pv_done, (sc - 1) & 1, abort_flag, status, kStatusTimeoutSoftmax)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after_sync();
+      const int qrow = w.q0 + 128 * t + r;
+      const bool valid_row = qrow < p.q_valid;
+      const float inv_l = 1.f / l;
+      uint16_t* dst = p.out + ((static_cast<size_t>(w.b) * p.Sq + qrow) * p.H + w.h) * D;
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t orr[32];
+        tmem_ld32(tO + c * 32, orr);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          uint4 o = make_uint4(0, 0, 0, 0);
+          if (valid_row) {
+            const float* f = reinterpret_cast<const float*>(&orr[8 * q4]);
+            o.x = pack_bf16x2(f[0] * inv_l, f[1] * inv_l);
+            o.y = pack_bf16x2(f[2] * inv_l, f[3] * inv_l);
+            o.z = pack_bf16x2(f[4] * inv_l, f[5] * inv_l);
+            o.w = pack_bf16x2(f[6] * inv_l, f[7] * inv_l);
+          }
+          *reinterpret_cast<uint4*>(dst + c * 32 + q4 * 8) = o;
+        }
+      }
+      tc_fence_before_sync();
+      mbar_arrive(smem_u32(&bars->o_free[t]));
+      p.lse[(static_cast<size_t>(w.b) * p.Sq + qrow) * p.H + w.h] =
+          valid_row ? (m_used + log2f(l)) * kLn2 : -INFINITY;
+    }
+  } else {
+    regs_dec<72>();
+    if (warp == 12) {
+      if (lane == 0) s_issuer();
+    } else if (warp == 13) {
+      if (lane == 0) pv_issuer();
+    } else if (kMode == kModeCross) {
+      // ---------------------------------------------------------- V pad rows (warps 14-15)
+      // K/V tiles are loaded up to Skv rows; rows past the batch's valid length are zeroed so
+      // that 0 * (pad contents) cannot reach O.
+      constexpr int kZeroThreads = 64;
+      const int at = tid - 448;
+      volatile int* go = &bars->aux_go;
+      int v_cnt = 0;
+      bool ok = true;
+      for (int it = it0; ok && it < p.n_items; it += it_step) {
+        const Item w = decode_item<kMode>(p, it);
+        if (w.n_live == 0) continue;
+        for (int j = 0; ok && j < w.n_kv; ++j) {
+          const int gv = v_cnt + j, s = gv % NSV;
+          if (!(ok = group_wait<kZeroThreads>(smem_u32(&bars->v_full[s]), (gv / NSV) & 1, abort_flag,
+                                              status, kStatusTimeoutRope, go, at)))
+            break;
+          const int nv = min(128, w.kv_valid - j * 128);
+          if (nv < 128) {
+            zero_rows<D, kZeroThreads>(sV0 + s * C::kTileBytes, nv, at);
+            fence_proxy_async_smem();
+          }
+          named_bar_sync(1, kZeroThreads);
+          if (at == 0) mbar_arrive(smem_u32(&bars->v_ready[s]));
+        }
+        v_cnt += w.n_kv;
+      }
+    }
+  }
+  }
+  __syncwarp();
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  if (warp == 1) tmem_dealloc(tbase, 512);
+}
