@@ -24,29 +24,26 @@
 //   pv_done[t] P_t,j V_j complete (commit)       -> softmax may rescale O_t / overwrite P_t;
 //                                                    the epilogue may read O_t
 //   o_free[t]  O_t read out by the epilogue      -> the next item's first PV may overwrite it
-// Shared memory at D = 128: Q0, Q1 (64 KB), two K stages (64 KB), one V stage (32 KB),
-// P0, P1 (64 KB). K is loaded one step ahead of V (S_j+1 is issued before P_j V_j), by its
-// own producer thread, so a K load never waits behind a V stage.
+// Shared memory at D = 128: Q0, Q1 (64 KB), a ring of three K/V slots (96 KB), P0, P1
+// (64 KB). K and V share the ring, K one tile ahead of V, which gives a K load about two key
+// steps and a V load about one to land (two K and one V stage would leave V a fraction).
 
 template <int D>
 struct CfgSp {
   static constexpr int kSub = D / 64;
   static constexpr int kTileBytes = 128 * D * 2;
-  static constexpr int kStagesK = (D == 128) ? 2 : 4;
-  static constexpr int kStagesV = (D == 128) ? 1 : 2;
+  static constexpr int kRing = (D == 128) ? 3 : 6;        // K/V ring slots
   static constexpr int kPBytes = 128 * 128 * 2;           // P tile: 128 query rows x 128 keys
   static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kOffQ + 2 * kTileBytes;
-  static constexpr int kOffV = kOffK + kStagesK * kTileBytes;
-  static constexpr int kOffP = kOffV + kStagesV * kTileBytes;
+  static constexpr int kOffR = kOffQ + 2 * kTileBytes;
+  static constexpr int kOffP = kOffR + kRing * kTileBytes;
   static constexpr int kOffBar = kOffP + 2 * kPBytes;
   static constexpr int kSmemBytes = kOffBar + 512 + 1024;  // barriers + alignment slack
 };
 
 struct BarsSp {
   uint64_t q_full, q_empty;
-  uint64_t k_full[4], k_empty[4];
-  uint64_t v_full[2], v_ready[2], v_empty[2];
+  uint64_t r_full[6], r_ready[6], r_empty[6];
   uint64_t s_full[2], s_free[2], p_full[2], pv_done[2], o_free[2];
   uint64_t drain[2];
   uint32_t tmem_base;
@@ -54,20 +51,26 @@ struct BarsSp {
   int aux_go;
 };
 
+// The key tiles a CTA visits, flattened over its items: tile g (g = 0 .. G-1) needs K_g for
+// the S products and V_g for the PV products. One ring of shared-memory slots holds both,
+// loaded in the order K_0, K_1, V_0, K_2, V_1, ..., K_G-1, V_G-2, V_G-1 (K one tile ahead of
+// V, as S_g+1 is computed before P_g V_g). Load number n goes to slot n % kRing.
+__device__ __forceinline__ int ring_load_k(int g) { return g == 0 ? 0 : 2 * g - 1; }
+__device__ __forceinline__ int ring_load_v(int g, int G) { return g == G - 1 ? 2 * G - 1 : 2 * g + 2; }
+
 template <int D, int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_sp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const KParams p, const WsParams ws) {
   static_assert(kMode == kModePlain || kMode == kModeCross || kMode == kModeRopeWs, "mode");
   using C = CfgSp<D>;
-  constexpr int NSK = C::kStagesK, NSV = C::kStagesV;
+  constexpr int R = C::kRing;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t s_base = smem_u32(smem);
   const uint32_t sQ = s_base + C::kOffQ;
-  const uint32_t sK0 = s_base + C::kOffK;
-  const uint32_t sV0 = s_base + C::kOffV;
+  const uint32_t sR = s_base + C::kOffR;
   const uint32_t sP = s_base + C::kOffP;
   BarsSp* bars = reinterpret_cast<BarsSp*>(smem + C::kOffBar);
 
@@ -80,14 +83,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     bars->abort = 0;
     mbar_init(b_q_full, 1);
     mbar_init(b_q_empty, 1);
-    for (int s = 0; s < NSK; ++s) {
-      mbar_init(smem_u32(&bars->k_full[s]), 1);
-      mbar_init(smem_u32(&bars->k_empty[s]), 1);
-    }
-    for (int s = 0; s < NSV; ++s) {
-      mbar_init(smem_u32(&bars->v_full[s]), 1);
-      mbar_init(smem_u32(&bars->v_ready[s]), 1);
-      mbar_init(smem_u32(&bars->v_empty[s]), 1);
+    for (int s = 0; s < R; ++s) {
+      mbar_init(smem_u32(&bars->r_full[s]), 1);
+      mbar_init(smem_u32(&bars->r_ready[s]), 1);
+      mbar_init(smem_u32(&bars->r_empty[s]), 1);
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(smem_u32(&bars->s_full[t]), 1);
@@ -141,6 +140,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_proxy_async_all();
   }
   const int it0 = blockIdx.x, it_step = gridDim.x;
+  // First item at or after `it` (in this CTA's sequence) that has work.
+  auto first_live = [&](int it) -> int {
+    while (it < p.n_items && decode_item<kMode>(p, it).n_live == 0) it += it_step;
+    return it;
+  };
+  // G: key tiles over all of this CTA's items.
+  auto count_tiles = [&]() -> int {
+    int G = 0;
+    for (int it = it0; it < p.n_items; it += it_step) {
+      const Item w = decode_item<kMode>(p, it);
+      if (w.n_live > 0) G += w.n_kv;
+    }
+    return G;
+  };
 
   // Two MMA issuers, one thread each: S products (warp 12) and PV products (warp 13). They
   // share no TMEM columns and each commit covers only the issuing thread's own MMAs, so they
@@ -162,8 +175,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!(ok = wait_bar(b_q_full, q_cnt))) break;
       for (int j = 0; ok && j < w.n_kv; ++j) {
         const int g = g0 + j;
-        if (!(ok = wait_bar(smem_u32(&bars->k_full[g % NSK]), g / NSK))) break;
-        const uint64_t db = smem_desc_sw128(sK0 + (g % NSK) * C::kTileBytes, 16, 1024);
+        const int n = ring_load_k(g), slot = n % R;
+        if (!(ok = wait_bar(smem_u32(&bars->r_full[slot]), n / R))) break;
+        const uint64_t db = smem_desc_sw128(sR + slot * C::kTileBytes, 16, 1024);
         for (int t = 0; t < w.n_live; ++t) {
           // S_t may be overwritten once the softmax has taken the previous S_t out of TMEM.
           const int ns = t ? ns1 : ns0;
@@ -179,7 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (t) ++ns1; else ++ns0;
         }
         if (!ok) break;
-        mma_commit(smem_u32(&bars->k_empty[g % NSK]));
+        mma_commit(smem_u32(&bars->r_empty[slot]));
       }
       if (!ok) break;
       mma_commit(b_q_empty);   // every S product of the item is issued: Q may be reloaded
@@ -196,16 +210,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ O_t (+)= P_t V_g
     constexpr uint32_t kIdO = idesc_bf16_f32(128, D, false, true);
     int g0 = 0, np0 = 0, np1 = 0, epi0 = 0, epi1 = 0;
+    const int G = count_tiles();
     bool ok = true;
     for (int it = it0; ok && it < p.n_items; it += it_step) {
       const Item w = decode_item<kMode>(p, it);
       if (w.n_live == 0) continue;
       for (int j = 0; ok && j < w.n_kv; ++j) {
-        const int g = g0 + j, sv = g % NSV;
-        if (!(ok = wait_bar(kMode == kModeCross ? smem_u32(&bars->v_ready[sv]) : smem_u32(&bars->v_full[sv]),
-                            g / NSV)))
+        const int g = g0 + j, n = ring_load_v(g, G), slot = n % R;
+        // Cross-attention: the V tile is used after its pad rows have been zeroed.
+        if (!(ok = wait_bar(kMode == kModeCross ? smem_u32(&bars->r_ready[slot]) : smem_u32(&bars->r_full[slot]),
+                            n / R)))
           break;
-        const uint64_t db = smem_desc_sw128(sV0 + sv * C::kTileBytes, 16384, 1024);
+        const uint64_t db = smem_desc_sw128(sR + slot * C::kTileBytes, 16384, 1024);
         for (int t = 0; t < w.n_live; ++t) {
           const int np = t ? np1 : np0, epi = t ? epi1 : epi0;
           if (!(ok = wait_bar(smem_u32(&bars->p_full[t]), np))) break;
@@ -224,7 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (t) ++np1; else ++np0;
         }
         if (!ok) break;
-        mma_commit(smem_u32(&bars->v_empty[sv]));
+        mma_commit(smem_u32(&bars->r_empty[slot]));
       }
       if (!ok) break;
       ++epi0;
@@ -241,8 +257,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < 4) {
     regs_dec<40>();
     if (warp == 0 && lane == 0) {
-      // ------------------------------------------------------------ producer: Q and K
-      int kv_cnt = 0, q_cnt = 0, k_issued = 0;
+      // ------------------------------------------------------------ producer: Q
+      int q_cnt = 0;
       bool ok = true;
       for (int it = it0; ok && it < p.n_items; it += it_step) {
         const Item w = decode_item<kMode>(p, it);
@@ -258,67 +274,74 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_4d(sQ + t * C::kTileBytes + c * 16384, &tm_q, b_q_full, c * 64, w.h,
                         w.q0 + 128 * t, w.b);
         ++q_cnt;
-        for (int j = 0; j < w.n_kv; ++j) {
-          if (j == (w.n_kv > kPrefetchLead ? w.n_kv - kPrefetchLead : 0)) {
-            // Warm L2 with the next item's Q tiles and first K/V tiles.
-            const int nit = it + it_step;
-            if (nit < p.n_items) {
-              const Item nw = decode_item<kMode>(p, nit);
-              for (int t = 0; t < nw.n_live; ++t)
+      }
+      if (*abort_flag && q_cnt > 0) drain_wait(b_q_full, (q_cnt - 1) & 1, status);
+    } else if (warp == 2 && lane == 0) {
+      // ------------------------------------------------------------ producer: K/V ring
+      const int G = count_tiles();
+      int n = 0;   // loads issued
+      bool ok = true;
+      auto load = [&](const CUtensorMap* map, const Item& w, int j) -> bool {
+        const int slot = n % R, use = n / R;
+        if (use > 0 && !bounded_wait(smem_u32(&bars->r_empty[slot]), (use - 1) & 1, abort_flag,
+                                     status, kStatusTimeoutLoad))
+          return false;
+        const uint32_t bar = smem_u32(&bars->r_full[slot]);
+        mbar_arrive_expect_tx(bar, C::kTileBytes);
 #pragma unroll
-                for (int c = 0; c < C::kSub; ++c)
-                  tma_prefetch_l2_4d(&tm_q, c * 64, nw.h, nw.q0 + 128 * t, nw.b);
-              for (int jj = 0; jj < nw.n_kv && jj < kPrefetchKV; ++jj)
+        for (int c = 0; c < C::kSub; ++c)
+          tma_load_4d(sR + slot * C::kTileBytes + c * 16384, map, bar, c * 64, w.h, j * 128, w.b);
+        ++n;
+        return true;
+      };
+      // Separate cursors (item, tile) for the K stream and the V stream.
+      int kit = first_live(it0), kj = 0, vit = kit, vj = 0;
+      Item kw{}, vw{};
+      if (kit < p.n_items) kw = vw = decode_item<kMode>(p, kit);
+      auto load_next_k = [&]() -> bool {
+        if (kj == (kw.n_kv > kPrefetchLead ? kw.n_kv - kPrefetchLead : 0)) {
+          // Warm L2 with the next item's Q tiles and first K/V tiles.
+          const int nit = first_live(kit + it_step);
+          if (nit < p.n_items) {
+            const Item nw = decode_item<kMode>(p, nit);
+            for (int t = 0; t < nw.n_live; ++t)
 #pragma unroll
-                for (int c = 0; c < C::kSub; ++c) {
-                  tma_prefetch_l2_4d(&tm_k, c * 64, nw.h, jj * 128, nw.b);
-                  tma_prefetch_l2_4d(&tm_v, c * 64, nw.h, jj * 128, nw.b);
-                }
-            }
+              for (int c = 0; c < C::kSub; ++c)
+                tma_prefetch_l2_4d(&tm_q, c * 64, nw.h, nw.q0 + 128 * t, nw.b);
+            for (int jj = 0; jj < nw.n_kv && jj < kPrefetchKV; ++jj)
+#pragma unroll
+              for (int c = 0; c < C::kSub; ++c) {
+                tma_prefetch_l2_4d(&tm_k, c * 64, nw.h, jj * 128, nw.b);
+                tma_prefetch_l2_4d(&tm_v, c * 64, nw.h, jj * 128, nw.b);
+              }
           }
-          const int g = kv_cnt + j, s = g % NSK, u = g / NSK;
-          if (u > 0 && !(ok = bounded_wait(smem_u32(&bars->k_empty[s]), (u - 1) & 1, abort_flag,
-                                           status, kStatusTimeoutLoad)))
-            break;
-          const uint32_t kf = smem_u32(&bars->k_full[s]);
-          mbar_arrive_expect_tx(kf, C::kTileBytes);
-#pragma unroll
-          for (int c = 0; c < C::kSub; ++c)
-            tma_load_4d(sK0 + s * C::kTileBytes + c * 16384, &tm_k, kf, c * 64, w.h, j * 128, w.b);
-          ++k_issued;
         }
-        kv_cnt += w.n_kv;
+        if (!load(&tm_k, kw, kj)) return false;
+        if (++kj == kw.n_kv) {
+          kj = 0;
+          kit = first_live(kit + it_step);
+          if (kit < p.n_items) kw = decode_item<kMode>(p, kit);
+        }
+        return true;
+      };
+      auto load_next_v = [&]() -> bool {
+        if (!load(&tm_v, vw, vj)) return false;
+        if (++vj == vw.n_kv) {
+          vj = 0;
+          vit = first_live(vit + it_step);
+          if (vit < p.n_items) vw = decode_item<kMode>(p, vit);
+        }
+        return true;
+      };
+      if (G > 0) ok = load_next_k();
+      for (int g = 0; ok && g < G; ++g) {
+        if (g + 1 < G && !(ok = load_next_k())) break;
+        ok = load_next_v();
       }
       if (*abort_flag) {
         // Let the copies still in flight land before the CTA releases its shared memory.
-        if (q_cnt > 0) drain_wait(b_q_full, (q_cnt - 1) & 1, status);
-        for (int g = k_issued - NSK > 0 ? k_issued - NSK : 0; g < k_issued; ++g)
-          drain_wait(smem_u32(&bars->k_full[g % NSK]), (g / NSK) & 1, status);
-      }
-    } else if (warp == 2 && lane == 0) {
-      // ------------------------------------------------------------ producer: V
-      int v_cnt = 0, v_issued = 0;
-      bool ok = true;
-      for (int it = it0; ok && it < p.n_items; it += it_step) {
-        const Item w = decode_item<kMode>(p, it);
-        if (w.n_live == 0) continue;
-        for (int j = 0; j < w.n_kv; ++j) {
-          const int g = v_cnt + j, s = g % NSV, u = g / NSV;
-          if (u > 0 && !(ok = bounded_wait(smem_u32(&bars->v_empty[s]), (u - 1) & 1, abort_flag,
-                                           status, kStatusTimeoutLoad)))
-            break;
-          const uint32_t vf = smem_u32(&bars->v_full[s]);
-          mbar_arrive_expect_tx(vf, C::kTileBytes);
-#pragma unroll
-          for (int c = 0; c < C::kSub; ++c)
-            tma_load_4d(sV0 + s * C::kTileBytes + c * 16384, &tm_v, vf, c * 64, w.h, j * 128, w.b);
-          ++v_issued;
-        }
-        v_cnt += w.n_kv;
-      }
-      if (*abort_flag) {
-        for (int g = v_issued - NSV > 0 ? v_issued - NSV : 0; g < v_issued; ++g)
-          drain_wait(smem_u32(&bars->v_full[g % NSV]), (g / NSV) & 1, status);
+        for (int x = n - R > 0 ? n - R : 0; x < n; ++x)
+          drain_wait(smem_u32(&bars->r_full[x % R]), (x / R) & 1, status);
       }
     }
   } else if (warp < 12) {
@@ -471,29 +494,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (kMode == kModeCross) {
       // ---------------------------------------------------------- V pad rows (warps 14-15)
       // K/V tiles are loaded up to Skv rows; rows past the batch's valid length are zeroed so
-      // that 0 * (pad contents) cannot reach O.
+      // that 0 * (pad contents) cannot reach O. Every ring load passes through here in order
+      // (K loads unchanged), so r_ready completes once per load, like r_full.
       constexpr int kZeroThreads = 64;
       const int at = tid - 448;
       volatile int* go = &bars->aux_go;
-      int v_cnt = 0;
+      const int G = count_tiles();
+      int vit = first_live(it0), vj = 0;
+      Item vw{};
+      if (vit < p.n_items) vw = decode_item<kMode>(p, vit);
       bool ok = true;
-      for (int it = it0; ok && it < p.n_items; it += it_step) {
-        const Item w = decode_item<kMode>(p, it);
-        if (w.n_live == 0) continue;
-        for (int j = 0; ok && j < w.n_kv; ++j) {
-          const int gv = v_cnt + j, s = gv % NSV;
-          if (!(ok = group_wait<kZeroThreads>(smem_u32(&bars->v_full[s]), (gv / NSV) & 1, abort_flag,
+      for (int n = 0; ok && n < 2 * G; ++n) {
+        const int slot = n % R;
+        if (!(ok = group_wait<kZeroThreads>(smem_u32(&bars->r_full[slot]), (n / R) & 1, abort_flag,
                                               status, kStatusTimeoutRope, go, at)))
-            break;
-          const int nv = min(128, w.kv_valid - j * 128);
+          break;
+        const bool is_v = (n == 2 * G - 1) || (n >= 2 && (n & 1) == 0);
+        if (is_v) {
+          const int nv = min(128, vw.kv_valid - vj * 128);
           if (nv < 128) {
-            zero_rows<D, kZeroThreads>(sV0 + s * C::kTileBytes, nv, at);
+            zero_rows<D, kZeroThreads>(sR + slot * C::kTileBytes, nv, at);
             fence_proxy_async_smem();
           }
-          named_bar_sync(1, kZeroThreads);
-          if (at == 0) mbar_arrive(smem_u32(&bars->v_ready[s]));
+          if (++vj == vw.n_kv) {
+            vj = 0;
+            vit = first_live(vit + it_step);
+            if (vit < p.n_items) vw = decode_item<kMode>(p, vit);
+          }
         }
-        v_cnt += w.n_kv;
+        named_bar_sync(1, kZeroThreads);
+        if (at == 0) mbar_arrive(smem_u32(&bars->r_ready[slot]));
       }
     }
   }
