@@ -128,16 +128,18 @@ int dit_attn_fwd(const void* q, const void* k, const void* v, int B, int Sq, int
 /* ---------------------------------------------------------------------------------------
  * dit_attn_fwd with RoPE, rotating every q and k row exactly once per call (same inputs,
  * outputs and numerics as dit_attn_fwd with tables). The launch first rotates the valid rows
- * of q and k with the given tables into fp16 copies in `workspace` (all CTAs, one grid-wide
- * barrier; the launch is cooperative), then runs the attention on those copies. Without a
+ * of q and k with the given tables into fp16 copies in `workspace` (all CTAs; the loads of
+ * the rotated rows wait until every CTA has finished, so the launch is cooperative), then runs
+ * the attention on those copies. Without a
  * workspace, dit_attn_fwd rotates each k tile again in every CTA that loads it.
  *
  * workspace: device buffer of at least dit_attn_workspace_bytes(B, Sq, Skv, H, D) bytes,
  * 256-byte aligned, owned by the caller; its contents on entry do not matter and are
  * overwritten. Calls that share a workspace must not overlap on the GPU.
  * All four tables are required. Errors as dit_attn_fwd, plus DIT_ERR_INVALID_ARG for a
- * missing or too small workspace, DIT_ERR_ALIGNMENT for a misaligned one, and DIT_ERR_CUDA if
- * the GPU cannot run the cooperative launch.
+ * missing or too small workspace, DIT_ERR_ALIGNMENT for a misaligned one, DIT_ERR_UNSUPPORTED
+ * when max(Sq, Skv) * H * D / 16 >= 2^30 (one batch of rows indexed in 32 bits), and
+ * DIT_ERR_CUDA if the GPU cannot run the cooperative launch.
  * ------------------------------------------------------------------------------------- */
 size_t dit_attn_workspace_bytes(int B, int Sq, int Skv, int H, int D);
 int dit_attn_fwd_ws(const void* q, const void* k, const void* v, int B, int Sq, int Skv, int H,

@@ -185,3 +185,25 @@ def test_workspace_rope_path_wan480_sampled(lib):
     compare(O, L, Or, Lr, case.q_valid, rows=rows, heads=heads)
     assert np.all(O[:, case.q_valid:] == 0) and np.all(L[:, case.q_valid:] == -np.inf)
     assert lib.dit_device_status() == 0
+
+
+@pytest.mark.parametrize("B,H,D,Sq,qv", [(1, 200, 64, 768, 300), (2, 90, 128, 768, 511)])
+def test_workspace_rounds_with_skipped_items_bitwise(lib, B, H, D, Sq, qv):
+    """More work items than CTAs, so the workspace path rotates in several rounds, and every
+    third item (query rows past q_valid) has no work, so a CTA skips a round now and then and
+    later uses heads that were rotated in the round it skipped. Bitwise equal to the per-tile
+    path (which has no rounds), and parity with the oracle on sampled rows and heads."""
+    case = AttnCase("wsrounds", B=B, H=H, D=D, Sq=Sq, Skv=Sq, q_valid=qv, kv_valid=Sq - 57,
+                    rope="1d", seed=91 + D)
+    q, k, v = make_qkv(case)
+    tabs = gpu_tables_self(lib, case)
+    qd, kd, vd = dev_bf16(q), dev_bf16(k), dev_bf16(v)
+    O1, L1 = lib.dit_attn_fwd(qd, kd, vd, case.q_valid, case.kv_valid, *tabs)
+    O2, L2 = lib.dit_attn_fwd_ws(qd, kd, vd, case.q_valid, case.kv_valid, *tabs)
+    torch.cuda.synchronize()
+    assert torch.equal(O1, O2) and torch.equal(L1, L2)
+    rows = sample_rows(case.q_valid, case.Sq, 12, seed=23)
+    heads = [0, H // 2, H - 1]
+    Or, Lr = oracle_self(case, q, k, v, rows=rows, heads=heads)
+    compare(O2.float().cpu().numpy(), L2.cpu().numpy(), Or, Lr, case.q_valid, rows=rows, heads=heads)
+    assert lib.dit_device_status() == 0

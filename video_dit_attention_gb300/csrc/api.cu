@@ -153,6 +153,8 @@ extern "C" int dit_attn_fwd_ws(const void* q, const void* k, const void* v, int 
   if (kv_valid_len < 0 || kv_valid_len > Skv) return DIT_ERR_INVALID_ARG;
   if (!cos_q || !sin_q || !cos_k || !sin_k || !workspace) return DIT_ERR_INVALID_ARG;
   if (workspace_bytes < attn_workspace_bytes(B, Sq, Skv, H, D)) return DIT_ERR_INVALID_ARG;
+  // The rotation phase indexes (row, head, 8-pair chunk) of one batch in 32 bits.
+  if (static_cast<long long>(Sq > Skv ? Sq : Skv) * H * (D / 16) >= (1ll << 30)) return DIT_ERR_UNSUPPORTED;
   if (!aligned(cos_q, 16) || !aligned(sin_q, 16) || !aligned(cos_k, 16) || !aligned(sin_k, 16) ||
       !aligned(workspace, 256))
     return DIT_ERR_ALIGNMENT;

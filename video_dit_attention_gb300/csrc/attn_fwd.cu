@@ -110,15 +110,15 @@ struct KParams {
   float* lse;
 };
 
-// Rotation-phase parameters of the workspace mode: raw inputs, their rotated fp16 copies
-// (which the TMA maps of q and k point at) and the grid barrier counter (zeroed before
-// launch). Kept apart from KParams so the other modes' parameter block stays small.
+// Workspace-mode parameters: raw inputs, their rotated fp16 copies (which the TMA maps of q
+// and k point at) and the count of CTAs done rotating (zeroed before launch). Kept apart
+// from KParams so the other modes' parameter block stays small.
 struct WsParams {
   const uint16_t* q_raw;
   const uint16_t* k_raw;
   uint16_t* q_rot;
   uint16_t* k_rot;
-  unsigned int* grid_bar;
+  unsigned int* rotated;
   int B;
 };
 
@@ -267,33 +267,47 @@ __device__ __forceinline__ Item decode_item(const KParams& p, int it) {
 // and barrier phase runs on counters that continue across items, so the loads, the rotation
 // and the first MMAs of the next item overlap the epilogue of the current one.
 // Writes the split-halves rotation of rows [0, valid) of x [B, S_rows, H, D] (bf16) as fp16
-// into y (same layout), with table rows [S_rows, D/2]; work items are (row, 8-pair chunk), so
-// consecutive threads read and write consecutive 16-byte chunks.
+// into y (same layout), with table rows [S_rows, D/2]. Work items are (row, 8-pair chunk);
+// within a batch the valid rows of all heads are contiguous, so consecutive threads read and
+// write consecutive 16-byte chunks. Each thread keeps four items in flight.
 template <int D>
 __device__ __forceinline__ void rotate_rows_fp16(const uint16_t* __restrict__ x, uint16_t* __restrict__ y,
                                                  const float* __restrict__ cos_t,
                                                  const float* __restrict__ sin_t, int B, int S_rows,
-                                                 int valid, int H, long long gtid, long long gthreads) {
-  constexpr int kHalf = D / 2, kChunks = kHalf / 8;
-  const long long items = static_cast<long long>(B) * valid * H * kChunks;
-  for (long long it = gtid; it < items; it += gthreads) {
-    const int ch = static_cast<int>(it % kChunks);
-    long long rest = it / kChunks;
-    const int h = static_cast<int>(rest % H);
-    rest /= H;
-    const int srow = static_cast<int>(rest % valid);
-    const int b = static_cast<int>(rest / valid);
-    const long long row = (static_cast<long long>(b) * S_rows + srow) * H + h;
-    const uint16_t* xr = x + row * D + ch * 8;
-    uint4 a = *reinterpret_cast<const uint4*>(xr);
-    uint4 bb = *reinterpret_cast<const uint4*>(xr + kHalf);
-    const float* ct = cos_t + static_cast<long long>(srow) * kHalf + ch * 8;
-    const float* st = sin_t + static_cast<long long>(srow) * kHalf + ch * 8;
-    rotate8(a, bb, __ldg(reinterpret_cast<const float4*>(ct)), __ldg(reinterpret_cast<const float4*>(ct + 4)),
-            __ldg(reinterpret_cast<const float4*>(st)), __ldg(reinterpret_cast<const float4*>(st + 4)));
-    uint16_t* yr = y + row * D + ch * 8;
-    *reinterpret_cast<uint4*>(yr) = a;
-    *reinterpret_cast<uint4*>(yr + kHalf) = bb;
+                                                 int valid, int H, int gtid, int gthreads) {
+  constexpr int kHalf = D / 2, kChunks = kHalf / 8, kU = 4;
+  const int per_b = valid * H * kChunks;
+  for (int b = 0; b < B; ++b) {
+    const size_t boff = static_cast<size_t>(b) * S_rows * H * D;
+    for (int i0 = gtid; i0 < per_b; i0 += kU * gthreads) {
+      uint4 a[kU], bb[kU];
+      float4 c0[kU], c1[kU], s0[kU], s1[kU];
+      size_t off[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int i = i0 + u * gthreads;
+        if (i < per_b) {
+          const int ch = i % kChunks, rh = i / kChunks, srow = rh / H;   // rh = srow * H + h
+          off[u] = boff + static_cast<size_t>(rh) * D + ch * 8;
+          a[u] = *reinterpret_cast<const uint4*>(x + off[u]);
+          bb[u] = *reinterpret_cast<const uint4*>(x + off[u] + kHalf);
+          const float* ct = cos_t + static_cast<size_t>(srow) * kHalf + ch * 8;
+          const float* st = sin_t + static_cast<size_t>(srow) * kHalf + ch * 8;
+          c0[u] = __ldg(reinterpret_cast<const float4*>(ct));
+          c1[u] = __ldg(reinterpret_cast<const float4*>(ct + 4));
+          s0[u] = __ldg(reinterpret_cast<const float4*>(st));
+          s1[u] = __ldg(reinterpret_cast<const float4*>(st + 4));
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        if (i0 + u * gthreads < per_b) {
+          rotate8(a[u], bb[u], c0[u], c1[u], s0[u], s1[u]);
+          *reinterpret_cast<uint4*>(y + off[u]) = a[u];
+          *reinterpret_cast<uint4*>(y + off[u] + kHalf) = bb[u];
+        }
+      }
+    }
   }
 }
 
@@ -304,8 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_cq,
                     const __grid_constant__ CUtensorMap tm_sq, const __grid_constant__ CUtensorMap tm_ck,
-                    const __grid_constant__ CUtensorMap tm_sk, const KParams p,
-                    const WsParams ws) {
+                    const __grid_constant__ CUtensorMap tm_sk, const KParams p) {
   using C = Cfg<D>;
   constexpr int NSK = C::kStagesK, NSV = C::kStagesV;
   extern __shared__ uint8_t smem_raw[];
@@ -369,40 +382,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tbase = bars->tmem_base;
-  if (kMode == kModeRopeWs) {
-    // ---------------------------------------------------------- phase 1: rotate q and k once
-    // Every q and k row is rotated exactly once (all CTAs, all threads), stored as fp16, and
-    // the attention below reads the rotated copies through its q/k TMA maps.
-    const long long gtid = static_cast<long long>(blockIdx.x) * kThreads + tid;
-    const long long gthreads = static_cast<long long>(gridDim.x) * kThreads;
-    rotate_rows_fp16<D>(ws.q_raw, ws.q_rot, p.cos_q, p.sin_q, ws.B, p.Sq, p.q_valid, p.H, gtid, gthreads);
-    int kv_max = p.kv_valid;
-    rotate_rows_fp16<D>(ws.k_raw, ws.k_rot, p.cos_k, p.sin_k, ws.B, p.Skv, kv_max, p.H, gtid, gthreads);
-    // Grid-wide barrier (the launch is cooperative, so every CTA is resident): the stores
-    // above must be visible, also to the async proxy, before any CTA's TMA reads them.
-    fence_proxy_async_all();
-    __threadfence();
-    __syncthreads();
-    if (tid == 0) {
-      atomicAdd(ws.grid_bar, 1u);
-      const uint64_t t0 = globaltimer_ns();
-      while (atomicAdd(ws.grid_bar, 0u) < gridDim.x) {
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
-          bars->abort = 1;
-          atomicOr(status, kStatusTimeoutGrid);
-          break;
-        }
-        __nanosleep(256);
-      }
-      __threadfence();
-    }
-    __syncthreads();
-    fence_proxy_async_all();
-  }
   const int it0 = blockIdx.x, it_step = gridDim.x;
 
-  // After a failed grid barrier no CTA touches the (possibly incomplete) rotated copies.
-  if (!(kMode == kModeRopeWs && *abort_flag)) {
+  {
   // Register budgets per warpgroup (40 / 200 / 200 / 72) add up to the launch's 512 x 128;
   // each is set at the top of its role's branch so that the role's code is compiled to it.
   // Warpgroup 0 holds the TMA producers, 1 and 2 the softmax, 3 the MMA issuer and the
@@ -870,11 +852,11 @@ cudaError_t launch_mode(const AttnArgs& a) {
   ws.k_raw = static_cast<const uint16_t*>(a.k);
   ws.q_rot = q_rot;
   ws.k_rot = k_rot;
-  ws.grid_bar = nullptr;
+  ws.rotated = nullptr;
   ws.B = a.B;
   if (kMode == kModeRopeWs) {
     const size_t k_bytes = (static_cast<size_t>(a.B) * a.Skv * a.H * D * 2 + 255) / 256 * 256;
-    ws.grid_bar = reinterpret_cast<unsigned int*>(static_cast<char*>(a.workspace) + q_bytes + k_bytes);
+    ws.rotated = reinterpret_cast<unsigned int*>(static_cast<char*>(a.workspace) + q_bytes + k_bytes);
   }
   static const int sm_count = [] {
     int dev = 0, n = 0;
@@ -889,7 +871,7 @@ cudaError_t launch_mode(const AttnArgs& a) {
     auto kern = attn_fwd_kernel<D, kMode>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::kSmemBytes);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kThreads, Cfg<D>::kSmemBytes, a.stream>>>(mq, mk, mv, mcq, msq, mck, msk, p, ws);
+    kern<<<grid, kThreads, Cfg<D>::kSmemBytes, a.stream>>>(mq, mk, mv, mcq, msq, mck, msk, p);
     return cudaGetLastError();
   } else {
     auto kern = attn_sp_kernel<D, kMode>;
@@ -899,9 +881,9 @@ cudaError_t launch_mode(const AttnArgs& a) {
       kern<<<grid, kThreads, CfgSp<D>::kSmemBytes, a.stream>>>(mq, mk, mv, p, ws);
       return cudaGetLastError();
     }
-    // The rotation phase ends in a grid-wide barrier: launch cooperatively so that every CTA
-    // is resident, after zeroing the barrier counter on the same stream.
-    e = cudaMemsetAsync(ws.grid_bar, 0, sizeof(unsigned int), a.stream);
+    // CTAs wait for rotated rows that other CTAs produce: launch cooperatively so that every
+    // CTA is resident, after zeroing the counter on the same stream.
+    e = cudaMemsetAsync(ws.rotated, 0, sizeof(unsigned int), a.stream);
     if (e != cudaSuccess) return e;
     void* args[] = {&mq, &mk, &mv, &p, &ws};
     return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kern), dim3(grid), dim3(kThreads),
@@ -914,7 +896,7 @@ cudaError_t launch_mode(const AttnArgs& a) {
 size_t attn_workspace_bytes(int B, int Sq, int Skv, int H, int D) {
   const size_t q = (static_cast<size_t>(B) * Sq * H * D * 2 + 255) / 256 * 256;
   const size_t k = (static_cast<size_t>(B) * Skv * H * D * 2 + 255) / 256 * 256;
-  return q + k + 256;
+  return q + k + 256;   // + the counter of CTAs done rotating
 }
 
 cudaError_t launch_attn_fwd(const AttnArgs& a, AttnMode mode) {

@@ -113,37 +113,43 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after_sync();
   const uint32_t tbase = bars->tmem_base;
   if (kMode == kModeRopeWs) {
-    // ---------------------------------------------------------- phase 1: rotate q and k once
-    const long long gtid = static_cast<long long>(blockIdx.x) * kThreads + tid;
-    const long long gthreads = static_cast<long long>(gridDim.x) * kThreads;
+    // ---------------------------------------------------- rotate q and k once, every thread
+    // The rotated rows are published through a counter: each thread's generic-proxy stores
+    // are fenced against the async proxy (the TMA loads that read them), then the CTA counts
+    // itself in with a device-scope release. Only the producers wait for the count.
+    const int gtid = blockIdx.x * kThreads + tid, gthreads = gridDim.x * kThreads;
     rotate_rows_fp16<D>(ws.q_raw, ws.q_rot, p.cos_q, p.sin_q, ws.B, p.Sq, p.q_valid, p.H, gtid, gthreads);
     rotate_rows_fp16<D>(ws.k_raw, ws.k_rot, p.cos_k, p.sin_k, ws.B, p.Skv, p.kv_valid, p.H, gtid, gthreads);
-    // Grid-wide barrier (cooperative launch: every CTA is resident). The rotated rows must be
-    // visible, also to the async proxy, before any CTA's TMA reads them.
     fence_proxy_async_all();
-    __threadfence();
     __syncthreads();
     if (tid == 0) {
-      atomicAdd(ws.grid_bar, 1u);
-      const uint64_t t0 = globaltimer_ns();
-      while (atomicAdd(ws.grid_bar, 0u) < gridDim.x) {
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
-          bars->abort = 1;
-          atomicOr(status, kStatusTimeoutGrid);
-          break;
-        }
-        __nanosleep(256);
-      }
       __threadfence();
+      atomicAdd(ws.rotated, 1u);
     }
-    __syncthreads();
-    fence_proxy_async_all();
   }
   const int it0 = blockIdx.x, it_step = gridDim.x;
   // First item at or after `it` (in this CTA's sequence) that has work.
   auto first_live = [&](int it) -> int {
     while (it < p.n_items && decode_item<kMode>(p, it).n_live == 0) it += it_step;
     return it;
+  };
+  // Workspace mode: a producer waits, before its first load, until every CTA has counted in
+  // its share of the rotation (`ready` remembers that it has).
+  auto wait_rotated = [&](bool& ready) -> bool {
+    if (kMode != kModeRopeWs || ready) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (ld_acquire_gpu(ws.rotated) < gridDim.x) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        *abort_flag = 1;
+        atomicOr(status, kStatusTimeoutGrid);
+        return false;
+      }
+      __nanosleep(128);
+    }
+    fence_proxy_async_all();   // the TMA loads that follow read what the other CTAs wrote
+    ready = true;
+    return true;
   };
   // G: key tiles over all of this CTA's items.
   auto count_tiles = [&]() -> int {
@@ -253,12 +259,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   };
 
-  if (!(kMode == kModeRopeWs && *abort_flag)) {
+  {
   if (warp < 4) {
     regs_dec<40>();
     if (warp == 0 && lane == 0) {
       // ------------------------------------------------------------ producer: Q
       int q_cnt = 0;
+      bool ready = false;
       bool ok = true;
       for (int it = it0; ok && it < p.n_items; it += it_step) {
         const Item w = decode_item<kMode>(p, it);
@@ -267,6 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (q_cnt > 0 && !(ok = bounded_wait(b_q_empty, (q_cnt - 1) & 1, abort_flag, status,
                                              kStatusTimeoutLoad)))
           break;
+        if (!(ok = wait_rotated(ready))) break;
         mbar_arrive_expect_tx(b_q_full, w.n_live * C::kTileBytes);
         for (int t = 0; t < w.n_live; ++t)
 #pragma unroll
@@ -296,6 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       // Separate cursors (item, tile) for the K stream and the V stream.
       int kit = first_live(it0), kj = 0, vit = kit, vj = 0;
+      bool k_ready = false;
       Item kw{}, vw{};
       if (kit < p.n_items) kw = vw = decode_item<kMode>(p, kit);
       auto load_next_k = [&]() -> bool {
@@ -316,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
           }
         }
-        if (!load(&tm_k, kw, kj)) return false;
+        if (!wait_rotated(k_ready) || !load(&tm_k, kw, kj)) return false;
         if (++kj == kw.n_kv) {
           kj = 0;
           kit = first_live(kit + it_step);

@@ -110,6 +110,13 @@ __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity,
   }
 }
 
+// Load with acquire semantics at device scope (pairs with a fence + atomic on another SM).
+__device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int* p) {
+  unsigned int v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 // ---------------------------------------------------------------------------
 // Proxy fences and named barriers
 // ---------------------------------------------------------------------------
