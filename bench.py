@@ -153,14 +153,18 @@ def gpu_id_for_smi(dev_index: int) -> str:
         return vis.split(",")[dev_index] if vis else str(dev_index)
 
 
+# The attention kernels' sources: a committed ncu summary applies while their hash matches.
+KERNEL_SOURCES = ("attn_fwd.cu", "attn_sp.cuh", "ptx.cuh")
+
+
 def profiled_traffic(name):
     """DRAM bytes per launch of the dominant kernel from the committed ncu summary of this
     workload, or None if there is none or the kernel sources changed since it was taken."""
     import hashlib
-    path = os.path.join(ROOT, "profiles", {"wan480": "attn_fwd_wan480x832x9.md"}.get(name, "-"))
+    path = os.path.join(ROOT, "profiles", {"wan480": "attn_sp_wan480x832x9.md"}.get(name, "-"))
     if not os.path.exists(path):
         return None
-    srcs = [os.path.join(ROOT, "video_dit_attention_gb300", "csrc", f) for f in ("attn_fwd.cu", "ptx.cuh")]
+    srcs = [os.path.join(ROOT, "video_dit_attention_gb300", "csrc", f) for f in KERNEL_SOURCES]
     h = hashlib.sha256(b"".join(open(f, "rb").read() for f in srcs)).hexdigest()[:16]
     sha = traffic = None
     for line in open(path):
@@ -216,6 +220,14 @@ def config_dict(name, spec, rope_mode="ws"):
         d["rope_path"] = _ROPE_PATH[rope_mode]
     d["l2"] = "3 rotating input sets, each larger than the 129 MB L2" if name != "tiny" else "tiny: L2-resident"
     return d
+
+
+def dominant_kernel(name, rope_mode):
+    if name == "cross":
+        return "attn_sp_kernel (cross mode)"
+    if rope_mode == "fused" and name != "cross":
+        return "attn_fwd_kernel (RoPE per loaded tile)"
+    return "attn_sp_kernel (workspace RoPE)"
 
 
 _ROPE_PATH = {
@@ -582,7 +594,7 @@ def main():
         "pct_of_bf16_peak": 100.0 * (units / max_el / 1e12) / (peak * world),
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": profiled_traffic(name),
-                     "kernel": "attn_fwd_kernel" if name != "cross" else "attn_fwd_kernel (cross mode)",
+                     "kernel": dominant_kernel(name, args.rope),
                      "kernel_ms": kern_s * 1e3, "algorithmic_bytes": wl.dominant_bytes(),
                      "peak_source": f"bf16_tflops (burst) of {peaks['source']} peaks"},
         "gpu_launches": wl.launches_per_step * args.steps,
