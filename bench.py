@@ -158,10 +158,13 @@ KERNEL_SOURCES = ("attn_fwd.cu", "attn_sp.cuh", "ptx.cuh")
 
 
 def profiled_traffic(name):
-    """DRAM bytes per launch of the dominant kernel from the committed ncu summary of this
-    workload, or None if there is none or the kernel sources changed since it was taken."""
+    """DRAM bytes per launch of the dominant kernel (per step of four launches for the sharded
+    workload) from the committed ncu summary of this workload, or None if there is none or the
+    kernel sources changed since it was taken."""
     import hashlib
-    path = os.path.join(ROOT, "profiles", {"wan480": "attn_sp_wan480x832x9.md"}.get(name, "-"))
+    path = os.path.join(ROOT, "profiles", {"wan480": "attn_sp_wan480x832x9.md", "wan720": "attn_sp_wan720p81f.md",
+                                           "cross": "attn_sp_cross_shortkv.md",
+                                           "sharded": "attn_sp_sharded_keys.md"}.get(name, "-"))
     if not os.path.exists(path):
         return None
     srcs = [os.path.join(ROOT, "video_dit_attention_gb300", "csrc", f) for f in KERNEL_SOURCES]
@@ -170,8 +173,8 @@ def profiled_traffic(name):
     for line in open(path):
         if line.startswith("kernel sources sha256"):
             sha = line.split(":")[-1].strip()
-        elif line.startswith("traffic_bytes_per_launch:"):
-            traffic = int(line.split(":")[1])
+        elif line.startswith(("traffic_bytes_per_launch:", "traffic_bytes_per_step:")):
+            traffic = int(line.split(":")[1])   # per step for sharded (four launches), like achieved
     return traffic if sha == h else None
 
 
@@ -406,6 +409,65 @@ class E2E:
         self.hl.copy_(self.l_u, non_blocking=True)
 
 
+# ----------------------------------------------------------------------------- HBM-bound kernels
+def measure_hbm_kernels(peaks):
+    """The standalone RoPE and the LSE merge, each timed with CUDA events over back-to-back
+    calls whose inputs rotate over sets larger than L2, and reported as algorithmic GB/s
+    against the measured HBM copy bandwidth. Not part of the timed attention step."""
+    import torch
+
+    from video_dit_attention_gb300 import dit_attn as lib
+    from video_dit_attention_gb300 import inputs as I
+    dev = torch.device("cuda")
+    gen = torch.Generator(device="cpu").manual_seed(5)
+    out = {}
+
+    def timed(fn, n, warm=5):
+        for i in range(warm):
+            fn(i)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for i in range(n):
+            fn(i)
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / 1e3 / n
+
+    # RoPE on the Wan 480 q and k (stacked as B = 2 rows of the same positions), out of place.
+    c = I.wan480_case()
+    cs, sn = lib.dit_rope_table_3d(c.Sq, c.grid, c.D, c.axis_dims, c.theta)
+    cs, sn = torch.from_numpy(cs).to(dev), torch.from_numpy(sn).to(dev)
+    xs = [torch.randn((2, c.Sq, c.H, c.D), generator=gen).to(torch.bfloat16).to(dev) for _ in range(2)]
+    ys = [torch.empty_like(x) for x in xs]
+    t = timed(lambda i: lib.dit_rope_split_halves(xs[i % 2], cs, sn, out=ys[i % 2]), 40)
+    nb = 2 * xs[0].numel() * 2
+    out["rope_split_halves"] = {
+        "workload": "Wan 480x832x9 q and k, [2, 4736, 40, 128] bf16, 3-D tables, out of place",
+        "bytes_per_call": nb, "us": t * 1e6, "GB_s": nb / t / 1e9, "frac_of_hbm": nb / t / 1e9 / peaks["hbm_gbs"],
+        "l2": "2 input sets of 97 MB, 194 MB moved per call (> 129 MB L2)"}
+    del xs, ys
+    # LSE merge of the sharded workload's 4 partials.
+    sc = I.sharded_case()
+    n = len(sc.shard_valid)
+    sets = []
+    for _ in range(4):
+        po = torch.randn((n, sc.B, sc.Sq, sc.H, sc.D), generator=gen).to(torch.bfloat16).to(dev)
+        pl = (torch.randn((n, sc.B, sc.Sq, sc.H), generator=gen) * 3).to(dev)
+        sets.append((po, pl, torch.empty((sc.B, sc.Sq, sc.H, sc.D), dtype=torch.bfloat16, device=dev),
+                     torch.empty((sc.B, sc.Sq, sc.H), dtype=torch.float32, device=dev)))
+    t = timed(lambda i: lib.dit_attn_lse_merge(sets[i % 4][0], sets[i % 4][1], out=sets[i % 4][2],
+                                               lse=sets[i % 4][3]), 200)
+    rows = sc.B * sc.Sq * sc.H
+    nb = rows * (n * (sc.D * 2 + 4) + sc.D * 2 + 4)
+    out["lse_merge"] = {
+        "workload": "4 partials of [1, 1024, 32, 128] bf16 + LSE -> merged O, LSE",
+        "bytes_per_call": nb, "us": t * 1e6, "GB_s": nb / t / 1e9, "frac_of_hbm": nb / t / 1e9 / peaks["hbm_gbs"],
+        "l2": "4 input sets of 43 MB rotate (170 MB > 129 MB L2)"}
+    torch.cuda.synchronize()
+    return out
+
+
 # ----------------------------------------------------------------------------- oracle arm
 def oracle_sample(name, spec, host, n_rows, n_heads, seed=0):
     """Runs the fp64 oracle once on (n_rows query rows) x (n_heads heads) of the workload;
@@ -509,6 +571,7 @@ def main():
     ap.add_argument("--rope", default="ws", choices=["ws", "fused"],
                     help="ws: rotate q/k once per call into a workspace (default); fused: rotate per tile")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-hbm-kernels", action="store_true", help="skip the RoPE / merge GB/s figures")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
@@ -602,6 +665,8 @@ def main():
     }
     if e2e is not None:
         line["e2e"] = e2e
+    if rank == 0 and not args.no_hbm_kernels:
+        line["hbm_kernels"] = measure_hbm_kernels(peaks)
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(name, spec, wl.host)
     print(json.dumps(line), flush=True)
