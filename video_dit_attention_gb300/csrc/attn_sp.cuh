@@ -462,35 +462,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(b_p_full);
       }
       if (!ok) break;
-      // Epilogue: wait for the last P_t V of this item, read O_t, normalise, store.
+      // Epilogue. Wait for the last P_t V of this item and take O_t out of TMEM, which then
+      // belongs to the next item (its first P_t V may start), then normalise and store.
       if (!warp_wait(b_pv_done, (sc - 1) & 1, abort_flag, status, kStatusTimeoutSoftmax)) {
         ok = false;
         break;
       }
       tc_fence_after_sync();
+      uint32_t orr[D / 32][32];
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) tmem_ld32_nowait(tO + c * 32, orr[c]);
+      tmem_ld_wait_tied(orr[0]);
+#pragma unroll
+      for (int c = 1; c < D / 32; ++c) tmem_reg_tie(orr[c]);
+      tc_fence_before_sync();
+      mbar_arrive(smem_u32(&bars->o_free[t]));
       const int qrow = w.q0 + 128 * t + r;
       const bool valid_row = qrow < p.q_valid;
       const float inv_l = 1.f / l;
-      uint16_t* dst = p.out + ((static_cast<size_t>(w.b) * p.Sq + qrow) * p.H + w.h) * D;
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t orr[32];
-        tmem_ld32(tO + c * 32, orr);
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          uint4 o = make_uint4(0, 0, 0, 0);
-          if (valid_row) {
-            const float* f = reinterpret_cast<const float*>(&orr[8 * q4]);
-            o.x = pack_bf16x2(f[0] * inv_l, f[1] * inv_l);
-            o.y = pack_bf16x2(f[2] * inv_l, f[3] * inv_l);
-            o.z = pack_bf16x2(f[4] * inv_l, f[5] * inv_l);
-            o.w = pack_bf16x2(f[6] * inv_l, f[7] * inv_l);
-          }
-          *reinterpret_cast<uint4*>(dst + c * 32 + q4 * 8) = o;
+      for (int u = 0; u < D / 8; ++u) {          // 16-byte unit u: columns 8u .. 8u + 7
+        uint4 o = make_uint4(0, 0, 0, 0);
+        if (valid_row) {
+          const uint32_t* f = &orr[u >> 2][(u & 3) * 8];
+          o.x = pack_bf16x2(__uint_as_float(f[0]) * inv_l, __uint_as_float(f[1]) * inv_l);
+          o.y = pack_bf16x2(__uint_as_float(f[2]) * inv_l, __uint_as_float(f[3]) * inv_l);
+          o.z = pack_bf16x2(__uint_as_float(f[4]) * inv_l, __uint_as_float(f[5]) * inv_l);
+          o.w = pack_bf16x2(__uint_as_float(f[6]) * inv_l, __uint_as_float(f[7]) * inv_l);
         }
+        *reinterpret_cast<uint4*>(p.out + ((static_cast<size_t>(w.b) * p.Sq + qrow) * p.H + w.h) * D + u * 8) = o;
       }
-      tc_fence_before_sync();
-      mbar_arrive(smem_u32(&bars->o_free[t]));
       p.lse[(static_cast<size_t>(w.b) * p.Sq + qrow) * p.H + w.h] =
           valid_row ? (m_used + log2f(l)) * kLn2 : -INFINITY;
     }
