@@ -274,7 +274,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (q_cnt > 0 && !(ok = bounded_wait(b_q_empty, (q_cnt - 1) & 1, abort_flag, status,
                                              kStatusTimeoutLoad)))
           break;
-        if (!(ok = wait_rotated(ready))) break;
+        ok = wait_rotated(ready);
+        if (!ok) break;
         mbar_arrive_expect_tx(b_q_full, w.n_live * C::kTileBytes);
         for (int t = 0; t < w.n_live; ++t)
 #pragma unroll
@@ -469,29 +470,54 @@ __global__ void __launch_bounds__(kThreads, 1)
         break;
       }
       tc_fence_after_sync();
-      uint32_t orr[D / 32][32];
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) tmem_ld32_nowait(tO + c * 32, orr[c]);
-      tmem_ld_wait_tied(orr[0]);
-#pragma unroll
-      for (int c = 1; c < D / 32; ++c) tmem_reg_tie(orr[c]);
-      tc_fence_before_sync();
-      mbar_arrive(smem_u32(&bars->o_free[t]));
       const int qrow = w.q0 + 128 * t + r;
       const bool valid_row = qrow < p.q_valid;
       const float inv_l = 1.f / l;
+      // The warp stages its 32 normalised rows in its own rows of the P_t buffer, in the P
+      // layout (row r, 16-byte unit x of 64-column chunk c at c * 16384 + r * 128 +
+      // ((x ^ (r & 7)) * 16)), so no other warp reads or writes those bytes. It then writes
+      // them out one D * 2-byte row per store instruction instead of 32 scattered pieces.
+      // O_t is read 32 columns at a time and released once the last piece is in registers.
 #pragma unroll
-      for (int u = 0; u < D / 8; ++u) {          // 16-byte unit u: columns 8u .. 8u + 7
-        uint4 o = make_uint4(0, 0, 0, 0);
-        if (valid_row) {
-          const uint32_t* f = &orr[u >> 2][(u & 3) * 8];
-          o.x = pack_bf16x2(__uint_as_float(f[0]) * inv_l, __uint_as_float(f[1]) * inv_l);
-          o.y = pack_bf16x2(__uint_as_float(f[2]) * inv_l, __uint_as_float(f[3]) * inv_l);
-          o.z = pack_bf16x2(__uint_as_float(f[4]) * inv_l, __uint_as_float(f[5]) * inv_l);
-          o.w = pack_bf16x2(__uint_as_float(f[6]) * inv_l, __uint_as_float(f[7]) * inv_l);
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t orr[32];
+        tmem_ld32(tO + c * 32, orr);
+        if (c == D / 32 - 1) {
+          tc_fence_before_sync();
+          mbar_arrive(smem_u32(&bars->o_free[t]));
         }
-        *reinterpret_cast<uint4*>(p.out + ((static_cast<size_t>(w.b) * p.Sq + qrow) * p.H + w.h) * D + u * 8) = o;
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {         // columns 32c + 8q4 .. + 7: 16-byte unit 4c + q4
+          const int u = 4 * c + q4;
+          uint4 o = make_uint4(0, 0, 0, 0);
+          if (valid_row) {
+            const uint32_t* f = &orr[8 * q4];
+            o.x = pack_bf16x2(__uint_as_float(f[0]) * inv_l, __uint_as_float(f[1]) * inv_l);
+            o.y = pack_bf16x2(__uint_as_float(f[2]) * inv_l, __uint_as_float(f[3]) * inv_l);
+            o.z = pack_bf16x2(__uint_as_float(f[4]) * inv_l, __uint_as_float(f[5]) * inv_l);
+            o.w = pack_bf16x2(__uint_as_float(f[6]) * inv_l, __uint_as_float(f[7]) * inv_l);
+          }
+          sts128(p_row + static_cast<uint32_t>(u >> 3) * 16384u + ((static_cast<uint32_t>(u & 7) ^ p_sw) << 4), o);
+        }
       }
+      __syncwarp();
+      if (D == 128 || lane < 16) {               // lane: bytes 8 * lane .. of a row
+        const int r0 = r & ~31;                  // first row of this warp
+        const uint32_t chunk = static_cast<uint32_t>(lane >> 4) * 16384u;
+        const uint32_t unit = static_cast<uint32_t>((lane >> 1) & 7), half = static_cast<uint32_t>(lane & 1) * 8u;
+        // Stores in flight per lane: more helps short items (cross-attention: +13 % at four)
+        // and plain attention slightly; the workspace mode measured best at one.
+        constexpr int kStoreUnroll = (kMode == kModeRopeWs) ? 1 : 4;
+#pragma unroll kStoreUnroll
+        for (int i = 0; i < 32; ++i) {
+          const int rr = r0 + i;
+          const uint32_t src = sP + t * C::kPBytes + chunk + static_cast<uint32_t>(rr) * 128u +
+                               ((unit ^ static_cast<uint32_t>(rr & 7)) << 4) + half;
+          uint16_t* dst = p.out + ((static_cast<size_t>(w.b) * p.Sq + w.q0 + 128 * t + rr) * p.H + w.h) * D;
+          *reinterpret_cast<uint2*>(dst + lane * 4) = lds64(src);
+        }
+      }
+      __syncwarp();
       p.lse[(static_cast<size_t>(w.b) * p.Sq + qrow) * p.H + w.h] =
           valid_row ? (m_used + log2f(l)) * kLn2 : -INFINITY;
     }
