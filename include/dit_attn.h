@@ -128,10 +128,11 @@ int dit_attn_fwd(const void* q, const void* k, const void* v, int B, int Sq, int
 /* ---------------------------------------------------------------------------------------
  * dit_attn_fwd with RoPE, rotating every q and k row exactly once per call (same inputs,
  * outputs and numerics as dit_attn_fwd with tables). The launch first rotates the valid rows
- * of q and k with the given tables into fp16 copies in `workspace` (all CTAs; the loads of
- * the rotated rows wait until every CTA has finished, so the launch is cooperative), then runs
- * the attention on those copies. Without a
- * workspace, dit_attn_fwd rotates each k tile again in every CTA that loads it.
+ * of k with the given tables into an fp16 copy in `workspace` (all CTAs; the loads of the
+ * rotated rows wait until every CTA has finished, so the launch is cooperative). It then runs
+ * the attention on that copy; each q tile, loaded once per CTA that uses it, is rotated in
+ * shared memory as it lands. Without a workspace, dit_attn_fwd rotates each k tile again in
+ * every CTA that loads it.
  *
  * workspace: device buffer of at least dit_attn_workspace_bytes(B, Sq, Skv, H, D) bytes,
  * 256-byte aligned, owned by the caller; its contents on entry do not matter and are
@@ -160,8 +161,9 @@ int dit_attn_fwd_ws(const void* q, const void* k, const void* v, int B, int Sq, 
  *
  * Scratch: a fixed array of DIT_ATTN_STATIC_SCRATCH_BYTES (96 MiB) of device memory,
  * declared in the library at file scope. The CUDA runtime reserves it on each device where
- * it loads the library's device code. The size fits the Wan 480p self-attention (B1, 4736
- * query and key rows, H40, D128), which needs 92.5 MiB.
+ * it loads the library's device code. The workspace holds the rotated keys: the Wan 480p
+ * self-attention (B1, 4736 key rows, H40, D128) needs 46.25 MiB, and the array fits up to
+ * 9728 key rows at H40, D128.
  *
  * Set-up: the first call on each device looks up the array's device address with that
  * device current, once, under a lock. Make that first call outside any stream capture.

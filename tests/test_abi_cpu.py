@@ -153,9 +153,9 @@ def test_static_scratch_entry_rejects_oversized_problems_before_any_cuda_call(cl
         [ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
     ws = clib.dit_attn_workspace_bytes
     ws.restype = ctypes.c_size_t
-    assert ws(1, 4992, 4992, 40, 128) > 96 << 20 >= ws(1, 4736, 4736, 40, 128)
-    assert fn(None, None, None, 1, 4992, 4992, 40, 128, 4992, 4992, None, None, None, None,
-              0.125, None, None, None) == -2            # DIT_ERR_UNSUPPORTED: needs 97.5 MiB
+    assert ws(1, 9856, 9856, 40, 128) > 96 << 20 >= ws(1, 9728, 9728, 40, 128) >= ws(1, 4736, 4736, 40, 128)
+    assert fn(None, None, None, 1, 9856, 9856, 40, 128, 9856, 9856, None, None, None, None,
+              0.125, None, None, None) == -2            # DIT_ERR_UNSUPPORTED: needs 96.25 MiB
     assert fn(None, None, None, 0, 128, 128, 1, 128, 1, 1, None, None, None, None,
               0.125, None, None, None) == -1            # DIT_ERR_INVALID_ARG
     assert fn(None, None, None, 1, 128, 128, 1, 96, 1, 1, None, None, None, None,

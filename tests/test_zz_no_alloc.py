@@ -73,7 +73,7 @@ def test_static_scratch_same_shape_twice(lib):
 
 
 def test_static_scratch_rejects_problems_beyond_its_size(lib):
-    B, S, H, D = 1, 4992, 40, 128            # needs 97.5 MiB > 96 MiB
+    B, S, H, D = 1, 9856, 40, 128            # 96.25 MiB of rotated keys > 96 MiB
     assert lib.dit_attn_workspace_bytes(B, S, S, H, D) > lib.DIT_ATTN_STATIC_SCRATCH_BYTES
     x = torch.zeros((B, S, H, D), dtype=torch.bfloat16, device="cuda")
     t = torch.zeros((S, D // 2), dtype=torch.float32, device="cuda")

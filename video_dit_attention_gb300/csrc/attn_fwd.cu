@@ -110,13 +110,11 @@ struct KParams {
   float* lse;
 };
 
-// Workspace-mode parameters: raw inputs, their rotated fp16 copies (which the TMA maps of q
-// and k point at) and the count of CTAs done rotating (zeroed before launch). Kept apart
-// from KParams so the other modes' parameter block stays small.
+// Workspace-mode parameters: the raw keys, their rotated fp16 copy (which the TMA map of k
+// points at) and the count of CTAs done rotating (zeroed before launch). Kept apart from
+// KParams so the other modes' parameter block stays small.
 struct WsParams {
-  const uint16_t* q_raw;
   const uint16_t* k_raw;
-  uint16_t* q_rot;
   uint16_t* k_rot;
   unsigned int* rotated;
   int B;
@@ -313,6 +311,29 @@ __device__ __forceinline__ void rotate_rows_fp16(const uint16_t* __restrict__ x,
         }
       }
     }
+  }
+}
+
+// Rotates, in place and into fp16, a landed [128 x D] bf16 tile in shared memory (128-byte
+// swizzle; D = 128: two 64-column sub-tiles, pair (i, i + 64) at the same offset of both;
+// D = 64: pair (i, i + 32) in units x and x + 4 of one row) with table rows cos_t / sin_t
+// [128, D/2] read from global memory. NT threads, this one is number `at`.
+template <int D, int NT>
+__device__ __forceinline__ void rotate_tile_smem(uint32_t tile, const float* __restrict__ cos_t,
+                                                 const float* __restrict__ sin_t, int at) {
+  constexpr int kHalf = D / 2, kUnits = kHalf / 8;   // 8-pair units per row
+#pragma unroll 2
+  for (int i = at; i < 128 * kUnits; i += NT) {
+    const int row = i / kUnits, x = i % kUnits;
+    const uint32_t offa = sw128_offset(row, x);
+    const uint32_t offb = (D == 128) ? 16384u + offa : sw128_offset(row, x + 4);
+    const float* ct = cos_t + row * kHalf + x * 8;
+    const float* st = sin_t + row * kHalf + x * 8;
+    uint4 a = lds128(tile + offa), b = lds128(tile + offb);
+    rotate8(a, b, __ldg(reinterpret_cast<const float4*>(ct)), __ldg(reinterpret_cast<const float4*>(ct + 4)),
+            __ldg(reinterpret_cast<const float4*>(st)), __ldg(reinterpret_cast<const float4*>(st + 4)));
+    sts128(tile + offa, a);
+    sts128(tile + offb, b);
   }
 }
 
@@ -813,12 +834,10 @@ template <int D, int kMode>
 cudaError_t launch_mode(const AttnArgs& a) {
   CUtensorMap mq, mk, mv;
   const int qext = a.q_valid > 0 ? a.q_valid : 1;
-  // Workspace mode: the q/k TMA maps read the rotated fp16 copies (2-byte elements either way).
-  const size_t q_elems = static_cast<size_t>(a.B) * a.Sq * a.H * D;
-  const size_t q_bytes = (q_elems * 2 + 255) / 256 * 256;
-  uint16_t* q_rot = kMode == kModeRopeWs ? static_cast<uint16_t*>(a.workspace) : nullptr;
-  uint16_t* k_rot = kMode == kModeRopeWs ? reinterpret_cast<uint16_t*>(static_cast<char*>(a.workspace) + q_bytes) : nullptr;
-  const void* q_src = kMode == kModeRopeWs ? static_cast<const void*>(q_rot) : a.q;
+  // Workspace mode: the k TMA map reads the rotated fp16 copy (2-byte elements either way);
+  // q is loaded raw and rotated in shared memory.
+  uint16_t* k_rot = kMode == kModeRopeWs ? static_cast<uint16_t*>(a.workspace) : nullptr;
+  const void* q_src = a.q;
   const void* k_src = kMode == kModeRopeWs ? static_cast<const void*>(k_rot) : a.k;
   // Cross-attention reads up to Skv rows and masks per batch on the device; self-attention
   // cuts the key/value extent to the valid length so pad rows are never even loaded.
@@ -853,15 +872,13 @@ cudaError_t launch_mode(const AttnArgs& a) {
   p.out = static_cast<uint16_t*>(a.out);
   p.lse = a.lse;
   WsParams ws;
-  ws.q_raw = static_cast<const uint16_t*>(a.q);
   ws.k_raw = static_cast<const uint16_t*>(a.k);
-  ws.q_rot = q_rot;
   ws.k_rot = k_rot;
   ws.rotated = nullptr;
   ws.B = a.B;
   if (kMode == kModeRopeWs) {
     const size_t k_bytes = (static_cast<size_t>(a.B) * a.Skv * a.H * D * 2 + 255) / 256 * 256;
-    ws.rotated = reinterpret_cast<unsigned int*>(static_cast<char*>(a.workspace) + q_bytes + k_bytes);
+    ws.rotated = reinterpret_cast<unsigned int*>(static_cast<char*>(a.workspace) + k_bytes);
   }
   static const int sm_count = [] {
     int dev = 0, n = 0;
@@ -899,9 +916,9 @@ cudaError_t launch_mode(const AttnArgs& a) {
 }  // namespace
 
 size_t attn_workspace_bytes(int B, int Sq, int Skv, int H, int D) {
-  const size_t q = (static_cast<size_t>(B) * Sq * H * D * 2 + 255) / 256 * 256;
+  (void)Sq;   // q is rotated in shared memory, tile by tile
   const size_t k = (static_cast<size_t>(B) * Skv * H * D * 2 + 255) / 256 * 256;
-  return q + k + 256;   // + the counter of CTAs done rotating
+  return k + 256;   // + the counter of CTAs done rotating
 }
 
 cudaError_t launch_attn_fwd(const AttnArgs& a, AttnMode mode) {

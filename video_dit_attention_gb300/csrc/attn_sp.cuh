@@ -42,7 +42,7 @@ struct CfgSp {
 };
 
 struct BarsSp {
-  uint64_t q_full, q_empty;
+  uint64_t q_full, q_ready, q_empty;
   uint64_t r_full[6], r_ready[6], r_empty[6];
   uint64_t s_full[2], s_free[2], p_full[2], pv_done[2], o_free[2];
   uint64_t drain[2];
@@ -78,10 +78,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abort_flag = &bars->abort;
   unsigned int* status = &g_dit_status;
   const uint32_t b_q_full = smem_u32(&bars->q_full), b_q_empty = smem_u32(&bars->q_empty);
+  const uint32_t b_q_ready = smem_u32(&bars->q_ready);
 
   if (tid == 0) {
     bars->abort = 0;
     mbar_init(b_q_full, 1);
+    mbar_init(b_q_ready, 1);
     mbar_init(b_q_empty, 1);
     for (int s = 0; s < R; ++s) {
       mbar_init(smem_u32(&bars->r_full[s]), 1);
@@ -112,27 +114,58 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tbase = bars->tmem_base;
-  if (kMode == kModeRopeWs) {
-    // ---------------------------------------------------- rotate q and k once, every thread
-    // The rotated rows are published through a counter: each thread's generic-proxy stores
-    // are fenced against the async proxy (the TMA loads that read them), then the CTA counts
-    // itself in with a device-scope release. Only the producers wait for the count.
-    const int gtid = blockIdx.x * kThreads + tid, gthreads = gridDim.x * kThreads;
-    rotate_rows_fp16<D>(ws.q_raw, ws.q_rot, p.cos_q, p.sin_q, ws.B, p.Sq, p.q_valid, p.H, gtid, gthreads);
-    rotate_rows_fp16<D>(ws.k_raw, ws.k_rot, p.cos_k, p.sin_k, ws.B, p.Skv, p.kv_valid, p.H, gtid, gthreads);
-    fence_proxy_async_all();
-    __syncthreads();
-    if (tid == 0) {
-      __threadfence();
-      atomicAdd(ws.rotated, 1u);
-    }
-  }
   const int it0 = blockIdx.x, it_step = gridDim.x;
   // First item at or after `it` (in this CTA's sequence) that has work.
   auto first_live = [&](int it) -> int {
     while (it < p.n_items && decode_item<kMode>(p, it).n_live == 0) it += it_step;
     return it;
   };
+  // Workspace mode: items whose Q was loaded and rotated before the roles start (0 or 1).
+  int pre_q = 0;
+  if (kMode == kModeRopeWs) {
+    // ------------------------------------------------- rotate k once; the first Q meanwhile
+    // Warps 0-13 rotate this CTA's share of the k rows. The rotated rows are published through
+    // a counter: each thread's generic-proxy stores are fenced against the async proxy (the
+    // TMA loads that read them), then the CTA counts itself in with a device-scope release;
+    // only the K/V producer waits for the count. Meanwhile warps 14-15 rotate the first
+    // item's Q tiles in shared memory (later ones as they land, in their role below).
+    const int fit = first_live(it0);
+    Item fw{};
+    if (fit < p.n_items) {
+      fw = decode_item<kMode>(p, fit);
+      pre_q = 1;
+    }
+    if (pre_q && tid == 0) {
+      mbar_arrive_expect_tx(b_q_full, fw.n_live * C::kTileBytes);
+      for (int t = 0; t < fw.n_live; ++t)
+#pragma unroll
+        for (int c = 0; c < C::kSub; ++c)
+          tma_load_4d(sQ + t * C::kTileBytes + c * 16384, &tm_q, b_q_full, c * 64, fw.h,
+                      fw.q0 + 128 * t, fw.b);
+    }
+    constexpr int kRotK = kThreads - 64;   // threads of warps 0-13
+    if (warp >= 14) {
+      const int at = tid - kRotK;
+      if (pre_q && group_wait<64>(b_q_full, 0, abort_flag, status, kStatusTimeoutRope, &bars->aux_go, at)) {
+        for (int t = 0; t < fw.n_live; ++t) {
+          const size_t row0 = static_cast<size_t>(fw.q0 + 128 * t) * (D / 2);
+          rotate_tile_smem<D, 64>(sQ + t * C::kTileBytes, p.cos_q + row0, p.sin_q + row0, at);
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(1, 64);
+        if (at == 0) mbar_arrive(b_q_ready);
+      }
+    } else {
+      rotate_rows_fp16<D>(ws.k_raw, ws.k_rot, p.cos_k, p.sin_k, ws.B, p.Skv, p.kv_valid, p.H,
+                          blockIdx.x * kRotK + tid, gridDim.x * kRotK);
+      fence_proxy_async_all();
+    }
+    __syncthreads();
+    if (tid == 0) {
+      __threadfence();
+      atomicAdd(ws.rotated, 1u);
+    }
+  }
   // Workspace mode: a producer waits, before its first load, until every CTA has counted in
   // its share of the rotation (`ready` remembers that it has).
   auto wait_rotated = [&](bool& ready) -> bool {
@@ -178,7 +211,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int it = it0; ok && it < p.n_items; it += it_step) {
       const Item w = decode_item<kMode>(p, it);
       if (w.n_live == 0) continue;
-      if (!(ok = wait_bar(b_q_full, q_cnt))) break;
+      // Workspace mode: Q is used once warps 14-15 have rotated it in shared memory.
+      if (!(ok = wait_bar(kMode == kModeRopeWs ? b_q_ready : b_q_full, q_cnt))) break;
       for (int j = 0; ok && j < w.n_kv; ++j) {
         const int g = g0 + j;
         const int n = ring_load_k(g), slot = n % R;
@@ -264,18 +298,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     regs_dec<40>();
     if (warp == 0 && lane == 0) {
       // ------------------------------------------------------------ producer: Q
-      int q_cnt = 0;
-      bool ready = false;
+      int q_cnt = pre_q;
+      bool skip = pre_q != 0;   // the first item's Q is already loaded
       bool ok = true;
       for (int it = it0; ok && it < p.n_items; it += it_step) {
         const Item w = decode_item<kMode>(p, it);
         if (w.n_live == 0) continue;
+        if (skip) {
+          skip = false;
+          continue;
+        }
         // The Q buffers are free once every S MMA of the previous item has completed.
         if (q_cnt > 0 && !(ok = bounded_wait(b_q_empty, (q_cnt - 1) & 1, abort_flag, status,
                                              kStatusTimeoutLoad)))
           break;
-        ok = wait_rotated(ready);
-        if (!ok) break;
         mbar_arrive_expect_tx(b_q_full, w.n_live * C::kTileBytes);
         for (int t = 0; t < w.n_live; ++t)
 #pragma unroll
@@ -527,6 +563,33 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) s_issuer();
     } else if (warp == 13) {
       if (lane == 0) pv_issuer();
+    } else if (kMode == kModeRopeWs) {
+      // ---------------------------------------------------------- Q rotation (warps 14-15)
+      constexpr int kRotThreads = 64;
+      const int at = tid - 448;
+      volatile int* go = &bars->aux_go;
+      int q_cnt = pre_q;
+      bool skip = pre_q != 0;   // the first item's Q was rotated before the roles started
+      bool ok = true;
+      for (int it = it0; ok && it < p.n_items; it += it_step) {
+        const Item w = decode_item<kMode>(p, it);
+        if (w.n_live == 0) continue;
+        if (skip) {
+          skip = false;
+          continue;
+        }
+        if (!(ok = group_wait<kRotThreads>(b_q_full, q_cnt & 1, abort_flag, status, kStatusTimeoutRope,
+                                           go, at)))
+          break;
+        for (int t = 0; t < w.n_live; ++t) {
+          const size_t row0 = static_cast<size_t>(w.q0 + 128 * t) * (D / 2);
+          rotate_tile_smem<D, kRotThreads>(sQ + t * C::kTileBytes, p.cos_q + row0, p.sin_q + row0, at);
+        }
+        fence_proxy_async_smem();
+        named_bar_sync(1, kRotThreads);
+        if (at == 0) mbar_arrive(b_q_ready);
+        ++q_cnt;
+      }
     } else if (kMode == kModeCross) {
       // ---------------------------------------------------------- V pad rows (warps 14-15)
       // K/V tiles are loaded up to Skv rows; rows past the batch's valid length are zeroed so
