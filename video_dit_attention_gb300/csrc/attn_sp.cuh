@@ -216,7 +216,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; ok && j < w.n_kv; ++j) {
         const int g = g0 + j;
         const int n = ring_load_k(g), slot = n % R;
-        if (!(ok = wait_bar(smem_u32(&bars->r_full[slot]), n / R))) break;
+        // Cross-attention: K too waits for the V-zeroing group (which passes every ring load
+        // in order), so that no slot is refilled before that group has seen its load.
+        if (!(ok = wait_bar(kMode == kModeCross ? smem_u32(&bars->r_ready[slot]) : smem_u32(&bars->r_full[slot]),
+                            n / R)))
+          break;
         const uint64_t db = smem_desc_sw128(sR + slot * C::kTileBytes, 16, 1024);
         for (int t = 0; t < w.n_live; ++t) {
           // S_t may be overwritten once the softmax has taken the previous S_t out of TMEM.
@@ -593,8 +597,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (kMode == kModeCross) {
       // ---------------------------------------------------------- V pad rows (warps 14-15)
       // K/V tiles are loaded up to Skv rows; rows past the batch's valid length are zeroed so
-      // that 0 * (pad contents) cannot reach O. Every ring load passes through here in order
-      // (K loads unchanged), so r_ready completes once per load, like r_full.
+      // that 0 * (pad contents) cannot reach O. Every ring load passes through here in order (K
+      // loads unchanged), and both issuers wait for r_ready, which therefore completes once per
+      // load like r_full. A slot is refilled only after its load was used, which needed
+      // r_ready, so this group never sees a slot's r_full move on by more than one phase.
       constexpr int kZeroThreads = 64;
       const int at = tid - 448;
       volatile int* go = &bars->aux_go;
