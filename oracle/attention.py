@@ -27,6 +27,7 @@ from __future__ import annotations
 
 import numpy as np
 
+from .qknorm import rms_norm_heads
 from .rope import rope_split_halves
 
 
@@ -53,7 +54,7 @@ def _rows_attention(qt: np.ndarray, kt: np.ndarray, vt: np.ndarray, scale: float
 
 
 def attention(q, k, v, q_valid, kv_valid, scale, angles_q=None, angles_k=None,
-              rows=None, heads=None):
+              rows=None, heads=None, norm_q=None, norm_k=None, eps=1e-6):
     """Masked softmax attention over BSHD tensors.
 
     q: [B, Sq, H, D]; k, v: [B, Skv, H, D] (any float dtype; upcast to fp64).
@@ -62,6 +63,8 @@ def attention(q, k, v, q_valid, kv_valid, scale, angles_q=None, angles_k=None,
     angles_q [Sq, D/2], angles_k [Skv, D/2]: RoPE angles per row, or None for no RoPE.
     rows: optional iterable of query rows to evaluate (default: all Sq rows).
     heads: optional iterable of heads to evaluate (default: all).
+    norm_q / norm_k [D]: per-head RMSNorm weights applied to q / k before the rotation
+    (oracle.qknorm), or None for no norm; eps is the norm's epsilon.
 
     Returns (O [B, len(rows), len(heads), D] fp64, LSE [B, len(rows), len(heads)] fp64).
     """
@@ -85,6 +88,10 @@ def attention(q, k, v, q_valid, kv_valid, scale, angles_q=None, angles_k=None,
         kb = k[b:b + 1, :L][:, :, heads].astype(np.float64)
         vb = v[b, :L][:, heads].astype(np.float64)
         qb = q[b:b + 1, qrows][:, :, heads].astype(np.float64)
+        if norm_k is not None:
+            kb = rms_norm_heads(kb, norm_k, eps)
+        if norm_q is not None:
+            qb = rms_norm_heads(qb, norm_q, eps)
         if angles_k is not None:
             kb = rope_split_halves(kb, angles_k[:L])
         if angles_q is not None:
