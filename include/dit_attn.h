@@ -150,6 +150,35 @@ int dit_attn_fwd_ws(const void* q, const void* k, const void* v, int B, int Sq, 
                     size_t workspace_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------------------
+ * dit_attn_fwd_ws with a per-head RMSNorm of q and k ahead of the rotation (Difflet PR #153,
+ * FLUX and Wan split-RoPE commits: the per-head q/k RMSNorm weights are permuted with the
+ * q/k channels into the split-halves order, so the norm acts in that layout just before the
+ * rotation). For each (b, s, h) row of q (weights norm_q) and of k (norm_k):
+ *   n = x / sqrt(mean_d(x_d^2) + eps) * w,  then the split-halves rotation of n,
+ * computed in fp32 from the bf16 inputs and rounded to fp16 for the tensor-core product, as
+ * in dit_attn_fwd_ws. norm_q, norm_k: device fp32 [D], 16-byte aligned, in the same channel
+ * order as q and k. eps >= 0 and finite (models normally use 1e-6). Workspace, tables,
+ * layouts, outputs and the remaining errors as dit_attn_fwd_ws; DIT_ERR_INVALID_ARG also for a
+ * missing weight vector or a bad eps, DIT_ERR_ALIGNMENT for a misaligned weight vector.
+ * ------------------------------------------------------------------------------------- */
+int dit_attn_fwd_ws_qknorm(const void* q, const void* k, const void* v, int B, int Sq, int Skv,
+                           int H, int D, int q_valid_len, int kv_valid_len, const float* norm_q,
+                           const float* norm_k, float eps, const float* cos_q, const float* sin_q,
+                           const float* cos_k, const float* sin_k, float softmax_scale, void* out,
+                           float* lse, void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------------------
+ * Standalone per-head RMSNorm then split-halves RoPE (the prologue dit_attn_fwd_ws_qknorm
+ * fuses): y[b,s,h,:] = rotate(x[b,s,h,:] / sqrt(mean(x^2) + eps) * w) with table row s.
+ * x, y: [B, S, H, D] bf16 (y may equal x); w: device fp32 [D]; cos, sin: [S, D/2] fp32.
+ * Arithmetic in fp32, one rounding to bf16 at the end.
+ * Errors: DIT_ERR_INVALID_ARG (null, sizes < 1, bad eps), DIT_ERR_UNSUPPORTED (D not 64/128),
+ * DIT_ERR_ALIGNMENT (any pointer not 16-byte aligned), DIT_ERR_CUDA.
+ * ------------------------------------------------------------------------------------- */
+int dit_qk_rmsnorm_rope(const void* x, void* y, const float* w, float eps, const float* cos,
+                        const float* sin, int B, int S, int H, int D, void* stream);
+
+/* ---------------------------------------------------------------------------------------
  * dit_attn_fwd_ws without a caller-supplied workspace. The pages have no counterpart: this
  * is a library convenience, not part of the method.
  *

@@ -133,7 +133,7 @@ extern "C" int dit_attn_fwd(const void* q, const void* k, const void* v, int B, 
                         !aligned(sin_k, 16)))
     return DIT_ERR_ALIGNMENT;
   AttnArgs a{q, k, v, B, Sq, Skv, H, D, q_valid_len, kv_valid_len, nullptr,
-             cos_q, sin_q, cos_k, sin_k, softmax_scale, out, lse, nullptr,
+             cos_q, sin_q, cos_k, sin_k, softmax_scale, out, lse, nullptr, nullptr, nullptr, 0.f,
              static_cast<cudaStream_t>(stream)};
   return cuda_status(launch_attn_fwd(a, n_tables == 4 ? kModeRope : kModePlain));
 }
@@ -159,9 +159,43 @@ extern "C" int dit_attn_fwd_ws(const void* q, const void* k, const void* v, int 
       !aligned(workspace, 256))
     return DIT_ERR_ALIGNMENT;
   AttnArgs a{q, k, v, B, Sq, Skv, H, D, q_valid_len, kv_valid_len, nullptr,
-             cos_q, sin_q, cos_k, sin_k, softmax_scale, out, lse, workspace,
+             cos_q, sin_q, cos_k, sin_k, softmax_scale, out, lse, workspace, nullptr, nullptr, 0.f,
              static_cast<cudaStream_t>(stream)};
   return cuda_status(launch_attn_fwd(a, kModeRopeWs));
+}
+
+extern "C" int dit_attn_fwd_ws_qknorm(const void* q, const void* k, const void* v, int B, int Sq,
+                                      int Skv, int H, int D, int q_valid_len, int kv_valid_len,
+                                      const float* norm_q, const float* norm_k, float eps,
+                                      const float* cos_q, const float* sin_q, const float* cos_k,
+                                      const float* sin_k, float softmax_scale, void* out, float* lse,
+                                      void* workspace, size_t workspace_bytes, void* stream) {
+  int st = check_attn_shapes(q, k, v, B, Sq, Skv, H, D, q_valid_len, softmax_scale, out, lse);
+  if (st != DIT_OK) return st;
+  if (kv_valid_len < 0 || kv_valid_len > Skv) return DIT_ERR_INVALID_ARG;
+  if (!cos_q || !sin_q || !cos_k || !sin_k || !workspace || !norm_q || !norm_k) return DIT_ERR_INVALID_ARG;
+  if (!(eps >= 0.f) || !std::isfinite(eps)) return DIT_ERR_INVALID_ARG;
+  if (workspace_bytes < attn_workspace_bytes(B, Sq, Skv, H, D)) return DIT_ERR_INVALID_ARG;
+  if (static_cast<long long>(Sq > Skv ? Sq : Skv) * H * (D / 16) >= (1ll << 30)) return DIT_ERR_UNSUPPORTED;
+  if (!aligned(cos_q, 16) || !aligned(sin_q, 16) || !aligned(cos_k, 16) || !aligned(sin_k, 16) ||
+      !aligned(norm_q, 16) || !aligned(norm_k, 16) || !aligned(workspace, 256))
+    return DIT_ERR_ALIGNMENT;
+  AttnArgs a{q, k, v, B, Sq, Skv, H, D, q_valid_len, kv_valid_len, nullptr,
+             cos_q, sin_q, cos_k, sin_k, softmax_scale, out, lse, workspace, norm_q, norm_k, eps,
+             static_cast<cudaStream_t>(stream)};
+  return cuda_status(launch_attn_fwd(a, kModeRopeWsNorm));
+}
+
+extern "C" int dit_qk_rmsnorm_rope(const void* x, void* y, const float* w, float eps,
+                                   const float* cos_tab, const float* sin_tab, int B, int S, int H,
+                                   int D, void* stream) {
+  if (!x || !y || !w || !cos_tab || !sin_tab || B < 1 || S < 1 || H < 1) return DIT_ERR_INVALID_ARG;
+  if (!(eps >= 0.f) || !std::isfinite(eps)) return DIT_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return DIT_ERR_UNSUPPORTED;
+  if (!aligned(x, 16) || !aligned(y, 16) || !aligned(w, 16) || !aligned(cos_tab, 16) || !aligned(sin_tab, 16))
+    return DIT_ERR_ALIGNMENT;
+  return cuda_status(launch_qk_rmsnorm_rope(x, y, w, eps, cos_tab, sin_tab, B, S, H, D,
+                                            static_cast<cudaStream_t>(stream)));
 }
 
 extern "C" int dit_cross_attn_shortkv(const void* q, const void* k, const void* v, int B, int Sq,
@@ -174,8 +208,8 @@ extern "C" int dit_cross_attn_shortkv(const void* q, const void* k, const void* 
   if (Skv > 512) return DIT_ERR_UNSUPPORTED;
   if (!aligned(kv_valid_len_dev, 4)) return DIT_ERR_ALIGNMENT;
   AttnArgs a{q, k, v, B, Sq, Skv, H, D, q_valid_len, Skv, kv_valid_len_dev,
-             nullptr, nullptr, nullptr, nullptr, softmax_scale, out, lse, nullptr,
-             static_cast<cudaStream_t>(stream)};
+             nullptr, nullptr, nullptr, nullptr, softmax_scale, out, lse, nullptr, nullptr, nullptr,
+             0.f, static_cast<cudaStream_t>(stream)};
   return cuda_status(launch_attn_fwd(a, kModeCross));
 }
 

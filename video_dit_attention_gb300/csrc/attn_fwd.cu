@@ -48,6 +48,7 @@
 #include "common.h"
 #include "exp2_fma.cuh"
 #include "ptx.cuh"
+#include "qknorm.cuh"
 
 namespace dit {
 
@@ -118,7 +119,15 @@ struct WsParams {
   uint16_t* k_rot;
   unsigned int* rotated;
   int B;
+  const float* norm_q;   // per-head q/k RMSNorm weights [D] (norm mode only)
+  const float* norm_k;
+  float norm_eps;
 };
+
+// The two RoPE workspace modes (without and with the q/k RMSNorm).
+__host__ __device__ constexpr bool is_ws_mode(int mode) {
+  return mode == kModeRopeWs || mode == kModeRopeWsNorm;
+}
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;
@@ -332,6 +341,76 @@ __device__ __forceinline__ void rotate_tile_smem(uint32_t tile, const float* __r
     uint4 a = lds128(tile + offa), b = lds128(tile + offb);
     rotate8(a, b, __ldg(reinterpret_cast<const float4*>(ct)), __ldg(reinterpret_cast<const float4*>(ct + 4)),
             __ldg(reinterpret_cast<const float4*>(st)), __ldg(reinterpret_cast<const float4*>(st + 4)));
+    sts128(tile + offa, a);
+    sts128(tile + offb, b);
+  }
+}
+
+// rotate_rows_fp16 with the per-head RMSNorm (weights w [D], eps) applied first. The D/16
+// threads of a row are adjacent lanes; they reduce its sum of squares with shuffles, so the
+// loop advances whole warps together (gtid's warp-aligned base) and every lane joins each
+// shuffle (a group is either a whole row or past the end). gthreads is a multiple of 32.
+template <int D>
+__device__ __forceinline__ void rotate_rows_fp16_norm(const uint16_t* __restrict__ x, uint16_t* __restrict__ y,
+                                                      const float* __restrict__ cos_t,
+                                                      const float* __restrict__ sin_t,
+                                                      const float* __restrict__ w, float eps, int B,
+                                                      int S_rows, int valid, int H, int gtid, int gthreads) {
+  constexpr int kHalf = D / 2, kChunks = kHalf / 8;
+  const int per_b = valid * H * kChunks;
+  const int lane = gtid & 31;
+  for (int b = 0; b < B; ++b) {
+    const size_t boff = static_cast<size_t>(b) * S_rows * H * D;
+    for (int base = gtid - lane; base < per_b; base += gthreads) {
+      const int i = base + lane;
+      const bool live = i < per_b;
+      const int ch = i % kChunks, rh = live ? i / kChunks : 0, srow = rh / H;
+      const size_t off = boff + static_cast<size_t>(rh) * D + ch * 8;
+      uint4 a = make_uint4(0, 0, 0, 0), bb = make_uint4(0, 0, 0, 0);
+      if (live) {
+        a = *reinterpret_cast<const uint4*>(x + off);
+        bb = *reinterpret_cast<const uint4*>(x + off + kHalf);
+      }
+      float ss = sumsq16(a, bb);
+#pragma unroll
+      for (int o = 1; o < kChunks; o <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      if (live) {
+        float wa[8], wb[8], cs[8], sn[8];
+        load8f(w + ch * 8, wa);
+        load8f(w + kHalf + ch * 8, wb);
+        load8f(cos_t + static_cast<size_t>(srow) * kHalf + ch * 8, cs);
+        load8f(sin_t + static_cast<size_t>(srow) * kHalf + ch * 8, sn);
+        norm_rotate8<true>(a, bb, rsqrtf(ss * (1.f / D) + eps), wa, wb, cs, sn);
+        *reinterpret_cast<uint4*>(y + off) = a;
+        *reinterpret_cast<uint4*>(y + off + kHalf) = bb;
+      }
+    }
+  }
+}
+
+// rotate_tile_smem with the per-head RMSNorm applied first (NT a multiple of 32: every lane
+// runs the same iterations, and the D/16 lanes of a row reduce its sum of squares).
+template <int D, int NT>
+__device__ __forceinline__ void rotate_tile_smem_norm(uint32_t tile, const float* __restrict__ cos_t,
+                                                      const float* __restrict__ sin_t,
+                                                      const float* __restrict__ w, float eps, int at) {
+  constexpr int kHalf = D / 2, kUnits = kHalf / 8;
+  static_assert(NT % 32 == 0 && (128 * kUnits) % NT == 0, "whole warps, whole rows");
+#pragma unroll 1
+  for (int i = at; i < 128 * kUnits; i += NT) {
+    const int row = i / kUnits, x = i % kUnits;
+    const uint32_t offa = sw128_offset(row, x);
+    const uint32_t offb = (D == 128) ? 16384u + offa : sw128_offset(row, x + 4);
+    uint4 a = lds128(tile + offa), b = lds128(tile + offb);
+    float ss = sumsq16(a, b);
+#pragma unroll
+    for (int o = 1; o < kUnits; o <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    float wa[8], wb[8], cs[8], sn[8];
+    load8f(w + x * 8, wa);
+    load8f(w + kHalf + x * 8, wb);
+    load8f(cos_t + row * kHalf + x * 8, cs);
+    load8f(sin_t + row * kHalf + x * 8, sn);
+    norm_rotate8<true>(a, b, rsqrtf(ss * (1.f / D) + eps), wa, wb, cs, sn);
     sts128(tile + offa, a);
     sts128(tile + offb, b);
   }
@@ -836,9 +915,9 @@ cudaError_t launch_mode(const AttnArgs& a) {
   const int qext = a.q_valid > 0 ? a.q_valid : 1;
   // Workspace mode: the k TMA map reads the rotated fp16 copy (2-byte elements either way);
   // q is loaded raw and rotated in shared memory.
-  uint16_t* k_rot = kMode == kModeRopeWs ? static_cast<uint16_t*>(a.workspace) : nullptr;
+  uint16_t* k_rot = is_ws_mode(kMode) ? static_cast<uint16_t*>(a.workspace) : nullptr;
   const void* q_src = a.q;
-  const void* k_src = kMode == kModeRopeWs ? static_cast<const void*>(k_rot) : a.k;
+  const void* k_src = is_ws_mode(kMode) ? static_cast<const void*>(k_rot) : a.k;
   // Cross-attention reads up to Skv rows and masks per batch on the device; self-attention
   // cuts the key/value extent to the valid length so pad rows are never even loaded.
   const int kvext = (kMode == kModeCross) ? a.Skv : (a.kv_valid > 0 ? a.kv_valid : 1);
@@ -876,7 +955,10 @@ cudaError_t launch_mode(const AttnArgs& a) {
   ws.k_rot = k_rot;
   ws.rotated = nullptr;
   ws.B = a.B;
-  if (kMode == kModeRopeWs) {
+  ws.norm_q = a.norm_q;
+  ws.norm_k = a.norm_k;
+  ws.norm_eps = a.norm_eps;
+  if (is_ws_mode(kMode)) {
     const size_t k_bytes = (static_cast<size_t>(a.B) * a.Skv * a.H * D * 2 + 255) / 256 * 256;
     ws.rotated = reinterpret_cast<unsigned int*>(static_cast<char*>(a.workspace) + k_bytes);
   }
@@ -899,7 +981,7 @@ cudaError_t launch_mode(const AttnArgs& a) {
     auto kern = attn_sp_kernel<D, kMode>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, CfgSp<D>::kSmemBytes);
     if (e != cudaSuccess) return e;
-    if (kMode != kModeRopeWs) {
+    if (!is_ws_mode(kMode)) {
       kern<<<grid, kThreads, CfgSp<D>::kSmemBytes, a.stream>>>(mq, mk, mv, p, ws);
       return cudaGetLastError();
     }
@@ -924,11 +1006,13 @@ size_t attn_workspace_bytes(int B, int Sq, int Skv, int H, int D) {
 cudaError_t launch_attn_fwd(const AttnArgs& a, AttnMode mode) {
   if (a.D == 128) {
     if (mode == kModeRopeWs) return launch_mode<128, kModeRopeWs>(a);
+    if (mode == kModeRopeWsNorm) return launch_mode<128, kModeRopeWsNorm>(a);
     if (mode == kModeRope) return launch_mode<128, kModeRope>(a);
     if (mode == kModeCross) return launch_mode<128, kModeCross>(a);
     return launch_mode<128, kModePlain>(a);
   }
   if (mode == kModeRopeWs) return launch_mode<64, kModeRopeWs>(a);
+  if (mode == kModeRopeWsNorm) return launch_mode<64, kModeRopeWsNorm>(a);
   if (mode == kModeRope) return launch_mode<64, kModeRope>(a);
   if (mode == kModeCross) return launch_mode<64, kModeCross>(a);
   return launch_mode<64, kModePlain>(a);

@@ -62,7 +62,8 @@ template <int D, int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_sp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const KParams p, const WsParams ws) {
-  static_assert(kMode == kModePlain || kMode == kModeCross || kMode == kModeRopeWs, "mode");
+  static_assert(kMode == kModePlain || kMode == kModeCross || is_ws_mode(kMode), "mode");
+  constexpr bool kWs = is_ws_mode(kMode), kNorm = kMode == kModeRopeWsNorm;
   using C = CfgSp<D>;
   constexpr int R = C::kRing;
   extern __shared__ uint8_t smem_raw[];
@@ -122,7 +123,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
   // Workspace mode: items whose Q was loaded and rotated before the roles start (0 or 1).
   int pre_q = 0;
-  if (kMode == kModeRopeWs) {
+  if (kWs) {
     // ------------------------------------------------- rotate k once; the first Q meanwhile
     // Warps 0-13 rotate this CTA's share of the k rows. The rotated rows are published through
     // a counter: each thread's generic-proxy stores are fenced against the async proxy (the
@@ -149,15 +150,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (pre_q && group_wait<64>(b_q_full, 0, abort_flag, status, kStatusTimeoutRope, &bars->aux_go, at)) {
         for (int t = 0; t < fw.n_live; ++t) {
           const size_t row0 = static_cast<size_t>(fw.q0 + 128 * t) * (D / 2);
-          rotate_tile_smem<D, 64>(sQ + t * C::kTileBytes, p.cos_q + row0, p.sin_q + row0, at);
+          if (kNorm)
+            rotate_tile_smem_norm<D, 64>(sQ + t * C::kTileBytes, p.cos_q + row0, p.sin_q + row0, ws.norm_q,
+                                         ws.norm_eps, at);
+          else
+            rotate_tile_smem<D, 64>(sQ + t * C::kTileBytes, p.cos_q + row0, p.sin_q + row0, at);
         }
         fence_proxy_async_smem();
         named_bar_sync(1, 64);
         if (at == 0) mbar_arrive(b_q_ready);
       }
     } else {
-      rotate_rows_fp16<D>(ws.k_raw, ws.k_rot, p.cos_k, p.sin_k, ws.B, p.Skv, p.kv_valid, p.H,
-                          blockIdx.x * kRotK + tid, gridDim.x * kRotK);
+      if (kNorm)
+        rotate_rows_fp16_norm<D>(ws.k_raw, ws.k_rot, p.cos_k, p.sin_k, ws.norm_k, ws.norm_eps, ws.B, p.Skv,
+                                 p.kv_valid, p.H, blockIdx.x * kRotK + tid, gridDim.x * kRotK);
+      else
+        rotate_rows_fp16<D>(ws.k_raw, ws.k_rot, p.cos_k, p.sin_k, ws.B, p.Skv, p.kv_valid, p.H,
+                            blockIdx.x * kRotK + tid, gridDim.x * kRotK);
       fence_proxy_async_all();
     }
     __syncthreads();
@@ -169,7 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Workspace mode: a producer waits, before its first load, until every CTA has counted in
   // its share of the rotation (`ready` remembers that it has).
   auto wait_rotated = [&](bool& ready) -> bool {
-    if (kMode != kModeRopeWs || ready) return true;
+    if (!kWs || ready) return true;
     const uint64_t t0 = globaltimer_ns();
     while (ld_acquire_gpu(ws.rotated) < gridDim.x) {
       if (*abort_flag) return false;
@@ -205,14 +214,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
   auto s_issuer = [&]() {
     // ------------------------------------------------------------ S_t = Q_t K_g^T
-    constexpr uint32_t kIdS = idesc_f16kind_f32(128, 128, kMode != kModeRopeWs, false, false);
+    constexpr uint32_t kIdS = idesc_f16kind_f32(128, 128, !kWs, false, false);
     int g0 = 0, q_cnt = 0, ns0 = 0, ns1 = 0;
     bool ok = true;
     for (int it = it0; ok && it < p.n_items; it += it_step) {
       const Item w = decode_item<kMode>(p, it);
       if (w.n_live == 0) continue;
       // Workspace mode: Q is used once warps 14-15 have rotated it in shared memory.
-      if (!(ok = wait_bar(kMode == kModeRopeWs ? b_q_ready : b_q_full, q_cnt))) break;
+      if (!(ok = wait_bar(kWs ? b_q_ready : b_q_full, q_cnt))) break;
       for (int j = 0; ok && j < w.n_kv; ++j) {
         const int g = g0 + j;
         const int n = ring_load_k(g), slot = n % R;
@@ -547,7 +556,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t unit = static_cast<uint32_t>((lane >> 1) & 7), half = static_cast<uint32_t>(lane & 1) * 8u;
         // Stores in flight per lane: more helps short items (cross-attention: +13 % at four)
         // and plain attention slightly; the workspace mode measured best at one.
-        constexpr int kStoreUnroll = (kMode == kModeRopeWs) ? 1 : 4;
+        constexpr int kStoreUnroll = kWs ? 1 : 4;
 #pragma unroll kStoreUnroll
         for (int i = 0; i < 32; ++i) {
           const int rr = r0 + i;
@@ -567,7 +576,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) s_issuer();
     } else if (warp == 13) {
       if (lane == 0) pv_issuer();
-    } else if (kMode == kModeRopeWs) {
+    } else if (kWs) {
       // ---------------------------------------------------------- Q rotation (warps 14-15)
       constexpr int kRotThreads = 64;
       const int at = tid - 448;
@@ -587,7 +596,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         for (int t = 0; t < w.n_live; ++t) {
           const size_t row0 = static_cast<size_t>(w.q0 + 128 * t) * (D / 2);
-          rotate_tile_smem<D, kRotThreads>(sQ + t * C::kTileBytes, p.cos_q + row0, p.sin_q + row0, at);
+          if (kNorm)
+            rotate_tile_smem_norm<D, kRotThreads>(sQ + t * C::kTileBytes, p.cos_q + row0, p.sin_q + row0,
+                                                  ws.norm_q, ws.norm_eps, at);
+          else
+            rotate_tile_smem<D, kRotThreads>(sQ + t * C::kTileBytes, p.cos_q + row0, p.sin_q + row0, at);
         }
         fence_proxy_async_smem();
         named_bar_sync(1, kRotThreads);

@@ -24,7 +24,10 @@ struct AttnArgs {
   float scale;
   void* out;
   float* lse;
-  void* workspace;              // RoPE workspace mode: rotated fp16 q/k and a grid barrier
+  void* workspace;              // RoPE workspace modes: rotated fp16 k and a CTA counter
+  const float* norm_q;          // per-head q/k RMSNorm weights [D] (kModeRopeWsNorm)
+  const float* norm_k;
+  float norm_eps;
   cudaStream_t stream;
 };
 
@@ -33,14 +36,18 @@ enum AttnMode : int {
   kModeRope = 1,   // RoPE fused into the q/k tile load
   kModeCross = 2,  // no RoPE, per-batch kv length read on the device
   kModeRopeWs = 3, // RoPE applied once per q/k tile into a workspace, then attention on it
+  kModeRopeWsNorm = 4,  // as kModeRopeWs, with per-head q/k RMSNorm before the rotation
 };
 
-// Workspace layout of kModeRopeWs: rotated q [B, Sq, H, D] fp16, rotated k [B, Skv, H, D]
-// fp16, then a 256-byte block holding the grid barrier counter; every part 256-byte aligned.
+// Workspace layout of the RoPE workspace modes: rotated k [B, Skv, H, D] fp16, then a
+// 256-byte block holding the count of CTAs done rotating; both 256-byte aligned.
 size_t attn_workspace_bytes(int B, int Sq, int Skv, int H, int D);
 
 cudaError_t launch_attn_fwd(const AttnArgs& a, AttnMode mode);
 
+cudaError_t launch_qk_rmsnorm_rope(const void* x, void* y, const float* w, float eps,
+                                   const float* cos_tab, const float* sin_tab, int B, int S, int H,
+                                   int D, cudaStream_t stream);
 cudaError_t launch_rope_split_halves(const void* x, void* y, const float* cos_tab,
                                      const float* sin_tab, int B, int S, int H, int D,
                                      cudaStream_t stream);

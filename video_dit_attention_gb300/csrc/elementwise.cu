@@ -8,6 +8,7 @@
 #include "common.h"
 #include "exp2_fma.cuh"
 #include "ptx.cuh"
+#include "qknorm.cuh"
 
 namespace dit {
 namespace {
@@ -70,6 +71,51 @@ __global__ void __launch_bounds__(256) rope_split_halves_kernel(const uint16_t* 
     uint16_t* yr = y + row * D + ch * 8;
     *reinterpret_cast<uint4*>(yr) = make_uint4(ya[0], ya[1], ya[2], ya[3]);
     *reinterpret_cast<uint4*>(yr + kHalf) = make_uint4(yb[0], yb[1], yb[2], yb[3]);
+  }
+}
+
+// ------------------------------------------------------------------------------------
+// Per-head RMSNorm then split-halves RoPE (qknorm.cuh), bf16 in and out. The D/16 threads
+// of a row are adjacent lanes of one warp; they reduce the row's sum of squares with
+// shuffles. The loop advances whole warps together so that every lane takes part in each
+// shuffle (a group of lanes is either a whole row or past the end).
+// ------------------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(256) qk_rmsnorm_rope_kernel(const uint16_t* x, uint16_t* y,
+                                                             const float* __restrict__ w, float eps,
+                                                             const float* __restrict__ cos_t,
+                                                             const float* __restrict__ sin_t,
+                                                             long long rows, int S, int H) {
+  constexpr int kHalf = D / 2, kChunks = kHalf / 8;
+  const long long items = rows * kChunks;
+  const int lane = threadIdx.x & 31;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long base = static_cast<long long>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31);
+       base < items; base += stride) {
+    const long long it = base + lane;
+    const bool valid = it < items;
+    const long long row = valid ? it / kChunks : 0;
+    const int ch = static_cast<int>(it % kChunks);
+    uint4 a = make_uint4(0, 0, 0, 0), b = make_uint4(0, 0, 0, 0);
+    if (valid) {
+      a = *reinterpret_cast<const uint4*>(x + row * D + ch * 8);
+      b = *reinterpret_cast<const uint4*>(x + row * D + kHalf + ch * 8);
+    }
+    float ss = sumsq16(a, b);
+#pragma unroll
+    for (int off = 1; off < kChunks; off <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    if (valid) {
+      const int s = static_cast<int>((row / H) % S);
+      const float inv = rsqrtf(ss * (1.f / D) + eps);
+      float wa[8], wb[8], cs[8], sn[8];
+      load8f(w + ch * 8, wa);
+      load8f(w + kHalf + ch * 8, wb);
+      load8f(cos_t + static_cast<long long>(s) * kHalf + ch * 8, cs);
+      load8f(sin_t + static_cast<long long>(s) * kHalf + ch * 8, sn);
+      norm_rotate8<false>(a, b, inv, wa, wb, cs, sn);
+      *reinterpret_cast<uint4*>(y + row * D + ch * 8) = a;
+      *reinterpret_cast<uint4*>(y + row * D + kHalf + ch * 8) = b;
+    }
   }
 }
 
@@ -167,6 +213,23 @@ cudaError_t launch_rope_split_halves(const void* x, void* y, const float* cos_ta
   else
     rope_split_halves_kernel<64><<<grid, 256, 0, stream>>>(
         static_cast<const uint16_t*>(x), static_cast<uint16_t*>(y), cos_tab, sin_tab, rows, S, H);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_qk_rmsnorm_rope(const void* x, void* y, const float* w, float eps,
+                                   const float* cos_tab, const float* sin_tab, int B, int S, int H,
+                                   int D, cudaStream_t stream) {
+  const long long rows = static_cast<long long>(B) * S * H;
+  const long long items = rows * (D / 16);
+  const int grid = grid_for(items, 256);
+  if (D == 128)
+    qk_rmsnorm_rope_kernel<128><<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(x),
+                                                          static_cast<uint16_t*>(y), w, eps, cos_tab,
+                                                          sin_tab, rows, S, H);
+  else
+    qk_rmsnorm_rope_kernel<64><<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(x),
+                                                         static_cast<uint16_t*>(y), w, eps, cos_tab,
+                                                         sin_tab, rows, S, H);
   return cudaGetLastError();
 }
 

@@ -44,6 +44,9 @@ _SIGNATURES = {
                          _vp, ctypes.c_size_t, _vp], _i),
     "dit_attn_fwd_ws_static": ([_vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _f, _vp,
                                 _vp, _vp], _i),
+    "dit_attn_fwd_ws_qknorm": ([_vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _vp, _vp, _f, _vp, _vp, _vp, _vp,
+                                _f, _vp, _vp, _vp, ctypes.c_size_t, _vp], _i),
+    "dit_qk_rmsnorm_rope": ([_vp, _vp, _vp, _f, _vp, _vp, _i, _i, _i, _i, _vp], _i),
 }
 for _name, (_args, _res) in _SIGNATURES.items():
     _fn = getattr(_lib, _name)
@@ -215,6 +218,60 @@ def dit_attn_fwd_ws(q, k, v, q_valid_len: int, kv_valid_len: int, cos_q, sin_q, 
         _ptr(cos_q), _ptr(sin_q), _ptr(cos_k), _ptr(sin_k), scale, _ptr(out), _ptr(lse),
         _ptr(workspace), workspace.numel(), _stream_handle(stream)))
     return out, lse
+
+
+def dit_attn_fwd_ws_qknorm(q, k, v, q_valid_len: int, kv_valid_len: int, norm_q, norm_k, cos_q, sin_q,
+                           cos_k, sin_k, eps: float = 1e-6, workspace=None, softmax_scale=None, out=None,
+                           lse=None, stream=None):
+    """dit_attn_fwd_ws with a per-head RMSNorm of q and k (weights norm_q, norm_k: fp32 CUDA
+    tensors [D]) ahead of the rotation."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, torch.bfloat16, 4)
+    B, Sq, H, D = q.shape
+    Skv = k.shape[1]
+    if tuple(k.shape) != (B, Skv, H, D) or v.shape != k.shape:
+        raise ValueError("k and v must be [B, Skv, H, D] matching q")
+    for t, n in ((norm_q, "norm_q"), (norm_k, "norm_k")):
+        _need(t, n, torch.float32, 1)
+        if t.shape[0] != D:
+            raise ValueError(f"{n} must be [{D}]")
+    for t, n, rows in ((cos_q, "cos_q", Sq), (sin_q, "sin_q", Sq), (cos_k, "cos_k", Skv), (sin_k, "sin_k", Skv)):
+        _need(t, n, torch.float32, 2)
+        if tuple(t.shape) != (rows, D // 2):
+            raise ValueError(f"{n} must be [{rows}, {D // 2}]")
+    need = dit_attn_workspace_bytes(B, Sq, Skv, H, D)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    _need(workspace, "workspace", torch.uint8, 1)
+    scale = 1.0 / math.sqrt(D) if softmax_scale is None else float(softmax_scale)
+    out, lse = _attn_outputs(q, out, lse)
+    _check("dit_attn_fwd_ws_qknorm", _lib.dit_attn_fwd_ws_qknorm(
+        _ptr(q), _ptr(k), _ptr(v), B, Sq, Skv, H, D, int(q_valid_len), int(kv_valid_len),
+        _ptr(norm_q), _ptr(norm_k), float(eps), _ptr(cos_q), _ptr(sin_q), _ptr(cos_k), _ptr(sin_k),
+        scale, _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(), _stream_handle(stream)))
+    return out, lse
+
+
+def dit_qk_rmsnorm_rope(x, w, cos, sin, eps: float = 1e-6, out=None, stream=None):
+    """y = split-halves RoPE of the per-head RMSNorm of x [B, S, H, D] bf16 (weights w: fp32
+    [D]; tables [S, D/2] fp32). out may be x itself (in place)."""
+    _need(x, "x", torch.bfloat16, 4)
+    B, S, H, D = x.shape
+    _need(w, "w", torch.float32, 1)
+    if w.shape[0] != D:
+        raise ValueError(f"w must be [{D}]")
+    _need(cos, "cos", torch.float32, 2)
+    _need(sin, "sin", torch.float32, 2)
+    if tuple(cos.shape) != (S, D // 2) or tuple(sin.shape) != (S, D // 2):
+        raise ValueError(f"tables must be [{S}, {D // 2}]")
+    if out is None:
+        out = torch.empty_like(x)
+    _need(out, "out", torch.bfloat16, 4)
+    if out.shape != x.shape:
+        raise ValueError("out must have x's shape")
+    _check("dit_qk_rmsnorm_rope", _lib.dit_qk_rmsnorm_rope(
+        _ptr(x), _ptr(out), _ptr(w), float(eps), _ptr(cos), _ptr(sin), B, S, H, D, _stream_handle(stream)))
+    return out
 
 
 # Size of the library's fixed device scratch array used by dit_attn_fwd_ws_static.

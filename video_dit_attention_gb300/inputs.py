@@ -191,3 +191,9 @@ def sample_rows(n_valid: int, n_total: int, count: int, seed: int) -> np.ndarray
     picks = set(int(x) for x in rng.integers(0, n_valid, size=count))
     rows = sorted(r for r in fixed | picks if 0 <= r < n_total)
     return np.asarray(rows, dtype=np.int64)
+
+
+def make_norm_weights(D: int, seed: int) -> np.ndarray:
+    """Synthetic per-head RMSNorm weights [D] fp32: 1 + 0.1 * N(0, 1) (no trained weights)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    return (1.0 + 0.1 * rng.standard_normal(D)).astype(np.float32)
