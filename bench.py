@@ -225,6 +225,10 @@ def config_dict(name, spec, rope_mode="ws"):
     return d
 
 
+def spec_has_no_rope(spec):
+    return getattr(spec, "rope", "1d") is None
+
+
 def dominant_kernel(name, rope_mode):
     if name == "cross":
         return "attn_sp_kernel (cross mode)"
@@ -250,7 +254,7 @@ def step_flops(name, spec):
 class GpuWorkload:
     """Device buffers and the launch sequence of one step."""
 
-    def __init__(self, name, spec, seed_offset=0, rope_mode="ws"):
+    def __init__(self, name, spec, seed_offset=0, rope_mode="ws", qknorm=False):
         import torch
 
         from video_dit_attention_gb300 import dit_attn as lib
@@ -258,7 +262,11 @@ class GpuWorkload:
         self.torch, self.lib, self.name, self.spec = torch, lib, name, spec
         self.rope_mode = rope_mode
         self.workspace = None
+        self.norms = None
         dev = torch.device("cuda")
+        if qknorm:
+            self.norms = tuple(torch.from_numpy(I.make_norm_weights(spec.D, seed=spec.seed + 900 + i)).to(dev)
+                               for i in range(2))
         bf = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(torch.bfloat16).to(dev)
         self.sets = []
         if name == "sharded":
@@ -319,7 +327,10 @@ class GpuWorkload:
     def attn(self, q, k, v, q_valid, kv_valid, tables, out, lse):
         """One self-attention launch: the two-phase RoPE path (rotation into the preallocated
         workspace) when a workspace is set, else the path with RoPE fused per tile."""
-        if self.workspace is not None:
+        if self.workspace is not None and self.norms is not None:
+            self.lib.dit_attn_fwd_ws_qknorm(q, k, v, q_valid, kv_valid, *self.norms, *tables,
+                                            workspace=self.workspace, out=out, lse=lse)
+        elif self.workspace is not None:
             self.lib.dit_attn_fwd_ws(q, k, v, q_valid, kv_valid, *tables, workspace=self.workspace,
                                      out=out, lse=lse)
         else:
@@ -446,6 +457,12 @@ def measure_hbm_kernels(peaks):
         "workload": "Wan 480x832x9 q and k, [2, 4736, 40, 128] bf16, 3-D tables, out of place",
         "bytes_per_call": nb, "us": t * 1e6, "GB_s": nb / t / 1e9, "frac_of_hbm": nb / t / 1e9 / peaks["hbm_gbs"],
         "l2": "2 input sets of 97 MB, 194 MB moved per call (> 129 MB L2)"}
+    w = torch.from_numpy(I.make_norm_weights(c.D, seed=7)).to(dev)
+    t = timed(lambda i: lib.dit_qk_rmsnorm_rope(xs[i % 2], w, cs, sn, out=ys[i % 2]), 40)
+    out["qk_rmsnorm_rope"] = {
+        "workload": "Wan 480x832x9 q and k, [2, 4736, 40, 128] bf16, per-head RMSNorm then 3-D RoPE",
+        "bytes_per_call": nb, "us": t * 1e6, "GB_s": nb / t / 1e9, "frac_of_hbm": nb / t / 1e9 / peaks["hbm_gbs"],
+        "l2": "2 input sets of 97 MB, 194 MB moved per call (> 129 MB L2)"}
     del xs, ys
     # LSE merge of the sharded workload's 4 partials.
     sc = I.sharded_case()
@@ -570,6 +587,8 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--rope", default="ws", choices=["ws", "fused"],
                     help="ws: rotate q/k once per call into a workspace (default); fused: rotate per tile")
+    ap.add_argument("--qknorm", action="store_true",
+                    help="per-head q/k RMSNorm fused before the rotation (workspace path, RoPE workloads)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-hbm-kernels", action="store_true", help="skip the RoPE / merge GB/s figures")
     args = ap.parse_args()
@@ -589,7 +608,9 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     peaks = load_peaks()
-    wl = GpuWorkload(name, spec, seed_offset=rank, rope_mode=args.rope)
+    if args.qknorm and (args.rope != "ws" or spec_has_no_rope(spec)):
+        raise SystemExit("--qknorm needs a RoPE workload on the workspace path")
+    wl = GpuWorkload(name, spec, seed_offset=rank, rope_mode=args.rope, qknorm=args.qknorm)
     flops = step_flops(name, spec)
     stream = torch.cuda.current_stream()
 
@@ -653,11 +674,13 @@ def main():
         "metric": METRIC, "value": units / max_el / 1e12, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": max_el / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic", "config": config_dict(name, spec, args.rope),
+        "data": "synthetic", "config": dict(config_dict(name, spec, args.rope), **(
+            {"qk_norm": "per-head RMSNorm before the rotation, synthetic weights 1 + 0.1 N(0,1), eps 1e-6"}
+            if args.qknorm else {})),
         "pct_of_bf16_peak": 100.0 * (units / max_el / 1e12) / (peak * world),
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": profiled_traffic(name),
-                     "kernel": dominant_kernel(name, args.rope),
+                     "kernel": dominant_kernel(name, args.rope) + (" + q/k RMSNorm" if args.qknorm else ""),
                      "kernel_ms": kern_s * 1e3, "algorithmic_bytes": wl.dominant_bytes(),
                      "peak_source": f"bf16_tflops (burst) of {peaks['source']} peaks"},
         "gpu_launches": wl.launches_per_step * args.steps,
