@@ -525,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // The warp stages its 32 normalised rows in its own rows of the P_t buffer, in the P
       // layout (row r, 16-byte unit x of 64-column chunk c at c * 16384 + r * 128 +
       // ((x ^ (r & 7)) * 16)), so no other warp reads or writes those bytes. It then writes
-      // them out one D * 2-byte row per store instruction instead of 32 scattered pieces.
+      // them out as whole rows, 16 bytes per lane, instead of 32 scattered pieces per row.
       // O_t is read 32 columns at a time and released once the last piece is in registers.
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
@@ -550,20 +550,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       __syncwarp();
-      if (D == 128 || lane < 16) {               // lane: bytes 8 * lane .. of a row
-        const int r0 = r & ~31;                  // first row of this warp
-        const uint32_t chunk = static_cast<uint32_t>(lane >> 4) * 16384u;
-        const uint32_t unit = static_cast<uint32_t>((lane >> 1) & 7), half = static_cast<uint32_t>(lane & 1) * 8u;
-        // Stores in flight per lane: more helps short items (cross-attention: +13 % at four)
-        // and plain attention slightly; the workspace mode measured best at one.
+      {
+        // 16 bytes per lane: D / 8 lanes cover one row, so one store instruction writes
+        // 32 / (D / 8) whole rows.
+        constexpr int kLPR = D / 8, kRPI = 32 / kLPR;
+        const int r0 = r & ~31, lu = lane % kLPR, lr = lane / kLPR;   // r0: first row of this warp
+        const uint32_t chunk = static_cast<uint32_t>(lu >> 3) * 16384u, unit = static_cast<uint32_t>(lu & 7);
+        // Stores in flight per lane: more helps short items (cross-attention) and plain
+        // attention slightly; the workspace mode measured best at one.
         constexpr int kStoreUnroll = kWs ? 1 : 4;
 #pragma unroll kStoreUnroll
-        for (int i = 0; i < 32; ++i) {
-          const int rr = r0 + i;
+        for (int i = 0; i < 32 / kRPI; ++i) {
+          const int rr = r0 + i * kRPI + lr;
           const uint32_t src = sP + t * C::kPBytes + chunk + static_cast<uint32_t>(rr) * 128u +
-                               ((unit ^ static_cast<uint32_t>(rr & 7)) << 4) + half;
+                               ((unit ^ static_cast<uint32_t>(rr & 7)) << 4);
           uint16_t* dst = p.out + ((static_cast<size_t>(w.b) * p.Sq + w.q0 + 128 * t + rr) * p.H + w.h) * D;
-          *reinterpret_cast<uint2*>(dst + lane * 4) = lds64(src);
+          *reinterpret_cast<uint4*>(dst + lu * 8) = lds128(src);
         }
       }
       __syncwarp();
