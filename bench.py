@@ -254,7 +254,7 @@ def step_flops(name, spec):
 class GpuWorkload:
     """Device buffers and the launch sequence of one step."""
 
-    def __init__(self, name, spec, seed_offset=0, rope_mode="ws", qknorm=False):
+    def __init__(self, name, spec, seed_offset=0, rope_mode="ws", qknorm=False, fixed_m=False):
         import torch
 
         from video_dit_attention_gb300 import dit_attn as lib
@@ -263,6 +263,8 @@ class GpuWorkload:
         self.rope_mode = rope_mode
         self.workspace = None
         self.norms = None
+        self.fixed_m = fixed_m
+        ws_bytes = lib.dit_attn_fixed_m_workspace_bytes if fixed_m else lib.dit_attn_workspace_bytes
         dev = torch.device("cuda")
         if qknorm:
             self.norms = tuple(torch.from_numpy(I.make_norm_weights(spec.D, seed=spec.seed + 900 + i)).to(dev)
@@ -292,8 +294,7 @@ class GpuWorkload:
                 self.sets.append((qq, kv, po, pl, out, lse))
             self.launches_per_step = len(spec.shard_valid) + 1
             if rope_mode == "ws":
-                nb = max(lib.dit_attn_workspace_bytes(spec.B, spec.Sq, npad, spec.H, spec.D)
-                         for npad in spec.shard_pad)
+                nb = max(ws_bytes(spec.B, spec.Sq, npad, spec.H, spec.D) for npad in spec.shard_pad)
                 self.workspace = torch.empty(nb, dtype=torch.uint8, device=dev)
         else:
             spec.seed += seed_offset
@@ -320,14 +321,17 @@ class GpuWorkload:
                 self.sets.append((qq, kk, vv, out, lse))
             self.launches_per_step = 1
             if rope_mode == "ws" and self.tables[0] is not None:
-                nb = lib.dit_attn_workspace_bytes(spec.B, spec.Sq, spec.Skv, spec.H, spec.D)
+                nb = ws_bytes(spec.B, spec.Sq, spec.Skv, spec.H, spec.D)
                 self.workspace = torch.empty(nb, dtype=torch.uint8, device=dev)
         torch.cuda.synchronize()
 
     def attn(self, q, k, v, q_valid, kv_valid, tables, out, lse):
         """One self-attention launch: the two-phase RoPE path (rotation into the preallocated
         workspace) when a workspace is set, else the path with RoPE fused per tile."""
-        if self.workspace is not None and self.norms is not None:
+        if self.workspace is not None and self.fixed_m:
+            self.lib.dit_attn_fwd_ws_fixed_m(q, k, v, q_valid, kv_valid, *tables, workspace=self.workspace,
+                                             out=out, lse=lse)
+        elif self.workspace is not None and self.norms is not None:
             self.lib.dit_attn_fwd_ws_qknorm(q, k, v, q_valid, kv_valid, *self.norms, *tables,
                                             workspace=self.workspace, out=out, lse=lse)
         elif self.workspace is not None:
@@ -589,6 +593,9 @@ def main():
                     help="ws: rotate q/k once per call into a workspace (default); fused: rotate per tile")
     ap.add_argument("--qknorm", action="store_true",
                     help="per-head q/k RMSNorm fused before the rotation (workspace path, RoPE workloads)")
+    ap.add_argument("--fixed-m", action="store_true",
+                    help="fixed-m softmax (32-row blocks whose norm bound allows it skip the running "
+                         "maximum; workspace path, RoPE workloads)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-hbm-kernels", action="store_true", help="skip the RoPE / merge GB/s figures")
     args = ap.parse_args()
@@ -610,7 +617,9 @@ def main():
     peaks = load_peaks()
     if args.qknorm and (args.rope != "ws" or spec_has_no_rope(spec)):
         raise SystemExit("--qknorm needs a RoPE workload on the workspace path")
-    wl = GpuWorkload(name, spec, seed_offset=rank, rope_mode=args.rope, qknorm=args.qknorm)
+    if args.fixed_m and (args.rope != "ws" or spec_has_no_rope(spec) or args.qknorm):
+        raise SystemExit("--fixed-m needs a RoPE workload on the workspace path, without --qknorm")
+    wl = GpuWorkload(name, spec, seed_offset=rank, rope_mode=args.rope, qknorm=args.qknorm, fixed_m=args.fixed_m)
     flops = step_flops(name, spec)
     stream = torch.cuda.current_stream()
 
@@ -676,11 +685,16 @@ def main():
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic", "config": dict(config_dict(name, spec, args.rope), **(
             {"qk_norm": "per-head RMSNorm before the rotation, synthetic weights 1 + 0.1 N(0,1), eps 1e-6"}
-            if args.qknorm else {})),
+            if args.qknorm else {}), **(
+            {"softmax": "fixed-m: 32-row blocks whose bound scale*|q|*max|k| allows it skip the running maximum"}
+            if args.fixed_m else {})),
         "pct_of_bf16_peak": 100.0 * (units / max_el / 1e12) / (peak * world),
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": profiled_traffic(name),
-                     "kernel": dominant_kernel(name, args.rope) + (" + q/k RMSNorm" if args.qknorm else ""),
+                     "frac": achieved / peak,
+                     # the profiled traffic is that of the default kernel; the variants have none
+                     "traffic": None if (args.qknorm or args.fixed_m) else profiled_traffic(name),
+                     "kernel": dominant_kernel(name, args.rope) + (" + q/k RMSNorm" if args.qknorm else "")
+                     + (" (fixed-m softmax)" if args.fixed_m else ""),
                      "kernel_ms": kern_s * 1e3, "algorithmic_bytes": wl.dominant_bytes(),
                      "peak_source": f"bf16_tflops (burst) of {peaks['source']} peaks"},
         "gpu_launches": wl.launches_per_step * args.steps,

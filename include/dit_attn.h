@@ -168,6 +168,38 @@ int dit_attn_fwd_ws_qknorm(const void* q, const void* k, const void* v, int B, i
                            float* lse, void* workspace, size_t workspace_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------------------
+ * dit_attn_fwd_ws with the fixed-m softmax (maxdiffusion PR #491, Wan fast inference: a
+ * "fixed-m per Q block" attention kernel takes per-block metadata from norm reductions over
+ * q and k, with pad rows excluded, and lets a block whose metadata allows it skip the online
+ * softmax). The pages give no formula; this library's metadata and proof:
+ *   bound of query row i:  m_i = softmax_scale * |q_i| * max_{j < kv_valid_len} |k_j|.
+ * By Cauchy-Schwarz no valid score s_ij = softmax_scale * q~_i . k~_j exceeds m_i, and the
+ * rotation preserves norms, so the raw rows give the bound of the rotated ones. A block of
+ * 32 consecutive query rows of one head (one warp) uses p_ij = exp(s_ij - m_i) with m_i
+ * fixed -- no running maximum, no rescaling of the accumulator -- when every valid row of
+ * the block has 2 m_i <= 64 ln 2: all its scores then lie in [-m_i, m_i], so its largest
+ * term is at least 2^-64 and no term exceeds 1. Other blocks take the online softmax. The
+ * key maximum runs over valid keys only and pad query rows take no part in the decision, so
+ * pad contents never move a block onto the online path. In exact arithmetic both paths give
+ * the plain softmax; O and LSE match dit_attn_fwd_ws within the same tolerances.
+ *
+ * workspace: device buffer of at least dit_attn_fixed_m_workspace_bytes(B, Sq, Skv, H, D)
+ * bytes, 256-byte aligned, owned by the caller, contents on entry irrelevant (the call clears
+ * what needs clearing on `stream`). n_online: NULL, or a device unsigned int (4-byte
+ * aligned) to which the call adds the number of 32-row blocks that took the online path;
+ * the caller zeroes it. Calls sharing a workspace or an n_online counter must not overlap.
+ * Everything else (arguments, layouts, tables, outputs, numerics) as dit_attn_fwd_ws.
+ * Errors: as dit_attn_fwd_ws (workspace checked against the size above), plus
+ * DIT_ERR_UNSUPPORTED when B * H > 24576 and DIT_ERR_ALIGNMENT for a misaligned n_online.
+ * ------------------------------------------------------------------------------------- */
+size_t dit_attn_fixed_m_workspace_bytes(int B, int Sq, int Skv, int H, int D);
+int dit_attn_fwd_ws_fixed_m(const void* q, const void* k, const void* v, int B, int Sq, int Skv,
+                            int H, int D, int q_valid_len, int kv_valid_len, const float* cos_q,
+                            const float* sin_q, const float* cos_k, const float* sin_k,
+                            float softmax_scale, void* out, float* lse, void* workspace,
+                            size_t workspace_bytes, unsigned int* n_online, void* stream);
+
+/* ---------------------------------------------------------------------------------------
  * Standalone per-head RMSNorm then split-halves RoPE (the prologue dit_attn_fwd_ws_qknorm
  * fuses): y[b,s,h,:] = rotate(x[b,s,h,:] / sqrt(mean(x^2) + eps) * w) with table row s.
  * x, y: [B, S, H, D] bf16 (y may equal x); w: device fp32 [D]; cos, sin: [S, D/2] fp32.

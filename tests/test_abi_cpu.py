@@ -160,3 +160,33 @@ def test_static_scratch_entry_rejects_oversized_problems_before_any_cuda_call(cl
               0.125, None, None, None) == -1            # DIT_ERR_INVALID_ARG
     assert fn(None, None, None, 1, 128, 128, 1, 96, 1, 1, None, None, None, None,
               0.125, None, None, None) == -2            # head dim not supported
+
+
+def test_fixed_m_entry_validation_before_any_cuda_call(clib):
+    wsb = clib.dit_attn_fixed_m_workspace_bytes
+    wsb.restype = ctypes.c_size_t
+    base = clib.dit_attn_workspace_bytes
+    base.restype = ctypes.c_size_t
+    # the ws layout, then the key-norm maxima [B*H] u32 and q row norms [B, Sq, H] fp32, 256-aligned
+    r256 = lambda n: (n + 255) // 256 * 256
+    assert wsb(1, 4736, 4736, 40, 128) == base(1, 4736, 4736, 40, 128) + r256(40 * 4) + r256(4736 * 40 * 4)
+    assert wsb(2, 384, 512, 3, 64) == base(2, 384, 512, 3, 64) + r256(2 * 3 * 4) + r256(2 * 384 * 3 * 4)
+    assert wsb(0, 128, 128, 1, 128) == 0 and wsb(1, 128, 128, 1, 96) == 0
+    fn = clib.dit_attn_fwd_ws_fixed_m
+    fn.restype = ctypes.c_int
+    fn.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 7 + [ctypes.c_void_p] * 4 + \
+        [ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t,
+         ctypes.c_void_p, ctypes.c_void_p]
+    P = 0x10000   # never dereferenced: every case below fails validation first
+    need = wsb(1, 256, 256, 2, 128)
+
+    def call(B=1, H=2, wsz=need, ws=P, cos=P, n_online=None, kv=256):
+        return fn(P, P, P, B, 256, 256, H, 128, 256, kv, cos, P, P, P, 0.088, P, P, ws, wsz, n_online, None)
+
+    assert call(cos=None) == -1                 # all four tables are required
+    assert call(ws=None) == -1
+    assert call(wsz=need - 1) == -1             # workspace too small
+    assert call(kv=257) == -1
+    assert call(B=1, H=24577, wsz=wsb(1, 256, 256, 24577, 128)) == -2   # B * H above 24576
+    assert call(n_online=P + 2) == -3           # misaligned counter
+    assert call(ws=P + 128) == -3               # workspace not 256-byte aligned

@@ -164,6 +164,33 @@ extern "C" int dit_attn_fwd_ws(const void* q, const void* k, const void* v, int 
   return cuda_status(launch_attn_fwd(a, kModeRopeWs));
 }
 
+extern "C" size_t dit_attn_fixed_m_workspace_bytes(int B, int Sq, int Skv, int H, int D) {
+  if (B < 1 || Sq < 1 || Skv < 1 || H < 1 || (D != 64 && D != 128)) return 0;
+  return attn_fixed_m_workspace_bytes(B, Sq, Skv, H, D);
+}
+
+extern "C" int dit_attn_fwd_ws_fixed_m(const void* q, const void* k, const void* v, int B, int Sq,
+                                       int Skv, int H, int D, int q_valid_len, int kv_valid_len,
+                                       const float* cos_q, const float* sin_q, const float* cos_k,
+                                       const float* sin_k, float softmax_scale, void* out, float* lse,
+                                       void* workspace, size_t workspace_bytes,
+                                       unsigned int* n_online, void* stream) {
+  int st = check_attn_shapes(q, k, v, B, Sq, Skv, H, D, q_valid_len, softmax_scale, out, lse);
+  if (st != DIT_OK) return st;
+  if (kv_valid_len < 0 || kv_valid_len > Skv) return DIT_ERR_INVALID_ARG;
+  if (!cos_q || !sin_q || !cos_k || !sin_k || !workspace) return DIT_ERR_INVALID_ARG;
+  if (workspace_bytes < attn_fixed_m_workspace_bytes(B, Sq, Skv, H, D)) return DIT_ERR_INVALID_ARG;
+  if (static_cast<long long>(Sq > Skv ? Sq : Skv) * H * (D / 16) >= (1ll << 30)) return DIT_ERR_UNSUPPORTED;
+  if (static_cast<long long>(B) * H > kFixedMMaxHeads) return DIT_ERR_UNSUPPORTED;
+  if (!aligned(cos_q, 16) || !aligned(sin_q, 16) || !aligned(cos_k, 16) || !aligned(sin_k, 16) ||
+      !aligned(workspace, 256) || !aligned(n_online, 4))
+    return DIT_ERR_ALIGNMENT;
+  AttnArgs a{q, k, v, B, Sq, Skv, H, D, q_valid_len, kv_valid_len, nullptr,
+             cos_q, sin_q, cos_k, sin_k, softmax_scale, out, lse, workspace, nullptr, nullptr, 0.f,
+             static_cast<cudaStream_t>(stream), n_online};
+  return cuda_status(launch_attn_fwd(a, kModeRopeWsFixedM));
+}
+
 extern "C" int dit_attn_fwd_ws_qknorm(const void* q, const void* k, const void* v, int B, int Sq,
                                       int Skv, int H, int D, int q_valid_len, int kv_valid_len,
                                       const float* norm_q, const float* norm_k, float eps,

@@ -122,11 +122,14 @@ struct WsParams {
   const float* norm_q;   // per-head q/k RMSNorm weights [D] (norm mode only)
   const float* norm_k;
   float norm_eps;
+  unsigned int* kmax;      // fixed-m mode: largest squared key norm per (b, h), float bits
+  float* qn;               // fixed-m mode: squared norm of each q row [B, Sq, H]
+  unsigned int* n_online;  // fixed-m mode: blocks that took the online path (may be null)
 };
 
-// The two RoPE workspace modes (without and with the q/k RMSNorm).
+// The RoPE workspace modes (plain, with the q/k RMSNorm, fixed-m softmax).
 __host__ __device__ constexpr bool is_ws_mode(int mode) {
-  return mode == kModeRopeWs || mode == kModeRopeWsNorm;
+  return mode == kModeRopeWs || mode == kModeRopeWsNorm || mode == kModeRopeWsFixedM;
 }
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
@@ -383,8 +386,89 @@ __device__ __forceinline__ void rotate_rows_fp16_norm(const uint16_t* __restrict
   }
 }
 
-// rotate_tile_smem with the per-head RMSNorm applied first (NT a multiple of 32: every lane
-// runs the same iterations, and the D/16 lanes of a row reduce its sum of squares).
+// rotate_rows_fp16 that also records, per (b, h), the largest squared norm of the key rows it
+// rotates: kmax_s[b * H + h] (shared memory; float bits, which order like unsigned integers
+// for non-negative values; zero on entry) through shared-memory atomicMax. The squared norm
+// is taken from the bf16 inputs: the rotation preserves it. The loop runs per warp so that
+// the D / 16 lanes holding one row can add their partial sums with shuffles.
+template <int D>
+__device__ __forceinline__ void rotate_rows_fp16_kmax(const uint16_t* __restrict__ x, uint16_t* __restrict__ y,
+                                                      const float* __restrict__ cos_t,
+                                                      const float* __restrict__ sin_t, int B, int S_rows,
+                                                      int valid, int H, int gtid, int gthreads,
+                                                      unsigned int* kmax_s) {
+  constexpr int kHalf = D / 2, kChunks = kHalf / 8, kU = 4;
+  const int per_b = valid * H * kChunks;
+  const int lane = gtid & 31;
+  for (int b = 0; b < B; ++b) {
+    const size_t boff = static_cast<size_t>(b) * S_rows * H * D;
+    for (int base = gtid - lane; base < per_b; base += kU * gthreads) {
+      uint4 a[kU], bb[kU];
+      float4 c0[kU], c1[kU], s0[kU], s1[kU];
+      size_t off[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int i = base + u * gthreads + lane;
+        a[u] = make_uint4(0, 0, 0, 0);
+        bb[u] = make_uint4(0, 0, 0, 0);
+        off[u] = 0;
+        if (i < per_b) {
+          const int ch = i % kChunks, rh = i / kChunks, srow = rh / H;   // rh = srow * H + h
+          off[u] = boff + static_cast<size_t>(rh) * D + ch * 8;
+          a[u] = *reinterpret_cast<const uint4*>(x + off[u]);
+          bb[u] = *reinterpret_cast<const uint4*>(x + off[u] + kHalf);
+          const float* ct = cos_t + static_cast<size_t>(srow) * kHalf + ch * 8;
+          const float* st = sin_t + static_cast<size_t>(srow) * kHalf + ch * 8;
+          c0[u] = __ldg(reinterpret_cast<const float4*>(ct));
+          c1[u] = __ldg(reinterpret_cast<const float4*>(ct + 4));
+          s0[u] = __ldg(reinterpret_cast<const float4*>(st));
+          s1[u] = __ldg(reinterpret_cast<const float4*>(st + 4));
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        float ss = sumsq16(a[u], bb[u]);
+#pragma unroll
+        for (int o = 1; o < kChunks; o <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        const int i = base + u * gthreads + lane;
+        if (i < per_b) {
+          if (i % kChunks == 0) atomicMax(kmax_s + b * H + (i / kChunks) % H, __float_as_uint(ss));
+          rotate8(a[u], bb[u], c0[u], c1[u], s0[u], s1[u]);
+          *reinterpret_cast<uint4*>(y + off[u]) = a[u];
+          *reinterpret_cast<uint4*>(y + off[u] + kHalf) = bb[u];
+        }
+      }
+    }
+  }
+}
+
+// rotate_tile_smem that also writes each row's squared norm (of the landed bf16 values; the
+// rotation preserves it) to qn_rows[row * stride].
+template <int D, int NT>
+__device__ __forceinline__ void rotate_tile_smem_sq(uint32_t tile, const float* __restrict__ cos_t,
+                                                    const float* __restrict__ sin_t, int at,
+                                                    float* __restrict__ qn_rows, int stride) {
+  constexpr int kHalf = D / 2, kUnits = kHalf / 8;
+  static_assert(NT % 32 == 0 && (128 * kUnits) % NT == 0, "whole warps, whole rows");
+#pragma unroll 1   // one unit in flight: it runs in the MMA issuers' 72-register budget
+  for (int i = at; i < 128 * kUnits; i += NT) {
+    const int row = i / kUnits, x = i % kUnits;
+    const uint32_t offa = sw128_offset(row, x);
+    const uint32_t offb = (D == 128) ? 16384u + offa : sw128_offset(row, x + 4);
+    const float* ct = cos_t + row * kHalf + x * 8;
+    const float* st = sin_t + row * kHalf + x * 8;
+    uint4 a = lds128(tile + offa), b = lds128(tile + offb);
+    float ss = sumsq16(a, b);
+#pragma unroll
+    for (int o = 1; o < kUnits; o <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if (x == 0) qn_rows[static_cast<size_t>(row) * stride] = ss;
+    rotate8(a, b, __ldg(reinterpret_cast<const float4*>(ct)), __ldg(reinterpret_cast<const float4*>(ct + 4)),
+            __ldg(reinterpret_cast<const float4*>(st)), __ldg(reinterpret_cast<const float4*>(st + 4)));
+    sts128(tile + offa, a);
+    sts128(tile + offb, b);
+  }
+}
+
 template <int D, int NT>
 __device__ __forceinline__ void rotate_tile_smem_norm(uint32_t tile, const float* __restrict__ cos_t,
                                                       const float* __restrict__ sin_t,
@@ -953,9 +1037,19 @@ cudaError_t launch_mode(const AttnArgs& a) {
   ws.norm_q = a.norm_q;
   ws.norm_k = a.norm_k;
   ws.norm_eps = a.norm_eps;
+  ws.kmax = nullptr;
+  ws.qn = nullptr;
+  ws.n_online = a.n_online;
+  size_t zero_bytes = sizeof(unsigned int);   // what the launch clears: the CTA counter
   if (is_ws_mode(kMode)) {
     const size_t k_bytes = (static_cast<size_t>(a.B) * a.Skv * a.H * D * 2 + 255) / 256 * 256;
     ws.rotated = reinterpret_cast<unsigned int*>(static_cast<char*>(a.workspace) + k_bytes);
+    if (kMode == kModeRopeWsFixedM) {
+      const size_t kmax_bytes = (static_cast<size_t>(a.B) * a.H * 4 + 255) / 256 * 256;
+      ws.kmax = reinterpret_cast<unsigned int*>(static_cast<char*>(a.workspace) + k_bytes + 256);
+      ws.qn = reinterpret_cast<float*>(static_cast<char*>(a.workspace) + k_bytes + 256 + kmax_bytes);
+      zero_bytes = 256 + kmax_bytes;   // the counter block and the key-norm maxima
+    }
   }
   static const int sm_count = [] {
     int dev = 0, n = 0;
@@ -982,7 +1076,7 @@ cudaError_t launch_mode(const AttnArgs& a) {
     }
     // CTAs wait for rotated rows that other CTAs produce: launch cooperatively so that every
     // CTA is resident, after zeroing the counter on the same stream.
-    e = cudaMemsetAsync(ws.rotated, 0, sizeof(unsigned int), a.stream);
+    e = cudaMemsetAsync(ws.rotated, 0, zero_bytes, a.stream);
     if (e != cudaSuccess) return e;
     void* args[] = {&mq, &mk, &mv, &p, &ws};
     return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kern), dim3(grid), dim3(kThreads),
@@ -998,16 +1092,24 @@ size_t attn_workspace_bytes(int B, int Sq, int Skv, int H, int D) {
   return k + 256;   // + the counter of CTAs done rotating
 }
 
+size_t attn_fixed_m_workspace_bytes(int B, int Sq, int Skv, int H, int D) {
+  const size_t kmax = (static_cast<size_t>(B) * H * 4 + 255) / 256 * 256;
+  const size_t qn = (static_cast<size_t>(B) * Sq * H * 4 + 255) / 256 * 256;
+  return attn_workspace_bytes(B, Sq, Skv, H, D) + kmax + qn;
+}
+
 cudaError_t launch_attn_fwd(const AttnArgs& a, AttnMode mode) {
   if (a.D == 128) {
     if (mode == kModeRopeWs) return launch_mode<128, kModeRopeWs>(a);
     if (mode == kModeRopeWsNorm) return launch_mode<128, kModeRopeWsNorm>(a);
+    if (mode == kModeRopeWsFixedM) return launch_mode<128, kModeRopeWsFixedM>(a);
     if (mode == kModeRope) return launch_mode<128, kModeRope>(a);
     if (mode == kModeCross) return launch_mode<128, kModeCross>(a);
     return launch_mode<128, kModePlain>(a);
   }
   if (mode == kModeRopeWs) return launch_mode<64, kModeRopeWs>(a);
   if (mode == kModeRopeWsNorm) return launch_mode<64, kModeRopeWsNorm>(a);
+  if (mode == kModeRopeWsFixedM) return launch_mode<64, kModeRopeWsFixedM>(a);
   if (mode == kModeRope) return launch_mode<64, kModeRope>(a);
   if (mode == kModeCross) return launch_mode<64, kModeCross>(a);
   return launch_mode<64, kModePlain>(a);

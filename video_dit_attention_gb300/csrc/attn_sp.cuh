@@ -28,6 +28,12 @@
 // (64 KB). K and V share the ring, K one tile ahead of V, which gives a K load about two key
 // steps and a V load about one to land (two K and one V stage would leave V a fraction).
 
+// Fixed-m softmax: a warp keeps its rows' bounds m as the maximum when every valid row has
+// 2 m <= kFixedMSpanLog2 (log2 units). The bound is widened by kFixedMSlack to cover the
+// fp16 rounding of the rotated q and k (2^-11 each) and the fp32 norms.
+constexpr float kFixedMSpanLog2 = 64.f;
+constexpr float kFixedMSlack = 1.f + 1.f / 256.f;
+
 template <int D>
 struct CfgSp {
   static constexpr int kSub = D / 64;
@@ -49,6 +55,7 @@ struct BarsSp {
   uint32_t tmem_base;
   int abort;
   int aux_go;
+  int qn_items;   // fixed-m mode: items whose q row norms are written (warps 14-15 count)
 };
 
 // The key tiles a CTA visits, flattened over its items: tile g (g = 0 .. G-1) needs K_g for
@@ -64,6 +71,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                    const __grid_constant__ CUtensorMap tm_v, const KParams p, const WsParams ws) {
   static_assert(kMode == kModePlain || kMode == kModeCross || is_ws_mode(kMode), "mode");
   constexpr bool kWs = is_ws_mode(kMode), kNorm = kMode == kModeRopeWsNorm;
+  constexpr bool kFixedM = kMode == kModeRopeWsFixedM;
   using C = CfgSp<D>;
   constexpr int R = C::kRing;
   extern __shared__ uint8_t smem_raw[];
@@ -83,6 +91,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     bars->abort = 0;
+    bars->qn_items = 0;
     mbar_init(b_q_full, 1);
     mbar_init(b_q_ready, 1);
     mbar_init(b_q_empty, 1);
@@ -153,23 +162,48 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (kNorm)
             rotate_tile_smem_norm<D, 64>(sQ + t * C::kTileBytes, p.cos_q + row0, p.sin_q + row0, ws.norm_q,
                                          ws.norm_eps, at);
+          else if (kFixedM)
+            rotate_tile_smem_sq<D, 64>(sQ + t * C::kTileBytes, p.cos_q + row0, p.sin_q + row0, at,
+                                       ws.qn + (static_cast<size_t>(fw.b) * p.Sq + fw.q0 + 128 * t) * p.H + fw.h, p.H);
           else
             rotate_tile_smem<D, 64>(sQ + t * C::kTileBytes, p.cos_q + row0, p.sin_q + row0, at);
         }
         fence_proxy_async_smem();
         named_bar_sync(1, 64);
-        if (at == 0) mbar_arrive(b_q_ready);
+        if (at == 0) {
+          if (kFixedM) st_release_cta(&bars->qn_items, 1);
+          mbar_arrive(b_q_ready);
+        }
       }
     } else {
+      // Fixed-m mode: the largest squared key norm of each (b, h) among this CTA's rows is
+      // gathered in the (still unused) K/V ring, then merged into the workspace below.
+      unsigned int* kmax_s = reinterpret_cast<unsigned int*>(smem + C::kOffR);
+      if (kFixedM) {
+        for (int i = tid; i < ws.B * p.H; i += kRotK) kmax_s[i] = 0u;
+        named_bar_sync(2, kRotK);
+      }
       if (kNorm)
         rotate_rows_fp16_norm<D>(ws.k_raw, ws.k_rot, p.cos_k, p.sin_k, ws.norm_k, ws.norm_eps, ws.B, p.Skv,
                                  p.kv_valid, p.H, blockIdx.x * kRotK + tid, gridDim.x * kRotK);
+      else if (kFixedM)
+        rotate_rows_fp16_kmax<D>(ws.k_raw, ws.k_rot, p.cos_k, p.sin_k, ws.B, p.Skv, p.kv_valid, p.H,
+                                 blockIdx.x * kRotK + tid, gridDim.x * kRotK, kmax_s);
       else
         rotate_rows_fp16<D>(ws.k_raw, ws.k_rot, p.cos_k, p.sin_k, ws.B, p.Skv, p.kv_valid, p.H,
                             blockIdx.x * kRotK + tid, gridDim.x * kRotK);
       fence_proxy_async_all();
     }
     __syncthreads();
+    if (kFixedM) {
+      // Merge this CTA's maxima before it counts itself in: the release below covers them.
+      if (warp < 14) {
+        const unsigned int* kmax_s = reinterpret_cast<const unsigned int*>(smem + C::kOffR);
+        for (int i = tid; i < ws.B * p.H; i += kRotK)
+          if (kmax_s[i] != 0u) atomicMax(ws.kmax + i, kmax_s[i]);
+      }
+      __syncthreads();
+    }
     if (tid == 0) {
       __threadfence();
       atomicAdd(ws.rotated, 1u);
@@ -192,6 +226,45 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_proxy_async_all();   // the TMA loads that follow read what the other CTAs wrote
     ready = true;
     return true;
+  };
+  // Fixed-m mode: a warp waits (lane 0 polls, bounded) until the count at `c`, published with
+  // a CTA-scope release, reaches `target`; the warp barrier passes the acquire to all lanes.
+  auto wait_count = [&](const int* c, int target) -> bool {
+    int ok = 1;
+    if (lane == 0) {
+      const uint64_t t0 = globaltimer_ns();
+      while (ld_acquire_cta(c) < target) {
+        if (*abort_flag) { ok = 0; break; }
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+          *abort_flag = 1;
+          atomicOr(status, kStatusTimeoutSoftmax);
+          ok = 0;
+          break;
+        }
+      }
+    }
+    __syncwarp();
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+  };
+  // Fixed-m mode: a warp waits until every CTA has counted in its rotation (and with it its
+  // key-norm maxima), with a device-scope acquire.
+  auto wait_grid = [&]() -> bool {
+    int ok = 1;
+    if (lane == 0) {
+      const uint64_t t0 = globaltimer_ns();
+      while (ld_acquire_gpu(ws.rotated) < gridDim.x) {
+        if (*abort_flag) { ok = 0; break; }
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+          *abort_flag = 1;
+          atomicOr(status, kStatusTimeoutGrid);
+          ok = 0;
+          break;
+        }
+        __nanosleep(64);
+      }
+    }
+    __syncwarp();
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
   };
   // G: key tiles over all of this CTA's items.
   auto count_tiles = [&]() -> int {
@@ -419,15 +492,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t b_p_full = smem_u32(&bars->p_full[t]), b_pv_done = smem_u32(&bars->pv_done[t]);
     const float sl2 = p.scale_log2;
     int sc = 0;   // S_t tiles consumed so far (= P_t tiles produced = PV_t products issued)
+    int qi = 0;   // live items seen so far (fixed-m mode)
     bool ok = true;
     for (int it = it0; ok && it < p.n_items; it += it_step) {
       const Item w = decode_item<kMode>(p, it);
       if (t >= w.n_live) {
         if (t == 0 || w.has1) write_empty_tile<D>(p, w.b, w.h, w.q0 + 128 * t, r, 128);
+        if (w.n_live > 0) ++qi;
         continue;
       }
       const int n_kv = w.n_kv, kv_valid = w.kv_valid;
       float m_used = -INFINITY, l = 0.f;
+      bool fixed = false;   // fixed-m mode: this warp's 32 rows skip the running maximum
+      if constexpr (kFixedM) {
+        // Row bound m = scale * |q_row| * max_j |k_j| (log2 units here): no valid score of the
+        // row exceeds it (Cauchy-Schwarz; the rotation keeps norms). The warp keeps m fixed,
+        // with no maximum and no rescaling, when every valid row has 2 m <= 64: then the
+        // row's largest term exp2(s - m) is at least 2^-64. Pad rows (zero q, bound 0) and
+        // pad keys (never in the maximum) cannot move a warp onto the online path.
+        if (!(ok = wait_count(&bars->qn_items, qi + 1))) break;
+        if (qi == 0 && !(ok = wait_grid())) break;
+        const int qrow0 = w.q0 + 128 * t + r;
+        const float kq = __uint_as_float(ws.kmax[w.b * p.H + w.h]);
+        const float qn = ws.qn[(static_cast<size_t>(w.b) * p.Sq + qrow0) * p.H + w.h];
+        const float mb = sl2 * sqrtf(qn * kq) * kFixedMSlack;
+        fixed = __all_sync(0xffffffffu, qrow0 >= p.q_valid || mb <= 0.5f * kFixedMSpanLog2);
+        if (fixed)
+          m_used = mb;
+        else if (lane == 0 && ws.n_online != nullptr)
+          atomicAdd(ws.n_online, 1u);
+      }
       for (int j = 0; j < n_kv; ++j, ++sc) {
         if (!warp_wait(b_s_full, sc & 1, abort_flag, status, kStatusTimeoutSoftmax)) {
           ok = false;
@@ -453,16 +547,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 32; ++i)
               if (c * 32 + i >= nv) sr[c][i] = 0xff800000u;
         }
-        float mx4[4];
+        float mt = -INFINITY;   // a fixed warp keeps m_used: no rescale, alpha = 1
+        if (!fixed) {
+          float mx4[4];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          mx4[c] = fmaxf(__uint_as_float(sr[c][0]), __uint_as_float(sr[c][1]));
+          for (int c = 0; c < 4; ++c) {
+            mx4[c] = fmaxf(__uint_as_float(sr[c][0]), __uint_as_float(sr[c][1]));
 #pragma unroll
-          for (int i = 2; i < 32; i += 2)
-            mx4[c] = fmax3(mx4[c], __uint_as_float(sr[c][i]), __uint_as_float(sr[c][i + 1]));
+            for (int i = 2; i < 32; i += 2)
+              mx4[c] = fmax3(mx4[c], __uint_as_float(sr[c][i]), __uint_as_float(sr[c][i + 1]));
+          }
+          const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+          mt = mx * sl2;
         }
-        const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-        const float mt = mx * sl2;
         const bool resc = mt > m_used + kRescaleThreshold;
         const float m_new = resc ? mt : m_used;
         const float alpha = ex2_approx(m_used - m_new);   // 1 if kept; 0 on the first tile
@@ -571,6 +668,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       p.lse[(static_cast<size_t>(w.b) * p.Sq + qrow) * p.H + w.h] =
           valid_row ? (m_used + log2f(l)) * kLn2 : -INFINITY;
+      ++qi;
     }
   } else {
     regs_dec<72>();
@@ -601,12 +699,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (kNorm)
             rotate_tile_smem_norm<D, kRotThreads>(sQ + t * C::kTileBytes, p.cos_q + row0, p.sin_q + row0,
                                                   ws.norm_q, ws.norm_eps, at);
+          else if (kFixedM)
+            rotate_tile_smem_sq<D, kRotThreads>(sQ + t * C::kTileBytes, p.cos_q + row0, p.sin_q + row0, at,
+                                                ws.qn + (static_cast<size_t>(w.b) * p.Sq + w.q0 + 128 * t) * p.H + w.h,
+                                                p.H);
           else
             rotate_tile_smem<D, kRotThreads>(sQ + t * C::kTileBytes, p.cos_q + row0, p.sin_q + row0, at);
         }
         fence_proxy_async_smem();
         named_bar_sync(1, kRotThreads);
-        if (at == 0) mbar_arrive(b_q_ready);
+        if (at == 0) {
+          // Fixed-m mode: the q row norms of this item (the CTA's live item number q_cnt) are
+          // written; the softmax warps read them after an acquire of this count.
+          if (kFixedM) st_release_cta(&bars->qn_items, q_cnt + 1);
+          mbar_arrive(b_q_ready);
+        }
         ++q_cnt;
       }
     } else if (kMode == kModeCross) {

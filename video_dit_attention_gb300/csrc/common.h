@@ -29,6 +29,7 @@ struct AttnArgs {
   const float* norm_k;
   float norm_eps;
   cudaStream_t stream;
+  unsigned int* n_online;       // fixed-m mode: count of 32-row blocks on the online path (may be null)
 };
 
 enum AttnMode : int {
@@ -37,11 +38,19 @@ enum AttnMode : int {
   kModeCross = 2,  // no RoPE, per-batch kv length read on the device
   kModeRopeWs = 3, // RoPE applied once per q/k tile into a workspace, then attention on it
   kModeRopeWsNorm = 4,  // as kModeRopeWs, with per-head q/k RMSNorm before the rotation
+  kModeRopeWsFixedM = 5,  // as kModeRopeWs; 32-row blocks whose norm bound allows it skip the
+                          // running maximum (fixed-m softmax)
 };
 
 // Workspace layout of the RoPE workspace modes: rotated k [B, Skv, H, D] fp16, then a
 // 256-byte block holding the count of CTAs done rotating; both 256-byte aligned.
 size_t attn_workspace_bytes(int B, int Sq, int Skv, int H, int D);
+
+// Fixed-m mode: the layout above, then the per-(b, h) largest squared key norm [B * H] (u32
+// float bits, zeroed before the launch) and the per-row squared q norm [B, Sq, H] fp32, each
+// 256-byte aligned. The shared-memory reduction needs B * H <= kFixedMMaxHeads.
+size_t attn_fixed_m_workspace_bytes(int B, int Sq, int Skv, int H, int D);
+constexpr int kFixedMMaxHeads = 24576;
 
 cudaError_t launch_attn_fwd(const AttnArgs& a, AttnMode mode);
 

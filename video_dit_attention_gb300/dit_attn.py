@@ -47,6 +47,9 @@ _SIGNATURES = {
     "dit_attn_fwd_ws_qknorm": ([_vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _vp, _vp, _f, _vp, _vp, _vp, _vp,
                                 _f, _vp, _vp, _vp, ctypes.c_size_t, _vp], _i),
     "dit_qk_rmsnorm_rope": ([_vp, _vp, _vp, _f, _vp, _vp, _i, _i, _i, _i, _vp], _i),
+    "dit_attn_fixed_m_workspace_bytes": ([_i, _i, _i, _i, _i], ctypes.c_size_t),
+    "dit_attn_fwd_ws_fixed_m": ([_vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _f, _vp,
+                                 _vp, _vp, ctypes.c_size_t, _vp, _vp], _i),
 }
 for _name, (_args, _res) in _SIGNATURES.items():
     _fn = getattr(_lib, _name)
@@ -249,6 +252,42 @@ def dit_attn_fwd_ws_qknorm(q, k, v, q_valid_len: int, kv_valid_len: int, norm_q,
         _ptr(q), _ptr(k), _ptr(v), B, Sq, Skv, H, D, int(q_valid_len), int(kv_valid_len),
         _ptr(norm_q), _ptr(norm_k), float(eps), _ptr(cos_q), _ptr(sin_q), _ptr(cos_k), _ptr(sin_k),
         scale, _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(), _stream_handle(stream)))
+    return out, lse
+
+
+def dit_attn_fixed_m_workspace_bytes(B: int, Sq: int, Skv: int, H: int, D: int) -> int:
+    """Bytes of device workspace dit_attn_fwd_ws_fixed_m needs (0 for an invalid shape)."""
+    return int(_lib.dit_attn_fixed_m_workspace_bytes(B, Sq, Skv, H, D))
+
+
+def dit_attn_fwd_ws_fixed_m(q, k, v, q_valid_len: int, kv_valid_len: int, cos_q, sin_q, cos_k, sin_k,
+                            workspace=None, n_online=None, softmax_scale=None, out=None, lse=None,
+                            stream=None):
+    """dit_attn_fwd_ws with the fixed-m softmax: 32-row query blocks whose norm bound allows it
+    skip the running maximum. n_online: None or an int32/uint32-sized CUDA tensor [1] to which
+    the call adds the number of blocks that took the online path (the caller zeroes it)."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, torch.bfloat16, 4)
+    B, Sq, H, D = q.shape
+    Skv = k.shape[1]
+    if tuple(k.shape) != (B, Skv, H, D) or v.shape != k.shape:
+        raise ValueError("k and v must be [B, Skv, H, D] matching q")
+    for t, n, rows in ((cos_q, "cos_q", Sq), (sin_q, "sin_q", Sq), (cos_k, "cos_k", Skv), (sin_k, "sin_k", Skv)):
+        _need(t, n, torch.float32, 2)
+        if tuple(t.shape) != (rows, D // 2):
+            raise ValueError(f"{n} must be [{rows}, {D // 2}]")
+    need = dit_attn_fixed_m_workspace_bytes(B, Sq, Skv, H, D)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    _need(workspace, "workspace", torch.uint8, 1)
+    if n_online is not None:
+        _need(n_online, "n_online", torch.int32, 1)
+    scale = 1.0 / math.sqrt(D) if softmax_scale is None else float(softmax_scale)
+    out, lse = _attn_outputs(q, out, lse)
+    _check("dit_attn_fwd_ws_fixed_m", _lib.dit_attn_fwd_ws_fixed_m(
+        _ptr(q), _ptr(k), _ptr(v), B, Sq, Skv, H, D, int(q_valid_len), int(kv_valid_len),
+        _ptr(cos_q), _ptr(sin_q), _ptr(cos_k), _ptr(sin_k), scale, _ptr(out), _ptr(lse),
+        _ptr(workspace), workspace.numel(), _ptr(n_online), _stream_handle(stream)))
     return out, lse
 
 
