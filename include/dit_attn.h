@@ -200,6 +200,37 @@ int dit_attn_fwd_ws_fixed_m(const void* q, const void* k, const void* v, int B, 
                             size_t workspace_bytes, unsigned int* n_online, void* stream);
 
 /* ---------------------------------------------------------------------------------------
+ * FP8 (e4m3) attention. The pages measure FP8 only for linear layers (mstar PR #376: a sizing
+ * experiment with rowwise FP8 linears cut the SP2 step by about a quarter); this applies the
+ * e4m3 format (OCP 8-bit floating point: 4 exponent bits, bias 7, 3 mantissa bits, largest
+ * value 448) to the attention of dit_attn_fwd. Steps:
+ *   1. q and k are rotated (split-halves RoPE; no rotation when the four tables are NULL) in
+ *      fp32; q~ is quantised per 128-row tile of a head, k~ and v per head: scale = amax /
+ *      448 over the valid rows (1 when 0), x8 = e4m3(x / scale), round to nearest even,
+ *      saturating. v is stored transposed. All of it goes to `workspace`.
+ *   2. S = q8 k8^T on the tensor cores (e4m3 operands, fp32 accumulation), times
+ *      softmax_scale * s_q * s_k. Softmax over key tiles of 128 with a running maximum m that
+ *      lags by at most 2 in log2 units (so p = 2^(s log2 e - m) <= 4); P8 = e4m3(112 p),
+ *      O += P8 v8 (e4m3, fp32).
+ *   3. O = O * s_v / (112 l) with l = sum p in fp32, LSE = m + ln l; pad rows O = 0, LSE = -inf.
+ * Results differ from exact attention by the e4m3 rounding (about 0.04 max-abs on O and 0.02
+ * on the LSE for unit-variance inputs, one rounding per operand); against a reference doing
+ * the same steps they agree to fp32 accumulation and rare one-step rounding differences.
+ * D must be 128. workspace: at least dit_attn_fp8_workspace_bytes(B, Sq, Skv, H, 128) bytes,
+ * 256-byte aligned, caller-owned, contents on entry irrelevant; calls sharing one must not
+ * overlap. Three launches on `stream` (two preparation kernels, then the attention).
+ * Everything else (arguments, layouts, pad handling) as dit_attn_fwd. Errors: as dit_attn_fwd;
+ * DIT_ERR_UNSUPPORTED for D != 128; DIT_ERR_INVALID_ARG for a missing or too small workspace
+ * or some but not all tables; DIT_ERR_ALIGNMENT for a misaligned workspace (256) or table (8).
+ * ------------------------------------------------------------------------------------- */
+size_t dit_attn_fp8_workspace_bytes(int B, int Sq, int Skv, int H, int D);
+int dit_attn_fwd_fp8(const void* q, const void* k, const void* v, int B, int Sq, int Skv, int H,
+                     int D, int q_valid_len, int kv_valid_len, const float* cos_q,
+                     const float* sin_q, const float* cos_k, const float* sin_k,
+                     float softmax_scale, void* out, float* lse, void* workspace,
+                     size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------------------
  * Standalone per-head RMSNorm then split-halves RoPE (the prologue dit_attn_fwd_ws_qknorm
  * fuses): y[b,s,h,:] = rotate(x[b,s,h,:] / sqrt(mean(x^2) + eps) * w) with table row s.
  * x, y: [B, S, H, D] bf16 (y may equal x); w: device fp32 [D]; cos, sin: [S, D/2] fp32.

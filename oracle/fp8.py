@@ -17,13 +17,14 @@ Steps (readings of this repository; the pages fix none of them):
    q8 = e4m3(q~ / s_q). k~ and v are scaled once per (b, h) over the valid rows, the same
    way. Pad rows quantise to 0.
 2. Scores s_ij = scale * s_q * s_k * (q8_i . k8_j), exact products of e4m3 values summed.
-3. Softmax over key tiles of 128 in order, with the running maximum m in log2 units: m is
-   replaced by a tile's maximum x whenever x > m (the first tile sets it), so every
-   p = 2^(x_ij - m) <= 1 (x_ij = s_ij * log2(e)) and 448 p fits e4m3 without saturating.
-   (The bf16 path may let m lag by up to 8, so p <= 2^8; 448 p would then saturate.)
-   l accumulates p; P8 = e4m3(448 p); O accumulates P8 . v8. When m moves, l and O are
-   multiplied by 2^(m_old - m_new).
-4. Output O = O * s_v / (448 * l), LSE = (m + log2 l) * ln 2; pad rows O = 0, LSE = -inf.
+3. Softmax over key tiles of 128 in order, with a running maximum m in log2 units that may
+   lag by up to 2: m is replaced by a tile's maximum x only when x > m + 2 (the first tile
+   sets it), so every p = 2^(x_ij - m) <= 4 (x_ij = s_ij * log2(e)) and P8 = e4m3(112 p)
+   fits e4m3 without saturating. (The bf16 path lets m lag by up to 8, p <= 2^8, which
+   448-based scaling could not hold; an exact maximum would rescale O far more often.)
+   l accumulates p; O accumulates P8 . v8. When m moves, l and O are multiplied by
+   2^(m_old - m_new).
+4. Output O = O * s_v / (112 * l), LSE = (m + log2 l) * ln 2; pad rows O = 0, LSE = -inf.
 """
 from __future__ import annotations
 
@@ -32,7 +33,8 @@ import math
 import numpy as np
 
 E4M3_MAX = 448.0
-RESCALE_THRESHOLD_LOG2 = 0.0
+RESCALE_THRESHOLD_LOG2 = 2.0
+P_SCALE = E4M3_MAX / 2.0 ** RESCALE_THRESHOLD_LOG2   # 112: 448 over the largest p (4)
 TILE = 128
 
 
@@ -130,7 +132,7 @@ def attention_fp8(qr, kr, v, q_valid: int, kv_valid: int, scale: float, rows=Non
     if kv_valid == 0:
         return O, L
     log2e = 1.0 / math.log(2.0)
-    pscale = E4M3_MAX if round_fn is e4m3_round else 1.0
+    pscale = P_SCALE if round_fn is e4m3_round else 1.0
     for b in range(B):
         for h in heads:
             for i in rows:

@@ -131,7 +131,8 @@ def test_planted_mistakes_are_caught():
         F.RESCALE_THRESHOLD_LOG2 = -1e9            # m moves on every tile ...
         O1, _ = attention_fp8(qr, kr, v, qv, kv, scale, round_fn=lambda x: x)
         assert np.max(np.abs(O1 - O2)) <= 1e-12   # ... and the result is the same
-        # ... but with e4m3 rounding a lagging m (as the bf16 path allows) lets 448 p saturate
+        # ... but with e4m3 rounding and P still scaled by 112 (for p <= 4), letting m lag
+        # by 8 saturates 112 p: the error pin fails
         F.RESCALE_THRESHOLD_LOG2 = 8.0
         O8, _ = attention_fp8(qr, kr, v, qv, kv, scale)
         assert np.max(np.abs(O8 - O2)) > 0.1

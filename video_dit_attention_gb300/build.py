@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libdit_attn.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-CUDA_SOURCES = ["attn_fwd.cu", "elementwise.cu", "api.cu"]
+CUDA_SOURCES = ["attn_fwd.cu", "elementwise.cu", "fp8.cu", "api.cu"]
 CXX_SOURCES = ["rope_table.cpp"]
 
 

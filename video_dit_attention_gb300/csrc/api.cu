@@ -74,6 +74,19 @@ bool encode_bshd_map(CUtensorMap* map, const void* base, int B, int s_extent, in
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_u8_map4(CUtensorMap* map, const void* base, const unsigned long long dims[4],
+                    const unsigned long long strides[3], const unsigned int box[4]) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t d[4] = {dims[0], dims[1], dims[2], dims[3]};
+  const cuuint64_t st[3] = {strides[0], strides[1], strides[2]};
+  const cuuint32_t bx[4] = {box[0], box[1], box[2], box[3]};
+  const cuuint32_t elem_strides[4] = {1, 1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), d, st, bx, elem_strides,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool encode_rows_map_f32(CUtensorMap* map, const float* base, int rows, int cols, int box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
@@ -189,6 +202,32 @@ extern "C" int dit_attn_fwd_ws_fixed_m(const void* q, const void* k, const void*
              cos_q, sin_q, cos_k, sin_k, softmax_scale, out, lse, workspace, nullptr, nullptr, 0.f,
              static_cast<cudaStream_t>(stream), n_online};
   return cuda_status(launch_attn_fwd(a, kModeRopeWsFixedM));
+}
+
+extern "C" size_t dit_attn_fp8_workspace_bytes(int B, int Sq, int Skv, int H, int D) {
+  if (B < 1 || Sq < 1 || Skv < 1 || H < 1 || D != 128) return 0;
+  return fp8_layout(B, Sq, Skv, H, D).total;
+}
+
+extern "C" int dit_attn_fwd_fp8(const void* q, const void* k, const void* v, int B, int Sq, int Skv,
+                                int H, int D, int q_valid_len, int kv_valid_len, const float* cos_q,
+                                const float* sin_q, const float* cos_k, const float* sin_k,
+                                float softmax_scale, void* out, float* lse, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+  int st = check_attn_shapes(q, k, v, B, Sq, Skv, H, D, q_valid_len, softmax_scale, out, lse);
+  if (st != DIT_OK) return st;
+  if (D != 128) return DIT_ERR_UNSUPPORTED;
+  if (kv_valid_len < 0 || kv_valid_len > Skv || !workspace) return DIT_ERR_INVALID_ARG;
+  const int n_tab = (cos_q != nullptr) + (sin_q != nullptr) + (cos_k != nullptr) + (sin_k != nullptr);
+  if (n_tab != 0 && n_tab != 4) return DIT_ERR_INVALID_ARG;
+  if (workspace_bytes < fp8_layout(B, Sq, Skv, H, D).total) return DIT_ERR_INVALID_ARG;
+  if (n_tab == 4 && (!aligned(cos_q, 8) || !aligned(sin_q, 8) || !aligned(cos_k, 8) || !aligned(sin_k, 8)))
+    return DIT_ERR_ALIGNMENT;
+  if (!aligned(workspace, 256)) return DIT_ERR_ALIGNMENT;
+  AttnArgs a{q, k, v, B, Sq, Skv, H, D, q_valid_len, kv_valid_len, nullptr,
+             cos_q, sin_q, cos_k, sin_k, softmax_scale, out, lse, workspace, nullptr, nullptr, 0.f,
+             static_cast<cudaStream_t>(stream), nullptr};
+  return cuda_status(launch_attn_fwd(a, kModeFp8));
 }
 
 extern "C" int dit_attn_fwd_ws_qknorm(const void* q, const void* k, const void* v, int B, int Sq,

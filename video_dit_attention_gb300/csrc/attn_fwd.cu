@@ -125,6 +125,10 @@ struct WsParams {
   unsigned int* kmax;      // fixed-m mode: largest squared key norm per (b, h), float bits
   float* qn;               // fixed-m mode: squared norm of each q row [B, Sq, H]
   unsigned int* n_online;  // fixed-m mode: blocks that took the online path (may be null)
+  const float* f8_sq;      // FP8 mode: q~ scale per (b, h, 128-row tile) [B, H, f8_nt_q]
+  const float* f8_sk;      // FP8 mode: k~ scale per (b, h)
+  const float* f8_sv;      // FP8 mode: v scale per (b, h)
+  int f8_nt_q;
 };
 
 // The RoPE workspace modes (plain, with the q/k RMSNorm, fixed-m softmax).
@@ -1000,10 +1004,31 @@ cudaError_t launch_mode(const AttnArgs& a) {
   // Cross-attention reads up to Skv rows and masks per batch on the device; self-attention
   // cuts the key/value extent to the valid length so pad rows are never even loaded.
   const int kvext = (kMode == kModeCross) ? a.Skv : (a.kv_valid > 0 ? a.kv_valid : 1);
-  if (!encode_bshd_map(&mq, q_src, a.B, qext, a.Sq, a.H, D) ||
-      !encode_bshd_map(&mk, k_src, a.B, kvext, a.Skv, a.H, D) ||
-      !encode_bshd_map(&mv, a.v, a.B, kvext, a.Skv, a.H, D))
+  [[maybe_unused]] Fp8Layout f8{};
+  if constexpr (kMode == kModeFp8) {
+    // Rotate and quantise q, k, v into the workspace, then read the e4m3 copies: q~ and k~
+    // as [B, S, H, D] bytes (one 128-byte row per token and head), v transposed [B, H, D, S].
+    f8 = fp8_layout(a.B, a.Sq, a.Skv, a.H, D);
+    const cudaError_t e8 = launch_fp8_prepare(a, f8);
+    if (e8 != cudaSuccess) return e8;
+    char* wsb = static_cast<char*>(a.workspace);
+    using u64 = unsigned long long;
+    const u64 HD = static_cast<u64>(a.H) * D;
+    const u64 dq[4] = {static_cast<u64>(D), static_cast<u64>(a.H), static_cast<u64>(qext), static_cast<u64>(a.B)};
+    const u64 sq[3] = {static_cast<u64>(D), HD, HD * a.Sq};
+    const u64 dk[4] = {static_cast<u64>(D), static_cast<u64>(a.H), static_cast<u64>(kvext), static_cast<u64>(a.B)};
+    const u64 sk[3] = {static_cast<u64>(D), HD, HD * a.Skv};
+    const u64 dv[4] = {static_cast<u64>(kvext), static_cast<u64>(D), static_cast<u64>(a.H), static_cast<u64>(a.B)};
+    const u64 sv[3] = {static_cast<u64>(a.Skv), static_cast<u64>(D) * a.Skv, HD * a.Skv};
+    const unsigned int box_rows[4] = {128, 1, 128, 1}, box_vt[4] = {128, 128, 1, 1};
+    if (!encode_u8_map4(&mq, wsb + f8.q8, dq, sq, box_rows) || !encode_u8_map4(&mk, wsb + f8.k8, dk, sk, box_rows) ||
+        !encode_u8_map4(&mv, wsb + f8.vt8, dv, sv, box_vt))
+      return cudaErrorInvalidValue;
+  } else if (!encode_bshd_map(&mq, q_src, a.B, qext, a.Sq, a.H, D) ||
+             !encode_bshd_map(&mk, k_src, a.B, kvext, a.Skv, a.H, D) ||
+             !encode_bshd_map(&mv, a.v, a.B, kvext, a.Skv, a.H, D)) {
     return cudaErrorInvalidValue;
+  }
   // RoPE tables [rows, D/2] fp32, read 32 rows at a time (a copy of the Q map when unused).
   CUtensorMap mcq = mq, msq = mq, mck = mq, msk = mq;
   if (kMode == kModeRope) {
@@ -1040,6 +1065,15 @@ cudaError_t launch_mode(const AttnArgs& a) {
   ws.kmax = nullptr;
   ws.qn = nullptr;
   ws.n_online = a.n_online;
+  ws.f8_sq = ws.f8_sk = ws.f8_sv = nullptr;
+  ws.f8_nt_q = 0;
+  if constexpr (kMode == kModeFp8) {
+    const char* wsb = static_cast<const char*>(a.workspace);
+    ws.f8_sq = reinterpret_cast<const float*>(wsb + f8.sq);
+    ws.f8_sk = reinterpret_cast<const float*>(wsb + f8.sk);
+    ws.f8_sv = reinterpret_cast<const float*>(wsb + f8.sv);
+    ws.f8_nt_q = f8.nt_q;
+  }
   size_t zero_bytes = sizeof(unsigned int);   // what the launch clears: the CTA counter
   if (is_ws_mode(kMode)) {
     const size_t k_bytes = (static_cast<size_t>(a.B) * a.Skv * a.H * D * 2 + 255) / 256 * 256;
@@ -1068,10 +1102,11 @@ cudaError_t launch_mode(const AttnArgs& a) {
     return cudaGetLastError();
   } else {
     auto kern = attn_sp_kernel<D, kMode>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, CfgSp<D>::kSmemBytes);
+    constexpr int kSmem = CfgSp<D, kMode == kModeFp8>::kSmemBytes;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
     if (!is_ws_mode(kMode)) {
-      kern<<<grid, kThreads, CfgSp<D>::kSmemBytes, a.stream>>>(mq, mk, mv, p, ws);
+      kern<<<grid, kThreads, kSmem, a.stream>>>(mq, mk, mv, p, ws);
       return cudaGetLastError();
     }
     // CTAs wait for rotated rows that other CTAs produce: launch cooperatively so that every
@@ -1080,7 +1115,7 @@ cudaError_t launch_mode(const AttnArgs& a) {
     if (e != cudaSuccess) return e;
     void* args[] = {&mq, &mk, &mv, &p, &ws};
     return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kern), dim3(grid), dim3(kThreads),
-                                       args, CfgSp<D>::kSmemBytes, a.stream);
+                                       args, kSmem, a.stream);
   }
 }
 
@@ -1103,6 +1138,7 @@ cudaError_t launch_attn_fwd(const AttnArgs& a, AttnMode mode) {
     if (mode == kModeRopeWs) return launch_mode<128, kModeRopeWs>(a);
     if (mode == kModeRopeWsNorm) return launch_mode<128, kModeRopeWsNorm>(a);
     if (mode == kModeRopeWsFixedM) return launch_mode<128, kModeRopeWsFixedM>(a);
+    if (mode == kModeFp8) return launch_mode<128, kModeFp8>(a);
     if (mode == kModeRope) return launch_mode<128, kModeRope>(a);
     if (mode == kModeCross) return launch_mode<128, kModeCross>(a);
     return launch_mode<128, kModePlain>(a);
@@ -1110,6 +1146,7 @@ cudaError_t launch_attn_fwd(const AttnArgs& a, AttnMode mode) {
   if (mode == kModeRopeWs) return launch_mode<64, kModeRopeWs>(a);
   if (mode == kModeRopeWsNorm) return launch_mode<64, kModeRopeWsNorm>(a);
   if (mode == kModeRopeWsFixedM) return launch_mode<64, kModeRopeWsFixedM>(a);
+  if (mode == kModeFp8) return cudaErrorInvalidValue;   // built for D = 128 only
   if (mode == kModeRope) return launch_mode<64, kModeRope>(a);
   if (mode == kModeCross) return launch_mode<64, kModeCross>(a);
   return launch_mode<64, kModePlain>(a);

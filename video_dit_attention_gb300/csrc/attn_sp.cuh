@@ -32,18 +32,30 @@
 // 2 m <= kFixedMSpanLog2 (log2 units). The bound is widened by kFixedMSlack to cover the
 // fp16 rounding of the rotated q and k (2^-11 each) and the fp32 norms.
 constexpr float kFixedMSpanLog2 = 64.f;
+
+// FP8 softmax: the running maximum may lag by up to kFp8RescaleThreshold (log2 units), so
+// p <= 4, and P is stored as e4m3(kFp8PScale * p) with kFp8PScale = 448 / 4 (no saturation).
+constexpr float kFp8RescaleThreshold = 2.f;
+constexpr float kFp8PScale = 112.f;
 constexpr float kFixedMSlack = 1.f + 1.f / 256.f;
 
-template <int D>
+// Shared-memory layout. bf16 modes: K/V tiles of 128 rows x D bf16 (D / 64 chunks of 128-byte
+// swizzled rows), P of 128 x 128 bf16 in two chunks. FP8 mode (D = 128): every operand tile
+// is 128 rows x 128 bytes (one chunk), so the ring has six slots, and O is staged for its
+// bf16 store in an area of its own.
+template <int D, bool kFp8 = false>
 struct CfgSp {
-  static constexpr int kSub = D / 64;
-  static constexpr int kTileBytes = 128 * D * 2;
-  static constexpr int kRing = (D == 128) ? 3 : 6;        // K/V ring slots
-  static constexpr int kPBytes = 128 * 128 * 2;           // P tile: 128 query rows x 128 keys
+  static constexpr int kElem = kFp8 ? 1 : 2;
+  static constexpr int kSub = D * kElem / 128;          // 128-byte chunks per operand row
+  static constexpr int kTileBytes = 128 * D * kElem;
+  static constexpr int kRing = (kFp8 || D != 128) ? 6 : 3;   // K/V ring slots
+  static constexpr int kPBytes = 128 * 128 * kElem;     // P tile: 128 query rows x 128 keys
+  static constexpr int kOBytes = kFp8 ? 128 * D * 2 : 0;   // FP8: bf16 O staging per query tile
   static constexpr int kOffQ = 0;
   static constexpr int kOffR = kOffQ + 2 * kTileBytes;
   static constexpr int kOffP = kOffR + kRing * kTileBytes;
-  static constexpr int kOffBar = kOffP + 2 * kPBytes;
+  static constexpr int kOffO = kOffP + 2 * kPBytes;
+  static constexpr int kOffBar = kOffO + 2 * kOBytes;
   static constexpr int kSmemBytes = kOffBar + 512 + 1024;  // barriers + alignment slack
 };
 
@@ -69,10 +81,12 @@ template <int D, int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_sp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const KParams p, const WsParams ws) {
-  static_assert(kMode == kModePlain || kMode == kModeCross || is_ws_mode(kMode), "mode");
+  static_assert(kMode == kModePlain || kMode == kModeCross || kMode == kModeFp8 || is_ws_mode(kMode), "mode");
+  constexpr bool kFp8 = kMode == kModeFp8;
+  static_assert(!kFp8 || D == 128, "the FP8 path is built for D = 128");
   constexpr bool kWs = is_ws_mode(kMode), kNorm = kMode == kModeRopeWsNorm;
   constexpr bool kFixedM = kMode == kModeRopeWsFixedM;
-  using C = CfgSp<D>;
+  using C = CfgSp<D, kFp8>;
   constexpr int R = C::kRing;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -81,6 +95,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sQ = s_base + C::kOffQ;
   const uint32_t sR = s_base + C::kOffR;
   const uint32_t sP = s_base + C::kOffP;
+  const uint32_t sO = s_base + C::kOffO;   // FP8: O staging (the bf16 modes stage O in P)
   BarsSp* bars = reinterpret_cast<BarsSp*>(smem + C::kOffBar);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -287,7 +302,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
   auto s_issuer = [&]() {
     // ------------------------------------------------------------ S_t = Q_t K_g^T
-    constexpr uint32_t kIdS = idesc_f16kind_f32(128, 128, !kWs, false, false);
+    // bf16 (or fp16 when q/k were rotated) operands, or e4m3 in the FP8 path (format 0 in
+    // both cases: f16 for kind::f16, e4m3 for kind::f8f6f4).
+    constexpr uint32_t kIdS = idesc_f16kind_f32(128, 128, !kWs && !kFp8, false, false);
+    constexpr int kKStep = kFp8 ? 32 : 16;   // K elements per MMA (32 bytes of each row)
     int g0 = 0, q_cnt = 0, ns0 = 0, ns1 = 0;
     bool ok = true;
     for (int it = it0; ok && it < p.n_items; it += it_step) {
@@ -311,9 +329,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint64_t da = smem_desc_sw128(sQ + t * C::kTileBytes, 16, 1024);
           const uint32_t d = tbase + t * 128;
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
+          for (int kk = 0; kk < D / kKStep; ++kk) {
             const uint64_t off = ((kk / 4) * 16384 + (kk % 4) * 32) >> 4;
-            mma_bf16_ss(d, da + off, db + off, kIdS, kk > 0);
+            if constexpr (kFp8)
+              mma_e4m3_ss(d, da + off, db + off, kIdS, kk > 0);
+            else
+              mma_bf16_ss(d, da + off, db + off, kIdS, kk > 0);
           }
           mma_commit(smem_u32(&bars->s_full[t]));
           if (t) ++ns1; else ++ns0;
@@ -334,7 +355,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
   auto pv_issuer = [&]() {
     // ------------------------------------------------------------ O_t (+)= P_t V_g
-    constexpr uint32_t kIdO = idesc_bf16_f32(128, D, false, true);
+    // bf16: A = P (K-major), B = V tile (MN-major). FP8: both e4m3 and K-major (V transposed).
+    constexpr uint32_t kIdO = kFp8 ? idesc_f16kind_f32(128, D, false, false, false) : idesc_bf16_f32(128, D, false, true);
     int g0 = 0, np0 = 0, np1 = 0, epi0 = 0, epi1 = 0;
     const int G = count_tiles();
     bool ok = true;
@@ -347,7 +369,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!(ok = wait_bar(kMode == kModeCross ? smem_u32(&bars->r_ready[slot]) : smem_u32(&bars->r_full[slot]),
                             n / R)))
           break;
-        const uint64_t db = smem_desc_sw128(sR + slot * C::kTileBytes, 16384, 1024);
+        const uint64_t db = smem_desc_sw128(sR + slot * C::kTileBytes, kFp8 ? 16 : 16384, 1024);
         for (int t = 0; t < w.n_live; ++t) {
           const int np = t ? np1 : np0, epi = t ? epi1 : epi0;
           if (!(ok = wait_bar(smem_u32(&bars->p_full[t]), np))) break;
@@ -356,11 +378,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (j == 0 && epi > 0 && !(ok = wait_bar(smem_u32(&bars->o_free[t]), epi - 1))) break;
           const uint64_t da = smem_desc_sw128(sP + t * C::kPBytes, 16, 1024);
           const uint32_t d = tbase + 256 + t * 128;
+          if constexpr (kFp8) {
+            // 128 keys in four K steps of 32 bytes, within the one 128-byte row of P and of V^T.
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const uint64_t offa = ((kk / 4) * 16384 + (kk % 4) * 32) >> 4;
-            mma_bf16_ss(d, da + offa, db + static_cast<uint64_t>(kk * 2048 >> 4), kIdO,
-                        (j > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < 4; ++kk)
+              mma_e4m3_ss(d, da + static_cast<uint64_t>(kk * 2), db + static_cast<uint64_t>(kk * 2), kIdO,
+                          (j > 0 || kk > 0) ? 1u : 0u);
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint64_t offa = ((kk / 4) * 16384 + (kk % 4) * 32) >> 4;
+              mma_bf16_ss(d, da + offa, db + static_cast<uint64_t>(kk * 2048 >> 4), kIdO,
+                          (j > 0 || kk > 0) ? 1u : 0u);
+            }
           }
           mma_commit(smem_u32(&bars->pv_done[t]));
           if (t) ++np1; else ++np0;
@@ -419,9 +449,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           return false;
         const uint32_t bar = smem_u32(&bars->r_full[slot]);
         mbar_arrive_expect_tx(bar, C::kTileBytes);
+        if (kFp8 && map == &tm_v) {
+          // FP8 V is stored transposed, [B, H, D, S]: the tile is D rows of 128 keys.
+          tma_load_4d(sR + slot * C::kTileBytes, map, bar, j * 128, 0, w.h, w.b);
+        } else {
 #pragma unroll
-        for (int c = 0; c < C::kSub; ++c)
-          tma_load_4d(sR + slot * C::kTileBytes + c * 16384, map, bar, c * 64, w.h, j * 128, w.b);
+          for (int c = 0; c < C::kSub; ++c)
+            tma_load_4d(sR + slot * C::kTileBytes + c * 16384, map, bar, c * 64, w.h, j * 128, w.b);
+        }
         ++n;
         return true;
       };
@@ -444,7 +479,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int c = 0; c < C::kSub; ++c) {
                 tma_prefetch_l2_4d(&tm_k, c * 64, nw.h, jj * 128, nw.b);
-                tma_prefetch_l2_4d(&tm_v, c * 64, nw.h, jj * 128, nw.b);
+                if (kFp8)
+                  tma_prefetch_l2_4d(&tm_v, jj * 128, 0, nw.h, nw.b);
+                else
+                  tma_prefetch_l2_4d(&tm_v, c * 64, nw.h, jj * 128, nw.b);
               }
           }
         }
@@ -503,6 +541,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const int n_kv = w.n_kv, kv_valid = w.kv_valid;
       float m_used = -INFINITY, l = 0.f;
+      // FP8: scores come out of the MMA in units of the q tile's and the head's k scales.
+      const float sl2e = kFp8 ? sl2 * ws.f8_sq[(w.b * p.H + w.h) * ws.f8_nt_q + (w.q0 >> 7) + t] *
+                                    ws.f8_sk[w.b * p.H + w.h]
+                              : sl2;
       bool fixed = false;   // fixed-m mode: this warp's 32 rows skip the running maximum
       if constexpr (kFixedM) {
         // Row bound m = scale * |q_row| * max_j |k_j| (log2 units here): no valid score of the
@@ -558,9 +600,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               mx4[c] = fmax3(mx4[c], __uint_as_float(sr[c][i]), __uint_as_float(sr[c][i + 1]));
           }
           const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-          mt = mx * sl2;
+          mt = mx * sl2e;
         }
-        const bool resc = mt > m_used + kRescaleThreshold;
+        // FP8 lets the maximum lag by at most 2 (p <= 4), so that 112 p fits e4m3.
+        const bool resc = mt > m_used + (kFp8 ? kFp8RescaleThreshold : kRescaleThreshold);
         const float m_new = resc ? mt : m_used;
         const float alpha = ex2_approx(m_used - m_new);   // 1 if kept; 0 on the first tile
         if (j > 0) {
@@ -587,21 +630,28 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int k = 0; k < 4; ++k) l4[k] = 0.f;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {           // 16 keys at a time: two 16-byte units
+        for (int c = 0; c < 8; ++c) {           // 16 keys at a time: two 16-byte units (bf16)
           uint32_t pk[8];
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             float x0, x1;
             fma2_bc(x0, x1, __uint_as_float(sr[c >> 1][(c & 1) * 16 + 2 * i]),
-                    __uint_as_float(sr[c >> 1][(c & 1) * 16 + 2 * i + 1]), sl2, neg_m);
+                    __uint_as_float(sr[c >> 1][(c & 1) * 16 + 2 * i + 1]), sl2e, neg_m);
             const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
             add2(l4[2 * (i & 1)], l4[2 * (i & 1) + 1], p0, p1);
-            pk[i] = pack_bf16x2(p0, p1);
+            pk[i] = kFp8 ? pack_e4m3x2(kFp8PScale * p0, kFp8PScale * p1) : pack_bf16x2(p0, p1);
           }
-          const uint32_t chunk = static_cast<uint32_t>(c >> 2) * 16384u;
-          const uint32_t x0 = static_cast<uint32_t>((2 * c) & 7), x1 = static_cast<uint32_t>((2 * c + 1) & 7);
-          sts128(p_row + chunk + ((x0 ^ p_sw) << 4), make_uint4(pk[0], pk[1], pk[2], pk[3]));
-          sts128(p_row + chunk + ((x1 ^ p_sw) << 4), make_uint4(pk[4], pk[5], pk[6], pk[7]));
+          if constexpr (kFp8) {
+            // 16 e4m3 keys: one 16-byte unit of the single 128-byte P row.
+            sts128(p_row + ((static_cast<uint32_t>(c) ^ p_sw) << 4),
+                   make_uint4(pk[0] | (pk[1] << 16), pk[2] | (pk[3] << 16), pk[4] | (pk[5] << 16),
+                              pk[6] | (pk[7] << 16)));
+          } else {
+            const uint32_t chunk = static_cast<uint32_t>(c >> 2) * 16384u;
+            const uint32_t x0 = static_cast<uint32_t>((2 * c) & 7), x1 = static_cast<uint32_t>((2 * c + 1) & 7);
+            sts128(p_row + chunk + ((x0 ^ p_sw) << 4), make_uint4(pk[0], pk[1], pk[2], pk[3]));
+            sts128(p_row + chunk + ((x1 ^ p_sw) << 4), make_uint4(pk[4], pk[5], pk[6], pk[7]));
+          }
         }
         l = l * alpha + ((l4[0] + l4[1]) + (l4[2] + l4[3]));
         fence_proxy_async_smem();   // P (generic stores) before the MMA's async-proxy reads
@@ -618,7 +668,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after_sync();
       const int qrow = w.q0 + 128 * t + r;
       const bool valid_row = qrow < p.q_valid;
-      const float inv_l = 1.f / l;
+      // FP8: O came out in units of kFp8PScale (P) and of the head's v scale.
+      const float inv_l = kFp8 ? ws.f8_sv[w.b * p.H + w.h] / (kFp8PScale * l) : 1.f / l;
+      const uint32_t st_row = kFp8 ? sO + t * C::kOBytes + r * 128 : p_row;   // staging row
       // The warp stages its 32 normalised rows in its own rows of the P_t buffer, in the P
       // layout (row r, 16-byte unit x of 64-column chunk c at c * 16384 + r * 128 +
       // ((x ^ (r & 7)) * 16)), so no other warp reads or writes those bytes. It then writes
@@ -643,7 +695,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             o.z = pack_bf16x2(__uint_as_float(f[4]) * inv_l, __uint_as_float(f[5]) * inv_l);
             o.w = pack_bf16x2(__uint_as_float(f[6]) * inv_l, __uint_as_float(f[7]) * inv_l);
           }
-          sts128(p_row + static_cast<uint32_t>(u >> 3) * 16384u + ((static_cast<uint32_t>(u & 7) ^ p_sw) << 4), o);
+          sts128(st_row + static_cast<uint32_t>(u >> 3) * 16384u + ((static_cast<uint32_t>(u & 7) ^ p_sw) << 4), o);
         }
       }
       __syncwarp();
@@ -659,7 +711,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll kStoreUnroll
         for (int i = 0; i < 32 / kRPI; ++i) {
           const int rr = r0 + i * kRPI + lr;
-          const uint32_t src = sP + t * C::kPBytes + chunk + static_cast<uint32_t>(rr) * 128u +
+          const uint32_t src = (kFp8 ? sO + t * C::kOBytes : sP + t * C::kPBytes) + chunk + static_cast<uint32_t>(rr) * 128u +
                                ((unit ^ static_cast<uint32_t>(rr & 7)) << 4);
           uint16_t* dst = p.out + ((static_cast<size_t>(w.b) * p.Sq + w.q0 + 128 * t + rr) * p.H + w.h) * D;
           *reinterpret_cast<uint4*>(dst + lu * 8) = lds128(src);

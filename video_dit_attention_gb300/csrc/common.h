@@ -40,6 +40,8 @@ enum AttnMode : int {
   kModeRopeWsNorm = 4,  // as kModeRopeWs, with per-head q/k RMSNorm before the rotation
   kModeRopeWsFixedM = 5,  // as kModeRopeWs; 32-row blocks whose norm bound allows it skip the
                           // running maximum (fixed-m softmax)
+  kModeFp8 = 6,           // e4m3 q~, k~ (rotated) and v (transposed) prepared in the workspace;
+                          // e4m3 tensor-core products, exact running maximum
 };
 
 // Workspace layout of the RoPE workspace modes: rotated k [B, Skv, H, D] fp16, then a
@@ -51,6 +53,17 @@ size_t attn_workspace_bytes(int B, int Sq, int Skv, int H, int D);
 // 256-byte aligned. The shared-memory reduction needs B * H <= kFixedMMaxHeads.
 size_t attn_fixed_m_workspace_bytes(int B, int Sq, int Skv, int H, int D);
 constexpr int kFixedMMaxHeads = 24576;
+
+// FP8 path workspace (D = 128): e4m3 q~ [B, Sq, H, D], k~ [B, Skv, H, D], v transposed
+// [B, H, D, Skv]; tile maxima of q~, k~, v; scales of q~ per tile [B, H, nt_q], of k~ and v per
+// head [B, H]. Offsets in bytes, each 256-byte aligned.
+struct Fp8Layout {
+  size_t q8, k8, vt8, amax_q, amax_k, amax_v, sq, sk, sv, total;
+  int nt_q, nt_k;
+};
+Fp8Layout fp8_layout(int B, int Sq, int Skv, int H, int D);
+// Rotation and quantisation of q, k, v into the workspace (two launches on a.stream).
+cudaError_t launch_fp8_prepare(const AttnArgs& a, const Fp8Layout& L);
 
 cudaError_t launch_attn_fwd(const AttnArgs& a, AttnMode mode);
 
@@ -76,6 +89,11 @@ cudaError_t read_device_status(unsigned int* out, bool clear);
 // 128 rows x 1 batch and the 128-byte swizzle. Returns false if the driver rejects it.
 bool encode_bshd_map(CUtensorMap* map, const void* base, int B, int s_extent, int s_rows, int H,
                      int D);
+
+// Encodes a 4-D TMA descriptor for a uint8 tensor (dims innermost first, strides in bytes of
+// dims 1..3) with the 128-byte swizzle; box[0] * 1 byte must be a multiple of 16.
+bool encode_u8_map4(CUtensorMap* map, const void* base, const unsigned long long dims[4],
+                    const unsigned long long strides[3], const unsigned int box[4]);
 
 // Encodes a TMA descriptor for a row-major fp32 matrix [rows, cols] (cols * 4 a multiple of
 // 16 bytes) read in unswizzled boxes of box_rows full rows.

@@ -48,6 +48,9 @@ _SIGNATURES = {
                                 _f, _vp, _vp, _vp, ctypes.c_size_t, _vp], _i),
     "dit_qk_rmsnorm_rope": ([_vp, _vp, _vp, _f, _vp, _vp, _i, _i, _i, _i, _vp], _i),
     "dit_attn_fixed_m_workspace_bytes": ([_i, _i, _i, _i, _i], ctypes.c_size_t),
+    "dit_attn_fp8_workspace_bytes": ([_i, _i, _i, _i, _i], ctypes.c_size_t),
+    "dit_attn_fwd_fp8": ([_vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _f, _vp, _vp,
+                          _vp, ctypes.c_size_t, _vp], _i),
     "dit_attn_fwd_ws_fixed_m": ([_vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _f, _vp,
                                  _vp, _vp, ctypes.c_size_t, _vp, _vp], _i),
 }
@@ -288,6 +291,41 @@ def dit_attn_fwd_ws_fixed_m(q, k, v, q_valid_len: int, kv_valid_len: int, cos_q,
         _ptr(q), _ptr(k), _ptr(v), B, Sq, Skv, H, D, int(q_valid_len), int(kv_valid_len),
         _ptr(cos_q), _ptr(sin_q), _ptr(cos_k), _ptr(sin_k), scale, _ptr(out), _ptr(lse),
         _ptr(workspace), workspace.numel(), _ptr(n_online), _stream_handle(stream)))
+    return out, lse
+
+
+def dit_attn_fp8_workspace_bytes(B: int, Sq: int, Skv: int, H: int, D: int) -> int:
+    """Bytes of device workspace dit_attn_fwd_fp8 needs (0 for an invalid shape or D != 128)."""
+    return int(_lib.dit_attn_fp8_workspace_bytes(B, Sq, Skv, H, D))
+
+
+def dit_attn_fwd_fp8(q, k, v, q_valid_len: int, kv_valid_len: int, cos_q=None, sin_q=None, cos_k=None,
+                     sin_k=None, workspace=None, softmax_scale=None, out=None, lse=None, stream=None):
+    """FP8 (e4m3) attention (D = 128): q~ quantised per 128-row tile, k~ and v per head, P as
+    e4m3(112 p) (the running maximum lags by at most 2 in log2 units); tables as in
+    dit_attn_fwd (all four, or none for no RoPE)."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, torch.bfloat16, 4)
+    B, Sq, H, D = q.shape
+    Skv = k.shape[1]
+    if tuple(k.shape) != (B, Skv, H, D) or v.shape != k.shape:
+        raise ValueError("k and v must be [B, Skv, H, D] matching q")
+    tabs = (cos_q, sin_q, cos_k, sin_k)
+    if any(t is not None for t in tabs):
+        for t, n, rows in zip(tabs, ("cos_q", "sin_q", "cos_k", "sin_k"), (Sq, Sq, Skv, Skv)):
+            _need(t, n, torch.float32, 2)
+            if tuple(t.shape) != (rows, D // 2):
+                raise ValueError(f"{n} must be [{rows}, {D // 2}]")
+    need = dit_attn_fp8_workspace_bytes(B, Sq, Skv, H, D)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    _need(workspace, "workspace", torch.uint8, 1)
+    scale = 1.0 / math.sqrt(D) if softmax_scale is None else float(softmax_scale)
+    out, lse = _attn_outputs(q, out, lse)
+    _check("dit_attn_fwd_fp8", _lib.dit_attn_fwd_fp8(
+        _ptr(q), _ptr(k), _ptr(v), B, Sq, Skv, H, D, int(q_valid_len), int(kv_valid_len),
+        *(_ptr(t) for t in tabs), scale, _ptr(out), _ptr(lse), _ptr(workspace), workspace.numel(),
+        _stream_handle(stream)))
     return out, lse
 
 
