@@ -254,7 +254,7 @@ def step_flops(name, spec):
 class GpuWorkload:
     """Device buffers and the launch sequence of one step."""
 
-    def __init__(self, name, spec, seed_offset=0, rope_mode="ws", qknorm=False, fixed_m=False):
+    def __init__(self, name, spec, seed_offset=0, rope_mode="ws", qknorm=False, fixed_m=False, fp8=False):
         import torch
 
         from video_dit_attention_gb300 import dit_attn as lib
@@ -264,7 +264,9 @@ class GpuWorkload:
         self.workspace = None
         self.norms = None
         self.fixed_m = fixed_m
-        ws_bytes = lib.dit_attn_fixed_m_workspace_bytes if fixed_m else lib.dit_attn_workspace_bytes
+        self.fp8 = fp8
+        ws_bytes = (lib.dit_attn_fp8_workspace_bytes if fp8 else
+                    lib.dit_attn_fixed_m_workspace_bytes if fixed_m else lib.dit_attn_workspace_bytes)
         dev = torch.device("cuda")
         if qknorm:
             self.norms = tuple(torch.from_numpy(I.make_norm_weights(spec.D, seed=spec.seed + 900 + i)).to(dev)
@@ -319,8 +321,8 @@ class GpuWorkload:
                 out = torch.empty_like(qq)
                 lse = torch.empty(tuple(qq.shape[:3]), dtype=torch.float32, device=dev)
                 self.sets.append((qq, kk, vv, out, lse))
-            self.launches_per_step = 1
-            if rope_mode == "ws" and self.tables[0] is not None:
+            self.launches_per_step = 3 if fp8 else 1
+            if fp8 or (rope_mode == "ws" and self.tables[0] is not None):
                 nb = ws_bytes(spec.B, spec.Sq, spec.Skv, spec.H, spec.D)
                 self.workspace = torch.empty(nb, dtype=torch.uint8, device=dev)
         torch.cuda.synchronize()
@@ -328,7 +330,10 @@ class GpuWorkload:
     def attn(self, q, k, v, q_valid, kv_valid, tables, out, lse):
         """One self-attention launch: the two-phase RoPE path (rotation into the preallocated
         workspace) when a workspace is set, else the path with RoPE fused per tile."""
-        if self.workspace is not None and self.fixed_m:
+        if self.fp8:
+            self.lib.dit_attn_fwd_fp8(q, k, v, q_valid, kv_valid, *tables, workspace=self.workspace,
+                                      out=out, lse=lse)
+        elif self.workspace is not None and self.fixed_m:
             self.lib.dit_attn_fwd_ws_fixed_m(q, k, v, q_valid, kv_valid, *tables, workspace=self.workspace,
                                              out=out, lse=lse)
         elif self.workspace is not None and self.norms is not None:
@@ -596,6 +601,9 @@ def main():
     ap.add_argument("--fixed-m", action="store_true",
                     help="fixed-m softmax (32-row blocks whose norm bound allows it skip the running "
                          "maximum; workspace path, RoPE workloads)")
+    ap.add_argument("--fp8", action="store_true",
+                    help="FP8 (e4m3) attention: q/k/v rotated and quantised into a workspace, e4m3 "
+                         "tensor-core products (D = 128 self-attention workloads)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-hbm-kernels", action="store_true", help="skip the RoPE / merge GB/s figures")
     args = ap.parse_args()
@@ -619,7 +627,10 @@ def main():
         raise SystemExit("--qknorm needs a RoPE workload on the workspace path")
     if args.fixed_m and (args.rope != "ws" or spec_has_no_rope(spec) or args.qknorm):
         raise SystemExit("--fixed-m needs a RoPE workload on the workspace path, without --qknorm")
-    wl = GpuWorkload(name, spec, seed_offset=rank, rope_mode=args.rope, qknorm=args.qknorm, fixed_m=args.fixed_m)
+    if args.fp8 and (name in ("cross", "sharded") or spec.D != 128 or args.qknorm or args.fixed_m or args.rope != "ws"):
+        raise SystemExit("--fp8 needs a D = 128 self-attention workload, without --qknorm / --fixed-m / --rope fused")
+    wl = GpuWorkload(name, spec, seed_offset=rank, rope_mode=args.rope, qknorm=args.qknorm, fixed_m=args.fixed_m,
+                     fp8=args.fp8)
     flops = step_flops(name, spec)
     stream = torch.cuda.current_stream()
 
@@ -679,24 +690,33 @@ def main():
     clocks = sampler.summary(t0, t1, load_t0)
     achieved = flops / kern_s / 1e12
     peak = peaks["bf16_tflops"]
+    peak_source = f"bf16_tflops (burst) of {peaks['source']} peaks"
+    if args.fp8:
+        # e4m3 products: the measured bf16 peak times the nominal fp8 / bf16 ratio (4.5 / 2.25)
+        peak = 2.0 * peaks["bf16_tflops"]
+        peak_source = f"2 x bf16_tflops (burst) of {peaks['source']} peaks (nominal fp8 / bf16 ratio)"
     line = {
         "metric": METRIC, "value": units / max_el / 1e12, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": max_el / args.steps * 1e3,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp8_e4m3" if args.fp8 else "bf16",
         "data": "synthetic", "config": dict(config_dict(name, spec, args.rope), **(
             {"qk_norm": "per-head RMSNorm before the rotation, synthetic weights 1 + 0.1 N(0,1), eps 1e-6"}
             if args.qknorm else {}), **(
             {"softmax": "fixed-m: 32-row blocks whose bound scale*|q|*max|k| allows it skip the running maximum"}
-            if args.fixed_m else {})),
+            if args.fixed_m else {}), **(
+            {"precision": "fp8 e4m3 operands (q per 128-row tile, k and v per head), P = e4m3(112 p), fp32 "
+                          "accumulation; the step includes the two preparation kernels"} if args.fp8 else {})),
         "pct_of_bf16_peak": 100.0 * (units / max_el / 1e12) / (peak * world),
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak,
                      # the profiled traffic is that of the default kernel; the variants have none
-                     "traffic": None if (args.qknorm or args.fixed_m) else profiled_traffic(name),
+                     "traffic": None if (args.qknorm or args.fixed_m or args.fp8) else profiled_traffic(name),
                      "kernel": dominant_kernel(name, args.rope) + (" + q/k RMSNorm" if args.qknorm else "")
-                     + (" (fixed-m softmax)" if args.fixed_m else ""),
+                     + (" (fixed-m softmax)" if args.fixed_m else "")
+                     + (" (fp8; timed with its two preparation kernels)" if args.fp8 else ""),
                      "kernel_ms": kern_s * 1e3, "algorithmic_bytes": wl.dominant_bytes(),
-                     "peak_source": f"bf16_tflops (burst) of {peaks['source']} peaks"},
+                     "peak_source": peak_source},
         "gpu_launches": wl.launches_per_step * args.steps,
         "clocks": clocks,
     }

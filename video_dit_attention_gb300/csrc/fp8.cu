@@ -91,9 +91,10 @@ __global__ void __launch_bounds__(256) fp8_amax_kernel(const Fp8Args a) {
   const float* ct = blk.kind < 2 ? a.cos_t[blk.kind] : nullptr;
   const float* st = blk.kind < 2 ? a.sin_t[blk.kind] : nullptr;
   float m = 0.f;
-  for (int rr = warp; rr < 128; rr += 8) {
+  const int n_rows = min(128, valid - blk.t * 128);   // valid rows of this tile (may be <= 0)
+#pragma unroll 4
+  for (int rr = warp; rr < n_rows; rr += 8) {
     const int row = blk.t * 128 + rr;
-    if (row >= valid) break;
     const uint16_t* xr = a.x[blk.kind] + ((static_cast<size_t>(blk.b) * S + row) * a.H + blk.h) * kD;
     float y[4];
     load_pairs(xr, ct ? ct + static_cast<size_t>(row) * (kD / 2) : nullptr,
@@ -134,7 +135,11 @@ __global__ void __launch_bounds__(256) fp8_quantize_kernel(const Fp8Args a) {
   }
   const float* ct = blk.kind < 2 ? a.cos_t[blk.kind] : nullptr;
   const float* st = blk.kind < 2 ? a.sin_t[blk.kind] : nullptr;
-  __shared__ __align__(16) uint8_t tile[kD * 128];   // v only: [d][key] for the transposed write
+  // v only: [d][key] for the transposed write, rows padded to 132 bytes so that the byte
+  // stores of one warp (channels 2l.., same key) fall in different banks.
+  constexpr int kTS = 132;
+  __shared__ __align__(16) uint8_t tile[kD * kTS];
+#pragma unroll 4
   for (int rr = warp; rr < 128; rr += 8) {
     const int row = blk.t * 128 + rr;
     uint32_t lo = 0, hi = 0;   // e4m3 of channels (2l, 2l+1) and (64+2l, 65+2l); pads stay 0
@@ -153,10 +158,10 @@ __global__ void __launch_bounds__(256) fp8_quantize_kernel(const Fp8Args a) {
         *reinterpret_cast<uint16_t*>(dst + kD / 2 + 2 * lane) = static_cast<uint16_t>(hi);
       }
     } else {
-      tile[(2 * lane) * 128 + rr] = static_cast<uint8_t>(lo & 0xff);
-      tile[(2 * lane + 1) * 128 + rr] = static_cast<uint8_t>(lo >> 8);
-      tile[(kD / 2 + 2 * lane) * 128 + rr] = static_cast<uint8_t>(hi & 0xff);
-      tile[(kD / 2 + 2 * lane + 1) * 128 + rr] = static_cast<uint8_t>(hi >> 8);
+      tile[(2 * lane) * kTS + rr] = static_cast<uint8_t>(lo & 0xff);
+      tile[(2 * lane + 1) * kTS + rr] = static_cast<uint8_t>(lo >> 8);
+      tile[(kD / 2 + 2 * lane) * kTS + rr] = static_cast<uint8_t>(hi & 0xff);
+      tile[(kD / 2 + 2 * lane + 1) * kTS + rr] = static_cast<uint8_t>(hi >> 8);
     }
   }
   if (blk.kind == 2) {
@@ -166,7 +171,8 @@ __global__ void __launch_bounds__(256) fp8_quantize_kernel(const Fp8Args a) {
       const int d = c >> 3, kc = (c & 7) * 16;
       if (blk.t * 128 + kc < a.Skv) {
         uint8_t* dst = a.vt8 + (static_cast<size_t>(bh) * kD + d) * a.Skv + blk.t * 128 + kc;
-        *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(tile + d * 128 + kc);
+        const uint32_t* src = reinterpret_cast<const uint32_t*>(tile + d * kTS + kc);   // 4-byte aligned
+        *reinterpret_cast<uint4*>(dst) = make_uint4(src[0], src[1], src[2], src[3]);
       }
     }
   }
