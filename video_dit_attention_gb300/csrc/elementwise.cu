@@ -97,21 +97,23 @@ __global__ void __launch_bounds__(256) qk_rmsnorm_rope_kernel(const uint16_t* x,
     const long long row = valid ? it / kChunks : 0;
     const int ch = static_cast<int>(it % kChunks);
     uint4 a = make_uint4(0, 0, 0, 0), b = make_uint4(0, 0, 0, 0);
+    // Weights and table rows are loaded together with the data, ahead of the shuffles, so
+    // that their latency overlaps the data's.
+    float wa[8], wb[8], cs[8], sn[8];
     if (valid) {
       a = *reinterpret_cast<const uint4*>(x + row * D + ch * 8);
       b = *reinterpret_cast<const uint4*>(x + row * D + kHalf + ch * 8);
+      const int s = static_cast<int>((row / H) % S);
+      load8f(w + ch * 8, wa);
+      load8f(w + kHalf + ch * 8, wb);
+      load8f(cos_t + static_cast<long long>(s) * kHalf + ch * 8, cs);
+      load8f(sin_t + static_cast<long long>(s) * kHalf + ch * 8, sn);
     }
     float ss = sumsq16(a, b);
 #pragma unroll
     for (int off = 1; off < kChunks; off <<= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
     if (valid) {
-      const int s = static_cast<int>((row / H) % S);
       const float inv = rsqrtf(ss * (1.f / D) + eps);
-      float wa[8], wb[8], cs[8], sn[8];
-      load8f(w + ch * 8, wa);
-      load8f(w + kHalf + ch * 8, wb);
-      load8f(cos_t + static_cast<long long>(s) * kHalf + ch * 8, cs);
-      load8f(sin_t + static_cast<long long>(s) * kHalf + ch * 8, sn);
       norm_rotate8<false>(a, b, inv, wa, wb, cs, sn);
       *reinterpret_cast<uint4*>(y + row * D + ch * 8) = a;
       *reinterpret_cast<uint4*>(y + row * D + kHalf + ch * 8) = b;
@@ -149,6 +151,56 @@ __global__ void __launch_bounds__(256) lse_merge_kernel(const uint16_t* __restri
         const float w = __expf(__ldg(pl + s * rows + row) - lse_row);
         const uint4 v = __ldg(reinterpret_cast<const uint4*>(po + s * part_stride + row * D + ch * 8));
         const uint32_t vw[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          acc[2 * q] = fmaf(w, bf16lo_to_f32(vw[q]), acc[2 * q]);
+          acc[2 * q + 1] = fmaf(w, bf16hi_to_f32(vw[q]), acc[2 * q + 1]);
+        }
+      }
+    }
+    *reinterpret_cast<uint4*>(out + row * D + ch * 8) =
+        make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                   pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+    if (ch == 0) lse[row] = lse_row;
+  }
+}
+
+// lse_merge_kernel for a fixed number of partials N (1..8): the N partial LSEs and the N
+// 16-byte pieces of partial O are all loaded before any arithmetic, so each thread has N + N
+// independent loads in flight instead of a chain through the loop.
+template <int D, int N>
+__global__ void __launch_bounds__(256) lse_merge_fixed_kernel(const uint16_t* __restrict__ po,
+                                                              const float* __restrict__ pl, long long rows,
+                                                              uint16_t* __restrict__ out,
+                                                              float* __restrict__ lse) {
+  constexpr int kTPR = D / 8;
+  const long long items = rows * kTPR;
+  const long long part_stride = rows * D;
+  for (long long it = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; it < items;
+       it += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long row = it / kTPR;
+    const int ch = static_cast<int>(it % kTPR);
+    float ls[N];
+    uint4 v[N];
+#pragma unroll
+    for (int s = 0; s < N; ++s) {
+      ls[s] = __ldg(pl + s * rows + row);
+      v[s] = __ldg(reinterpret_cast<const uint4*>(po + s * part_stride + row * D + ch * 8));
+    }
+    float m = ls[0];
+#pragma unroll
+    for (int s = 1; s < N; ++s) m = fmaxf(m, ls[s]);
+    float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    float lse_row = -INFINITY;
+    if (m > -INFINITY) {
+      float tot = 0.f;
+#pragma unroll
+      for (int s = 0; s < N; ++s) tot += __expf(ls[s] - m);
+      lse_row = m + __logf(tot);
+#pragma unroll
+      for (int s = 0; s < N; ++s) {
+        const float w = __expf(ls[s] - lse_row);
+        const uint32_t vw[4] = {v[s].x, v[s].y, v[s].z, v[s].w};
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           acc[2 * q] = fmaf(w, bf16lo_to_f32(vw[q]), acc[2 * q]);
@@ -238,6 +290,22 @@ cudaError_t launch_lse_merge(const void* partial_o, const float* partial_lse, in
   const long long rows = static_cast<long long>(B) * S * H;
   const long long items = rows * (D / 8);
   const int grid = grid_for(items, 256);
+  const uint16_t* po = static_cast<const uint16_t*>(partial_o);
+  uint16_t* o = static_cast<uint16_t*>(out);
+  if (n >= 1 && n <= 8) {
+    // One instantiation per (D, n): the partials' loads are unrolled.
+    using Fn = void (*)(const uint16_t*, const float*, long long, uint16_t*, float*);
+    static constexpr Fn k128[8] = {lse_merge_fixed_kernel<128, 1>, lse_merge_fixed_kernel<128, 2>,
+                                   lse_merge_fixed_kernel<128, 3>, lse_merge_fixed_kernel<128, 4>,
+                                   lse_merge_fixed_kernel<128, 5>, lse_merge_fixed_kernel<128, 6>,
+                                   lse_merge_fixed_kernel<128, 7>, lse_merge_fixed_kernel<128, 8>};
+    static constexpr Fn k64[8] = {lse_merge_fixed_kernel<64, 1>, lse_merge_fixed_kernel<64, 2>,
+                                  lse_merge_fixed_kernel<64, 3>, lse_merge_fixed_kernel<64, 4>,
+                                  lse_merge_fixed_kernel<64, 5>, lse_merge_fixed_kernel<64, 6>,
+                                  lse_merge_fixed_kernel<64, 7>, lse_merge_fixed_kernel<64, 8>};
+    (D == 128 ? k128 : k64)[n - 1]<<<grid, 256, 0, stream>>>(po, partial_lse, rows, o, lse);
+    return cudaGetLastError();
+  }
   if (D == 128)
     lse_merge_kernel<128><<<grid, 256, 0, stream>>>(static_cast<const uint16_t*>(partial_o),
                                                     partial_lse, n, rows,
