@@ -190,3 +190,33 @@ def test_fixed_m_entry_validation_before_any_cuda_call(clib):
     assert call(B=1, H=24577, wsz=wsb(1, 256, 256, 24577, 128)) == -2   # B * H above 24576
     assert call(n_online=P + 2) == -3           # misaligned counter
     assert call(ws=P + 128) == -3               # workspace not 256-byte aligned
+
+
+def test_fp8_entry_validation_before_any_cuda_call(clib):
+    wsb = clib.dit_attn_fp8_workspace_bytes
+    wsb.restype = ctypes.c_size_t
+    r256 = lambda n: (n + 255) // 256 * 256
+    B, Sq, Skv, H, D = 1, 4736, 4736, 40, 128
+    ntq, ntk = Sq // 128, Skv // 128
+    # e4m3 q~, k~, v^T, then tile maxima (q, k, v), q scales per tile, k and v scales per head
+    expect = (r256(B * Sq * H * D) + r256(B * Skv * H * D) + r256(B * H * D * Skv) + r256(B * H * ntq * 4)
+              + 2 * r256(B * H * ntk * 4) + r256(B * H * ntq * 4) + 2 * r256(B * H * 4))
+    assert wsb(B, Sq, Skv, H, D) == expect
+    assert wsb(1, 128, 128, 1, 64) == 0 and wsb(0, 128, 128, 1, 128) == 0
+    fn = clib.dit_attn_fwd_fp8
+    fn.restype = ctypes.c_int
+    fn.argtypes = [ctypes.c_void_p] * 3 + [ctypes.c_int] * 7 + [ctypes.c_void_p] * 4 + \
+        [ctypes.c_float, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+    P = 0x10000   # never dereferenced: every case below fails validation first
+    need = wsb(1, 256, 256, 2, 128)
+
+    def call(D=128, wsz=need, ws=P, tabs=(P, P, P, P), kv=256):
+        return fn(P, P, P, 1, 256, 256, 2, D, 256, kv, *tabs, 0.088, P, P, ws, wsz, None)
+
+    assert call(D=64, wsz=10 ** 9) == -2        # built for D = 128 only
+    assert call(ws=None) == -1
+    assert call(wsz=need - 1) == -1
+    assert call(tabs=(P, None, P, P)) == -1     # some tables but not all four
+    assert call(kv=257) == -1
+    assert call(ws=P + 64) == -3                # workspace not 256-byte aligned
+    assert call(tabs=(P + 4, P, P, P)) == -3    # table not 8-byte aligned
