@@ -382,7 +382,17 @@ class GpuWorkload:
 
 class E2E:
     """Host-buffer path through the C-ABI: pinned host q/k/v (unpadded) -> H2D -> pad ->
-    attention -> unpad -> D2H of O and LSE (self-attention and cross workloads)."""
+    attention -> unpad -> D2H of O and LSE (self-attention and cross workloads).
+
+    Steps are pipelined over two buffer sets: step i's upload runs on a copy stream while
+    step i-1 computes, and its download on another copy stream while step i+1 computes;
+    events order each set's reuse. Every step still moves its own inputs and outputs, inside
+    the timed region. With B = 1 the valid rows are a contiguous prefix of the padded
+    buffers, so the upload writes straight into them and the download reads straight from
+    the padded outputs (no pad / unpad launches); with B > 1 dit_pad_tokens and
+    dit_unpad_tokens gather the rows on the device."""
+
+    NBUF = 2
 
     def __init__(self, wl):
         torch = wl.torch
@@ -394,39 +404,77 @@ class E2E:
         pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(torch.bfloat16).pin_memory()
         self.hq, self.hk, self.hv = pin(q[:, :Lq]), pin(k[:, :Lk]), pin(v[:, :Lk])
         dev = torch.device("cuda")
-        self.dq = torch.empty(self.hq.shape, dtype=torch.bfloat16, device=dev)
-        self.dk = torch.empty(self.hk.shape, dtype=torch.bfloat16, device=dev)
-        self.dv = torch.empty(self.hv.shape, dtype=torch.bfloat16, device=dev)
-        self.qp = torch.empty((sp.B, sp.Sq, sp.H, sp.D), dtype=torch.bfloat16, device=dev)
-        self.kp = torch.empty((sp.B, sp.Skv, sp.H, sp.D), dtype=torch.bfloat16, device=dev)
-        self.vp = torch.empty_like(self.kp)
-        self.out = torch.empty_like(self.qp)
-        self.lse = torch.empty((sp.B, sp.Sq, sp.H), dtype=torch.float32, device=dev)
-        self.o_u = torch.empty((sp.B, Lq, sp.H, sp.D), dtype=torch.bfloat16, device=dev)
-        self.l_u = torch.empty((sp.B, Lq, sp.H), dtype=torch.float32, device=dev)
-        self.ho = torch.empty(self.o_u.shape, dtype=torch.bfloat16).pin_memory()
-        self.hl = torch.empty(self.l_u.shape, dtype=torch.float32).pin_memory()
+        self.direct = sp.B == 1
+        self.sets = []
+        for _ in range(self.NBUF):
+            st = {}
+            st["qp"] = torch.empty((sp.B, sp.Sq, sp.H, sp.D), dtype=torch.bfloat16, device=dev)
+            st["kp"] = torch.empty((sp.B, sp.Skv, sp.H, sp.D), dtype=torch.bfloat16, device=dev)
+            st["vp"] = torch.empty_like(st["kp"])
+            st["out"] = torch.empty_like(st["qp"])
+            st["lse"] = torch.empty((sp.B, sp.Sq, sp.H), dtype=torch.float32, device=dev)
+            if not self.direct:
+                st["dq"] = torch.empty(self.hq.shape, dtype=torch.bfloat16, device=dev)
+                st["dk"] = torch.empty(self.hk.shape, dtype=torch.bfloat16, device=dev)
+                st["dv"] = torch.empty(self.hv.shape, dtype=torch.bfloat16, device=dev)
+                st["o_u"] = torch.empty((sp.B, Lq, sp.H, sp.D), dtype=torch.bfloat16, device=dev)
+                st["l_u"] = torch.empty((sp.B, Lq, sp.H), dtype=torch.float32, device=dev)
+            st["ho"] = torch.empty((sp.B, Lq, sp.H, sp.D), dtype=torch.bfloat16).pin_memory()
+            st["hl"] = torch.empty((sp.B, Lq, sp.H), dtype=torch.float32).pin_memory()
+            st["ev_in"], st["ev_done"], st["ev_out"] = (torch.cuda.Event() for _ in range(3))
+            self.sets.append(st)
+        # One upload stream: three (one per tensor) measured the same (about 190 GB/s in all).
+        self.s_h2d, self.s_d2h = torch.cuda.Stream(), torch.cuda.Stream()
         self.Lq, self.Lk = Lq, Lk
         self.h2d = sum(t.numel() * t.element_size() for t in (self.hq, self.hk, self.hv))
-        self.d2h = self.ho.numel() * 2 + self.hl.numel() * 4
-        self.launches_per_step = 6
+        self.d2h = self.sets[0]["ho"].numel() * 2 + self.sets[0]["hl"].numel() * 4
+        self.launches_per_step = 1 if self.direct else 6
+        self.last = None
 
-    def step(self):
+    def step(self, i):
+        torch = self.torch
         lib, wl, sp = self.wl.lib, self.wl, self.wl.spec
-        self.dq.copy_(self.hq, non_blocking=True)
-        self.dk.copy_(self.hk, non_blocking=True)
-        self.dv.copy_(self.hv, non_blocking=True)
-        lib.dit_pad_tokens(self.dq, sp.Sq, out=self.qp)
-        lib.dit_pad_tokens(self.dk, sp.Skv, out=self.kp)
-        lib.dit_pad_tokens(self.dv, sp.Skv, out=self.vp)
-        if wl.name == "cross":
-            lib.dit_cross_attn_shortkv(self.qp, self.kp, self.vp, sp.q_valid, wl.kv_dev, out=self.out, lse=self.lse)
+        st = self.sets[i % self.NBUF]
+        cs = torch.cuda.current_stream()
+        Lq, Lk = self.Lq, self.Lk
+        if self.direct:
+            dsts = (st["qp"][:, :Lq], st["kp"][:, :Lk], st["vp"][:, :Lk])
         else:
-            wl.attn(self.qp, self.kp, self.vp, sp.q_valid, int(sp.kv_valid), wl.tables, self.out, self.lse)
-        lib.dit_unpad_tokens(self.out, self.Lq, out=self.o_u)
-        lib.dit_unpad_tokens(self.lse, self.Lq, out=self.l_u)
-        self.ho.copy_(self.o_u, non_blocking=True)
-        self.hl.copy_(self.l_u, non_blocking=True)
+            dsts = (st["dq"], st["dk"], st["dv"])
+        with torch.cuda.stream(self.s_h2d):
+            self.s_h2d.wait_event(st["ev_done"])        # the set's previous compute has read it
+            for dst, src in zip(dsts, (self.hq, self.hk, self.hv)):
+                dst.copy_(src, non_blocking=True)
+            st["ev_in"].record(self.s_h2d)
+        cs.wait_event(st["ev_in"])
+        cs.wait_event(st["ev_out"])                      # the set's previous download is done
+        if not self.direct:
+            lib.dit_pad_tokens(st["dq"], sp.Sq, out=st["qp"])
+            lib.dit_pad_tokens(st["dk"], sp.Skv, out=st["kp"])
+            lib.dit_pad_tokens(st["dv"], sp.Skv, out=st["vp"])
+        if wl.name == "cross":
+            lib.dit_cross_attn_shortkv(st["qp"], st["kp"], st["vp"], sp.q_valid, wl.kv_dev, out=st["out"],
+                                       lse=st["lse"])
+        else:
+            wl.attn(st["qp"], st["kp"], st["vp"], sp.q_valid, int(sp.kv_valid), wl.tables, st["out"], st["lse"])
+        if self.direct:
+            o_src, l_src = st["out"][:, :Lq], st["lse"][:, :Lq]
+        else:
+            lib.dit_unpad_tokens(st["out"], Lq, out=st["o_u"])
+            lib.dit_unpad_tokens(st["lse"], Lq, out=st["l_u"])
+            o_src, l_src = st["o_u"], st["l_u"]
+        st["ev_done"].record(cs)
+        with torch.cuda.stream(self.s_d2h):
+            self.s_d2h.wait_event(st["ev_done"])
+            st["ho"].copy_(o_src, non_blocking=True)
+            st["hl"].copy_(l_src, non_blocking=True)
+            st["ev_out"].record(self.s_d2h)
+        self.last = st
+
+    def finish(self):
+        """Makes the current stream wait for the last step's download."""
+        if self.last is not None:
+            self.torch.cuda.current_stream().wait_event(self.last["ev_out"])
 
 
 # ----------------------------------------------------------------------------- HBM-bound kernels
@@ -663,23 +711,29 @@ def main():
     e2e = None
     if name != "sharded":
         ee = E2E(wl)
-        for _ in range(max(3, min(args.warmup, 10))):
-            ee.step()
+        for i in range(max(3, min(args.warmup, 10))):
+            ee.step(i)
+        ee.finish()
         torch.cuda.synchronize()
         n_e2e = max(3, min(args.steps, 200 if name != "wan720" else 10))
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         barrier(world)
         torch.cuda.synchronize()
         a.record(stream)
-        for _ in range(n_e2e):
-            ee.step()
+        for i in range(n_e2e):
+            ee.step(i)
+        ee.finish()          # the last download is inside the timed region
         b.record(stream)
         torch.cuda.synchronize()
         barrier(world)
         e_el, e_units = reduce_over_ranks(a.elapsed_time(b) / 1e3, flops * n_e2e, world)
         e2e = {"value": e_units / e_el / 1e12, "unit": "TFLOP/s", "h2d_bytes_per_step": ee.h2d,
                "d2h_bytes_per_step": ee.d2h, "steps": n_e2e,
-               "path": "pinned host q/k/v -> H2D -> dit_pad_tokens -> attention -> dit_unpad_tokens -> D2H O, LSE"}
+               "path": ("pinned host q/k/v -> H2D -> " + ("(B = 1: into the padded buffers) " if ee.direct else
+                                                          "dit_pad_tokens -> ")
+                        + "attention -> " + ("" if ee.direct else "dit_unpad_tokens -> ")
+                        + "D2H O, LSE; steps pipelined over two buffer sets (uploads, compute and "
+                          "downloads on three streams)")}
     sampler.stop()
 
     max_el, units = reduce_over_ranks(elapsed, flops * args.steps, world)
