@@ -18,8 +18,10 @@ sequence stays padded between blocks): the attention launch(es) of the workload 
 valid tokens (4 * B * H * Lq * Lkv * D per attention) over all ranks. Three distinct input
 sets rotate between steps, so every step reads inputs that are not L2-resident. `e2e` is the
 same metric through the C-ABI with host buffers: every step copies the unpadded q/k/v from
-pinned host memory, pads them with dit_pad_tokens, runs the attention, unpads O and LSE with
-dit_unpad_tokens and copies them back. RoPE runs inside the attention launch: by default
+pinned host memory into the padded layout (straight into the padded buffers when B = 1, else
+through dit_pad_tokens), runs the attention, takes O and LSE back out (dit_unpad_tokens when
+B > 1) and copies them to pinned host memory; consecutive steps overlap their copies with the
+compute of their neighbours (two buffer sets, three streams). RoPE runs inside the attention launch: by default
 (`--rope ws`) every q/k row is rotated once into a preallocated fp16 workspace before a grid
 barrier, with `--rope fused` each loaded tile is rotated in shared memory instead.
 `--impl reference` times the fp64 CPU oracle instead,
