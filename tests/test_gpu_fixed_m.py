@@ -137,3 +137,15 @@ def test_fixed_m_wan480_sampled(lib):
     Or, Lr = attention(q, k, v, case.q_valid, case.kv_valid, case.scale, aq, ak, rows=rows, heads=heads)
     compare(O, L, Or, Lr, case.q_valid, rows=rows, heads=heads)
     assert np.all(O[:, case.q_valid:] == 0) and np.all(L[:, case.q_valid:] == -np.inf)
+
+
+@pytest.mark.parametrize("qv,kv", [(1, 1), (129, 1), (1, 300), (200, 127), (128, 129)])
+def test_fixed_m_ragged_and_degenerate_lengths(lib, qv, kv):
+    case = AttnCase(f"fm-edge-{qv}-{kv}", B=1, H=2, D=64, Sq=256, Skv=384, q_valid=qv, kv_valid=kv,
+                    rope="1d", seed=170 + qv + kv)
+    q, k, v = make_qkv(case)
+    O, L, n_online = _run(lib, case, q, k, v)
+    assert n_online == 0
+    aq, ak = oracle_angles_self(case)
+    Or, Lr = attention(q, k, v, case.q_valid, case.kv_valid, case.scale, aq, ak)
+    compare(O, L, Or, Lr, case.q_valid)

@@ -104,3 +104,27 @@ def test_fp8_wan480_sampled(lib):
     Or, Lr = _oracle(case, q, k, v, rows=rows, heads=heads)
     _compare(O, L, Or, Lr, case.q_valid, rows=rows, heads=heads)
     assert np.all(O[:, case.q_valid:] == 0) and np.all(L[:, case.q_valid:] == -np.inf)
+
+
+@pytest.mark.parametrize("qv,kv", [(1, 1), (129, 1), (1, 300), (200, 127), (128, 129)])
+def test_fp8_ragged_and_degenerate_lengths(lib, qv, kv):
+    case = AttnCase(f"fp8-edge-{qv}-{kv}", B=1, H=2, D=128, Sq=256, Skv=384, q_valid=qv, kv_valid=kv,
+                    rope="1d", seed=155 + qv + kv)
+    q, k, v = make_qkv(case)
+    O, L = _run(lib, case, q, k, v)
+    Or, Lr = _oracle(case, q, k, v)
+    _compare(O, L, Or, Lr, case.q_valid)
+
+
+@pytest.mark.parametrize("qv,kv", [(0, 300), (200, 0)])
+def test_fp8_empty_inputs(lib, qv, kv):
+    """No valid query row, or no valid key: O = 0 and LSE = -inf everywhere."""
+    case = AttnCase("fp8-empty", B=1, H=2, D=128, Sq=256, Skv=384, q_valid=256, kv_valid=384, rope=None, seed=160)
+    q, k, v = make_qkv(case)
+    cq, sq = lib.dit_rope_table_1d(256, 256, 128, 10000.0, 0)
+    ck, sk = lib.dit_rope_table_1d(384, 384, 128, 10000.0, 0)
+    tabs = tuple(torch.from_numpy(t).cuda() for t in (cq, sq, ck, sk))
+    out, lse = lib.dit_attn_fwd_fp8(dev_bf16(q), dev_bf16(k), dev_bf16(v), qv, kv, *tabs)
+    torch.cuda.synchronize()
+    assert lib.dit_device_status() == 0
+    assert torch.all(out == 0) and torch.all(lse == -math.inf)
