@@ -7,13 +7,17 @@
  *   - self-attention with the pad keys masked out and the RoPE rotation fused into the
  *     q/k tile load, emitting O and the log-sum-exp (LSE),
  *   - short-KV cross-attention of video queries against a text sequence,
- *   - the merge of partial attention results over key shards through their LSEs.
+ *   - the merge of partial attention results over key shards through their LSEs,
+ * and three variants of the self-attention: with a per-head q/k RMSNorm ahead of the
+ * rotation, with the fixed-m softmax (norm-bounded maximum per 32-row block), and with
+ * e4m3 (FP8) tensor-core products.
  * Sources: Difflet PR #153 "TPU sequence parallelism: ... Wan padding + split RoPE"
  * (row padding to whole tiles, pad keys dropped exactly, identity rotation for pad rows,
  * split-halves RoPE); maxdiffusion PR #491 (Wan fast inference: lane padding to a
  * multiple of 128, pad keys masked through the real KV length, fused short-KV
  * cross-attention); mstar PR #376 (LTX-2.5 TP/SP: attention that also returns the LSE in
- * natural log, attention over sharded keys merged through the LSE).
+ * natural log, attention over sharded keys merged through the LSE; rowwise FP8 linears as
+ * the motivation for the FP8 variant).
  *
  * Conventions for every call
  *   - Tensors are contiguous BSHD: q/k/v/out [B, S, H, D] bf16 (raw 16-bit storage passed
