@@ -225,7 +225,7 @@ int dit_attn_fwd_ws_fixed_m(const void* q, const void* k, const void* v, int B, 
  * overlap. Three launches on `stream` (two preparation kernels, then the attention).
  * Everything else (arguments, layouts, pad handling) as dit_attn_fwd. Errors: as dit_attn_fwd;
  * DIT_ERR_UNSUPPORTED for D != 128; DIT_ERR_INVALID_ARG for a missing or too small workspace
- * or some but not all tables; DIT_ERR_ALIGNMENT for a misaligned workspace (256) or table (8).
+ * or some but not all tables; DIT_ERR_ALIGNMENT for a misaligned workspace (256) or table (16).
  * ------------------------------------------------------------------------------------- */
 size_t dit_attn_fp8_workspace_bytes(int B, int Sq, int Skv, int H, int D);
 int dit_attn_fwd_fp8(const void* q, const void* k, const void* v, int B, int Sq, int Skv, int H,

@@ -219,4 +219,5 @@ def test_fp8_entry_validation_before_any_cuda_call(clib):
     assert call(tabs=(P, None, P, P)) == -1     # some tables but not all four
     assert call(kv=257) == -1
     assert call(ws=P + 64) == -3                # workspace not 256-byte aligned
-    assert call(tabs=(P + 4, P, P, P)) == -3    # table not 8-byte aligned
+    assert call(tabs=(P + 4, P, P, P)) == -3    # tables must be 16-byte aligned
+    assert call(tabs=(P, P, P + 8, P)) == -3

@@ -221,7 +221,7 @@ extern "C" int dit_attn_fwd_fp8(const void* q, const void* k, const void* v, int
   const int n_tab = (cos_q != nullptr) + (sin_q != nullptr) + (cos_k != nullptr) + (sin_k != nullptr);
   if (n_tab != 0 && n_tab != 4) return DIT_ERR_INVALID_ARG;
   if (workspace_bytes < fp8_layout(B, Sq, Skv, H, D).total) return DIT_ERR_INVALID_ARG;
-  if (n_tab == 4 && (!aligned(cos_q, 8) || !aligned(sin_q, 8) || !aligned(cos_k, 8) || !aligned(sin_k, 8)))
+  if (n_tab == 4 && (!aligned(cos_q, 16) || !aligned(sin_q, 16) || !aligned(cos_k, 16) || !aligned(sin_k, 16)))
     return DIT_ERR_ALIGNMENT;
   if (!aligned(workspace, 256)) return DIT_ERR_ALIGNMENT;
   AttnArgs a{q, k, v, B, Sq, Skv, H, D, q_valid_len, kv_valid_len, nullptr,

@@ -46,26 +46,38 @@ __device__ __forceinline__ Fp8Block fp8_block(int B, int H, int nt_q, int nt_k) 
   return r;
 }
 
-// The four channels of a row that lane `lane` holds: (2l, 2l+1) of the first half and the
-// matching pair of the second half, rotated when cos/sin rows are given.
-__device__ __forceinline__ void load_pairs(const uint16_t* __restrict__ xr, const float* ct, const float* st,
-                                           int lane, float (&y)[4]) {
-  const uint32_t a = *reinterpret_cast<const uint32_t*>(xr + 2 * lane);
-  const uint32_t b = *reinterpret_cast<const uint32_t*>(xr + kD / 2 + 2 * lane);
-  const float x1l = bf16lo_to_f32(a), x1h = bf16hi_to_f32(a);
-  const float x2l = bf16lo_to_f32(b), x2h = bf16hi_to_f32(b);
+// The sixteen channels of a row that lane unit u (0..7) holds: 8u .. 8u+7 of the first half
+// and the matching eight of the second half, rotated when cos/sin rows are given (pair i is
+// channels (i, i + 64)). Eight lanes cover a row with two 128-byte segments.
+__device__ __forceinline__ void load_unit(const uint16_t* __restrict__ xr, const float* ct, const float* st,
+                                          int u, float (&y)[16]) {
+  const uint4 a = *reinterpret_cast<const uint4*>(xr + 8 * u);
+  const uint4 b = *reinterpret_cast<const uint4*>(xr + kD / 2 + 8 * u);
+  const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+  float x1[8], x2[8];
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    x1[2 * w] = bf16lo_to_f32(aw[w]);
+    x1[2 * w + 1] = bf16hi_to_f32(aw[w]);
+    x2[2 * w] = bf16lo_to_f32(bw[w]);
+    x2[2 * w + 1] = bf16hi_to_f32(bw[w]);
+  }
   if (ct != nullptr) {
-    const float2 c = *reinterpret_cast<const float2*>(ct + 2 * lane);
-    const float2 s = *reinterpret_cast<const float2*>(st + 2 * lane);
-    y[0] = fmaf(x1l, c.x, -x2l * s.x);
-    y[1] = fmaf(x1h, c.y, -x2h * s.y);
-    y[2] = fmaf(x1l, s.x, x2l * c.x);
-    y[3] = fmaf(x1h, s.y, x2h * c.y);
+    const float4 c0 = *reinterpret_cast<const float4*>(ct + 8 * u), c1 = *reinterpret_cast<const float4*>(ct + 8 * u + 4);
+    const float4 s0 = *reinterpret_cast<const float4*>(st + 8 * u), s1 = *reinterpret_cast<const float4*>(st + 8 * u + 4);
+    const float cs[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+    const float sn[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      y[i] = fmaf(x1[i], cs[i], -x2[i] * sn[i]);
+      y[8 + i] = fmaf(x1[i], sn[i], x2[i] * cs[i]);
+    }
   } else {
-    y[0] = x1l;
-    y[1] = x1h;
-    y[2] = x2l;
-    y[3] = x2h;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      y[i] = x1[i];
+      y[8 + i] = x2[i];
+    }
   }
 }
 
@@ -83,23 +95,24 @@ struct Fp8Args {
   float* sv;               // [B, H]
 };
 
-// 256 threads: warp w takes rows w, w + 8, ... of the 128-row tile.
+// 256 threads: warp w takes rows 4w .. 4w + 3, then 32 further on, ...; eight lanes per row.
 __global__ void __launch_bounds__(256) fp8_amax_kernel(const Fp8Args a) {
   const Fp8Block blk = fp8_block(a.B, a.H, a.nt_q, a.nt_k);
   const int S = blk.kind == 0 ? a.Sq : a.Skv, valid = blk.kind == 0 ? a.q_valid : a.kv_valid;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, u = lane & 7;
   const float* ct = blk.kind < 2 ? a.cos_t[blk.kind] : nullptr;
   const float* st = blk.kind < 2 ? a.sin_t[blk.kind] : nullptr;
   float m = 0.f;
   const int n_rows = min(128, valid - blk.t * 128);   // valid rows of this tile (may be <= 0)
-#pragma unroll 4
-  for (int rr = warp; rr < n_rows; rr += 8) {
+#pragma unroll 2
+  for (int rr = warp * 4 + (lane >> 3); rr < n_rows; rr += 32) {
     const int row = blk.t * 128 + rr;
     const uint16_t* xr = a.x[blk.kind] + ((static_cast<size_t>(blk.b) * S + row) * a.H + blk.h) * kD;
-    float y[4];
-    load_pairs(xr, ct ? ct + static_cast<size_t>(row) * (kD / 2) : nullptr,
-               st ? st + static_cast<size_t>(row) * (kD / 2) : nullptr, lane, y);
-    m = fmaxf(m, fmaxf(fmaxf(fabsf(y[0]), fabsf(y[1])), fmaxf(fabsf(y[2]), fabsf(y[3]))));
+    float y[16];
+    load_unit(xr, ct ? ct + static_cast<size_t>(row) * (kD / 2) : nullptr,
+              st ? st + static_cast<size_t>(row) * (kD / 2) : nullptr, u, y);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(y[i]));
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -135,33 +148,35 @@ __global__ void __launch_bounds__(256) fp8_quantize_kernel(const Fp8Args a) {
   }
   const float* ct = blk.kind < 2 ? a.cos_t[blk.kind] : nullptr;
   const float* st = blk.kind < 2 ? a.sin_t[blk.kind] : nullptr;
-  // v only: [d][key] for the transposed write, rows padded to 132 bytes so that the byte
-  // stores of one warp (channels 2l.., same key) fall in different banks.
+  // v only: [d][key] for the transposed write, rows padded to 132 bytes (the 16 byte
+  // stores of a lane go to channels 8u + i and 64 + 8u + i of one key).
   constexpr int kTS = 132;
   __shared__ __align__(16) uint8_t tile[kD * kTS];
-#pragma unroll 4
-  for (int rr = warp; rr < 128; rr += 8) {
+  const int u = lane & 7;
+#pragma unroll 2
+  for (int rr = warp * 4 + (lane >> 3); rr < 128; rr += 32) {
     const int row = blk.t * 128 + rr;
-    uint32_t lo = 0, hi = 0;   // e4m3 of channels (2l, 2l+1) and (64+2l, 65+2l); pads stay 0
+    uint32_t e[4] = {0u, 0u, 0u, 0u};   // e4m3 of the 16 channels, 4 per word; pads stay 0
     if (row < valid) {
       const uint16_t* xr = a.x[blk.kind] + ((static_cast<size_t>(blk.b) * S + row) * a.H + blk.h) * kD;
-      float y[4];
-      load_pairs(xr, ct ? ct + static_cast<size_t>(row) * (kD / 2) : nullptr,
-                 st ? st + static_cast<size_t>(row) * (kD / 2) : nullptr, lane, y);
-      lo = pack_e4m3x2(y[0] / scale, y[1] / scale);
-      hi = pack_e4m3x2(y[2] / scale, y[3] / scale);
+      float y[16];
+      load_unit(xr, ct ? ct + static_cast<size_t>(row) * (kD / 2) : nullptr,
+                st ? st + static_cast<size_t>(row) * (kD / 2) : nullptr, u, y);
+#pragma unroll
+      for (int w = 0; w < 4; ++w)
+        e[w] = pack_e4m3x2(y[4 * w] / scale, y[4 * w + 1] / scale) |
+               (pack_e4m3x2(y[4 * w + 2] / scale, y[4 * w + 3] / scale) << 16);
     }
     if (blk.kind < 2) {
-      if (row < S) {
-        uint8_t* dst = (blk.kind == 0 ? a.q8 : a.k8) + ((static_cast<size_t>(blk.b) * S + row) * a.H + blk.h) * kD;
-        *reinterpret_cast<uint16_t*>(dst + 2 * lane) = static_cast<uint16_t>(lo);
-        *reinterpret_cast<uint16_t*>(dst + kD / 2 + 2 * lane) = static_cast<uint16_t>(hi);
-      }
+      uint8_t* dst = (blk.kind == 0 ? a.q8 : a.k8) + ((static_cast<size_t>(blk.b) * S + row) * a.H + blk.h) * kD;
+      *reinterpret_cast<uint2*>(dst + 8 * u) = make_uint2(e[0], e[1]);
+      *reinterpret_cast<uint2*>(dst + kD / 2 + 8 * u) = make_uint2(e[2], e[3]);
     } else {
-      tile[(2 * lane) * kTS + rr] = static_cast<uint8_t>(lo & 0xff);
-      tile[(2 * lane + 1) * kTS + rr] = static_cast<uint8_t>(lo >> 8);
-      tile[(kD / 2 + 2 * lane) * kTS + rr] = static_cast<uint8_t>(hi & 0xff);
-      tile[(kD / 2 + 2 * lane + 1) * kTS + rr] = static_cast<uint8_t>(hi >> 8);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        tile[(8 * u + i) * kTS + rr] = static_cast<uint8_t>(e[i >> 2] >> (8 * (i & 3)));
+        tile[(kD / 2 + 8 * u + i) * kTS + rr] = static_cast<uint8_t>(e[2 + (i >> 2)] >> (8 * (i & 3)));
+      }
     }
   }
   if (blk.kind == 2) {
