@@ -328,12 +328,13 @@ __device__ __forceinline__ void rotate_rows_fp16(const uint16_t* __restrict__ x,
 // Rotates, in place and into fp16, a landed [128 x D] bf16 tile in shared memory (128-byte
 // swizzle; D = 128: two 64-column sub-tiles, pair (i, i + 64) at the same offset of both;
 // D = 64: pair (i, i + 32) in units x and x + 4 of one row) with table rows cos_t / sin_t
-// [128, D/2] read from global memory. NT threads, this one is number `at`.
-template <int D, int NT>
+// [128, D/2] read from global memory. NT threads, this one is number `at`; each thread has
+// kUnroll row units in flight.
+template <int D, int NT, int kUnroll = 2>
 __device__ __forceinline__ void rotate_tile_smem(uint32_t tile, const float* __restrict__ cos_t,
                                                  const float* __restrict__ sin_t, int at) {
   constexpr int kHalf = D / 2, kUnits = kHalf / 8;   // 8-pair units per row
-#pragma unroll 2
+#pragma unroll kUnroll
   for (int i = at; i < 128 * kUnits; i += NT) {
     const int row = i / kUnits, x = i % kUnits;
     const uint32_t offa = sw128_offset(row, x);

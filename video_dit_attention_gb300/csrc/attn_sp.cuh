@@ -108,7 +108,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bars->abort = 0;
     bars->qn_items = 0;
     mbar_init(b_q_full, 1);
-    mbar_init(b_q_ready, 1);
+    mbar_init(b_q_ready, kMode == kModeRopeWs ? 8 : 1);   // workspace RoPE: the 8 softmax warps
     mbar_init(b_q_empty, 1);
     for (int s = 0; s < R; ++s) {
       mbar_init(smem_u32(&bars->r_full[s]), 1);
@@ -153,7 +153,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // a counter: each thread's generic-proxy stores are fenced against the async proxy (the
     // TMA loads that read them), then the CTA counts itself in with a device-scope release;
     // only the K/V producer waits for the count. Meanwhile warps 14-15 rotate the first
-    // item's Q tiles in shared memory (later ones as they land, in their role below).
+    // item's Q tiles in shared memory (later ones as they land: in their role below, or, in
+    // the workspace RoPE mode, in the softmax warpgroups).
     const int fit = first_live(it0);
     Item fw{};
     if (fit < p.n_items) {
@@ -187,7 +188,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         named_bar_sync(1, 64);
         if (at == 0) {
           if (kFixedM) st_release_cta(&bars->qn_items, 1);
-          mbar_arrive(b_q_ready);
+          for (int x = 0; x < (kMode == kModeRopeWs ? 8 : 1); ++x) mbar_arrive(b_q_ready);
         }
       }
     } else {
@@ -530,13 +531,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t b_p_full = smem_u32(&bars->p_full[t]), b_pv_done = smem_u32(&bars->pv_done[t]);
     const float sl2 = p.scale_log2;
     int sc = 0;   // S_t tiles consumed so far (= P_t tiles produced = PV_t products issued)
-    int qi = 0;   // live items seen so far (fixed-m mode)
+    int qi = 0;   // live items seen so far
+    // Workspace RoPE mode: once its last P_t of live item qi is out, each softmax warpgroup
+    // rotates its tile t of the next live item's Q in shared memory, and each warp arrives on
+    // q_ready, so that the next item's S products start while this item's epilogue runs.
+    // (Warps 14-15 alone took about 16K cycles per item for the whole Q; the 256 softmax
+    // threads take the tile they will use, with nothing else to do until the last P_t V.)
+    auto rotate_next = [&](int it_cur) -> bool {
+      if constexpr (kMode == kModeRopeWs) {
+        const int nit = first_live(it_cur + it_step);
+        if (nit >= p.n_items) return true;
+        const Item nw = decode_item<kMode>(p, nit);
+        if (!warp_wait(b_q_full, (qi + 1) & 1, abort_flag, status, kStatusTimeoutRope)) return false;
+        if (t < nw.n_live) {
+          const size_t row0 = static_cast<size_t>(nw.q0 + 128 * t) * (D / 2);
+          rotate_tile_smem<D, 128, 4>(sQ + t * C::kTileBytes, p.cos_q + row0, p.sin_q + row0, r);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(b_q_ready);
+      }
+      return true;
+    };
     bool ok = true;
     for (int it = it0; ok && it < p.n_items; it += it_step) {
       const Item w = decode_item<kMode>(p, it);
       if (t >= w.n_live) {
         if (t == 0 || w.has1) write_empty_tile<D>(p, w.b, w.h, w.q0 + 128 * t, r, 128);
-        if (w.n_live > 0) ++qi;
+        if (w.n_live > 0) {
+          if (!(ok = rotate_next(it))) break;
+          ++qi;
+        }
         continue;
       }
       const int n_kv = w.n_kv, kv_valid = w.kv_valid;
@@ -659,6 +684,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive(b_p_full);
       }
       if (!ok) break;
+      if (!(ok = rotate_next(it))) break;
       // Epilogue. Wait for the last P_t V of this item and take O_t out of TMEM, which then
       // belongs to the next item (its first P_t V may start), then normalise and store.
       if (!warp_wait(b_pv_done, (sc - 1) & 1, abort_flag, status, kStatusTimeoutSoftmax)) {
@@ -728,7 +754,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) s_issuer();
     } else if (warp == 13) {
       if (lane == 0) pv_issuer();
-    } else if (kWs) {
+    } else if (kWs && kMode != kModeRopeWs) {
       // ---------------------------------------------------------- Q rotation (warps 14-15)
       constexpr int kRotThreads = 64;
       const int at = tid - 448;
