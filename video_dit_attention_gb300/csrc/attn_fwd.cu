@@ -449,13 +449,14 @@ __device__ __forceinline__ void rotate_rows_fp16_kmax(const uint16_t* __restrict
 
 // rotate_tile_smem that also writes each row's squared norm (of the landed bf16 values; the
 // rotation preserves it) to qn_rows[row * stride].
-template <int D, int NT>
+// kUnroll row units in flight per thread.
+template <int D, int NT, int kUnroll = 1>
 __device__ __forceinline__ void rotate_tile_smem_sq(uint32_t tile, const float* __restrict__ cos_t,
                                                     const float* __restrict__ sin_t, int at,
                                                     float* __restrict__ qn_rows, int stride) {
   constexpr int kHalf = D / 2, kUnits = kHalf / 8;
   static_assert(NT % 32 == 0 && (128 * kUnits) % NT == 0, "whole warps, whole rows");
-#pragma unroll 1   // one unit in flight: it runs in the MMA issuers' 72-register budget
+#pragma unroll kUnroll
   for (int i = at; i < 128 * kUnits; i += NT) {
     const int row = i / kUnits, x = i % kUnits;
     const uint32_t offa = sw128_offset(row, x);
@@ -474,13 +475,15 @@ __device__ __forceinline__ void rotate_tile_smem_sq(uint32_t tile, const float* 
   }
 }
 
-template <int D, int NT>
+// rotate_tile_smem after a per-row RMSNorm with weights w (eps): kUnroll row units in flight
+// per thread.
+template <int D, int NT, int kUnroll = 1>
 __device__ __forceinline__ void rotate_tile_smem_norm(uint32_t tile, const float* __restrict__ cos_t,
                                                       const float* __restrict__ sin_t,
                                                       const float* __restrict__ w, float eps, int at) {
   constexpr int kHalf = D / 2, kUnits = kHalf / 8;
   static_assert(NT % 32 == 0 && (128 * kUnits) % NT == 0, "whole warps, whole rows");
-#pragma unroll 1
+#pragma unroll kUnroll
   for (int i = at; i < 128 * kUnits; i += NT) {
     const int row = i / kUnits, x = i % kUnits;
     const uint32_t offa = sw128_offset(row, x);

@@ -17,6 +17,8 @@
 // the tensor core idle between groups; two issuers overlap that cost. They touch disjoint
 // TMEM columns and every commit covers only its own thread's MMAs, so they need no ordering
 // between them beyond the barriers below. Cross-attention zeroes V pad rows in warps 14-15.
+// Workspace modes: warps 14-15 rotate the first item's Q tiles; each later item's tile t is
+// rotated by softmax warpgroup t once it has written its last P_t of the item before.
 // Synchronisation per query-tile slot t (all waits bounded):
 //   s_full[t]  S_t,j computed (commit)          -> softmax t
 //   s_free[t]  S_t,j loaded into registers       -> issuer may overwrite S_t (4 warp arrivals)
@@ -24,6 +26,7 @@
 //   pv_done[t] P_t,j V_j complete (commit)       -> softmax may rescale O_t / overwrite P_t;
 //                                                    the epilogue may read O_t
 //   o_free[t]  O_t read out by the epilogue      -> the next item's first PV may overwrite it
+//   q_ready    (workspace modes) Q rotated       -> S products of the item (8 warp arrivals)
 // Shared memory at D = 128: Q0, Q1 (64 KB), a ring of three K/V slots (96 KB), P0, P1
 // (64 KB). K and V share the ring, K one tile ahead of V, which gives a K load about two key
 // steps and a V load about one to land (two K and one V stage would leave V a fraction).
@@ -67,7 +70,6 @@ struct BarsSp {
   uint32_t tmem_base;
   int abort;
   int aux_go;
-  int qn_items;   // fixed-m mode: items whose q row norms are written (warps 14-15 count)
 };
 
 // The key tiles a CTA visits, flattened over its items: tile g (g = 0 .. G-1) needs K_g for
@@ -106,9 +108,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (tid == 0) {
     bars->abort = 0;
-    bars->qn_items = 0;
     mbar_init(b_q_full, 1);
-    mbar_init(b_q_ready, kMode == kModeRopeWs ? 8 : 1);   // workspace RoPE: the 8 softmax warps
+    mbar_init(b_q_ready, kWs ? 8 : 1);   // workspace modes: the 8 softmax warps
     mbar_init(b_q_empty, 1);
     for (int s = 0; s < R; ++s) {
       mbar_init(smem_u32(&bars->r_full[s]), 1);
@@ -153,8 +154,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // a counter: each thread's generic-proxy stores are fenced against the async proxy (the
     // TMA loads that read them), then the CTA counts itself in with a device-scope release;
     // only the K/V producer waits for the count. Meanwhile warps 14-15 rotate the first
-    // item's Q tiles in shared memory (later ones as they land: in their role below, or, in
-    // the workspace RoPE mode, in the softmax warpgroups).
+    // item's Q tiles in shared memory (the softmax warpgroups rotate later ones).
     const int fit = first_live(it0);
     Item fw{};
     if (fit < p.n_items) {
@@ -186,10 +186,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         fence_proxy_async_smem();
         named_bar_sync(1, 64);
-        if (at == 0) {
-          if (kFixedM) st_release_cta(&bars->qn_items, 1);
-          for (int x = 0; x < (kMode == kModeRopeWs ? 8 : 1); ++x) mbar_arrive(b_q_ready);
-        }
+        if (at == 0)
+          for (int x = 0; x < 8; ++x) mbar_arrive(b_q_ready);   // stands in for the 8 softmax warps
       }
     } else {
       // Fixed-m mode: the largest squared key norm of each (b, h) among this CTA's rows is
@@ -243,25 +241,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     ready = true;
     return true;
   };
-  // Fixed-m mode: a warp waits (lane 0 polls, bounded) until the count at `c`, published with
-  // a CTA-scope release, reaches `target`; the warp barrier passes the acquire to all lanes.
-  auto wait_count = [&](const int* c, int target) -> bool {
-    int ok = 1;
-    if (lane == 0) {
-      const uint64_t t0 = globaltimer_ns();
-      while (ld_acquire_cta(c) < target) {
-        if (*abort_flag) { ok = 0; break; }
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
-          *abort_flag = 1;
-          atomicOr(status, kStatusTimeoutSoftmax);
-          ok = 0;
-          break;
-        }
-      }
-    }
-    __syncwarp();
-    return __shfl_sync(0xffffffffu, ok, 0) != 0;
-  };
   // Fixed-m mode: a warp waits until every CTA has counted in its rotation (and with it its
   // key-norm maxima), with a device-scope acquire.
   auto wait_grid = [&]() -> bool {
@@ -312,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int it = it0; ok && it < p.n_items; it += it_step) {
       const Item w = decode_item<kMode>(p, it);
       if (w.n_live == 0) continue;
-      // Workspace mode: Q is used once warps 14-15 have rotated it in shared memory.
+      // Workspace modes: Q is used once it is rotated in shared memory (q_ready).
       if (!(ok = wait_bar(kWs ? b_q_ready : b_q_full, q_cnt))) break;
       for (int j = 0; ok && j < w.n_kv; ++j) {
         const int g = g0 + j;
@@ -532,20 +511,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float sl2 = p.scale_log2;
     int sc = 0;   // S_t tiles consumed so far (= P_t tiles produced = PV_t products issued)
     int qi = 0;   // live items seen so far
-    // Workspace RoPE mode: once its last P_t of live item qi is out, each softmax warpgroup
-    // rotates its tile t of the next live item's Q in shared memory, and each warp arrives on
-    // q_ready, so that the next item's S products start while this item's epilogue runs.
+    // Workspace modes: once its last P_t of live item qi is out, each softmax warpgroup
+    // rotates (and, per mode, normalises or takes the row norms of) its tile t of the next
+    // live item's Q in shared memory, and each warp arrives on q_ready, so that the next
+    // item's S products start while this item's epilogue runs.
     // (Warps 14-15 alone took about 16K cycles per item for the whole Q; the 256 softmax
     // threads take the tile they will use, with nothing else to do until the last P_t V.)
     auto rotate_next = [&](int it_cur) -> bool {
-      if constexpr (kMode == kModeRopeWs) {
+      if constexpr (kWs) {
         const int nit = first_live(it_cur + it_step);
         if (nit >= p.n_items) return true;
         const Item nw = decode_item<kMode>(p, nit);
         if (!warp_wait(b_q_full, (qi + 1) & 1, abort_flag, status, kStatusTimeoutRope)) return false;
         if (t < nw.n_live) {
           const size_t row0 = static_cast<size_t>(nw.q0 + 128 * t) * (D / 2);
-          rotate_tile_smem<D, 128, 4>(sQ + t * C::kTileBytes, p.cos_q + row0, p.sin_q + row0, r);
+          // Unroll depths as measured best per mode (code placement: with one unit in flight
+          // the norm and fixed-m modes ran 13-15 % slower at 720p too).
+          if constexpr (kNorm)
+            rotate_tile_smem_norm<D, 128, 4>(sQ + t * C::kTileBytes, p.cos_q + row0, p.sin_q + row0, ws.norm_q,
+                                             ws.norm_eps, r);
+          else if constexpr (kFixedM)
+            rotate_tile_smem_sq<D, 128, 2>(sQ + t * C::kTileBytes, p.cos_q + row0, p.sin_q + row0, r,
+                                           ws.qn + (static_cast<size_t>(nw.b) * p.Sq + nw.q0 + 128 * t) * p.H + nw.h,
+                                           p.H);
+          else
+            rotate_tile_smem<D, 128, 4>(sQ + t * C::kTileBytes, p.cos_q + row0, p.sin_q + row0, r);
         }
         fence_proxy_async_smem();
         __syncwarp();
@@ -577,7 +567,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // with no maximum and no rescaling, when every valid row has 2 m <= 64: then the
         // row's largest term exp2(s - m) is at least 2^-64. Pad rows (zero q, bound 0) and
         // pad keys (never in the maximum) cannot move a warp onto the online path.
-        if (!(ok = wait_count(&bars->qn_items, qi + 1))) break;
+        // The q row norms of this item were written before q_ready's phase qi completed (by
+        // warps 14-15 for the first item, else by this warpgroup in rotate_next); the wait's
+        // acquire makes them visible. The phase after it needs this warp's own arrival.
+        if (!(ok = warp_wait(b_q_ready, qi & 1, abort_flag, status, kStatusTimeoutSoftmax))) break;
         if (qi == 0 && !(ok = wait_grid())) break;
         const int qrow0 = w.q0 + 128 * t + r;
         const float kq = __uint_as_float(ws.kmax[w.b * p.H + w.h]);
@@ -754,46 +747,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) s_issuer();
     } else if (warp == 13) {
       if (lane == 0) pv_issuer();
-    } else if (kWs && kMode != kModeRopeWs) {
-      // ---------------------------------------------------------- Q rotation (warps 14-15)
-      constexpr int kRotThreads = 64;
-      const int at = tid - 448;
-      volatile int* go = &bars->aux_go;
-      int q_cnt = pre_q;
-      bool skip = pre_q != 0;   // the first item's Q was rotated before the roles started
-      bool ok = true;
-      for (int it = it0; ok && it < p.n_items; it += it_step) {
-        const Item w = decode_item<kMode>(p, it);
-        if (w.n_live == 0) continue;
-        if (skip) {
-          skip = false;
-          continue;
-        }
-        if (!(ok = group_wait<kRotThreads>(b_q_full, q_cnt & 1, abort_flag, status, kStatusTimeoutRope,
-                                           go, at)))
-          break;
-        for (int t = 0; t < w.n_live; ++t) {
-          const size_t row0 = static_cast<size_t>(w.q0 + 128 * t) * (D / 2);
-          if (kNorm)
-            rotate_tile_smem_norm<D, kRotThreads>(sQ + t * C::kTileBytes, p.cos_q + row0, p.sin_q + row0,
-                                                  ws.norm_q, ws.norm_eps, at);
-          else if (kFixedM)
-            rotate_tile_smem_sq<D, kRotThreads>(sQ + t * C::kTileBytes, p.cos_q + row0, p.sin_q + row0, at,
-                                                ws.qn + (static_cast<size_t>(w.b) * p.Sq + w.q0 + 128 * t) * p.H + w.h,
-                                                p.H);
-          else
-            rotate_tile_smem<D, kRotThreads>(sQ + t * C::kTileBytes, p.cos_q + row0, p.sin_q + row0, at);
-        }
-        fence_proxy_async_smem();
-        named_bar_sync(1, kRotThreads);
-        if (at == 0) {
-          // Fixed-m mode: the q row norms of this item (the CTA's live item number q_cnt) are
-          // written; the softmax warps read them after an acquire of this count.
-          if (kFixedM) st_release_cta(&bars->qn_items, q_cnt + 1);
-          mbar_arrive(b_q_ready);
-        }
-        ++q_cnt;
-      }
     } else if (kMode == kModeCross) {
       // ---------------------------------------------------------- V pad rows (warps 14-15)
       // K/V tiles are loaded up to Skv rows; rows past the batch's valid length are zeroed so
