@@ -2,7 +2,9 @@
 
 This layer only marshals arguments: it checks tensor placement, dtype, layout and shapes,
 allocates outputs with torch (device memory only), passes raw pointers and the current CUDA
-stream, and raises ``DitError`` on a non-zero status. Every step of the computation runs in
+stream, and raises ``DitError`` on a non-zero status. At the end, attn_self, attn_cross,
+attn_sharded, merge and rope take unpadded tensors and compose those calls (pad, cached RoPE
+tables, attention, unpad). Every step of the computation runs in
 the library's CUDA kernels; there is no fallback. Importing this module raises ImportError
 if the library has not been built (``video_dit_attention_gb300/build.py``).
 """
@@ -14,6 +16,8 @@ import os
 
 import numpy as np
 import torch
+
+from .padding import TILE, plan_token_padding
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libdit_attn.so")
@@ -458,3 +462,241 @@ def dit_exp2_fma_eval(x, out=None, stream=None):
     _need(out, "out", torch.float32)
     _check("dit_exp2_fma_eval", _lib.dit_exp2_fma_eval(_ptr(x), _ptr(out), x.numel(), _stream_handle(stream)))
     return out
+
+
+# ----------------------------------------------------------------------------- unpadded layer
+# What a model calls: unpadded [B, L, H, D] bf16 tensors in, unpadded O [B, L, H, D] bf16 and
+# LSE [B, L, H] fp32 (natural log) out. Each call pads to whole 128-row tiles on the device
+# (dit_pad_tokens; pad rows keep whatever the buffer held, since no kernel reads them), takes
+# its RoPE tables from a per-geometry cache (built once by the host table functions and kept
+# on the device, as the pages build them once per forward and share them across blocks),
+# calls one attention entry point and cuts the pad (dit_unpad_tokens). Sequences already a
+# whole number of tiles go in and out without copies.
+_MODES = ("exact", "fixed_m", "fp8")
+_TABLE_CACHE: dict = {}
+_TABLE_CACHE_MAX = 64
+
+
+def _tiles(n: int) -> int:
+    """Padded length of n rows: whole tiles, at least one (a 0-row key set still needs a
+    buffer; its valid length 0 gives O = 0 and LSE = -inf)."""
+    return max(TILE, plan_token_padding(n))
+
+
+def rope_tables(S_pad: int, D: int, rope, device, L: int = None, pos_offset: int = 0,
+                theta: float = 10000.0, axis_dims=(44, 42, 42)):
+    """Device (cos, sin) [S_pad, D/2] fp32 tables, cached per geometry and device.
+
+    rope = "1d": positions pos_offset .. pos_offset + L - 1 on rows 0 .. L - 1.
+    rope = (T, Hh, W): the 3-D latent grid (rows 0 .. T*Hh*W - 1, t slowest).
+    Rows past the valid ones are the identity rotation."""
+    dev = torch.device(device)
+    if dev.type == "cuda" and dev.index is None:
+        dev = torch.device("cuda", torch.cuda.current_device())
+    if rope == "1d":
+        if L is None:
+            raise ValueError("rope_tables: a 1-D table needs L")
+        key = ("1d", S_pad, D, int(L), int(pos_offset), float(theta), str(dev))
+    else:
+        grid = tuple(int(x) for x in rope)
+        key = ("3d", S_pad, D, grid, tuple(int(x) for x in axis_dims), float(theta), str(dev))
+    hit = _TABLE_CACHE.get(key)
+    if hit is not None:
+        return hit
+    if rope == "1d":
+        c, s = dit_rope_table_1d(S_pad, int(L), D, theta, int(pos_offset))
+    else:
+        c, s = dit_rope_table_3d(S_pad, key[3], D, axis_dims, theta)
+    if len(_TABLE_CACHE) >= _TABLE_CACHE_MAX:
+        _TABLE_CACHE.clear()
+    hit = (torch.from_numpy(c).to(dev), torch.from_numpy(s).to(dev))
+    _TABLE_CACHE[key] = hit
+    return hit
+
+
+def _pad(x, S_pad, stream):
+    if x.shape[1] == S_pad:
+        return x
+    if x.shape[1] == 0:       # nothing to copy (and an empty tensor has no data pointer)
+        return torch.empty((x.shape[0], S_pad) + tuple(x.shape[2:]), dtype=x.dtype, device=x.device)
+    return dit_pad_tokens(x, S_pad, stream=stream)
+
+
+def _unpad(x, L, stream):
+    return x if x.shape[1] == L else dit_unpad_tokens(x, L, stream=stream)
+
+
+def _check_grid(rope, Lq, Lk):
+    if rope is None or rope == "1d":
+        return
+    try:
+        grid = tuple(int(x) for x in rope)
+    except TypeError:
+        raise ValueError(f'rope must be None, "1d" or a (T, Hh, W) grid, got {rope!r}') from None
+    if len(grid) != 3 or min(grid) < 1:
+        raise ValueError(f"a 3-D RoPE grid is (T, Hh, W) with positive sizes, got {rope!r}")
+    if Lq != Lk or grid[0] * grid[1] * grid[2] != Lq:
+        raise ValueError(f"a 3-D grid {grid} needs Lq = Lk = T*Hh*W (got Lq={Lq}, Lk={Lk})")
+
+
+def attn_self(q, k, v, rope=None, *, mode: str = "exact", norm_q=None, norm_k=None, eps: float = 1e-6,
+              q_pos_offset: int = 0, k_pos_offset: int = 0, theta: float = 10000.0, axis_dims=(44, 42, 42),
+              softmax_scale=None, stream=None):
+    """Attention of unpadded q [B, Lq, H, D] over unpadded k, v [B, Lk, H, D] (bf16, CUDA).
+
+    rope: None; "1d" (query i at position q_pos_offset + i, key j at k_pos_offset + j); or a
+    (T, Hh, W) latent grid for 3-D RoPE (Lq = Lk = T*Hh*W).
+    mode: "exact" (dit_attn_fwd_ws with RoPE, dit_attn_fwd without), "fixed_m"
+    (dit_attn_fwd_ws_fixed_m, needs RoPE) or "fp8" (dit_attn_fwd_fp8, D = 128).
+    norm_q, norm_k: fp32 CUDA [D] weights of a per-head RMSNorm of q and k ahead of the
+    rotation (dit_attn_fwd_ws_qknorm: exact mode, with RoPE).
+    Returns (out [B, Lq, H, D] bf16, lse [B, Lq, H] fp32)."""
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be [B, L, H, D]")
+    B, Lq, H, D = q.shape
+    Lk = k.shape[1]
+    if tuple(k.shape) != (B, Lk, H, D) or v.shape != k.shape:
+        raise ValueError("k and v must be [B, Lk, H, D] matching q")
+    if mode not in _MODES:
+        raise ValueError(f"mode must be one of {_MODES}, got {mode!r}")
+    normed = norm_q is not None or norm_k is not None
+    if normed and (norm_q is None or norm_k is None):
+        raise ValueError("give both norm_q and norm_k, or neither")
+    if normed and (rope is None or mode != "exact"):
+        raise ValueError("the fused q/k RMSNorm runs in the exact mode with RoPE")
+    if mode == "fixed_m" and rope is None:
+        raise ValueError("the fixed-m mode runs with RoPE")
+    _check_grid(rope, Lq, Lk)
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, torch.bfloat16, 4)
+    if Lq == 0:
+        return (torch.empty((B, 0, H, D), dtype=torch.bfloat16, device=q.device),
+                torch.empty((B, 0, H), dtype=torch.float32, device=q.device))
+    Sq, Skv = _tiles(Lq), _tiles(Lk)
+    qp, kp, vp = _pad(q, Sq, stream), _pad(k, Skv, stream), _pad(v, Skv, stream)
+    if rope is None:
+        tabs = ()
+    elif rope == "1d":
+        tabs = rope_tables(Sq, D, "1d", q.device, L=Lq, pos_offset=q_pos_offset, theta=theta) + \
+               rope_tables(Skv, D, "1d", q.device, L=Lk, pos_offset=k_pos_offset, theta=theta)
+    else:
+        t3 = rope_tables(Sq, D, rope, q.device, theta=theta, axis_dims=axis_dims)
+        tabs = t3 + t3
+    kw = dict(softmax_scale=softmax_scale, stream=stream)
+    if mode == "fp8":
+        op, lp = dit_attn_fwd_fp8(qp, kp, vp, Lq, Lk, *tabs, **kw)
+    elif mode == "fixed_m":
+        op, lp = dit_attn_fwd_ws_fixed_m(qp, kp, vp, Lq, Lk, *tabs, **kw)
+    elif normed:
+        op, lp = dit_attn_fwd_ws_qknorm(qp, kp, vp, Lq, Lk, norm_q, norm_k, *tabs, eps=eps, **kw)
+    elif tabs:
+        op, lp = dit_attn_fwd_ws(qp, kp, vp, Lq, Lk, *tabs, **kw)
+    else:
+        op, lp = dit_attn_fwd(qp, kp, vp, Lq, Lk, **kw)
+    return _unpad(op, Lq, stream), _unpad(lp, Lq, stream)
+
+
+def attn_cross(q, k, v, kv_valid_len, *, softmax_scale=None, stream=None):
+    """Short-KV cross-attention of unpadded q [B, Lq, H, D] against k, v [B, Lk, H, D]
+    (bf16, CUDA, Lk <= 512): batch b attends to its first kv_valid_len[b] keys
+    (a sequence of B host integers in [0, Lk]). No RoPE.
+    Returns (out [B, Lq, H, D] bf16, lse [B, Lq, H] fp32)."""
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be [B, L, H, D]")
+    B, Lq, H, D = q.shape
+    Lk = k.shape[1]
+    if tuple(k.shape) != (B, Lk, H, D) or v.shape != k.shape:
+        raise ValueError("k and v must be [B, Lk, H, D] matching q")
+    if Lk > 512:
+        raise ValueError(f"the short-KV path takes at most 512 keys, got {Lk}")
+    lens = [int(x) for x in kv_valid_len]
+    if len(lens) != B or min(lens) < 0 or max(lens) > Lk:
+        raise ValueError(f"kv_valid_len must hold B={B} integers in [0, {Lk}], got {lens}")
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, n, torch.bfloat16, 4)
+    if Lq == 0:
+        return (torch.empty((B, 0, H, D), dtype=torch.bfloat16, device=q.device),
+                torch.empty((B, 0, H), dtype=torch.float32, device=q.device))
+    Sq, Skv = _tiles(Lq), _tiles(Lk)
+    qp, kp, vp = _pad(q, Sq, stream), _pad(k, Skv, stream), _pad(v, Skv, stream)
+    kv_dev = torch.tensor(lens, dtype=torch.int32).to(q.device)
+    op, lp = dit_cross_attn_shortkv(qp, kp, vp, Lq, kv_dev, softmax_scale=softmax_scale, stream=stream)
+    return _unpad(op, Lq, stream), _unpad(lp, Lq, stream)
+
+
+def attn_sharded(q, shards, rope="1d", *, q_pos_offset: int = 0, theta: float = 10000.0,
+                 softmax_scale=None, stream=None):
+    """Attention of unpadded q [B, Lq, H, D] over keys held in shards [(k_0, v_0), (k_1, v_1),
+    ...] (each [B, L_s, H, D] bf16, CUDA, in global key order): one partial (O_s, LSE_s) per
+    shard, then the LSE merge. With rope = "1d" every key keeps its global position (shard s
+    starts after the keys of shards 0 .. s-1) and query i sits at q_pos_offset + i; rope =
+    None runs without RoPE. Returns (out [B, Lq, H, D] bf16, lse [B, Lq, H] fp32)."""
+    if rope not in (None, "1d"):
+        raise ValueError('attn_sharded takes rope = "1d" or None')
+    if not 1 <= len(shards) <= 64:
+        raise ValueError(f"between 1 and 64 shards, got {len(shards)}")
+    if q.dim() != 4:
+        raise ValueError("q must be [B, L, H, D]")
+    B, Lq, H, D = q.shape
+    for s, (ks, vs) in enumerate(shards):
+        if ks.dim() != 4 or tuple(ks.shape) != (B, ks.shape[1], H, D) or vs.shape != ks.shape:
+            raise ValueError(f"shard {s}: k and v must be [B, L_s, H, D] matching q")
+    _need(q, "q", torch.bfloat16, 4)
+    for s, (ks, vs) in enumerate(shards):
+        _need(ks, f"k[{s}]", torch.bfloat16, 4)
+        _need(vs, f"v[{s}]", torch.bfloat16, 4)
+    if Lq == 0:
+        return (torch.empty((B, 0, H, D), dtype=torch.bfloat16, device=q.device),
+                torch.empty((B, 0, H), dtype=torch.float32, device=q.device))
+    n, Sq = len(shards), _tiles(Lq)
+    qp = _pad(q, Sq, stream)
+    po = torch.empty((n, B, Sq, H, D), dtype=torch.bfloat16, device=q.device)
+    pl = torch.empty((n, B, Sq, H), dtype=torch.float32, device=q.device)
+    tq = rope_tables(Sq, D, "1d", q.device, L=Lq, pos_offset=q_pos_offset, theta=theta) if rope else ()
+    offset = 0
+    for s, (ks, vs) in enumerate(shards):
+        Ls = ks.shape[1]
+        Ss = _tiles(Ls)
+        kp, vp = _pad(ks, Ss, stream), _pad(vs, Ss, stream)
+        if rope:
+            tk = rope_tables(Ss, D, "1d", q.device, L=Ls, pos_offset=offset, theta=theta)
+            dit_attn_fwd_ws(qp, kp, vp, Lq, Ls, *tq, *tk, softmax_scale=softmax_scale, out=po[s], lse=pl[s],
+                            stream=stream)
+        else:
+            dit_attn_fwd(qp, kp, vp, Lq, Ls, softmax_scale=softmax_scale, out=po[s], lse=pl[s], stream=stream)
+        offset += Ls
+    op, lp = dit_attn_lse_merge(po, pl, stream=stream)
+    return _unpad(op, Lq, stream), _unpad(lp, Lq, stream)
+
+
+def merge(partial_o, partial_lse, stream=None):
+    """LSE merge of n partials, given stacked ([n, B, S, H, D] bf16, [n, B, S, H] fp32) or as
+    sequences of n [B, S, H, D] / [B, S, H] tensors. Returns (out, lse)."""
+    if isinstance(partial_o, (list, tuple)):
+        partial_o = torch.stack(list(partial_o))
+    if isinstance(partial_lse, (list, tuple)):
+        partial_lse = torch.stack(list(partial_lse))
+    return dit_attn_lse_merge(partial_o.contiguous(), partial_lse.contiguous(), stream=stream)
+
+
+def rope(x, rope, *, pos_offset: int = 0, norm=None, eps: float = 1e-6, theta: float = 10000.0,
+         axis_dims=(44, 42, 42), out=None, stream=None):
+    """Split-halves RoPE of unpadded x [B, L, H, D] bf16 (CUDA): rope = "1d" (row i at
+    position pos_offset + i) or a (T, Hh, W) grid (L = T*Hh*W). With norm (fp32 CUDA [D]
+    weights) a per-head RMSNorm comes first (dit_qk_rmsnorm_rope). out may be x."""
+    if x.dim() != 4:
+        raise ValueError("x must be [B, L, H, D]")
+    B, L, H, D = x.shape
+    if rope is None:
+        raise ValueError('rope must be "1d" or a (T, Hh, W) grid')
+    _check_grid(rope, L, L)
+    _need(x, "x", torch.bfloat16, 4)
+    if L == 0:
+        return x if out is None else out
+    if rope == "1d":
+        c, s = rope_tables(L, D, "1d", x.device, L=L, pos_offset=pos_offset, theta=theta)
+    else:
+        c, s = rope_tables(L, D, rope, x.device, theta=theta, axis_dims=axis_dims)
+    if norm is not None:
+        return dit_qk_rmsnorm_rope(x, norm, c, s, eps=eps, out=out, stream=stream)
+    return dit_rope_split_halves(x, c, s, out=out, stream=stream)
