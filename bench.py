@@ -159,14 +159,16 @@ def gpu_id_for_smi(dev_index: int) -> str:
 KERNEL_SOURCES = ("attn_fwd.cu", "attn_sp.cuh", "ptx.cuh")
 
 
-def profiled_traffic(name):
+def profiled_traffic(name, variant=""):
     """DRAM bytes per launch of the dominant kernel (per step of four launches for the sharded
-    workload) from the committed ncu summary of this workload, or None if there is none or the
-    kernel sources changed since it was taken."""
+    workload) from the committed ncu summary of this workload (and kernel variant: "qknorm",
+    "fixed_m"), or None if there is none or the kernel sources changed since it was taken."""
     import hashlib
-    path = os.path.join(ROOT, "profiles", {"wan480": "attn_sp_wan480x832x9.md", "wan720": "attn_sp_wan720p81f.md",
-                                           "cross": "attn_sp_cross_shortkv.md",
-                                           "sharded": "attn_sp_sharded_keys.md"}.get(name, "-"))
+    base = {"wan480": "attn_sp_wan480x832x9", "wan720": "attn_sp_wan720p81f", "cross": "attn_sp_cross_shortkv",
+            "sharded": "attn_sp_sharded_keys"}.get(name)
+    if base is None:
+        return None
+    path = os.path.join(ROOT, "profiles", base + (f"_{variant}" if variant else "") + ".md")
     if not os.path.exists(path):
         return None
     srcs = [os.path.join(ROOT, "video_dit_attention_gb300", "csrc", f) for f in KERNEL_SOURCES]
@@ -766,8 +768,9 @@ def main():
         "pct_of_bf16_peak": 100.0 * (units / max_el / 1e12) / (peak * world),
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak,
-                     # the profiled traffic is that of the default kernel; the variants have none
-                     "traffic": None if (args.qknorm or args.fixed_m or args.fp8) else profiled_traffic(name),
+                     # FP8 is timed with its preparation kernels: no single-kernel traffic
+                     "traffic": None if args.fp8 else profiled_traffic(
+                         name, "qknorm" if args.qknorm else ("fixed_m" if args.fixed_m else "")),
                      "kernel": dominant_kernel(name, args.rope) + (" + q/k RMSNorm" if args.qknorm else "")
                      + (" (fixed-m softmax)" if args.fixed_m else "")
                      + (" (fp8; timed with its two preparation kernels)" if args.fp8 else ""),
