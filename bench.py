@@ -768,9 +768,10 @@ def main():
         "pct_of_bf16_peak": 100.0 * (units / max_el / 1e12) / (peak * world),
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak,
-                     # FP8 is timed with its preparation kernels: no single-kernel traffic
-                     "traffic": None if args.fp8 else profiled_traffic(
-                         name, "qknorm" if args.qknorm else ("fixed_m" if args.fixed_m else "")),
+                     # FP8 is timed with its preparation kernels: no single-kernel traffic;
+                     # the per-tile RoPE kernel has no committed capture
+                     "traffic": None if (args.fp8 or (args.rope == "fused" and name != "cross")) else
+                     profiled_traffic(name, "qknorm" if args.qknorm else ("fixed_m" if args.fixed_m else "")),
                      "kernel": dominant_kernel(name, args.rope) + (" + q/k RMSNorm" if args.qknorm else "")
                      + (" (fixed-m softmax)" if args.fixed_m else "")
                      + (" (fp8; timed with its two preparation kernels)" if args.fp8 else ""),
