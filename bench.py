@@ -4,9 +4,10 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 
 Workloads (synthetic, seeded; the token grids of the Wan / LTX runs the pages describe):
-  wan480  (default) Wan 480x832x9 self-attention: B1 H40 D128, 3x30x52 = 4680 tokens padded
-          to 4736, 3-D split-halves RoPE inside the attention launch, pad keys masked.
-  wan720  Wan 720p 81-frame self-attention: 21x45x80 = 75,600 tokens padded to 75,648.
+  wan720  (default) Wan 720p 81-frame self-attention: B1 H40 D128, 21x45x80 = 75,600 tokens
+          padded to 75,648, 3-D split-halves RoPE inside the attention launch, pad keys masked.
+          The largest single-GPU workload (117 TFLOP of valid work per call).
+  wan480  Wan 480x832x9 self-attention: 3x30x52 = 4680 tokens padded to 4736, same layout.
   cross   short-KV cross-attention: B2 H40 D128, 4680 (4736) queries x 512 text slots,
           per-batch valid lengths uniform on [1, 512].
   sharded 1024 queries over 37,800 keys in 4 shards (partials + LSE merge), B1 H32 D128.
@@ -26,6 +27,15 @@ compute of their neighbours (two buffer sets, three streams). RoPE runs inside t
 barrier, with `--rope fused` each loaded tile is rotated in shared memory instead.
 `--impl reference` times the fp64 CPU oracle instead,
 on the host cores, on a bounded sample of the same workload.
+
+Peaks: the attention kernel's fraction is taken against the measured bf16 GEMM peak of
+MEASURED_PEAKS.json, the sustained figure when the timed region runs longer than a second
+of back-to-back launches (720p: 20 launches of ~78 ms), else the burst figure; the line also
+carries the fraction of the nominal 2.25 PFLOP/s dense bf16 rate. All fractions come from
+CUDA-event kernel time; `roofline.ncu_kernel_ms` repeats the committed ncu duration of the
+same kernel sources where one exists. With the default workload the line also holds `also`,
+timed kernel-only records of the other D = 128 workloads (Wan 480, short-KV cross,
+sharded keys), each with its own clock record.
 
 Multi-GPU: `python -m torch.distributed.run --nproc-per-node N bench.py --gpus N`; each rank
 runs an independent replica (the problems are independent; no data-path collective), the
@@ -132,12 +142,26 @@ class ClockSampler:
             except Exception:
                 self.proc.kill()
 
-    def summary(self, t0, t1, load_t0):
+    def summary(self, t0, t1, busy_t0, busy_t1=None):
+        """Median SM clock and the throttle reasons seen over the timed region [t0, t1]. When that
+        region holds fewer than three samples (shorter than three sampling intervals), the
+        summary covers the whole GPU-busy window [busy_t0, busy_t1] instead (warm-up, timed
+        steps and the e2e leg), and `window` says so."""
         win = [s for s in self.samples if t0 <= s[0] <= t1]
         where = "timed region"
-        if len(win) < 2:
-            win = [s for s in self.samples if load_t0 <= s[0] <= t1]
-            where = "warm-up and timed region (timed region shorter than the sampling interval)"
+        if len(win) < 3:
+            hi = t1 if busy_t1 is None else busy_t1
+            win = [s for s in self.samples if busy_t0 <= s[0] <= hi]
+            where = ("GPU-busy window: warm-up, timed steps and e2e leg (the timed region is shorter "
+                     "than three 100 ms sampling intervals)")
+        if len(win) < 3:
+            # still too short: the three samples nearest the timed region (at most 0.5 s away)
+            mid = 0.5 * (t0 + t1)
+            near = sorted((s for s in self.samples if abs(s[0] - mid) <= 0.5 + 0.5 * (t1 - t0)),
+                          key=lambda s: abs(s[0] - mid))[:3]
+            if len(near) > len(win):
+                win = near
+                where = "the 3 samples nearest the timed region (it is shorter than the sampling interval)"
         if not win:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "window": "none"}
         reasons = sorted({self.NAMES[i] for s in win for i, v in enumerate(s[3]) if v.lower() == "active"})
@@ -159,10 +183,12 @@ def gpu_id_for_smi(dev_index: int) -> str:
 KERNEL_SOURCES = ("attn_fwd.cu", "attn_sp.cuh", "ptx.cuh")
 
 
-def profiled_traffic(name, variant=""):
-    """DRAM bytes per launch of the dominant kernel (per step of four launches for the sharded
-    workload) from the committed ncu summary of this workload (and kernel variant: "qknorm",
-    "fixed_m"), or None if there is none or the kernel sources changed since it was taken."""
+def profiled(name, variant=""):
+    """Figures of the committed ncu summary of this workload (and kernel variant: "qknorm",
+    "fixed_m"): {"traffic": DRAM bytes per launch of the dominant kernel (per step of four
+    launches for the sharded workload), "ncu_kernel_ms": its ncu duration per launch (per
+    step for sharded) or None}, or None if there is no summary or the kernel sources changed
+    since it was taken."""
     import hashlib
     base = {"wan480": "attn_sp_wan480x832x9", "wan720": "attn_sp_wan720p81f", "cross": "attn_sp_cross_shortkv",
             "sharded": "attn_sp_sharded_keys"}.get(name)
@@ -173,13 +199,17 @@ def profiled_traffic(name, variant=""):
         return None
     srcs = [os.path.join(ROOT, "video_dit_attention_gb300", "csrc", f) for f in KERNEL_SOURCES]
     h = hashlib.sha256(b"".join(open(f, "rb").read() for f in srcs)).hexdigest()[:16]
-    sha = traffic = None
+    sha = traffic = ncu_ms = None
     for line in open(path):
         if line.startswith("kernel sources sha256"):
             sha = line.split(":")[-1].strip()
         elif line.startswith(("traffic_bytes_per_launch:", "traffic_bytes_per_step:")):
             traffic = int(line.split(":")[1])   # per step for sharded (four launches), like achieved
-    return traffic if sha == h else None
+        elif line.startswith(("ncu_ms_per_launch:", "ncu_ms_per_step:")):
+            ncu_ms = float(line.split(":")[1])
+    if sha != h:
+        return None
+    return {"traffic": traffic, "ncu_kernel_ms": ncu_ms}
 
 
 def blas_threads():
@@ -639,12 +669,88 @@ def run_reference(args, name, spec, rank, world):
 
 
 # ----------------------------------------------------------------------------- main
+NOMINAL_BF16_TFLOPS = 2250.0   # GB300 dense bf16 tensor rate (vendor figure, no sparsity)
+SUSTAINED_AFTER_S = 1.0        # a timed region longer than this is judged against the sustained peak
+DEFAULT_STEPS = {"wan720": 20, "sharded": 200}
+
+
+def time_steps(wl, steps, warmup, world, stream):
+    """Warm-up, then `steps` timed steps bracketed by a barrier and a device synchronize on
+    both sides, with events around the dominant kernel of each step. Returns (elapsed
+    seconds of the timed region on the device, mean dominant-kernel seconds per step,
+    host time at the start and end of the timed region, host time before the warm-up)."""
+    import torch
+    busy_t0 = time.time()
+    for i in range(warmup):
+        wl.step(i)
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    start.record(stream)
+    for i in range(steps):
+        wl.step(i, evs[i])
+    end.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    t1 = time.time()
+    elapsed = start.elapsed_time(end) / 1e3
+    kern_s = sum(a.elapsed_time(b) for a, b in evs) / 1e3 / steps
+    status = wl.lib.dit_device_status()
+    if status != 0:
+        raise SystemExit(f"device status word {status:#x}: a kernel gave up on a bounded wait")
+    return elapsed, kern_s, t0, t1, busy_t0
+
+
+def pick_peak(peaks, elapsed_s, fp8=False):
+    """(peak TFLOP/s, description): sustained for a timed region longer than SUSTAINED_AFTER_S
+    of back-to-back launches, burst otherwise; fp8 takes twice the bf16 figure (the nominal
+    fp8 / bf16 ratio, 4.5 / 2.25)."""
+    key = "bf16_tflops_sustained" if elapsed_s > SUSTAINED_AFTER_S else "bf16_tflops"
+    kind = "sustained" if key == "bf16_tflops_sustained" else "burst"
+    peak, src = peaks[key], f"{key} ({kind}) of {peaks['source']} peaks"
+    if fp8:
+        return 2.0 * peak, f"2 x {src} (nominal fp8 / bf16 ratio)"
+    return peak, src + f" (timed region {elapsed_s:.2f} s: {kind})"
+
+
+def also_records(peaks, sampler, names, world, stream):
+    """Kernel-only records of other workloads in the same run: value, kernel time and the
+    fraction of the measured peak, each with the clocks seen over its own window."""
+    import torch
+    out = {}
+    for name in names:
+        spec = workload_spec(name)
+        wl = GpuWorkload(name, spec)
+        steps = 100 if name == "sharded" else 200
+        elapsed, kern_s, t0, t1, busy_t0 = time_steps(wl, steps, 5, world, stream)
+        flops = step_flops(name, spec)
+        peak, peak_src = pick_peak(peaks, elapsed)
+        achieved = flops / kern_s / 1e12
+        prof = profiled(name) or {}
+        out[name] = {"workload": config_dict(name, spec)["workload"], "steps": steps, "warmup": 5,
+                     "value": flops * steps / elapsed / 1e12, "unit": "TFLOP/s",
+                     "ms_per_step": elapsed / steps * 1e3, "kernel": dominant_kernel(name, "ws"),
+                     "kernel_ms": kern_s * 1e3, "achieved": achieved, "peak": peak, "peak_source": peak_src,
+                     "frac": achieved / peak, "frac_of_nominal_bf16": achieved / NOMINAL_BF16_TFLOPS,
+                     "traffic": prof.get("traffic"), "ncu_kernel_ms": prof.get("ncu_kernel_ms"),
+                     "algorithmic_bytes": wl.dominant_bytes(),
+                     "clocks": sampler.summary(t0, t1, busy_t0, time.time())}
+        del wl
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
-    ap.add_argument("--warmup", type=int, default=20)
-    ap.add_argument("--workload", default="wan480", choices=["wan480", "wan720", "cross", "sharded", "tiny"])
+    ap.add_argument("--steps", type=int, default=None,
+                    help="timed steps (default: 20 for wan720, 200 for sharded, else 1000)")
+    ap.add_argument("--warmup", type=int, default=None, help="warm-up steps (default: 3 for wan720, else 20)")
+    ap.add_argument("--workload", default="wan720", choices=["wan480", "wan720", "cross", "sharded", "tiny"])
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--rope", default="ws", choices=["ws", "fused"],
                     help="ws: rotate q/k once per call into a workspace (default); fused: rotate per tile")
@@ -658,11 +764,17 @@ def main():
                          "tensor-core products (D = 128 self-attention workloads)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-hbm-kernels", action="store_true", help="skip the RoPE / merge GB/s figures")
+    ap.add_argument("--no-also", action="store_true",
+                    help="skip the kernel-only records of the other workloads (default workload only)")
     args = ap.parse_args()
+    name = args.workload
+    if args.steps is None:
+        args.steps = DEFAULT_STEPS.get(name, 1000)
+    if args.warmup is None:
+        args.warmup = 3 if name == "wan720" else 20
     if args.warmup < 3:
         raise SystemExit("--warmup must be >= 3")
     rank, world, local = dist_env()
-    name = args.workload
     spec = workload_spec(name)
 
     if args.impl == "reference":
@@ -687,29 +799,7 @@ def main():
     stream = torch.cuda.current_stream()
 
     sampler = ClockSampler(gpu_id_for_smi(local))
-    load_t0 = time.time()
-    for i in range(args.warmup):
-        wl.step(i)
-    torch.cuda.synchronize()
-
-    # timed region: K steps, barrier + synchronize on both sides, per-launch events
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    torch.cuda.synchronize()
-    t0 = time.time()
-    start.record(stream)
-    for i in range(args.steps):
-        wl.step(i, evs[i])
-    end.record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    t1 = time.time()
-    elapsed = start.elapsed_time(end) / 1e3
-    kern_s = sum(a.elapsed_time(b) for a, b in evs) / 1e3 / args.steps
-    status = wl.lib.dit_device_status()
-    if status != 0:
-        raise SystemExit(f"device status word {status:#x}: a kernel gave up on a bounded wait")
+    elapsed, kern_s, t0, t1, busy_t0 = time_steps(wl, args.steps, args.warmup, world, stream)
 
     # e2e through the C-ABI with host buffers (self / cross workloads)
     e2e = None
@@ -738,23 +828,36 @@ def main():
                         + "attention -> " + ("" if ee.direct else "dit_unpad_tokens -> ")
                         + "D2H O, LSE; steps pipelined over two buffer sets (uploads, compute and "
                           "downloads on three streams)")}
-    sampler.stop()
+        del ee
+    busy_t1 = time.time()
+    launches = wl.launches_per_step * args.steps
+    host = wl.host
+    dom_bytes = wl.dominant_bytes()
+    del wl
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
 
     max_el, units = reduce_over_ranks(elapsed, flops * args.steps, world)
+    also = None
+    if (rank == 0 and world == 1 and not args.no_also and name == "wan720" and args.rope == "ws"
+            and not (args.qknorm or args.fixed_m or args.fp8)):
+        also = also_records(peaks, sampler, ("wan480", "cross", "sharded"), world, stream)
+    sampler.stop()
     if rank != 0:
         if world > 1:
             torch.distributed.destroy_process_group()
         return
-    clocks = sampler.summary(t0, t1, load_t0)
+    clocks = sampler.summary(t0, t1, busy_t0, busy_t1)
     achieved = flops / kern_s / 1e12
-    peak = peaks["bf16_tflops"]
-    peak_source = f"bf16_tflops (burst) of {peaks['source']} peaks"
-    if args.fp8:
-        # e4m3 products: the measured bf16 peak times the nominal fp8 / bf16 ratio (4.5 / 2.25)
-        peak = 2.0 * peaks["bf16_tflops"]
-        peak_source = f"2 x bf16_tflops (burst) of {peaks['source']} peaks (nominal fp8 / bf16 ratio)"
+    peak, peak_source = pick_peak(peaks, elapsed, fp8=args.fp8)
+    variant = "qknorm" if args.qknorm else ("fixed_m" if args.fixed_m else "")
+    # FP8 is timed with its preparation kernels: no single-kernel traffic; the per-tile RoPE
+    # kernel has no committed capture
+    prof = None if (args.fp8 or (args.rope == "fused" and name != "cross")) else profiled(name, variant)
+    prof = prof or {}
+    value = units / max_el / 1e12
     line = {
-        "metric": METRIC, "value": units / max_el / 1e12, "unit": "TFLOP/s", "n_gpus": world,
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": max_el / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "fp8_e4m3" if args.fp8 else "bf16",
@@ -765,27 +868,32 @@ def main():
             if args.fixed_m else {}), **(
             {"precision": "fp8 e4m3 operands (q per 128-row tile, k and v per head), P = e4m3(112 p), fp32 "
                           "accumulation; the step includes the two preparation kernels"} if args.fp8 else {})),
-        "pct_of_bf16_peak": 100.0 * (units / max_el / 1e12) / (peak * world),
+        "pct_of_bf16_peak": 100.0 * value / (peak * world),
+        "pct_of_nominal_bf16_dense": 100.0 * value / ((2.0 if args.fp8 else 1.0) * NOMINAL_BF16_TFLOPS * world),
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak,
-                     # FP8 is timed with its preparation kernels: no single-kernel traffic;
-                     # the per-tile RoPE kernel has no committed capture
-                     "traffic": None if (args.fp8 or (args.rope == "fused" and name != "cross")) else
-                     profiled_traffic(name, "qknorm" if args.qknorm else ("fixed_m" if args.fixed_m else "")),
+                     "frac_of_burst": achieved / ((2.0 if args.fp8 else 1.0) * peaks["bf16_tflops"]),
+                     "frac_of_nominal": achieved / ((2.0 if args.fp8 else 1.0) * NOMINAL_BF16_TFLOPS),
+                     "traffic": prof.get("traffic"),
+                     "ncu_kernel_ms": prof.get("ncu_kernel_ms"),
                      "kernel": dominant_kernel(name, args.rope) + (" + q/k RMSNorm" if args.qknorm else "")
                      + (" (fixed-m softmax)" if args.fixed_m else "")
                      + (" (fp8; timed with its two preparation kernels)" if args.fp8 else ""),
-                     "kernel_ms": kern_s * 1e3, "algorithmic_bytes": wl.dominant_bytes(),
-                     "peak_source": peak_source},
-        "gpu_launches": wl.launches_per_step * args.steps,
+                     "kernel_ms": kern_s * 1e3, "algorithmic_bytes": dom_bytes,
+                     "peak_source": peak_source,
+                     "target": "attention >= 60 % of the measured dense bf16 peak (fractions from CUDA-event "
+                               "kernel time)"},
+        "gpu_launches": launches,
         "clocks": clocks,
     }
     if e2e is not None:
         line["e2e"] = e2e
+    if also is not None:
+        line["also"] = also
     if rank == 0 and not args.no_hbm_kernels:
         line["hbm_kernels"] = measure_hbm_kernels(peaks)
     if not args.no_cpu_baseline and world == 1:
-        line["cpu_baseline"] = cpu_baseline(name, spec, wl.host)
+        line["cpu_baseline"] = cpu_baseline(name, spec, host)
     print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()

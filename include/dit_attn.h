@@ -60,10 +60,19 @@ const char* dit_status_string(int status);
 int dit_last_cuda_error(void);
 
 /* Reads the current device's status word into *status_out (host pointer) and clears it if
- * `clear` is non-zero. Bits are set by kernels that gave up on a bounded internal wait
+ * `clear` is non-zero. Bits 0-5 are set by kernels that gave up on a bounded internal wait
  * (each wait is limited to about two seconds, after which the kernel records the bit,
- * releases its resources and exits instead of hanging). Synchronizes the current device.
+ * releases its resources and exits instead of hanging); bit 6 by a cross-attention call
+ * that was given a key length outside its range (see dit_cross_attn_shortkv).
+ * Synchronizes the current device.
  * Returns DIT_OK, DIT_ERR_INVALID_ARG (null pointer) or DIT_ERR_CUDA. */
+#define DIT_STATUS_TIMEOUT_LOAD 0x01u    /* a TMA producer waited too long for a free slot    */
+#define DIT_STATUS_TIMEOUT_MMA 0x02u     /* an MMA issuer waited too long for its operands    */
+#define DIT_STATUS_TIMEOUT_SOFTMAX 0x04u /* a softmax / epilogue thread waited too long       */
+#define DIT_STATUS_TIMEOUT_AUX 0x08u     /* a rotation / zeroing thread waited too long       */
+#define DIT_STATUS_TIMEOUT_DRAIN 0x10u   /* cleanup after a timeout did not see work finish   */
+#define DIT_STATUS_TIMEOUT_GRID 0x20u    /* a CTA waited too long at a grid-wide barrier      */
+#define DIT_STATUS_BAD_KV_LENGTH 0x40u   /* a device-side key length outside [0, Skv]          */
 int dit_device_status(unsigned int* status_out, int clear);
 
 /* ---------------------------------------------------------------------------------------
@@ -265,13 +274,13 @@ int dit_qk_rmsnorm_rope(const void* x, void* y, const float* w, float eps, const
  * device current, once, under a lock. Make that first call outside any stream capture.
  *
  * Zero state: nothing in the array has to start at zero. Each call clears the grid-barrier
- * word on `stream` before its kernel starts, and the rotated q/k copies are written before
- * they are read.
+ * word on `stream` before its kernel starts, and the rotated k copy is written before
+ * it is read.
  *
  * Overlap: there is one array per device per process. Two calls in flight on the same
  * device at the same time share it. That happens with calls on two streams, or from two
  * host threads with no ordering between them. Such calls race: they overwrite each other's
- * rotated copies and barrier word, and their results are wrong. Order such calls on one
+ * rotated k copies and barrier word, and their results are wrong. Order such calls on one
  * stream, or use dit_attn_fwd_ws with one workspace per stream.
  *
  * Arguments, outputs and numerics are those of dit_attn_fwd_ws; all four tables are
@@ -289,7 +298,12 @@ int dit_attn_fwd_ws_static(const void* q, const void* k, const void* v, int B, i
  * Short-KV cross-attention (maxdiffusion PR #491: fused short-KV cross-attention of the video
  * queries against the text sequence). As dit_attn_fwd without RoPE, with one valid key
  * length per batch read on the device: kv_valid_len_dev[b] in [0, Skv] (int32, device
- * array of B entries; values outside are clamped into that range). Skv <= 512.
+ * array of B entries). Skv <= 512.
+ * Fails closed on the device: a batch whose length lies outside [0, Skv] is not clamped
+ * into range. All of its query rows get out = 0 and lse = -inf, and the kernel sets
+ * DIT_STATUS_BAD_KV_LENGTH in the device status word (read it with dit_device_status). The
+ * lengths live in device memory, so the call cannot check them before it returns without
+ * a host synchronisation; the status bit keeps the call asynchronous.
  * Errors as dit_attn_fwd; DIT_ERR_UNSUPPORTED also for Skv > 512.
  * ------------------------------------------------------------------------------------- */
 int dit_cross_attn_shortkv(const void* q, const void* k, const void* v, int B, int Sq,

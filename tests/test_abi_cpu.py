@@ -221,3 +221,41 @@ def test_fp8_entry_validation_before_any_cuda_call(clib):
     assert call(ws=P + 64) == -3                # workspace not 256-byte aligned
     assert call(tabs=(P + 4, P, P, P)) == -3    # tables must be 16-byte aligned
     assert call(tabs=(P, P, P + 8, P)) == -3
+
+
+def test_status_bits_agree_between_header_binding_and_kernels():
+    """The status-word bits the header documents are the ones the kernels set and the
+    binding names."""
+    text = open(HEADER).read()
+    hdr = {m.group(1): int(m.group(2), 16) for m in re.finditer(r"#define (DIT_STATUS_\w+) 0x([0-9a-fA-F]+)u", text)}
+    ptx = open(os.path.join(ROOT, "video_dit_attention_gb300", "csrc", "ptx.cuh")).read()
+    kern = {m.group(1): 1 << int(m.group(2)) for m in re.finditer(r"(kStatus\w+) = 1u << (\d+)", ptx)}
+    pairs = {"DIT_STATUS_TIMEOUT_LOAD": "kStatusTimeoutLoad", "DIT_STATUS_TIMEOUT_MMA": "kStatusTimeoutMma",
+             "DIT_STATUS_TIMEOUT_SOFTMAX": "kStatusTimeoutSoftmax", "DIT_STATUS_TIMEOUT_AUX": "kStatusTimeoutRope",
+             "DIT_STATUS_TIMEOUT_DRAIN": "kStatusTimeoutDrain", "DIT_STATUS_TIMEOUT_GRID": "kStatusTimeoutGrid",
+             "DIT_STATUS_BAD_KV_LENGTH": "kStatusBadKvLength"}
+    assert set(hdr) == set(pairs) and set(kern) == set(pairs.values())
+    for h, k in pairs.items():
+        assert hdr[h] == kern[k], h
+    import ast
+    src = open(os.path.join(ROOT, "video_dit_attention_gb300", "dit_attn.py")).read()
+    consts = {t.id: n.value.value for n in ast.parse(src).body if isinstance(n, ast.Assign)
+              for t in n.targets if isinstance(t, ast.Name) and t.id.startswith("DIT_STATUS_")}
+    assert consts == hdr
+
+
+def test_test_hook_library_is_separate_from_the_product():
+    """The test-only library exports the hook (and the product calls); the product library
+    does not contain it."""
+    test_lib = os.path.join(ROOT, "video_dit_attention_gb300", "libdit_attn_testhooks.so")
+    if not os.path.exists(test_lib):
+        from video_dit_attention_gb300.build import build
+        build()
+    t = ctypes.CDLL(test_lib)
+    assert hasattr(t, "dit_test_set_wait_hooks")
+    for name in declared_functions():
+        assert hasattr(t, name), name
+    p = ctypes.CDLL(LIB)
+    assert not hasattr(p, "dit_test_set_wait_hooks")
+    hdr = open(os.path.join(ROOT, "include", "dit_attn_test_hooks.h")).read()
+    assert "int dit_test_set_wait_hooks(unsigned long long wait_limit_ns, int skip_load);" in hdr

@@ -43,6 +43,28 @@ def test_cross_pad_garbage_is_nan_safe(lib):
     compare(O2, L2, Or, Lr, case.q_valid)
 
 
+@pytest.mark.parametrize("bad", [513, -1, 2 ** 31 - 1])
+def test_cross_out_of_range_length_fails_closed(lib, bad):
+    """A device-side key length outside [0, Skv] is not clamped: that batch's rows get
+    O = 0 / LSE = -inf and the status word reports DIT_STATUS_BAD_KV_LENGTH; the other batch
+    is computed as usual, and the next call with good lengths leaves the status clear."""
+    case = AttnCase("crossbad", B=2, H=3, D=128, Sq=256, Skv=512, q_valid=200, kv_valid=[300, 130], seed=73)
+    q, k, v = make_qkv(case)
+    assert lib.dit_device_status() == 0
+    kv = torch.tensor([bad, 130], dtype=torch.int32, device="cuda")
+    out, lse = lib.dit_cross_attn_shortkv(dev_bf16(q), dev_bf16(k), dev_bf16(v), case.q_valid, kv)
+    torch.cuda.synchronize()
+    assert lib.dit_device_status() == lib.DIT_STATUS_BAD_KV_LENGTH
+    O, L = out.float().cpu().numpy(), lse.cpu().numpy()
+    assert np.all(O[0] == 0) and np.all(L[0] == -np.inf)
+    Or, Lr = attention(q[1:], k[1:], v[1:], case.q_valid, [130], case.scale)
+    compare(O[1:], L[1:], Or, Lr, case.q_valid)
+    O2, L2 = _run_cross(lib, case, q, k, v)
+    assert lib.dit_device_status() == 0
+    Or2, Lr2 = attention(q, k, v, case.q_valid, case.kv_valid, case.scale)
+    compare(O2, L2, Or2, Lr2, case.q_valid)
+
+
 def test_cross_workload_full(lib):
     case = cross_case()
     q, k, v = make_qkv(case)

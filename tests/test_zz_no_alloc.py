@@ -57,7 +57,7 @@ def test_static_scratch_two_problems_in_a_row(lib):
 
 def test_static_scratch_same_shape_twice(lib):
     """Two calls of one shape with different inputs: nothing of the first call's scratch
-    (rotated copies, barrier word) leaks into the second."""
+    (rotated k copy, barrier word) leaks into the second."""
     c1 = AttnCase("ws-static", B=2, H=3, D=128, Sq=640, Skv=768, q_valid=601, kv_valid=700,
                   rope="1d", seed=90)
     c2 = dataclasses.replace(c1, seed=91)

@@ -1,5 +1,7 @@
 // C-ABI entry points (include/dit_attn.h): argument validation, TMA descriptor encoding and
-// kernel launches. No device memory is allocated here; every buffer belongs to the caller.
+// kernel launches. No device memory is allocated at call time; every buffer belongs to the
+// caller, except one fixed file-scope device array (end of this file) that only
+// dit_attn_fwd_ws_static uses as its workspace.
 
 #include <cmath>
 #include <cstdint>

@@ -254,7 +254,8 @@ __device__ __forceinline__ void write_empty_tile(const KParams& p, int b, int h,
 // One unit of work: query rows q0 .. q0 + 255 (two 128-row tiles) of one (b, h).
 struct Item {
   int b, h, q0, n_live, n_kv, kv_valid;
-  bool has1;   // tile 1 (rows q0 + 128 ..) lies inside the padded sequence
+  bool has1;      // tile 1 (rows q0 + 128 ..) lies inside the padded sequence
+  bool bad_len;   // cross-attention: the batch's device-side key length is outside [0, Skv]
 };
 
 template <int kMode>
@@ -265,7 +266,15 @@ __device__ __forceinline__ Item decode_item(const KParams& p, int it) {
   w.b = bh / p.H;
   w.q0 = pair * 256;
   int kv = p.kv_valid;
-  if (kMode == kModeCross) kv = min(max(p.kv_valid_dev[w.b], 0), p.Skv);
+  w.bad_len = false;
+  if (kMode == kModeCross) {
+    // Fail closed: a length outside [0, Skv] is not clamped into range. The batch is treated
+    // as having no keys (its rows get O = 0, LSE = -inf) and the call reports it through the
+    // device status word.
+    const int raw = p.kv_valid_dev[w.b];
+    w.bad_len = raw < 0 || raw > p.Skv;
+    kv = w.bad_len ? 0 : raw;
+  }
   w.kv_valid = kv;
   // Tile t is live if it holds a valid query row and there is at least one key.
   w.has1 = w.q0 + 128 < p.Sq;
@@ -1089,13 +1098,13 @@ cudaError_t launch_mode(const AttnArgs& a) {
       zero_bytes = 256 + kmax_bytes;   // the counter block and the key-norm maxima
     }
   }
-  static const int sm_count = [] {
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess &&
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
-      return n;
-    return 148;
-  }();
+  // SM count of the current device, asked on every launch (an attribute query is cheap), so
+  // that calls on devices with different SM counts each size their persistent grid right.
+  int dev = 0, sm_count = 0;
+  cudaError_t qe = cudaGetDevice(&dev);
+  if (qe == cudaSuccess) qe = cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev);
+  if (qe != cudaSuccess) return qe;
+  if (sm_count < 1) return cudaErrorInvalidDevice;
   const int grid = p.n_items < sm_count ? p.n_items : sm_count;   // persistent: one CTA per SM
   if constexpr (kMode == kModeRope) {
     // Per-tile RoPE needs shared memory for its table ring, so it keeps P in TMEM.
@@ -1169,3 +1178,15 @@ cudaError_t read_device_status(unsigned int* out, bool clear) {
 }
 
 }  // namespace dit
+
+#ifdef DIT_TEST_HOOKS
+#include "../../include/dit_attn_test_hooks.h"
+
+extern "C" int dit_test_set_wait_hooks(unsigned long long wait_limit_ns, int skip_load) {
+  if (wait_limit_ns == 0) return -1;
+  cudaError_t e = cudaMemcpyToSymbol(dit::g_dit_test_wait_limit_ns, &wait_limit_ns, sizeof(wait_limit_ns));
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(dit::g_dit_test_skip_load, &skip_load, sizeof(skip_load));
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  return e == cudaSuccess ? 0 : -4;
+}
+#endif

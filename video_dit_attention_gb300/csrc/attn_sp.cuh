@@ -230,7 +230,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t t0 = globaltimer_ns();
     while (ld_acquire_gpu(ws.rotated) < gridDim.x) {
       if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (globaltimer_ns() - t0 > wait_limit_ns()) {
         *abort_flag = 1;
         atomicOr(status, kStatusTimeoutGrid);
         return false;
@@ -249,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t t0 = globaltimer_ns();
       while (ld_acquire_gpu(ws.rotated) < gridDim.x) {
         if (*abort_flag) { ok = 0; break; }
-        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+        if (globaltimer_ns() - t0 > wait_limit_ns()) {
           *abort_flag = 1;
           atomicOr(status, kStatusTimeoutGrid);
           ok = 0;
@@ -327,11 +327,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       g0 += w.n_kv;
       ++q_cnt;
     }
-    if (*abort_flag) {
-      // Wait for every MMA this thread issued before TMEM and shared memory are released.
-      mma_commit(smem_u32(&bars->drain[0]));
-      drain_wait(smem_u32(&bars->drain[0]), 0, status);
-    }
+    // Wait for every MMA this thread issued before TMEM and shared memory are released. On
+    // the normal path the softmax has already waited for each of them; after an abort some
+    // may still be running when the other roles reach the final barrier.
+    mma_commit(smem_u32(&bars->drain[0]));
+    drain_wait(smem_u32(&bars->drain[0]), 0, status);
   };
   auto pv_issuer = [&]() {
     // ------------------------------------------------------------ O_t (+)= P_t V_g
@@ -383,10 +383,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (w.n_live == 2) ++epi1;
       g0 += w.n_kv;
     }
-    if (*abort_flag) {
-      mma_commit(smem_u32(&bars->drain[1]));
-      drain_wait(smem_u32(&bars->drain[1]), 0, status);
-    }
+    mma_commit(smem_u32(&bars->drain[1]));   // as for the S issuer
+    drain_wait(smem_u32(&bars->drain[1]), 0, status);
   };
 
   {
@@ -416,7 +414,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         w.q0 + 128 * t, w.b);
         ++q_cnt;
       }
-      if (*abort_flag && q_cnt > 0) drain_wait(b_q_full, (q_cnt - 1) & 1, status);
+      // The last Q load has landed before the CTA exits (it has already on the normal path).
+      if (q_cnt > 0) drain_wait(b_q_full, (q_cnt - 1) & 1, status);
     } else if (warp == 2 && lane == 0) {
       // ------------------------------------------------------------ producer: K/V ring
       const int G = count_tiles();
@@ -427,6 +426,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (use > 0 && !bounded_wait(smem_u32(&bars->r_empty[slot]), (use - 1) & 1, abort_flag,
                                      status, kStatusTimeoutLoad))
           return false;
+#ifdef DIT_TEST_HOOKS
+        if (n == g_dit_test_skip_load) {   // test build only: counted, never issued
+          ++n;
+          return true;
+        }
+#endif
         const uint32_t bar = smem_u32(&bars->r_full[slot]);
         mbar_arrive_expect_tx(bar, C::kTileBytes);
         if (kFp8 && map == &tm_v) {
@@ -488,10 +493,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (g + 1 < G && !(ok = load_next_k())) break;
         ok = load_next_v();
       }
-      if (*abort_flag) {
-        // Let the copies still in flight land before the CTA releases its shared memory.
-        for (int x = n - R > 0 ? n - R : 0; x < n; ++x)
+      {
+        // Let the copies still in flight land before the CTA releases its shared memory (on the
+        // normal path every load has been consumed, so these waits return at once).
+        for (int x = n - R > 0 ? n - R : 0; x < n; ++x) {
+#ifdef DIT_TEST_HOOKS
+          if (x == g_dit_test_skip_load) continue;   // never issued: nothing to land
+#endif
           drain_wait(smem_u32(&bars->r_full[x % R]), (x / R) & 1, status);
+        }
       }
     }
   } else if (warp < 12) {
@@ -548,6 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Item w = decode_item<kMode>(p, it);
       if (t >= w.n_live) {
         if (t == 0 || w.has1) write_empty_tile<D>(p, w.b, w.h, w.q0 + 128 * t, r, 128);
+        if (kMode == kModeCross && w.bad_len && t == 0 && r == 0) atomicOr(status, kStatusBadKvLength);
         if (w.n_live > 0) {
           if (!(ok = rotate_next(it))) break;
           ++qi;

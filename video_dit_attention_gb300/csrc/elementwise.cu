@@ -13,14 +13,13 @@
 namespace dit {
 namespace {
 
+// Grid of a grid-stride kernel: enough CTAs for the items, at most 8 per SM of the current
+// device (asked per launch, so devices with different SM counts each get their own cap).
 int grid_for(long long items, int threads) {
-  static const int sm_count = [] {
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) == cudaSuccess &&
-        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
-      return n;
-    return 148;
-  }();
+  int dev = 0, sm_count = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sm_count < 1)
+    sm_count = 1;   // the loops stride over the grid, so any grid size is correct
   const long long need = (items + threads - 1) / threads;
   const long long cap = static_cast<long long>(sm_count) * 8;
   long long g = need < cap ? need : cap;

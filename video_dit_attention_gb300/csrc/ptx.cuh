@@ -22,12 +22,26 @@ enum : unsigned int {
   kStatusTimeoutRope = 1u << 3,   // a rotation thread gave up waiting for a landed tile
   kStatusTimeoutDrain = 1u << 4,  // cleanup after an abort did not see in-flight work finish
   kStatusTimeoutGrid = 1u << 5,   // a CTA gave up waiting at the grid-wide barrier
+  kStatusBadKvLength = 1u << 6,   // cross-attention: a device-side key length outside [0, Skv]
 };
 
 // Upper bound on any single wait, in nanoseconds of %globaltimer. Every wait in
 // these kernels normally completes in microseconds; after this long the kernel
 // records a status bit, lets its other roles fall through and exits cleanly.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+#ifdef DIT_TEST_HOOKS
+// Test-only build (libdit_attn_testhooks.so, never the product library): the limit is a
+// device variable that a test shortens, so that a wait it makes run out gives up within
+// milliseconds instead of seconds.
+__device__ unsigned long long g_dit_test_wait_limit_ns = kWaitLimitNs;
+// Number of the K/V ring load that the attention kernel's producer counts but never issues
+// (-1: none). The consumers of that load then wait until the limit runs out.
+__device__ int g_dit_test_skip_load = -1;
+__device__ __forceinline__ uint64_t wait_limit_ns() { return g_dit_test_wait_limit_ns; }
+#else
+__device__ __forceinline__ constexpr uint64_t wait_limit_ns() { return kWaitLimitNs; }
+#endif
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
@@ -75,7 +89,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 
 // Waits for the phase with the given parity to complete. Returns false if the CTA
 // is aborting (another role gave up) or if this wait itself ran past
-// kWaitLimitNs; in the latter case it raises the CTA abort flag and ORs `code`
+// wait_limit_ns(); in the latter case it raises the CTA abort flag and ORs `code`
 // into the device status word. Never spins forever.
 __device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity,
                                              volatile int* cta_abort,
@@ -86,7 +100,7 @@ __device__ __forceinline__ bool bounded_wait(uint32_t bar, uint32_t parity,
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 63u) == 0) {
       if (*cta_abort) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (globaltimer_ns() - t0 > wait_limit_ns()) {
         *cta_abort = 1;
         atomicOr(dev_status, code);
         return false;
@@ -103,7 +117,7 @@ __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity,
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (globaltimer_ns() - t0 > wait_limit_ns()) {
       atomicOr(dev_status, kStatusTimeoutDrain);
       return false;
     }

@@ -108,8 +108,20 @@ def dit_status_string(status: int) -> str:
     return _lib.dit_status_string(status).decode()
 
 
+# Bits of the device status word (include/dit_attn.h).
+DIT_STATUS_TIMEOUT_LOAD = 0x01
+DIT_STATUS_TIMEOUT_MMA = 0x02
+DIT_STATUS_TIMEOUT_SOFTMAX = 0x04
+DIT_STATUS_TIMEOUT_AUX = 0x08
+DIT_STATUS_TIMEOUT_DRAIN = 0x10
+DIT_STATUS_TIMEOUT_GRID = 0x20
+DIT_STATUS_BAD_KV_LENGTH = 0x40
+
+
 def dit_device_status(clear: bool = True) -> int:
-    """Status word of the current device (bits of kernels that gave up on a bounded wait)."""
+    """Status word of the current device: bits of kernels that gave up on a bounded wait
+    (DIT_STATUS_TIMEOUT_*) and of cross-attention calls given a key length out of range
+    (DIT_STATUS_BAD_KV_LENGTH)."""
     out = ctypes.c_uint(0)
     _check("dit_device_status", _lib.dit_device_status(ctypes.byref(out), 1 if clear else 0))
     return int(out.value)
