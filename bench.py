@@ -180,7 +180,7 @@ def gpu_id_for_smi(dev_index: int) -> str:
 
 
 # The attention kernels' sources: a committed ncu summary applies while their hash matches.
-KERNEL_SOURCES = ("attn_fwd.cu", "attn_sp.cuh", "ptx.cuh")
+KERNEL_SOURCES = ("attn_fwd.cu", "attn_sp.cuh", "ptx.cuh", "cross_attn.cu")
 
 
 def profiled(name, variant=""):
@@ -241,7 +241,8 @@ def config_dict(name, spec, rope_mode="ws"):
         return {"workload": "sharded-key attention + LSE merge", "B": spec.B, "H": spec.H, "D": spec.D,
                 "queries": spec.Sq, "keys": sum(spec.shard_valid), "shards": list(spec.shard_valid),
                 "rope": "1-D split halves, theta 10000, global key positions",
-                "rope_path": _ROPE_PATH[rope_mode],
+                "rope_path": "one dit_attn_fwd_sharded call: every shard's k rotated once into an fp16 "
+                             "workspace, all key chunks attended in one launch, partials merged",
                 "l2": "3 rotating input sets of 0.69 GB each (> 129 MB L2)"}
     d = {"workload": {"wan480": "Wan 480x832x9 self-attention", "wan720": "Wan 720p 81-frame self-attention",
                       "tiny": "tiny self-attention", "cross": "short-KV cross-attention"}[name],
@@ -265,8 +266,10 @@ def spec_has_no_rope(spec):
 
 def dominant_kernel(name, rope_mode):
     if name == "cross":
-        return "attn_sp_kernel (cross mode)"
-    if rope_mode == "fused" and name != "cross":
+        return "cross_attn_kernel (K/V of a head resident in shared memory)"
+    if name == "sharded":
+        return "attn_sp_kernel (sharded keys: all key chunks in one launch) + lse_merge_fixed_kernel"
+    if rope_mode == "fused":
         return "attn_fwd_kernel (RoPE per loaded tile)"
     return "attn_sp_kernel (workspace RoPE)"
 
@@ -322,16 +325,15 @@ class GpuWorkload:
                 qq = torch.roll(base[0], r, dims=2).contiguous()
                 kv = [(torch.roll(k, r, dims=2).contiguous(), torch.roll(v, r, dims=2).contiguous())
                       for k, v in base[1]]
-                n = len(kv)
-                po = torch.empty((n,) + tuple(qq.shape), dtype=torch.bfloat16, device=dev)
-                pl = torch.empty((n,) + tuple(qq.shape[:3]), dtype=torch.float32, device=dev)
+                entries = [(k, v, n, ck, sk) for (k, v), n, (ck, sk) in zip(kv, spec.shard_valid, self.tk)]
                 out = torch.empty_like(qq)
                 lse = torch.empty(tuple(qq.shape[:3]), dtype=torch.float32, device=dev)
-                self.sets.append((qq, kv, po, pl, out, lse))
-            self.launches_per_step = len(spec.shard_valid) + 1
-            if rope_mode == "ws":
-                nb = max(ws_bytes(spec.B, spec.Sq, npad, spec.H, spec.D) for npad in spec.shard_pad)
-                self.workspace = torch.empty(nb, dtype=torch.uint8, device=dev)
+                self.sets.append((qq, entries, out, lse))
+            # one dit_attn_fwd_sharded call: the attention launch over all key chunks, the merge
+            self.launches_per_step = 2
+            nb = lib.dit_attn_sharded_workspace_bytes(spec.B, spec.Sq, spec.H, spec.D, spec.shard_pad,
+                                                      spec.shard_valid)
+            self.workspace = torch.empty(nb, dtype=torch.uint8, device=dev)
         else:
             spec.seed += seed_offset
             q, k, v = I.make_qkv(spec)
@@ -381,18 +383,17 @@ class GpuWorkload:
 
     def step(self, i, ev=None):
         """Launches one step on the current stream; ev = (start, end) events around the
-        dominant kernel (the attention launch; for `sharded`, the four partial launches)."""
+        dominant kernel (the attention launch; for `sharded`, the one call: the attention launch
+        over all key chunks and the merge of their partials)."""
         lib, spec = self.lib, self.spec
         s = self.sets[i % len(self.sets)]
         if ev is not None:
             ev[0].record()
         if self.name == "sharded":
-            qq, kv, po, pl, out, lse = s
-            for j, ((k, v), (ck, sk), n) in enumerate(zip(kv, self.tk, spec.shard_valid)):
-                self.attn(qq, k, v, spec.q_valid, n, (self.tq[0], self.tq[1], ck, sk), po[j], pl[j])
+            qq, entries, out, lse = s
+            lib.dit_attn_fwd_sharded(qq, entries, spec.q_valid, *self.tq, workspace=self.workspace, out=out, lse=lse)
             if ev is not None:
                 ev[1].record()
-            lib.dit_attn_lse_merge(po, pl, out=out, lse=lse)
             return
         qq, kk, vv, out, lse = s
         if self.name == "cross":
@@ -407,8 +408,9 @@ class GpuWorkload:
         O and LSE written)."""
         sp = self.spec
         if self.name == "sharded":
+            # q and k, v read once, O and LSE written once (the partials stay on the device)
             kv = sum(2 * sp.B * n * sp.H * sp.D * 2 for n in sp.shard_valid)
-            return kv + len(sp.shard_valid) * (sp.B * sp.q_valid * sp.H * (sp.D * 2 * 2 + 4))
+            return kv + sp.B * sp.q_valid * sp.H * (sp.D * 2 * 2 + 4)
         Lkv = sum(sp.kv_valid) if self.name == "cross" else sp.B * int(sp.kv_valid)
         return (sp.B * sp.q_valid * sp.H * sp.D * 2 + 2 * Lkv * sp.H * sp.D * 2
                 + sp.B * sp.q_valid * sp.H * (sp.D * 2 + 4))
@@ -766,6 +768,9 @@ def main():
     ap.add_argument("--no-hbm-kernels", action="store_true", help="skip the RoPE / merge GB/s figures")
     ap.add_argument("--no-also", action="store_true",
                     help="skip the kernel-only records of the other workloads (default workload only)")
+    ap.add_argument("--heads", type=int, default=None,
+                    help="profiling only: run the workload with this many heads (a smaller ncu capture "
+                         "whose per-head figures scale to the full workload); marks the line reduced")
     args = ap.parse_args()
     name = args.workload
     if args.steps is None:
@@ -776,6 +781,10 @@ def main():
         raise SystemExit("--warmup must be >= 3")
     rank, world, local = dist_env()
     spec = workload_spec(name)
+    if args.heads is not None:
+        if not 1 <= args.heads <= spec.H:
+            raise SystemExit(f"--heads must be in [1, {spec.H}]")
+        spec.H = args.heads
 
     if args.impl == "reference":
         run_reference(args, name, spec, rank, world)
@@ -862,6 +871,8 @@ def main():
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "fp8_e4m3" if args.fp8 else "bf16",
         "data": "synthetic", "config": dict(config_dict(name, spec, args.rope), **(
+            {"reduced": f"{spec.H} heads instead of the workload's (profiling run; not a bench value)"}
+            if args.heads is not None else {}), **(
             {"qk_norm": "per-head RMSNorm before the rotation, synthetic weights 1 + 0.1 N(0,1), eps 1e-6"}
             if args.qknorm else {}), **(
             {"softmax": "fixed-m: 32-row blocks whose bound scale*|q|*max|k| allows it skip the running maximum"}

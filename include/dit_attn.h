@@ -312,6 +312,47 @@ int dit_cross_attn_shortkv(const void* q, const void* k, const void* v, int B, i
                            float* lse, void* stream);
 
 /* ---------------------------------------------------------------------------------------
+ * Attention of one query block over keys held in shards, in one call (mstar PR #376:
+ * attention over sharded keys, each shard's partial output and log-sum-exp merged through
+ * the LSE; Difflet PR #153: every token keeps its rotary angle, so shard s rotates its keys
+ * at their global positions). Computes exactly what dit_attn_fwd with RoPE would over the
+ * concatenation of the shards' valid keys:
+ *   for query row i < q_valid_len:  lse_i = ln sum_{s, j < valid_s} exp(score_sj),
+ *   out_i = sum_{s, j} exp(score_sj - lse_i) v_sj,  score_sj = softmax_scale q~_i . k~_sj,
+ * with q~ rotated by (cos_q, sin_q) and the keys of shard s by (cos_k[s], sin_k[s]).
+ * Pad query rows and rows with no valid key at all get out = 0, lse = -inf.
+ *
+ * One cooperative launch rotates every shard's valid k rows into an fp16 copy in the
+ * workspace and runs the attention of all shards at once: the shards are cut into key chunks
+ * of whole 128-row tiles of near-equal length, so that chunks x B x H x (256-row query blocks)
+ * gives enough work items to fill the GPU; each chunk writes a partial (O, LSE) to the
+ * workspace. A second launch merges the partials (dit_attn_lse_merge's kernel).
+ *
+ * q: [B, Sq, H, D] bf16; out: [B, Sq, H, D] bf16; lse: [B, Sq, H] fp32; cos_q, sin_q:
+ * [Sq, D/2] fp32. k_shards[s], v_shards[s]: [B, shard_padded[s], H, D] bf16 (device pointers
+ * held in host arrays of n_shards entries); cos_k[s], sin_k[s]: [shard_padded[s], D/2] fp32
+ * at the shard's global key positions; shard_valid[s] in [0, shard_padded[s]] (host int
+ * arrays). 1 <= n_shards <= 64, at most 16 of them non-empty; shard_padded[s] a multiple of
+ * 128 (0 allowed for an empty shard, whose pointers are then not used). Numerics as dit_attn_fwd_ws (fp16 rotated q~, k~; bf16 P; fp32 accumulation); the
+ * partials are bf16, merged in fp32.
+ * workspace: at least dit_attn_sharded_workspace_bytes(...) bytes (same B, Sq, H, D and shard
+ * lengths), 256-byte aligned, caller-owned, contents on entry irrelevant; calls sharing one
+ * must not overlap. The chunk plan, and with it the workspace size, depends only on the
+ * arguments, not on the device.
+ * Errors: DIT_ERR_INVALID_ARG (null pointer, bad length or scale, workspace too small),
+ * DIT_ERR_UNSUPPORTED (D not 64/128, a length not a multiple of 128, more than 16 non-empty
+ * shards, sizes past 32-bit row indexing), DIT_ERR_ALIGNMENT, DIT_ERR_CUDA.
+ * ------------------------------------------------------------------------------------- */
+size_t dit_attn_sharded_workspace_bytes(int B, int Sq, int H, int D, int n_shards,
+                                        const int* shard_padded, const int* shard_valid);
+int dit_attn_fwd_sharded(const void* q, int B, int Sq, int H, int D, int q_valid_len,
+                         int n_shards, const void* const* k_shards, const void* const* v_shards,
+                         const int* shard_padded, const int* shard_valid, const float* cos_q,
+                         const float* sin_q, const float* const* cos_k, const float* const* sin_k,
+                         float softmax_scale, void* out, float* lse, void* workspace,
+                         size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------------------
  * LSE merge of partial results over key shards (mstar PR #376, attention over sharded keys):
  *   lse = ln sum_s exp(lse_s),  out = sum_s exp(lse_s - lse) * O_s.
  * A row whose n partial LSEs are all -inf (no shard saw a key) gets out = 0, lse = -inf.

@@ -259,3 +259,43 @@ def test_test_hook_library_is_separate_from_the_product():
     assert not hasattr(p, "dit_test_set_wait_hooks")
     hdr = open(os.path.join(ROOT, "include", "dit_attn_test_hooks.h")).read()
     assert "int dit_test_set_wait_hooks(unsigned long long wait_limit_ns, int skip_load);" in hdr
+
+
+def test_sharded_workspace_size_and_argument_checks(clib):
+    """The chunk plan (and so the workspace size) depends only on the arguments; invalid
+    shard descriptions give 0 / the documented statuses before any CUDA call."""
+    f = clib.dit_attn_sharded_workspace_bytes
+    f.restype = ctypes.c_size_t
+    ia = lambda v: (ctypes.c_int * len(v))(*v)
+    pad, val = [9472, 9472, 9472, 9472], [9472, 9472, 9472, 9384]
+    n = f(1, 1024, 32, 128, 4, ia(pad), ia(val))
+    rot = sum(1 * p * 32 * 128 * 2 for p in pad)
+    # the plan cuts the 4 shards into 8 chunks of 37 tiles (128 items each: ~6 per SM)
+    chunks = 8
+    assert n == rot + 256 + chunks * 1024 * 32 * 128 * 2 + chunks * 1024 * 32 * 4
+    assert f(1, 1024, 32, 128, 4, ia(pad), ia(val)) == n
+    assert f(1, 1024, 32, 96, 4, ia(pad), ia(val)) == 0          # D not supported
+    assert f(1, 1024, 32, 128, 0, ia(pad), ia(val)) == 0         # no shard
+    assert f(1, 1024, 32, 128, 1, ia([100]), ia([50])) == 0      # padded length not whole tiles
+    assert f(1, 1024, 32, 128, 1, ia([128]), ia([129])) == 0     # valid > padded
+    assert f(1, 1000, 32, 128, 1, ia([128]), ia([100])) == 0     # Sq not whole tiles
+    assert f(1, 1024, 32, 128, 17, ia([128] * 17), ia([1] * 17)) == 0   # more than 16 non-empty shards
+    assert f(1, 1024, 32, 128, 2, ia([0, 128]), ia([0, 100])) > 0        # an empty shard may have no rows
+    assert f(1, 1024, 32, 128, 1, ia([0]), ia([0])) > 0                  # no key at all: one empty chunk
+    g = clib.dit_attn_fwd_sharded
+    g.restype = ctypes.c_int
+    vp = ctypes.c_void_p
+    fake = vp(256)
+    ptrs = (vp * 1)(fake)
+    args = [fake, 1, 256, 2, 128, 200, 1, ptrs, ptrs, ia([256]), ia([200]), fake, fake, ptrs, ptrs,
+            ctypes.c_float(0.088), fake, fake, fake, ctypes.c_size_t(1 << 30), None]
+    a = list(args); a[0] = None
+    assert g(*a) == -1                       # null q
+    a = list(args); a[15] = ctypes.c_float(0.0)
+    assert g(*a) == -1                       # bad scale
+    a = list(args); a[19] = ctypes.c_size_t(16)
+    assert g(*a) == -1                       # workspace too small
+    a = list(args); a[4] = 96
+    assert g(*a) == -2                       # D
+    a = list(args); a[18] = vp(256 + 8)
+    assert g(*a) == -3                       # workspace not 256-byte aligned

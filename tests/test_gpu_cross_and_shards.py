@@ -30,6 +30,20 @@ def test_cross_small(lib, kv):
     compare(O, L, Or, Lr, case.q_valid)
 
 
+@pytest.mark.parametrize("D,kv", [(128, [300, 512]), (128, [129, 256]), (64, [511, 1]), (64, [385, 128])])
+def test_cross_many_tiles_per_cta(lib, D, kv):
+    """800 query tiles over the persistent grid (about five per CTA), so each CTA keeps a
+    head's keys resident over several tiles, crosses head boundaries inside its range, and,
+    for texts longer than 256 keys, alternates the order of the two key halves from tile to
+    tile. Full comparison with the oracle."""
+    case = AttnCase("crossmany", B=2, H=20, D=D, Sq=2560, Skv=512, q_valid=2500, kv_valid=kv, seed=74 + D)
+    q, k, v = make_qkv(case)
+    O, L = _run_cross(lib, case, q, k, v)
+    Or, Lr = attention(q, k, v, case.q_valid, kv, case.scale)
+    compare(O, L, Or, Lr, case.q_valid)
+    assert lib.dit_device_status() == 0
+
+
 def test_cross_pad_garbage_is_nan_safe(lib):
     case = AttnCase("crossnan", B=2, H=2, D=64, Sq=256, Skv=256, q_valid=256, kv_valid=[77, 200], seed=71)
     q, k, v = make_qkv(case)
@@ -143,6 +157,50 @@ def test_sharded_workload_full_size_sampled_rows(lib):
     compare(O, L, Or, Lr, case.q_valid, rows=rows, heads=heads)
     assert np.all(np.isfinite(L))
     assert lib.dit_device_status() == 0
+
+
+def _sharded_one_call(lib, case, q, shards):
+    """dit_attn_fwd_sharded: all shards in one launch (key chunks, RoPE at global positions),
+    then the merge."""
+    D = case.D
+    cq, sq = lib.dit_rope_table_1d(case.Sq, case.q_valid, D, case.theta, 0)
+    entries = []
+    for (k, v), off, nv, npad in zip(shards, case.offsets, case.shard_valid, case.shard_pad):
+        ck, sk = lib.dit_rope_table_1d(npad, nv, D, case.theta, off)
+        entries.append((dev_bf16(k), dev_bf16(v), nv, torch.from_numpy(ck).cuda(), torch.from_numpy(sk).cuda()))
+    ws = torch.full((lib.dit_attn_sharded_workspace_bytes(case.B, case.Sq, case.H, D, case.shard_pad,
+                                                          case.shard_valid),), 0x7F, dtype=torch.uint8, device="cuda")
+    out, lse = lib.dit_attn_fwd_sharded(dev_bf16(q), entries, case.q_valid, torch.from_numpy(cq).cuda(),
+                                        torch.from_numpy(sq).cuda(), workspace=ws)
+    torch.cuda.synchronize()
+    assert lib.dit_device_status() == 0
+    return out.float().cpu().numpy(), lse.cpu().numpy()
+
+
+@pytest.mark.parametrize("D,B,valid", [(128, 1, (300, 128, 1, 77)), (64, 2, (1000, 0, 513)),
+                                       (128, 2, (0, 0)), (128, 1, (2700,) * 5 + (129,))])
+def test_sharded_one_call_equals_unsharded(lib, D, B, valid):
+    """Shards of 1 key, of whole tiles, empty shards, all shards empty, and enough keys that
+    shards are cut into several chunks: the one-call result equals unsharded attention."""
+    case = ShardedCase("sh1", B=B, H=3, D=D, Sq=384, q_valid=333, shard_valid=valid, seed=75 + D + B)
+    q, shards = make_sharded(case)
+    O, L = _sharded_one_call(lib, case, q, shards)
+    if sum(valid) == 0:
+        assert np.all(O == 0) and np.all(L == -np.inf)
+        return
+    Or, Lr = _oracle_unsharded(case, q, shards, None, None)
+    compare(O, L, Or, Lr, case.q_valid)
+
+
+def test_sharded_one_call_workload_sampled_rows(lib):
+    case = sharded_case()
+    q, shards = make_sharded(case)
+    O, L = _sharded_one_call(lib, case, q, shards)
+    rows = sample_rows(case.q_valid, case.Sq, 40, seed=19)
+    heads = [0, 7, 31]
+    Or, Lr = _oracle_unsharded(case, q, shards, rows, heads)
+    compare(O, L, Or, Lr, case.q_valid, rows=rows, heads=heads)
+    assert np.all(np.isfinite(L))
 
 
 @pytest.mark.parametrize("D,rope", [(64, "1d"), (128, "1d"), (128, "3d")])

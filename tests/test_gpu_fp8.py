@@ -1,5 +1,15 @@
-"""GPU parity of the FP8 (e4m3) attention (dit_attn_fwd_fp8) against the fp64 oracle that takes
-the same steps (oracle.fp8.attention_fp8: same rotation, same per-tile / per-head scales, same
+"""GPU parity of the FP8 (e4m3) attention (dit_attn_fwd_fp8).
+
+Primary check, independent of how the kernel orders its steps: the GPU result against
+exact fp64 attention of the dequantised operands (the plain oracle on e4m3 codes times the
+documented per-tile / per-head scales), within a bound derived from the e4m3 format for
+the rounding of the probabilities and the fp32 arithmetic (oracle.fp8_bound); then, by the
+triangle inequality with that exactly computed operand effect, against exact attention of
+the unquantised inputs. Inputs already on the e4m3 grid with power-of-two scales pin the
+path to closed forms (q = 0 gives the mean of v and ln L; one key gives v_0 and its score).
+
+Diagnostic check: the fp64 program that takes the same steps as the kernel
+(oracle.fp8.attention_fp8: same rotation, same per-tile / per-head scales, same
 e4m3 rounding of q~, k~, v and of 112 p, same tiles and running maximum).
 
 Tolerances, derived from what can still differ between the two: the GPU rotates and divides
@@ -17,7 +27,8 @@ import torch
 
 from helpers import dev_bf16, gpu_tables_self, oracle_angles_self
 from oracle.attention import attention
-from oracle.fp8 import attention_fp8
+from oracle import fp8_bound as FB
+from oracle.fp8 import attention_fp8, e4m3_round
 from oracle.rope import rope_split_halves
 from video_dit_attention_gb300.inputs import AttnCase, make_qkv, sample_rows, wan480_case
 
@@ -66,18 +77,88 @@ CASES = [
 ]
 
 
+def _format_bound_check(case, q, k, v, O, L, rows, heads):
+    """|O - O_q| <= bound_O and |LSE - LSE_q| <= bound_LSE on the valid rows (O_q, LSE_q: exact
+    attention of the dequantised operands), hence |O - O_exact| <= |O_q - O_exact| + bound_O;
+    the format-only bound covers |O_q - O_exact|. Returns the largest errors seen."""
+    aq, ak = oracle_angles_self(case)
+    qr = q if aq is None else rope_split_halves(q, aq)
+    kr = k if ak is None else rope_split_halves(k, ak)
+    rows = np.asarray([r for r in rows if r < case.q_valid])
+    n_kv = int(case.kv_valid)
+    Oq, Lq = FB.exact_quantized(qr, kr, v, case.q_valid, n_kv, case.scale, rows=rows, heads=heads)
+    bO, bL = FB.p_rounding_bound(qr, kr, v, case.q_valid, n_kv, case.scale, rows, heads)
+    Og = O[:, rows][:, :, heads]
+    Lg = L[:, rows][:, :, heads]
+    eO, eL = np.abs(Og - Oq), np.abs(Lg - Lq)
+    assert np.all(eO <= bO), f"O off the dequantised-operand result by {np.max(eO - bO):.3e} beyond the bound"
+    assert np.all(eL <= bL), f"LSE off by {np.max(eL - bL):.3e} beyond the bound"
+    Oe, Le = attention(q, k, v, case.q_valid, n_kv, case.scale, aq, ak, rows=rows, heads=heads)
+    assert np.all(np.abs(Og - Oe) <= np.abs(Oq - Oe) + bO)
+    assert np.all(np.abs(Oq - Oe) <= FB.operand_bound(qr, kr, v, case.q_valid, n_kv, case.scale, rows, heads))
+    return float(np.max(eO)), float(np.max(eL)), float(np.max(np.abs(Og - Oe)))
+
+
 @pytest.mark.parametrize("case", CASES, ids=lambda c: c.name)
-def test_fp8_matches_the_fp8_oracle(lib, case):
+def test_fp8_within_the_format_bound_of_exact_attention(lib, case):
+    q, k, v = make_qkv(case)
+    O, L = _run(lib, case, q, k, v)
+    n = case.q_valid
+    assert np.all(O[:, n:] == 0) and np.all(L[:, n:] == -np.inf)
+    rows = sample_rows(case.q_valid, case.Sq, 40, seed=3)
+    _format_bound_check(case, q, k, v, O, L, rows, list(range(case.H)))
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: c.name)
+def test_fp8_matches_the_same_steps_oracle(lib, case):
+    """Diagnostic: the fp64 program that takes the kernel's steps."""
     q, k, v = make_qkv(case)
     O, L = _run(lib, case, q, k, v)
     Or, Lr = _oracle(case, q, k, v)
     _compare(O, L, Or, Lr, case.q_valid)
-    # and it stays within the format's distance of exact attention
-    aq, ak = oracle_angles_self(case)
-    Oe, Le = attention(q, k, v, case.q_valid, case.kv_valid, case.scale, aq, ak)
-    n = case.q_valid
-    assert np.max(np.abs(O[:, :n] - Oe[:, :n])) <= 0.1
-    assert np.max(np.abs(L[:, :n] - Le[:, :n])) <= 0.1
+
+
+def _grid_values(rng, shape, amax_pow2):
+    """e4m3 values times 2^e (e = amax_pow2), with one element of magnitude 448 * 2^e in
+    every 128-row tile of every head: each scale amax / 448 is then 2^e, a power of two, and
+    quantising moves nothing. Such values are exact in bf16."""
+    x = e4m3_round(rng.standard_normal(shape) * 60.0)
+    x[:, ::128, :, 0] = 448.0
+    return x * 2.0 ** amax_pow2
+
+
+def test_fp8_on_grid_inputs_closed_forms(lib):
+    """Inputs whose quantisation is exact (no RoPE): q = 0 gives O = mean of the valid v and
+    LSE = ln L; a single key gives O = v_0 exactly and LSE = its score; and in general the
+    result is within the P-rounding bound of exact attention itself."""
+    rng = np.random.Generator(np.random.PCG64(171))
+    B, H, D, S = 1, 2, 128, 384
+    k = _grid_values(rng, (B, S, H, D), -7)
+    v = _grid_values(rng, (B, S, H, D), -7)
+    # q = 0: uniform weights
+    case = AttnCase("fp8-grid-q0", B=B, H=H, D=D, Sq=S, Skv=S, q_valid=300, kv_valid=333, rope=None)
+    q0 = np.zeros((B, S, H, D))
+    O, L = _run(lib, case, q0, k, v)
+    mean = v[:, :333].mean(axis=1)                      # [B, H, D]
+    assert np.max(np.abs(O[:, :300] - mean[:, None])) <= 2.0 ** -8 * np.max(np.abs(mean)) + 1e-6
+    assert np.max(np.abs(L[:, :300] - math.log(333))) <= 1e-5
+    # one key: O = v_0 exactly (an e4m3 value times a power of two is exact in bf16)
+    q = _grid_values(rng, (B, S, H, D), -7)
+    case1 = AttnCase("fp8-grid-l1", B=B, H=H, D=D, Sq=S, Skv=S, q_valid=S, kv_valid=1, rope=None)
+    O, L = _run(lib, case1, q, k, v)
+    assert np.array_equal(O[0, :, 0], np.broadcast_to(v[0, 0, 0], (S, D)))
+    assert np.array_equal(O[0, :, 1], np.broadcast_to(v[0, 0, 1], (S, D)))
+    s0 = np.einsum("bshd,bhd->bsh", q, k[:, 0]) * case1.scale
+    assert np.max(np.abs(L - s0)) <= 1e-5 * (1.0 + np.max(np.abs(s0)))
+    # general: exact attention of the unquantised inputs, within the P-rounding bound
+    case2 = AttnCase("fp8-grid", B=B, H=H, D=D, Sq=S, Skv=S, q_valid=S, kv_valid=S, rope=None)
+    O, L = _run(lib, case2, q, k, v)
+    rows = sample_rows(S, S, 40, seed=4)
+    Oe, Le = attention(q, k, v, S, S, case2.scale, rows=rows, heads=[0, 1])
+    Oq, Lq = FB.exact_quantized(q, k, v, S, S, case2.scale, rows=rows, heads=[0, 1])
+    assert np.array_equal(Oq, Oe) and np.array_equal(Lq, Le)   # the quantisation is exact here
+    bO, bL = FB.p_rounding_bound(q, k, v, S, S, case2.scale, rows, [0, 1])
+    assert np.all(np.abs(O[:, rows] - Oe) <= bO) and np.all(np.abs(L[:, rows] - Le) <= bL)
 
 
 def test_fp8_pad_contents_do_not_reach_valid_rows(lib):
@@ -101,6 +182,7 @@ def test_fp8_wan480_sampled(lib):
     O, L = _run(lib, case, q, k, v)
     rows = sample_rows(case.q_valid, case.Sq, 16, seed=51)
     heads = [7, 33]
+    _format_bound_check(case, q, k, v, O, L, rows, heads)
     Or, Lr = _oracle(case, q, k, v, rows=rows, heads=heads)
     _compare(O, L, Or, Lr, case.q_valid, rows=rows, heads=heads)
     assert np.all(O[:, case.q_valid:] == 0) and np.all(L[:, case.q_valid:] == -np.inf)

@@ -278,7 +278,75 @@ extern "C" int dit_cross_attn_shortkv(const void* q, const void* k, const void* 
   AttnArgs a{q, k, v, B, Sq, Skv, H, D, q_valid_len, Skv, kv_valid_len_dev,
              nullptr, nullptr, nullptr, nullptr, softmax_scale, out, lse, nullptr, nullptr, nullptr,
              0.f, static_cast<cudaStream_t>(stream)};
-  return cuda_status(launch_attn_fwd(a, kModeCross));
+  return cuda_status(launch_cross_attn(a));
+}
+
+namespace {
+// Shared checks and the plan of the sharded entry points.
+int sharded_setup(int B, int Sq, int H, int D, int n_shards, const void* const* k_shards,
+                  const void* const* v_shards, const int* shard_padded, const int* shard_valid,
+                  const float* const* cos_k, const float* const* sin_k, bool need_ptrs, KeyShard* ks,
+                  ShardPlan* plan) {
+  if (B < 1 || Sq < 1 || H < 1 || n_shards < 1 || n_shards > 64 || !shard_padded || !shard_valid)
+    return DIT_ERR_INVALID_ARG;
+  if (D != 64 && D != 128) return DIT_ERR_UNSUPPORTED;
+  if ((Sq % 128) != 0 || H > 65535 || B > 65535) return DIT_ERR_UNSUPPORTED;
+  if (need_ptrs && (!k_shards || !v_shards || !cos_k || !sin_k)) return DIT_ERR_INVALID_ARG;
+  for (int s = 0; s < n_shards; ++s) {
+    // an empty shard may have no rows at all (padded length 0); it is never read
+    if (shard_padded[s] < 0 || (shard_padded[s] % 128) != 0) return DIT_ERR_UNSUPPORTED;
+    if (shard_valid[s] < 0 || shard_valid[s] > shard_padded[s]) return DIT_ERR_INVALID_ARG;
+    if (static_cast<long long>(shard_padded[s]) * H * (D / 16) >= (1ll << 30)) return DIT_ERR_UNSUPPORTED;
+    ks[s].S_pad = shard_padded[s];
+    ks[s].valid = shard_valid[s];
+    if (need_ptrs && shard_padded[s] > 0) {
+      if (!k_shards[s] || !v_shards[s] || !cos_k[s] || !sin_k[s]) return DIT_ERR_INVALID_ARG;
+      if (!aligned(k_shards[s], 16) || !aligned(v_shards[s], 16) || !aligned(cos_k[s], 16) || !aligned(sin_k[s], 16))
+        return DIT_ERR_ALIGNMENT;
+      ks[s].k = k_shards[s];
+      ks[s].v = v_shards[s];
+      ks[s].cos_k = cos_k[s];
+      ks[s].sin_k = sin_k[s];
+    }
+  }
+  if (static_cast<long long>(Sq) * H * (D / 16) >= (1ll << 30)) return DIT_ERR_UNSUPPORTED;
+  if (!plan_shards(B, Sq, H, D, n_shards, ks, 0, plan)) return DIT_ERR_UNSUPPORTED;
+  return DIT_OK;
+}
+}  // namespace
+
+extern "C" size_t dit_attn_sharded_workspace_bytes(int B, int Sq, int H, int D, int n_shards,
+                                                   const int* shard_padded, const int* shard_valid) {
+  KeyShard ks[64] = {};
+  ShardPlan plan;
+  if (sharded_setup(B, Sq, H, D, n_shards, nullptr, nullptr, shard_padded, shard_valid, nullptr, nullptr, false,
+                    ks, &plan) != DIT_OK)
+    return 0;
+  return plan.total;
+}
+
+extern "C" int dit_attn_fwd_sharded(const void* q, int B, int Sq, int H, int D, int q_valid_len,
+                                    int n_shards, const void* const* k_shards, const void* const* v_shards,
+                                    const int* shard_padded, const int* shard_valid, const float* cos_q,
+                                    const float* sin_q, const float* const* cos_k,
+                                    const float* const* sin_k, float softmax_scale, void* out, float* lse,
+                                    void* workspace, size_t workspace_bytes, void* stream) {
+  if (!q || !out || !lse || !cos_q || !sin_q || !workspace) return DIT_ERR_INVALID_ARG;
+  if (!(softmax_scale > 0.f) || !std::isfinite(softmax_scale)) return DIT_ERR_INVALID_ARG;
+  if (q_valid_len < 0 || q_valid_len > Sq) return DIT_ERR_INVALID_ARG;
+  KeyShard ks[64] = {};
+  ShardPlan plan;
+  const int st = sharded_setup(B, Sq, H, D, n_shards, k_shards, v_shards, shard_padded, shard_valid, cos_k,
+                               sin_k, true, ks, &plan);
+  if (st != DIT_OK) return st;
+  if (workspace_bytes < plan.total) return DIT_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(lse, 4) || !aligned(cos_q, 16) || !aligned(sin_q, 16) ||
+      !aligned(workspace, 256))
+    return DIT_ERR_ALIGNMENT;
+  AttnArgs a{q, nullptr, nullptr, B, Sq, 0, H, D, q_valid_len, 0, nullptr,
+             cos_q, sin_q, nullptr, nullptr, softmax_scale, out, lse, workspace, nullptr, nullptr, 0.f,
+             static_cast<cudaStream_t>(stream), nullptr};
+  return cuda_status(launch_attn_sharded(a, n_shards, ks, plan));
 }
 
 extern "C" int dit_attn_lse_merge(const void* partial_o, const float* partial_lse, int n, int B,

@@ -45,6 +45,10 @@
 
 #include <cuda_bf16.h>
 
+#include <cstring>
+#include <mutex>
+#include <type_traits>
+
 #include "common.h"
 #include "exp2_fma.cuh"
 #include "ptx.cuh"
@@ -101,6 +105,8 @@ struct KParams {
   int Sq, Skv, H;
   int n_pairs, n_items;   // query-tile pairs per (b, h); B * H * n_pairs work items
   int q_valid, kv_valid;
+  int n_bh;                          // sharded mode: B * H
+  int chunk_valid[kMaxKeyChunks];    // sharded mode: valid keys of each key chunk
   const int32_t* kv_valid_dev;
   const float* cos_q;
   const float* sin_q;
@@ -131,10 +137,33 @@ struct WsParams {
   int f8_nt_q;
 };
 
-// The RoPE workspace modes (plain, with the q/k RMSNorm, fixed-m softmax).
+// The RoPE workspace modes (plain, with the q/k RMSNorm, fixed-m softmax, sharded keys).
 __host__ __device__ constexpr bool is_ws_mode(int mode) {
-  return mode == kModeRopeWs || mode == kModeRopeWsNorm || mode == kModeRopeWsFixedM;
+  return mode == kModeRopeWs || mode == kModeRopeWsNorm || mode == kModeRopeWsFixedM ||
+         mode == kModeRopeWsSharded;
 }
+
+// Sharded-keys mode: the keys come in chunks (whole 128-row tiles of one shard each). Chunk c
+// has its own raw k rows, rotated copy, table rows, and TMA maps of the rotated k and of v,
+// and its own partial output (O_c, LSE_c), merged afterwards through the LSE.
+struct KeyChunk {
+  const uint16_t* k_raw;   // first row of the chunk in its shard's raw k [B, S_rows, H, D]
+  uint16_t* k_rot;         // the same row in the shard's rotated copy (same layout)
+  const float* cos_k;      // table rows of the chunk (global key positions)
+  const float* sin_k;
+  int S_rows;              // rows per batch of the shard (its padded length)
+  int valid;               // valid keys in the chunk
+};
+struct ShardParams {
+  CUtensorMap km[kMaxKeyChunks];   // rotated k of each chunk, extent = its valid rows
+  CUtensorMap vm[kMaxKeyChunks];   // v of each chunk, extent = its valid rows
+  KeyChunk c[kMaxKeyChunks];
+  int n_chunks;
+  long long po_stride, pl_stride;  // elements between consecutive chunks' partial O / LSE
+};
+struct NoShards {};
+template <int kMode>
+using ShardArg = typename std::conditional<kMode == kModeRopeWsSharded, ShardParams, NoShards>::type;
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;
@@ -240,20 +269,21 @@ __device__ __forceinline__ void zero_rows(uint32_t tile, int first_row, int at) 
 // O = 0, LSE = -inf for the 128 rows of the query tile starting at q_first (a tile that is
 // all pad rows, or a problem with no keys). `tid` ranges over `nthr` cooperating threads.
 template <int D>
-__device__ __forceinline__ void write_empty_tile(const KParams& p, int b, int h, int q_first,
-                                                 int tid, int nthr) {
+__device__ __forceinline__ void write_empty_tile(const KParams& p, uint16_t* out, float* lse, int b, int h,
+                                                 int q_first, int tid, int nthr) {
   for (int i = tid; i < 128 * (D / 8); i += nthr) {
     const int row = i / (D / 8), ch = i % (D / 8);
-    uint16_t* dst = p.out + ((static_cast<size_t>(b) * p.Sq + q_first + row) * p.H + h) * D + ch * 8;
+    uint16_t* dst = out + ((static_cast<size_t>(b) * p.Sq + q_first + row) * p.H + h) * D + ch * 8;
     *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
   }
   for (int r = tid; r < 128; r += nthr)
-    p.lse[(static_cast<size_t>(b) * p.Sq + q_first + r) * p.H + h] = -INFINITY;
+    lse[(static_cast<size_t>(b) * p.Sq + q_first + r) * p.H + h] = -INFINITY;
 }
 
 // One unit of work: query rows q0 .. q0 + 255 (two 128-row tiles) of one (b, h).
 struct Item {
   int b, h, q0, n_live, n_kv, kv_valid;
+  int chunk;      // sharded mode: key chunk of the item
   bool has1;      // tile 1 (rows q0 + 128 ..) lies inside the padded sequence
   bool bad_len;   // cross-attention: the batch's device-side key length is outside [0, Skv]
 };
@@ -261,11 +291,19 @@ struct Item {
 template <int kMode>
 __device__ __forceinline__ Item decode_item(const KParams& p, int it) {
   Item w;
-  const int pair = it % p.n_pairs, bh = it / p.n_pairs;
+  const int pair = it % p.n_pairs;
+  int bh = it / p.n_pairs;
+  w.chunk = 0;
+  int kv = p.kv_valid;
+  if (kMode == kModeRopeWsSharded) {
+    // items in the order (chunk, b, h, query-tile pair): neighbouring CTAs share a chunk's K/V
+    w.chunk = bh / p.n_bh;
+    bh -= w.chunk * p.n_bh;
+    kv = p.chunk_valid[w.chunk];
+  }
   w.h = bh % p.H;
   w.b = bh / p.H;
   w.q0 = pair * 256;
-  int kv = p.kv_valid;
   w.bad_len = false;
   if (kMode == kModeCross) {
     // Fail closed: a length outside [0, Skv] is not clamped into range. The batch is treated
@@ -704,7 +742,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int it = it0; ok && it < p.n_items; it += it_step) {
       const Item w = decode_item<kMode>(p, it);
       if (t >= w.n_live) {
-        if (t == 0 || w.has1) write_empty_tile<D>(p, w.b, w.h, w.q0 + 128 * t, r, 128);
+        if (t == 0 || w.has1) write_empty_tile<D>(p, p.out, p.lse, w.b, w.h, w.q0 + 128 * t, r, 128);
         continue;
       }
       const int n_kv = w.n_kv, kv_valid = w.kv_valid;
@@ -1119,20 +1157,173 @@ cudaError_t launch_mode(const AttnArgs& a) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
     if (!is_ws_mode(kMode)) {
-      kern<<<grid, kThreads, kSmem, a.stream>>>(mq, mk, mv, p, ws);
+      kern<<<grid, kThreads, kSmem, a.stream>>>(mq, mk, mv, p, ws, NoShards{});
       return cudaGetLastError();
     }
     // CTAs wait for rotated rows that other CTAs produce: launch cooperatively so that every
     // CTA is resident, after zeroing the counter on the same stream.
     e = cudaMemsetAsync(ws.rotated, 0, zero_bytes, a.stream);
     if (e != cudaSuccess) return e;
-    void* args[] = {&mq, &mk, &mv, &p, &ws};
+    NoShards ns{};
+    void* args[] = {&mq, &mk, &mv, &p, &ws, &ns};
     return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kern), dim3(grid), dim3(kThreads),
                                        args, kSmem, a.stream);
   }
 }
 
+// Sharded keys in one cooperative launch: every CTA rotates its share of all chunks' k rows
+// (the grid counter gates the loads of rotated rows, as in the workspace mode), then the work
+// items (chunk, b, h, query-tile pair) run with the chunk's maps and write its partial.
+template <int D>
+cudaError_t launch_sharded_mode(const AttnArgs& a, const KeyShard* shards, const ShardPlan& plan) {
+  constexpr int kMode = kModeRopeWsSharded;
+  CUtensorMap mq;
+  const int qext = a.q_valid > 0 ? a.q_valid : 1;
+  if (!encode_bshd_map(&mq, a.q, a.B, qext, a.Sq, a.H, D)) return cudaErrorInvalidValue;
+  char* wsb = static_cast<char*>(a.workspace);
+  ShardParams sh;
+  std::memset(&sh, 0, sizeof(sh));
+  sh.n_chunks = plan.n_chunks;
+  sh.po_stride = static_cast<long long>(a.B) * a.Sq * a.H * D;
+  sh.pl_stride = static_cast<long long>(a.B) * a.Sq * a.H;
+  KParams p;
+  std::memset(&p, 0, sizeof(p));
+  const size_t row_bytes = static_cast<size_t>(a.H) * D * 2;
+  for (int c = 0; c < plan.n_chunks; ++c) {
+    const KeyShard& ks = shards[plan.shard[c]];
+    const size_t r0 = static_cast<size_t>(plan.row0[c]);
+    KeyChunk& kc = sh.c[c];
+    kc.k_raw = reinterpret_cast<const uint16_t*>(static_cast<const char*>(ks.k) + r0 * row_bytes);
+    kc.k_rot = reinterpret_cast<uint16_t*>(wsb + plan.rot_off[c] + r0 * row_bytes);
+    kc.cos_k = ks.cos_k + r0 * (D / 2);
+    kc.sin_k = ks.sin_k + r0 * (D / 2);
+    kc.S_rows = ks.S_pad;
+    kc.valid = plan.valid[c];
+    // An empty chunk (every shard empty) is never read: its maps only need to be valid, so
+    // they point at the workspace with one row per batch.
+    const bool empty = plan.valid[c] == 0;
+    const int ext = empty ? 1 : plan.valid[c];
+    const int rows = empty ? 1 : ks.S_pad;
+    const void* vbase = empty ? static_cast<const void*>(kc.k_rot) : static_cast<const char*>(ks.v) + r0 * row_bytes;
+    if (!encode_bshd_map(&sh.km[c], kc.k_rot, a.B, ext, rows, a.H, D) ||
+        !encode_bshd_map(&sh.vm[c], vbase, a.B, ext, rows, a.H, D))
+      return cudaErrorInvalidValue;
+    p.chunk_valid[c] = plan.valid[c];
+  }
+  p.Sq = a.Sq;
+  p.Skv = 0;
+  p.H = a.H;
+  p.n_pairs = (a.Sq + 255) / 256;
+  p.n_bh = a.B * a.H;
+  const long long n_items = static_cast<long long>(plan.n_chunks) * a.B * a.H * p.n_pairs;
+  if (n_items >= (1ll << 31)) return cudaErrorInvalidValue;
+  p.n_items = static_cast<int>(n_items);
+  p.q_valid = a.q_valid;
+  p.kv_valid = 0;
+  p.kv_valid_dev = nullptr;
+  p.cos_q = a.cos_q;
+  p.sin_q = a.sin_q;
+  p.cos_k = p.sin_k = nullptr;
+  p.scale_log2 = a.scale * kLog2e;
+  p.out = reinterpret_cast<uint16_t*>(wsb + plan.po_off);
+  p.lse = reinterpret_cast<float*>(wsb + plan.pl_off);
+  WsParams ws;
+  std::memset(&ws, 0, sizeof(ws));
+  ws.rotated = reinterpret_cast<unsigned int*>(wsb + plan.counter_off);
+  ws.B = a.B;
+  int dev = 0, sm_count = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sm_count, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return e;
+  if (sm_count < 1) return cudaErrorInvalidDevice;
+  const int grid = p.n_items < sm_count ? p.n_items : sm_count;
+  auto kern = attn_sp_kernel<D, kMode>;
+  constexpr int kSmem = CfgSp<D, false>::kSmemBytes;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  if (e != cudaSuccess) return e;
+  e = cudaMemsetAsync(ws.rotated, 0, sizeof(unsigned int), a.stream);
+  if (e != cudaSuccess) return e;
+  // the first map arguments are unused in this mode (each chunk has its own)
+  void* args[] = {&mq, &mq, &mq, &p, &ws, &sh};
+  return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kern), dim3(grid), dim3(kThreads), args,
+                                     kSmem, a.stream);
+}
+
 }  // namespace
+
+bool plan_shards(int B, int Sq, int H, int D, int n_shards, const KeyShard* shards, int sm_count,
+                 ShardPlan* plan) {
+  std::memset(plan, 0, sizeof(*plan));
+  // Rotated k of every shard in the workspace, one after another (each 256-byte aligned).
+  size_t off = 0, shard_off[64] = {};
+  if (n_shards < 1 || n_shards > 64) return false;
+  for (int s = 0; s < n_shards; ++s) {
+    shard_off[s] = off;
+    off += (static_cast<size_t>(B) * shards[s].S_pad * H * D * 2 + 255) / 256 * 256;
+  }
+  // Key tiles per shard, and a chunk length (in tiles) that gives at least about six work
+  // items per SM: items per chunk = B * H * query-tile pairs.
+  const long long items_per_chunk = static_cast<long long>(B) * H * ((Sq + 255) / 256);
+  (void)sm_count;   // the plan uses a fixed target so that workspace sizes do not depend on the device
+  long long total_tiles = 0;
+  int nonempty = 0;
+  for (int s = 0; s < n_shards; ++s)
+    if (shards[s].valid > 0) {
+      total_tiles += (shards[s].valid + 127) / 128;
+      ++nonempty;
+    }
+  if (nonempty > kMaxKeyChunks) return false;
+  long long want = (kShardTargetItems + items_per_chunk - 1) / items_per_chunk;   // chunks wanted
+  if (want < nonempty) want = nonempty;
+  if (want > kMaxKeyChunks) want = kMaxKeyChunks;
+  long long chunk_tiles = total_tiles > 0 ? (total_tiles + want - 1) / want : 1;
+  if (chunk_tiles < 1) chunk_tiles = 1;
+  for (;; ++chunk_tiles) {   // grow the chunks until they fit in kMaxKeyChunks
+    int n = 0;
+    for (int s = 0; s < n_shards; ++s)
+      if (shards[s].valid > 0) n += static_cast<int>(((shards[s].valid + 127) / 128 + chunk_tiles - 1) / chunk_tiles);
+    if (n <= kMaxKeyChunks) break;
+  }
+  int n = 0;
+  for (int s = 0; s < n_shards; ++s) {
+    if (shards[s].valid <= 0) continue;
+    const int tiles = (shards[s].valid + 127) / 128;
+    const int parts = static_cast<int>((tiles + chunk_tiles - 1) / chunk_tiles);
+    int t0 = 0;
+    for (int k = 0; k < parts; ++k) {
+      const int nt = tiles / parts + (k < tiles % parts ? 1 : 0);   // near-equal parts
+      plan->shard[n] = s;
+      plan->row0[n] = t0 * 128;
+      const int end = (t0 + nt) * 128 < shards[s].valid ? (t0 + nt) * 128 : shards[s].valid;
+      plan->valid[n] = end - t0 * 128;
+      plan->rot_off[n] = shard_off[s];
+      t0 += nt;
+      ++n;
+    }
+  }
+  if (n == 0) {   // no key at all: one empty chunk, whose items write O = 0, LSE = -inf
+    plan->shard[0] = 0;
+    plan->valid[0] = 0;
+    plan->rot_off[0] = shard_off[0];
+    n = 1;
+  }
+  plan->n_chunks = n;
+  plan->counter_off = off;
+  plan->po_off = off + 256;
+  const size_t po = (static_cast<size_t>(n) * B * Sq * H * D * 2 + 255) / 256 * 256;
+  plan->pl_off = plan->po_off + po;
+  plan->total = plan->pl_off + (static_cast<size_t>(n) * B * Sq * H * 4 + 255) / 256 * 256;
+  return true;
+}
+
+cudaError_t launch_attn_sharded(const AttnArgs& a, int n_shards, const KeyShard* shards, const ShardPlan& plan) {
+  (void)n_shards;
+  cudaError_t e = a.D == 128 ? launch_sharded_mode<128>(a, shards, plan) : launch_sharded_mode<64>(a, shards, plan);
+  if (e != cudaSuccess) return e;
+  char* wsb = static_cast<char*>(a.workspace);
+  return launch_lse_merge(wsb + plan.po_off, reinterpret_cast<const float*>(wsb + plan.pl_off), plan.n_chunks, a.B,
+                          a.Sq, a.H, a.D, a.out, a.lse, a.stream);
+}
 
 size_t attn_workspace_bytes(int B, int Sq, int Skv, int H, int D) {
   (void)Sq;   // q is rotated in shared memory, tile by tile
@@ -1163,6 +1354,26 @@ cudaError_t launch_attn_fwd(const AttnArgs& a, AttnMode mode) {
   if (mode == kModeRope) return launch_mode<64, kModeRope>(a);
   if (mode == kModeCross) return launch_mode<64, kModeCross>(a);
   return launch_mode<64, kModePlain>(a);
+}
+
+cudaError_t device_status_ptr(unsigned int** out) {
+  // Device address of this device's status word, looked up once per device (kernels in other
+  // translation units receive it as a parameter).
+  static std::mutex mu;
+  static unsigned int* ptrs[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_dit_status);
+    if (e != cudaSuccess) return e;
+    ptrs[dev] = static_cast<unsigned int*>(p);
+  }
+  *out = ptrs[dev];
+  return cudaSuccess;
 }
 
 cudaError_t read_device_status(unsigned int* out, bool clear) {

@@ -82,12 +82,14 @@ __device__ __forceinline__ int ring_load_v(int g, int G) { return g == G - 1 ? 2
 template <int D, int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_sp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                   const __grid_constant__ CUtensorMap tm_v, const KParams p, const WsParams ws) {
+                   const __grid_constant__ CUtensorMap tm_v, const KParams p, const WsParams ws,
+                   const __grid_constant__ ShardArg<kMode> sh) {
   static_assert(kMode == kModePlain || kMode == kModeCross || kMode == kModeFp8 || is_ws_mode(kMode), "mode");
   constexpr bool kFp8 = kMode == kModeFp8;
   static_assert(!kFp8 || D == 128, "the FP8 path is built for D = 128");
   constexpr bool kWs = is_ws_mode(kMode), kNorm = kMode == kModeRopeWsNorm;
   constexpr bool kFixedM = kMode == kModeRopeWsFixedM;
+  constexpr bool kShard = kMode == kModeRopeWsSharded;
   using C = CfgSp<D, kFp8>;
   constexpr int R = C::kRing;
   extern __shared__ uint8_t smem_raw[];
@@ -141,6 +143,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after_sync();
   const uint32_t tbase = bars->tmem_base;
   const int it0 = blockIdx.x, it_step = gridDim.x;
+  // TMA maps of an item's keys and values (per key chunk in the sharded mode).
+  auto kmap = [&](const Item& w) -> const CUtensorMap* {
+    if constexpr (kShard) return &sh.km[w.chunk];
+    else return &tm_k;
+  };
+  auto vmap = [&](const Item& w) -> const CUtensorMap* {
+    if constexpr (kShard) return &sh.vm[w.chunk];
+    else return &tm_v;
+  };
   // First item at or after `it` (in this CTA's sequence) that has work.
   auto first_live = [&](int it) -> int {
     while (it < p.n_items && decode_item<kMode>(p, it).n_live == 0) it += it_step;
@@ -203,7 +214,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       else if (kFixedM)
         rotate_rows_fp16_kmax<D>(ws.k_raw, ws.k_rot, p.cos_k, p.sin_k, ws.B, p.Skv, p.kv_valid, p.H,
                                  blockIdx.x * kRotK + tid, gridDim.x * kRotK, kmax_s);
-      else
+      else if constexpr (kShard) {
+        for (int c = 0; c < sh.n_chunks; ++c)
+          rotate_rows_fp16<D>(sh.c[c].k_raw, sh.c[c].k_rot, sh.c[c].cos_k, sh.c[c].sin_k, ws.B, sh.c[c].S_rows,
+                              sh.c[c].valid, p.H, blockIdx.x * kRotK + tid, gridDim.x * kRotK);
+      } else
         rotate_rows_fp16<D>(ws.k_raw, ws.k_rot, p.cos_k, p.sin_k, ws.B, p.Skv, p.kv_valid, p.H,
                             blockIdx.x * kRotK + tid, gridDim.x * kRotK);
       fence_proxy_async_all();
@@ -463,15 +478,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int jj = 0; jj < nw.n_kv && jj < kPrefetchKV; ++jj)
 #pragma unroll
               for (int c = 0; c < C::kSub; ++c) {
-                tma_prefetch_l2_4d(&tm_k, c * 64, nw.h, jj * 128, nw.b);
+                tma_prefetch_l2_4d(kmap(nw), c * 64, nw.h, jj * 128, nw.b);
                 if (kFp8)
                   tma_prefetch_l2_4d(&tm_v, jj * 128, 0, nw.h, nw.b);
                 else
-                  tma_prefetch_l2_4d(&tm_v, c * 64, nw.h, jj * 128, nw.b);
+                  tma_prefetch_l2_4d(vmap(nw), c * 64, nw.h, jj * 128, nw.b);
               }
           }
         }
-        if (!wait_rotated(k_ready) || !load(&tm_k, kw, kj)) return false;
+        if (!wait_rotated(k_ready) || !load(kmap(kw), kw, kj)) return false;
         if (++kj == kw.n_kv) {
           kj = 0;
           kit = first_live(kit + it_step);
@@ -480,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       };
       auto load_next_v = [&]() -> bool {
-        if (!load(&tm_v, vw, vj)) return false;
+        if (!load(vmap(vw), vw, vj)) return false;
         if (++vj == vw.n_kv) {
           vj = 0;
           vit = first_live(vit + it_step);
@@ -556,8 +571,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int it = it0; ok && it < p.n_items; it += it_step) {
       const Item w = decode_item<kMode>(p, it);
+      // this item's output: the partial (O, LSE) of its key chunk in the sharded mode
+      uint16_t* out_b = p.out;
+      float* lse_b = p.lse;
+      if constexpr (kShard) {
+        out_b += w.chunk * sh.po_stride;
+        lse_b += w.chunk * sh.pl_stride;
+      }
       if (t >= w.n_live) {
-        if (t == 0 || w.has1) write_empty_tile<D>(p, w.b, w.h, w.q0 + 128 * t, r, 128);
+        if (t == 0 || w.has1) write_empty_tile<D>(p, out_b, lse_b, w.b, w.h, w.q0 + 128 * t, r, 128);
         if (kMode == kModeCross && w.bad_len && t == 0 && r == 0) atomicOr(status, kStatusBadKvLength);
         if (w.n_live > 0) {
           if (!(ok = rotate_next(it))) break;
@@ -743,12 +765,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int rr = r0 + i * kRPI + lr;
           const uint32_t src = (kFp8 ? sO + t * C::kOBytes : sP + t * C::kPBytes) + chunk + static_cast<uint32_t>(rr) * 128u +
                                ((unit ^ static_cast<uint32_t>(rr & 7)) << 4);
-          uint16_t* dst = p.out + ((static_cast<size_t>(w.b) * p.Sq + w.q0 + 128 * t + rr) * p.H + w.h) * D;
+          uint16_t* dst = out_b + ((static_cast<size_t>(w.b) * p.Sq + w.q0 + 128 * t + rr) * p.H + w.h) * D;
           *reinterpret_cast<uint4*>(dst + lu * 8) = lds128(src);
         }
       }
       __syncwarp();
-      p.lse[(static_cast<size_t>(w.b) * p.Sq + qrow) * p.H + w.h] =
+      lse_b[(static_cast<size_t>(w.b) * p.Sq + qrow) * p.H + w.h] =
           valid_row ? (m_used + log2f(l)) * kLn2 : -INFINITY;
       ++qi;
     }

@@ -42,7 +42,39 @@ enum AttnMode : int {
                           // running maximum (fixed-m softmax)
   kModeFp8 = 6,           // e4m3 q~, k~ (rotated) and v (transposed) prepared in the workspace;
                           // e4m3 tensor-core products, exact running maximum
+  kModeRopeWsSharded = 7, // as kModeRopeWs over several key chunks in one launch, one partial
+                          // (O, LSE) per chunk
 };
+
+// Sharded keys: at most this many key chunks per launch (the partials are merged through
+// their LSEs afterwards).
+constexpr int kMaxKeyChunks = 16;
+// One key shard as the caller hands it in: raw k and v [B, S_pad, H, D] bf16, its RoPE tables
+// [S_pad, D/2] at the shard's global key positions, its padded and valid lengths.
+struct KeyShard {
+  const void* k;
+  const void* v;
+  const float* cos_k;
+  const float* sin_k;
+  int S_pad, valid;
+};
+// How the shards are cut into key chunks of whole 128-row tiles, and where the workspace puts
+// the rotated k of each shard, the CTA counter and the partial outputs.
+struct ShardPlan {
+  int n_chunks;
+  int shard[kMaxKeyChunks], row0[kMaxKeyChunks], valid[kMaxKeyChunks];
+  size_t rot_off[kMaxKeyChunks];   // byte offset of each chunk's shard's rotated copy
+  size_t counter_off, po_off, pl_off, total;
+};
+// Cuts the shards into chunks of near-equal length so that there are about kShardTargetItems
+// work items (six per SM of a 152-SM GB300; a fixed number, so that the plan and the workspace
+// size do not depend on the device); returns false if the shards cannot be planned (more than
+// kMaxKeyChunks non-empty shards, or more than 64 shards).
+constexpr long long kShardTargetItems = 6 * 152;
+bool plan_shards(int B, int Sq, int H, int D, int n_shards, const KeyShard* shards, int sm_count,
+                 ShardPlan* plan);
+cudaError_t launch_attn_sharded(const AttnArgs& a, int n_shards, const KeyShard* shards,
+                                const ShardPlan& plan);
 
 // Workspace layout of the RoPE workspace modes: rotated k [B, Skv, H, D] fp16, then a
 // 256-byte block holding the count of CTAs done rotating; both 256-byte aligned.
@@ -83,6 +115,12 @@ cudaError_t launch_copy_rows(const void* src, void* dst, int B, int L, long long
 cudaError_t launch_exp2_fma(const float* x, float* y, long long n, cudaStream_t stream);
 
 cudaError_t read_device_status(unsigned int* out, bool clear);
+// Device address of the current device's status word.
+cudaError_t device_status_ptr(unsigned int** out);
+
+// Short-KV cross-attention (Skv <= 512, per-batch key lengths on the device): the kernel in
+// cross_attn.cu, which keeps a head's keys and values resident in shared memory.
+cudaError_t launch_cross_attn(const AttnArgs& a);
 
 // Encodes a TMA descriptor for a BSHD bf16 tensor [B, S_rows, H, D] whose sequence extent is
 // cut to `s_extent` rows (reads past it return zeros), with a box of 64 channels x 1 head x

@@ -57,6 +57,9 @@ _SIGNATURES = {
                           _vp, ctypes.c_size_t, _vp], _i),
     "dit_attn_fwd_ws_fixed_m": ([_vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _f, _vp,
                                  _vp, _vp, ctypes.c_size_t, _vp, _vp], _i),
+    "dit_attn_sharded_workspace_bytes": ([_i, _i, _i, _i, _i, _vp, _vp], ctypes.c_size_t),
+    "dit_attn_fwd_sharded": ([_vp, _i, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _f, _vp, _vp,
+                              _vp, ctypes.c_size_t, _vp], _i),
 }
 for _name, (_args, _res) in _SIGNATURES.items():
     _fn = getattr(_lib, _name)
@@ -418,6 +421,53 @@ def dit_cross_attn_shortkv(q, k, v, q_valid_len: int, kv_valid_len_dev, softmax_
     return out, lse
 
 
+def _int_array(vals):
+    return (ctypes.c_int * len(vals))(*[int(x) for x in vals])
+
+
+def _ptr_array(ts):
+    return (ctypes.c_void_p * len(ts))(*[t.data_ptr() for t in ts])
+
+
+def dit_attn_sharded_workspace_bytes(B: int, Sq: int, H: int, D: int, shard_padded, shard_valid) -> int:
+    n = len(shard_padded)
+    return int(_lib.dit_attn_sharded_workspace_bytes(B, Sq, H, D, n, _int_array(shard_padded),
+                                                     _int_array(shard_valid)))
+
+
+def dit_attn_fwd_sharded(q, shards, q_valid_len: int, cos_q, sin_q, softmax_scale=None, workspace=None,
+                         out=None, lse=None, stream=None):
+    """Attention of padded q [B, Sq, H, D] over key shards in one call: shards is a sequence of
+    (k_s, v_s, valid_s, cos_k_s, sin_k_s) with k_s, v_s [B, S_s, H, D] bf16 (S_s a multiple of
+    128) and the shard's tables [S_s, D/2] fp32 at its global key positions."""
+    _need(q, "q", torch.bfloat16, 4)
+    B, Sq, H, D = q.shape
+    ks, vs, valid, ck, sk = [], [], [], [], []
+    for i, (k, v, n, c, sn) in enumerate(shards):
+        _need(k, f"k[{i}]", torch.bfloat16, 4)
+        _need(v, f"v[{i}]", torch.bfloat16, 4)
+        _need(c, f"cos_k[{i}]", torch.float32, 2)
+        _need(sn, f"sin_k[{i}]", torch.float32, 2)
+        if tuple(k.shape) != (B, k.shape[1], H, D) or v.shape != k.shape:
+            raise ValueError(f"shard {i}: k and v must be [B, S_s, H, D] matching q")
+        ks.append(k); vs.append(v); valid.append(int(n)); ck.append(c); sk.append(sn)
+    padded = [k.shape[1] for k in ks]
+    _need(cos_q, "cos_q", torch.float32, 2)
+    _need(sin_q, "sin_q", torch.float32, 2)
+    scale = 1.0 / math.sqrt(D) if softmax_scale is None else float(softmax_scale)
+    need = dit_attn_sharded_workspace_bytes(B, Sq, H, D, padded, valid)
+    if need == 0:
+        raise DitError("dit_attn_sharded_workspace_bytes", -2)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    out, lse = _attn_outputs(q, out, lse)
+    _check("dit_attn_fwd_sharded", _lib.dit_attn_fwd_sharded(
+        _ptr(q), B, Sq, H, D, int(q_valid_len), len(ks), _ptr_array(ks), _ptr_array(vs), _int_array(padded),
+        _int_array(valid), _ptr(cos_q), _ptr(sin_q), _ptr_array(ck), _ptr_array(sk), scale, _ptr(out), _ptr(lse),
+        _ptr(workspace), int(workspace.numel() * workspace.element_size()), _stream_handle(stream)))
+    return out, lse
+
+
 def dit_attn_lse_merge(partial_o, partial_lse, out=None, lse=None, stream=None):
     """Merges n partials: partial_o [n, B, S, H, D] bf16, partial_lse [n, B, S, H] fp32."""
     _need(partial_o, "partial_o", torch.bfloat16, 5)
@@ -639,10 +689,11 @@ def attn_cross(q, k, v, kv_valid_len, *, softmax_scale=None, stream=None):
 def attn_sharded(q, shards, rope="1d", *, q_pos_offset: int = 0, theta: float = 10000.0,
                  softmax_scale=None, stream=None):
     """Attention of unpadded q [B, Lq, H, D] over keys held in shards [(k_0, v_0), (k_1, v_1),
-    ...] (each [B, L_s, H, D] bf16, CUDA, in global key order): one partial (O_s, LSE_s) per
-    shard, then the LSE merge. With rope = "1d" every key keeps its global position (shard s
-    starts after the keys of shards 0 .. s-1) and query i sits at q_pos_offset + i; rope =
-    None runs without RoPE. Returns (out [B, Lq, H, D] bf16, lse [B, Lq, H] fp32)."""
+    ...] (each [B, L_s, H, D] bf16, CUDA, in global key order). With rope = "1d" every key
+    keeps its global position (shard s starts after the keys of shards 0 .. s-1) and query i
+    sits at q_pos_offset + i: one dit_attn_fwd_sharded call (all shards in one launch, then
+    the LSE merge). rope = None runs one partial per shard without RoPE, then the merge.
+    Returns (out [B, Lq, H, D] bf16, lse [B, Lq, H] fp32)."""
     if rope not in (None, "1d"):
         raise ValueError('attn_sharded takes rope = "1d" or None')
     if not 1 <= len(shards) <= 64:
@@ -662,21 +713,25 @@ def attn_sharded(q, shards, rope="1d", *, q_pos_offset: int = 0, theta: float = 
                 torch.empty((B, 0, H), dtype=torch.float32, device=q.device))
     n, Sq = len(shards), _tiles(Lq)
     qp = _pad(q, Sq, stream)
+    if rope:
+        tq = rope_tables(Sq, D, "1d", q.device, L=Lq, pos_offset=q_pos_offset, theta=theta)
+        entries, offset = [], 0
+        for ks, vs in shards:
+            Ls = ks.shape[1]
+            Ss = _tiles(Ls)
+            kp, vp = _pad(ks, Ss, stream), _pad(vs, Ss, stream)
+            tk = rope_tables(Ss, D, "1d", q.device, L=Ls, pos_offset=offset, theta=theta)
+            entries.append((kp, vp, Ls, *tk))
+            offset += Ls
+        op, lp = dit_attn_fwd_sharded(qp, entries, Lq, *tq, softmax_scale=softmax_scale, stream=stream)
+        return _unpad(op, Lq, stream), _unpad(lp, Lq, stream)
     po = torch.empty((n, B, Sq, H, D), dtype=torch.bfloat16, device=q.device)
     pl = torch.empty((n, B, Sq, H), dtype=torch.float32, device=q.device)
-    tq = rope_tables(Sq, D, "1d", q.device, L=Lq, pos_offset=q_pos_offset, theta=theta) if rope else ()
-    offset = 0
     for s, (ks, vs) in enumerate(shards):
         Ls = ks.shape[1]
         Ss = _tiles(Ls)
         kp, vp = _pad(ks, Ss, stream), _pad(vs, Ss, stream)
-        if rope:
-            tk = rope_tables(Ss, D, "1d", q.device, L=Ls, pos_offset=offset, theta=theta)
-            dit_attn_fwd_ws(qp, kp, vp, Lq, Ls, *tq, *tk, softmax_scale=softmax_scale, out=po[s], lse=pl[s],
-                            stream=stream)
-        else:
-            dit_attn_fwd(qp, kp, vp, Lq, Ls, softmax_scale=softmax_scale, out=po[s], lse=pl[s], stream=stream)
-        offset += Ls
+        dit_attn_fwd(qp, kp, vp, Lq, Ls, softmax_scale=softmax_scale, out=po[s], lse=pl[s], stream=stream)
     op, lp = dit_attn_lse_merge(po, pl, stream=stream)
     return _unpad(op, Lq, stream), _unpad(lp, Lq, stream)
 
