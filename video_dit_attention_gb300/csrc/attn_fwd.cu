@@ -105,8 +105,6 @@ struct KParams {
   int Sq, Skv, H;
   int n_pairs, n_items;   // query-tile pairs per (b, h); B * H * n_pairs work items
   int q_valid, kv_valid;
-  int n_bh;                          // sharded mode: B * H
-  int chunk_valid[kMaxKeyChunks];    // sharded mode: valid keys of each key chunk
   const int32_t* kv_valid_dev;
   const float* cos_q;
   const float* sin_q;
@@ -159,11 +157,20 @@ struct ShardParams {
   CUtensorMap vm[kMaxKeyChunks];   // v of each chunk, extent = its valid rows
   KeyChunk c[kMaxKeyChunks];
   int n_chunks;
+  int n_bh;                        // B * H
   long long po_stride, pl_stride;  // elements between consecutive chunks' partial O / LSE
 };
 struct NoShards {};
 template <int kMode>
 using ShardArg = typename std::conditional<kMode == kModeRopeWsSharded, ShardParams, NoShards>::type;
+// Partial-LSE stride of the sharded mode (0 for the others, which have no ShardParams).
+template <int kMode>
+struct ShardStride {
+  __device__ static long long pl(const ShardArg<kMode>& sh) {
+    if constexpr (kMode == kModeRopeWsSharded) return sh.pl_stride;
+    else return 0;
+  }
+};
 
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;
@@ -291,19 +298,12 @@ struct Item {
 template <int kMode>
 __device__ __forceinline__ Item decode_item(const KParams& p, int it) {
   Item w;
-  const int pair = it % p.n_pairs;
-  int bh = it / p.n_pairs;
-  w.chunk = 0;
-  int kv = p.kv_valid;
-  if (kMode == kModeRopeWsSharded) {
-    // items in the order (chunk, b, h, query-tile pair): neighbouring CTAs share a chunk's K/V
-    w.chunk = bh / p.n_bh;
-    bh -= w.chunk * p.n_bh;
-    kv = p.chunk_valid[w.chunk];
-  }
+  const int pair = it % p.n_pairs, bh = it / p.n_pairs;
   w.h = bh % p.H;
   w.b = bh / p.H;
   w.q0 = pair * 256;
+  w.chunk = 0;
+  int kv = p.kv_valid;
   w.bad_len = false;
   if (kMode == kModeCross) {
     // Fail closed: a length outside [0, Skv] is not clamped into range. The batch is treated
@@ -315,6 +315,28 @@ __device__ __forceinline__ Item decode_item(const KParams& p, int it) {
   }
   w.kv_valid = kv;
   // Tile t is live if it holds a valid query row and there is at least one key.
+  w.has1 = w.q0 + 128 < p.Sq;
+  const bool live0 = (w.q0 < p.q_valid) && kv > 0;
+  const bool live1 = w.has1 && (w.q0 + 128 < p.q_valid) && kv > 0;
+  w.n_live = live1 ? 2 : (live0 ? 1 : 0);
+  w.n_kv = (kv + 127) / 128;
+  return w;
+}
+
+// Sharded mode: items in the order (key chunk, b, h, query-tile pair), so neighbouring CTAs
+// share a chunk's K/V; the chunk's valid keys replace the one kv length.
+__device__ __forceinline__ Item decode_item_sh(const KParams& p, const ShardParams& sh, int it) {
+  Item w;
+  const int pair = it % p.n_pairs;
+  int bh = it / p.n_pairs;
+  w.chunk = bh / sh.n_bh;
+  bh -= w.chunk * sh.n_bh;
+  w.h = bh % p.H;
+  w.b = bh / p.H;
+  w.q0 = pair * 256;
+  const int kv = sh.c[w.chunk].valid;
+  w.kv_valid = kv;
+  w.bad_len = false;
   w.has1 = w.q0 + 128 < p.Sq;
   const bool live0 = (w.q0 < p.q_valid) && kv > 0;
   const bool live1 = w.has1 && (w.q0 + 128 < p.q_valid) && kv > 0;
@@ -1208,13 +1230,12 @@ cudaError_t launch_sharded_mode(const AttnArgs& a, const KeyShard* shards, const
     if (!encode_bshd_map(&sh.km[c], kc.k_rot, a.B, ext, rows, a.H, D) ||
         !encode_bshd_map(&sh.vm[c], vbase, a.B, ext, rows, a.H, D))
       return cudaErrorInvalidValue;
-    p.chunk_valid[c] = plan.valid[c];
   }
   p.Sq = a.Sq;
   p.Skv = 0;
   p.H = a.H;
   p.n_pairs = (a.Sq + 255) / 256;
-  p.n_bh = a.B * a.H;
+  sh.n_bh = a.B * a.H;
   const long long n_items = static_cast<long long>(plan.n_chunks) * a.B * a.H * p.n_pairs;
   if (n_items >= (1ll << 31)) return cudaErrorInvalidValue;
   p.n_items = static_cast<int>(n_items);

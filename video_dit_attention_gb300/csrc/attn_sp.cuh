@@ -143,6 +143,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after_sync();
   const uint32_t tbase = bars->tmem_base;
   const int it0 = blockIdx.x, it_step = gridDim.x;
+  // Work item `it` (the sharded mode decodes its key chunk too).
+  auto dec = [&](int it) -> Item {
+    if constexpr (kShard) return decode_item_sh(p, sh, it);
+    else return decode_item<kMode>(p, it);
+  };
   // TMA maps of an item's keys and values (per key chunk in the sharded mode).
   auto kmap = [&](const Item& w) -> const CUtensorMap* {
     if constexpr (kShard) return &sh.km[w.chunk];
@@ -154,7 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
   // First item at or after `it` (in this CTA's sequence) that has work.
   auto first_live = [&](int it) -> int {
-    while (it < p.n_items && decode_item<kMode>(p, it).n_live == 0) it += it_step;
+    while (it < p.n_items && dec(it).n_live == 0) it += it_step;
     return it;
   };
   // Workspace mode: items whose Q was loaded and rotated before the roles start (0 or 1).
@@ -169,7 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int fit = first_live(it0);
     Item fw{};
     if (fit < p.n_items) {
-      fw = decode_item<kMode>(p, fit);
+      fw = dec(fit);
       pre_q = 1;
     }
     if (pre_q && tid == 0) {
@@ -280,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto count_tiles = [&]() -> int {
     int G = 0;
     for (int it = it0; it < p.n_items; it += it_step) {
-      const Item w = decode_item<kMode>(p, it);
+      const Item w = dec(it);
       if (w.n_live > 0) G += w.n_kv;
     }
     return G;
@@ -304,7 +309,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int g0 = 0, q_cnt = 0, ns0 = 0, ns1 = 0;
     bool ok = true;
     for (int it = it0; ok && it < p.n_items; it += it_step) {
-      const Item w = decode_item<kMode>(p, it);
+      const Item w = dec(it);
       if (w.n_live == 0) continue;
       // Workspace modes: Q is used once it is rotated in shared memory (q_ready).
       if (!(ok = wait_bar(kWs ? b_q_ready : b_q_full, q_cnt))) break;
@@ -356,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int G = count_tiles();
     bool ok = true;
     for (int it = it0; ok && it < p.n_items; it += it_step) {
-      const Item w = decode_item<kMode>(p, it);
+      const Item w = dec(it);
       if (w.n_live == 0) continue;
       for (int j = 0; ok && j < w.n_kv; ++j) {
         const int g = g0 + j, n = ring_load_v(g, G), slot = n % R;
@@ -411,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool skip = pre_q != 0;   // the first item's Q is already loaded
       bool ok = true;
       for (int it = it0; ok && it < p.n_items; it += it_step) {
-        const Item w = decode_item<kMode>(p, it);
+        const Item w = dec(it);
         if (w.n_live == 0) continue;
         if (skip) {
           skip = false;
@@ -464,13 +469,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       int kit = first_live(it0), kj = 0, vit = kit, vj = 0;
       bool k_ready = false;
       Item kw{}, vw{};
-      if (kit < p.n_items) kw = vw = decode_item<kMode>(p, kit);
+      if (kit < p.n_items) kw = vw = dec(kit);
       auto load_next_k = [&]() -> bool {
         if (kj == (kw.n_kv > kPrefetchLead ? kw.n_kv - kPrefetchLead : 0)) {
           // Warm L2 with the next item's Q tiles and first K/V tiles.
           const int nit = first_live(kit + it_step);
           if (nit < p.n_items) {
-            const Item nw = decode_item<kMode>(p, nit);
+            const Item nw = dec(nit);
             for (int t = 0; t < nw.n_live; ++t)
 #pragma unroll
               for (int c = 0; c < C::kSub; ++c)
@@ -490,7 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (++kj == kw.n_kv) {
           kj = 0;
           kit = first_live(kit + it_step);
-          if (kit < p.n_items) kw = decode_item<kMode>(p, kit);
+          if (kit < p.n_items) kw = dec(kit);
         }
         return true;
       };
@@ -499,7 +504,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (++vj == vw.n_kv) {
           vj = 0;
           vit = first_live(vit + it_step);
-          if (vit < p.n_items) vw = decode_item<kMode>(p, vit);
+          if (vit < p.n_items) vw = dec(vit);
         }
         return true;
       };
@@ -546,7 +551,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if constexpr (kWs) {
         const int nit = first_live(it_cur + it_step);
         if (nit >= p.n_items) return true;
-        const Item nw = decode_item<kMode>(p, nit);
+        const Item nw = dec(nit);
         if (!warp_wait(b_q_full, (qi + 1) & 1, abort_flag, status, kStatusTimeoutRope)) return false;
         if (t < nw.n_live) {
           const size_t row0 = static_cast<size_t>(nw.q0 + 128 * t) * (D / 2);
@@ -570,16 +575,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     bool ok = true;
     for (int it = it0; ok && it < p.n_items; it += it_step) {
-      const Item w = decode_item<kMode>(p, it);
-      // this item's output: the partial (O, LSE) of its key chunk in the sharded mode
-      uint16_t* out_b = p.out;
-      float* lse_b = p.lse;
-      if constexpr (kShard) {
-        out_b += w.chunk * sh.po_stride;
-        lse_b += w.chunk * sh.pl_stride;
-      }
+      const Item w = dec(it);
       if (t >= w.n_live) {
-        if (t == 0 || w.has1) write_empty_tile<D>(p, out_b, lse_b, w.b, w.h, w.q0 + 128 * t, r, 128);
+        if (t == 0 || w.has1) {
+          if constexpr (kShard)   // the partial (O, LSE) of the item's key chunk
+            write_empty_tile<D>(p, p.out + w.chunk * sh.po_stride, p.lse + w.chunk * sh.pl_stride, w.b, w.h,
+                                w.q0 + 128 * t, r, 128);
+          else
+            write_empty_tile<D>(p, p.out, p.lse, w.b, w.h, w.q0 + 128 * t, r, 128);
+        }
         if (kMode == kModeCross && w.bad_len && t == 0 && r == 0) atomicOr(status, kStatusBadKvLength);
         if (w.n_live > 0) {
           if (!(ok = rotate_next(it))) break;
@@ -765,12 +769,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int rr = r0 + i * kRPI + lr;
           const uint32_t src = (kFp8 ? sO + t * C::kOBytes : sP + t * C::kPBytes) + chunk + static_cast<uint32_t>(rr) * 128u +
                                ((unit ^ static_cast<uint32_t>(rr & 7)) << 4);
-          uint16_t* dst = out_b + ((static_cast<size_t>(w.b) * p.Sq + w.q0 + 128 * t + rr) * p.H + w.h) * D;
+          uint16_t* dst = p.out + ((static_cast<size_t>(w.b) * p.Sq + w.q0 + 128 * t + rr) * p.H + w.h) * D;
+          if constexpr (kShard) dst += w.chunk * sh.po_stride;
           *reinterpret_cast<uint4*>(dst + lu * 8) = lds128(src);
         }
       }
       __syncwarp();
-      lse_b[(static_cast<size_t>(w.b) * p.Sq + qrow) * p.H + w.h] =
+      (kShard ? p.lse + w.chunk * ShardStride<kMode>::pl(sh) : p.lse)[(static_cast<size_t>(w.b) * p.Sq + qrow) * p.H + w.h] =
           valid_row ? (m_used + log2f(l)) * kLn2 : -INFINITY;
       ++qi;
     }
@@ -793,7 +798,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int G = count_tiles();
       int vit = first_live(it0), vj = 0;
       Item vw{};
-      if (vit < p.n_items) vw = decode_item<kMode>(p, vit);
+      if (vit < p.n_items) vw = dec(vit);
       bool ok = true;
       for (int n = 0; ok && n < 2 * G; ++n) {
         const int slot = n % R;
@@ -810,7 +815,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (++vj == vw.n_kv) {
             vj = 0;
             vit = first_live(vit + it_step);
-            if (vit < p.n_items) vw = decode_item<kMode>(p, vit);
+            if (vit < p.n_items) vw = dec(vit);
           }
         }
         named_bar_sync(1, kZeroThreads);

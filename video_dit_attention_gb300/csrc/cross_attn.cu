@@ -22,24 +22,28 @@
 //     tiles. When L_b > 256 a query tile visits its keys in two halves of up to 256 with the
 //     online softmax, and the fill is reloaded per half (consecutive tiles alternate the order
 //     of the halves, so each tile reloads only one).
-//   - TMEM: S (256 columns, 128 lanes = query rows) and O double-buffered (2 x D columns). P is
-//     written as bf16 into shared memory (the K-major A operand of the P.V product), so the
-//     S columns are free as soon as the softmax has loaded them: S of tile t + 1 is computed
-//     while the softmax of tile t runs, and P_t V while the softmax of tile t + 1 starts.
+//   - TMEM: S (256 columns, 128 lanes = query rows), P (bf16, 128 columns) and O (D columns).
+//     P has columns of its own, so the S columns are free as soon as the softmax has loaded
+//     them: S of tile t + 1 is computed while the softmax of tile t runs, and P_t V while
+//     the softmax of tile t + 1 starts. O of a tile is taken out by the epilogue warps before
+//     the next tile's first P.V overwrites it. (Writing each thread's row straight to global
+//     memory, 32 scattered 16-byte pieces per warp store, took about 4,300 cycles per tile
+//     and slowed the MMA issue and the Q loads beside it: O goes out through a staged tile
+//     and a TMA store.)
 //   - One thread issues every MMA, in the order S_0, S_1, P_0 V, S_2, P_1 V, ... (S of the next
 //     step goes first unless that step needs a new fill, which must wait for the release of
 //     the current one).
 //   - Two softmax warpgroups share each tile: warpgroup A owns key columns 0-127 of the S
 //     block, warpgroup B columns 128-255, one thread per query row. The row maximum and the
 //     row sum are exchanged between the two threads of a row through shared memory (a named
-//     barrier per pair of warps that share a TMEM lane quarter). The epilogue of tile t runs
-//     after P of tile t + 1 is out: warpgroup A normalises and stores O columns [0, D/2),
-//     warpgroup B [D/2, D), straight from registers (each thread writes its row), and
-//     warpgroup A writes the LSE.
+//     barrier per pair of warps that share a TMEM lane quarter).
 //   - Warp 3 zeroes the V rows past L_b of the fill's last V tile, so that 0 * (pad contents)
 //     cannot reach O. K pad rows need nothing: their score columns are masked to -inf.
 //   - The single Q buffer is refilled once S of its tile is done; the producer warms L2 with
 //     the next two query tiles, so the refill comes from L2.
+//   - Warps 12-15 are the epilogue: for each tile they read O out of TMEM, normalise it with
+//     the rows' (m, l) handed over by the softmax, stage it in shared memory and store it
+//     with one TMA store, so none of that sits between two tiles' softmax.
 // Every wait is bounded (ptx.cuh); on a timeout the CTA records a status bit, drains its
 // copies and MMAs, frees TMEM and exits.
 
@@ -51,11 +55,13 @@
 namespace dit {
 namespace {
 
-constexpr int kXThreads = 384;   // warps 0-3: load / TMEM / MMA / V zeroing; 4-11: softmax
+constexpr int kXThreads = 512;   // warps 0-3: load / TMEM / MMA / V zeroing; 4-11: softmax; 12-15: epilogue
 constexpr float kXLn2 = 0.69314718055994530942f;
 constexpr float kXLog2e = 1.44269504088896340736f;
 constexpr float kXRescale = 8.0f;   // log2 units: O is rescaled only if the maximum grows by > 2^8
 constexpr int kLenCache = 128;      // per-batch key lengths kept in shared memory
+constexpr uint32_t kXColP = 256;    // TMEM columns: S [0, 256), P [256, 384), O [384, 384 + D)
+constexpr uint32_t kXColO = 384;
 
 template <int D>
 struct XCfg {
@@ -65,9 +71,10 @@ struct XCfg {
   static constexpr int kOffQ = 0;                  // one Q buffer
   static constexpr int kOffK = kOffQ + kTile;      // K: chunk c holds rows 0..255 at c * 2 kChunk
   static constexpr int kOffV = kOffK + 2 * kTile;  // V: two 128-row tiles
-  static constexpr int kOffP = kOffV + 2 * kTile;  // P: 128 rows x 256 keys bf16, 4 chunks of 64 keys
-  static constexpr int kOffX = kOffP + 4 * kChunk; // row maximum / sum exchange [2][128] fp32
-  static constexpr int kOffLen = kOffX + 2 * 128 * 4;   // key lengths of the first kLenCache batches
+  static constexpr int kOffO = kOffV + 2 * kTile;  // O staging tile (TMA store source)
+  static constexpr int kOffX = kOffO + kTile;      // row maximum / sum exchange [2][128] fp32
+  static constexpr int kOffML = kOffX + 2 * 128 * 4;    // (m, l) of each row for the epilogue [2 tiles][128]
+  static constexpr int kOffLen = kOffML + 2 * 128 * 8;  // key lengths of the first kLenCache batches
   static constexpr int kOffBar = kOffLen + kLenCache * 4;
   static constexpr int kSmem = kOffBar + 256 + 1024;   // barriers + alignment slack
 };
@@ -77,10 +84,11 @@ struct XBars {
   uint64_t q_full, q_empty;
   uint64_t kv_full, kv_ready, kv_empty;
   uint64_t s_full, s_free, p_full, pv_done;
-  uint64_t o_free[2];
+  uint64_t o_done, o_free, ml_full;
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
+  int epi_go;   // outcome of the epilogue group's last wait, broadcast to the group
 };
 
 struct XParams {
@@ -206,14 +214,15 @@ __device__ __forceinline__ bool x_next(const XParams& p, const int* len_s, int g
 template <int D>
 __global__ void __launch_bounds__(kXThreads, 1)
     cross_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                      const __grid_constant__ CUtensorMap tm_v, const XParams p) {
+                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                      const XParams p) {
   using C = XCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t s_base = smem_u32(smem);
   const uint32_t sQ = s_base + C::kOffQ, sK = s_base + C::kOffK, sV = s_base + C::kOffV;
-  const uint32_t sP = s_base + C::kOffP;
+  const uint32_t sO = s_base + C::kOffO;
   float* xch = reinterpret_cast<float*>(smem + C::kOffX);   // [wg][row]
   XBars* bars = reinterpret_cast<XBars*>(smem + C::kOffBar);
   int* len_s = reinterpret_cast<int*>(smem + C::kOffLen);
@@ -237,8 +246,9 @@ __global__ void __launch_bounds__(kXThreads, 1)
     mbar_init(smem_u32(&bars->s_free), 8);
     mbar_init(smem_u32(&bars->p_full), 8);
     mbar_init(smem_u32(&bars->pv_done), 1);
-    mbar_init(smem_u32(&bars->o_free[0]), 8);
-    mbar_init(smem_u32(&bars->o_free[1]), 8);
+    mbar_init(smem_u32(&bars->o_done), 1);
+    mbar_init(smem_u32(&bars->o_free), 4);
+    mbar_init(smem_u32(&bars->ml_full), 4);
     mbar_init(smem_u32(&bars->drain), 1);
     fence_mbar_init();
   }
@@ -250,12 +260,12 @@ __global__ void __launch_bounds__(kXThreads, 1)
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_o);
   }
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tbase = bars->tmem_base;
-  const uint32_t b_q_full = smem_u32(&bars->q_full), b_q_empty = smem_u32(&bars->q_empty);
   const uint32_t b_kv_full = smem_u32(&bars->kv_full), b_kv_ready = smem_u32(&bars->kv_ready);
   const uint32_t b_kv_empty = smem_u32(&bars->kv_empty);
   const uint32_t b_s_full = smem_u32(&bars->s_full), b_s_free = smem_u32(&bars->s_free);
@@ -269,7 +279,7 @@ __global__ void __launch_bounds__(kXThreads, 1)
   };
 
   if (warp < 4) {
-    regs_dec<64>();
+    regs_dec<56>();
     if (warp == 0 && lane == 0) {
       // ------------------------------------------------------------------ producer
       int q_cnt = 0, fill = 0;
@@ -278,12 +288,14 @@ __global__ void __launch_bounds__(kXThreads, 1)
         const XTile t = x_decode(p, len_s, g, g0, g1);
         if (!t.live) continue;
         // one Q buffer: free once every S product of the previous tile has completed
-        if (q_cnt >= 1 && !(ok = bounded_wait(b_q_empty, (q_cnt - 1) & 1, abort_flag, status, kStatusTimeoutLoad)))
+        if (q_cnt >= 1 && !(ok = bounded_wait(smem_u32(&bars->q_empty), (q_cnt - 1) & 1, abort_flag, status,
+                                              kStatusTimeoutLoad)))
           break;
-        mbar_arrive_expect_tx(b_q_full, C::kTile);
+        const uint32_t qb = smem_u32(&bars->q_full);
+        mbar_arrive_expect_tx(qb, C::kTile);
 #pragma unroll
         for (int c = 0; c < C::kSub; ++c)
-          tma_load_4d(sQ + c * C::kChunk, &tm_q, b_q_full, c * 64, t.h, t.qt * 128, t.b);
+          tma_load_4d(sQ + c * C::kChunk, &tm_q, qb, c * 64, t.h, t.qt * 128, t.b);
         ++q_cnt;
         // Warm L2 with the next two query tiles, so that each refill of the buffer is an L2 hit.
         for (int ga = g + 1; ga <= g + 2 && ga < g1; ++ga) {
@@ -311,7 +323,7 @@ __global__ void __launch_bounds__(kXThreads, 1)
       }
       // Let the copies in flight land before the CTA releases its shared memory (on the
       // normal path each has been waited for already, and these return at once).
-      if (q_cnt > 0) drain_wait(b_q_full, (q_cnt - 1) & 1, status);
+      if (q_cnt > 0) drain_wait(smem_u32(&bars->q_full), (q_cnt - 1) & 1, status);
       if (fill > 0) drain_wait(b_kv_full, (fill - 1) & 1, status);
     } else if (warp == 2 && lane == 0) {
       // ------------------------------------------------------------------ MMA issuer
@@ -326,9 +338,9 @@ __global__ void __launch_bounds__(kXThreads, 1)
       };
       // S = Q K^T of one step into the S columns.
       auto issue_s = [&](const XPos& x) -> bool {
-        if (x.s == 0 && !wait(b_q_full, x.tcnt)) return false;           // Q of the tile
-        if (!wait(b_kv_full, x.fill)) return false;                     // its keys
-        if (x.step > 0 && !wait(b_s_free, x.step - 1)) return false;     // previous S taken out
+        if (x.s == 0 && !wait(smem_u32(&bars->q_full), x.tcnt)) return false;   // Q of the tile
+        if (!wait(b_kv_full, x.fill)) return false;                             // its keys
+        if (x.step > 0 && !wait(b_s_free, x.step - 1)) return false;             // previous S taken out
         const uint64_t da = smem_desc_sw128(sQ, 16, 1024);
         const uint64_t db = smem_desc_sw128(sK, 16, 1024);
         const uint32_t idS = x.st.nkt == 2 ? kIdS2 : kIdS1;
@@ -339,28 +351,26 @@ __global__ void __launch_bounds__(kXThreads, 1)
           mma_bf16_ss(tbase, da + offa, db + offb, idS, kk > 0);
         }
         mma_commit(b_s_full);
-        if (x.s == x.ns - 1) mma_commit(b_q_empty);   // the tile's last S: Q may be reloaded
+        if (x.s == x.ns - 1) mma_commit(smem_u32(&bars->q_empty));   // the tile's last S: Q may be reloaded
         return true;
       };
-      // O (+)= P V of one step, P from shared memory (4 chunks of 64 keys).
+      // O (+)= P V of one step, P from TMEM (bf16 pairs; keys 128 j .. of the step at columns
+      // 256 + 64 j ..).
       auto issue_pv = [&](const XPos& x) -> bool {
-        const int ob = x.tcnt & 1;
         if (!wait(b_p_full, x.step)) return false;
-        if (x.s == 0 && x.tcnt >= 2 && !wait(smem_u32(&bars->o_free[ob]), (x.tcnt - 2) >> 1)) return false;
+        // the first step of a tile overwrites O: the previous tile's O has been read out
+        if (x.s == 0 && x.tcnt >= 1 && !wait(smem_u32(&bars->o_free), x.tcnt - 1)) return false;
         if (!wait(b_kv_ready, x.fill)) return false;
-        const uint32_t d_o = tbase + 256 + ob * D;
-        const uint64_t dp = smem_desc_sw128(sP, 16, 1024);
+        const uint32_t d_o = tbase + kXColO;
         for (int j = 0; j < x.st.nkt; ++j) {
           const uint64_t dv = smem_desc_sw128(sV + j * C::kTile, C::kChunk, 1024);
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            const int ka = j * 8 + kk;   // K step over the step's keys
-            const uint64_t offa = ((ka / 4) * C::kChunk + (ka % 4) * 32) >> 4;
-            mma_bf16_ss(d_o, dp + offa, dv + static_cast<uint64_t>(kk * 2048 >> 4), kIdO,
+          for (int kk = 0; kk < 8; ++kk)
+            mma_bf16_ts(d_o, tbase + kXColP + j * 64 + kk * 8, dv + static_cast<uint64_t>(kk * 2048 >> 4), kIdO,
                         (x.s > 0 || j > 0 || kk > 0) ? 1u : 0u);
-          }
         }
         mma_commit(b_pv_done);
+        if (x.s == x.ns - 1) mma_commit(smem_u32(&bars->o_done));   // the tile's O is complete
         if (x.st.release) mma_commit(b_kv_empty);
         return true;
       };
@@ -413,8 +423,8 @@ __global__ void __launch_bounds__(kXThreads, 1)
         }
       }
     }
-  } else {
-    regs_inc<216>();
+  } else if (warp < 12) {
+    regs_inc<200>();
     // -------------------------------------------------------------------- softmax + epilogue
     // The 256 threads of both warpgroups meet at named barriers (the row exchanges of a pair
     // of warps, the end of each tile). So that a timeout can never leave a thread waiting at
@@ -430,55 +440,14 @@ __global__ void __launch_bounds__(kXThreads, 1)
     float* x_mine = xch + wg * 128 + r;
     const float* x_other = xch + (1 - wg) * 128 + r;
     const float sl2 = p.scale_log2;
-    // This thread's P row: 16-byte unit x of 64-key chunk c at c * 16384 + r * 128 +
-    // ((x ^ (r & 7)) * 16), the 128-byte swizzle of the MMA's K-major A operand; warpgroup w
-    // writes chunks 2w and 2w + 1.
-    const uint32_t p_row = sP + static_cast<uint32_t>(wg) * 2u * C::kChunk + static_cast<uint32_t>(r) * 128u;
-    const uint32_t p_sw = static_cast<uint32_t>(r & 7);
+    const uint32_t tP = tbase + lane_off + kXColP + wg * 64;   // this warpgroup's P columns
+    const uint32_t tO = tbase + lane_off + kXColO + wg * (D / 2);   // its O columns
+    float2* ml = reinterpret_cast<float2*>(smem + C::kOffML);     // [2][128] (m, l) per row
     // Bounded wait by lane 0, outcome broadcast to the warp.
     auto wwait = [&](uint32_t bar, int phase) -> bool {
       int got = 0;
       if (lane == 0) got = bounded_wait(bar, phase & 1, abort_flag, status, kStatusTimeoutSoftmax) ? 1 : 0;
       return __shfl_sync(0xffffffffu, got, 0) != 0;
-    };
-    // The epilogue of a tile runs after P of the next tile is out (its O is complete by then).
-    bool pend = false;
-    int pend_b = 0, pend_h = 0, pend_qt = 0, pend_ob = 0;
-    float pend_m = 0.f, pend_l = 1.f;
-    auto epilogue = [&]() {
-      const uint32_t tO = tbase + lane_off + 256 + pend_ob * D + wg * (D / 2);
-      uint32_t orr[D / 2];
-#pragma unroll
-      for (int c = 0; c < D / 64; ++c) {
-        uint32_t part[32];
-        tmem_ld32(tO + c * 32, part);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) orr[c * 32 + i] = part[i];
-      }
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bars->o_free[pend_ob]));   // O may be overwritten
-      const int qrow = pend_qt * 128 + r;
-      const bool valid_row = qrow < p.q_valid;
-      const float inv_l = 1.f / pend_l;
-      uint4* dst = reinterpret_cast<uint4*>(p.out + ((static_cast<size_t>(pend_b) * p.Sq + qrow) * p.H + pend_h) * D +
-                                            wg * (D / 2));
-#pragma unroll
-      for (int u = 0; u < D / 16; ++u) {
-        uint4 o = make_uint4(0, 0, 0, 0);
-        if (valid_row) {
-          const uint32_t* f = &orr[8 * u];
-          o.x = pack_bf16x2(__uint_as_float(f[0]) * inv_l, __uint_as_float(f[1]) * inv_l);
-          o.y = pack_bf16x2(__uint_as_float(f[2]) * inv_l, __uint_as_float(f[3]) * inv_l);
-          o.z = pack_bf16x2(__uint_as_float(f[4]) * inv_l, __uint_as_float(f[5]) * inv_l);
-          o.w = pack_bf16x2(__uint_as_float(f[6]) * inv_l, __uint_as_float(f[7]) * inv_l);
-        }
-        dst[u] = o;
-      }
-      if (wg == 0)
-        p.lse[(static_cast<size_t>(pend_b) * p.Sq + qrow) * p.H + pend_h] =
-            valid_row ? (pend_m + log2f(pend_l)) * kXLn2 : -INFINITY;
-      pend = false;
     };
     int step = 0, tcnt = 0;
     bool ok = true;
@@ -489,8 +458,6 @@ __global__ void __launch_bounds__(kXThreads, 1)
         if (t.bad && wg == 0 && r == 0) atomicOr(status, kStatusBadKvLength);
         continue;
       }
-      const int ob = tcnt & 1;
-      const uint32_t tO = tbase + lane_off + 256 + ob * D;
       float m_run = -INFINITY, l_mine = 0.f;
       const int ns = x_n_steps(t);
       for (int s = 0; s < ns; ++s, ++step) {
@@ -548,8 +515,8 @@ __global__ void __launch_bounds__(kXThreads, 1)
         const bool resc = mt > m_run + kXRescale;
         const float m_new = resc ? mt : m_run;
         const float alpha = ex2_approx(m_run - m_new);   // 1 if kept; 0 on the first step
-        // The previous step's P V must be complete before P is rewritten (one P buffer) and,
-        // within a tile, before O is rescaled; both warpgroups take the same decision.
+        // The previous step's P V must be complete before P is rewritten and before O is
+        // rescaled; both warpgroups take the same decision (same maxima).
         if (step > 0) {
           ok = ok && wwait(b_pv_done, step - 1);
           if (ok) tc_fence_after_sync();
@@ -557,12 +524,11 @@ __global__ void __launch_bounds__(kXThreads, 1)
         if (ok && s > 0 && __any_sync(0xffffffffu, resc)) {
 #pragma unroll
           for (int c = 0; c < D / 64; ++c) {
-            uint32_t orr[32];
-            const uint32_t a = tO + wg * (D / 2) + c * 32;
-            tmem_ld32(a, orr);
+            uint32_t o32[32];
+            tmem_ld32(tO + c * 32, o32);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
-            tmem_st32(a, orr);
+            for (int i = 0; i < 32; ++i) o32[i] = __float_as_uint(__uint_as_float(o32[i]) * alpha);
+            tmem_st32(tO + c * 32, o32);
           }
         }
         m_run = m_new;
@@ -571,7 +537,7 @@ __global__ void __launch_bounds__(kXThreads, 1)
           const float neg_m = -m_run;
           float l4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {   // 16 keys at a time: two 16-byte units of P
+          for (int c = 0; c < 8; ++c) {   // 16 keys at a time: 8 bf16 pairs, 8 TMEM columns
             uint32_t pk[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
@@ -582,40 +548,27 @@ __global__ void __launch_bounds__(kXThreads, 1)
               add2(l4[2 * (i & 1)], l4[2 * (i & 1) + 1], p0, p1);
               pk[i] = pack_bf16x2(p0, p1);
             }
-            const uint32_t chunk = static_cast<uint32_t>(c >> 2) * C::kChunk;
-            const uint32_t u0 = static_cast<uint32_t>((2 * c) & 7), u1 = static_cast<uint32_t>((2 * c + 1) & 7);
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(p_row + chunk + ((u0 ^ p_sw) << 4)),
-                         "r"(pk[0]), "r"(pk[1]), "r"(pk[2]), "r"(pk[3])
-                         : "memory");
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(p_row + chunk + ((u1 ^ p_sw) << 4)),
-                         "r"(pk[4]), "r"(pk[5]), "r"(pk[6]), "r"(pk[7])
-                         : "memory");
+            tmem_st8_nowait(tP + c * 8, pk);
           }
           ls = (l4[0] + l4[1]) + (l4[2] + l4[3]);
+          tmem_st_wait();
         }
         l_mine = l_mine * alpha + ls;
         if (ok) {
-          fence_proxy_async_smem();   // P (generic stores) before the MMA's async-proxy reads
-          tc_fence_before_sync();     // and the O rescale (tcgen05.st) before the next P V
+          tc_fence_before_sync();   // P and the O rescale (tcgen05.st) before the P V
           __syncwarp();
           if (lane == 0) mbar_arrive(b_p_full);
         }
-        // The previous tile's O is complete (its last P V was waited for above): store it
-        // while this step's P V runs.
-        if (s == 0 && pend && ok) epilogue();
       }
-      // Row sum over both column blocks.
+      // Row sum over both column blocks; warpgroup A hands (m, l) of its rows to the epilogue.
       named_bar_sync(pair_bar, 64);
       *x_mine = l_mine;
       named_bar_sync(pair_bar, 64);
-      const float l = l_mine + *x_other;
-      pend = true;
-      pend_b = t.b;
-      pend_h = t.h;
-      pend_qt = t.qt;
-      pend_ob = ob;
-      pend_m = m_run;
-      pend_l = l;
+      if (wg == 0) {
+        ml[(tcnt & 1) * 128 + r] = make_float2(m_run, l_mine + *x_other);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bars->ml_full));
+      }
       ++tcnt;
       // Every one of the 256 threads got through this tile's waits.
       if (!named_bar_and(1, 256, ok)) {
@@ -623,10 +576,80 @@ __global__ void __launch_bounds__(kXThreads, 1)
         break;
       }
     }
-    if (ok && pend && wwait(b_pv_done, step - 1)) {
+  } else {
+    regs_dec<56>();
+    // -------------------------------------------------------------------- epilogue (warps 12-15)
+    // For every live tile: wait for its O (o_done) and its rows' (m, l); read O out of TMEM
+    // 32 columns at a time, normalise, stage the tile in the 128-byte swizzle of its TMA map,
+    // release O (o_free) and store the tile with one TMA store; write the LSE. Each wait is
+    // taken by one thread and its outcome broadcast to the group, so the group's named
+    // barriers see the same decisions in all 128 threads.
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const int et = tid - 384;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t tO = tbase + lane_off + kXColO;
+    const uint32_t p_sw = static_cast<uint32_t>(r & 7);
+    const float2* ml = reinterpret_cast<const float2*>(smem + C::kOffML);
+    volatile int* go = &bars->epi_go;
+    auto gwait = [&](uint32_t bar, int phase) -> bool {
+      if (et == 0) *go = bounded_wait(bar, phase & 1, abort_flag, status, kStatusTimeoutSoftmax) ? 1 : 0;
+      named_bar_sync(6, 128);
+      const bool res = *go != 0;
+      named_bar_sync(6, 128);   // every thread has read the outcome before the next wait writes it
+      return res;
+    };
+    int tcnt = 0;
+    for (int g = g0; g < g1; ++g) {
+      const XTile t = x_decode(p, len_s, g, g0, g1);
+      if (!t.live) continue;
+      if (!gwait(smem_u32(&bars->ml_full), tcnt)) break;
+      const float2 mlr = ml[(tcnt & 1) * 128 + r];
+      if (!gwait(smem_u32(&bars->o_done), tcnt)) break;
       tc_fence_after_sync();
-      epilogue();
+      const int qrow = t.qt * 128 + r;
+      const bool valid_row = qrow < p.q_valid;
+      const float inv_l = 1.f / mlr.y;
+      if (et == 0) bulk_wait_read();   // the previous store has read the staging tile
+      named_bar_sync(6, 128);
+#pragma unroll
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t o32[32];
+        tmem_ld32(tO + c * 32, o32);
+        if (c == D / 32 - 1) {
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&bars->o_free));   // O may be overwritten
+        }
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {   // columns 32c + 8q4 .. + 7: 16-byte unit 4c + q4
+          uint4 o = make_uint4(0, 0, 0, 0);
+          if (valid_row) {
+            const uint32_t* f = &o32[8 * q4];
+            o.x = pack_bf16x2(__uint_as_float(f[0]) * inv_l, __uint_as_float(f[1]) * inv_l);
+            o.y = pack_bf16x2(__uint_as_float(f[2]) * inv_l, __uint_as_float(f[3]) * inv_l);
+            o.z = pack_bf16x2(__uint_as_float(f[4]) * inv_l, __uint_as_float(f[5]) * inv_l);
+            o.w = pack_bf16x2(__uint_as_float(f[6]) * inv_l, __uint_as_float(f[7]) * inv_l);
+          }
+          const int cu = 4 * c + q4;   // 16-byte unit of the row
+          const uint32_t addr = sO + static_cast<uint32_t>(cu >> 3) * C::kChunk + static_cast<uint32_t>(r) * 128u +
+                                ((static_cast<uint32_t>(cu & 7) ^ p_sw) << 4);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(o.x), "r"(o.y), "r"(o.z), "r"(o.w)
+                       : "memory");
+        }
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(6, 128);
+      if (et == 0) {
+#pragma unroll
+        for (int c = 0; c < C::kSub; ++c) tma_store_4d(&tm_o, sO + c * C::kChunk, c * 64, t.h, t.qt * 128, t.b);
+        bulk_commit_group();
+      }
+      p.lse[(static_cast<size_t>(t.b) * p.Sq + qrow) * p.H + t.h] =
+          valid_row ? (mlr.x + log2f(mlr.y)) * kXLn2 : -INFINITY;
+      ++tcnt;
     }
+    if (et == 0) bulk_wait_all();
   }
   __syncwarp();
   tc_fence_before_sync();
@@ -638,12 +661,12 @@ __global__ void __launch_bounds__(kXThreads, 1)
 }  // namespace
 
 cudaError_t launch_cross_attn(const AttnArgs& a) {
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   const int qext = a.q_valid > 0 ? a.q_valid : 1;
   // Q rows past q_valid read as zeros; K and V are read up to Skv rows and masked per batch
   // on the device.
   if (!encode_bshd_map(&mq, a.q, a.B, qext, a.Sq, a.H, a.D) || !encode_bshd_map(&mk, a.k, a.B, a.Skv, a.Skv, a.H, a.D) ||
-      !encode_bshd_map(&mv, a.v, a.B, a.Skv, a.Skv, a.H, a.D))
+      !encode_bshd_map(&mv, a.v, a.B, a.Skv, a.Skv, a.H, a.D) || !encode_bshd_map(&mo, a.out, a.B, a.Sq, a.Sq, a.H, a.D))
     return cudaErrorInvalidValue;
   XParams p;
   p.B = a.B;
@@ -674,11 +697,11 @@ cudaError_t launch_cross_attn(const AttnArgs& a) {
   if (a.D == 128) {
     e = cudaFuncSetAttribute(cross_attn_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
-    cross_attn_kernel<128><<<grid, kXThreads, kSmem, a.stream>>>(mq, mk, mv, p);
+    cross_attn_kernel<128><<<grid, kXThreads, kSmem, a.stream>>>(mq, mk, mv, mo, p);
   } else {
     e = cudaFuncSetAttribute(cross_attn_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
-    cross_attn_kernel<64><<<grid, kXThreads, kSmem, a.stream>>>(mq, mk, mv, p);
+    cross_attn_kernel<64><<<grid, kXThreads, kSmem, a.stream>>>(mq, mk, mv, mo, p);
   }
   return cudaGetLastError();
 }
