@@ -1,8 +1,9 @@
 // Flash-attention forward for sm_103a on tcgen05 tensor cores, with exact pad-key masking,
 // natural-log LSE output and (optionally) split-halves RoPE fused into the q/k tile load.
 // This file holds the kernel for RoPE applied per loaded tile (P kept in TMEM); the plain,
-// cross-attention and workspace-RoPE modes run attn_sp_kernel (attn_sp.cuh, P staged in
-// shared memory), which shares the helpers, work items and parameters defined here.
+// workspace-RoPE, sharded-keys and FP8 modes run attn_sp_kernel (attn_sp.cuh, P staged in
+// shared memory), which shares the helpers, work items and parameters defined here. Short-KV
+// cross-attention has a kernel of its own (cross_attn.cu).
 //
 // What it computes (Difflet PR #153: pad keys dropped exactly, pad rows rotated by the
 // identity; maxdiffusion PR #491: the real KV length as the ragged tail; mstar PR #376: the
@@ -30,8 +31,7 @@
 //                Epilogue: O / l to bf16, LSE.
 //   warps 13-15  auxiliary: RoPE rotation of the landed Q and K tiles in shared memory
 //                (pairs (i, i + D/2) sit at the same swizzled offset of the two 64-column
-//                halves of a row), or, for cross-attention, zeroing of V rows past the
-//                per-batch valid length so that 0 * (pad garbage) cannot reach O.
+//                halves of a row).
 //                The rotation is computed in fp32 from the bf16 inputs and stored as fp16
 //                (11-bit significand, 8x finer than bf16; saturating at +-65504), and S =
 //                q~ k~^T then runs as an fp16 x fp16 MMA at the same tensor-core rate. Without
@@ -105,7 +105,6 @@ struct KParams {
   int Sq, Skv, H;
   int n_pairs, n_items;   // query-tile pairs per (b, h); B * H * n_pairs work items
   int q_valid, kv_valid;
-  const int32_t* kv_valid_dev;
   const float* cos_q;
   const float* sin_q;
   const float* cos_k;
@@ -259,20 +258,6 @@ struct Rotator {
   }
 };
 
-// Zeroes rows [first_row, 128) of a landed [128 x D] V tile (all sub-tiles), with NT threads.
-template <int D, int NT = kAuxThreads>
-__device__ __forceinline__ void zero_rows(uint32_t tile, int first_row, int at) {
-  constexpr int kSub = D / 64;
-  const int nrows = 128 - first_row;
-  const int nchunks = nrows * 8 * kSub;
-  for (int i = at; i < nchunks; i += NT) {
-    const int sub = i / (nrows * 8);
-    const int rem = i % (nrows * 8);
-    const int row = first_row + rem / 8;
-    sts128(tile + sub * 16384 + row * 128 + (rem % 8) * 16, make_uint4(0, 0, 0, 0));
-  }
-}
-
 // O = 0, LSE = -inf for the 128 rows of the query tile starting at q_first (a tile that is
 // all pad rows, or a problem with no keys). `tid` ranges over `nthr` cooperating threads.
 template <int D>
@@ -292,7 +277,6 @@ struct Item {
   int b, h, q0, n_live, n_kv, kv_valid;
   int chunk;      // sharded mode: key chunk of the item
   bool has1;      // tile 1 (rows q0 + 128 ..) lies inside the padded sequence
-  bool bad_len;   // cross-attention: the batch's device-side key length is outside [0, Skv]
 };
 
 template <int kMode>
@@ -303,16 +287,7 @@ __device__ __forceinline__ Item decode_item(const KParams& p, int it) {
   w.b = bh / p.H;
   w.q0 = pair * 256;
   w.chunk = 0;
-  int kv = p.kv_valid;
-  w.bad_len = false;
-  if (kMode == kModeCross) {
-    // Fail closed: a length outside [0, Skv] is not clamped into range. The batch is treated
-    // as having no keys (its rows get O = 0, LSE = -inf) and the call reports it through the
-    // device status word.
-    const int raw = p.kv_valid_dev[w.b];
-    w.bad_len = raw < 0 || raw > p.Skv;
-    kv = w.bad_len ? 0 : raw;
-  }
+  const int kv = p.kv_valid;
   w.kv_valid = kv;
   // Tile t is live if it holds a valid query row and there is at least one key.
   w.has1 = w.q0 + 128 < p.Sq;
@@ -336,7 +311,6 @@ __device__ __forceinline__ Item decode_item_sh(const KParams& p, const ShardPara
   w.q0 = pair * 256;
   const int kv = sh.c[w.chunk].valid;
   w.kv_valid = kv;
-  w.bad_len = false;
   w.has1 = w.q0 + 128 < p.Sq;
   const bool live0 = (w.q0 < p.q_valid) && kv > 0;
   const bool live1 = w.has1 && (w.q0 + 128 < p.q_valid) && kv > 0;
@@ -890,7 +864,7 @@ __global__ void __launch_bounds__(kThreads, 1)
      if (lane == 0) {
       // ------------------------------------------------------------ MMA issuer
       // S = Q K^T: fp16 operands after the fused rotation, the raw bf16 inputs otherwise.
-      constexpr uint32_t kIdS = idesc_f16kind_f32(128, 128, kMode == kModePlain || kMode == kModeCross,
+      constexpr uint32_t kIdS = idesc_f16kind_f32(128, 128, kMode == kModePlain,
                                                   false, false);
       constexpr uint32_t kIdO = idesc_bf16_f32(128, D, false, true);
       int kv_cnt = 0, q_cnt = 0;
@@ -907,7 +881,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       auto wait_v = [&](int g) -> bool {
         const int s = g % NSV;
-        const uint32_t vbar = (kMode == kModeCross) ? smem_u32(&bars->v_ready[s]) : smem_u32(&bars->v_full[s]);
+        const uint32_t vbar = smem_u32(&bars->v_full[s]);
         if (!bounded_wait(vbar, (g / NSV) & 1, abort_flag, status, kStatusTimeoutMma)) return false;
         tc_fence_after_sync();
         return true;
@@ -1035,25 +1009,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         kv_cnt += w.n_kv;
         ++q_cnt;
       }
-    } else if (kMode == kModeCross) {
-      for (int it = it0; ok && it < p.n_items; it += it_step) {
-        const Item w = decode_item<kMode>(p, it);
-        if (w.n_live == 0) continue;
-        for (int j = 0; ok && j < w.n_kv; ++j) {
-          const int gv = kv_cnt + j, s = gv % NSV;
-          if (!(ok = group_wait(smem_u32(&bars->v_full[s]), (gv / NSV) & 1, abort_flag, status,
-                                kStatusTimeoutRope, go, at)))
-            break;
-          const int nv = min(128, w.kv_valid - j * 128);
-          if (nv < 128) {
-            zero_rows<D>(sV0 + s * C::kTileBytes, nv, at);
-            fence_proxy_async_smem();
-          }
-          named_bar_sync(1, kAuxThreads);
-          if (at == 0) mbar_arrive(smem_u32(&bars->v_ready[s]));
-        }
-        kv_cnt += w.n_kv;
-      }
     }
     }
   }
@@ -1076,7 +1031,7 @@ cudaError_t launch_mode(const AttnArgs& a) {
   const void* k_src = is_ws_mode(kMode) ? static_cast<const void*>(k_rot) : a.k;
   // Cross-attention reads up to Skv rows and masks per batch on the device; self-attention
   // cuts the key/value extent to the valid length so pad rows are never even loaded.
-  const int kvext = (kMode == kModeCross) ? a.Skv : (a.kv_valid > 0 ? a.kv_valid : 1);
+  const int kvext = a.kv_valid > 0 ? a.kv_valid : 1;
   [[maybe_unused]] Fp8Layout f8{};
   if constexpr (kMode == kModeFp8) {
     // Rotate and quantise q, k, v into the workspace, then read the e4m3 copies: q~ and k~
@@ -1119,7 +1074,6 @@ cudaError_t launch_mode(const AttnArgs& a) {
   p.n_items = a.B * a.H * p.n_pairs;
   p.q_valid = a.q_valid;
   p.kv_valid = a.kv_valid;
-  p.kv_valid_dev = a.kv_valid_dev;
   p.cos_q = a.cos_q;
   p.sin_q = a.sin_q;
   p.cos_k = a.cos_k;
@@ -1241,7 +1195,6 @@ cudaError_t launch_sharded_mode(const AttnArgs& a, const KeyShard* shards, const
   p.n_items = static_cast<int>(n_items);
   p.q_valid = a.q_valid;
   p.kv_valid = 0;
-  p.kv_valid_dev = nullptr;
   p.cos_q = a.cos_q;
   p.sin_q = a.sin_q;
   p.cos_k = p.sin_k = nullptr;
@@ -1365,7 +1318,6 @@ cudaError_t launch_attn_fwd(const AttnArgs& a, AttnMode mode) {
     if (mode == kModeRopeWsFixedM) return launch_mode<128, kModeRopeWsFixedM>(a);
     if (mode == kModeFp8) return launch_mode<128, kModeFp8>(a);
     if (mode == kModeRope) return launch_mode<128, kModeRope>(a);
-    if (mode == kModeCross) return launch_mode<128, kModeCross>(a);
     return launch_mode<128, kModePlain>(a);
   }
   if (mode == kModeRopeWs) return launch_mode<64, kModeRopeWs>(a);
@@ -1373,7 +1325,6 @@ cudaError_t launch_attn_fwd(const AttnArgs& a, AttnMode mode) {
   if (mode == kModeRopeWsFixedM) return launch_mode<64, kModeRopeWsFixedM>(a);
   if (mode == kModeFp8) return cudaErrorInvalidValue;   // built for D = 128 only
   if (mode == kModeRope) return launch_mode<64, kModeRope>(a);
-  if (mode == kModeCross) return launch_mode<64, kModeCross>(a);
   return launch_mode<64, kModePlain>(a);
 }
 

@@ -1,6 +1,6 @@
-// Attention kernel with P staged in shared memory: the plain, cross-attention and
-// workspace-RoPE modes. Included by attn_fwd.cu inside its namespace, after the helpers it
-// uses (KParams, WsParams, Item, decode_item, write_empty_tile, zero_rows,
+// Attention kernel with P staged in shared memory: the plain, workspace-RoPE (with the q/k
+// RMSNorm, fixed-m, sharded-keys variants) and FP8 modes. Included by attn_fwd.cu inside its namespace, after the helpers it
+// uses (KParams, WsParams, Item, decode_item, write_empty_tile,
 // rotate_rows_fp16, warp_wait, group_wait, sts128).
 //
 // Same mathematics, work items, persistence and warp roles as attn_fwd_kernel. What changes
@@ -16,7 +16,7 @@
 // commits and barrier polls, close to the 64 cycles a 128 x 128 x 16 product takes, and left
 // the tensor core idle between groups; two issuers overlap that cost. They touch disjoint
 // TMEM columns and every commit covers only its own thread's MMAs, so they need no ordering
-// between them beyond the barriers below. Cross-attention zeroes V pad rows in warps 14-15.
+// between them beyond the barriers below.
 // Workspace modes: warps 14-15 rotate the first item's Q tiles; each later item's tile t is
 // rotated by softmax warpgroup t once it has written its last P_t of the item before.
 // Synchronisation per query-tile slot t (all waits bounded):
@@ -64,7 +64,7 @@ struct CfgSp {
 
 struct BarsSp {
   uint64_t q_full, q_ready, q_empty;
-  uint64_t r_full[6], r_ready[6], r_empty[6];
+  uint64_t r_full[6], r_empty[6];
   uint64_t s_full[2], s_free[2], p_full[2], pv_done[2], o_free[2];
   uint64_t drain[2];
   uint32_t tmem_base;
@@ -84,7 +84,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     attn_sp_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const KParams p, const WsParams ws,
                    const __grid_constant__ ShardArg<kMode> sh) {
-  static_assert(kMode == kModePlain || kMode == kModeCross || kMode == kModeFp8 || is_ws_mode(kMode), "mode");
+  static_assert(kMode == kModePlain || kMode == kModeFp8 || is_ws_mode(kMode), "mode");
   constexpr bool kFp8 = kMode == kModeFp8;
   static_assert(!kFp8 || D == 128, "the FP8 path is built for D = 128");
   constexpr bool kWs = is_ws_mode(kMode), kNorm = kMode == kModeRopeWsNorm;
@@ -115,7 +115,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(b_q_empty, 1);
     for (int s = 0; s < R; ++s) {
       mbar_init(smem_u32(&bars->r_full[s]), 1);
-      mbar_init(smem_u32(&bars->r_ready[s]), 1);
       mbar_init(smem_u32(&bars->r_empty[s]), 1);
     }
     for (int t = 0; t < 2; ++t) {
@@ -316,11 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; ok && j < w.n_kv; ++j) {
         const int g = g0 + j;
         const int n = ring_load_k(g), slot = n % R;
-        // Cross-attention: K too waits for the V-zeroing group (which passes every ring load
-        // in order), so that no slot is refilled before that group has seen its load.
-        if (!(ok = wait_bar(kMode == kModeCross ? smem_u32(&bars->r_ready[slot]) : smem_u32(&bars->r_full[slot]),
-                            n / R)))
-          break;
+        if (!(ok = wait_bar(smem_u32(&bars->r_full[slot]), n / R))) break;
         const uint64_t db = smem_desc_sw128(sR + slot * C::kTileBytes, 16, 1024);
         for (int t = 0; t < w.n_live; ++t) {
           // S_t may be overwritten once the softmax has taken the previous S_t out of TMEM.
@@ -365,10 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (w.n_live == 0) continue;
       for (int j = 0; ok && j < w.n_kv; ++j) {
         const int g = g0 + j, n = ring_load_v(g, G), slot = n % R;
-        // Cross-attention: the V tile is used after its pad rows have been zeroed.
-        if (!(ok = wait_bar(kMode == kModeCross ? smem_u32(&bars->r_ready[slot]) : smem_u32(&bars->r_full[slot]),
-                            n / R)))
-          break;
+        if (!(ok = wait_bar(smem_u32(&bars->r_full[slot]), n / R))) break;
         const uint64_t db = smem_desc_sw128(sR + slot * C::kTileBytes, kFp8 ? 16 : 16384, 1024);
         for (int t = 0; t < w.n_live; ++t) {
           const int np = t ? np1 : np0, epi = t ? epi1 : epi0;
@@ -584,7 +576,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           else
             write_empty_tile<D>(p, p.out, p.lse, w.b, w.h, w.q0 + 128 * t, r, 128);
         }
-        if (kMode == kModeCross && w.bad_len && t == 0 && r == 0) atomicOr(status, kStatusBadKvLength);
         if (w.n_live > 0) {
           if (!(ok = rotate_next(it))) break;
           ++qi;
@@ -761,7 +752,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr int kLPR = D / 8, kRPI = 32 / kLPR;
         const int r0 = r & ~31, lu = lane % kLPR, lr = lane / kLPR;   // r0: first row of this warp
         const uint32_t chunk = static_cast<uint32_t>(lu >> 3) * 16384u, unit = static_cast<uint32_t>(lu & 7);
-        // Stores in flight per lane: more helps short items (cross-attention) and plain
+        // Stores in flight per lane: more helps short items and plain
         // attention slightly; the workspace mode measured best at one.
         constexpr int kStoreUnroll = kWs ? 1 : 4;
 #pragma unroll kStoreUnroll
@@ -785,42 +776,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) s_issuer();
     } else if (warp == 13) {
       if (lane == 0) pv_issuer();
-    } else if (kMode == kModeCross) {
-      // ---------------------------------------------------------- V pad rows (warps 14-15)
-      // K/V tiles are loaded up to Skv rows; rows past the batch's valid length are zeroed so
-      // that 0 * (pad contents) cannot reach O. Every ring load passes through here in order (K
-      // loads unchanged), and both issuers wait for r_ready, which therefore completes once per
-      // load like r_full. A slot is refilled only after its load was used, which needed
-      // r_ready, so this group never sees a slot's r_full move on by more than one phase.
-      constexpr int kZeroThreads = 64;
-      const int at = tid - 448;
-      volatile int* go = &bars->aux_go;
-      const int G = count_tiles();
-      int vit = first_live(it0), vj = 0;
-      Item vw{};
-      if (vit < p.n_items) vw = dec(vit);
-      bool ok = true;
-      for (int n = 0; ok && n < 2 * G; ++n) {
-        const int slot = n % R;
-        if (!(ok = group_wait<kZeroThreads>(smem_u32(&bars->r_full[slot]), (n / R) & 1, abort_flag,
-                                              status, kStatusTimeoutRope, go, at)))
-          break;
-        const bool is_v = (n == 2 * G - 1) || (n >= 2 && (n & 1) == 0);
-        if (is_v) {
-          const int nv = min(128, vw.kv_valid - vj * 128);
-          if (nv < 128) {
-            zero_rows<D, kZeroThreads>(sR + slot * C::kTileBytes, nv, at);
-            fence_proxy_async_smem();
-          }
-          if (++vj == vw.n_kv) {
-            vj = 0;
-            vit = first_live(vit + it_step);
-            if (vit < p.n_items) vw = dec(vit);
-          }
-        }
-        named_bar_sync(1, kZeroThreads);
-        if (at == 0) mbar_arrive(smem_u32(&bars->r_ready[slot]));
-      }
     }
   }
   }

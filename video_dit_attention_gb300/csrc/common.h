@@ -7,8 +7,8 @@
 
 namespace dit {
 
-// One attention launch: self-attention (optionally with fused RoPE) or short-KV
-// cross-attention. Pointers are device pointers; shapes as in include/dit_attn.h.
+// One attention call: self-attention (optionally with RoPE), short-KV cross-attention or
+// sharded keys. Pointers are device pointers; shapes as in include/dit_attn.h.
 struct AttnArgs {
   const void* q;
   const void* k;
@@ -35,7 +35,6 @@ struct AttnArgs {
 enum AttnMode : int {
   kModePlain = 0,  // no RoPE, one kv length
   kModeRope = 1,   // RoPE fused into the q/k tile load
-  kModeCross = 2,  // no RoPE, per-batch kv length read on the device
   kModeRopeWs = 3, // RoPE applied once per q/k tile into a workspace, then attention on it
   kModeRopeWsNorm = 4,  // as kModeRopeWs, with per-head q/k RMSNorm before the rotation
   kModeRopeWsFixedM = 5,  // as kModeRopeWs; 32-row blocks whose norm bound allows it skip the

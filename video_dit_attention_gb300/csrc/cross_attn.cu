@@ -25,25 +25,22 @@
 //   - TMEM: S (256 columns, 128 lanes = query rows), P (bf16, 128 columns) and O (D columns).
 //     P has columns of its own, so the S columns are free as soon as the softmax has loaded
 //     them: S of tile t + 1 is computed while the softmax of tile t runs, and P_t V while
-//     the softmax of tile t + 1 starts. O of a tile is taken out by the epilogue warps before
-//     the next tile's first P.V overwrites it. (Writing each thread's row straight to global
-//     memory, 32 scattered 16-byte pieces per warp store, took about 4,300 cycles per tile
-//     and slowed the MMA issue and the Q loads beside it: O goes out through a staged tile
-//     and a TMA store.)
+//     the softmax of tile t + 1 starts. O is read out to registers before P of the next tile
+//     is released, then staged in shared memory and written with one TMA store per tile
+//     while the next P.V runs. (Writing each thread's row straight to global memory, 32
+//     scattered 16-byte pieces per warp store, took about 4,300 cycles per tile and slowed
+//     the MMA issue and the Q loads beside it.)
 //   - One thread issues every MMA, in the order S_0, S_1, P_0 V, S_2, P_1 V, ... (S of the next
 //     step goes first unless that step needs a new fill, which must wait for the release of
 //     the current one).
 //   - Two softmax warpgroups share each tile: warpgroup A owns key columns 0-127 of the S
 //     block, warpgroup B columns 128-255, one thread per query row. The row maximum and the
 //     row sum are exchanged between the two threads of a row through shared memory (a named
-//     barrier per pair of warps that share a TMEM lane quarter).
+//     barrier per pair of warps that share a TMEM lane quarter). Warpgroup A normalises and
+//     stages O columns [0, D/2), warpgroup B [D/2, D); warpgroup A writes the LSE.
 //   - Warp 3 zeroes the V rows past L_b of the fill's last V tile, so that 0 * (pad contents)
 //     cannot reach O. K pad rows need nothing: their score columns are masked to -inf.
-//   - The single Q buffer is refilled once S of its tile is done; the producer warms L2 with
-//     the next two query tiles, so the refill comes from L2.
-//   - Warps 12-15 are the epilogue: for each tile they read O out of TMEM, normalise it with
-//     the rows' (m, l) handed over by the softmax, stage it in shared memory and store it
-//     with one TMA store, so none of that sits between two tiles' softmax.
+//   - Q is double-buffered; the producer also warms L2 with the next two query tiles.
 // Every wait is bounded (ptx.cuh); on a timeout the CTA records a status bit, drains its
 // copies and MMAs, frees TMEM and exits.
 
@@ -55,7 +52,7 @@
 namespace dit {
 namespace {
 
-constexpr int kXThreads = 512;   // warps 0-3: load / TMEM / MMA / V zeroing; 4-11: softmax; 12-15: epilogue
+constexpr int kXThreads = 384;   // warps 0-3: load / TMEM / MMA / V zeroing; 4-11: softmax
 constexpr float kXLn2 = 0.69314718055994530942f;
 constexpr float kXLog2e = 1.44269504088896340736f;
 constexpr float kXRescale = 8.0f;   // log2 units: O is rescaled only if the maximum grows by > 2^8
@@ -68,27 +65,25 @@ struct XCfg {
   static constexpr int kSub = D / 64;              // 64-column (128-byte) chunks per row
   static constexpr int kTile = 128 * D * 2;        // one 128-row bf16 tile
   static constexpr int kChunk = 128 * 128;         // one 128-row chunk (16 KB)
-  static constexpr int kOffQ = 0;                  // one Q buffer
-  static constexpr int kOffK = kOffQ + kTile;      // K: chunk c holds rows 0..255 at c * 2 kChunk
+  static constexpr int kOffQ = 0;                  // two Q buffers
+  static constexpr int kOffK = kOffQ + 2 * kTile;  // K: chunk c holds rows 0..255 at c * 2 kChunk
   static constexpr int kOffV = kOffK + 2 * kTile;  // V: two 128-row tiles
   static constexpr int kOffO = kOffV + 2 * kTile;  // O staging tile (TMA store source)
   static constexpr int kOffX = kOffO + kTile;      // row maximum / sum exchange [2][128] fp32
-  static constexpr int kOffML = kOffX + 2 * 128 * 4;    // (m, l) of each row for the epilogue [2 tiles][128]
-  static constexpr int kOffLen = kOffML + 2 * 128 * 8;  // key lengths of the first kLenCache batches
+  static constexpr int kOffLen = kOffX + 2 * 128 * 4;   // key lengths of the first kLenCache batches
   static constexpr int kOffBar = kOffLen + kLenCache * 4;
   static constexpr int kSmem = kOffBar + 256 + 1024;   // barriers + alignment slack
 };
 static_assert(XCfg<128>::kSmem <= 232448, "shared memory of the D = 128 cross kernel");
 
 struct XBars {
-  uint64_t q_full, q_empty;
+  uint64_t q_full[2], q_empty[2];
   uint64_t kv_full, kv_ready, kv_empty;
   uint64_t s_full, s_free, p_full, pv_done;
-  uint64_t o_done, o_free, ml_full;
+  uint64_t o_free;
   uint64_t drain;
   uint32_t tmem_base;
   int abort;
-  int epi_go;   // outcome of the epilogue group's last wait, broadcast to the group
 };
 
 struct XParams {
@@ -237,8 +232,10 @@ __global__ void __launch_bounds__(kXThreads, 1)
   if (tid < kLenCache && tid < p.B) len_s[tid] = p.kv_len[tid];
   if (tid == 0) {
     bars->abort = 0;
-    mbar_init(smem_u32(&bars->q_full), 1);
-    mbar_init(smem_u32(&bars->q_empty), 1);
+    mbar_init(smem_u32(&bars->q_full[0]), 1);
+    mbar_init(smem_u32(&bars->q_full[1]), 1);
+    mbar_init(smem_u32(&bars->q_empty[0]), 1);
+    mbar_init(smem_u32(&bars->q_empty[1]), 1);
     mbar_init(smem_u32(&bars->kv_full), 1);
     mbar_init(smem_u32(&bars->kv_ready), 1);
     mbar_init(smem_u32(&bars->kv_empty), 1);
@@ -246,9 +243,7 @@ __global__ void __launch_bounds__(kXThreads, 1)
     mbar_init(smem_u32(&bars->s_free), 8);
     mbar_init(smem_u32(&bars->p_full), 8);
     mbar_init(smem_u32(&bars->pv_done), 1);
-    mbar_init(smem_u32(&bars->o_done), 1);
-    mbar_init(smem_u32(&bars->o_free), 4);
-    mbar_init(smem_u32(&bars->ml_full), 4);
+    mbar_init(smem_u32(&bars->o_free), 8);
     mbar_init(smem_u32(&bars->drain), 1);
     fence_mbar_init();
   }
@@ -279,7 +274,7 @@ __global__ void __launch_bounds__(kXThreads, 1)
   };
 
   if (warp < 4) {
-    regs_dec<56>();
+    regs_dec<64>();
     if (warp == 0 && lane == 0) {
       // ------------------------------------------------------------------ producer
       int q_cnt = 0, fill = 0;
@@ -287,15 +282,16 @@ __global__ void __launch_bounds__(kXThreads, 1)
       for (int g = g0; ok && g < g1; ++g) {
         const XTile t = x_decode(p, len_s, g, g0, g1);
         if (!t.live) continue;
-        // one Q buffer: free once every S product of the previous tile has completed
-        if (q_cnt >= 1 && !(ok = bounded_wait(smem_u32(&bars->q_empty), (q_cnt - 1) & 1, abort_flag, status,
-                                              kStatusTimeoutLoad)))
+        // Q buffer q_cnt & 1: free once every S product of the tile before last has completed
+        const int buf = q_cnt & 1;
+        if (q_cnt >= 2 && !(ok = bounded_wait(smem_u32(&bars->q_empty[buf]), ((q_cnt - 2) >> 1) & 1, abort_flag,
+                                              status, kStatusTimeoutLoad)))
           break;
-        const uint32_t qb = smem_u32(&bars->q_full);
+        const uint32_t qb = smem_u32(&bars->q_full[buf]);
         mbar_arrive_expect_tx(qb, C::kTile);
 #pragma unroll
         for (int c = 0; c < C::kSub; ++c)
-          tma_load_4d(sQ + c * C::kChunk, &tm_q, qb, c * 64, t.h, t.qt * 128, t.b);
+          tma_load_4d(sQ + buf * C::kTile + c * C::kChunk, &tm_q, qb, c * 64, t.h, t.qt * 128, t.b);
         ++q_cnt;
         // Warm L2 with the next two query tiles, so that each refill of the buffer is an L2 hit.
         for (int ga = g + 1; ga <= g + 2 && ga < g1; ++ga) {
@@ -323,7 +319,8 @@ __global__ void __launch_bounds__(kXThreads, 1)
       }
       // Let the copies in flight land before the CTA releases its shared memory (on the
       // normal path each has been waited for already, and these return at once).
-      if (q_cnt > 0) drain_wait(smem_u32(&bars->q_full), (q_cnt - 1) & 1, status);
+      for (int n = q_cnt - 2 > 0 ? q_cnt - 2 : 0; n < q_cnt; ++n)
+        drain_wait(smem_u32(&bars->q_full[n & 1]), (n >> 1) & 1, status);
       if (fill > 0) drain_wait(b_kv_full, (fill - 1) & 1, status);
     } else if (warp == 2 && lane == 0) {
       // ------------------------------------------------------------------ MMA issuer
@@ -338,10 +335,11 @@ __global__ void __launch_bounds__(kXThreads, 1)
       };
       // S = Q K^T of one step into the S columns.
       auto issue_s = [&](const XPos& x) -> bool {
-        if (x.s == 0 && !wait(smem_u32(&bars->q_full), x.tcnt)) return false;   // Q of the tile
-        if (!wait(b_kv_full, x.fill)) return false;                             // its keys
-        if (x.step > 0 && !wait(b_s_free, x.step - 1)) return false;             // previous S taken out
-        const uint64_t da = smem_desc_sw128(sQ, 16, 1024);
+        const int buf = x.tcnt & 1;
+        if (x.s == 0 && !wait(smem_u32(&bars->q_full[buf]), x.tcnt >> 1)) return false;   // Q of the tile
+        if (!wait(b_kv_full, x.fill)) return false;                                       // its keys
+        if (x.step > 0 && !wait(b_s_free, x.step - 1)) return false;                       // previous S taken out
+        const uint64_t da = smem_desc_sw128(sQ + buf * C::kTile, 16, 1024);
         const uint64_t db = smem_desc_sw128(sK, 16, 1024);
         const uint32_t idS = x.st.nkt == 2 ? kIdS2 : kIdS1;
 #pragma unroll
@@ -351,7 +349,7 @@ __global__ void __launch_bounds__(kXThreads, 1)
           mma_bf16_ss(tbase, da + offa, db + offb, idS, kk > 0);
         }
         mma_commit(b_s_full);
-        if (x.s == x.ns - 1) mma_commit(smem_u32(&bars->q_empty));   // the tile's last S: Q may be reloaded
+        if (x.s == x.ns - 1) mma_commit(smem_u32(&bars->q_empty[buf]));   // the tile's last S: Q may be reloaded
         return true;
       };
       // O (+)= P V of one step, P from TMEM (bf16 pairs; keys 128 j .. of the step at columns
@@ -370,7 +368,6 @@ __global__ void __launch_bounds__(kXThreads, 1)
                         (x.s > 0 || j > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(b_pv_done);
-        if (x.s == x.ns - 1) mma_commit(smem_u32(&bars->o_done));   // the tile's O is complete
         if (x.st.release) mma_commit(b_kv_empty);
         return true;
       };
@@ -423,8 +420,8 @@ __global__ void __launch_bounds__(kXThreads, 1)
         }
       }
     }
-  } else if (warp < 12) {
-    regs_inc<200>();
+  } else {
+    regs_inc<216>();
     // -------------------------------------------------------------------- softmax + epilogue
     // The 256 threads of both warpgroups meet at named barriers (the row exchanges of a pair
     // of warps, the end of each tile). So that a timeout can never leave a thread waiting at
@@ -442,14 +439,66 @@ __global__ void __launch_bounds__(kXThreads, 1)
     const float sl2 = p.scale_log2;
     const uint32_t tP = tbase + lane_off + kXColP + wg * 64;   // this warpgroup's P columns
     const uint32_t tO = tbase + lane_off + kXColO + wg * (D / 2);   // its O columns
-    float2* ml = reinterpret_cast<float2*>(smem + C::kOffML);     // [2][128] (m, l) per row
+    const uint32_t p_sw = static_cast<uint32_t>(r & 7);
     // Bounded wait by lane 0, outcome broadcast to the warp.
     auto wwait = [&](uint32_t bar, int phase) -> bool {
       int got = 0;
       if (lane == 0) got = bounded_wait(bar, phase & 1, abort_flag, status, kStatusTimeoutSoftmax) ? 1 : 0;
       return __shfl_sync(0xffffffffu, got, 0) != 0;
     };
-    int step = 0, tcnt = 0;
+    // The previous tile's output, read out of TMEM before P of the next tile is released.
+    bool pend = false;
+    int pend_b = 0, pend_h = 0, pend_qt = 0;
+    float pend_m = 0.f, pend_l = 1.f;
+    auto read_o = [&](uint32_t (&orr)[D / 2]) {
+#pragma unroll
+      for (int c = 0; c < D / 64; ++c) {
+        uint32_t part[32];
+        tmem_ld32(tO + c * 32, part);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) orr[c * 32 + i] = part[i];
+      }
+      tc_fence_before_sync();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_u32(&bars->o_free));   // O may be overwritten
+    };
+    // Normalise the read-out O, stage it in the 128-byte swizzle of the tile's TMA map and
+    // store the tile (one thread), and the LSE. All 256 threads call this.
+    auto store_o = [&](const uint32_t (&orr)[D / 2], bool ok_now) {
+      const int qrow = pend_qt * 128 + r;
+      const bool valid_row = qrow < p.q_valid;
+      const float inv_l = 1.f / pend_l;
+      if (tid == 128) bulk_wait_read();   // the previous store has read the staging tile
+      named_bar_sync(1, 256);
+#pragma unroll
+      for (int u = 0; u < D / 16; ++u) {
+        uint4 o = make_uint4(0, 0, 0, 0);
+        if (valid_row) {
+          const uint32_t* f = &orr[8 * u];
+          o.x = pack_bf16x2(__uint_as_float(f[0]) * inv_l, __uint_as_float(f[1]) * inv_l);
+          o.y = pack_bf16x2(__uint_as_float(f[2]) * inv_l, __uint_as_float(f[3]) * inv_l);
+          o.z = pack_bf16x2(__uint_as_float(f[4]) * inv_l, __uint_as_float(f[5]) * inv_l);
+          o.w = pack_bf16x2(__uint_as_float(f[6]) * inv_l, __uint_as_float(f[7]) * inv_l);
+        }
+        const int cu = wg * (D / 16) + u;   // 16-byte unit of the full row
+        const uint32_t addr = sO + static_cast<uint32_t>(cu >> 3) * C::kChunk + static_cast<uint32_t>(r) * 128u +
+                              ((static_cast<uint32_t>(cu & 7) ^ p_sw) << 4);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(o.x), "r"(o.y), "r"(o.z), "r"(o.w)
+                     : "memory");
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(1, 256);
+      if (tid == 128 && ok_now) {
+#pragma unroll
+        for (int c = 0; c < C::kSub; ++c) tma_store_4d(&tm_o, sO + c * C::kChunk, c * 64, pend_h, pend_qt * 128, pend_b);
+        bulk_commit_group();
+      }
+      if (wg == 0 && ok_now)
+        p.lse[(static_cast<size_t>(pend_b) * p.Sq + qrow) * p.H + pend_h] =
+            valid_row ? (pend_m + log2f(pend_l)) * kXLn2 : -INFINITY;
+      pend = false;
+    };
+    int step = 0;
     bool ok = true;
     for (int g = g0; g < g1; ++g) {
       const XTile t = x_decode(p, len_s, g, g0, g1);
@@ -515,8 +564,8 @@ __global__ void __launch_bounds__(kXThreads, 1)
         const bool resc = mt > m_run + kXRescale;
         const float m_new = resc ? mt : m_run;
         const float alpha = ex2_approx(m_run - m_new);   // 1 if kept; 0 on the first step
-        // The previous step's P V must be complete before P is rewritten and before O is
-        // rescaled; both warpgroups take the same decision (same maxima).
+        // The previous step's P V must be complete before P is rewritten and before O is read
+        // out or rescaled; both warpgroups take the same decision (same maxima).
         if (step > 0) {
           ok = ok && wwait(b_pv_done, step - 1);
           if (ok) tc_fence_after_sync();
@@ -554,102 +603,58 @@ __global__ void __launch_bounds__(kXThreads, 1)
           tmem_st_wait();
         }
         l_mine = l_mine * alpha + ls;
-        if (ok) {
+        // The previous tile's O is complete (its last P V was waited for above): take it out
+        // of TMEM before this step's P is released, since this P V overwrites O.
+        if (s == 0 && pend) {
+          uint32_t orr[D / 2];
+          if (ok) {
+            read_o(orr);
+          } else {
+#pragma unroll
+            for (int i = 0; i < D / 2; ++i) orr[i] = 0u;
+          }
+          if (ok) {
+            tc_fence_before_sync();   // P (tcgen05.st) before the P V
+            __syncwarp();
+            if (lane == 0) mbar_arrive(b_p_full);
+          }
+          store_o(orr, ok);   // staged and stored while this P V runs
+        } else if (ok) {
           tc_fence_before_sync();   // P and the O rescale (tcgen05.st) before the P V
           __syncwarp();
           if (lane == 0) mbar_arrive(b_p_full);
         }
       }
-      // Row sum over both column blocks; warpgroup A hands (m, l) of its rows to the epilogue.
+      // Row sum over both column blocks.
       named_bar_sync(pair_bar, 64);
       *x_mine = l_mine;
       named_bar_sync(pair_bar, 64);
-      if (wg == 0) {
-        ml[(tcnt & 1) * 128 + r] = make_float2(m_run, l_mine + *x_other);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&bars->ml_full));
-      }
-      ++tcnt;
+      pend = true;
+      pend_b = t.b;
+      pend_h = t.h;
+      pend_qt = t.qt;
+      pend_m = m_run;
+      pend_l = l_mine + *x_other;
       // Every one of the 256 threads got through this tile's waits.
       if (!named_bar_and(1, 256, ok)) {
         ok = false;
         break;
       }
     }
-  } else {
-    regs_dec<56>();
-    // -------------------------------------------------------------------- epilogue (warps 12-15)
-    // For every live tile: wait for its O (o_done) and its rows' (m, l); read O out of TMEM
-    // 32 columns at a time, normalise, stage the tile in the 128-byte swizzle of its TMA map,
-    // release O (o_free) and store the tile with one TMA store; write the LSE. Each wait is
-    // taken by one thread and its outcome broadcast to the group, so the group's named
-    // barriers see the same decisions in all 128 threads.
-    const int quarter = warp & 3;
-    const int r = quarter * 32 + lane;
-    const int et = tid - 384;
-    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t tO = tbase + lane_off + kXColO;
-    const uint32_t p_sw = static_cast<uint32_t>(r & 7);
-    const float2* ml = reinterpret_cast<const float2*>(smem + C::kOffML);
-    volatile int* go = &bars->epi_go;
-    auto gwait = [&](uint32_t bar, int phase) -> bool {
-      if (et == 0) *go = bounded_wait(bar, phase & 1, abort_flag, status, kStatusTimeoutSoftmax) ? 1 : 0;
-      named_bar_sync(6, 128);
-      const bool res = *go != 0;
-      named_bar_sync(6, 128);   // every thread has read the outcome before the next wait writes it
-      return res;
-    };
-    int tcnt = 0;
-    for (int g = g0; g < g1; ++g) {
-      const XTile t = x_decode(p, len_s, g, g0, g1);
-      if (!t.live) continue;
-      if (!gwait(smem_u32(&bars->ml_full), tcnt)) break;
-      const float2 mlr = ml[(tcnt & 1) * 128 + r];
-      if (!gwait(smem_u32(&bars->o_done), tcnt)) break;
-      tc_fence_after_sync();
-      const int qrow = t.qt * 128 + r;
-      const bool valid_row = qrow < p.q_valid;
-      const float inv_l = 1.f / mlr.y;
-      if (et == 0) bulk_wait_read();   // the previous store has read the staging tile
-      named_bar_sync(6, 128);
+    if (ok && pend) {
+      // the last tile: every thread passed the last tile-end barrier with ok
+      uint32_t orr[D / 2];
+      const bool got = wwait(b_pv_done, step - 1);
+      if (got) {
+        tc_fence_after_sync();
+        read_o(orr);
+      } else {
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t o32[32];
-        tmem_ld32(tO + c * 32, o32);
-        if (c == D / 32 - 1) {
-          tc_fence_before_sync();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(smem_u32(&bars->o_free));   // O may be overwritten
-        }
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {   // columns 32c + 8q4 .. + 7: 16-byte unit 4c + q4
-          uint4 o = make_uint4(0, 0, 0, 0);
-          if (valid_row) {
-            const uint32_t* f = &o32[8 * q4];
-            o.x = pack_bf16x2(__uint_as_float(f[0]) * inv_l, __uint_as_float(f[1]) * inv_l);
-            o.y = pack_bf16x2(__uint_as_float(f[2]) * inv_l, __uint_as_float(f[3]) * inv_l);
-            o.z = pack_bf16x2(__uint_as_float(f[4]) * inv_l, __uint_as_float(f[5]) * inv_l);
-            o.w = pack_bf16x2(__uint_as_float(f[6]) * inv_l, __uint_as_float(f[7]) * inv_l);
-          }
-          const int cu = 4 * c + q4;   // 16-byte unit of the row
-          const uint32_t addr = sO + static_cast<uint32_t>(cu >> 3) * C::kChunk + static_cast<uint32_t>(r) * 128u +
-                                ((static_cast<uint32_t>(cu & 7) ^ p_sw) << 4);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(o.x), "r"(o.y), "r"(o.z), "r"(o.w)
-                       : "memory");
-        }
+        for (int i = 0; i < D / 2; ++i) orr[i] = 0u;
       }
-      fence_proxy_async_smem();
-      named_bar_sync(6, 128);
-      if (et == 0) {
-#pragma unroll
-        for (int c = 0; c < C::kSub; ++c) tma_store_4d(&tm_o, sO + c * C::kChunk, c * 64, t.h, t.qt * 128, t.b);
-        bulk_commit_group();
-      }
-      p.lse[(static_cast<size_t>(t.b) * p.Sq + qrow) * p.H + t.h] =
-          valid_row ? (mlr.x + log2f(mlr.y)) * kXLn2 : -INFINITY;
-      ++tcnt;
+      store_o(orr, got);
     }
-    if (et == 0) bulk_wait_all();
+    if (tid == 128) bulk_wait_all();
   }
   __syncwarp();
   tc_fence_before_sync();
