@@ -185,8 +185,8 @@ KERNEL_SOURCES = ("attn_fwd.cu", "attn_sp.cuh", "ptx.cuh", "cross_attn.cu")
 
 def profiled(name, variant=""):
     """Figures of the committed ncu summary of this workload (and kernel variant: "qknorm",
-    "fixed_m"): {"traffic": DRAM bytes per launch of the dominant kernel (per step of four
-    launches for the sharded workload), "ncu_kernel_ms": its ncu duration per launch (per
+    "fixed_m"): {"traffic": DRAM bytes per launch of the dominant kernel (per step, the attention
+    launch and the merge, for the sharded workload), "ncu_kernel_ms": its ncu duration per launch (per
     step for sharded) or None}, or None if there is no summary or the kernel sources changed
     since it was taken."""
     import hashlib
@@ -204,7 +204,7 @@ def profiled(name, variant=""):
         if line.startswith("kernel sources sha256"):
             sha = line.split(":")[-1].strip()
         elif line.startswith(("traffic_bytes_per_launch:", "traffic_bytes_per_step:")):
-            traffic = int(line.split(":")[1])   # per step for sharded (four launches), like achieved
+            traffic = int(line.split(":")[1])   # per step for sharded (attention + merge), like achieved
         elif line.startswith(("ncu_ms_per_launch:", "ncu_ms_per_step:")):
             ncu_ms = float(line.split(":")[1])
     if sha != h:
