@@ -44,6 +44,29 @@ def test_cross_many_tiles_per_cta(lib, D, kv):
     assert lib.dit_device_status() == 0
 
 
+@pytest.mark.parametrize("D,kv,grow", [(128, [250, 256], 1), (128, [400, 512], 2), (64, [512, 300], 3)])
+def test_cross_growing_maximum(lib, D, kv, grow):
+    """Keys of one 128-key block scaled by 4 (exact in bf16), so that for many rows its scores
+    exceed those of the block visited first by more than the softmax lets its reference trail
+    (8 in log2 units, plus up to 1 for the reference's rounding up): with at most 256 keys
+    the P already written for the earlier block is rescaled; with more, O of the earlier steps
+    is. grow = the scaled block (1: keys 128-255, 2: 256-383, 3: 384-511). Odd query rows
+    are scaled by 1/8, so that they see no such jump and the rescale runs on warps where only
+    some rows need it. (Scaling by 8 takes the bf16 rounding of P alone past the O tolerance:
+    a step-by-step simulation of the kernel's arithmetic gives 0.0234 there, 0.016 at 4.)"""
+    case = AttnCase("crossgrow", B=2, H=4, D=D, Sq=768, Skv=512, q_valid=700, kv_valid=kv, seed=90 + grow)
+    q, k, v = make_qkv(case)
+    k[:, 128 * grow:128 * (grow + 1)] *= 4.0
+    q[:, 1::2] *= 0.125
+    s = np.einsum("qhd,khd->hqk", q[0, :700].astype(np.float64), k[0].astype(np.float64)) * case.scale / np.log(2)
+    jump = s[:, :, 128 * grow:128 * (grow + 1)].max(-1) - s[:, :, :128].max(-1)
+    assert np.mean(jump > 9.0) > 0.2 and np.mean(jump < 8.0) > 0.2
+    O, L = _run_cross(lib, case, q, k, v)
+    Or, Lr = attention(q, k, v, case.q_valid, kv, case.scale)
+    compare(O, L, Or, Lr, case.q_valid)
+    assert lib.dit_device_status() == 0
+
+
 def test_cross_pad_garbage_is_nan_safe(lib):
     case = AttnCase("crossnan", B=2, H=2, D=64, Sq=256, Skv=256, q_valid=256, kv_valid=[77, 200], seed=71)
     q, k, v = make_qkv(case)

@@ -12,37 +12,48 @@
 //
 // Design (one GPU, sm_103a). The text is short (at most 512 keys), so the work per query
 // tile is small (one or two 128-key tiles at the drawn lengths) and the query/output stream
-// dominates: 97 MB of Q in and 97 MB of O out at B2 H40, against 21 MB of K and V.
+// dominates: 97 MB of Q in and 97 MB of O out at B2 H40, against 21 MB of K and V. What
+// limits such a kernel is the chain of dependent steps per query tile (Q load, S product,
+// softmax, P.V product, read-out of O, store), not any one unit, so the design keeps two of
+// these chains in flight per SM and gives them nothing to wait for from each other.
 //   - Work is a flat list of 128-row query tiles over (b, h, tile). CTA c of a persistent grid
-//     takes the contiguous range [c T / G, (c + 1) T / G), so every CTA has the same number of
-//     tiles and walks one or two heads.
-//   - The keys and values of the current (b, h) are loaded once into shared memory (a "fill")
-//     and stay there for all of the CTA's query tiles of that head: K as one 256-row operand
-//     (two 128-row tiles, so S = Q K^T is one N = 256 product per K step), V as two 128-row
-//     tiles. When L_b > 256 a query tile visits its keys in two halves of up to 256 with the
-//     online softmax, and the fill is reloaded per half (consecutive tiles alternate the order
-//     of the halves, so each tile reloads only one).
-//   - TMEM: S (256 columns, 128 lanes = query rows), P (bf16, 128 columns) and O (D columns).
-//     P has columns of its own, so the S columns are free as soon as the softmax has loaded
-//     them: S of tile t + 1 is computed while the softmax of tile t runs, and P_t V while
-//     the softmax of tile t + 1 starts. O is read out to registers before P of the next tile
-//     is released, then staged in shared memory and written with one TMA store per tile
-//     while the next P.V runs. (Writing each thread's row straight to global memory, 32
-//     scattered 16-byte pieces per warp store, took about 4,300 cycles per tile and slowed
-//     the MMA issue and the Q loads beside it.)
-//   - One thread issues every MMA, in the order S_0, S_1, P_0 V, S_2, P_1 V, ... (S of the next
-//     step goes first unless that step needs a new fill, which must wait for the release of
-//     the current one).
-//   - Two softmax warpgroups share each tile: warpgroup A owns key columns 0-127 of the S
-//     block, warpgroup B columns 128-255, one thread per query row. The row maximum and the
-//     row sum are exchanged between the two threads of a row through shared memory (a named
-//     barrier per pair of warps that share a TMEM lane quarter). Warpgroup A normalises and
-//     stages O columns [0, D/2), warpgroup B [D/2, D); warpgroup A writes the LSE.
-//   - Warp 3 zeroes the V rows past L_b of the fill's last V tile, so that 0 * (pad contents)
-//     cannot reach O. K pad rows need nothing: their score columns are masked to -inf.
-//   - Q is double-buffered; the producer also warms L2 with the next two query tiles.
+//     takes the contiguous range [c T / G, (c + 1) T / G). The live tiles of the range (a
+//     valid query row and at least one key) are numbered n = 0, 1, ...; tile n belongs to
+//     softmax warpgroup n & 1 and to Q buffer n % 3. Each warpgroup owns its tiles outright:
+//     one thread per query row holds every key column of that row, so the row maximum and
+//     sum need no exchange between warpgroups.
+//   - The keys and values of the current (b, h) stay in shared memory (a "fill", 256 rows of
+//     K and of V) for all of the CTA's tiles of that head. When L_b > 256 a tile visits its
+//     keys in two halves (key tiles {0, 1} and {2, n_kv - 1}); the two tiles of a pair
+//     (in-run indices 2p and 2p + 1, one per warpgroup) visit the halves in the order
+//     (p & 1, 1 - (p & 1)), so a pair's second half is the next pair's first and a run of
+//     P pairs needs P + 1 fills. A fill is released when both MMA issuers have arrived on it:
+//     by a commit after their last product on it, or, for an issuer with no product on it, by
+//     a plain arrival once it has landed.
+//   - TMEM: each warpgroup has 256 columns. With n_kv <= 2, S = Q K^T is one product of N =
+//     128 n_kv keys into columns [0, 128 n_kv); the softmax writes P (bf16 pairs) over the
+//     columns it has already read, [0, 64 n_kv); O = P V (tensor-memory A operand) goes to
+//     columns [128, 128 + D), over S columns that are dead by then. With n_kv > 2 each key
+//     tile is a step of its own (S in [0, 128), P in [0, 64)), with the online softmax across
+//     steps. A warpgroup's next S is issued once its previous P.V is complete (and, when it
+//     covers O's columns, once O has been read out).
+//   - The softmax keeps a reference m that trails the running maximum by at most kXRescale
+//     (log2 units) and is an integer: when a block's maximum exceeds m + kXRescale, m becomes
+//     its ceiling, and what the row has accumulated (P of earlier blocks of the same product,
+//     or O) is scaled by the power of two 2^(m_old - m_new), which is exact.
+//   - Epilogue: O is read out of TMEM, normalised, staged in the tile's own Q buffer (Q is
+//     dead once the tile's products have completed) in the 128-byte swizzle and written by one
+//     TMA store; the buffer goes back to the Q producer once the store has read it.
+//   - Roles: warp 0 loads Q (three buffers; the next two tiles are warmed in L2); warp 1 owns
+//     TMEM, loads the fills and zeroes the V rows past L_b of a fill's last V tile (so that
+//     0 * (pad contents) cannot reach O; K pad rows need nothing, their score columns are
+//     masked to -inf); warps 2 and 3 issue the MMAs of softmax warpgroups 0 and 1; warps 4-7
+//     and 8-11 are the two softmax warpgroups.
 // Every wait is bounded (ptx.cuh); on a timeout the CTA records a status bit, drains its
-// copies and MMAs, frees TMEM and exits.
+// copies and MMAs, frees TMEM and exits. The only named barrier is each warpgroup's own
+// epilogue barrier, which every thread of the warpgroup reaches at each of its tiles (a
+// thread whose wait failed skips the tensor-memory work, not the barrier) and where the
+// 128 threads decide together whether to go on.
 
 #include <cuda_bf16.h>
 
@@ -52,39 +63,38 @@
 namespace dit {
 namespace {
 
-constexpr int kXThreads = 384;   // warps 0-3: load / TMEM / MMA / V zeroing; 4-11: softmax
+constexpr int kXThreads = 384;   // warps 0-3: Q loads, TMEM + fills, two MMA issuers; 4-11: softmax
 constexpr float kXLn2 = 0.69314718055994530942f;
 constexpr float kXLog2e = 1.44269504088896340736f;
-constexpr float kXRescale = 8.0f;   // log2 units: O is rescaled only if the maximum grows by > 2^8
+constexpr float kXRescale = 8.0f;   // log2 units: the reference may trail the maximum by up to 8
 constexpr int kLenCache = 128;      // per-batch key lengths kept in shared memory
-constexpr uint32_t kXColP = 256;    // TMEM columns: S [0, 256), P [256, 384), O [384, 384 + D)
-constexpr uint32_t kXColO = 384;
+constexpr int kXQBufs = 3;          // Q buffers (each also stages its tile's O)
+constexpr uint32_t kXRegion = 256;  // TMEM columns per softmax warpgroup
+constexpr uint32_t kXColO = 128;    // O within a region: columns [128, 128 + D)
 
 template <int D>
 struct XCfg {
   static constexpr int kSub = D / 64;              // 64-column (128-byte) chunks per row
   static constexpr int kTile = 128 * D * 2;        // one 128-row bf16 tile
   static constexpr int kChunk = 128 * 128;         // one 128-row chunk (16 KB)
-  static constexpr int kOffQ = 0;                  // two Q buffers
-  static constexpr int kOffK = kOffQ + 2 * kTile;  // K: chunk c holds rows 0..255 at c * 2 kChunk
+  static constexpr int kOffQ = 0;                  // kXQBufs Q buffers
+  static constexpr int kOffK = kOffQ + kXQBufs * kTile;  // K: chunk c holds rows 0..255 at c * 2 kChunk
   static constexpr int kOffV = kOffK + 2 * kTile;  // V: two 128-row tiles
-  static constexpr int kOffO = kOffV + 2 * kTile;  // O staging tile (TMA store source)
-  static constexpr int kOffX = kOffO + kTile;      // row maximum / sum exchange [2][128] fp32
-  static constexpr int kOffLen = kOffX + 2 * 128 * 4;   // key lengths of the first kLenCache batches
+  static constexpr int kOffLen = kOffV + 2 * kTile;      // key lengths of the first kLenCache batches
   static constexpr int kOffBar = kOffLen + kLenCache * 4;
-  static constexpr int kSmem = kOffBar + 256 + 1024;   // barriers + alignment slack
+  static constexpr int kSmem = kOffBar + 256 + 1024;     // barriers + alignment slack
 };
 static_assert(XCfg<128>::kSmem <= 232448, "shared memory of the D = 128 cross kernel");
 
 struct XBars {
-  uint64_t q_full[2], q_empty[2];
+  uint64_t q_full[kXQBufs], q_empty[kXQBufs];
   uint64_t kv_full, kv_ready, kv_empty;
-  uint64_t s_full, s_free, p_full, pv_done;
-  uint64_t o_free;
-  uint64_t drain;
+  uint64_t s_full[2], p_full[2], pv_done[2], o_free[2];
+  uint64_t drain[2];
   uint32_t tmem_base;
   int abort;
 };
+static_assert(sizeof(XBars) <= 256, "barrier block");
 
 struct XParams {
   int B, Sq, Skv, H, q_valid;
@@ -97,15 +107,16 @@ struct XParams {
   unsigned int* status;
 };
 
-// One query tile of the CTA's range and where it sits in its (b, h) run.
+// One query tile of the CTA's range and where it sits in its run (the live tiles of its
+// (b, h) inside the range, which are consecutive).
 struct XTile {
   int b, h, qt;
   int L;        // valid keys (0 for a bad or empty length)
   int n_kv;     // 128-key tiles holding them
   bool live;    // has a valid query row and at least one key
   bool bad;     // the batch's length was outside [0, Skv]
-  int i;        // index of this tile among the live tiles of its (b, h) run in this CTA
-  bool last;    // last live tile of that run
+  int i;        // index of this tile in its run
+  int len;      // live tiles in the run
 };
 
 // Every role decodes every tile of its range; the key lengths of the first kLenCache batches
@@ -123,42 +134,63 @@ __device__ __forceinline__ XTile x_decode(const XParams& p, const int* len_s, in
   const int n_live_qt = (p.q_valid + 127) >> 7;   // live tiles are a prefix of each head
   t.live = t.L > 0 && t.qt < n_live_qt;
   const int qt_first = (g0 / p.n_qt == bh) ? g0 - bh * p.n_qt : 0;
-  const int qt_end = (min(g1, (bh + 1) * p.n_qt) - bh * p.n_qt);   // one past the run's last tile
+  const int qt_end = min(min(g1, (bh + 1) * p.n_qt) - bh * p.n_qt, n_live_qt);   // one past the run
   t.i = t.qt - qt_first;
-  t.last = t.qt == min(qt_end, n_live_qt) - 1;
+  t.len = qt_end - qt_first;
   return t;
 }
 
-// The key steps of a live tile: one step of up to 256 keys when L <= 256; else two halves
-// (key tiles {0, 1} and {2, n_kv - 1}), in the order (0, 1) for even i and (1, 0) for odd i,
-// so that a tile's first half is the previous tile's last one.
+// Fills of a run: one when n_kv <= 2, else pairs + 1 (fill k holds key half k & 1).
+__device__ __forceinline__ int x_run_fills(const XTile& t) { return t.n_kv <= 2 ? 1 : ((t.len + 1) >> 1) + 1; }
+// Key tiles of fill k of the run: first tile and count.
+__device__ __forceinline__ void x_fill_tiles(const XTile& t, int k, int& kt0, int& cnt) {
+  if (t.n_kv <= 2) {
+    kt0 = 0;
+    cnt = t.n_kv;
+  } else {
+    const int half = k & 1;
+    kt0 = 2 * half;
+    cnt = half ? t.n_kv - 2 : 2;
+  }
+}
+
+// The products of a live tile. n_kv <= 2: one step over all its keys. n_kv > 2: one step per
+// key tile, the tiles of the first half visited, then those of the second.
 struct XStep {
-  int kt0, nkt;     // first key tile and number of key tiles (1 or 2)
-  bool new_fill;    // this step loads a new fill (the previous one is released first)
-  bool release;     // the fill is released after this step's products
+  int fill;         // fill of the run it reads (0-based within the run)
+  int j0;           // first slot of the fill it reads
+  int kt;           // first key tile
+  int nkt;          // key tiles in the product (1 or 2)
+  bool group_end;   // last step of the tile that reads this fill
+  bool first_half;  // n_kv > 2: the step reads the pair's first half
 };
-
-__device__ __forceinline__ int x_n_steps(const XTile& t) { return t.n_kv > 2 ? 2 : 1; }
-
+__device__ __forceinline__ int x_n_steps(const XTile& t) { return t.n_kv <= 2 ? 1 : t.n_kv; }
 __device__ __forceinline__ XStep x_step(const XTile& t, int s) {
   XStep st;
   if (t.n_kv <= 2) {
-    st.kt0 = 0;
+    st.fill = 0;
+    st.j0 = 0;
+    st.kt = 0;
     st.nkt = t.n_kv;
-    st.new_fill = t.i == 0;
-    st.release = t.last;
+    st.group_end = true;
+    st.first_half = false;
     return st;
   }
-  const int half = ((t.i & 1) == 0) ? s : 1 - s;
-  st.kt0 = half ? 2 : 0;
-  st.nkt = half ? t.n_kv - 2 : 2;
-  st.new_fill = s == 1 || t.i == 0;
-  st.release = s == 0 || t.last;
+  const int pair = t.i >> 1;
+  const int h0 = pair & 1;
+  const int c0 = h0 ? t.n_kv - 2 : 2;   // key tiles of the half visited first
+  st.first_half = s < c0;
+  const int half = st.first_half ? h0 : 1 - h0;
+  st.j0 = st.first_half ? s : s - c0;
+  st.kt = 2 * half + st.j0;
+  st.nkt = 1;
+  st.fill = st.first_half ? pair : pair + 1;
+  st.group_end = st.first_half ? (s == c0 - 1) : (s == t.n_kv - 1);
   return st;
 }
 
 // O = 0 and LSE = -inf for one tile's rows (columns [c0, c0 + D/2) of O by this warpgroup;
-// the LSE by warpgroup A), written directly.
+// the LSE by warpgroup 0), written directly.
 template <int D>
 __device__ __forceinline__ void x_write_empty(const XParams& p, const XTile& t, int wg, int r) {
   const int row = t.qt * 128 + r;
@@ -168,42 +200,21 @@ __device__ __forceinline__ void x_write_empty(const XParams& p, const XTile& t, 
   if (wg == 0) p.lse[(static_cast<size_t>(t.b) * p.Sq + row) * p.H + t.h] = -INFINITY;
 }
 
-// Position in a CTA's sequence of key steps (live tiles only, each with one or two steps).
-struct XPos {
-  int g;        // tile index in the flat list (the CTA's range is [g0, g1))
-  int s;        // step within the tile
-  XTile t;
-  XStep st;
-  int ns;       // steps of the tile
-  int tcnt;     // live tiles before this one (O buffer tcnt & 1)
-  int fill;     // index of the fill this step reads
-  int step;     // steps before this one
-};
-
-// Advances `pos` to the next key step of the CTA's live tiles; false at the end. Start with
-// pos.g = g0 - 1, pos.s = pos.ns = 0, pos.tcnt = pos.fill = pos.step = -1 (first call moves
-// to the first step, with tcnt = step = 0 and fill = 0).
-__device__ __forceinline__ bool x_next(const XParams& p, const int* len_s, int g0, int g1, XPos& pos) {
-  if (pos.g >= g0 && pos.s + 1 < pos.ns) {
-    ++pos.s;
-  } else {
-    int g = pos.g + 1;
-    XTile t{};
-    for (; g < g1; ++g) {
-      t = x_decode(p, len_s, g, g0, g1);
-      if (t.live) break;
-    }
-    if (g >= g1) return false;
-    pos.g = g;
-    pos.t = t;
-    pos.s = 0;
-    pos.ns = x_n_steps(t);
-    ++pos.tcnt;
-  }
-  pos.st = x_step(pos.t, pos.s);
-  if (pos.st.new_fill) ++pos.fill;
-  ++pos.step;
-  return true;
+// Scales the fp32 columns [taddr, taddr + 32) of this thread's lane by a (warp-collective).
+__device__ __forceinline__ void x_scale_f32_cols(uint32_t taddr, float a) {
+  uint32_t v[32];
+  tmem_ld32(taddr, v);
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * a);
+  tmem_st32(taddr, v);
+}
+// Scales 32 columns of bf16 pairs by a (a power of two, so exactly; warp-collective).
+__device__ __forceinline__ void x_scale_bf16_cols(uint32_t taddr, float a) {
+  uint32_t v[32];
+  tmem_ld32(taddr, v);
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = pack_bf16x2(bf16lo_to_f32(v[i]) * a, bf16hi_to_f32(v[i]) * a);
+  tmem_st32(taddr, v);
 }
 
 template <int D>
@@ -217,8 +228,6 @@ __global__ void __launch_bounds__(kXThreads, 1)
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t s_base = smem_u32(smem);
   const uint32_t sQ = s_base + C::kOffQ, sK = s_base + C::kOffK, sV = s_base + C::kOffV;
-  const uint32_t sO = s_base + C::kOffO;
-  float* xch = reinterpret_cast<float*>(smem + C::kOffX);   // [wg][row]
   XBars* bars = reinterpret_cast<XBars*>(smem + C::kOffBar);
   int* len_s = reinterpret_cast<int*>(smem + C::kOffLen);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -232,19 +241,20 @@ __global__ void __launch_bounds__(kXThreads, 1)
   if (tid < kLenCache && tid < p.B) len_s[tid] = p.kv_len[tid];
   if (tid == 0) {
     bars->abort = 0;
-    mbar_init(smem_u32(&bars->q_full[0]), 1);
-    mbar_init(smem_u32(&bars->q_full[1]), 1);
-    mbar_init(smem_u32(&bars->q_empty[0]), 1);
-    mbar_init(smem_u32(&bars->q_empty[1]), 1);
+    for (int i = 0; i < kXQBufs; ++i) {
+      mbar_init(smem_u32(&bars->q_full[i]), 1);
+      mbar_init(smem_u32(&bars->q_empty[i]), 1);
+    }
     mbar_init(smem_u32(&bars->kv_full), 1);
     mbar_init(smem_u32(&bars->kv_ready), 1);
-    mbar_init(smem_u32(&bars->kv_empty), 1);
-    mbar_init(smem_u32(&bars->s_full), 1);
-    mbar_init(smem_u32(&bars->s_free), 8);
-    mbar_init(smem_u32(&bars->p_full), 8);
-    mbar_init(smem_u32(&bars->pv_done), 1);
-    mbar_init(smem_u32(&bars->o_free), 8);
-    mbar_init(smem_u32(&bars->drain), 1);
+    mbar_init(smem_u32(&bars->kv_empty), 2);   // one arrival per MMA issuer
+    for (int w = 0; w < 2; ++w) {
+      mbar_init(smem_u32(&bars->s_full[w]), 1);
+      mbar_init(smem_u32(&bars->p_full[w]), 4);
+      mbar_init(smem_u32(&bars->pv_done[w]), 1);
+      mbar_init(smem_u32(&bars->o_free[w]), 4);
+      mbar_init(smem_u32(&bars->drain[w]), 1);
+    }
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -263,150 +273,80 @@ __global__ void __launch_bounds__(kXThreads, 1)
   const uint32_t tbase = bars->tmem_base;
   const uint32_t b_kv_full = smem_u32(&bars->kv_full), b_kv_ready = smem_u32(&bars->kv_ready);
   const uint32_t b_kv_empty = smem_u32(&bars->kv_empty);
-  const uint32_t b_s_full = smem_u32(&bars->s_full), b_s_free = smem_u32(&bars->s_free);
-  const uint32_t b_p_full = smem_u32(&bars->p_full), b_pv_done = smem_u32(&bars->pv_done);
-  auto start_pos = [&]() {
-    XPos pos;
-    pos.g = g0 - 1;
-    pos.s = pos.ns = 0;
-    pos.tcnt = pos.fill = pos.step = -1;
-    return pos;
-  };
 
   if (warp < 4) {
     regs_dec<64>();
     if (warp == 0 && lane == 0) {
-      // ------------------------------------------------------------------ producer
-      int q_cnt = 0, fill = 0;
+      // ------------------------------------------------------------------ Q producer
+      int n = -1, issued = 0;
       bool ok = true;
       for (int g = g0; ok && g < g1; ++g) {
         const XTile t = x_decode(p, len_s, g, g0, g1);
         if (!t.live) continue;
-        // Q buffer q_cnt & 1: free once every S product of the tile before last has completed
-        const int buf = q_cnt & 1;
-        if (q_cnt >= 2 && !(ok = bounded_wait(smem_u32(&bars->q_empty[buf]), ((q_cnt - 2) >> 1) & 1, abort_flag,
-                                              status, kStatusTimeoutLoad)))
+        ++n;
+        const int buf = n % kXQBufs;
+        // The buffer is free once tile n - 3's output store has read it.
+        if (n >= kXQBufs && !(ok = bounded_wait(smem_u32(&bars->q_empty[buf]), (n / kXQBufs - 1) & 1, abort_flag,
+                                                 status, kStatusTimeoutLoad)))
           break;
         const uint32_t qb = smem_u32(&bars->q_full[buf]);
         mbar_arrive_expect_tx(qb, C::kTile);
 #pragma unroll
         for (int c = 0; c < C::kSub; ++c)
           tma_load_4d(sQ + buf * C::kTile + c * C::kChunk, &tm_q, qb, c * 64, t.h, t.qt * 128, t.b);
-        ++q_cnt;
-        // Warm L2 with the next two query tiles, so that each refill of the buffer is an L2 hit.
+        issued = n + 1;
+        // Warm L2 with the next two query tiles, so that each refill of a buffer is an L2 hit.
         for (int ga = g + 1; ga <= g + 2 && ga < g1; ++ga) {
           const XTile ta = x_decode(p, len_s, ga, g0, g1);
           if (ta.live)
 #pragma unroll
             for (int c = 0; c < C::kSub; ++c) tma_prefetch_l2_4d(&tm_q, c * 64, ta.h, ta.qt * 128, ta.b);
         }
-        for (int s = 0; ok && s < x_n_steps(t); ++s) {
-          const XStep st = x_step(t, s);
-          if (!st.new_fill) continue;
-          if (fill > 0 && !(ok = bounded_wait(b_kv_empty, (fill - 1) & 1, abort_flag, status, kStatusTimeoutLoad)))
-            break;
-          mbar_arrive_expect_tx(b_kv_full, 2 * st.nkt * C::kTile);
-          for (int j = 0; j < st.nkt; ++j) {
-            const int key0 = (st.kt0 + j) * 128;
-#pragma unroll
-            for (int c = 0; c < C::kSub; ++c) {
-              tma_load_4d(sK + c * 2 * C::kChunk + j * C::kChunk, &tm_k, b_kv_full, c * 64, t.h, key0, t.b);
-              tma_load_4d(sV + j * C::kTile + c * C::kChunk, &tm_v, b_kv_full, c * 64, t.h, key0, t.b);
-            }
-          }
-          ++fill;
-        }
       }
       // Let the copies in flight land before the CTA releases its shared memory (on the
       // normal path each has been waited for already, and these return at once).
-      for (int n = q_cnt - 2 > 0 ? q_cnt - 2 : 0; n < q_cnt; ++n)
-        drain_wait(smem_u32(&bars->q_full[n & 1]), (n >> 1) & 1, status);
-      if (fill > 0) drain_wait(b_kv_full, (fill - 1) & 1, status);
-    } else if (warp == 2 && lane == 0) {
-      // ------------------------------------------------------------------ MMA issuer
-      constexpr uint32_t kIdS1 = idesc_f16kind_f32(128, 128, true, false, false);
-      constexpr uint32_t kIdS2 = idesc_f16kind_f32(128, 256, true, false, false);
-      constexpr uint32_t kIdO = idesc_bf16_f32(128, D, false, true);
-      bool ok = true;
-      auto wait = [&](uint32_t bar, int phase) -> bool {
-        if (!bounded_wait(bar, phase & 1, abort_flag, status, kStatusTimeoutMma)) return false;
-        tc_fence_after_sync();
-        return true;
-      };
-      // S = Q K^T of one step into the S columns.
-      auto issue_s = [&](const XPos& x) -> bool {
-        const int buf = x.tcnt & 1;
-        if (x.s == 0 && !wait(smem_u32(&bars->q_full[buf]), x.tcnt >> 1)) return false;   // Q of the tile
-        if (!wait(b_kv_full, x.fill)) return false;                                       // its keys
-        if (x.step > 0 && !wait(b_s_free, x.step - 1)) return false;                       // previous S taken out
-        const uint64_t da = smem_desc_sw128(sQ + buf * C::kTile, 16, 1024);
-        const uint64_t db = smem_desc_sw128(sK, 16, 1024);
-        const uint32_t idS = x.st.nkt == 2 ? kIdS2 : kIdS1;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint64_t offa = ((kk / 4) * C::kChunk + (kk % 4) * 32) >> 4;
-          const uint64_t offb = ((kk / 4) * 2 * C::kChunk + (kk % 4) * 32) >> 4;
-          mma_bf16_ss(tbase, da + offa, db + offb, idS, kk > 0);
-        }
-        mma_commit(b_s_full);
-        if (x.s == x.ns - 1) mma_commit(smem_u32(&bars->q_empty[buf]));   // the tile's last S: Q may be reloaded
-        return true;
-      };
-      // O (+)= P V of one step, P from TMEM (bf16 pairs; keys 128 j .. of the step at columns
-      // 256 + 64 j ..).
-      auto issue_pv = [&](const XPos& x) -> bool {
-        if (!wait(b_p_full, x.step)) return false;
-        // the first step of a tile overwrites O: the previous tile's O has been read out
-        if (x.s == 0 && x.tcnt >= 1 && !wait(smem_u32(&bars->o_free), x.tcnt - 1)) return false;
-        if (!wait(b_kv_ready, x.fill)) return false;
-        const uint32_t d_o = tbase + kXColO;
-        for (int j = 0; j < x.st.nkt; ++j) {
-          const uint64_t dv = smem_desc_sw128(sV + j * C::kTile, C::kChunk, 1024);
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_bf16_ts(d_o, tbase + kXColP + j * 64 + kk * 8, dv + static_cast<uint64_t>(kk * 2048 >> 4), kIdO,
-                        (x.s > 0 || j > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(b_pv_done);
-        if (x.st.release) mma_commit(b_kv_empty);
-        return true;
-      };
-      XPos cur = start_pos();
-      if (x_next(p, len_s, g0, g1, cur)) {
-        ok = issue_s(cur);
-        while (ok) {
-          XPos nxt = cur;
-          const bool more = x_next(p, len_s, g0, g1, nxt);
-          // S of the next step first when it reads keys already in shared memory
-          const bool early = more && !nxt.st.new_fill;
-          if (early && !(ok = issue_s(nxt))) break;
-          if (!(ok = issue_pv(cur))) break;
-          if (!more) break;
-          if (!early && !(ok = issue_s(nxt))) break;
-          cur = nxt;
-        }
-      }
-      // Every MMA of this thread completes before TMEM and shared memory are released.
-      mma_commit(smem_u32(&bars->drain));
-      drain_wait(smem_u32(&bars->drain), 0, status);
-    } else if (warp == 3) {
-      // ------------------------------------------------------------------ V pad rows
-      int fill = 0;
+      for (int m = issued > kXQBufs ? issued - kXQBufs : 0; m < issued; ++m)
+        drain_wait(smem_u32(&bars->q_full[m % kXQBufs]), (m / kXQBufs) & 1, status);
+    } else if (warp == 1) {
+      // ------------------------------------------------------------------ fills + V pad rows
+      int e = 0;
       bool ok = true;
       for (int g = g0; ok && g < g1; ++g) {
         const XTile t = x_decode(p, len_s, g, g0, g1);
-        if (!t.live) continue;
-        for (int s = 0; ok && s < x_n_steps(t); ++s) {
-          const XStep st = x_step(t, s);
-          if (!st.new_fill) continue;
-          int got = 0;
-          if (lane == 0) got = bounded_wait(b_kv_full, fill & 1, abort_flag, status, kStatusTimeoutRope) ? 1 : 0;
-          if (!(ok = __shfl_sync(0xffffffffu, got, 0) != 0)) break;
-          const int jl = st.nkt - 1;                            // the fill's last V tile
-          const int nv = min(128, t.L - (st.kt0 + jl) * 128);   // its valid rows (>= 1)
+        if (!t.live || t.i != 0) continue;   // once per run, at its first tile
+        const int nf = x_run_fills(t);
+        for (int k = 0; k < nf; ++k, ++e) {
+          int kt0, cnt;
+          x_fill_tiles(t, k, kt0, cnt);
+          // 0: the previous fill was not released (nothing issued); 1: issued, not landed;
+          // 2: landed.
+          int got = 1;
+          if (lane == 0) {
+            if (e > 0 && !bounded_wait(b_kv_empty, (e - 1) & 1, abort_flag, status, kStatusTimeoutLoad)) {
+              got = 0;
+            } else {
+              mbar_arrive_expect_tx(b_kv_full, 2 * cnt * C::kTile);
+              for (int j = 0; j < cnt; ++j) {
+                const int key0 = (kt0 + j) * 128;
+#pragma unroll
+                for (int c = 0; c < C::kSub; ++c) {
+                  tma_load_4d(sK + c * 2 * C::kChunk + j * C::kChunk, &tm_k, b_kv_full, c * 64, t.h, key0, t.b);
+                  tma_load_4d(sV + j * C::kTile + c * C::kChunk, &tm_v, b_kv_full, c * 64, t.h, key0, t.b);
+                }
+              }
+              if (bounded_wait(b_kv_full, e & 1, abort_flag, status, kStatusTimeoutRope)) got = 2;
+              else drain_wait(b_kv_full, e & 1, status);   // the copies land before the CTA exits
+            }
+          }
+          if (__shfl_sync(0xffffffffu, got, 0) != 2) {
+            ok = false;
+            break;
+          }
+          const int jl = cnt - 1;                           // the fill's last V tile
+          const int nv = min(128, t.L - (kt0 + jl) * 128);  // its valid rows (>= 1)
           if (nv < 128) {
             const uint32_t tile = sV + jl * C::kTile;
-            const int n16 = (128 - nv) * 8;                     // 16-byte units per chunk
+            const int n16 = (128 - nv) * 8;                 // 16-byte units per chunk
             for (int c = 0; c < C::kSub; ++c)
               for (int u = lane; u < n16; u += 32)
                 asm volatile("st.shared.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(tile + c * C::kChunk + nv * 128 + u * 16),
@@ -416,89 +356,114 @@ __global__ void __launch_bounds__(kXThreads, 1)
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(b_kv_ready);
-          ++fill;
         }
       }
+    } else if (lane == 0) {
+      // ------------------------------------------------------------------ MMA issuers (warps 2, 3)
+      const int w = warp - 2;   // the softmax warpgroup served
+      constexpr uint32_t kIdS1 = idesc_f16kind_f32(128, 128, true, false, false);
+      constexpr uint32_t kIdS2 = idesc_f16kind_f32(128, 256, true, false, false);
+      constexpr uint32_t kIdO = idesc_bf16_f32(128, D, false, true);
+      const uint32_t region = tbase + static_cast<uint32_t>(w) * kXRegion;
+      const uint32_t b_s_full = smem_u32(&bars->s_full[w]), b_p_full = smem_u32(&bars->p_full[w]);
+      const uint32_t b_pv_done = smem_u32(&bars->pv_done[w]), b_o_free = smem_u32(&bars->o_free[w]);
+      bool ok = true;
+      auto wait = [&](uint32_t bar, int phase) -> bool {
+        if (!bounded_wait(bar, phase & 1, abort_flag, status, kStatusTimeoutMma)) return false;
+        tc_fence_after_sync();
+        return true;
+      };
+      int n = -1, k = 0, tcnt = 0, e_run = 0, e_total = 0, released = 0;
+      for (int g = g0; ok && g < g1; ++g) {
+        const XTile t = x_decode(p, len_s, g, g0, g1);
+        if (!t.live) continue;
+        ++n;
+        if (t.i == 0) {
+          e_run = e_total;
+          e_total += x_run_fills(t);
+        }
+        if ((n & 1) != w) continue;
+        const int buf = n % kXQBufs;
+        const int ns = x_n_steps(t);
+        for (int s = 0; ok && s < ns; ++s, ++k) {
+          const XStep st = x_step(t, s);
+          const int e = e_run + st.fill;
+          // Fills before e that this warpgroup does not read: arrive once each has landed.
+          while (ok && released < e) {
+            if (!(ok = wait(b_kv_full, released))) break;
+            mbar_arrive(b_kv_empty);
+            ++released;
+          }
+          if (!ok) break;
+          if (s == 0 && !(ok = wait(smem_u32(&bars->q_full[buf]), n / kXQBufs))) break;
+          if (!(ok = wait(b_kv_full, e))) break;
+          // The previous P V of this warpgroup is complete: its P columns may be overwritten.
+          if (k > 0 && !(ok = wait(b_pv_done, k - 1))) break;
+          // An S of 256 keys covers O's columns: the previous tile's O has been read out.
+          const bool s_over_o = st.nkt == 2;
+          if (s == 0 && tcnt > 0 && s_over_o && !(ok = wait(b_o_free, tcnt - 1))) break;
+          {
+            const uint64_t da = smem_desc_sw128(sQ + buf * C::kTile, 16, 1024);
+            const uint64_t db = smem_desc_sw128(sK + st.j0 * C::kChunk, 16, 1024);
+            const uint32_t idS = st.nkt == 2 ? kIdS2 : kIdS1;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint64_t offa = ((kk / 4) * C::kChunk + (kk % 4) * 32) >> 4;
+              const uint64_t offb = ((kk / 4) * 2 * C::kChunk + (kk % 4) * 32) >> 4;
+              mma_bf16_ss(region, da + offa, db + offb, idS, kk > 0);
+            }
+            mma_commit(b_s_full);
+          }
+          if (!(ok = wait(b_p_full, k))) break;
+          // The first P V of a tile overwrites O: the previous tile's O has been read out.
+          if (s == 0 && tcnt > 0 && !s_over_o && !(ok = wait(b_o_free, tcnt - 1))) break;
+          if (!(ok = wait(b_kv_ready, e))) break;
+          for (int j = 0; j < st.nkt; ++j) {
+            const uint64_t dv = smem_desc_sw128(sV + (st.j0 + j) * C::kTile, C::kChunk, 1024);
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_bf16_ts(region + kXColO, region + j * 64 + kk * 8, dv + static_cast<uint64_t>(kk * 2048 >> 4),
+                          kIdO, (s > 0 || j > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(b_pv_done);
+          // Release the fill after this warpgroup's last product on it: a pair's first half is
+          // the previous pair's second, read already; otherwise this warpgroup's next tile of
+          // the run (i + 2), if there is one, reads the same fill.
+          if (st.group_end && (st.first_half || t.i + 2 >= t.len)) {
+            mma_commit(b_kv_empty);
+            released = e + 1;
+          }
+        }
+        ++tcnt;
+      }
+      while (ok && released < e_total) {
+        if (!(ok = wait(b_kv_full, released))) break;
+        mbar_arrive(b_kv_empty);
+        ++released;
+      }
+      // Every MMA of this thread completes before TMEM and shared memory are released.
+      mma_commit(smem_u32(&bars->drain[w]));
+      drain_wait(smem_u32(&bars->drain[w]), 0, status);
     }
   } else {
     regs_inc<216>();
     // -------------------------------------------------------------------- softmax + epilogue
-    // The 256 threads of both warpgroups meet at named barriers (the row exchanges of a pair
-    // of warps, the end of each tile). So that a timeout can never leave a thread waiting at
-    // one of them, a thread whose bounded wait fails still runs every barrier of the current
-    // tile (skipping the tensor-memory work), and all 256 decide together, at the barrier that
-    // ends each tile, whether to go on.
-    const int wg = (warp - 4) >> 2;           // 0: key columns 0-127 of the S block, 1: 128-255
+    const int wg = (warp - 4) >> 2;            // warpgroup: tiles n with n & 1 == wg
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;         // query row within the tile = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t tS = tbase + lane_off + wg * 128;
-    const int pair_bar = 2 + quarter;          // named barrier of warps (4 + q, 8 + q)
-    float* x_mine = xch + wg * 128 + r;
-    const float* x_other = xch + (1 - wg) * 128 + r;
+    const uint32_t tR = tbase + lane_off + static_cast<uint32_t>(wg) * kXRegion;   // this row's region
+    const uint32_t b_s_full = smem_u32(&bars->s_full[wg]), b_p_full = smem_u32(&bars->p_full[wg]);
+    const uint32_t b_pv_done = smem_u32(&bars->pv_done[wg]), b_o_free = smem_u32(&bars->o_free[wg]);
+    const bool elected = quarter == 0 && lane == 0;   // issues this warpgroup's stores
     const float sl2 = p.scale_log2;
-    const uint32_t tP = tbase + lane_off + kXColP + wg * 64;   // this warpgroup's P columns
-    const uint32_t tO = tbase + lane_off + kXColO + wg * (D / 2);   // its O columns
     const uint32_t p_sw = static_cast<uint32_t>(r & 7);
-    // Bounded wait by lane 0, outcome broadcast to the warp.
     auto wwait = [&](uint32_t bar, int phase) -> bool {
       int got = 0;
       if (lane == 0) got = bounded_wait(bar, phase & 1, abort_flag, status, kStatusTimeoutSoftmax) ? 1 : 0;
       return __shfl_sync(0xffffffffu, got, 0) != 0;
     };
-    // The previous tile's output, read out of TMEM before P of the next tile is released.
-    bool pend = false;
-    int pend_b = 0, pend_h = 0, pend_qt = 0;
-    float pend_m = 0.f, pend_l = 1.f;
-    auto read_o = [&](uint32_t (&orr)[D / 2]) {
-#pragma unroll
-      for (int c = 0; c < D / 64; ++c) {
-        uint32_t part[32];
-        tmem_ld32(tO + c * 32, part);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) orr[c * 32 + i] = part[i];
-      }
-      tc_fence_before_sync();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_u32(&bars->o_free));   // O may be overwritten
-    };
-    // Normalise the read-out O, stage it in the 128-byte swizzle of the tile's TMA map and
-    // store the tile (one thread), and the LSE. All 256 threads call this.
-    auto store_o = [&](const uint32_t (&orr)[D / 2], bool ok_now) {
-      const int qrow = pend_qt * 128 + r;
-      const bool valid_row = qrow < p.q_valid;
-      const float inv_l = 1.f / pend_l;
-      if (tid == 128) bulk_wait_read();   // the previous store has read the staging tile
-      named_bar_sync(1, 256);
-#pragma unroll
-      for (int u = 0; u < D / 16; ++u) {
-        uint4 o = make_uint4(0, 0, 0, 0);
-        if (valid_row) {
-          const uint32_t* f = &orr[8 * u];
-          o.x = pack_bf16x2(__uint_as_float(f[0]) * inv_l, __uint_as_float(f[1]) * inv_l);
-          o.y = pack_bf16x2(__uint_as_float(f[2]) * inv_l, __uint_as_float(f[3]) * inv_l);
-          o.z = pack_bf16x2(__uint_as_float(f[4]) * inv_l, __uint_as_float(f[5]) * inv_l);
-          o.w = pack_bf16x2(__uint_as_float(f[6]) * inv_l, __uint_as_float(f[7]) * inv_l);
-        }
-        const int cu = wg * (D / 16) + u;   // 16-byte unit of the full row
-        const uint32_t addr = sO + static_cast<uint32_t>(cu >> 3) * C::kChunk + static_cast<uint32_t>(r) * 128u +
-                              ((static_cast<uint32_t>(cu & 7) ^ p_sw) << 4);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(o.x), "r"(o.y), "r"(o.z), "r"(o.w)
-                     : "memory");
-      }
-      fence_proxy_async_smem();
-      named_bar_sync(1, 256);
-      if (tid == 128 && ok_now) {
-#pragma unroll
-        for (int c = 0; c < C::kSub; ++c) tma_store_4d(&tm_o, sO + c * C::kChunk, c * 64, pend_h, pend_qt * 128, pend_b);
-        bulk_commit_group();
-      }
-      if (wg == 0 && ok_now)
-        p.lse[(static_cast<size_t>(pend_b) * p.Sq + qrow) * p.H + pend_h] =
-            valid_row ? (pend_m + log2f(pend_l)) * kXLn2 : -INFINITY;
-      pend = false;
-    };
-    int step = 0;
+    int n = -1, k = 0;
     bool ok = true;
     for (int g = g0; g < g1; ++g) {
       const XTile t = x_decode(p, len_s, g, g0, g1);
@@ -507,37 +472,31 @@ __global__ void __launch_bounds__(kXThreads, 1)
         if (t.bad && wg == 0 && r == 0) atomicOr(status, kStatusBadKvLength);
         continue;
       }
-      float m_run = -INFINITY, l_mine = 0.f;
+      ++n;
+      if ((n & 1) != wg) continue;
+      const int buf = n % kXQBufs;
+      float m_run = -INFINITY, l_run = 0.f;   // reference (an integer once set) and row sum
       const int ns = x_n_steps(t);
-      for (int s = 0; s < ns; ++s, ++step) {
+      for (int s = 0; s < ns; ++s, ++k) {
         const XStep st = x_step(t, s);
-        const bool mine = wg < st.nkt;
-        const int nv = mine ? min(128, t.L - (st.kt0 + wg) * 128) : 0;   // my valid keys
-        ok = ok && wwait(b_s_full, step);
+        ok = ok && wwait(b_s_full, k);
         if (ok) tc_fence_after_sync();
-        uint32_t sr[4][32];
-        float mx = -INFINITY;
-        if (ok && mine) {
+        for (int bb = 0; bb < st.nkt; ++bb) {
+          const int nv = min(128, t.L - (st.kt + bb) * 128);   // valid keys of this block (>= 1)
+          uint32_t sr[4][32];
+          if (ok) {
 #pragma unroll
-          for (int c = 0; c < 4; ++c) tmem_ld32_nowait(tS + c * 32, sr[c]);
-          tmem_ld_wait_tied(sr[0]);
-          tmem_reg_tie(sr[1]);
-          tmem_reg_tie(sr[2]);
-          tmem_reg_tie(sr[3]);
-        } else {
-          // No key tile of mine in this step (or the wait failed): defined values, all masked.
+            for (int c = 0; c < 4; ++c) tmem_ld32_nowait(tR + bb * 128 + c * 32, sr[c]);
+            tmem_ld_wait_tied(sr[0]);
+            tmem_reg_tie(sr[1]);
+            tmem_reg_tie(sr[2]);
+            tmem_reg_tie(sr[3]);
+          } else {
 #pragma unroll
-          for (int c = 0; c < 4; ++c)
+            for (int c = 0; c < 4; ++c)
 #pragma unroll
-            for (int i = 0; i < 32; ++i) sr[c][i] = 0xff800000u;
-        }
-        if (ok) {
-          // S is in registers: the next S product may overwrite the columns.
-          tc_fence_before_sync();
-          __syncwarp();
-          if (lane == 0) mbar_arrive(b_s_free);
-        }
-        if (ok && mine) {
+              for (int i = 0; i < 32; ++i) sr[c][i] = 0u;
+          }
           if (nv < 128) {
 #pragma unroll
             for (int c = 0; c < 4; ++c)
@@ -553,36 +512,27 @@ __global__ void __launch_bounds__(kXThreads, 1)
             for (int i = 2; i < 32; i += 2)
               mx4[c] = fmax3(mx4[c], __uint_as_float(sr[c][i]), __uint_as_float(sr[c][i + 1]));
           }
-          mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-        }
-        // Row maximum over both column blocks: exchange with the partner thread of this row
-        // (the first barrier: the partner has read the previous exchange).
-        named_bar_sync(pair_bar, 64);
-        *x_mine = mx;
-        named_bar_sync(pair_bar, 64);
-        const float mt = fmaxf(mx, *x_other) * sl2;
-        const bool resc = mt > m_run + kXRescale;
-        const float m_new = resc ? mt : m_run;
-        const float alpha = ex2_approx(m_run - m_new);   // 1 if kept; 0 on the first step
-        // The previous step's P V must be complete before P is rewritten and before O is read
-        // out or rescaled; both warpgroups take the same decision (same maxima).
-        if (step > 0) {
-          ok = ok && wwait(b_pv_done, step - 1);
-          if (ok) tc_fence_after_sync();
-        }
-        if (ok && s > 0 && __any_sync(0xffffffffu, resc)) {
-#pragma unroll
-          for (int c = 0; c < D / 64; ++c) {
-            uint32_t o32[32];
-            tmem_ld32(tO + c * 32, o32);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) o32[i] = __float_as_uint(__uint_as_float(o32[i]) * alpha);
-            tmem_st32(tO + c * 32, o32);
+          const float mt = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * sl2;
+          const bool first = s == 0 && bb == 0;
+          const bool grow = first || mt > m_run + kXRescale;
+          const float m_new = grow ? ceilf(mt) : m_run;
+          const float alpha = first ? 0.f : ex2_approx(m_run - m_new);   // a power of two
+          // What this row accumulated against the old reference moves to the new one: P of the
+          // product's earlier blocks, or O of the earlier steps (their P V is complete, since
+          // this step's S was issued after it).
+          if (ok && __any_sync(0xffffffffu, grow && !first)) {
+            const float a = (grow && !first) ? alpha : 1.f;
+            if (bb > 0) {
+              tmem_st_wait();
+#pragma unroll 1
+              for (int c = 0; c < bb * 2; ++c) x_scale_bf16_cols(tR + c * 32, a);
+            } else {
+#pragma unroll 1
+              for (int c = 0; c < D / 32; ++c) x_scale_f32_cols(tR + kXColO + c * 32, a);
+            }
           }
-        }
-        m_run = m_new;
-        float ls = 0.f;
-        if (ok && mine) {
+          l_run *= alpha;
+          m_run = m_new;
           const float neg_m = -m_run;
           float l4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -597,64 +547,73 @@ __global__ void __launch_bounds__(kXThreads, 1)
               add2(l4[2 * (i & 1)], l4[2 * (i & 1) + 1], p0, p1);
               pk[i] = pack_bf16x2(p0, p1);
             }
-            tmem_st8_nowait(tP + c * 8, pk);
+            if (ok) tmem_st8_nowait(tR + bb * 64 + c * 8, pk);
           }
-          ls = (l4[0] + l4[1]) + (l4[2] + l4[3]);
-          tmem_st_wait();
+          l_run += (l4[0] + l4[1]) + (l4[2] + l4[3]);
         }
-        l_mine = l_mine * alpha + ls;
-        // The previous tile's O is complete (its last P V was waited for above): take it out
-        // of TMEM before this step's P is released, since this P V overwrites O.
-        if (s == 0 && pend) {
-          uint32_t orr[D / 2];
-          if (ok) {
-            read_o(orr);
-          } else {
-#pragma unroll
-            for (int i = 0; i < D / 2; ++i) orr[i] = 0u;
-          }
-          if (ok) {
-            tc_fence_before_sync();   // P (tcgen05.st) before the P V
-            __syncwarp();
-            if (lane == 0) mbar_arrive(b_p_full);
-          }
-          store_o(orr, ok);   // staged and stored while this P V runs
-        } else if (ok) {
-          tc_fence_before_sync();   // P and the O rescale (tcgen05.st) before the P V
+        if (ok) {
+          tmem_st_wait();
+          tc_fence_before_sync();   // P (tcgen05.st) and any rescale before the P V
           __syncwarp();
           if (lane == 0) mbar_arrive(b_p_full);
         }
       }
-      // Row sum over both column blocks.
-      named_bar_sync(pair_bar, 64);
-      *x_mine = l_mine;
-      named_bar_sync(pair_bar, 64);
-      pend = true;
-      pend_b = t.b;
-      pend_h = t.h;
-      pend_qt = t.qt;
-      pend_m = m_run;
-      pend_l = l_mine + *x_other;
-      // Every one of the 256 threads got through this tile's waits.
-      if (!named_bar_and(1, 256, ok)) {
+      // Epilogue: O out of TMEM, normalised, staged in this tile's Q buffer, one TMA store.
+      uint32_t orr[D / 32][32];
+      ok = ok && wwait(b_pv_done, k - 1);
+      if (ok) {
+        tc_fence_after_sync();
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) tmem_ld32_nowait(tR + kXColO + c * 32, orr[c]);
+        tmem_ld_wait_tied(orr[0]);
+#pragma unroll
+        for (int c = 1; c < D / 32; ++c) tmem_reg_tie(orr[c]);
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(b_o_free);   // O may be overwritten
+      } else {
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) orr[c][i] = 0u;
+      }
+      const int qrow = t.qt * 128 + r;
+      const bool valid_row = qrow < p.q_valid;
+      const float inv_l = 1.f / l_run;
+      const uint32_t sO = sQ + buf * C::kTile;
+#pragma unroll
+      for (int u = 0; u < D / 8; ++u) {   // 16-byte units of the row
+        uint4 o = make_uint4(0, 0, 0, 0);
+        if (valid_row) {
+          const uint32_t* f = &orr[u >> 2][(u & 3) * 8];
+          o.x = pack_bf16x2(__uint_as_float(f[0]) * inv_l, __uint_as_float(f[1]) * inv_l);
+          o.y = pack_bf16x2(__uint_as_float(f[2]) * inv_l, __uint_as_float(f[3]) * inv_l);
+          o.z = pack_bf16x2(__uint_as_float(f[4]) * inv_l, __uint_as_float(f[5]) * inv_l);
+          o.w = pack_bf16x2(__uint_as_float(f[6]) * inv_l, __uint_as_float(f[7]) * inv_l);
+        }
+        const uint32_t addr = sO + static_cast<uint32_t>(u >> 3) * C::kChunk + static_cast<uint32_t>(r) * 128u +
+                              ((static_cast<uint32_t>(u & 7) ^ p_sw) << 4);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(o.x), "r"(o.y), "r"(o.z), "r"(o.w)
+                     : "memory");
+      }
+      fence_proxy_async_smem();
+      // Every thread of the warpgroup has staged its row and got through this tile's waits;
+      // otherwise all 128 stop here together.
+      if (!named_bar_and(1 + wg, 128, ok)) {
         ok = false;
         break;
       }
-    }
-    if (ok && pend) {
-      // the last tile: every thread passed the last tile-end barrier with ok
-      uint32_t orr[D / 2];
-      const bool got = wwait(b_pv_done, step - 1);
-      if (got) {
-        tc_fence_after_sync();
-        read_o(orr);
-      } else {
+      if (elected) {
 #pragma unroll
-        for (int i = 0; i < D / 2; ++i) orr[i] = 0u;
+        for (int c = 0; c < C::kSub; ++c) tma_store_4d(&tm_o, sO + c * C::kChunk, c * 64, t.h, t.qt * 128, t.b);
+        bulk_commit_group();
+        bulk_wait_read();                              // the store has read the buffer
+        mbar_arrive(smem_u32(&bars->q_empty[buf]));    // tile n + 3's Q may land in it
       }
-      store_o(orr, got);
+      p.lse[(static_cast<size_t>(t.b) * p.Sq + qrow) * p.H + t.h] =
+          valid_row ? (m_run + log2f(l_run)) * kXLn2 : -INFINITY;
     }
-    if (tid == 128) bulk_wait_all();
+    if (elected) bulk_wait_all();
   }
   __syncwarp();
   tc_fence_before_sync();
