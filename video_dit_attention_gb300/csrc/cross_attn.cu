@@ -41,19 +41,21 @@
 //     (log2 units) and is an integer: when a block's maximum exceeds m + kXRescale, m becomes
 //     its ceiling, and what the row has accumulated (P of earlier blocks of the same product,
 //     or O) is scaled by the power of two 2^(m_old - m_new), which is exact.
-//   - Epilogue: O is read out of TMEM, normalised, staged in the tile's own Q buffer (Q is
-//     dead once the tile's products have completed) in the 128-byte swizzle and written by one
-//     TMA store; the buffer goes back to the Q producer once the store has read it.
-//   - Roles: warp 0 loads Q (three buffers; the next two tiles are warmed in L2); warp 1 owns
+//   - Epilogue: O is read out of TMEM, normalised and staged in the tile's own Q buffer (Q is
+//     dead once the tile's products have completed) in the 128-byte swizzle. The Q loader
+//     writes it with one TMA store and, once the store has read the buffer, loads tile n + 3's
+//     Q into it; the softmax warps never wait for a store.
+//   - Warpgroup 1's first S waits for warpgroup 0's first S to complete, which puts the two
+//     chains out of phase: while one warpgroup exponentiates, the other's products run.
+//   - Roles: warp 0 loads Q and stores O (three buffers; the next two tiles are warmed in L2); warp 1 owns
 //     TMEM, loads the fills and zeroes the V rows past L_b of a fill's last V tile (so that
 //     0 * (pad contents) cannot reach O; K pad rows need nothing, their score columns are
 //     masked to -inf); warps 2 and 3 issue the MMAs of softmax warpgroups 0 and 1; warps 4-7
 //     and 8-11 are the two softmax warpgroups.
-// Every wait is bounded (ptx.cuh); on a timeout the CTA records a status bit, drains its
-// copies and MMAs, frees TMEM and exits. The only named barrier is each warpgroup's own
-// epilogue barrier, which every thread of the warpgroup reaches at each of its tiles (a
-// thread whose wait failed skips the tensor-memory work, not the barrier) and where the
-// 128 threads decide together whether to go on.
+// Every wait is bounded (ptx.cuh); on a timeout the CTA records a status bit, raises its
+// abort flag (the other roles' waits then give up at once), drains its copies and MMAs,
+// frees TMEM and exits. No named barrier is used after the set-up, so no thread can be left
+// waiting at one.
 
 #include <cuda_bf16.h>
 
@@ -87,10 +89,11 @@ struct XCfg {
 static_assert(XCfg<128>::kSmem <= 232448, "shared memory of the D = 128 cross kernel");
 
 struct XBars {
-  uint64_t q_full[kXQBufs], q_empty[kXQBufs];
+  uint64_t q_full[kXQBufs], o_staged[kXQBufs];
   uint64_t kv_full, kv_ready, kv_empty;
   uint64_t s_full[2], p_full[2], pv_done[2], o_free[2];
   uint64_t drain[2];
+  uint64_t started;   // warpgroup 0's first S is complete (one phase only)
   uint32_t tmem_base;
   int abort;
 };
@@ -107,37 +110,82 @@ struct XParams {
   unsigned int* status;
 };
 
-// One query tile of the CTA's range and where it sits in its run (the live tiles of its
+// One live query tile of the CTA's range and where it sits in its run (the live tiles of its
 // (b, h) inside the range, which are consecutive).
 struct XTile {
   int b, h, qt;
-  int L;        // valid keys (0 for a bad or empty length)
+  int L;        // valid keys (>= 1)
   int n_kv;     // 128-key tiles holding them
-  bool live;    // has a valid query row and at least one key
-  bool bad;     // the batch's length was outside [0, Skv]
   int i;        // index of this tile in its run
   int len;      // live tiles in the run
 };
 
-// Every role decodes every tile of its range; the key lengths of the first kLenCache batches
-// are read from shared memory (a global load per tile sat on the MMA issuer's critical path).
-__device__ __forceinline__ XTile x_decode(const XParams& p, const int* len_s, int g, int g0, int g1) {
-  XTile t;
-  const int bh = g / p.n_qt;
-  t.qt = g - bh * p.n_qt;
-  t.b = bh / p.H;
-  t.h = bh - t.b * p.H;
-  const int raw = t.b < kLenCache ? len_s[t.b] : p.kv_len[t.b];
-  t.bad = raw < 0 || raw > p.Skv;
-  t.L = t.bad ? 0 : raw;
-  t.n_kv = (t.L + 127) >> 7;
+// Walks the CTA's range [g0, g1) of flat tiles head by head, with the coordinates kept
+// incrementally (the threads that issue MMAs and loads share their schedulers with busy
+// softmax warps, so a per-tile decode with divisions sat on the critical path). The key
+// lengths of the first kLenCache batches are read from shared memory.
+struct XWalk {
+  int g, g1;          // next flat tile and the end of the range
+  int b, h, qt;       // coordinates of flat tile g
+  int L, n_kv;        // key length of batch b (0 for a bad or empty length)
+  bool bad;           // batch b's length lies outside [0, Skv]
+  int qt_first;       // first tile of the current head inside the range
+  int run_len;        // live tiles of the current head inside the range
+};
+__device__ __forceinline__ void x_walk_head(XWalk& w, const XParams& p, const int* len_s) {
+  const int raw = w.b < kLenCache ? len_s[w.b] : p.kv_len[w.b];
+  w.bad = raw < 0 || raw > p.Skv;
+  w.L = w.bad ? 0 : raw;
+  w.n_kv = (w.L + 127) >> 7;
+  w.qt_first = w.qt;
   const int n_live_qt = (p.q_valid + 127) >> 7;   // live tiles are a prefix of each head
-  t.live = t.L > 0 && t.qt < n_live_qt;
-  const int qt_first = (g0 / p.n_qt == bh) ? g0 - bh * p.n_qt : 0;
-  const int qt_end = min(min(g1, (bh + 1) * p.n_qt) - bh * p.n_qt, n_live_qt);   // one past the run
-  t.i = t.qt - qt_first;
-  t.len = qt_end - qt_first;
-  return t;
+  const int end_qt = min(p.n_qt, w.qt + (w.g1 - w.g));
+  w.run_len = w.L > 0 ? max(0, min(end_qt, n_live_qt) - w.qt) : 0;
+}
+__device__ __forceinline__ void x_walk_init(XWalk& w, const XParams& p, const int* len_s, int g0, int g1) {
+  w.g = g0;
+  w.g1 = g1;
+  const int bh = g0 / p.n_qt;
+  w.qt = g0 - bh * p.n_qt;
+  w.b = bh / p.H;
+  w.h = bh - w.b * p.H;
+  if (g0 < g1) x_walk_head(w, p, len_s);
+}
+// To the first tile of the next head.
+__device__ __forceinline__ void x_walk_next_head(XWalk& w, const XParams& p, const int* len_s) {
+  w.g += p.n_qt - w.qt;
+  w.qt = 0;
+  if (++w.h == p.H) {
+    w.h = 0;
+    ++w.b;
+  }
+  if (w.g < w.g1) x_walk_head(w, p, len_s);
+}
+// The next live tile of the range; false at its end.
+__device__ __forceinline__ bool x_walk_next(XWalk& w, const XParams& p, const int* len_s, XTile& t) {
+  while (w.g < w.g1) {
+    if (w.qt - w.qt_first < w.run_len) {
+      t.b = w.b;
+      t.h = w.h;
+      t.qt = w.qt;
+      t.L = w.L;
+      t.n_kv = w.n_kv;
+      t.i = w.qt - w.qt_first;
+      t.len = w.run_len;
+      ++w.g;
+      if (++w.qt == p.n_qt) {
+        w.qt = 0;
+        if (++w.h == p.H) {
+          w.h = 0;
+          ++w.b;
+        }
+        if (w.g < w.g1) x_walk_head(w, p, len_s);
+      }
+      return true;
+    }
+    x_walk_next_head(w, p, len_s);
+  }
+  return false;
 }
 
 // Fills of a run: one when n_kv <= 2, else pairs + 1 (fill k holds key half k & 1).
@@ -192,12 +240,44 @@ __device__ __forceinline__ XStep x_step(const XTile& t, int s) {
 // O = 0 and LSE = -inf for one tile's rows (columns [c0, c0 + D/2) of O by this warpgroup;
 // the LSE by warpgroup 0), written directly.
 template <int D>
-__device__ __forceinline__ void x_write_empty(const XParams& p, const XTile& t, int wg, int r) {
-  const int row = t.qt * 128 + r;
-  uint16_t* dst = p.out + ((static_cast<size_t>(t.b) * p.Sq + row) * p.H + t.h) * D + wg * (D / 2);
+__device__ __forceinline__ void x_write_empty(const XParams& p, int b, int h, int qt, int wg, int r) {
+  const int row = qt * 128 + r;
+  uint16_t* dst = p.out + ((static_cast<size_t>(b) * p.Sq + row) * p.H + h) * D + wg * (D / 2);
 #pragma unroll
   for (int u = 0; u < D / 16; ++u) reinterpret_cast<uint4*>(dst)[u] = make_uint4(0, 0, 0, 0);
-  if (wg == 0) p.lse[(static_cast<size_t>(t.b) * p.Sq + row) * p.H + t.h] = -INFINITY;
+  if (wg == 0) p.lse[(static_cast<size_t>(b) * p.Sq + row) * p.H + h] = -INFINITY;
+}
+
+// Non-blocking test of a phase (the thread is never suspended): true once the phase with this
+// parity has completed.
+__device__ __forceinline__ bool x_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// bounded_wait (ptx.cuh) by polling: the MMA issuers wait this way, so that each resumes as
+// soon as the phase completes.
+__device__ __forceinline__ bool x_poll(uint32_t bar, uint32_t parity, volatile int* cta_abort, unsigned int* dev_status,
+                                       unsigned int code) {
+  if (x_test_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (x_test_wait(bar, parity)) return true;
+    if ((it & 63u) == 0) {
+      if (*cta_abort) return false;
+      if (globaltimer_ns() - t0 > wait_limit_ns()) {
+        *cta_abort = 1;
+        atomicOr(dev_status, code);
+        return false;
+      }
+    }
+  }
 }
 
 // Scales the fp32 columns [taddr, taddr + 32) of this thread's lane by a (warp-collective).
@@ -243,7 +323,7 @@ __global__ void __launch_bounds__(kXThreads, 1)
     bars->abort = 0;
     for (int i = 0; i < kXQBufs; ++i) {
       mbar_init(smem_u32(&bars->q_full[i]), 1);
-      mbar_init(smem_u32(&bars->q_empty[i]), 1);
+      mbar_init(smem_u32(&bars->o_staged[i]), 4);   // the four warps of the tile's warpgroup
     }
     mbar_init(smem_u32(&bars->kv_full), 1);
     mbar_init(smem_u32(&bars->kv_ready), 1);
@@ -255,6 +335,7 @@ __global__ void __launch_bounds__(kXThreads, 1)
       mbar_init(smem_u32(&bars->o_free[w]), 4);
       mbar_init(smem_u32(&bars->drain[w]), 1);
     }
+    mbar_init(smem_u32(&bars->started), 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -277,33 +358,51 @@ __global__ void __launch_bounds__(kXThreads, 1)
   if (warp < 4) {
     regs_dec<64>();
     if (warp == 0 && lane == 0) {
-      // ------------------------------------------------------------------ Q producer
-      int n = -1, issued = 0;
+      // ------------------------------------------------------------------ Q loads, O stores
+      // Tile n's Q lands in buffer n % 3, and its O is staged there by its warpgroup; this
+      // thread stores it, and once the store has read the buffer, loads tile n + 3's Q into it.
+      int n = -1, issued = 0, stored = 0;
+      int cb[kXQBufs] = {}, ch[kXQBufs] = {}, cq[kXQBufs] = {};   // coordinates of each buffer's tile
       bool ok = true;
-      for (int g = g0; ok && g < g1; ++g) {
-        const XTile t = x_decode(p, len_s, g, g0, g1);
-        if (!t.live) continue;
+      auto store = [&](int m) -> bool {   // tile m's O, once its warpgroup has staged it
+        const int b = m % kXQBufs;
+        if (!bounded_wait(smem_u32(&bars->o_staged[b]), (m / kXQBufs) & 1, abort_flag, status, kStatusTimeoutLoad))
+          return false;
+#pragma unroll
+        for (int c = 0; c < C::kSub; ++c) tma_store_4d(&tm_o, sQ + b * C::kTile + c * C::kChunk, c * 64, ch[b], cq[b], cb[b]);
+        bulk_commit_group();
+        stored = m + 1;
+        return true;
+      };
+      XWalk w, ahead;
+      x_walk_init(w, p, len_s, g0, g1);
+      ahead = w;
+      XTile t, ta;
+      for (int i = 0; i < 2; ++i) x_walk_next(ahead, p, len_s, ta);   // two tiles ahead of w
+      while (ok && x_walk_next(w, p, len_s, t)) {
         ++n;
         const int buf = n % kXQBufs;
-        // The buffer is free once tile n - 3's output store has read it.
-        if (n >= kXQBufs && !(ok = bounded_wait(smem_u32(&bars->q_empty[buf]), (n / kXQBufs - 1) & 1, abort_flag,
-                                                 status, kStatusTimeoutLoad)))
-          break;
+        if (n >= kXQBufs) {
+          if (!(ok = store(n - kXQBufs))) break;
+          bulk_wait_read();   // the buffer has been read out
+        }
         const uint32_t qb = smem_u32(&bars->q_full[buf]);
         mbar_arrive_expect_tx(qb, C::kTile);
 #pragma unroll
         for (int c = 0; c < C::kSub; ++c)
           tma_load_4d(sQ + buf * C::kTile + c * C::kChunk, &tm_q, qb, c * 64, t.h, t.qt * 128, t.b);
+        cb[buf] = t.b;
+        ch[buf] = t.h;
+        cq[buf] = t.qt * 128;
         issued = n + 1;
-        // Warm L2 with the next two query tiles, so that each refill of a buffer is an L2 hit.
-        for (int ga = g + 1; ga <= g + 2 && ga < g1; ++ga) {
-          const XTile ta = x_decode(p, len_s, ga, g0, g1);
-          if (ta.live)
+        // Warm L2 with the tile two ahead, so that each refill of a buffer is an L2 hit.
+        if (x_walk_next(ahead, p, len_s, ta))
 #pragma unroll
-            for (int c = 0; c < C::kSub; ++c) tma_prefetch_l2_4d(&tm_q, c * 64, ta.h, ta.qt * 128, ta.b);
-        }
+          for (int c = 0; c < C::kSub; ++c) tma_prefetch_l2_4d(&tm_q, c * 64, ta.h, ta.qt * 128, ta.b);
       }
-      // Let the copies in flight land before the CTA releases its shared memory (on the
+      for (int m = stored; ok && m < issued; ++m) ok = store(m);
+      bulk_wait_all();
+      // Let the loads in flight land before the CTA releases its shared memory (on the
       // normal path each has been waited for already, and these return at once).
       for (int m = issued > kXQBufs ? issued - kXQBufs : 0; m < issued; ++m)
         drain_wait(smem_u32(&bars->q_full[m % kXQBufs]), (m / kXQBufs) & 1, status);
@@ -311,9 +410,11 @@ __global__ void __launch_bounds__(kXThreads, 1)
       // ------------------------------------------------------------------ fills + V pad rows
       int e = 0;
       bool ok = true;
-      for (int g = g0; ok && g < g1; ++g) {
-        const XTile t = x_decode(p, len_s, g, g0, g1);
-        if (!t.live || t.i != 0) continue;   // once per run, at its first tile
+      XWalk w;
+      x_walk_init(w, p, len_s, g0, g1);
+      XTile t;
+      while (ok && x_walk_next(w, p, len_s, t)) {
+        if (t.i != 0) continue;   // once per run, at its first tile
         const int nf = x_run_fills(t);
         for (int k = 0; k < nf; ++k, ++e) {
           int kt0, cnt;
@@ -368,15 +469,17 @@ __global__ void __launch_bounds__(kXThreads, 1)
       const uint32_t b_s_full = smem_u32(&bars->s_full[w]), b_p_full = smem_u32(&bars->p_full[w]);
       const uint32_t b_pv_done = smem_u32(&bars->pv_done[w]), b_o_free = smem_u32(&bars->o_free[w]);
       bool ok = true;
+      // Polled waits: the issuer resumes as soon as the phase completes.
       auto wait = [&](uint32_t bar, int phase) -> bool {
-        if (!bounded_wait(bar, phase & 1, abort_flag, status, kStatusTimeoutMma)) return false;
+        if (!x_poll(bar, phase & 1, abort_flag, status, kStatusTimeoutMma)) return false;
         tc_fence_after_sync();
         return true;
       };
       int n = -1, k = 0, tcnt = 0, e_run = 0, e_total = 0, released = 0;
-      for (int g = g0; ok && g < g1; ++g) {
-        const XTile t = x_decode(p, len_s, g, g0, g1);
-        if (!t.live) continue;
+      XWalk wk;
+      x_walk_init(wk, p, len_s, g0, g1);
+      XTile t;
+      while (ok && x_walk_next(wk, p, len_s, t)) {
         ++n;
         if (t.i == 0) {
           e_run = e_total;
@@ -402,6 +505,9 @@ __global__ void __launch_bounds__(kXThreads, 1)
           // An S of 256 keys covers O's columns: the previous tile's O has been read out.
           const bool s_over_o = st.nkt == 2;
           if (s == 0 && tcnt > 0 && s_over_o && !(ok = wait(b_o_free, tcnt - 1))) break;
+          // Warpgroup 1 starts once warpgroup 0's first S is complete, so that the two chains
+          // run out of phase: one warpgroup's softmax while the other's products run.
+          if (w == 1 && k == 0 && !(ok = wait(smem_u32(&bars->started), 0))) break;
           {
             const uint64_t da = smem_desc_sw128(sQ + buf * C::kTile, 16, 1024);
             const uint64_t db = smem_desc_sw128(sK + st.j0 * C::kChunk, 16, 1024);
@@ -413,6 +519,7 @@ __global__ void __launch_bounds__(kXThreads, 1)
               mma_bf16_ss(region, da + offa, db + offb, idS, kk > 0);
             }
             mma_commit(b_s_full);
+            if (w == 0 && k == 0) mma_commit(smem_u32(&bars->started));
           }
           if (!(ok = wait(b_p_full, k))) break;
           // The first P V of a tile overwrites O: the previous tile's O has been read out.
@@ -455,7 +562,6 @@ __global__ void __launch_bounds__(kXThreads, 1)
     const uint32_t tR = tbase + lane_off + static_cast<uint32_t>(wg) * kXRegion;   // this row's region
     const uint32_t b_s_full = smem_u32(&bars->s_full[wg]), b_p_full = smem_u32(&bars->p_full[wg]);
     const uint32_t b_pv_done = smem_u32(&bars->pv_done[wg]), b_o_free = smem_u32(&bars->o_free[wg]);
-    const bool elected = quarter == 0 && lane == 0;   // issues this warpgroup's stores
     const float sl2 = p.scale_log2;
     const uint32_t p_sw = static_cast<uint32_t>(r & 7);
     auto wwait = [&](uint32_t bar, int phase) -> bool {
@@ -463,15 +569,21 @@ __global__ void __launch_bounds__(kXThreads, 1)
       if (lane == 0) got = bounded_wait(bar, phase & 1, abort_flag, status, kStatusTimeoutSoftmax) ? 1 : 0;
       return __shfl_sync(0xffffffffu, got, 0) != 0;
     };
-    int n = -1, k = 0;
+    XWalk w;
+    x_walk_init(w, p, len_s, g0, g1);
+    // Tiles of the range with no valid query row or no key: O = 0, LSE = -inf, written
+    // directly while the first products are on their way; a bad key length is reported.
+    while (w.g < w.g1) {
+      const int end_qt = min(p.n_qt, w.qt + (w.g1 - w.g));
+      if (w.bad && wg == 0 && r == 0) atomicOr(status, kStatusBadKvLength);
+      for (int qt = w.qt_first + w.run_len; qt < end_qt; ++qt) x_write_empty<D>(p, w.b, w.h, qt, wg, r);
+      x_walk_next_head(w, p, len_s);
+    }
+    x_walk_init(w, p, len_s, g0, g1);
+    int n = -1, k = 0, tcnt = 0;
     bool ok = true;
-    for (int g = g0; g < g1; ++g) {
-      const XTile t = x_decode(p, len_s, g, g0, g1);
-      if (!t.live) {
-        x_write_empty<D>(p, t, wg, r);
-        if (t.bad && wg == 0 && r == 0) atomicOr(status, kStatusBadKvLength);
-        continue;
-      }
+    XTile t;
+    while (x_walk_next(w, p, len_s, t)) {
       ++n;
       if ((n & 1) != wg) continue;
       const int buf = n % kXQBufs;
@@ -481,38 +593,30 @@ __global__ void __launch_bounds__(kXThreads, 1)
         const XStep st = x_step(t, s);
         ok = ok && wwait(b_s_full, k);
         if (ok) tc_fence_after_sync();
+        // Each 128-key block in two passes over its TMEM columns, 32 at a time (small loops
+        // keep the code that the softmax warps run between tiles in the instruction cache):
+        // the block's row maximum, then the exponentials, their sum and P.
         for (int bb = 0; bb < st.nkt; ++bb) {
           const int nv = min(128, t.L - (st.kt + bb) * 128);   // valid keys of this block (>= 1)
-          uint32_t sr[4][32];
+          const uint32_t tS = tR + bb * 128;
+          float mx = -INFINITY;
           if (ok) {
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+              uint32_t v[32];
+              tmem_ld32(tS + c * 32, v);
+              const int lim = nv - c * 32;   // valid columns of this chunk
+              float m0 = -INFINITY, m1 = -INFINITY;
 #pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_ld32_nowait(tR + bb * 128 + c * 32, sr[c]);
-            tmem_ld_wait_tied(sr[0]);
-            tmem_reg_tie(sr[1]);
-            tmem_reg_tie(sr[2]);
-            tmem_reg_tie(sr[3]);
-          } else {
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-#pragma unroll
-              for (int i = 0; i < 32; ++i) sr[c][i] = 0u;
+              for (int i = 0; i < 32; i += 4) {
+                m0 = fmax3(m0, i < lim ? __uint_as_float(v[i]) : -INFINITY, i + 1 < lim ? __uint_as_float(v[i + 1]) : -INFINITY);
+                m1 = fmax3(m1, i + 2 < lim ? __uint_as_float(v[i + 2]) : -INFINITY,
+                           i + 3 < lim ? __uint_as_float(v[i + 3]) : -INFINITY);
+              }
+              mx = fmax3(mx, m0, m1);
+            }
           }
-          if (nv < 128) {
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-#pragma unroll
-              for (int i = 0; i < 32; ++i)
-                if (c * 32 + i >= nv) sr[c][i] = 0xff800000u;
-          }
-          float mx4[4];
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            mx4[c] = fmaxf(__uint_as_float(sr[c][0]), __uint_as_float(sr[c][1]));
-#pragma unroll
-            for (int i = 2; i < 32; i += 2)
-              mx4[c] = fmax3(mx4[c], __uint_as_float(sr[c][i]), __uint_as_float(sr[c][i + 1]));
-          }
-          const float mt = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * sl2;
+          const float mt = mx * sl2;
           const bool first = s == 0 && bb == 0;
           const bool grow = first || mt > m_run + kXRescale;
           const float m_new = grow ? ceilf(mt) : m_run;
@@ -535,19 +639,26 @@ __global__ void __launch_bounds__(kXThreads, 1)
           m_run = m_new;
           const float neg_m = -m_run;
           float l4[4] = {0.f, 0.f, 0.f, 0.f};
+          if (ok) {
+            // P of chunk c goes to columns 64 bb + 16 c .. + 15, which hold S this thread has
+            // already read (of this block's chunks <= c, or of block 0 for block 1).
+#pragma unroll 1
+            for (int c = 0; c < 4; ++c) {
+              uint32_t v[32];
+              tmem_ld32(tS + c * 32, v);
+              const int lim = nv - c * 32;
+              uint32_t pk[16];
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {   // 16 keys at a time: 8 bf16 pairs, 8 TMEM columns
-            uint32_t pk[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              float x0, x1;
-              fma2_bc(x0, x1, __uint_as_float(sr[c >> 1][(c & 1) * 16 + 2 * i]),
-                      __uint_as_float(sr[c >> 1][(c & 1) * 16 + 2 * i + 1]), sl2, neg_m);
-              const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-              add2(l4[2 * (i & 1)], l4[2 * (i & 1) + 1], p0, p1);
-              pk[i] = pack_bf16x2(p0, p1);
+              for (int i = 0; i < 16; ++i) {
+                float x0, x1;
+                fma2_bc(x0, x1, __uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]), sl2, neg_m);
+                const float p0 = 2 * i < lim ? ex2_approx(x0) : 0.f;
+                const float p1 = 2 * i + 1 < lim ? ex2_approx(x1) : 0.f;
+                add2(l4[2 * (i & 1)], l4[2 * (i & 1) + 1], p0, p1);
+                pk[i] = pack_bf16x2(p0, p1);
+              }
+              tmem_st16_nowait(tR + bb * 64 + c * 16, pk);
             }
-            if (ok) tmem_st8_nowait(tR + bb * 64 + c * 8, pk);
           }
           l_run += (l4[0] + l4[1]) + (l4[2] + l4[3]);
         }
@@ -558,7 +669,8 @@ __global__ void __launch_bounds__(kXThreads, 1)
           if (lane == 0) mbar_arrive(b_p_full);
         }
       }
-      // Epilogue: O out of TMEM, normalised, staged in this tile's Q buffer, one TMA store.
+      // Epilogue: O out of TMEM, normalised, staged in this tile's Q buffer (the Q loader
+      // stores it).
       uint32_t orr[D / 32][32];
       ok = ok && wwait(b_pv_done, k - 1);
       if (ok) {
@@ -596,24 +708,14 @@ __global__ void __launch_bounds__(kXThreads, 1)
         asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(o.x), "r"(o.y), "r"(o.z), "r"(o.w)
                      : "memory");
       }
-      fence_proxy_async_smem();
-      // Every thread of the warpgroup has staged its row and got through this tile's waits;
-      // otherwise all 128 stop here together.
-      if (!named_bar_and(1 + wg, 128, ok)) {
-        ok = false;
-        break;
-      }
-      if (elected) {
-#pragma unroll
-        for (int c = 0; c < C::kSub; ++c) tma_store_4d(&tm_o, sO + c * C::kChunk, c * 64, t.h, t.qt * 128, t.b);
-        bulk_commit_group();
-        bulk_wait_read();                              // the store has read the buffer
-        mbar_arrive(smem_u32(&bars->q_empty[buf]));    // tile n + 3's Q may land in it
-      }
+      fence_proxy_async_smem();   // the staged row, before the store (async proxy) reads it
+      __syncwarp();
+      if (!ok) break;
+      if (lane == 0) mbar_arrive(smem_u32(&bars->o_staged[buf]));
       p.lse[(static_cast<size_t>(t.b) * p.Sq + qrow) * p.H + t.h] =
           valid_row ? (m_run + log2f(l_run)) * kXLn2 : -INFINITY;
+      ++tcnt;
     }
-    if (elected) bulk_wait_all();
   }
   __syncwarp();
   tc_fence_before_sync();
