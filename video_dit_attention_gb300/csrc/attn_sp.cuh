@@ -652,54 +652,97 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool resc = mt > m_used + (kFp8 ? kFp8RescaleThreshold : kRescaleThreshold);
         const float m_new = resc ? mt : m_used;
         const float alpha = ex2_approx(m_used - m_new);   // 1 if kept; 0 on the first tile
-        if (j > 0) {
-          // P_t,j-1 V_j-1 must be complete before O_t is rescaled and before P_t is rewritten.
-          if (!warp_wait(b_pv_done, (sc - 1) & 1, abort_flag, status, kStatusTimeoutSoftmax)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after_sync();
-          if (__any_sync(0xffffffffu, resc)) {
+        if constexpr (kFp8) {
+          // FP8: P_t,j is computed into registers first; only its store into the P_t buffer (and
+          // the rescale of O_t) waits for P_t,j-1 V_j-1, so the exponentials overlap that
+          // product (861 -> 1009 TFLOP/s at Wan 480; the bf16 modes measured 10 % slower this way).
+          const float neg_m = -m_new;
+          float l4[4];
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-              uint32_t orr[32];
-              tmem_ld32(tO + c * 32, orr);
+          for (int k = 0; k < 4; ++k) l4[k] = 0.f;
+          uint32_t pk[8][4];   // 16 keys per c: four e4m3 quads
 #pragma unroll
-              for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
-              tmem_st32(tO + c * 32, orr);
+          for (int c = 0; c < 8; ++c) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              float x0, x1;
+              fma2_bc(x0, x1, __uint_as_float(sr[c >> 1][(c & 1) * 16 + 2 * i]),
+                      __uint_as_float(sr[c >> 1][(c & 1) * 16 + 2 * i + 1]), sl2e, neg_m);
+              const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+              add2(l4[2 * (i & 1)], l4[2 * (i & 1) + 1], p0, p1);
+              const uint32_t e = pack_e4m3x2(kFp8PScale * p0, kFp8PScale * p1);
+              if (i & 1)
+                pk[c][i >> 1] |= e << 16;
+              else
+                pk[c][i >> 1] = e;
             }
           }
-        }
-        m_used = m_new;
-        const float neg_m = -m_used;
-        float l4[4];
+          if (j > 0) {
+            // P_t,j-1 V_j-1 must be complete before O_t is rescaled and before P_t is rewritten.
+            if (!warp_wait(b_pv_done, (sc - 1) & 1, abort_flag, status, kStatusTimeoutSoftmax)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after_sync();
+            if (__any_sync(0xffffffffu, resc)) {
 #pragma unroll
-        for (int k = 0; k < 4; ++k) l4[k] = 0.f;
+              for (int c = 0; c < D / 32; ++c) {
+                uint32_t orr[32];
+                tmem_ld32(tO + c * 32, orr);
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {           // 16 keys at a time: two 16-byte units (bf16)
-          uint32_t pk[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            float x0, x1;
-            fma2_bc(x0, x1, __uint_as_float(sr[c >> 1][(c & 1) * 16 + 2 * i]),
-                    __uint_as_float(sr[c >> 1][(c & 1) * 16 + 2 * i + 1]), sl2e, neg_m);
-            const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
-            add2(l4[2 * (i & 1)], l4[2 * (i & 1) + 1], p0, p1);
-            pk[i] = kFp8 ? pack_e4m3x2(kFp8PScale * p0, kFp8PScale * p1) : pack_bf16x2(p0, p1);
+                for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
+                tmem_st32(tO + c * 32, orr);
+              }
+            }
           }
-          if constexpr (kFp8) {
-            // 16 e4m3 keys: one 16-byte unit of the single 128-byte P row.
-            sts128(p_row + ((static_cast<uint32_t>(c) ^ p_sw) << 4),
-                   make_uint4(pk[0] | (pk[1] << 16), pk[2] | (pk[3] << 16), pk[4] | (pk[5] << 16),
-                              pk[6] | (pk[7] << 16)));
-          } else {
+          m_used = m_new;
+#pragma unroll
+          for (int c = 0; c < 8; ++c)   // 16 e4m3 keys: one 16-byte unit of the single 128-byte P row
+            sts128(p_row + ((static_cast<uint32_t>(c) ^ p_sw) << 4), make_uint4(pk[c][0], pk[c][1], pk[c][2], pk[c][3]));
+          l = l * alpha + ((l4[0] + l4[1]) + (l4[2] + l4[3]));
+        } else {
+          if (j > 0) {
+            // P_t,j-1 V_j-1 must be complete before O_t is rescaled and before P_t is rewritten.
+            if (!warp_wait(b_pv_done, (sc - 1) & 1, abort_flag, status, kStatusTimeoutSoftmax)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after_sync();
+            if (__any_sync(0xffffffffu, resc)) {
+#pragma unroll
+              for (int c = 0; c < D / 32; ++c) {
+                uint32_t orr[32];
+                tmem_ld32(tO + c * 32, orr);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) orr[i] = __float_as_uint(__uint_as_float(orr[i]) * alpha);
+                tmem_st32(tO + c * 32, orr);
+              }
+            }
+          }
+          m_used = m_new;
+          const float neg_m = -m_used;
+          float l4[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) l4[k] = 0.f;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {           // 16 keys at a time: two 16-byte units (bf16)
+            uint32_t pk[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              float x0, x1;
+              fma2_bc(x0, x1, __uint_as_float(sr[c >> 1][(c & 1) * 16 + 2 * i]),
+                      __uint_as_float(sr[c >> 1][(c & 1) * 16 + 2 * i + 1]), sl2e, neg_m);
+              const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+              add2(l4[2 * (i & 1)], l4[2 * (i & 1) + 1], p0, p1);
+              pk[i] = pack_bf16x2(p0, p1);
+            }
             const uint32_t chunk = static_cast<uint32_t>(c >> 2) * 16384u;
             const uint32_t x0 = static_cast<uint32_t>((2 * c) & 7), x1 = static_cast<uint32_t>((2 * c + 1) & 7);
             sts128(p_row + chunk + ((x0 ^ p_sw) << 4), make_uint4(pk[0], pk[1], pk[2], pk[3]));
             sts128(p_row + chunk + ((x1 ^ p_sw) << 4), make_uint4(pk[4], pk[5], pk[6], pk[7]));
           }
+          l = l * alpha + ((l4[0] + l4[1]) + (l4[2] + l4[3]));
         }
-        l = l * alpha + ((l4[0] + l4[1]) + (l4[2] + l4[3]));
         fence_proxy_async_smem();   // P (generic stores) before the MMA's async-proxy reads
         tc_fence_before_sync();     // and the O rescale (tcgen05.st) before the next PV
         mbar_arrive(b_p_full);
