@@ -22,7 +22,7 @@
 // Synchronisation per query-tile slot t (all waits bounded):
 //   s_full[t]  S_t,j computed (commit)          -> softmax t
 //   s_free[t]  S_t,j loaded into registers       -> issuer may overwrite S_t (4 warp arrivals)
-//   p_full[t]  P_t,j stored in shared memory     -> issuer may run P_t,j V_j (128 arrivals)
+//   p_full[t]  P_t,j stored in shared memory     -> issuer may run P_t,j V_j (4 warp arrivals)
 //   pv_done[t] P_t,j V_j complete (commit)       -> softmax may rescale O_t / overwrite P_t;
 //                                                    the epilogue may read O_t
 //   o_free[t]  O_t read out by the epilogue      -> the next item's first PV may overwrite it
@@ -120,9 +120,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = 0; t < 2; ++t) {
       mbar_init(smem_u32(&bars->s_full[t]), 1);
       mbar_init(smem_u32(&bars->s_free[t]), 4);
-      mbar_init(smem_u32(&bars->p_full[t]), 128);
+      mbar_init(smem_u32(&bars->p_full[t]), 4);
       mbar_init(smem_u32(&bars->pv_done[t]), 1);
-      mbar_init(smem_u32(&bars->o_free[t]), 128);
+      mbar_init(smem_u32(&bars->o_free[t]), 4);
     }
     mbar_init(smem_u32(&bars->drain[0]), 1);
     mbar_init(smem_u32(&bars->drain[1]), 1);
@@ -745,7 +745,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         fence_proxy_async_smem();   // P (generic stores) before the MMA's async-proxy reads
         tc_fence_before_sync();     // and the O rescale (tcgen05.st) before the next PV
-        mbar_arrive(b_p_full);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(b_p_full);   // one arrival per warp
       }
       if (!ok) break;
       if (!(ok = rotate_next(it))) break;
@@ -772,7 +773,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(tO + c * 32, orr);
         if (c == D / 32 - 1) {
           tc_fence_before_sync();
-          mbar_arrive(smem_u32(&bars->o_free[t]));
+          __syncwarp();
+          if (lane == 0) mbar_arrive(smem_u32(&bars->o_free[t]));
         }
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4) {         // columns 32c + 8q4 .. + 7: 16-byte unit 4c + q4
