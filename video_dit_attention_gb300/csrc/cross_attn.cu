@@ -37,10 +37,11 @@
 //     tile is a step of its own (S in [0, 128), P in [0, 64)), with the online softmax across
 //     steps. A warpgroup's next S is issued once its previous P.V is complete (and, when it
 //     covers O's columns, once O has been read out).
-//   - The softmax keeps a reference m that trails the running maximum by at most kXRescale
-//     (log2 units) and is an integer: when a block's maximum exceeds m + kXRescale, m becomes
-//     its ceiling, and what the row has accumulated (P of earlier blocks of the same product,
-//     or O) is scaled by the power of two 2^(m_old - m_new), which is exact.
+//   - The softmax reads S once, 32 columns at a time, and keeps a reference m that trails the
+//     running maximum by at most kXRescale (log2 units) and is an integer: when a chunk's
+//     maximum exceeds m + kXRescale, m becomes its ceiling, and what the row has accumulated
+//     (P of the product's earlier chunks, O of earlier steps, the sum) is scaled by the power
+//     of two 2^(m_old - m_new), which is exact.
 //   - Epilogue: O is read out of TMEM, normalised and staged in the tile's own Q buffer (Q is
 //     dead once the tile's products have completed) in the 128-byte swizzle. The Q loader
 //     writes it with one TMA store and, once the store has read the buffer, loads tile n + 3's
@@ -288,13 +289,13 @@ __device__ __forceinline__ void x_scale_f32_cols(uint32_t taddr, float a) {
   for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * a);
   tmem_st32(taddr, v);
 }
-// Scales 32 columns of bf16 pairs by a (a power of two, so exactly; warp-collective).
-__device__ __forceinline__ void x_scale_bf16_cols(uint32_t taddr, float a) {
-  uint32_t v[32];
-  tmem_ld32(taddr, v);
+// Scales 16 columns of bf16 pairs by a (a power of two, so exactly; warp-collective).
+__device__ __forceinline__ void x_scale_bf16_cols16(uint32_t taddr, float a) {
+  uint32_t v[16];
+  tmem_ld16(taddr, v);
 #pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = pack_bf16x2(bf16lo_to_f32(v[i]) * a, bf16hi_to_f32(v[i]) * a);
-  tmem_st32(taddr, v);
+  for (int i = 0; i < 16; ++i) v[i] = pack_bf16x2(bf16lo_to_f32(v[i]) * a, bf16hi_to_f32(v[i]) * a);
+  tmem_st16(taddr, v);
 }
 
 template <int D>
@@ -593,75 +594,62 @@ __global__ void __launch_bounds__(kXThreads, 1)
         const XStep st = x_step(t, s);
         ok = ok && wwait(b_s_full, k);
         if (ok) tc_fence_after_sync();
-        // Each 128-key block in two passes over its TMEM columns, 32 at a time (small loops
-        // keep the code that the softmax warps run between tiles in the instruction cache):
-        // the block's row maximum, then the exponentials, their sum and P.
-        for (int bb = 0; bb < st.nkt; ++bb) {
-          const int nv = min(128, t.L - (st.kt + bb) * 128);   // valid keys of this block (>= 1)
-          const uint32_t tS = tR + bb * 128;
-          float mx = -INFINITY;
-          if (ok) {
+        // One pass over the step's S columns, 32 at a time (a small loop keeps the code that
+        // the softmax warps run between tiles in the instruction cache). Each chunk's maximum
+        // may move the reference: when it lies more than kXRescale above it, what the row has
+        // accumulated (P of the step's earlier chunks, O of the earlier steps, the sum) is
+        // scaled by the exact power of two 2^(m_old - m_new) first. P of chunk q goes to
+        // columns 16 q .. 16 q + 15, which hold S this thread has already read (chunk q / 2).
+        float l4[4] = {0.f, 0.f, 0.f, 0.f};
+        if (ok) {
+          const int nq = 4 * st.nkt;
+          const int lim0 = t.L - st.kt * 128;   // valid keys of the step, from its first column
 #pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-              uint32_t v[32];
-              tmem_ld32(tS + c * 32, v);
-              const int lim = nv - c * 32;   // valid columns of this chunk
-              float m0 = -INFINITY, m1 = -INFINITY;
+          for (int q = 0; q < nq; ++q) {
+            uint32_t v[32];
+            tmem_ld32(tR + q * 32, v);
+            const int lim = lim0 - q * 32;   // valid columns of this chunk
+            float m0 = -INFINITY, m1 = -INFINITY;
 #pragma unroll
-              for (int i = 0; i < 32; i += 4) {
-                m0 = fmax3(m0, i < lim ? __uint_as_float(v[i]) : -INFINITY, i + 1 < lim ? __uint_as_float(v[i + 1]) : -INFINITY);
-                m1 = fmax3(m1, i + 2 < lim ? __uint_as_float(v[i + 2]) : -INFINITY,
-                           i + 3 < lim ? __uint_as_float(v[i + 3]) : -INFINITY);
-              }
-              mx = fmax3(mx, m0, m1);
+            for (int i = 0; i < 32; i += 4) {
+              m0 = fmax3(m0, i < lim ? __uint_as_float(v[i]) : -INFINITY, i + 1 < lim ? __uint_as_float(v[i + 1]) : -INFINITY);
+              m1 = fmax3(m1, i + 2 < lim ? __uint_as_float(v[i + 2]) : -INFINITY,
+                         i + 3 < lim ? __uint_as_float(v[i + 3]) : -INFINITY);
             }
-          }
-          const float mt = mx * sl2;
-          const bool first = s == 0 && bb == 0;
-          const bool grow = first || mt > m_run + kXRescale;
-          const float m_new = grow ? ceilf(mt) : m_run;
-          const float alpha = first ? 0.f : ex2_approx(m_run - m_new);   // a power of two
-          // What this row accumulated against the old reference moves to the new one: P of the
-          // product's earlier blocks, or O of the earlier steps (their P V is complete, since
-          // this step's S was issued after it).
-          if (ok && __any_sync(0xffffffffu, grow && !first)) {
-            const float a = (grow && !first) ? alpha : 1.f;
-            if (bb > 0) {
+            const float mt = fmaxf(m0, m1) * sl2;
+            const bool first = s == 0 && q == 0;
+            const bool grow = !first && mt > m_run + kXRescale;
+            if (first) m_run = ceilf(mt);   // the tile's first chunk has a valid column
+            if (__any_sync(0xffffffffu, grow)) {
+              const float m_new = grow ? ceilf(mt) : m_run;
+              const float a = ex2_approx(m_run - m_new);   // a power of two; 1 where m stays
+              l_run = (l_run + ((l4[0] + l4[1]) + (l4[2] + l4[3]))) * a;
+              l4[0] = l4[1] = l4[2] = l4[3] = 0.f;
+              m_run = m_new;
               tmem_st_wait();
 #pragma unroll 1
-              for (int c = 0; c < bb * 2; ++c) x_scale_bf16_cols(tR + c * 32, a);
-            } else {
+              for (int g = 0; g < q; ++g) x_scale_bf16_cols16(tR + g * 16, a);
+              // O of the earlier steps: their P V is complete (this step's S was issued after it).
+              if (s > 0) {
 #pragma unroll 1
-              for (int c = 0; c < D / 32; ++c) x_scale_f32_cols(tR + kXColO + c * 32, a);
-            }
-          }
-          l_run *= alpha;
-          m_run = m_new;
-          const float neg_m = -m_run;
-          float l4[4] = {0.f, 0.f, 0.f, 0.f};
-          if (ok) {
-            // P of chunk c goes to columns 64 bb + 16 c .. + 15, which hold S this thread has
-            // already read (of this block's chunks <= c, or of block 0 for block 1).
-#pragma unroll 1
-            for (int c = 0; c < 4; ++c) {
-              uint32_t v[32];
-              tmem_ld32(tS + c * 32, v);
-              const int lim = nv - c * 32;
-              uint32_t pk[16];
-#pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                float x0, x1;
-                fma2_bc(x0, x1, __uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]), sl2, neg_m);
-                const float p0 = 2 * i < lim ? ex2_approx(x0) : 0.f;
-                const float p1 = 2 * i + 1 < lim ? ex2_approx(x1) : 0.f;
-                add2(l4[2 * (i & 1)], l4[2 * (i & 1) + 1], p0, p1);
-                pk[i] = pack_bf16x2(p0, p1);
+                for (int c = 0; c < D / 32; ++c) x_scale_f32_cols(tR + kXColO + c * 32, a);
               }
-              tmem_st16_nowait(tR + bb * 64 + c * 16, pk);
             }
+            const float neg_m = -m_run;
+            uint32_t pk[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              float x0, x1;
+              fma2_bc(x0, x1, __uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]), sl2, neg_m);
+              const float p0 = 2 * i < lim ? ex2_approx(x0) : 0.f;
+              const float p1 = 2 * i + 1 < lim ? ex2_approx(x1) : 0.f;
+              add2(l4[2 * (i & 1)], l4[2 * (i & 1) + 1], p0, p1);
+              pk[i] = pack_bf16x2(p0, p1);
+            }
+            tmem_st16_nowait(tR + q * 16, pk);
           }
-          l_run += (l4[0] + l4[1]) + (l4[2] + l4[3]);
         }
+        l_run += (l4[0] + l4[1]) + (l4[2] + l4[3]);
         if (ok) {
           tmem_st_wait();
           tc_fence_before_sync();   // P (tcgen05.st) and any rescale before the P V
