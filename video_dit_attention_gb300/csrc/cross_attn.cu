@@ -60,6 +60,8 @@
 
 #include <cuda_bf16.h>
 
+#include <type_traits>
+
 #include "common.h"
 #include "ptx.cuh"
 
@@ -236,6 +238,11 @@ __device__ __forceinline__ XStep x_step(const XTile& t, int s) {
   st.fill = st.first_half ? pair : pair + 1;
   st.group_end = st.first_half ? (s == c0 - 1) : (s == t.n_kv - 1);
   return st;
+}
+
+// 16-key groups holding a step's valid keys (1 .. 8 nkt).
+__device__ __forceinline__ int x_groups(const XTile& t, const XStep& st) {
+  return (min(128 * st.nkt, t.L - 128 * st.kt) + 15) >> 4;
 }
 
 // O = 0 and LSE = -inf for one tile's rows (columns [c0, c0 + D/2) of O by this warpgroup;
@@ -463,8 +470,6 @@ __global__ void __launch_bounds__(kXThreads, 1)
     } else if (lane == 0) {
       // ------------------------------------------------------------------ MMA issuers (warps 2, 3)
       const int w = warp - 2;   // the softmax warpgroup served
-      constexpr uint32_t kIdS1 = idesc_f16kind_f32(128, 128, true, false, false);
-      constexpr uint32_t kIdS2 = idesc_f16kind_f32(128, 256, true, false, false);
       constexpr uint32_t kIdO = idesc_bf16_f32(128, D, false, true);
       const uint32_t region = tbase + static_cast<uint32_t>(w) * kXRegion;
       const uint32_t b_s_full = smem_u32(&bars->s_full[w]), b_p_full = smem_u32(&bars->p_full[w]);
@@ -512,7 +517,9 @@ __global__ void __launch_bounds__(kXThreads, 1)
           {
             const uint64_t da = smem_desc_sw128(sQ + buf * C::kTile, 16, 1024);
             const uint64_t db = smem_desc_sw128(sK + st.j0 * C::kChunk, 16, 1024);
-            const uint32_t idS = st.nkt == 2 ? kIdS2 : kIdS1;
+            // N covers the step's valid keys in whole 16-key groups (the softmax never reads
+            // the columns past them, and P V never reads the keys past them).
+            const uint32_t idS = idesc_f16kind_f32(128, 16u * static_cast<uint32_t>(x_groups(t, st)), true, false, false);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
               const uint64_t offa = ((kk / 4) * C::kChunk + (kk % 4) * 32) >> 4;
@@ -526,13 +533,15 @@ __global__ void __launch_bounds__(kXThreads, 1)
           // The first P V of a tile overwrites O: the previous tile's O has been read out.
           if (s == 0 && tcnt > 0 && !s_over_o && !(ok = wait(b_o_free, tcnt - 1))) break;
           if (!(ok = wait(b_kv_ready, e))) break;
-          for (int j = 0; j < st.nkt; ++j) {
-            const uint64_t dv = smem_desc_sw128(sV + (st.j0 + j) * C::kTile, C::kChunk, 1024);
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-              mma_bf16_ts(region + kXColO, region + j * 64 + kk * 8, dv + static_cast<uint64_t>(kk * 2048 >> 4),
-                          kIdO, (s > 0 || j > 0 || kk > 0) ? 1u : 0u);
-          }
+          // The 16-key groups holding the step's valid keys: group gi reads P columns 8 gi ..
+          // and rows 16 (gi % 8) .. of V tile gi / 8.
+          const int ng = x_groups(t, st);
+          const uint64_t dv0 = smem_desc_sw128(sV + st.j0 * C::kTile, C::kChunk, 1024);
+#pragma unroll 1
+          for (int gi = 0; gi < ng; ++gi)
+            mma_bf16_ts(region + kXColO, region + gi * 8,
+                        dv0 + static_cast<uint64_t>(((gi >> 3) * C::kTile + (gi & 7) * 2048) >> 4), kIdO,
+                        (s > 0 || gi > 0) ? 1u : 0u);
           mma_commit(b_pv_done);
           // Release the fill after this warpgroup's last product on it: a pair's first half is
           // the previous pair's second, read already; otherwise this warpgroup's next tile of
@@ -600,56 +609,70 @@ __global__ void __launch_bounds__(kXThreads, 1)
         // accumulated (P of the step's earlier chunks, O of the earlier steps, the sum) is
         // scaled by the exact power of two 2^(m_old - m_new) first. P of chunk q goes to
         // columns 16 q .. 16 q + 15, which hold S this thread has already read (chunk q / 2).
-        float l4[4] = {0.f, 0.f, 0.f, 0.f};
-        if (ok) {
-          const int nq = 4 * st.nkt;
-          const int lim0 = t.L - st.kt * 128;   // valid keys of the step, from its first column
-#pragma unroll 1
-          for (int q = 0; q < nq; ++q) {
-            uint32_t v[32];
-            tmem_ld32(tR + q * 32, v);
-            const int lim = lim0 - q * 32;   // valid columns of this chunk
-            float m0 = -INFINITY, m1 = -INFINITY;
+        float l_step = 0.f;   // sum of this step's P so far
+        // Chunk q of the step: S columns 32 q .. + 31 (of which `lim` are valid keys); its
+        // maximum, a rescale if the reference has to move, the exponentials and P. MASKED:
+        // the chunk has fewer than 32 valid keys (only the step's last chunk can).
+        auto chunk = [&](int q, int lim, auto masked_tag) {
+          constexpr bool kMasked = decltype(masked_tag)::value;
+          uint32_t v[32];
+          tmem_ld32(tR + q * 32, v);
+          auto sv = [&](int i) -> float {
+            return (kMasked && i >= lim) ? -INFINITY : __uint_as_float(v[i]);
+          };
+          float m0 = -INFINITY, m1 = -INFINITY;
 #pragma unroll
-            for (int i = 0; i < 32; i += 4) {
-              m0 = fmax3(m0, i < lim ? __uint_as_float(v[i]) : -INFINITY, i + 1 < lim ? __uint_as_float(v[i + 1]) : -INFINITY);
-              m1 = fmax3(m1, i + 2 < lim ? __uint_as_float(v[i + 2]) : -INFINITY,
-                         i + 3 < lim ? __uint_as_float(v[i + 3]) : -INFINITY);
-            }
-            const float mt = fmaxf(m0, m1) * sl2;
-            const bool first = s == 0 && q == 0;
-            const bool grow = !first && mt > m_run + kXRescale;
-            if (first) m_run = ceilf(mt);   // the tile's first chunk has a valid column
-            if (__any_sync(0xffffffffu, grow)) {
-              const float m_new = grow ? ceilf(mt) : m_run;
-              const float a = ex2_approx(m_run - m_new);   // a power of two; 1 where m stays
-              l_run = (l_run + ((l4[0] + l4[1]) + (l4[2] + l4[3]))) * a;
-              l4[0] = l4[1] = l4[2] = l4[3] = 0.f;
-              m_run = m_new;
-              tmem_st_wait();
-#pragma unroll 1
-              for (int g = 0; g < q; ++g) x_scale_bf16_cols16(tR + g * 16, a);
-              // O of the earlier steps: their P V is complete (this step's S was issued after it).
-              if (s > 0) {
-#pragma unroll 1
-                for (int c = 0; c < D / 32; ++c) x_scale_f32_cols(tR + kXColO + c * 32, a);
-              }
-            }
-            const float neg_m = -m_run;
-            uint32_t pk[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              float x0, x1;
-              fma2_bc(x0, x1, __uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]), sl2, neg_m);
-              const float p0 = 2 * i < lim ? ex2_approx(x0) : 0.f;
-              const float p1 = 2 * i + 1 < lim ? ex2_approx(x1) : 0.f;
-              add2(l4[2 * (i & 1)], l4[2 * (i & 1) + 1], p0, p1);
-              pk[i] = pack_bf16x2(p0, p1);
-            }
-            tmem_st16_nowait(tR + q * 16, pk);
+          for (int i = 0; i < 32; i += 4) {
+            m0 = fmax3(m0, sv(i), sv(i + 1));
+            m1 = fmax3(m1, sv(i + 2), sv(i + 3));
           }
+          const float mt = fmaxf(m0, m1) * sl2;
+          const bool first = s == 0 && q == 0;
+          const bool grow = !first && mt > m_run + kXRescale;
+          if (first) m_run = ceilf(mt);   // the tile's first chunk has a valid column
+          if (__any_sync(0xffffffffu, grow)) {
+            const float m_new = grow ? ceilf(mt) : m_run;
+            const float a = ex2_approx(m_run - m_new);   // a power of two; 1 where m stays
+            l_run = (l_run + l_step) * a;
+            l_step = 0.f;
+            m_run = m_new;
+            tmem_st_wait();
+#pragma unroll 1
+            for (int g = 0; g < q; ++g) x_scale_bf16_cols16(tR + g * 16, a);
+            // O of the earlier steps: their P V is complete (this step's S was issued after it).
+            if (s > 0) {
+#pragma unroll 1
+              for (int c = 0; c < D / 32; ++c) x_scale_f32_cols(tR + kXColO + c * 32, a);
+            }
+          }
+          const float neg_m = -m_run;
+          float l4[4] = {0.f, 0.f, 0.f, 0.f};
+          uint32_t pk[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            float x0, x1;
+            fma2_bc(x0, x1, __uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]), sl2, neg_m);
+            float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+            if (kMasked) {
+              p0 = 2 * i < lim ? p0 : 0.f;
+              p1 = 2 * i + 1 < lim ? p1 : 0.f;
+            }
+            add2(l4[2 * (i & 1)], l4[2 * (i & 1) + 1], p0, p1);
+            pk[i] = pack_bf16x2(p0, p1);
+          }
+          tmem_st16_nowait(tR + q * 16, pk);
+          l_step += (l4[0] + l4[1]) + (l4[2] + l4[3]);
+        };
+        if (ok) {
+          const int lim0 = min(128 * st.nkt, t.L - st.kt * 128);   // valid keys of the step
+          const int nfull = lim0 >> 5;                               // chunks with 32 of them
+#pragma unroll 1
+          for (int q = 0; q < nfull; ++q) chunk(q, 32, std::false_type{});
+          // The last chunk with valid keys, if partial. P V reads only the step's valid keys
+          // in whole 16-key groups, so no P column past them is read.
+          if ((lim0 & 31) != 0) chunk(nfull, lim0 & 31, std::true_type{});
         }
-        l_run += (l4[0] + l4[1]) + (l4[2] + l4[3]);
+        l_run += l_step;
         if (ok) {
           tmem_st_wait();
           tc_fence_before_sync();   // P (tcgen05.st) and any rescale before the P V
