@@ -179,8 +179,10 @@ def gpu_id_for_smi(dev_index: int) -> str:
         return vis.split(",")[dev_index] if vis else str(dev_index)
 
 
-# The attention kernels' sources: a committed ncu summary applies while their hash matches.
-KERNEL_SOURCES = ("attn_fwd.cu", "attn_sp.cuh", "ptx.cuh", "cross_attn.cu")
+# The sources of the kernel each workload's summary covers: a committed ncu summary applies
+# while their hash matches (the cross workload runs cross_attn_kernel, the others
+# attn_sp_kernel).
+KERNEL_SOURCES = {"cross": ("cross_attn.cu", "ptx.cuh"), None: ("attn_fwd.cu", "attn_sp.cuh", "ptx.cuh")}
 
 
 def profiled(name, variant=""):
@@ -197,7 +199,8 @@ def profiled(name, variant=""):
     path = os.path.join(ROOT, "profiles", base + (f"_{variant}" if variant else "") + ".md")
     if not os.path.exists(path):
         return None
-    srcs = [os.path.join(ROOT, "video_dit_attention_gb300", "csrc", f) for f in KERNEL_SOURCES]
+    srcs = [os.path.join(ROOT, "video_dit_attention_gb300", "csrc", f)
+            for f in KERNEL_SOURCES.get(name, KERNEL_SOURCES[None])]
     h = hashlib.sha256(b"".join(open(f, "rb").read() for f in srcs)).hexdigest()[:16]
     sha = traffic = ncu_ms = None
     for line in open(path):
