@@ -48,10 +48,11 @@ def test_cross_many_tiles_per_cta(lib, D, kv):
 def test_cross_growing_maximum(lib, D, kv, grow):
     """Keys of one 128-key block scaled by 4 (exact in bf16), so that for many rows its scores
     exceed those of the block visited first by more than the softmax lets its reference trail
-    (8 in log2 units, plus up to 1 for the reference's rounding up): with at most 256 keys
-    the P already written for the earlier block is rescaled; with more, O of the earlier steps
-    is. grow = the scaled block (1: keys 128-255, 2: 256-383, 3: 384-511). Odd query rows
-    are scaled by 1/8, so that they see no such jump and the rescale runs on warps where only
+    (8 in log2 units, plus up to 1 for the reference's rounding up). With at most 256 keys
+    one product covers both blocks and its maximum is taken before any exponential; with
+    more, each key tile is a product of its own and O of the earlier products is rescaled.
+    grow = the scaled block (1: keys 128-255, 2: 256-383, 3: 384-511). Odd query rows are
+    scaled by 1/8, so that they see no such jump and the rescale runs on warps where only
     some rows need it. (Scaling by 8 takes the bf16 rounding of P alone past the O tolerance:
     a step-by-step simulation of the kernel's arithmetic gives 0.0234 there, 0.016 at 4.)"""
     case = AttnCase("crossgrow", B=2, H=4, D=D, Sq=768, Skv=512, q_valid=700, kv_valid=kv, seed=90 + grow)

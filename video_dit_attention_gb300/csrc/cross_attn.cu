@@ -13,51 +13,53 @@
 // Design (one GPU, sm_103a). The text is short (at most 512 keys), so the work per query
 // tile is small (one or two 128-key tiles at the drawn lengths) and the query/output stream
 // dominates: 97 MB of Q in and 97 MB of O out at B2 H40, against 21 MB of K and V. What
-// limits such a kernel is the chain of dependent steps per query tile (Q load, S product,
-// softmax, P.V product, read-out of O, store), not any one unit, so the design keeps two of
-// these chains in flight per SM and gives them nothing to wait for from each other.
+// limits such a kernel is the chain of dependent steps per query tile (S product, softmax,
+// P.V product, read-out of O), so the CTA runs its tiles one after another through all eight
+// softmax warps, and the products of a tile's neighbours run while its softmax does.
 //   - Work is a flat list of 128-row query tiles over (b, h, tile). CTA c of a persistent grid
 //     takes the contiguous range [c T / G, (c + 1) T / G). The live tiles of the range (a
-//     valid query row and at least one key) are numbered n = 0, 1, ...; tile n belongs to
-//     softmax warpgroup n & 1 and to Q buffer n % 3. Each warpgroup owns its tiles outright:
-//     one thread per query row holds every key column of that row, so the row maximum and
-//     sum need no exchange between warpgroups.
+//     valid query row and at least one key) are numbered n = 0, 1, ...; tile n uses TMEM
+//     region n & 1 (256 columns) and Q buffer n & 1.
+//   - Softmax: the two warps of a lane quarter (w and w + 4) share its 32 query rows. Warp-
+//     group 0 takes the first half of a product's keys, warpgroup 1 the second. Each thread
+//     finds its half's row maximum; the pair exchange it through shared memory (a slot per
+//     row and warpgroup, double-buffered, and an mbarrier per quarter), take the larger as
+//     the row's reference m (its ceiling, an integer in log2 units) and exponentiate their
+//     halves against it. The two partial row sums go across at the next exchange.
+//   - TMEM, per region: S of up to 256 keys in columns [0, 128 nkt). Each half's P (bf16
+//     pairs) goes over S columns its own warpgroup has read already: warpgroup 0's to
+//     [0, 32 nkt) in key order, warpgroup 1's to [96 nkt, 128 nkt), its 32-key chunks taken
+//     from the last to the first. O = P V (tensor-memory A operand) goes to [64, 64 + D) for a
+//     product of two key tiles and to [128, 128 + D) for one of one key tile: S columns that
+//     are dead once the softmax is done.
+//   - Overlap: the softmax warps read tile n - 1's O out of its region in the middle of tile
+//     n's exponentials (of its last product), as soon as tile n - 1's P V is complete; the
+//     read-out frees the region, and tile n + 1's S is issued into it at once. While the
+//     softmax warps work on tile n, the tensor pipe runs tile n - 1's P V and tile n + 1's S.
+//   - Q and O: tile n's Q lands in buffer n & 1. Once its S has completed the buffer is dead,
+//     and the softmax stages tile n - 1's normalised O there (128-byte swizzle); the Q loader
+//     writes it out with one TMA store and, once the store has read the buffer, loads tile
+//     n + 2's Q into it. (A scattered store of O from registers, 32 rows per instruction,
+//     measured far slower.)
 //   - The keys and values of the current (b, h) stay in shared memory (a "fill", 256 rows of
 //     K and of V) for all of the CTA's tiles of that head. When L_b > 256 a tile visits its
-//     keys in two halves (key tiles {0, 1} and {2, n_kv - 1}); the two tiles of a pair
-//     (in-run indices 2p and 2p + 1, one per warpgroup) visit the halves in the order
-//     (p & 1, 1 - (p & 1)), so a pair's second half is the next pair's first and a run of
-//     P pairs needs P + 1 fills. A fill is released when both MMA issuers have arrived on it:
-//     by a commit after their last product on it, or, for an issuer with no product on it, by
-//     a plain arrival once it has landed.
-//   - TMEM: each warpgroup has 256 columns. With n_kv <= 2, S = Q K^T is one product of N =
-//     128 n_kv keys into columns [0, 128 n_kv); the softmax writes P (bf16 pairs) over the
-//     columns it has already read, [0, 64 n_kv); O = P V (tensor-memory A operand) goes to
-//     columns [128, 128 + D), over S columns that are dead by then. With n_kv > 2 each key
-//     tile is a step of its own (S in [0, 128), P in [0, 64)), with the online softmax across
-//     steps. A warpgroup's next S is issued once its previous P.V is complete (and, when it
-//     covers O's columns, once O has been read out).
-//   - The softmax reads S once, 32 columns at a time, and keeps a reference m that trails the
-//     running maximum by at most kXRescale (log2 units) and is an integer: when a chunk's
-//     maximum exceeds m + kXRescale, m becomes its ceiling, and what the row has accumulated
-//     (P of the product's earlier chunks, O of earlier steps, the sum) is scaled by the power
-//     of two 2^(m_old - m_new), which is exact.
-//   - Epilogue: O is read out of TMEM, normalised and staged in the tile's own Q buffer (Q is
-//     dead once the tile's products have completed) in the 128-byte swizzle. The Q loader
-//     writes it with one TMA store and, once the store has read the buffer, loads tile n + 3's
-//     Q into it; the softmax warps never wait for a store.
-//   - Warpgroup 1's first S waits for warpgroup 0's first S to complete, which puts the two
-//     chains out of phase: while one warpgroup exponentiates, the other's products run.
-//   - Roles: warp 0 loads Q and stores O (three buffers; the next two tiles are warmed in L2); warp 1 owns
-//     TMEM, loads the fills and zeroes the V rows past L_b of a fill's last V tile (so that
-//     0 * (pad contents) cannot reach O; K pad rows need nothing, their score columns are
-//     masked to -inf); warps 2 and 3 issue the MMAs of softmax warpgroups 0 and 1; warps 4-7
-//     and 8-11 are the two softmax warpgroups.
+//     keys in two halves (key tiles {0, 1} and {2, n_kv - 1}), one product per key tile, with
+//     the online softmax across products: the reference moves only when a product's maximum
+//     exceeds it by more than kXRescale, and O and the sums are then scaled by the power of
+//     two 2^(m_old - m_new), which is exact. Tile i of a run visits half i & 1 first, so
+//     consecutive tiles share the fill at their boundary and a run of P tiles reads P + 1
+//     fills. A fill is released when both MMA issuers have committed their last product on it.
+//   - Roles: warp 0 loads Q and stores O (two buffers; the tile two ahead is warmed in L2);
+//     warp 1 owns TMEM, loads the fills and zeroes the V rows past L_b of a fill's last V
+//     tile (so that 0 * (pad contents) cannot reach O; K pad rows need nothing, their score
+//     columns are masked to -inf); warp 2 issues the S products, warp 3 the P V products;
+//     warps 4-11 are the softmax.
 // Every wait is bounded (ptx.cuh); on a timeout the CTA records a status bit, raises its
 // abort flag (the other roles' waits then give up at once), drains its copies and MMAs,
 // frees TMEM and exits. No named barrier is used after the set-up, so no thread can be left
 // waiting at one.
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 
 #include <type_traits>
@@ -68,14 +70,13 @@
 namespace dit {
 namespace {
 
-constexpr int kXThreads = 384;   // warps 0-3: Q loads, TMEM + fills, two MMA issuers; 4-11: softmax
+constexpr int kXThreads = 384;   // warps 0-3: Q loads, TMEM + fills, S issuer, P V issuer; 4-11: softmax
 constexpr float kXLn2 = 0.69314718055994530942f;
 constexpr float kXLog2e = 1.44269504088896340736f;
 constexpr float kXRescale = 8.0f;   // log2 units: the reference may trail the maximum by up to 8
 constexpr int kLenCache = 128;      // per-batch key lengths kept in shared memory
-constexpr int kXQBufs = 3;          // Q buffers (each also stages its tile's O)
-constexpr uint32_t kXRegion = 256;  // TMEM columns per softmax warpgroup
-constexpr uint32_t kXColO = 128;    // O within a region: columns [128, 128 + D)
+constexpr int kXQBufs = 2;          // Q buffers (tile n in buffer n & 1)
+constexpr uint32_t kXRegion = 256;  // TMEM columns per region (tile n in region n & 1)
 
 template <int D>
 struct XCfg {
@@ -85,18 +86,19 @@ struct XCfg {
   static constexpr int kOffQ = 0;                  // kXQBufs Q buffers
   static constexpr int kOffK = kOffQ + kXQBufs * kTile;  // K: chunk c holds rows 0..255 at c * 2 kChunk
   static constexpr int kOffV = kOffK + 2 * kTile;  // V: two 128-row tiles
-  static constexpr int kOffLen = kOffV + 2 * kTile;      // key lengths of the first kLenCache batches
+  static constexpr int kOffX = kOffV + 2 * kTile;  // exchange slots: float2 [2 buffers][2 warpgroups][128 rows]
+  static constexpr int kOffLen = kOffX + 2 * 2 * 128 * 8;  // key lengths of the first kLenCache batches
   static constexpr int kOffBar = kOffLen + kLenCache * 4;
   static constexpr int kSmem = kOffBar + 256 + 1024;     // barriers + alignment slack
 };
 static_assert(XCfg<128>::kSmem <= 232448, "shared memory of the D = 128 cross kernel");
 
 struct XBars {
-  uint64_t q_full[kXQBufs], o_staged[kXQBufs];
+  uint64_t q_full[kXQBufs], q_empty[kXQBufs], o_staged[kXQBufs];
   uint64_t kv_full, kv_ready, kv_empty;
-  uint64_t s_full[2], p_full[2], pv_done[2], o_free[2];
+  uint64_t s_full[2], p_full[2], pv_done[2], o_free[2];   // per TMEM region
+  uint64_t xch[4];                                       // per lane quarter: the softmax exchange
   uint64_t drain[2];
-  uint64_t started;   // warpgroup 0's first S is complete (one phase only)
   uint32_t tmem_base;
   int abort;
 };
@@ -109,7 +111,7 @@ struct XParams {
   const int32_t* kv_len;
   float scale_log2;
   float* lse;
-  uint16_t* out;     // for the direct writes of empty tiles
+  uint16_t* out;
   unsigned int* status;
 };
 
@@ -191,8 +193,8 @@ __device__ __forceinline__ bool x_walk_next(XWalk& w, const XParams& p, const in
   return false;
 }
 
-// Fills of a run: one when n_kv <= 2, else pairs + 1 (fill k holds key half k & 1).
-__device__ __forceinline__ int x_run_fills(const XTile& t) { return t.n_kv <= 2 ? 1 : ((t.len + 1) >> 1) + 1; }
+// Fills of a run: one when n_kv <= 2, else len + 1 (fill k holds key half k & 1).
+__device__ __forceinline__ int x_run_fills(const XTile& t) { return t.n_kv <= 2 ? 1 : t.len + 1; }
 // Key tiles of fill k of the run: first tile and count.
 __device__ __forceinline__ void x_fill_tiles(const XTile& t, int k, int& kt0, int& cnt) {
   if (t.n_kv <= 2) {
@@ -205,15 +207,15 @@ __device__ __forceinline__ void x_fill_tiles(const XTile& t, int k, int& kt0, in
   }
 }
 
-// The products of a live tile. n_kv <= 2: one step over all its keys. n_kv > 2: one step per
-// key tile, the tiles of the first half visited, then those of the second.
+// The products of a live tile. n_kv <= 2: one product over all its keys. n_kv > 2: one
+// product per key tile, the tiles of the half visited first (half i & 1, in fill i), then
+// those of the other (in fill i + 1).
 struct XStep {
-  int fill;         // fill of the run it reads (0-based within the run)
-  int j0;           // first slot of the fill it reads
-  int kt;           // first key tile
-  int nkt;          // key tiles in the product (1 or 2)
-  bool group_end;   // last step of the tile that reads this fill
-  bool first_half;  // n_kv > 2: the step reads the pair's first half
+  int fill;      // fill of the run it reads (0-based within the run)
+  int j0;        // first slot of the fill it reads
+  int kt;        // first key tile
+  int nkt;       // key tiles in the product (1 or 2)
+  bool release;  // the last product of the run that reads this fill
 };
 __device__ __forceinline__ int x_n_steps(const XTile& t) { return t.n_kv <= 2 ? 1 : t.n_kv; }
 __device__ __forceinline__ XStep x_step(const XTile& t, int s) {
@@ -223,27 +225,30 @@ __device__ __forceinline__ XStep x_step(const XTile& t, int s) {
     st.j0 = 0;
     st.kt = 0;
     st.nkt = t.n_kv;
-    st.group_end = true;
-    st.first_half = false;
+    st.release = t.i == t.len - 1;
     return st;
   }
-  const int pair = t.i >> 1;
-  const int h0 = pair & 1;
+  const int h0 = t.i & 1;
   const int c0 = h0 ? t.n_kv - 2 : 2;   // key tiles of the half visited first
-  st.first_half = s < c0;
-  const int half = st.first_half ? h0 : 1 - h0;
-  st.j0 = st.first_half ? s : s - c0;
+  const bool first = s < c0;
+  const int half = first ? h0 : 1 - h0;
+  st.j0 = first ? s : s - c0;
   st.kt = 2 * half + st.j0;
   st.nkt = 1;
-  st.fill = st.first_half ? pair : pair + 1;
-  st.group_end = st.first_half ? (s == c0 - 1) : (s == t.n_kv - 1);
+  st.fill = first ? t.i : t.i + 1;
+  // Fill i is read by tile i - 1's second half and tile i's first half; the run's last
+  // fill by its last tile's second half.
+  st.release = first ? s == c0 - 1 : (s == t.n_kv - 1 && t.i == t.len - 1);
   return st;
 }
 
-// 16-key groups holding a step's valid keys (1 .. 8 nkt).
+// 16-key groups holding a product's valid keys (1 .. 8 nkt).
 __device__ __forceinline__ int x_groups(const XTile& t, const XStep& st) {
   return (min(128 * st.nkt, t.L - 128 * st.kt) + 15) >> 4;
 }
+// First TMEM column of O within a region: [64, 64 + D) after a product of two key tiles,
+// [128, 128 + D) after products of one.
+__device__ __forceinline__ uint32_t x_ocol(const XTile& t) { return t.n_kv == 2 ? 64u : 128u; }
 
 // O = 0 and LSE = -inf for one tile's rows (columns [c0, c0 + D/2) of O by this warpgroup;
 // the LSE by warpgroup 0), written directly.
@@ -296,15 +301,6 @@ __device__ __forceinline__ void x_scale_f32_cols(uint32_t taddr, float a) {
   for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * a);
   tmem_st32(taddr, v);
 }
-// Scales 16 columns of bf16 pairs by a (a power of two, so exactly; warp-collective).
-__device__ __forceinline__ void x_scale_bf16_cols16(uint32_t taddr, float a) {
-  uint32_t v[16];
-  tmem_ld16(taddr, v);
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = pack_bf16x2(bf16lo_to_f32(v[i]) * a, bf16hi_to_f32(v[i]) * a);
-  tmem_st16(taddr, v);
-}
-
 template <int D>
 __global__ void __launch_bounds__(kXThreads, 1)
     cross_attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -331,19 +327,20 @@ __global__ void __launch_bounds__(kXThreads, 1)
     bars->abort = 0;
     for (int i = 0; i < kXQBufs; ++i) {
       mbar_init(smem_u32(&bars->q_full[i]), 1);
-      mbar_init(smem_u32(&bars->o_staged[i]), 4);   // the four warps of the tile's warpgroup
+      mbar_init(smem_u32(&bars->q_empty[i]), 1);
+      mbar_init(smem_u32(&bars->o_staged[i]), 8);   // one arrival per softmax warp
     }
     mbar_init(smem_u32(&bars->kv_full), 1);
     mbar_init(smem_u32(&bars->kv_ready), 1);
-    mbar_init(smem_u32(&bars->kv_empty), 2);   // one arrival per MMA issuer
-    for (int w = 0; w < 2; ++w) {
-      mbar_init(smem_u32(&bars->s_full[w]), 1);
-      mbar_init(smem_u32(&bars->p_full[w]), 4);
-      mbar_init(smem_u32(&bars->pv_done[w]), 1);
-      mbar_init(smem_u32(&bars->o_free[w]), 4);
-      mbar_init(smem_u32(&bars->drain[w]), 1);
+    mbar_init(smem_u32(&bars->kv_empty), 2);   // one commit per MMA issuer
+    for (int r = 0; r < 2; ++r) {
+      mbar_init(smem_u32(&bars->s_full[r]), 1);
+      mbar_init(smem_u32(&bars->p_full[r]), 8);   // one arrival per softmax warp
+      mbar_init(smem_u32(&bars->pv_done[r]), 1);
+      mbar_init(smem_u32(&bars->o_free[r]), 8);
+      mbar_init(smem_u32(&bars->drain[r]), 1);
     }
-    mbar_init(smem_u32(&bars->started), 1);
+    for (int q = 0; q < 4; ++q) mbar_init(smem_u32(&bars->xch[q]), 2);   // one arrival per warp of the pair
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -364,23 +361,40 @@ __global__ void __launch_bounds__(kXThreads, 1)
   const uint32_t b_kv_empty = smem_u32(&bars->kv_empty);
 
   if (warp < 4) {
-    regs_dec<64>();
+    regs_dec<72>();
     if (warp == 0 && lane == 0) {
       // ------------------------------------------------------------------ Q loads, O stores
-      // Tile n's Q lands in buffer n % 3, and its O is staged there by its warpgroup; this
-      // thread stores it, and once the store has read the buffer, loads tile n + 3's Q into it.
-      int n = -1, issued = 0, stored = 0;
-      int cb[kXQBufs] = {}, ch[kXQBufs] = {}, cq[kXQBufs] = {};   // coordinates of each buffer's tile
+      // Buffer b holds, in turn, Q of tile m (m & 1 == b) and, once that tile's last S has
+      // completed, the O of tile m - 1, which the softmax stages there during tile m's last
+      // product. Step m of this thread stores O(m - 3) out of buffer m & 1 and, once the store
+      // has read it, loads Q(m) into it. After the last of the N live tiles, step N hands
+      // buffer N & 1 to the softmax for O(N - 1) (a plain arrival on its q_full), and steps
+      // N + 1 and N + 2 store the last two O.
+      int m = 0;
       bool ok = true;
-      auto store = [&](int m) -> bool {   // tile m's O, once its warpgroup has staged it
-        const int b = m % kXQBufs;
-        if (!bounded_wait(smem_u32(&bars->o_staged[b]), (m / kXQBufs) & 1, abort_flag, status, kStatusTimeoutLoad))
-          return false;
+      // Coordinates (b, h, first row) of tiles m - 1, m - 2 and m - 3, shifted at every step.
+      int b1 = 0, h1 = 0, q1 = 0, b2 = 0, h2 = 0, q2 = 0, b3 = 0, h3 = 0, q3 = 0;
+      auto shift = [&](int b, int h, int q) {
+        b3 = b2; h3 = h2; q3 = q2;
+        b2 = b1; h2 = h1; q2 = q1;
+        b1 = b; h1 = h; q1 = q;
+      };
+      int n_live = 1 << 30;   // live tiles: known once the walk has ended
+      auto free_buffer = [&]() -> bool {   // buffer m & 1, for step m
+        const int b = m & 1;
+        if (m >= 3) {
+          const int j = m - 3;   // staged in buffer (j + 1) & 1 == b during tile j + 1
+          if (!bounded_wait(smem_u32(&bars->o_staged[b]), (j >> 1) & 1, abort_flag, status, kStatusTimeoutLoad))
+            return false;
 #pragma unroll
-        for (int c = 0; c < C::kSub; ++c) tma_store_4d(&tm_o, sQ + b * C::kTile + c * C::kChunk, c * 64, ch[b], cq[b], cb[b]);
-        bulk_commit_group();
-        stored = m + 1;
-        return true;
+          for (int c = 0; c < C::kSub; ++c)
+            tma_store_4d(&tm_o, sQ + b * C::kTile + c * C::kChunk, c * 64, h3, q3, b3);
+          bulk_commit_group();
+          bulk_wait_read();   // the buffer has been read out
+        }
+        // The buffer's previous Q (tile m - 2, if there is one) has been read by its last S.
+        return m < kXQBufs || m - 2 >= n_live ||
+               bounded_wait(smem_u32(&bars->q_empty[b]), ((m >> 1) - 1) & 1, abort_flag, status, kStatusTimeoutLoad);
       };
       XWalk w, ahead;
       x_walk_init(w, p, len_s, g0, g1);
@@ -388,32 +402,36 @@ __global__ void __launch_bounds__(kXThreads, 1)
       XTile t, ta;
       for (int i = 0; i < 2; ++i) x_walk_next(ahead, p, len_s, ta);   // two tiles ahead of w
       while (ok && x_walk_next(w, p, len_s, t)) {
-        ++n;
-        const int buf = n % kXQBufs;
-        if (n >= kXQBufs) {
-          if (!(ok = store(n - kXQBufs))) break;
-          bulk_wait_read();   // the buffer has been read out
-        }
+        const int buf = m & 1;
+        if (!(ok = free_buffer())) break;
         const uint32_t qb = smem_u32(&bars->q_full[buf]);
         mbar_arrive_expect_tx(qb, C::kTile);
 #pragma unroll
         for (int c = 0; c < C::kSub; ++c)
           tma_load_4d(sQ + buf * C::kTile + c * C::kChunk, &tm_q, qb, c * 64, t.h, t.qt * 128, t.b);
-        cb[buf] = t.b;
-        ch[buf] = t.h;
-        cq[buf] = t.qt * 128;
-        issued = n + 1;
-        // Warm L2 with the tile two ahead, so that each refill of a buffer is an L2 hit.
+        shift(t.b, t.h, t.qt * 128);
+        ++m;
+        // Warm L2 with the tile two ahead.
         if (x_walk_next(ahead, p, len_s, ta))
 #pragma unroll
           for (int c = 0; c < C::kSub; ++c) tma_prefetch_l2_4d(&tm_q, c * 64, ta.h, ta.qt * 128, ta.b);
       }
-      for (int m = stored; ok && m < issued; ++m) ok = store(m);
+      n_live = m;
+      bool handed = false;   // buffer n_live & 1 went to the softmax (its q_full moved on)
+      for (; ok && n_live > 0 && m < n_live + 3; ++m) {
+        if (!(ok = free_buffer())) break;
+        if (m == n_live) {
+          mbar_arrive(smem_u32(&bars->q_full[m & 1]));
+          handed = true;
+        }
+        shift(0, 0, 0);
+      }
       bulk_wait_all();
       // Let the loads in flight land before the CTA releases its shared memory (on the
-      // normal path each has been waited for already, and these return at once).
-      for (int m = issued > kXQBufs ? issued - kXQBufs : 0; m < issued; ++m)
-        drain_wait(smem_u32(&bars->q_full[m % kXQBufs]), (m / kXQBufs) & 1, status);
+      // normal path each has been waited for already, and these return at once). Once the
+      // buffer was handed over, tile n_live - 2's load had landed (its S had completed).
+      for (int j = n_live > kXQBufs ? n_live - kXQBufs : 0; j < n_live; ++j)
+        if (!(handed && j == n_live - 2)) drain_wait(smem_u32(&bars->q_full[j & 1]), (j >> 1) & 1, status);
     } else if (warp == 1) {
       // ------------------------------------------------------------------ fills + V pad rows
       int e = 0;
@@ -468,12 +486,9 @@ __global__ void __launch_bounds__(kXThreads, 1)
         }
       }
     } else if (lane == 0) {
-      // ------------------------------------------------------------------ MMA issuers (warps 2, 3)
-      const int w = warp - 2;   // the softmax warpgroup served
-      constexpr uint32_t kIdO = idesc_bf16_f32(128, D, false, true);
-      const uint32_t region = tbase + static_cast<uint32_t>(w) * kXRegion;
-      const uint32_t b_s_full = smem_u32(&bars->s_full[w]), b_p_full = smem_u32(&bars->p_full[w]);
-      const uint32_t b_pv_done = smem_u32(&bars->pv_done[w]), b_o_free = smem_u32(&bars->o_free[w]);
+      // ------------------------------------------------------------------ MMA issuers
+      // Warp 2 issues every S = Q K^T, warp 3 every O += P V, each in tile order.
+      const bool is_s = warp == 2;
       bool ok = true;
       // Polled waits: the issuer resumes as soon as the phase completes.
       auto wait = [&](uint32_t bar, int phase) -> bool {
@@ -481,7 +496,9 @@ __global__ void __launch_bounds__(kXThreads, 1)
         tc_fence_after_sync();
         return true;
       };
-      int n = -1, k = 0, tcnt = 0, e_run = 0, e_total = 0, released = 0;
+      constexpr uint32_t kIdO = idesc_bf16_f32(128, D, false, true);
+      int n = -1, e_run = 0, e_total = 0;
+      int ks0 = 0, ks1 = 0;   // products so far in regions 0 and 1 (scalars: no local memory)
       XWalk wk;
       x_walk_init(wk, p, len_s, g0, g1);
       XTile t;
@@ -491,89 +508,72 @@ __global__ void __launch_bounds__(kXThreads, 1)
           e_run = e_total;
           e_total += x_run_fills(t);
         }
-        if ((n & 1) != w) continue;
-        const int buf = n % kXQBufs;
+        const int rg = n & 1;
+        const uint32_t region = tbase + static_cast<uint32_t>(rg) * kXRegion;
         const int ns = x_n_steps(t);
-        for (int s = 0; ok && s < ns; ++s, ++k) {
+        for (int s = 0; ok && s < ns; ++s) {
           const XStep st = x_step(t, s);
           const int e = e_run + st.fill;
-          // Fills before e that this warpgroup does not read: arrive once each has landed.
-          while (ok && released < e) {
-            if (!(ok = wait(b_kv_full, released))) break;
-            mbar_arrive(b_kv_empty);
-            ++released;
-          }
-          if (!ok) break;
-          if (s == 0 && !(ok = wait(smem_u32(&bars->q_full[buf]), n / kXQBufs))) break;
-          if (!(ok = wait(b_kv_full, e))) break;
-          // The previous P V of this warpgroup is complete: its P columns may be overwritten.
-          if (k > 0 && !(ok = wait(b_pv_done, k - 1))) break;
-          // An S of 256 keys covers O's columns: the previous tile's O has been read out.
-          const bool s_over_o = st.nkt == 2;
-          if (s == 0 && tcnt > 0 && s_over_o && !(ok = wait(b_o_free, tcnt - 1))) break;
-          // Warpgroup 1 starts once warpgroup 0's first S is complete, so that the two chains
-          // run out of phase: one warpgroup's softmax while the other's products run.
-          if (w == 1 && k == 0 && !(ok = wait(smem_u32(&bars->started), 0))) break;
-          {
-            const uint64_t da = smem_desc_sw128(sQ + buf * C::kTile, 16, 1024);
+          const int ng = x_groups(t, st);
+          const int kr = rg ? ks1 : ks0;   // this product's index in its region
+          if (is_s) {
+            if (s == 0) {
+              if (!(ok = wait(smem_u32(&bars->q_full[rg]), n >> 1))) break;
+              // The region's previous tile has been read out (its P V complete, O read).
+              if (n >= 2 && !(ok = wait(smem_u32(&bars->o_free[rg]), (n >> 1) - 1))) break;
+            } else if (!(ok = wait(smem_u32(&bars->pv_done[rg]), kr - 1))) {
+              break;   // (above: the previous product's P has been read; S goes over it)
+            }
+            if (!(ok = wait(b_kv_full, e))) break;
+            const uint64_t da = smem_desc_sw128(sQ + rg * C::kTile, 16, 1024);
             const uint64_t db = smem_desc_sw128(sK + st.j0 * C::kChunk, 16, 1024);
-            // N covers the step's valid keys in whole 16-key groups (the softmax never reads
-            // the columns past them, and P V never reads the keys past them).
-            const uint32_t idS = idesc_f16kind_f32(128, 16u * static_cast<uint32_t>(x_groups(t, st)), true, false, false);
+            // N covers the product's valid keys in whole 16-key groups (the softmax never
+            // reads the columns past them, and P V never reads the keys past them).
+            const uint32_t idS = idesc_f16kind_f32(128, 16u * static_cast<uint32_t>(ng), true, false, false);
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
               const uint64_t offa = ((kk / 4) * C::kChunk + (kk % 4) * 32) >> 4;
               const uint64_t offb = ((kk / 4) * 2 * C::kChunk + (kk % 4) * 32) >> 4;
               mma_bf16_ss(region, da + offa, db + offb, idS, kk > 0);
             }
-            mma_commit(b_s_full);
-            if (w == 0 && k == 0) mma_commit(smem_u32(&bars->started));
-          }
-          if (!(ok = wait(b_p_full, k))) break;
-          // The first P V of a tile overwrites O: the previous tile's O has been read out.
-          if (s == 0 && tcnt > 0 && !s_over_o && !(ok = wait(b_o_free, tcnt - 1))) break;
-          if (!(ok = wait(b_kv_ready, e))) break;
-          // The 16-key groups holding the step's valid keys: group gi reads P columns 8 gi ..
-          // and rows 16 (gi % 8) .. of V tile gi / 8.
-          const int ng = x_groups(t, st);
-          const uint64_t dv0 = smem_desc_sw128(sV + st.j0 * C::kTile, C::kChunk, 1024);
+            mma_commit(smem_u32(&bars->s_full[rg]));
+            if (s == ns - 1) mma_commit(smem_u32(&bars->q_empty[rg]));   // Q is read
+          } else {
+            if (!(ok = wait(smem_u32(&bars->p_full[rg]), kr))) break;
+            if (!(ok = wait(b_kv_ready, e))) break;
+            // Group gi (keys 16 gi ..) reads P columns 8 gi .. (warpgroup 1's half, from group
+            // 4 nkt on, lies 64 nkt columns further) and rows 16 (gi % 8) .. of V tile gi / 8.
+            const int hb = 4 * st.nkt;
+            const uint32_t hoff = 64u * static_cast<uint32_t>(st.nkt);
+            const uint32_t dO = region + x_ocol(t);
+            const uint64_t dv0 = smem_desc_sw128(sV + st.j0 * C::kTile, C::kChunk, 1024);
 #pragma unroll 1
-          for (int gi = 0; gi < ng; ++gi)
-            mma_bf16_ts(region + kXColO, region + gi * 8,
-                        dv0 + static_cast<uint64_t>(((gi >> 3) * C::kTile + (gi & 7) * 2048) >> 4), kIdO,
-                        (s > 0 || gi > 0) ? 1u : 0u);
-          mma_commit(b_pv_done);
-          // Release the fill after this warpgroup's last product on it: a pair's first half is
-          // the previous pair's second, read already; otherwise this warpgroup's next tile of
-          // the run (i + 2), if there is one, reads the same fill.
-          if (st.group_end && (st.first_half || t.i + 2 >= t.len)) {
-            mma_commit(b_kv_empty);
-            released = e + 1;
+            for (int gi = 0; gi < ng; ++gi)
+              mma_bf16_ts(dO, region + 8u * static_cast<uint32_t>(gi) + (gi >= hb ? hoff : 0u),
+                          dv0 + static_cast<uint64_t>(((gi >> 3) * C::kTile + (gi & 7) * 2048) >> 4), kIdO,
+                          (s > 0 || gi > 0) ? 1u : 0u);
+            mma_commit(smem_u32(&bars->pv_done[rg]));
           }
+          if (st.release) mma_commit(b_kv_empty);
+          if (rg) ++ks1;
+          else ++ks0;
         }
-        ++tcnt;
-      }
-      while (ok && released < e_total) {
-        if (!(ok = wait(b_kv_full, released))) break;
-        mbar_arrive(b_kv_empty);
-        ++released;
       }
       // Every MMA of this thread completes before TMEM and shared memory are released.
-      mma_commit(smem_u32(&bars->drain[w]));
-      drain_wait(smem_u32(&bars->drain[w]), 0, status);
+      const uint32_t b_drain = smem_u32(&bars->drain[is_s ? 0 : 1]);
+      mma_commit(b_drain);
+      drain_wait(b_drain, 0, status);
     }
   } else {
-    regs_inc<216>();
+    regs_inc<208>();
     // -------------------------------------------------------------------- softmax + epilogue
-    const int wg = (warp - 4) >> 2;            // warpgroup: tiles n with n & 1 == wg
+    const int wg = (warp - 4) >> 2;            // 0: first half of each product's keys; 1: second
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;         // query row within the tile = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-    const uint32_t tR = tbase + lane_off + static_cast<uint32_t>(wg) * kXRegion;   // this row's region
-    const uint32_t b_s_full = smem_u32(&bars->s_full[wg]), b_p_full = smem_u32(&bars->p_full[wg]);
-    const uint32_t b_pv_done = smem_u32(&bars->pv_done[wg]), b_o_free = smem_u32(&bars->o_free[wg]);
+    const uint32_t b_x = smem_u32(&bars->xch[quarter]);
+    float2* xslot = reinterpret_cast<float2*>(smem + C::kOffX);
     const float sl2 = p.scale_log2;
-    const uint32_t p_sw = static_cast<uint32_t>(r & 7);
     auto wwait = [&](uint32_t bar, int phase) -> bool {
       int got = 0;
       if (lane == 0) got = bounded_wait(bar, phase & 1, abort_flag, status, kStatusTimeoutSoftmax) ? 1 : 0;
@@ -590,62 +590,168 @@ __global__ void __launch_bounds__(kXThreads, 1)
       x_walk_next_head(w, p, len_s);
     }
     x_walk_init(w, p, len_s, g0, g1);
-    int n = -1, k = 0, tcnt = 0;
     bool ok = true;
+    int n = -1, xc = 0;
+    int ks0 = 0, ks1 = 0;   // products so far in regions 0 and 1 (scalars: no local memory)
+    // Exchange with the partner thread (same row, other warpgroup): (a, b) out, theirs in.
+    auto exchange = [&](float a, float b, float& pa, float& pb) {
+      xslot[((xc & 1) * 2 + wg) * 128 + r] = make_float2(a, b);
+      __syncwarp();                            // the warp's slots, before its arrival releases them
+      if (lane == 0) mbar_arrive(b_x);
+      ok = ok && wwait(b_x, xc);
+      __syncwarp();                            // lane 0's acquire, before the warp reads
+      const float2 v = xslot[((xc & 1) * 2 + (wg ^ 1)) * 128 + r];
+      pa = v.x;
+      pb = v.y;
+      ++xc;
+    };
+    // The previous tile, whose O is read out and written during this one.
+    bool pend = false;
+    int pv_n = 0, pv_rg = 0, pv_k = 0, pv_b = 0, pv_h = 0, pv_qt = 0;
+    uint32_t pv_ocol = 0;
+    float pv_m = 0.f, pv_l = 0.f, pv_lt = 1.f;
+    // Reads this thread's half of the previous tile's O (once its P V has completed), frees
+    // the region, stages the normalised O in Q buffer (pv_n + 1) & 1 (the current tile's,
+    // whose last S has completed) for the Q loader's store, and writes (warpgroup 0) the LSE.
+    auto finish_prev = [&]() {
+      uint32_t o[D / 64][32];
+      if (ok) {
+        const uint32_t src = tbase + lane_off + static_cast<uint32_t>(pv_rg) * kXRegion + pv_ocol + wg * (D / 2);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) tmem_ld32_nowait(src + c * 32, o[c]);
+        tmem_ld_wait_tied(o[0]);
+#pragma unroll
+        for (int c = 1; c < D / 64; ++c) tmem_reg_tie(o[c]);
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bars->o_free[pv_rg]));   // the region may be reused
+        const int qrow = pv_qt * 128 + r;
+        const bool valid_row = qrow < p.q_valid;
+        const float inv_l = 1.f / pv_lt;
+        const uint32_t sO = sQ + static_cast<uint32_t>((pv_n + 1) & 1) * C::kTile;
+#pragma unroll
+        for (int u = 0; u < D / 16; ++u) {   // 16-byte units of this thread's half row
+          uint4 v = make_uint4(0, 0, 0, 0);
+          if (valid_row) {
+            const uint32_t* f = &o[u >> 2][(u & 3) * 8];
+            v.x = pack_bf16x2(__uint_as_float(f[0]) * inv_l, __uint_as_float(f[1]) * inv_l);
+            v.y = pack_bf16x2(__uint_as_float(f[2]) * inv_l, __uint_as_float(f[3]) * inv_l);
+            v.z = pack_bf16x2(__uint_as_float(f[4]) * inv_l, __uint_as_float(f[5]) * inv_l);
+            v.w = pack_bf16x2(__uint_as_float(f[6]) * inv_l, __uint_as_float(f[7]) * inv_l);
+          }
+          const uint32_t uu = static_cast<uint32_t>(wg * (D / 16) + u);   // unit within the row
+          const uint32_t addr = sO + (uu >> 3) * C::kChunk + static_cast<uint32_t>(r) * 128u +
+                                (((uu & 7u) ^ static_cast<uint32_t>(r & 7)) << 4);
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                       : "memory");
+        }
+        fence_proxy_async_smem();   // the staged rows, before the store (async proxy) reads them
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&bars->o_staged[(pv_n + 1) & 1]));
+        if (wg == 0)
+          p.lse[(static_cast<size_t>(pv_b) * p.Sq + qrow) * p.H + pv_h] =
+              valid_row ? (pv_m + log2f(pv_lt)) * kXLn2 : -INFINITY;
+      }
+      pend = false;
+    };
     XTile t;
-    while (x_walk_next(w, p, len_s, t)) {
+    // One pass per live tile, and a last one (no tile) that reads out the last tile's O.
+    for (;;) {
+      const bool have = x_walk_next(w, p, len_s, t);
+      if (!have && !pend) break;
       ++n;
-      if ((n & 1) != wg) continue;
-      const int buf = n % kXQBufs;
-      float m_run = -INFINITY, l_run = 0.f;   // reference (an integer once set) and row sum
-      const int ns = x_n_steps(t);
-      for (int s = 0; s < ns; ++s, ++k) {
+      const int rg = n & 1;
+      const uint32_t tR = tbase + lane_off + static_cast<uint32_t>(rg) * kXRegion;   // this row's region
+      const uint32_t ocol = have ? x_ocol(t) : 0u;
+      float m_run = 0.f, l_run = 0.f;   // reference (an integer) and this thread's partial sum
+      const int ns = have ? x_n_steps(t) : 0;
+      for (int s = 0; s < ns; ++s) {
         const XStep st = x_step(t, s);
-        ok = ok && wwait(b_s_full, k);
+        const int rg_k = rg ? ks1++ : ks0++;
+        ok = ok && wwait(smem_u32(&bars->s_full[rg]), rg_k);
         if (ok) tc_fence_after_sync();
-        // One pass over the step's S columns, 32 at a time (a small loop keeps the code that
-        // the softmax warps run between tiles in the instruction cache). Each chunk's maximum
-        // may move the reference: when it lies more than kXRescale above it, what the row has
-        // accumulated (P of the step's earlier chunks, O of the earlier steps, the sum) is
-        // scaled by the exact power of two 2^(m_old - m_new) first. P of chunk q goes to
-        // columns 16 q .. 16 q + 15, which hold S this thread has already read (chunk q / 2).
-        float l_step = 0.f;   // sum of this step's P so far
-        // Chunk q of the step: S columns 32 q .. + 31 (of which `lim` are valid keys); its
-        // maximum, a rescale if the reference has to move, the exponentials and P. MASKED:
-        // the chunk has fewer than 32 valid keys (only the step's last chunk can).
-        auto chunk = [&](int q, int lim, auto masked_tag) {
+        const int half = 64 * st.nkt;                                   // keys per warpgroup
+        const int lim0 = min(128 * st.nkt, t.L - st.kt * 128);          // valid keys of the product
+        const int mine = max(0, min(half, lim0 - wg * half));           // of them in this half
+        const int nch = (mine + 31) >> 5;                               // its 32-key chunks
+        const uint32_t sS = tR + static_cast<uint32_t>(wg * half);      // its S columns
+        const uint32_t sP = tR + static_cast<uint32_t>(wg * 96 * st.nkt);   // its P columns
+        // Maximum of this half (log2 units).
+        float mx = -INFINITY;
+        if (ok) {
+          const int nfull = mine >> 5;
+          int j = 0;
+#pragma unroll 1
+          for (; j + 1 < nfull; j += 2) {   // two full chunks per wait
+            uint32_t v[32], u[32];
+            tmem_ld32_nowait(sS + 32 * j, v);
+            tmem_ld32_nowait(sS + 32 * j + 32, u);
+            tmem_ld_wait_tied(v);
+            tmem_reg_tie(u);
+            float m0 = -INFINITY, m1 = -INFINITY, m2 = -INFINITY, m3 = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < 32; i += 4) {
+              m0 = fmax3(m0, __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
+              m1 = fmax3(m1, __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
+              m2 = fmax3(m2, __uint_as_float(u[i]), __uint_as_float(u[i + 1]));
+              m3 = fmax3(m3, __uint_as_float(u[i + 2]), __uint_as_float(u[i + 3]));
+            }
+            mx = fmax3(mx, fmax3(m0, m1, m2), m3);
+          }
+#pragma unroll 1
+          for (; j < nch; ++j) {
+            uint32_t v[32];
+            tmem_ld32(sS + 32 * j, v);
+            const int lim = mine - 32 * j;
+            float m0 = -INFINITY, m1 = -INFINITY;
+            if (lim >= 32) {
+#pragma unroll
+              for (int i = 0; i < 32; i += 4) {
+                m0 = fmax3(m0, __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
+                m1 = fmax3(m1, __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
+              }
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; i += 2) {
+                m0 = fmaxf(m0, i < lim ? __uint_as_float(v[i]) : -INFINITY);
+                m1 = fmaxf(m1, i + 1 < lim ? __uint_as_float(v[i + 1]) : -INFINITY);
+              }
+            }
+            mx = fmax3(mx, m0, m1);
+          }
+          mx *= sl2;
+        }
+        // The pair's maximum; with the first product of a tile, the previous tile's partial
+        // sums go across too.
+        float pmx = -INFINITY, pl = 0.f;
+        if (ok) exchange(mx, pend && s == 0 ? pv_l : 0.f, pmx, pl);
+        if (pend && s == 0) pv_lt = pv_l + pl;
+        const float mt = fmaxf(mx, pmx);
+        const bool grow = s > 0 && mt > m_run + kXRescale;   // the same in both threads of the pair
+        if (s == 0) m_run = ceilf(mt);                          // the product has a valid key
+        // The rescale reads and writes TMEM with warp-collective instructions, so the whole
+        // warp takes the branch (a = 1 in the rows whose reference stays). O of the earlier
+        // products is complete (this product's S was issued after their P V); P of this one
+        // is not written yet.
+        if (__any_sync(0xffffffffu, grow)) {
+          const float m_new = grow ? ceilf(mt) : m_run;
+          const float a = ex2_approx(m_run - m_new);   // a power of two; 1 where m stays
+          l_run *= a;
+          m_run = m_new;
+          if (ok) {
+#pragma unroll 1
+            for (int c = 0; c < D / 64; ++c) x_scale_f32_cols(tR + ocol + wg * (D / 2) + c * 32, a);
+          }
+        }
+        // Exponentials: chunk j (S columns 32 j .. of this half) to P columns 16 j .. of this
+        // half's P range. Warpgroup 1 walks its chunks from the last, so that each P lands on
+        // S columns it has read already.
+        const float neg_m = -m_run;
+        float l_step = 0.f;
+        auto chunk = [&](int j, int lim, auto masked_tag) {
           constexpr bool kMasked = decltype(masked_tag)::value;
           uint32_t v[32];
-          tmem_ld32(tR + q * 32, v);
-          auto sv = [&](int i) -> float {
-            return (kMasked && i >= lim) ? -INFINITY : __uint_as_float(v[i]);
-          };
-          float m0 = -INFINITY, m1 = -INFINITY;
-#pragma unroll
-          for (int i = 0; i < 32; i += 4) {
-            m0 = fmax3(m0, sv(i), sv(i + 1));
-            m1 = fmax3(m1, sv(i + 2), sv(i + 3));
-          }
-          const float mt = fmaxf(m0, m1) * sl2;
-          const bool first = s == 0 && q == 0;
-          const bool grow = !first && mt > m_run + kXRescale;
-          if (first) m_run = ceilf(mt);   // the tile's first chunk has a valid column
-          if (__any_sync(0xffffffffu, grow)) {
-            const float m_new = grow ? ceilf(mt) : m_run;
-            const float a = ex2_approx(m_run - m_new);   // a power of two; 1 where m stays
-            l_run = (l_run + l_step) * a;
-            l_step = 0.f;
-            m_run = m_new;
-            tmem_st_wait();
-#pragma unroll 1
-            for (int g = 0; g < q; ++g) x_scale_bf16_cols16(tR + g * 16, a);
-            // O of the earlier steps: their P V is complete (this step's S was issued after it).
-            if (s > 0) {
-#pragma unroll 1
-              for (int c = 0; c < D / 32; ++c) x_scale_f32_cols(tR + kXColO + c * 32, a);
-            }
-          }
-          const float neg_m = -m_run;
+          tmem_ld32(sS + 32 * j, v);
           float l4[4] = {0.f, 0.f, 0.f, 0.f};
           uint32_t pk[16];
 #pragma unroll
@@ -660,72 +766,72 @@ __global__ void __launch_bounds__(kXThreads, 1)
             add2(l4[2 * (i & 1)], l4[2 * (i & 1) + 1], p0, p1);
             pk[i] = pack_bf16x2(p0, p1);
           }
-          tmem_st16_nowait(tR + q * 16, pk);
+          tmem_st16_nowait(sP + 16 * j, pk);
           l_step += (l4[0] + l4[1]) + (l4[2] + l4[3]);
         };
+        // The previous tile's O is read out during this tile's last product (whose Q buffer,
+        // dead then, takes it), as soon as its P V has completed: the chunk loop stops when
+        // it has, the O goes out, and the loop resumes.
+        bool poll = pend && s == ns - 1;
+        int idx = 0;
         if (ok) {
-          const int lim0 = min(128 * st.nkt, t.L - st.kt * 128);   // valid keys of the step
-          const int nfull = lim0 >> 5;                               // chunks with 32 of them
 #pragma unroll 1
-          for (int q = 0; q < nfull; ++q) chunk(q, 32, std::false_type{});
-          // The last chunk with valid keys, if partial. P V reads only the step's valid keys
-          // in whole 16-key groups, so no P column past them is read.
-          if ((lim0 & 31) != 0) chunk(nfull, lim0 & 31, std::true_type{});
+          for (;;) {
+            bool hit = false;
+#pragma unroll 1
+            for (; idx < nch; ++idx) {
+              const int j = wg ? nch - 1 - idx : idx;
+              const int lim = mine - 32 * j;
+              if (lim >= 32) chunk(j, 32, std::false_type{});
+              else chunk(j, lim, std::true_type{});
+              if (poll) {
+                int got = 0;
+                if (lane == 0) got = x_test_wait(smem_u32(&bars->pv_done[pv_rg]), pv_k & 1) ? 1 : 0;
+                if (__shfl_sync(0xffffffffu, got, 0)) {
+                  ++idx;
+                  hit = true;
+                  break;
+                }
+              }
+            }
+            if (!hit) break;
+            tc_fence_after_sync();
+            finish_prev();
+            poll = false;
+          }
         }
         l_run += l_step;
         if (ok) {
           tmem_st_wait();
-          tc_fence_before_sync();   // P (tcgen05.st) and any rescale before the P V
+          tc_fence_before_sync();   // P (tcgen05.st) and any O rescale before the P V
           __syncwarp();
-          if (lane == 0) mbar_arrive(b_p_full);
+          if (lane == 0) mbar_arrive(smem_u32(&bars->p_full[rg]));
         }
       }
-      // Epilogue: O out of TMEM, normalised, staged in this tile's Q buffer (the Q loader
-      // stores it).
-      uint32_t orr[D / 32][32];
-      ok = ok && wwait(b_pv_done, k - 1);
-      if (ok) {
-        tc_fence_after_sync();
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) tmem_ld32_nowait(tR + kXColO + c * 32, orr[c]);
-        tmem_ld_wait_tied(orr[0]);
-#pragma unroll
-        for (int c = 1; c < D / 32; ++c) tmem_reg_tie(orr[c]);
-        tc_fence_before_sync();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(b_o_free);   // O may be overwritten
-      } else {
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c)
-#pragma unroll
-          for (int i = 0; i < 32; ++i) orr[c][i] = 0u;
+      if (!have) {
+        // The last tile's partial sums, and the buffer for its O: the Q loader hands over
+        // buffer n & 1 with a plain arrival.
+        float unused, pl = 0.f;
+        if (ok) exchange(0.f, pv_l, unused, pl);
+        pv_lt = pv_l + pl;
+        ok = ok && wwait(smem_u32(&bars->q_full[n & 1]), n >> 1);
       }
-      const int qrow = t.qt * 128 + r;
-      const bool valid_row = qrow < p.q_valid;
-      const float inv_l = 1.f / l_run;
-      const uint32_t sO = sQ + buf * C::kTile;
-#pragma unroll
-      for (int u = 0; u < D / 8; ++u) {   // 16-byte units of the row
-        uint4 o = make_uint4(0, 0, 0, 0);
-        if (valid_row) {
-          const uint32_t* f = &orr[u >> 2][(u & 3) * 8];
-          o.x = pack_bf16x2(__uint_as_float(f[0]) * inv_l, __uint_as_float(f[1]) * inv_l);
-          o.y = pack_bf16x2(__uint_as_float(f[2]) * inv_l, __uint_as_float(f[3]) * inv_l);
-          o.z = pack_bf16x2(__uint_as_float(f[4]) * inv_l, __uint_as_float(f[5]) * inv_l);
-          o.w = pack_bf16x2(__uint_as_float(f[6]) * inv_l, __uint_as_float(f[7]) * inv_l);
-        }
-        const uint32_t addr = sO + static_cast<uint32_t>(u >> 3) * C::kChunk + static_cast<uint32_t>(r) * 128u +
-                              ((static_cast<uint32_t>(u & 7) ^ p_sw) << 4);
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(o.x), "r"(o.y), "r"(o.z), "r"(o.w)
-                     : "memory");
+      if (pend) {   // not read out during the tile
+        ok = ok && wwait(smem_u32(&bars->pv_done[pv_rg]), pv_k);
+        if (ok) tc_fence_after_sync();
+        finish_prev();
       }
-      fence_proxy_async_smem();   // the staged row, before the store (async proxy) reads it
-      __syncwarp();
-      if (!ok) break;
-      if (lane == 0) mbar_arrive(smem_u32(&bars->o_staged[buf]));
-      p.lse[(static_cast<size_t>(t.b) * p.Sq + qrow) * p.H + t.h] =
-          valid_row ? (m_run + log2f(l_run)) * kXLn2 : -INFINITY;
-      ++tcnt;
+      if (!have) break;
+      pend = true;
+      pv_n = n;
+      pv_rg = rg;
+      pv_k = (rg ? ks1 : ks0) - 1;   // its last product's P V
+      pv_b = t.b;
+      pv_h = t.h;
+      pv_qt = t.qt;
+      pv_ocol = ocol;
+      pv_m = m_run;
+      pv_l = l_run;
     }
   }
   __syncwarp();
