@@ -1,12 +1,13 @@
 """A bounded wait that runs out, on the GPU, without faulting or hanging it.
 
-Every wait in the attention kernel (mbarrier, named barrier, grid counter) gives up after a
-time limit: it records a bit in the device status word, raises the CTA's abort flag so the
-other roles fall through, waits (again with a limit) for its own copies and MMAs in flight,
-frees tensor memory and returns. These tests exercise that path through the test-only
-library libdit_attn_testhooks.so (the product sources compiled with DIT_TEST_HOOKS), whose
-wait limit a test can shorten and whose K/V producer can be told to count one load without
-issuing it, a flag that nothing else sets. Nothing faults or traps: the kernel gives up and
+Every wait in the attention kernels (self-attention and short-KV cross-attention: mbarrier,
+named barrier, grid counter) gives up after a time limit: it records a bit in the device
+status word, raises the CTA's abort flag so the other roles fall through, waits (again with
+a limit) for its own copies and MMAs in flight, frees tensor memory and returns. These tests
+exercise that path through the test-only library libdit_attn_testhooks.so (the product
+sources compiled with DIT_TEST_HOOKS), whose wait limit a test can shorten and whose K/V
+producers can be told to count one load (or one fill) without issuing it, a flag that
+nothing else sets. Nothing faults or traps: the kernel gives up and
 exits, and the next call on the same device computes the right result.
 """
 import ctypes
@@ -89,6 +90,52 @@ def test_wait_runs_out_and_kernel_recovers(lib, tlib, skip_load):
     assert _status(tlib) == 0
     compare(out.float().cpu().numpy(), lse.cpu().numpy(), Or, Lr, case.q_valid)
     O2, L2 = lib.dit_attn_fwd(qd, kd, vd, case.q_valid, case.kv_valid)
+    torch.cuda.synchronize()
+    assert lib.dit_device_status() == 0
+    assert torch.equal(O2, out) and torch.equal(L2, lse)
+
+
+def _cross_call(t, case, qd, kd, vd, kv, out, lse):
+    """dit_cross_attn_shortkv through the given library."""
+    return t.dit_cross_attn_shortkv(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), case.B, case.Sq, case.Skv,
+                                    case.H, case.D, case.q_valid, kv.data_ptr(), case.scale, out.data_ptr(),
+                                    lse.data_ptr(), None)
+
+
+@pytest.mark.parametrize("skip_fill", [0, 1])
+def test_cross_wait_runs_out_and_kernel_recovers(lib, tlib, skip_fill):
+    """Short-KV cross-attention, four CTAs of one query tile each over 300 text keys (so a tile
+    reads two fills: key tiles 0-1, then key tile 2). Each CTA's fill warp counts fill
+    `skip_fill` without issuing it: with 0 the first S product's wait runs out; with 1 the
+    tile's first two products complete and the third one's wait runs out, with the softmax
+    warps, the P.V issuer and the Q loader waiting at their next steps. The call returns well
+    within a second with timeout bits only (no drain failure), the bits clear, and the next
+    calls, through this library and through the product library, match the oracle."""
+    case = AttnCase("xstall", B=1, H=2, D=128, Sq=256, Skv=512, q_valid=200, kv_valid=[300], seed=98)
+    q, k, v = make_qkv(case)
+    qd, kd, vd = dev_bf16(q), dev_bf16(k), dev_bf16(v)
+    kv = torch.tensor(case.kv_valid, dtype=torch.int32, device="cuda")
+    out = torch.empty_like(qd)
+    lse = torch.empty((case.B, case.Sq, case.H), dtype=torch.float32, device="cuda")
+    assert _status(tlib) == 0
+    assert tlib.dit_test_set_wait_hooks(50_000_000, skip_fill) == 0   # 50 ms, one fill skipped
+    t0 = time.perf_counter()
+    assert _cross_call(tlib, case, qd, kd, vd, kv, out, lse) == 0
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    st = _status(tlib)
+    assert st != 0 and (st & ~TIMEOUT_BITS) == 0, f"status {st:#x}"
+    assert not (st & DRAIN_BIT)
+    assert wall < 2.0, f"the stalled call took {wall:.2f} s"
+    assert _status(tlib) == 0
+
+    assert tlib.dit_test_set_wait_hooks(2_000_000_000, -1) == 0
+    Or, Lr = attention(q, k, v, case.q_valid, case.kv_valid, case.scale)
+    assert _cross_call(tlib, case, qd, kd, vd, kv, out, lse) == 0
+    torch.cuda.synchronize()
+    assert _status(tlib) == 0
+    compare(out.float().cpu().numpy(), lse.cpu().numpy(), Or, Lr, case.q_valid)
+    O2, L2 = lib.dit_cross_attn_shortkv(qd, kd, vd, case.q_valid, kv)
     torch.cuda.synchronize()
     assert lib.dit_device_status() == 0
     assert torch.equal(O2, out) and torch.equal(L2, lse)

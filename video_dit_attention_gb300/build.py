@@ -21,7 +21,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libdit_attn.so")
 TEST_LIB = os.path.join(HERE, "libdit_attn_testhooks.so")
-TEST_HOOK_SOURCES = ["attn_fwd.cu"]   # recompiled with -DDIT_TEST_HOOKS for the test library
+TEST_HOOK_SOURCES = ["attn_fwd.cu", "cross_attn.cu"]   # recompiled with -DDIT_TEST_HOOKS for the test library
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CUDA_SOURCES = ["attn_fwd.cu", "cross_attn.cu", "elementwise.cu", "fp8.cu", "api.cu"]
 CXX_SOURCES = ["rope_table.cpp"]

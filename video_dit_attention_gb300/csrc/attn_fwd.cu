@@ -1369,6 +1369,7 @@ extern "C" int dit_test_set_wait_hooks(unsigned long long wait_limit_ns, int ski
   if (wait_limit_ns == 0) return -1;
   cudaError_t e = cudaMemcpyToSymbol(dit::g_dit_test_wait_limit_ns, &wait_limit_ns, sizeof(wait_limit_ns));
   if (e == cudaSuccess) e = cudaMemcpyToSymbol(dit::g_dit_test_skip_load, &skip_load, sizeof(skip_load));
+  if (e == cudaSuccess) e = dit::cross_attn_set_test_hooks(wait_limit_ns, skip_load);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   return e == cudaSuccess ? 0 : -4;
 }

@@ -120,6 +120,10 @@ cudaError_t device_status_ptr(unsigned int** out);
 // Short-KV cross-attention (Skv <= 512, per-batch key lengths on the device): the kernel in
 // cross_attn.cu, which keeps a head's keys and values resident in shared memory.
 cudaError_t launch_cross_attn(const AttnArgs& a);
+#ifdef DIT_TEST_HOOKS
+// Test library only: the wait limit and skipped fill of the cross-attention kernel's unit.
+cudaError_t cross_attn_set_test_hooks(unsigned long long wait_limit_ns, int skip_fill);
+#endif
 
 // Encodes a TMA descriptor for a BSHD bf16 tensor [B, S_rows, H, D] whose sequence extent is
 // cut to `s_extent` rows (reads past it return zeros), with a box of 64 channels x 1 head x

@@ -449,20 +449,27 @@ __global__ void __launch_bounds__(kXThreads, 1)
           // 2: landed.
           int got = 1;
           if (lane == 0) {
+#ifdef DIT_TEST_HOOKS
+            const bool skip = e == g_dit_test_skip_load;   // test build only: counted, never issued
+#else
+            constexpr bool skip = false;
+#endif
             if (e > 0 && !bounded_wait(b_kv_empty, (e - 1) & 1, abort_flag, status, kStatusTimeoutLoad)) {
               got = 0;
             } else {
-              mbar_arrive_expect_tx(b_kv_full, 2 * cnt * C::kTile);
-              for (int j = 0; j < cnt; ++j) {
-                const int key0 = (kt0 + j) * 128;
+              if (!skip) {
+                mbar_arrive_expect_tx(b_kv_full, 2 * cnt * C::kTile);
+                for (int j = 0; j < cnt; ++j) {
+                  const int key0 = (kt0 + j) * 128;
 #pragma unroll
-                for (int c = 0; c < C::kSub; ++c) {
-                  tma_load_4d(sK + c * 2 * C::kChunk + j * C::kChunk, &tm_k, b_kv_full, c * 64, t.h, key0, t.b);
-                  tma_load_4d(sV + j * C::kTile + c * C::kChunk, &tm_v, b_kv_full, c * 64, t.h, key0, t.b);
+                  for (int c = 0; c < C::kSub; ++c) {
+                    tma_load_4d(sK + c * 2 * C::kChunk + j * C::kChunk, &tm_k, b_kv_full, c * 64, t.h, key0, t.b);
+                    tma_load_4d(sV + j * C::kTile + c * C::kChunk, &tm_v, b_kv_full, c * 64, t.h, key0, t.b);
+                  }
                 }
               }
               if (bounded_wait(b_kv_full, e & 1, abort_flag, status, kStatusTimeoutRope)) got = 2;
-              else drain_wait(b_kv_full, e & 1, status);   // the copies land before the CTA exits
+              else if (!skip) drain_wait(b_kv_full, e & 1, status);   // the copies land before the CTA exits
             }
           }
           if (__shfl_sync(0xffffffffu, got, 0) != 2) {
@@ -888,5 +895,13 @@ cudaError_t launch_cross_attn(const AttnArgs& a) {
   }
   return cudaGetLastError();
 }
+
+#ifdef DIT_TEST_HOOKS
+cudaError_t cross_attn_set_test_hooks(unsigned long long wait_limit_ns, int skip_fill) {
+  cudaError_t e = cudaMemcpyToSymbol(g_dit_test_wait_limit_ns, &wait_limit_ns, sizeof(wait_limit_ns));
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_dit_test_skip_load, &skip_fill, sizeof(skip_fill));
+  return e;
+}
+#endif
 
 }  // namespace dit

@@ -33,11 +33,13 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;
 #ifdef DIT_TEST_HOOKS
 // Test-only build (libdit_attn_testhooks.so, never the product library): the limit is a
 // device variable that a test shortens, so that a wait it makes run out gives up within
-// milliseconds instead of seconds.
-__device__ unsigned long long g_dit_test_wait_limit_ns = kWaitLimitNs;
-// Number of the K/V ring load that the attention kernel's producer counts but never issues
-// (-1: none). The consumers of that load then wait until the limit runs out.
-__device__ int g_dit_test_skip_load = -1;
+// milliseconds instead of seconds. Each translation unit compiled for the test library has
+// its own copy of these (internal linkage) and its own setter.
+static __device__ unsigned long long g_dit_test_wait_limit_ns = kWaitLimitNs;
+// Number of the load that a kernel's K/V producer counts but never issues (-1: none): a K/V
+// ring load of the attention kernel, a fill of the cross-attention kernel. The consumers of
+// that load then wait until the limit runs out.
+static __device__ int g_dit_test_skip_load = -1;
 __device__ __forceinline__ uint64_t wait_limit_ns() { return g_dit_test_wait_limit_ns; }
 #else
 __device__ __forceinline__ constexpr uint64_t wait_limit_ns() { return kWaitLimitNs; }
