@@ -48,7 +48,9 @@
 //     exceeds it by more than kXRescale, and O and the sums are then scaled by the power of
 //     two 2^(m_old - m_new), which is exact. Tile i of a run visits half i & 1 first, so
 //     consecutive tiles share the fill at their boundary and a run of P tiles reads P + 1
-//     fills. A fill is released when both MMA issuers have committed their last product on it.
+//     fills. A fill's K lands on a barrier of its own, ahead of its V, so that the first S
+//     product of a head waits only for K. A fill is released when both MMA issuers have
+//     committed their last product on it.
 //   - Roles: warp 0 loads Q and stores O (two buffers; the tile two ahead is warmed in L2);
 //     warp 1 owns TMEM, loads the fills and zeroes the V rows past L_b of a fill's last V
 //     tile (so that 0 * (pad contents) cannot reach O; K pad rows need nothing, their score
@@ -95,7 +97,7 @@ static_assert(XCfg<128>::kSmem <= 232448, "shared memory of the D = 128 cross ke
 
 struct XBars {
   uint64_t q_full[kXQBufs], q_empty[kXQBufs], o_staged[kXQBufs];
-  uint64_t kv_full, kv_ready, kv_empty;
+  uint64_t kv_full, kv_ready, kv_empty, k_full;   // kv_full: V of a fill; k_full: its K
   uint64_t s_full[2], p_full[2], pv_done[2], o_free[2];   // per TMEM region
   uint64_t xch[4];                                       // per lane quarter: the softmax exchange
   uint64_t drain[2];
@@ -331,6 +333,7 @@ __global__ void __launch_bounds__(kXThreads, 1)
       mbar_init(smem_u32(&bars->o_staged[i]), 8);   // one arrival per softmax warp
     }
     mbar_init(smem_u32(&bars->kv_full), 1);
+    mbar_init(smem_u32(&bars->k_full), 1);
     mbar_init(smem_u32(&bars->kv_ready), 1);
     mbar_init(smem_u32(&bars->kv_empty), 2);   // one commit per MMA issuer
     for (int r = 0; r < 2; ++r) {
@@ -358,6 +361,7 @@ __global__ void __launch_bounds__(kXThreads, 1)
   tc_fence_after_sync();
   const uint32_t tbase = bars->tmem_base;
   const uint32_t b_kv_full = smem_u32(&bars->kv_full), b_kv_ready = smem_u32(&bars->kv_ready);
+  const uint32_t b_k_full = smem_u32(&bars->k_full);
   const uint32_t b_kv_empty = smem_u32(&bars->kv_empty);
 
   if (warp < 4) {
@@ -458,18 +462,25 @@ __global__ void __launch_bounds__(kXThreads, 1)
               got = 0;
             } else {
               if (!skip) {
-                mbar_arrive_expect_tx(b_kv_full, 2 * cnt * C::kTile);
-                for (int j = 0; j < cnt; ++j) {
-                  const int key0 = (kt0 + j) * 128;
+                // K first (the S products need only K), then V on a barrier of its own.
+                mbar_arrive_expect_tx(b_k_full, cnt * C::kTile);
+                mbar_arrive_expect_tx(b_kv_full, cnt * C::kTile);
+                for (int j = 0; j < cnt; ++j)
 #pragma unroll
-                  for (int c = 0; c < C::kSub; ++c) {
-                    tma_load_4d(sK + c * 2 * C::kChunk + j * C::kChunk, &tm_k, b_kv_full, c * 64, t.h, key0, t.b);
-                    tma_load_4d(sV + j * C::kTile + c * C::kChunk, &tm_v, b_kv_full, c * 64, t.h, key0, t.b);
-                  }
-                }
+                  for (int c = 0; c < C::kSub; ++c)
+                    tma_load_4d(sK + c * 2 * C::kChunk + j * C::kChunk, &tm_k, b_k_full, c * 64, t.h, (kt0 + j) * 128, t.b);
+                for (int j = 0; j < cnt; ++j)
+#pragma unroll
+                  for (int c = 0; c < C::kSub; ++c)
+                    tma_load_4d(sV + j * C::kTile + c * C::kChunk, &tm_v, b_kv_full, c * 64, t.h, (kt0 + j) * 128, t.b);
               }
-              if (bounded_wait(b_kv_full, e & 1, abort_flag, status, kStatusTimeoutRope)) got = 2;
-              else if (!skip) drain_wait(b_kv_full, e & 1, status);   // the copies land before the CTA exits
+              if (bounded_wait(b_kv_full, e & 1, abort_flag, status, kStatusTimeoutRope) &&
+                  bounded_wait(b_k_full, e & 1, abort_flag, status, kStatusTimeoutRope)) {
+                got = 2;
+              } else if (!skip) {   // the copies land before the CTA exits
+                drain_wait(b_kv_full, e & 1, status);
+                drain_wait(b_k_full, e & 1, status);
+              }
             }
           }
           if (__shfl_sync(0xffffffffu, got, 0) != 2) {
@@ -531,7 +542,7 @@ __global__ void __launch_bounds__(kXThreads, 1)
             } else if (!(ok = wait(smem_u32(&bars->pv_done[rg]), kr - 1))) {
               break;   // (above: the previous product's P has been read; S goes over it)
             }
-            if (!(ok = wait(b_kv_full, e))) break;
+            if (!(ok = wait(b_k_full, e))) break;
             const uint64_t da = smem_desc_sw128(sQ + rg * C::kTile, 16, 1024);
             const uint64_t db = smem_desc_sw128(sK + st.j0 * C::kChunk, 16, 1024);
             // N covers the product's valid keys in whole 16-key groups (the softmax never
