@@ -44,6 +44,20 @@ def test_cross_many_tiles_per_cta(lib, D, kv):
     assert lib.dit_device_status() == 0
 
 
+@pytest.mark.parametrize("D,kv", [(128, [300, 200]), (64, [512, 129])])
+def test_cross_one_tile_per_head(lib, D, kv):
+    """One query tile per (batch, head) and 600 heads over the persistent grid, so every CTA
+    range crosses several heads: each tile is a run of its own, with a fill of its own (two
+    when the text is longer than 256 keys), and the ranges hold one to four tiles, so the Q
+    loader's hand-over of the last buffer runs with every small tile count."""
+    case = AttnCase("crossheads", B=2, H=300, D=D, Sq=128, Skv=512, q_valid=77, kv_valid=kv, seed=88 + D)
+    q, k, v = make_qkv(case)
+    O, L = _run_cross(lib, case, q, k, v)
+    Or, Lr = attention(q, k, v, case.q_valid, kv, case.scale)
+    compare(O, L, Or, Lr, case.q_valid)
+    assert lib.dit_device_status() == 0
+
+
 @pytest.mark.parametrize("D,kv,grow", [(128, [250, 256], 1), (128, [400, 512], 2), (64, [512, 300], 3)])
 def test_cross_growing_maximum(lib, D, kv, grow):
     """Keys of one 128-key block scaled by 4 (exact in bf16), so that for many rows its scores
